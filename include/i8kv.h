@@ -1,0 +1,164 @@
+/*
+ * i8kv.h -- C ABI of the INT8 KV-cache paged-attention library for GB300 (sm_103a).
+ *
+ * The operation is the one described in two pages of a blog series:
+ *   [KV] "gfx936 DCU上实现INT8 KV与INT8 MMAC Attention推理优化" (part 1)
+ *   [PV] "gfx936 DCU上实现INT8 PV MMAC：V Scale融合、概率量化与Fragment分组" (part 3)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers are DEVICE pointers unless a parameter says otherwise.  The caller
+ *    owns every buffer; the library allocates nothing and keeps no state besides
+ *    a per-thread last-error string and one device-side error word.
+ *  - bf16 tensors are passed as `const uint16_t*` (raw bf16 bit patterns).
+ *  - All launches are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL is the legacy default stream).  Nothing synchronizes.
+ *  - Argument errors are reported synchronously through the status code, before
+ *    anything is launched; i8kv_last_error() gives a one-line reason.  A launch
+ *    failure reported by the CUDA runtime maps to I8KV_ERR_CUDA.
+ *  - Inputs are never written.  Outputs are fully overwritten.
+ *  - Paged layouts ([KV] §2.3), with bs = block_size (16 is the only size the
+ *    kernels accept), NB blocks in the pool, Hkv KV heads and head_dim D:
+ *        K cache   int8  [NB, Hkv, D/16, bs, 16]   16 head-dims per 16-byte chunk
+ *        V cache   int8  [NB, Hkv, D, bs]          tokens inner-most
+ *        K/V scale fp32  [NB, bs, Hkv]             one scale per (token, KV head)
+ *    A token at slot s lives in block s / bs at offset s % bs.  A sequence's
+ *    token at position p lives in block block_table[p / bs], offset p % bs.
+ *  - Cache and Q/out pointers must be 16-byte aligned.
+ *  - Supported shapes: D in {128, 256}; Hq % Hkv == 0 with G = Hq / Hkv <= 8;
+ *    query head h reads KV head h / G.
+ *  - Quantization is symmetric INT8 with an fp32 absmax/127 scale per (token,
+ *    head) vector; codes are clamp(round_half_even(x / scale), -127, 127); a
+ *    vector of zeros gets scale 0 and zero codes ([KV] §2.1).
+ */
+#ifndef I8KV_H_
+#define I8KV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  I8KV_OK = 0,
+  I8KV_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer            */
+  I8KV_ERR_UNSUPPORTED = 2, /* valid but not implemented (D, G, block size, partition) */
+  I8KV_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required           */
+  I8KV_ERR_CUDA = 4,        /* the CUDA runtime reported an error at launch         */
+  I8KV_ERR_DEVICE = 5       /* a kernel recorded a failure in the device error word */
+} i8kv_status;
+
+/* One-line description of the last non-OK status returned on this host thread.
+ * Copies at most n-1 bytes plus a terminating NUL into buf (host memory). */
+i8kv_status i8kv_last_error(char* buf, size_t n);
+
+/* Reads and clears the device error word (synchronizes the device).  *code is
+ * 0 when no kernel recorded a failure; otherwise the first failure's code:
+ * 1 = a pipeline wait exceeded its time limit, 2 = a block-table or slot entry
+ * out of range (checked kernels only).  Returns I8KV_ERR_DEVICE if *code != 0. */
+i8kv_status i8kv_device_error(int* code);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int i8kv_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* KV producer ([KV] §2.2 "fused KV producer", steps 3-6, without RoPE).     */
+/* For every token t < T with slot_mapping[t] >= 0 and every KV head h:      */
+/*   quantize k[t,h,:] and v[t,h,:] (bf16 [T, Hkv, D]) per the rule above,   */
+/*   store the codes at slot_mapping[t] in k_cache / v_cache and the scales  */
+/*   in k_scale / v_scale.  slot_mapping[t] < 0 skips token t.               */
+/* When q != NULL also quantize q (bf16 [T, Hq, D]) per (token, q-head) into */
+/*   q_i8 (int8 [T, Hq, D]) and q_scale (fp32 [T, Hq]) -- the query is       */
+/*   quantized once and reused by every history partition ([KV] §2.2).       */
+/* Slots must lie inside the pool (num_blocks * block_size); two tokens with */
+/* the same slot race.  The output codes and scales are bit-exact with the   */
+/* fp32 IEEE evaluation of the formula (division, not reciprocal).           */
+/* ------------------------------------------------------------------------ */
+i8kv_status i8kv_kv_quant_write(const uint16_t* k, const uint16_t* v, const int32_t* slot_mapping, int T, int Hkv,
+                                int D, int block_size, int num_blocks, int8_t* k_cache, int8_t* v_cache,
+                                float* k_scale, float* v_scale, const uint16_t* q, int Hq, int8_t* q_i8,
+                                float* q_scale, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* INT8 paged decode attention ([PV] §2-§3, [KV] §3.3).                     */
+/* For sequence b (history L = seq_lens[b], every cached token 0..L-1) and   */
+/* query head h (int8 q_i8[b,h,:] with scale q_scale[b,h]):                  */
+/*   score_t = acc_t * sQ * sK_t * softmax_scale, acc_t = sum_d q*k (int32);  */
+/*   history is cut into partitions of `partition` tokens; in partition g:    */
+/*   m_g = max score, l_g = sum exp(score - m_g), P_t = exp(score_t - m_g)/l_g,*/
+/*   W_t = P_t * sV_t; every 32-token group (aligned to position 0) of one   */
+/*   query row is quantized with sW = max W / 127, Wq = round(W / sW), and   */
+/*   o_g += sW * (Wq x Vq) with an int32 contraction; partitions are merged   */
+/*   by log-sum-exp: O = sum_g l_g e^(m_g-M) o_g / sum_g l_g e^(m_g-M).      */
+/* out: fp32 [B, Hq, D].  seq_lens[b] == 0 gives a zero row.                 */
+/* block_tables: int32 [B, max_blocks]; entries past ceil(L/bs) are unused.  */
+/* softmax_scale <= 0 selects 1/sqrt(D).  partition must be 256.             */
+/* workspace: device memory of at least i8kv_decode_workspace_bytes(...)     */
+/*   bytes, ZERO-FILLED ONCE before its first use.  Every call leaves its    */
+/*   counters at zero again, so it may be reused by later calls on the same  */
+/*   stream; calls that overlap in time need separate workspaces.  After a   */
+/*   call that returned an error, zero-fill it again.                        */
+/* ------------------------------------------------------------------------ */
+size_t i8kv_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_blocks, int block_size, int partition);
+
+i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
+                                        const int8_t* v_cache, const float* k_scale, const float* v_scale,
+                                        const int32_t* block_tables, const int32_t* seq_lens, int B, int Hq, int Hkv,
+                                        int D, int block_size, int max_blocks, float softmax_scale, int partition,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* INT8 prefix-prefill chunk ([PV] §2.1, [KV] §3.2): one online softmax over */
+/* the cached history and the chunk itself.  Chunk query j (absolute         */
+/* position history_len + j) attends to cache positions 0..history_len + j   */
+/* of the sequence described by block_table (int32, covering at least        */
+/* history_len + chunk_len positions); the chunk's own K/V must already be   */
+/* in the cache (written by i8kv_kv_quant_write).  Running state (m, l, o):  */
+/*   alpha = exp(m - m'), p~_t = exp(score_t - m'), W_t = p~_t * sV_t        */
+/*   (unnormalized), per (query row, 32-token group) sW = max W / 127,       */
+/*   Wq = round(W / sW), o = alpha o + sum sW (Wq x Vq), l = alpha l + sum p~,*/
+/*   O = o / l.                                                               */
+/* q_i8: int8 [chunk_len, Hq, D], q_scale: fp32 [chunk_len, Hq].             */
+/* out: fp32 [chunk_len, Hq, D].  softmax_scale <= 0 selects 1/sqrt(D).      */
+/* ------------------------------------------------------------------------ */
+i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
+                                  const int8_t* v_cache, const float* k_scale, const float* v_scale,
+                                  const int32_t* block_table, int history_len, int chunk_len, int Hq, int Hkv, int D,
+                                  int block_size, float softmax_scale, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Debug: raw int32 QK accumulators acc[b, h, t] = sum_d q_i8[b,h,d] *        */
+/* K_i8[b, t, h / G, d] for t < seq_lens[b]; 0 for t in [seq_lens[b],        */
+/* max_len).  Uses the decode kernel's paged-K addressing and MMA fragments, */
+/* so a bit-exact match validates both ([PV] §2: the int32 accumulator).     */
+/* acc: int32 [B, Hq, max_len].                                              */
+/* ------------------------------------------------------------------------ */
+i8kv_status i8kv_debug_qk_i32(int32_t* acc, const int8_t* q_i8, const int8_t* k_cache, const int32_t* block_tables,
+                              const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size, int max_blocks,
+                              int max_len, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* BF16-KV comparison path (the pages' BF16 control: same paging, bf16      */
+/* elements, bf16 tensor-core contractions, fp32 softmax; [KV] §4.2).       */
+/*   K cache bf16 [NB, Hkv, D/8, bs, 8], V cache bf16 [NB, Hkv, D, bs].      */
+/* ------------------------------------------------------------------------ */
+i8kv_status i8kv_bf16_kv_write(const uint16_t* k, const uint16_t* v, const int32_t* slot_mapping, int T, int Hkv,
+                               int D, int block_size, int num_blocks, uint16_t* k_cache, uint16_t* v_cache,
+                               void* stream);
+
+/* Plain softmax decode attention over the bf16 cache with the same 256-token
+ * partitions and log-sum-exp merge.  q: bf16 [B, Hq, D]; out: fp32 [B, Hq, D].
+ * The workspace follows the same rules and size as the INT8 decode's. */
+i8kv_status i8kv_bf16_paged_decode_attn(float* out, const uint16_t* q, const uint16_t* k_cache,
+                                        const uint16_t* v_cache, const int32_t* block_tables,
+                                        const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
+                                        int max_blocks, float softmax_scale, int partition, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* I8KV_H_ */
