@@ -24,7 +24,13 @@
  *        K/V scale fp32  [NB, bs, Hkv]             one scale per (token, KV head)
  *    A token at slot s lives in block s / bs at offset s % bs.  A sequence's
  *    token at position p lives in block block_table[p / bs], offset p % bs.
- *  - Cache and Q/out pointers must be 16-byte aligned.
+ *  - Cache, scale, Q and workspace pointers must be 16-byte aligned.
+ *  - num_blocks is the pool size (blocks).  Kernels that read the cache check
+ *    every block-table entry against it: an entry outside [0, num_blocks) is
+ *    not read, the result is undefined, and the device error word records 2.
+ *    A sequence length above max_blocks * block_size is clamped and recorded
+ *    the same way.  Host-side checks cannot see device data, so these are the
+ *    only checks on table contents.
  *  - Supported shapes: D in {128, 256}; Hq % Hkv == 0 with G = Hq / Hkv <= 8;
  *    query head h reads KV head h / G.
  *  - Quantization is symmetric INT8 with an fp32 absmax/127 scale per (token,
@@ -57,7 +63,8 @@ i8kv_status i8kv_last_error(char* buf, size_t n);
 /* Reads and clears the device error word (synchronizes the device).  *code is
  * 0 when no kernel recorded a failure; otherwise the first failure's code:
  * 1 = a pipeline wait exceeded its time limit, 2 = a block-table or slot entry
- * out of range (checked kernels only).  Returns I8KV_ERR_DEVICE if *code != 0. */
+ * or sequence length out of range (the access was skipped).  Returns
+ * I8KV_ERR_DEVICE if *code != 0. */
 i8kv_status i8kv_device_error(int* code);
 
 /* Library version (major * 10000 + minor * 100 + patch). */
@@ -68,12 +75,15 @@ int i8kv_version(void);
 /* For every token t < T with slot_mapping[t] >= 0 and every KV head h:      */
 /*   quantize k[t,h,:] and v[t,h,:] (bf16 [T, Hkv, D]) per the rule above,   */
 /*   store the codes at slot_mapping[t] in k_cache / v_cache and the scales  */
-/*   in k_scale / v_scale.  slot_mapping[t] < 0 skips token t.               */
+/*   in k_scale / v_scale.                                                   */
 /* When q != NULL also quantize q (bf16 [T, Hq, D]) per (token, q-head) into */
 /*   q_i8 (int8 [T, Hq, D]) and q_scale (fp32 [T, Hq]) -- the query is       */
 /*   quantized once and reused by every history partition ([KV] §2.2).       */
 /* Slots must lie inside the pool (num_blocks * block_size); two tokens with */
-/* the same slot race.  The output codes and scales are bit-exact with the   */
+/* the same slot race.  A slot >= num_blocks * block_size is skipped and    */
+/* recorded in the device error word (2).  slot < 0 skips only the K/V      */
+/* write; the query row is still quantized.                                 */
+/* The output codes and scales are bit-exact with the                       */
 /* fp32 IEEE evaluation of the formula (division, not reciprocal).           */
 /* ------------------------------------------------------------------------ */
 i8kv_status i8kv_kv_quant_write(const uint16_t* k, const uint16_t* v, const int32_t* slot_mapping, int T, int Hkv,
@@ -106,8 +116,8 @@ size_t i8kv_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_blocks
 i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
                                         const int8_t* v_cache, const float* k_scale, const float* v_scale,
                                         const int32_t* block_tables, const int32_t* seq_lens, int B, int Hq, int Hkv,
-                                        int D, int block_size, int max_blocks, float softmax_scale, int partition,
-                                        void* workspace, size_t workspace_bytes, void* stream);
+                                        int D, int block_size, int max_blocks, int num_blocks, float softmax_scale,
+                                        int partition, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* INT8 prefix-prefill chunk ([PV] §2.1, [KV] §3.2): one online softmax over */
@@ -126,7 +136,7 @@ i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const fl
 i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
                                   const int8_t* v_cache, const float* k_scale, const float* v_scale,
                                   const int32_t* block_table, int history_len, int chunk_len, int Hq, int Hkv, int D,
-                                  int block_size, float softmax_scale, void* stream);
+                                  int block_size, int num_blocks, float softmax_scale, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Debug: raw int32 QK accumulators acc[b, h, t] = sum_d q_i8[b,h,d] *        */
@@ -137,7 +147,7 @@ i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q
 /* ------------------------------------------------------------------------ */
 i8kv_status i8kv_debug_qk_i32(int32_t* acc, const int8_t* q_i8, const int8_t* k_cache, const int32_t* block_tables,
                               const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size, int max_blocks,
-                              int max_len, void* stream);
+                              int num_blocks, int max_len, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* BF16-KV comparison path (the pages' BF16 control: same paging, bf16      */
@@ -154,8 +164,8 @@ i8kv_status i8kv_bf16_kv_write(const uint16_t* k, const uint16_t* v, const int32
 i8kv_status i8kv_bf16_paged_decode_attn(float* out, const uint16_t* q, const uint16_t* k_cache,
                                         const uint16_t* v_cache, const int32_t* block_tables,
                                         const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
-                                        int max_blocks, float softmax_scale, int partition, void* workspace,
-                                        size_t workspace_bytes, void* stream);
+                                        int max_blocks, int num_blocks, float softmax_scale, int partition,
+                                        void* workspace, size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,25 @@
+"""INT8 KV-cache paged attention for GB300 (sm_103a).
+
+The compute lives in libi8kv.so (hand-written CUDA, C ABI in include/i8kv.h);
+this package holds its sources (csrc/), the in-tree build (build.py) and the
+thin ctypes binding (binding.py)."""
+from .binding import (  # noqa: F401
+    BLOCK_SIZE,
+    PARTITION,
+    I8KVError,
+    alloc_bf16_cache,
+    alloc_int8_cache,
+    bf16_kv_write,
+    bf16_paged_decode_attn,
+    debug_qk_i32,
+    decode_workspace,
+    decode_workspace_bytes,
+    device_error,
+    int8_paged_decode_attn,
+    int8_prefix_attn,
+    kv_quant_write,
+    last_error,
+    lib,
+    library_path,
+    version,
+)

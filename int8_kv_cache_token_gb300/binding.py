@@ -1,0 +1,228 @@
+"""Thin Python binding of libi8kv.so (the C ABI in include/i8kv.h).
+
+Argument marshalling only: every function checks dtypes/shapes/devices of the
+torch tensors it is given, passes their device pointers and the current CUDA
+stream to the C entry point of the same name, and raises I8KVError on a non-OK
+status.  All arithmetic happens in the CUDA kernels.  There is no fallback: if
+the library is not built, or a call fails, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE = range(6)
+BLOCK_SIZE = 16
+PARTITION = 256
+
+
+class I8KVError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"i8kv status {status}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_Z = ctypes.c_size_t
+
+_SIGS = {
+    "i8kv_last_error": [ctypes.c_char_p, _Z],
+    "i8kv_device_error": [ctypes.POINTER(ctypes.c_int)],
+    "i8kv_version": [],
+    "i8kv_kv_quant_write": [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P],
+    "i8kv_decode_workspace_bytes": [_I, _I, _I, _I, _I, _I, _I],
+    "i8kv_int8_paged_decode_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z,
+                                    _P],
+    "i8kv_int8_prefix_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P],
+    "i8kv_debug_qk_i32": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
+    "i8kv_bf16_kv_write": [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P],
+    "i8kv_bf16_paged_decode_attn": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P],
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libi8kv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise I8KVError(ERR_CUDA, f"{path} is missing: build it with int8_kv_cache_token_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        for name, args in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = _I
+        L.i8kv_decode_workspace_bytes.restype = _Z
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    buf = ctypes.create_string_buffer(512)
+    lib().i8kv_last_error(buf, 512)
+    return buf.value.decode(errors="replace")
+
+
+def _check(status: int):
+    if status != OK:
+        raise I8KVError(status, last_error())
+
+
+def version() -> int:
+    return int(lib().i8kv_version())
+
+
+def device_error() -> int:
+    """Synchronize, read and clear the device error word (0 = no failure)."""
+    code = ctypes.c_int(0)
+    st = lib().i8kv_device_error(ctypes.byref(code))
+    if st not in (OK, ERR_DEVICE):
+        _check(st)
+    return int(code.value)
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise I8KVError(ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise I8KVError(ERR_INVALID_ARG, f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise I8KVError(ERR_INVALID_ARG, f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _bf16(t, name):
+    """bf16 tensors travel as raw 16-bit payloads (torch.bfloat16 or int16/uint16 bit patterns)."""
+    if t is None:
+        return None
+    if t.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise I8KVError(ERR_INVALID_ARG, f"{name} must be bfloat16 (or its 16-bit pattern), got {t.dtype}")
+    return _ptr(t, None, name)
+
+
+# ----------------------------------------------------------------------------- cache helpers
+def alloc_int8_cache(num_blocks: int, Hkv: int, D: int, device="cuda"):
+    """Zeroed INT8 cache tensors in the library's layouts."""
+    return dict(
+        k_cache=torch.zeros((num_blocks, Hkv, D // 16, BLOCK_SIZE, 16), dtype=torch.int8, device=device),
+        v_cache=torch.zeros((num_blocks, Hkv, D, BLOCK_SIZE), dtype=torch.int8, device=device),
+        k_scale=torch.zeros((num_blocks, BLOCK_SIZE, Hkv), dtype=torch.float32, device=device),
+        v_scale=torch.zeros((num_blocks, BLOCK_SIZE, Hkv), dtype=torch.float32, device=device),
+    )
+
+
+def alloc_bf16_cache(num_blocks: int, Hkv: int, D: int, device="cuda"):
+    return dict(
+        k_cache=torch.zeros((num_blocks, Hkv, D // 8, BLOCK_SIZE, 8), dtype=torch.bfloat16, device=device),
+        v_cache=torch.zeros((num_blocks, Hkv, D, BLOCK_SIZE), dtype=torch.bfloat16, device=device),
+    )
+
+
+def _cache_geom(k_cache: torch.Tensor, elems_per_chunk: int):
+    if k_cache.dim() != 5 or k_cache.shape[3] != BLOCK_SIZE or k_cache.shape[4] != elems_per_chunk:
+        raise I8KVError(ERR_INVALID_ARG, f"k_cache shape {tuple(k_cache.shape)} is not [NB, Hkv, D/x, 16, x]")
+    NB, Hkv, nchunk = k_cache.shape[:3]
+    return NB, Hkv, nchunk * elems_per_chunk
+
+
+# ----------------------------------------------------------------------------- producer
+def kv_quant_write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, q=None, q_i8=None, q_scale=None,
+                   stream=None):
+    """Quantize k, v [T, Hkv, D] (bf16) into the paged INT8 cache at slot_mapping [T];
+    with q [T, Hq, D] also write q_i8 [T, Hq, D] and q_scale [T, Hq]."""
+    NB, Hkv, D = _cache_geom(k_cache, 16)
+    T = k.shape[0]
+    Hq = 0 if q is None else q.shape[1]
+    _check(lib().i8kv_kv_quant_write(
+        _bf16(k, "k"), _bf16(v, "v"), _ptr(slot_mapping, torch.int32, "slot_mapping"), T, Hkv, D, BLOCK_SIZE, NB,
+        _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
+        _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
+        _bf16(q, "q"), Hq, _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
+        _stream(stream)))
+
+
+def bf16_kv_write(k, v, slot_mapping, k_cache, v_cache, stream=None):
+    NB, Hkv, D = _cache_geom(k_cache, 8)
+    _check(lib().i8kv_bf16_kv_write(
+        _bf16(k, "k"), _bf16(v, "v"), _ptr(slot_mapping, torch.int32, "slot_mapping"), k.shape[0], Hkv, D,
+        BLOCK_SIZE, NB, _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- decode
+def decode_workspace_bytes(B: int, Hq: int, Hkv: int, D: int, max_blocks: int) -> int:
+    return int(lib().i8kv_decode_workspace_bytes(B, Hq, Hkv, D, max_blocks, BLOCK_SIZE, PARTITION))
+
+
+def decode_workspace(B: int, Hq: int, Hkv: int, D: int, max_blocks: int, device="cuda") -> torch.Tensor:
+    """A zero-filled decode workspace (reusable by later calls on the same stream)."""
+    n = decode_workspace_bytes(B, Hq, Hkv, D, max_blocks)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def int8_paged_decode_attn(out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
+                           workspace, softmax_scale: float = 0.0, partition: int = PARTITION, stream=None):
+    """out [B, Hq, D] fp32 <- INT8 paged decode attention of q_i8 [B, Hq, D] over the cache."""
+    NB, Hkv, D = _cache_geom(k_cache, 16)
+    B, Hq, _ = q_i8.shape
+    _check(lib().i8kv_int8_paged_decode_attn(
+        _ptr(out, torch.float32, "out"), _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
+        _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
+        _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
+        _ptr(block_tables, torch.int32, "block_tables"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        B, Hq, Hkv, D, BLOCK_SIZE, block_tables.shape[1], NB, float(softmax_scale), partition,
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def bf16_paged_decode_attn(out, q, k_cache, v_cache, block_tables, seq_lens, workspace, softmax_scale: float = 0.0,
+                           partition: int = PARTITION, stream=None):
+    NB, Hkv, D = _cache_geom(k_cache, 8)
+    B, Hq, _ = q.shape
+    _check(lib().i8kv_bf16_paged_decode_attn(
+        _ptr(out, torch.float32, "out"), _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"),
+        _ptr(block_tables, torch.int32, "block_tables"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        B, Hq, Hkv, D, BLOCK_SIZE, block_tables.shape[1], NB, float(softmax_scale), partition,
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def debug_qk_i32(acc, q_i8, k_cache, block_tables, seq_lens, stream=None):
+    """acc [B, Hq, max_len] int32 <- raw INT8 QK accumulators."""
+    NB, Hkv, D = _cache_geom(k_cache, 16)
+    B, Hq, _ = q_i8.shape
+    _check(lib().i8kv_debug_qk_i32(
+        _ptr(acc, torch.int32, "acc"), _ptr(q_i8, torch.int8, "q_i8"), _ptr(k_cache, torch.int8, "k_cache"),
+        _ptr(block_tables, torch.int32, "block_tables"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        B, Hq, Hkv, D, BLOCK_SIZE, block_tables.shape[1], NB, acc.shape[2], _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- prefix
+def int8_prefix_attn(out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, history_len: int,
+                     softmax_scale: float = 0.0, stream=None):
+    """out [C, Hq, D] fp32 <- INT8 prefix-chunk attention of q_i8 [C, Hq, D] over history + chunk."""
+    NB, Hkv, D = _cache_geom(k_cache, 16)
+    C, Hq, _ = q_i8.shape
+    _check(lib().i8kv_int8_prefix_attn(
+        _ptr(out, torch.float32, "out"), _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
+        _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
+        _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
+        _ptr(block_table, torch.int32, "block_table"), int(history_len), C, Hq, Hkv, D, BLOCK_SIZE, NB,
+        float(softmax_scale), _stream(stream)))

@@ -1,0 +1,245 @@
+// api.cu -- the extern "C" boundary declared in include/i8kv.h: argument
+// checking, status codes, the last-error string and the launches.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/i8kv.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+i8kv_status fail(i8kv_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+
+i8kv_status fail(i8kv_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+i8kv_status from_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return I8KV_OK;
+  return fail(I8KV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define REQUIRE(cond, status, ...) \
+  do {                             \
+    if (!(cond)) return fail(status, __VA_ARGS__); \
+  } while (0)
+
+i8kv_status check_heads(int Hq, int Hkv, int D) {
+  REQUIRE(Hq > 0 && Hkv > 0, I8KV_ERR_INVALID_ARG, "Hq=%d Hkv=%d must be positive", Hq, Hkv);
+  REQUIRE(Hq % Hkv == 0, I8KV_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  REQUIRE(Hq / Hkv <= 8, I8KV_ERR_UNSUPPORTED, "G=Hq/Hkv=%d > 8 is not supported", Hq / Hkv);
+  REQUIRE(D == 128 || D == 256, I8KV_ERR_UNSUPPORTED, "head_dim %d not supported (128 or 256)", D);
+  REQUIRE(Hkv <= 8, I8KV_ERR_UNSUPPORTED, "Hkv=%d > 8 is not supported", Hkv);
+  return I8KV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+i8kv_status i8kv_last_error(char* buf, size_t n) {
+  if (buf && n) {
+    std::strncpy(buf, g_last_error.c_str(), n - 1);
+    buf[n - 1] = '\0';
+  }
+  return I8KV_OK;
+}
+
+i8kv_status i8kv_device_error(int* code) {
+  REQUIRE(code != nullptr, I8KV_ERR_INVALID_ARG, "code is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return from_cuda(e, "i8kv_device_error: synchronize");
+  int v = 0;
+  cudaError_t (*readers[])(int*) = {i8kv::read_error_producer, i8kv::read_error_decode, i8kv::read_error_prefix};
+  for (auto rd : readers) {
+    int x = 0;
+    e = rd(&x);
+    if (e != cudaSuccess) return from_cuda(e, "i8kv_device_error: read");
+    if (v == 0) v = x;
+  }
+  *code = v;
+  if (v != 0) return fail(I8KV_ERR_DEVICE, "a kernel recorded device error %d", v);
+  return I8KV_OK;
+}
+
+int i8kv_version(void) { return 100; }
+
+i8kv_status i8kv_kv_quant_write(const uint16_t* k, const uint16_t* v, const int32_t* slot_mapping, int T, int Hkv,
+                                int D, int block_size, int num_blocks, int8_t* k_cache, int8_t* v_cache,
+                                float* k_scale, float* v_scale, const uint16_t* q, int Hq, int8_t* q_i8,
+                                float* q_scale, void* stream) {
+  REQUIRE(T >= 0, I8KV_ERR_INVALID_ARG, "T=%d < 0", T);
+  REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+  REQUIRE(D == 128 || D == 256, I8KV_ERR_UNSUPPORTED, "head_dim %d not supported (128 or 256)", D);
+  REQUIRE(Hkv > 0 && Hkv <= 8, I8KV_ERR_UNSUPPORTED, "Hkv=%d not in 1..8", Hkv);
+  REQUIRE(num_blocks > 0, I8KV_ERR_INVALID_ARG, "num_blocks=%d", num_blocks);
+  if (T == 0) return I8KV_OK;
+  REQUIRE(k && v && slot_mapping && k_cache && v_cache && k_scale && v_scale, I8KV_ERR_INVALID_ARG,
+          "null K/V/slot/cache/scale pointer");
+  REQUIRE(aligned16(k) && aligned16(v) && aligned16(k_cache) && aligned16(v_cache), I8KV_ERR_INVALID_ARG,
+          "K/V inputs and caches must be 16-byte aligned");
+  if (q) {
+    REQUIRE(Hq > 0, I8KV_ERR_INVALID_ARG, "Hq=%d with a query", Hq);
+    REQUIRE(q_i8 && q_scale, I8KV_ERR_INVALID_ARG, "q given without q_i8/q_scale");
+    REQUIRE(aligned16(q) && aligned16(q_i8), I8KV_ERR_INVALID_ARG, "q and q_i8 must be 16-byte aligned");
+  }
+  i8kv::ProducerParams p{k, v, slot_mapping, T, Hkv, D, num_blocks, k_cache, v_cache, k_scale, v_scale,
+                         q, q ? Hq : 0, q_i8, q_scale};
+  return from_cuda(i8kv::launch_kv_quant_write(p, static_cast<cudaStream_t>(stream)), "kv_quant_write launch");
+}
+
+size_t i8kv_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_blocks, int block_size, int partition) {
+  (void)Hq;
+  (void)block_size;
+  (void)partition;
+  if (B <= 0 || Hkv <= 0 || max_blocks <= 0 || (D != 128 && D != 256)) return 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return i8kv::decode_workspace_bytes(B, Hkv, D, i8kv::decode_grid(dev, B, Hkv, max_blocks));
+}
+
+static i8kv_status decode_common(i8kv::DecodeParams& p, const void* q, const float* q_scale, bool int8,
+                                 const void* k_cache, const void* v_cache, const float* k_scale,
+                                 const float* v_scale, const int32_t* block_tables, const int32_t* seq_lens, int B,
+                                 int Hq, int Hkv, int D, int block_size, int max_blocks, int num_blocks,
+                                 float softmax_scale, int partition, void* workspace, size_t workspace_bytes,
+                                 float* out) {
+  REQUIRE(B >= 0, I8KV_ERR_INVALID_ARG, "B=%d < 0", B);
+  i8kv_status s = check_heads(Hq, Hkv, D);
+  if (s != I8KV_OK) return s;
+  REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+  REQUIRE(partition == 256, I8KV_ERR_UNSUPPORTED, "partition %d not supported (256)", partition);
+  REQUIRE(max_blocks > 0 && num_blocks > 0, I8KV_ERR_INVALID_ARG, "max_blocks=%d num_blocks=%d", max_blocks,
+          num_blocks);
+  REQUIRE(out && q && k_cache && v_cache && block_tables && seq_lens, I8KV_ERR_INVALID_ARG, "null pointer");
+  if (int8) REQUIRE(q_scale && k_scale && v_scale, I8KV_ERR_INVALID_ARG, "null scale pointer");
+  REQUIRE(aligned16(k_cache) && aligned16(v_cache) && aligned16(q), I8KV_ERR_INVALID_ARG,
+          "caches and q must be 16-byte aligned");
+  if (int8) REQUIRE(aligned16(k_scale) && aligned16(v_scale), I8KV_ERR_INVALID_ARG, "scales must be 16-byte aligned");
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int grid = i8kv::decode_grid(dev, B, Hkv, max_blocks);
+  const size_t need = i8kv::decode_workspace_bytes(B, Hkv, D, grid);
+  REQUIRE(workspace != nullptr && workspace_bytes >= need, I8KV_ERR_WORKSPACE,
+          "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+  REQUIRE(aligned16(workspace), I8KV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  const size_t slots = (size_t)B * Hkv + grid;
+  float* ws = static_cast<float*>(workspace);
+  p.out = out;
+  p.q = q;
+  p.q_scale = q_scale;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.D = D;
+  p.max_blocks = max_blocks;
+  p.num_blocks = num_blocks;
+  p.sm_scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
+  p.ws_part = ws;
+  p.ws_count = reinterpret_cast<int*>(ws + slots * (8 * (size_t)D + 16));
+  p.grid = grid;
+  return I8KV_OK;
+}
+
+i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
+                                        const int8_t* v_cache, const float* k_scale, const float* v_scale,
+                                        const int32_t* block_tables, const int32_t* seq_lens, int B, int Hq, int Hkv,
+                                        int D, int block_size, int max_blocks, int num_blocks, float softmax_scale,
+                                        int partition, void* workspace, size_t workspace_bytes, void* stream) {
+  i8kv::DecodeParams p{};
+  i8kv_status s = decode_common(p, q_i8, q_scale, true, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
+                                B, Hq, Hkv, D, block_size, max_blocks, num_blocks, softmax_scale, partition,
+                                workspace, workspace_bytes, out);
+  if (s != I8KV_OK || B == 0) return s;
+  return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "int8 decode launch");
+}
+
+i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
+                                  const int8_t* v_cache, const float* k_scale, const float* v_scale,
+                                  const int32_t* block_table, int history_len, int chunk_len, int Hq, int Hkv, int D,
+                                  int block_size, int num_blocks, float softmax_scale, void* stream) {
+  REQUIRE(history_len >= 0 && chunk_len >= 0, I8KV_ERR_INVALID_ARG, "history_len=%d chunk_len=%d", history_len,
+          chunk_len);
+  i8kv_status s = check_heads(Hq, Hkv, D);
+  if (s != I8KV_OK) return s;
+  REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+  REQUIRE(num_blocks > 0, I8KV_ERR_INVALID_ARG, "num_blocks=%d", num_blocks);
+  if (chunk_len == 0) return I8KV_OK;
+  REQUIRE(out && q_i8 && q_scale && k_cache && v_cache && k_scale && v_scale && block_table, I8KV_ERR_INVALID_ARG,
+          "null pointer");
+  REQUIRE(aligned16(k_cache) && aligned16(v_cache) && aligned16(q_i8) && aligned16(k_scale) && aligned16(v_scale),
+          I8KV_ERR_INVALID_ARG, "caches, scales and q must be 16-byte aligned");
+  i8kv::PrefixParams p{out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, history_len, chunk_len,
+                       Hq, Hkv, Hq / Hkv, D, num_blocks, softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D)};
+  return from_cuda(i8kv::launch_int8_prefix(p, static_cast<cudaStream_t>(stream)), "int8 prefix launch");
+}
+
+i8kv_status i8kv_debug_qk_i32(int32_t* acc, const int8_t* q_i8, const int8_t* k_cache, const int32_t* block_tables,
+                              const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size, int max_blocks,
+                              int num_blocks, int max_len, void* stream) {
+  REQUIRE(B >= 0 && max_len >= 0, I8KV_ERR_INVALID_ARG, "B=%d max_len=%d", B, max_len);
+  i8kv_status s = check_heads(Hq, Hkv, D);
+  if (s != I8KV_OK) return s;
+  REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+  REQUIRE(max_blocks > 0 && num_blocks > 0, I8KV_ERR_INVALID_ARG, "max_blocks=%d num_blocks=%d", max_blocks,
+          num_blocks);
+  if (B == 0 || max_len == 0) return I8KV_OK;
+  REQUIRE(acc && q_i8 && k_cache && block_tables && seq_lens, I8KV_ERR_INVALID_ARG, "null pointer");
+  REQUIRE(aligned16(k_cache) && aligned16(q_i8), I8KV_ERR_INVALID_ARG, "k_cache and q must be 16-byte aligned");
+  i8kv::DebugQKParams p{acc, q_i8, k_cache, block_tables, seq_lens, B, Hq, Hkv, Hq / Hkv, D, max_blocks, num_blocks,
+                        max_len};
+  return from_cuda(i8kv::launch_debug_qk(p, static_cast<cudaStream_t>(stream)), "debug qk launch");
+}
+
+i8kv_status i8kv_bf16_kv_write(const uint16_t* k, const uint16_t* v, const int32_t* slot_mapping, int T, int Hkv,
+                               int D, int block_size, int num_blocks, uint16_t* k_cache, uint16_t* v_cache,
+                               void* stream) {
+  REQUIRE(T >= 0, I8KV_ERR_INVALID_ARG, "T=%d < 0", T);
+  REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+  REQUIRE(D == 128 || D == 256, I8KV_ERR_UNSUPPORTED, "head_dim %d not supported (128 or 256)", D);
+  REQUIRE(Hkv > 0, I8KV_ERR_INVALID_ARG, "Hkv=%d", Hkv);
+  REQUIRE(num_blocks > 0, I8KV_ERR_INVALID_ARG, "num_blocks=%d", num_blocks);
+  if (T == 0) return I8KV_OK;
+  REQUIRE(k && v && slot_mapping && k_cache && v_cache, I8KV_ERR_INVALID_ARG, "null pointer");
+  REQUIRE(aligned16(k) && aligned16(v) && aligned16(k_cache) && aligned16(v_cache), I8KV_ERR_INVALID_ARG,
+          "K/V inputs and caches must be 16-byte aligned");
+  i8kv::ProducerParams p{k, v, slot_mapping, T, Hkv, D, num_blocks, nullptr, nullptr, nullptr, nullptr,
+                         nullptr, 0, nullptr, nullptr};
+  return from_cuda(i8kv::launch_bf16_kv_write(p, k_cache, v_cache, static_cast<cudaStream_t>(stream)),
+                   "bf16 kv write launch");
+}
+
+i8kv_status i8kv_bf16_paged_decode_attn(float* out, const uint16_t* q, const uint16_t* k_cache,
+                                        const uint16_t* v_cache, const int32_t* block_tables,
+                                        const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
+                                        int max_blocks, int num_blocks, float softmax_scale, int partition,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  i8kv::DecodeParams p{};
+  i8kv_status s = decode_common(p, q, nullptr, false, k_cache, v_cache, nullptr, nullptr, block_tables, seq_lens, B,
+                                Hq, Hkv, D, block_size, max_blocks, num_blocks, softmax_scale, partition, workspace,
+                                workspace_bytes, out);
+  if (s != I8KV_OK || B == 0) return s;
+  return from_cuda(i8kv::launch_bf16_decode(p, static_cast<cudaStream_t>(stream)), "bf16 decode launch");
+}
+
+}  // extern "C"

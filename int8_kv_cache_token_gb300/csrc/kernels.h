@@ -1,0 +1,83 @@
+// kernels.h -- internal launch interface between the C-ABI layer (api.cu) and
+// the kernels.  Host-side argument checking happens in api.cu; these launchers
+// assume valid arguments.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace i8kv {
+
+struct ProducerParams {
+  const uint16_t* k;
+  const uint16_t* v;
+  const int32_t* slots;
+  int T, Hkv, D, num_blocks;
+  int8_t* k_cache;
+  int8_t* v_cache;
+  float* k_scale;
+  float* v_scale;
+  const uint16_t* q;  // nullable
+  int Hq;
+  int8_t* q_i8;
+  float* q_scale;
+};
+
+// Decode (INT8 and BF16-KV variants share the work split and the workspace).
+struct DecodeParams {
+  float* out;                 // [B, Hq, D]
+  const void* q;              // int8 [B, Hq, D] (INT8 path) or bf16 [B, Hq, D] (BF16 path)
+  const float* q_scale;       // [B, Hq] (INT8 path)
+  const void* k_cache;
+  const void* v_cache;
+  const float* k_scale;       // INT8 path
+  const float* v_scale;
+  const int32_t* block_tables;  // [B, max_blocks]
+  const int32_t* seq_lens;      // [B]
+  int B, Hq, Hkv, G, D, max_blocks, num_blocks;
+  float sm_scale;
+  float* ws_part;             // [(B*Hkv + grid) slots][8 rows * D + 16]
+  int* ws_count;              // [B*Hkv]
+  int grid;                   // CTAs launched (the work split depends on it)
+};
+
+// Debug QK: int32 accumulators through the decode kernel's QK fragments.
+struct DebugQKParams {
+  int32_t* acc;               // [B, Hq, max_len]
+  const int8_t* q;            // [B, Hq, D]
+  const int8_t* k_cache;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  int B, Hq, Hkv, G, D, max_blocks, num_blocks, max_len;
+};
+
+struct PrefixParams {
+  float* out;                 // [C, Hq, D]
+  const int8_t* q;            // [C, Hq, D]
+  const float* q_scale;       // [C, Hq]
+  const int8_t* k_cache;
+  const int8_t* v_cache;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* block_table;
+  int H, C, Hq, Hkv, G, D, num_blocks;
+  float sm_scale;
+};
+
+// Per-translation-unit device error words (read and cleared).
+cudaError_t read_error_producer(int* value);
+cudaError_t read_error_decode(int* value);
+cudaError_t read_error_prefix(int* value);
+
+cudaError_t launch_kv_quant_write(const ProducerParams& p, cudaStream_t stream);
+cudaError_t launch_bf16_kv_write(const ProducerParams& p, uint16_t* k_cache, uint16_t* v_cache, cudaStream_t stream);
+
+// Per-device decode geometry: CTAs per launch and dynamic shared memory.
+int decode_grid(int device, int B, int Hkv, int max_blocks);
+size_t decode_workspace_bytes(int B, int Hkv, int D, int grid);
+cudaError_t launch_int8_decode(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_bf16_decode(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_debug_qk(const DebugQKParams& p, cudaStream_t stream);
+cudaError_t launch_int8_prefix(const PrefixParams& p, cudaStream_t stream);
+
+}  // namespace i8kv

@@ -1,0 +1,70 @@
+"""The C-ABI library builds, loads and exports every entry point include/i8kv.h
+declares; host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from int8_kv_cache_token_gb300 import build
+    return ctypes.CDLL(build.build())
+
+
+def declared_entry_points():
+    text = open(os.path.join(ROOT, "include", "i8kv.h"), encoding="utf-8").read()
+    return sorted(set(re.findall(r"^(?:i8kv_status|size_t|int)\s+(i8kv_\w+)\s*\(", text, re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_entry_points()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/i8kv.h but not exported"
+
+
+def test_version(lib):
+    assert lib.i8kv_version() == 100
+
+
+def _last_error(lib):
+    buf = ctypes.create_string_buffer(256)
+    lib.i8kv_last_error(buf, 256)
+    return buf.value.decode()
+
+
+def test_argument_checks_without_gpu(lib):
+    P = ctypes.c_void_p
+    # unsupported block size
+    f = lib.i8kv_kv_quant_write
+    f.restype = ctypes.c_int
+    assert f(P(16), P(16), P(16), 4, 4, 256, 8, 10, P(16), P(16), P(16), P(16), None, 0, None, None, None) == 2
+    assert "block_size" in _last_error(lib)
+    # unsupported head_dim
+    assert f(P(16), P(16), P(16), 4, 4, 64, 16, 10, P(16), P(16), P(16), P(16), None, 0, None, None, None) == 2
+    # null pointers with T > 0
+    assert f(None, P(16), P(16), 4, 4, 256, 16, 10, P(16), P(16), P(16), P(16), None, 0, None, None, None) == 1
+    # misaligned cache pointer
+    assert f(P(16), P(16), P(16), 4, 4, 256, 16, 10, P(17), P(16), P(16), P(16), None, 0, None, None, None) == 1
+    assert "aligned" in _last_error(lib)
+    # T == 0 is a no-op
+    assert f(None, None, None, 0, 4, 256, 16, 10, None, None, None, None, None, 0, None, None, None) == 0
+    # decode: Hq not a multiple of Hkv, G > 8, partition != 256
+    d = lib.i8kv_int8_paged_decode_attn
+    d.restype = ctypes.c_int
+    d.argtypes = [P] * 9 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int, P, ctypes.c_size_t, P]
+    args = [P(16)] * 9
+    assert d(*args, 1, 10, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20, None) == 1
+    assert d(*args, 1, 72, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20, None) == 2
+    assert d(*args, 1, 24, 4, 256, 16, 8, 10, 0.0, 512, P(16), 1 << 20, None) == 2
+    assert "partition" in _last_error(lib)
+    # prefix: chunk_len == 0 is a no-op; negative history rejected
+    pf = lib.i8kv_int8_prefix_attn
+    pf.restype = ctypes.c_int
+    pf.argtypes = [P] * 8 + [ctypes.c_int] * 7 + [ctypes.c_float, P]
+    assert pf(*([P(16)] * 8), 100, 0, 24, 4, 256, 16, 10, 0.0, None) == 0
+    assert pf(*([P(16)] * 8), -1, 5, 24, 4, 256, 16, 10, 0.0, None) == 1
