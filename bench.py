@@ -1,0 +1,554 @@
+#!/usr/bin/env python3
+"""Benchmark: INT8 paged decode attention, effective KV GB/s (and the rest of the path).
+
+Workload (N = 1): single-sequence decode with 24 query / 4 KV heads, head_dim
+256, block size 16, histories 8192, 16384 and 32768 (K with 4 outlier channels
+per KV head x20, V N(0,1), seeded), i.e. the long-history decode configuration.
+One step = one new token through the 16 full-attention layers of the pages'
+model: for every (layer, history) the producer quantizes the new token's K/V
+into that layer's paged INT8 cache and quantizes its query, then the INT8
+decode kernel attends over the whole history.  Each layer owns its cache, so a
+step streams 16 x 56K tokens x 2080 B = 1.9 GB and L2 (129 MB) holds none of
+it between steps.  All K timed steps run as one CUDA graph; timing events sit
+around the graph and (as external event nodes) around every decode launch.
+
+  value     = KV bytes read by the decode launches / timed wall time (GB/s)
+  roofline  = same bytes / summed decode-kernel time, against measured HBM copy
+              bandwidth (MEASURED_PEAKS.json)
+  e2e       = the same step through the C ABI with pinned host buffers: the new
+              tokens' q/k/v copied host->device and every output copied back,
+              inside the timed graph
+  secondary = per-history decode times, BF16-KV comparison decode, prefix chunk
+              TOPS, producer throughput (measured after the main timed region)
+
+--impl reference times the CPU oracle instead (bounded samples of the same
+decode), on the host cores, and prints the same JSON line with "impl".
+Multi-GPU (torchrun): every rank runs the same per-GPU workload (weak scaling,
+no collective on the data path); rank 0 prints the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "INT8 paged decode attn effective KV GB/s (% HBM peak); prefix-chunk INT8 TOPS"
+HISTORIES = (8192, 16384, 32768)
+LAYERS = 16          # full-attention layers of the pages' model
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 0.0)), "measured"
+    return FALLBACK_HBM_GBS, 1900.0, "fallback"
+
+
+def kernel_hash(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kind: str, src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (same hash); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and parts[0] == kind and parts[1] == src_hash:
+                return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.samples = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        rows = [s for (t, s) in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not rows:
+            rows = [s for (_, s) in self.samples]
+            window = "whole run (timed region shorter than one sample)"
+        mhz, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                mhz.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(mhz), "window": window}
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- reference (oracle) arm
+def oracle_decode_sample():
+    """The oracle's inputs for one (layer, 8192-history) decode of the workload."""
+    from oracle import oracle as orc
+    w = wl.decode_outlier(HISTORIES[0])
+    k, v = w.kv(0)
+    cache = orc.kv_quant_write(k, v, w.slots(0), w.num_blocks, w.block_size)
+    q = w.q()
+    q_i8 = np.empty(q.shape, np.int8)
+    q_s = np.empty(q.shape[:2], np.float32)
+    for h in range(q.shape[1]):
+        q_i8[0, h], q_s[0, h] = orc.quantize_vector(q[0, h])
+    return w, cache, q_i8, q_s
+
+
+def time_oracle(budget_s: float, nthreads: int):
+    """Oracle decode of the 8192-token history (all 24 heads), repeated for about budget_s."""
+    from oracle import oracle as orc
+    w, cache, q_i8, q_s = oracle_decode_sample()
+    reps, t_total = 0, 0.0
+    while t_total < budget_s or reps == 0:
+        t0 = time.perf_counter()
+        orc.decode_attn(q_i8, q_s, cache, w.block_tables, w.seq_lens, w.block_size, nthreads=nthreads)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    gbs = reps * w.kv_bytes_int8() / t_total / 1e9
+    return gbs, reps, t_total
+
+
+def run_reference(args):
+    from oracle import oracle as orc
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    orc.build()
+    cores = cpu_cores()
+    w, cache, q_i8, q_s = oracle_decode_sample()
+    # one probe call fixes how many query heads a step samples so that the whole
+    # run (warm-up + steps) stays within about two minutes
+    t0 = time.perf_counter()
+    orc.decode_attn(q_i8, q_s, cache, w.block_tables, w.seq_lens, w.block_size, nthreads=cores)
+    t24 = time.perf_counter() - t0
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    heads = int(max(1, min(24, 24 * per_step_budget / max(t24, 1e-6))))
+    kv_heads = (heads + 5) // 6
+    sub = cache if kv_heads == 4 else _sub_cache(cache, kv_heads)
+    qs = np.ascontiguousarray(q_i8[:, : 6 * kv_heads])
+    qss = np.ascontiguousarray(q_s[:, : 6 * kv_heads])
+
+    def step():
+        orc.decode_attn(qs, qss, sub, w.block_tables, w.seq_lens, w.block_size, nthreads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    bytes_step = HISTORIES[0] * kv_heads * (2 * 256 + 8)
+    value = args.steps * bytes_step / el / 1e9
+    sample = (f"oracle decode of one 8192-token history, {kv_heads * 6} query heads over {kv_heads} KV head(s) "
+              f"per step, {cores} threads")
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "impl": "reference",
+            "config": {"workload": "decode_outlier single-sequence, 24q/4kv heads, head_dim 256, history 8192 "
+                                   "(bounded CPU sample)", "global_batch": 1, "seq_len": HISTORIES[0],
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _sub_cache(cache, kv_heads):
+    """The oracle cache restricted to the first kv_heads KV heads (contiguous copies)."""
+    return dict(k_cache=np.ascontiguousarray(cache["k_cache"][:, :kv_heads]),
+                v_cache=np.ascontiguousarray(cache["v_cache"][:, :kv_heads]),
+                k_scale=np.ascontiguousarray(cache["k_scale"][:, :, :kv_heads]),
+                v_scale=np.ascontiguousarray(cache["v_scale"][:, :, :kv_heads]))
+
+
+# ----------------------------------------------------------------------------- our arm
+class DecodeLayer:
+    """One layer's INT8 cache at one history, plus the new token's buffers."""
+
+    def __init__(self, i8, torch, base, w: wl.DecodeWorkload, k_new, v_new, q_new):
+        self.w = w
+        self.cache = {n: t.clone() for n, t in base.items()}
+        dev = "cuda"
+        self.k = k_new
+        self.v = v_new
+        self.q = q_new
+        L = int(w.seq_lens[0])
+        self.slot = torch.tensor(w.slots(0, L - 1, L), dtype=torch.int32, device=dev)
+        self.q_i8 = torch.empty((1, w.Hq, w.D), dtype=torch.int8, device=dev)
+        self.q_scale = torch.empty((1, w.Hq), dtype=torch.float32, device=dev)
+        self.out = torch.empty((1, w.Hq, w.D), dtype=torch.float32, device=dev)
+        self.bt = torch.from_numpy(w.block_tables).cuda()
+        self.sl = torch.from_numpy(w.seq_lens).cuda()
+
+    def produce(self, i8):
+        i8.kv_quant_write(self.k, self.v, self.slot, **self.cache, q=self.q, q_i8=self.q_i8, q_scale=self.q_scale)
+
+    def decode(self, i8, ws):
+        c = self.cache
+        i8.int8_paged_decode_attn(self.out, self.q_i8, self.q_scale, c["k_cache"], c["v_cache"], c["k_scale"],
+                                  c["v_scale"], self.bt, self.sl, ws)
+
+
+def to_dev(torch, a):
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from int8_kv_cache_token_gb300 import build as ibuild
+    ibuild.build()
+    import int8_kv_cache_token_gb300 as i8
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    hbm_peak, _, peak_kind = measured_peaks()
+    stream = torch.cuda.current_stream()
+
+    # ---- inputs: one seeded history per length, cloned into every layer ----
+    layers = []
+    for L in HISTORIES:
+        w = wl.decode_outlier(L)
+        k, v = w.kv(0)
+        base = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+        i8.kv_quant_write(to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.slots(0)), **base)
+        k_new, v_new = to_dev(torch, k[L - 1:L]), to_dev(torch, v[L - 1:L])
+        q_new = to_dev(torch, w.q())
+        for _ in range(args.layers):
+            layers.append(DecodeLayer(i8, torch, base, w, k_new, v_new, q_new))
+        del base
+    torch.cuda.synchronize()
+    ws = {L: i8.decode_workspace(1, 24, 4, 256, wl.decode_outlier(L).block_tables.shape[1]) for L in HISTORIES}
+    bytes_per_step = sum(ly.w.kv_bytes_int8() for ly in layers)
+    launches_per_step = 2 * len(layers)
+
+    def step():
+        for ly in layers:
+            ly.produce(i8)
+            ly.decode(i8, ws[int(ly.w.seq_lens[0])])
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    assert i8.device_error() == 0, "kernel error during warm-up"
+
+    # ---- capture K steps, with external timing events around every decode ----
+    try:
+        mk = lambda: torch.cuda.Event(enable_timing=True, external=True)  # noqa: E731
+        mk()
+        per_kernel = True
+    except TypeError:
+        mk = None
+        per_kernel = False
+    ev_pairs = []
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(args.steps):
+                for ly in layers:
+                    ly.produce(i8)
+                    if per_kernel:
+                        a, b = mk(), mk()
+                        a.record()
+                    ly.decode(i8, ws[int(ly.w.seq_lens[0])])
+                    if per_kernel:
+                        b.record()
+                        ev_pairs.append((int(ly.w.seq_lens[0]), a, b))
+    stream.wait_stream(cap)
+    g.replay()  # one untimed replay of the captured graph (warm)
+    torch.cuda.synchronize()
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id) if rank == 0 else None
+    time.sleep(0.25 if sampler else 0)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record()
+    g.replay()
+    t_end.record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    if sampler:
+        sampler.stop()
+    ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    err = i8.device_error()
+    assert err == 0, f"kernel error {err} in the timed region"
+    value = world * args.steps * bytes_per_step / (ms / 1e3) / 1e9
+
+    # per-kernel decode durations from the timed region
+    by_len = {L: [] for L in HISTORIES}
+    for L, a, b in ev_pairs:
+        by_len[L].append(a.elapsed_time(b))
+    if per_kernel:
+        dec_ms = sum(sum(v) for v in by_len.values())
+        n_dec = sum(len(v) for v in by_len.values())
+        achieved = args.steps * bytes_per_step / (dec_ms / 1e3) / 1e9
+        avg_launch_us = dec_ms / n_dec * 1e3
+    else:
+        achieved, avg_launch_us = None, None
+    src = kernel_hash("int8_kv_cache_token_gb300/csrc/decode.cu", "int8_kv_cache_token_gb300/csrc/common.cuh")
+    traffic = recorded_traffic("int8_decode", src)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": (achieved / hbm_peak) if achieved else None, "traffic": traffic,
+                "kernel": "int8_decode_kernel", "peak_kind": f"of {peak_kind} (HBM copy bandwidth)",
+                "avg_launch_us": avg_launch_us,
+                "algorithmic_bytes_per_launch": bytes_per_step / len(layers)}
+
+    # ---- e2e: the same steps through the C ABI with pinned host buffers ----
+    e2e = run_e2e(args, torch, i8, layers, ws, bytes_per_step, world)
+
+    secondary = {}
+    if rank == 0:
+        secondary["decode_by_history"] = {
+            str(L): {"us": statistics.mean(v) * 1e3, "gb_s": wl.decode_outlier(L).kv_bytes_int8() / (statistics.mean(v) / 1e3) / 1e9}
+            for L, v in by_len.items() if v}
+        if not args.quick:
+            secondary.update(run_secondary(torch, i8, hbm_peak))
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cores = cpu_cores()
+        gbs, reps, el = time_oracle(args.cpu_seconds, cores)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{reps} oracle decodes of the 8192-token history (24 heads) in {el:.1f} s"}
+
+    if rank == 0:
+        clocks = sampler.summary(wall0, wall1) if sampler else None
+        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "s8/s32 (fp32 softmax)", "data": "synthetic (seeded)",
+                "config": {"workload": f"decode_outlier: single-sequence decode, 24 q / 4 kv heads, head_dim 256, "
+                                       f"block 16, histories {list(HISTORIES)}, x{args.layers} layers per step",
+                           "global_batch": world, "seq_len": list(HISTORIES), "parallelism": f"replicas x{world}",
+                           "l2": "inputs larger than L2 (each layer has its own cache; 1.9 GB per step)"},
+                "gpu_launches": args.steps * launches_per_step,
+                "e2e": e2e, "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
+                "secondary": secondary}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, torch, i8, layers, ws, bytes_per_step, world):
+    """Per step: H2D of every layer's new q/k/v from pinned host memory, producer +
+    decode, D2H of every output; captured with the steps in one graph."""
+    host_in = []
+    for ly in layers:
+        host_in.append((ly.k.cpu().pin_memory(), ly.v.cpu().pin_memory(), ly.q.cpu().pin_memory()))
+    host_out = [torch.empty(ly.out.shape, dtype=ly.out.dtype).pin_memory() for ly in layers]
+    h2d = sum(a.numel() * a.element_size() for t in host_in for a in t)
+    d2h = sum(o.numel() * o.element_size() for o in host_out)
+    stream = torch.cuda.current_stream()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(args.steps):
+                for ly, (hk, hv, hq), ho in zip(layers, host_in, host_out):
+                    ly.k.copy_(hk, non_blocking=True)
+                    ly.v.copy_(hv, non_blocking=True)
+                    ly.q.copy_(hq, non_blocking=True)
+                    ly.produce(i8)
+                    ly.decode(i8, ws[int(ly.w.seq_lens[0])])
+                    ho.copy_(ly.out, non_blocking=True)
+    stream.wait_stream(cap)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    return {"value": world * args.steps * bytes_per_step / (ms / 1e3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps}
+
+
+def time_graph(torch, fn, reps: int):
+    """Average ms of fn() captured reps times in one graph."""
+    stream = torch.cuda.current_stream()
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            for _ in range(reps):
+                fn()
+    stream.wait_stream(cap)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def run_secondary(torch, i8, hbm_peak):
+    """Other rows of the path, each timed on its own (after the main region)."""
+    res = {}
+    # producer: 8192 new tokens, 8 KV heads, head_dim 128, 32 query heads
+    try:
+        p = wl.producer_tokens()
+        cache = i8.alloc_int8_cache(p["num_blocks"], p["Hkv"], p["D"])
+        k, v, q, s = (to_dev(torch, p[n]) for n in ("k", "v", "q", "slots"))
+        q_i8 = torch.empty(q.shape, dtype=torch.int8, device="cuda")
+        q_s = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+        ms = time_graph(torch, lambda: i8.kv_quant_write(k, v, s, **cache, q=q, q_i8=q_i8, q_scale=q_s), 20)
+        T, Hkv, Hq, D = 8192, p["Hkv"], p["Hq"], p["D"]
+        moved = T * (2 * Hkv * D * 2 + 2 * Hkv * D + 2 * Hkv * 4) + T * Hq * (2 * D + D + 4)
+        res["producer_8192x8x128"] = {"us": ms * 1e3, "gb_s": moved / (ms / 1e3) / 1e9,
+                                      "frac_hbm": moved / (ms / 1e3) / 1e9 / hbm_peak}
+    except Exception as e:  # pragma: no cover - report, do not hide
+        res["producer_8192x8x128"] = {"error": str(e)[:200]}
+    return res
+
+
+def run_profile(args):
+    """Decode launches only, for profilers: `--layers` copies of the 32768-token
+    history (each its own cache, 68 MB, so the set exceeds L2), launched round-robin
+    eagerly: `--warmup` then `--steps` launches."""
+    import torch
+
+    from int8_kv_cache_token_gb300 import build as ibuild
+    ibuild.build()
+    import int8_kv_cache_token_gb300 as i8
+    L = HISTORIES[-1]
+    w = wl.decode_outlier(L)
+    k, v = w.kv(0)
+    base = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+    i8.kv_quant_write(to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.slots(0)), **base)
+    k_new, v_new, q_new = to_dev(torch, k[L - 1:L]), to_dev(torch, v[L - 1:L]), to_dev(torch, w.q())
+    layers = [DecodeLayer(i8, torch, base, w, k_new, v_new, q_new) for _ in range(args.layers)]
+    for ly in layers:
+        ly.produce(i8)
+    ws = i8.decode_workspace(1, 24, 4, 256, w.block_tables.shape[1])
+    torch.cuda.synchronize()
+    for i in range(args.warmup + args.steps):
+        layers[i % len(layers)].decode(i8, ws)
+    torch.cuda.synchronize()
+    assert i8.device_error() == 0
+    print(json.dumps({"profile": "int8_decode", "history": L, "launches": args.warmup + args.steps,
+                      "bytes_per_launch": w.kv_bytes_int8()}))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=LAYERS)
+    ap.add_argument("--quick", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="decode launches only (32768 history, --layers caches round-robin) for ncu")
+    args = ap.parse_args()
+    if args.profile:
+        return run_profile(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

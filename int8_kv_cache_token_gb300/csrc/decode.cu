@@ -99,7 +99,7 @@ __device__ __forceinline__ void walk_next(Walk& w, const int32_t* seq_lens, int 
   }
 }
 
-// CTA whose unit range [c*U/N, (c+1)*U/N) holds unit u.
+// CTA whose unit range [c*U/N, (c+1)*U/N) holds unit u (N <= U: no empty ranges).
 __device__ __forceinline__ int cta_of(long long u, long long U, int N) {
   return (int)(((u + 1) * N + U - 1) / U - 1);
 }
@@ -201,10 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
       total += u;
     }
     const long long U = total;
-    const long long ub = U * c / N, ue = U * (c + 1) / N;
+    // Only the first min(N, U) CTAs take units, so every working CTA has at
+    // least one and the CTAs covering a pair are consecutive.
+    const int Nw = (int)(U < N ? U : N);
+    const long long ub = c < Nw ? U * c / Nw : 0, ue = c < Nw ? U * (c + 1) / Nw : 0;
     if (lane == 0) {
       ctrl[0] = (int)(ue - ub);
       ctrl[8] = 0;
+      ctrl[10] = Nw;
     }
     if (ue > ub) {
       // find the sequence holding unit ub
@@ -260,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
   w0.L = clamp_len(p.seq_lens[w0.b], maxL);
   w0.np = (w0.L + kPart - 1) / kPart;
   const long long U = (long long)ctrl[6] | ((long long)ctrl[7] << 31);
+  const int Nw = ctrl[10];
 
   if (warp == kCWarps) {
     // ================= producer warp =================
@@ -505,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
     const bool seg_end = (i == n_units - 1) || (nx.b * Hkv + nx.kvh != pair);
     if (seg_end) {
       const long long Up = wk.ub + (long long)wk.kvh * wk.np;
-      const int cf = cta_of(Up, U, N), cl = cta_of(Up + wk.np - 1, U, N);
+      const int cf = cta_of(Up, U, Nw), cl = cta_of(Up + wk.np - 1, U, Nw);
       if (cf == cl) {
 #pragma unroll
         for (int dt = 0; dt < NDT; ++dt)
@@ -645,8 +650,15 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   const int ns = pick_slots(D, p.Hkv, max_smem_optin(dev));
   if (ns == 0) return cudaErrorInvalidConfiguration;
   const size_t smem = decode_layout(D, p.Hkv, ns).total;
-  cudaError_t e = cudaFuncSetAttribute(int8_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  // Raise the dynamic shared-memory limit once per device (to the opt-in
+  // maximum), so that launches captured into a CUDA graph make no attribute call.
+  static int attr_set[64] = {0};
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(int8_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         max_smem_optin(dev));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = 1;
+  }
   int8_decode_kernel<D><<<p.grid, kThreads, smem, stream>>>(p, ns);
   return cudaGetLastError();
 }
@@ -678,11 +690,14 @@ cudaError_t launch_debug_qk(const DebugQKParams& p, cudaStream_t stream) {
   const long long grid = (long long)p.B * p.Hkv * nparts;
   if (grid == 0) return cudaSuccess;
   const size_t smem = (size_t)kPart * p.D;
+  cudaError_t e;
   if (p.D == 256) {
-    cudaFuncSetAttribute(debug_qk_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(debug_qk_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     debug_qk_kernel<256><<<(unsigned)grid, 256, smem, stream>>>(p);
   } else {
-    cudaFuncSetAttribute(debug_qk_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(debug_qk_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     debug_qk_kernel<128><<<(unsigned)grid, 256, smem, stream>>>(p);
   }
   return cudaGetLastError();
