@@ -498,6 +498,26 @@ def run_secondary(torch, i8, hbm_peak):
                                       "frac_hbm": moved / (ms / 1e3) / 1e9 / hbm_peak}
     except Exception as e:  # pragma: no cover - report, do not hide
         res["producer_8192x8x128"] = {"error": str(e)[:200]}
+    # prefix chunk: 2048 queries after 16384 cached tokens, 24 q / 4 kv heads, head_dim 256
+    try:
+        w = wl.prefix_chunk()
+        k, v = w.kv()
+        cache = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+        i8.kv_quant_write(to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.slots()), **cache)
+        qd = to_dev(torch, w.q())
+        q_i8 = torch.empty(qd.shape, dtype=torch.int8, device="cuda")
+        q_s = torch.empty(qd.shape[:2], dtype=torch.float32, device="cuda")
+        dummy = torch.zeros((w.chunk, w.Hkv, w.D), dtype=torch.bfloat16, device="cuda")
+        none = torch.full((w.chunk,), -1, dtype=torch.int32, device="cuda")
+        i8.kv_quant_write(dummy, dummy, none, **cache, q=qd, q_i8=q_i8, q_scale=q_s)
+        out = torch.empty((w.chunk, w.Hq, w.D), dtype=torch.float32, device="cuda")
+        bt = to_dev(torch, w.block_table)
+        ms = time_graph(torch, lambda: i8.int8_prefix_attn(out, q_i8, q_s, cache["k_cache"], cache["v_cache"],
+                                                           cache["k_scale"], cache["v_scale"], bt, w.history), 5)
+        res["prefix_16384+2048"] = {"ms": ms, "int8_tops": w.int8_ops() / (ms / 1e3) / 1e12,
+                                    "pairs": w.pairs(), "ops": w.int8_ops()}
+    except Exception as e:  # pragma: no cover
+        res["prefix_16384+2048"] = {"error": str(e)[:200]}
     return res
 
 

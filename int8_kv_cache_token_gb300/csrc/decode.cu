@@ -2,29 +2,40 @@
 //
 // Source: "gfx936 DCU上实现INT8 PV MMAC：V Scale融合、概率量化与Fragment分组"
 // §1 (W = P x sV, 32-token groups, sW = max W / 127), §2 (score recovery
-// acc x sQ x sK / sqrt(d), online softmax), §2.2 (decode: 256-token partitions,
-// P normalized inside the partition, log-sum-exp merge), §3 (P on the A side,
-// V on the B side of the INT8 MMA; int32 bound 32 x 127 x 127 per group) and
-// "gfx936 DCU上实现INT8 KV与INT8 MMAC Attention推理优化" §3.3 (the decode data
-// flow) and §2.3 (cache layouts).
+// acc x sQ x sK / sqrt(d), online softmax), §2.2 (decode: 256-token partitions
+// merged by log-sum-exp), §3 (P on the A side, V on the B side of the INT8
+// MMA; int32 bound 32 x 127 x 127 per group) and "gfx936 DCU上实现INT8 KV与
+// INT8 MMAC Attention推理优化" §3.3 (the decode data flow) and §2.3 (layouts).
 //
 // GB300 design (not the pages' gfx936 one):
 //  * Work unit = (sequence, KV head, 256-token partition).  A persistent grid of
-//    one CTA per SM takes a contiguous range of units, so one CTA usually walks
-//    several partitions of the same (sequence, KV head) and merges them
-//    locally; pairs that span CTAs leave one partial per CTA in the workspace
-//    and the last CTA to finish (an atomic ticket, no waiting) merges them.
-//  * Warp 8 is a TMA producer: per unit it issues 16 bulk copies of K pages and
-//    32 of scale rows (one item), then 16 of V pages (a second item), into a
-//    ring of shared-memory slots guarded by full/empty mbarriers.
-//  * Warps 0-7 consume.  GQA packs the G <= 8 query heads of one KV head into
-//    the N = 8 side of mma.sync.m16n8k32 s8: QK has M = 16 tokens (one block),
-//    K = 32 head-dims; PV has M = 16 head-dims, N = 8 query rows, K = the 32
-//    tokens of one probability group, so every INT8 MMA consumes exactly one
-//    aligned group and its scale sW is applied to that MMA's int32 result.
-//  * Warp w computes QK, softmax terms and the W quantization of group w; the
-//    quantized W fragments go through shared memory to all warps; warp w then
-//    owns head-dims [w*D/8, (w+1)*D/8) of the PV output for the whole range.
+//    one CTA per SM takes a contiguous range of units; pairs (sequence, KV head)
+//    that span CTAs leave one partial per CTA in the workspace and the last CTA
+//    to finish a pair (an atomic ticket, no waiting) merges them by
+//    log-sum-exp.
+//  * Warp 8 is a TMA producer: per unit it issues 16 bulk copies of K pages (one
+//    ring item) and 16 of V pages (a second item) into a ring of shared-memory
+//    slots guarded by full/empty mbarriers.
+//  * Warps 0-7 consume, each on its own 32-token group of every partition
+//    (warp w: tokens 32w .. 32w+31), with no CTA barrier per partition: every
+//    warp runs its own online softmax (m, l, o) over its groups.  The pages
+//    normalize P inside a 256-token partition before quantizing W; here the
+//    normalization of each group is carried in the running state instead.  The
+//    group quantization Wq = round(W / (max W / 127)) does not change when all
+//    W of a group are scaled by one positive factor, so the codes are the
+//    pages' codes and the output is the same up to fp32 rounding.  At the end of
+//    a CTA's share of a pair the 8 warps' states merge deterministically
+//    (log-sum-exp, tree order) through shared memory.
+//  * GQA packs the G <= 8 query heads of one KV head into the N = 8 side of the
+//    MMAs.  QK: M = 16 tokens (one block), K = head-dims.  PV: M = 16 head-dims,
+//    N = 8 query rows, K = the tokens of one probability group, so each group's
+//    contraction is one accumulator and its sW scales exactly that result.
+//  * The INT8 x INT8 contractions run on the f16 tensor path: every int8 code is
+//    exact in f16, every product (<= 127^2) is exact, and every partial sum is
+//    an integer below 2^22 (QK over 256 dims: <= 4,129,024; PV over one group:
+//    <= 516,128), so the fp32 accumulator holds the exact int32 result.  On
+//    sm_103a this path has about 4x the throughput of mma.sync s8; the debug QK
+//    entry point checks the accumulators bit for bit against integer QK.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -34,38 +45,28 @@ namespace {
 
 constexpr int kPart = 256;   // partition (tokens) -- the pages' decode partition
 constexpr int kBS = 16;      // block size
-constexpr int kGroup = 32;   // probability group = K of one INT8 MMA
+constexpr int kGroup = 32;   // probability group
 constexpr int kCWarps = 8;   // consumer warps (one per group of a partition)
 constexpr int kThreads = (kCWarps + 1) * 32;
 constexpr int kRows = 8;     // query rows in the MMA N dimension
-constexpr int kWStride = 36; // padded row stride (floats) of the per-warp W staging
 __host__ __device__ constexpr int kSlotFloats(int D) { return kRows * D + 2 * kRows; }
 
 struct SmemLayout {
-  int nslots, nsslots;
-  size_t ring, scales, wbuf, wqf, swr, redmax, redsum, bars, ctrl, total;
+  int nslots;
+  size_t ring, merge, wq, bars, ctrl, total;
 };
 
-__host__ __device__ inline SmemLayout decode_layout(int D, int Hkv, int nslots) {
+__host__ __device__ inline SmemLayout decode_layout(int D, int nslots) {
   SmemLayout L;
   L.nslots = nslots;
-  L.nsslots = (nslots + 2) / 2;
   const size_t item = (size_t)kPart * D;
   size_t off = 0;
   L.ring = off;
   off += (size_t)nslots * item;
-  L.scales = off;
-  off += (size_t)L.nsslots * 2 * kPart * Hkv * sizeof(float);
-  L.wbuf = off;
-  off += (size_t)kCWarps * kRows * kWStride * sizeof(float);
-  L.wqf = off;
-  off += (size_t)kCWarps * 32 * sizeof(uint2);
-  L.swr = off;
-  off += (size_t)kCWarps * kRows * sizeof(float);
-  L.redmax = off;
-  off += (size_t)kCWarps * kRows * sizeof(float);
-  L.redsum = off;
-  off += (size_t)kCWarps * kRows * sizeof(float);
+  L.merge = off;  // 4 warp states [8 rows][D] + l [8] (+ maxima [8 warps][8 rows])
+  off += (size_t)(4 * (kRows * D + 2 * kRows) + kCWarps * kRows) * sizeof(float);
+  L.wq = off;     // per-warp transpose of the quantized W: [8 rows][32 tokens] int8
+  off += (size_t)kCWarps * kRows * kGroup;
   L.bars = off;
   off += (size_t)2 * nslots * sizeof(uint64_t);
   L.ctrl = off;
@@ -120,56 +121,98 @@ __device__ __forceinline__ void pipe_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// QK for the two 16-token blocks (2w, 2w+1) of a warp:
-// acc[m][0..3] = (token g, row 2t), (token g, row 2t+1), (token g+8, row 2t), (token g+8, row 2t+1)
-// of block 2w+m.  `kpages` holds 16 K pages [D/16][16 tokens][16 B].
-template <int D>
-__device__ __forceinline__ void qk_warp(const int8_t* kpages, int warp, int lane, const uint32_t (&qf)[D / 32][2],
-                                        int (&acc)[2][4]) {
-  const int mi = lane >> 3, ri = lane & 7;
-#pragma unroll
-  for (int m = 0; m < 2; ++m) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[m][i] = 0;
-    const int8_t* page = kpages + (size_t)(2 * warp + m) * (D * kBS);
-    const int8_t* row = page + (mi >> 1) * (kBS * 16) + (ri + 8 * (mi & 1)) * 16;
-#pragma unroll
-    for (int s = 0; s < D / 32; ++s) {
-      uint32_t a[4];
-      ldmatrix_x4(a, row + (size_t)(2 * s) * (kBS * 16));
-      mma_s8_16832(acc[m], a, qf[s][0], qf[s][1]);
-    }
-  }
+// Four int8 codes (little-endian) -> f16x2 {c0, c1} and {c2, c3}, exactly:
+// byte b becomes the f16 1024 + (b ^ 0x80) = 1152 + c, then 1152 is subtracted.
+__device__ __forceinline__ void s8x4_to_f16(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = x ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, 0x5140);
+  hi = __byte_perm(u, 0x64646464u, 0x7362);
+  const uint32_t bias = 0x64806480u;  // f16x2 (1152, 1152)
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(bias));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(bias));
 }
 
-// B-operand fragments of the GQA-packed query rows: row g of the N-tile is query
-// head kvh*G + g; qf[s] = dims {32s+4t..+3} and {32s+16+4t..+3}.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One exact INT8 m16n8k32 step on the f16 tensor path.  The s8 A fragment
+// (rows g / g+8 x k 4t..4t+3 and 16+4t..16+4t+3, as ldmatrix delivers it) is
+// split into two k16 MMAs over k {0..15} and {16..31}; inside each the f16
+// fragment order pairs logical k (2t, 2t+1 | 2t+8, 2t+9) with physical k
+// (4t, 4t+1 | 4t+2, 4t+3).  b[0..3] is B in the matching f16 form (b[0], b[1]
+// for k 0..15, b[2], b[3] for k 16..31).  The same permutation on both
+// operands leaves the sum unchanged.
+__device__ __forceinline__ void mma_s8a_f16b(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+  uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
+  s8x4_to_f16(a[0], a0l, a0h);
+  s8x4_to_f16(a[1], a1l, a1h);
+  s8x4_to_f16(a[2], a2l, a2h);
+  s8x4_to_f16(a[3], a3l, a3h);
+  mma_f16_16816(d, a0l, a1l, a0h, a1h, b[0], b[1]);
+  mma_f16_16816(d, a2l, a3l, a2h, a3h, b[2], b[3]);
+}
+
+// s8 B fragment (k 4t..4t+3 and 16+4t..16+4t+3 of column g) -> the f16 form above.
+__device__ __forceinline__ void s8b_to_f16(uint32_t x0, uint32_t x1, uint32_t (&b)[4]) {
+  s8x4_to_f16(x0, b[0], b[1]);
+  s8x4_to_f16(x1, b[2], b[3]);
+}
+
+// Query fragments (B operand of QK, f16 form) of the GQA-packed rows: column g of
+// the N-tile is query head kvh*G + g; per 32-dim step s the s8 fragment holds
+// dims 32s + {4t..4t+3} and 32s + 16 + {4t..4t+3}.
 template <int D>
 __device__ __forceinline__ void load_q_frags(const int8_t* q, int b, int Hq, int kvh, int G, int lane,
-                                             uint32_t (&qf)[D / 32][2]) {
+                                             uint32_t (&qf)[D / 32][4]) {
   const int g = lane >> 2, t = lane & 3;
   const int8_t* row = q + ((size_t)b * Hq + kvh * G + g) * D;
 #pragma unroll
   for (int s = 0; s < D / 32; ++s) {
-    qf[s][0] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(row + 32 * s + 4 * t)) : 0u;
-    qf[s][1] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(row + 32 * s + 16 + 4 * t)) : 0u;
+    const uint32_t x0 = g < G ? __ldg(reinterpret_cast<const uint32_t*>(row + 32 * s + 4 * t)) : 0u;
+    const uint32_t x1 = g < G ? __ldg(reinterpret_cast<const uint32_t*>(row + 32 * s + 16 + 4 * t)) : 0u;
+    s8b_to_f16(x0, x1, qf[s]);
+  }
+}
+
+// QK for the two 16-token blocks (2w, 2w+1) of warp w's group:
+// acc[m][0..3] = (token g, row 2t), (token g, row 2t+1), (token g+8, row 2t),
+// (token g+8, row 2t+1) of block 2w+m.  kpages holds 16 K pages [D/16][16][16 B].
+template <int D>
+__device__ __forceinline__ void qk_warp(const int8_t* kpages, int warp, int lane, const uint32_t (&qf)[D / 32][4],
+                                        float (&acc)[2][4]) {
+  const int mi = lane >> 3, ri = lane & 7;
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
+    const int8_t* row =
+        kpages + (size_t)(2 * warp + m) * (D * kBS) + (mi >> 1) * (kBS * 16) + (ri + 8 * (mi & 1)) * 16;
+#pragma unroll
+    for (int s = 0; s < D / 32; ++s) {
+      uint32_t a[4];
+      ldmatrix_x4(a, row + (size_t)(2 * s) * (kBS * 16));
+      mma_s8a_f16b(acc[m], a, qf[s]);
+    }
   }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p, int nslots) {
-  constexpr int NDT = D / 16 / kCWarps;  // PV head-dim tiles per warp
+  constexpr int NDT = D / 16;  // PV head-dim tiles (every warp covers all of D for its group)
   constexpr int kPage = D * kBS;
   constexpr int kItem = kPart * D;
+  constexpr int kWS = kRows * D + 2 * kRows;  // one warp state in the merge buffer
   extern __shared__ __align__(1024) uint8_t smem[];
-  const SmemLayout lay = decode_layout(D, p.Hkv, nslots);
+  const SmemLayout lay = decode_layout(D, nslots);
   int8_t* ring = reinterpret_cast<int8_t*>(smem + lay.ring);
-  float* scales = reinterpret_cast<float*>(smem + lay.scales);
-  float* wbuf = reinterpret_cast<float*>(smem + lay.wbuf);
-  uint2* wqf = reinterpret_cast<uint2*>(smem + lay.wqf);
-  float* swr = reinterpret_cast<float*>(smem + lay.swr);
-  float* redmax = reinterpret_cast<float*>(smem + lay.redmax);
-  float* redsum = reinterpret_cast<float*>(smem + lay.redsum);
+  float* mbuf = reinterpret_cast<float*>(smem + lay.merge);
+  int8_t* wqs = reinterpret_cast<int8_t*>(smem + lay.wq);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
   uint64_t* empty = full + nslots;
   int* ctrl = reinterpret_cast<int*>(smem + lay.ctrl);
@@ -179,7 +222,6 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
   const int B = p.B, Hkv = p.Hkv, G = p.G, Hq = p.Hq;
   const int N = gridDim.x, c = blockIdx.x;
   const int maxL = p.max_blocks * kBS;
-  const int scale_floats = kPart * Hkv;  // one of sK / sV for one unit
 
   // ---- work split: every CTA scans seq_lens (warp 0) ----
   if (warp == 0) {
@@ -211,7 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
       ctrl[10] = Nw;
     }
     if (ue > ub) {
-      // find the sequence holding unit ub
       long long run = 0;
       for (int b0 = 0; b0 < B; b0 += 32) {
         const int b = b0 + lane;
@@ -225,8 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
         const long long ex = run + incl - u, in = run + incl;
         const unsigned hit = __ballot_sync(0xffffffffu, u > 0 && ex <= ub && ub < in);
         if (hit) {
-          const int src = __ffs(hit) - 1;
-          if (lane == src) {
+          if (lane == __ffs(hit) - 1) {
             const int L = clamp_len(p.seq_lens[b], maxL);
             const int np = (L + kPart - 1) / kPart;
             const long long local = ub - ex;
@@ -272,49 +312,28 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
     const int8_t* vc = static_cast<const int8_t*>(p.v_cache);
     const uint64_t pol = policy_evict_first();
     Walk wk = w0;
-    const int j = lane & 15;
     for (int i = 0; i < n_units; ++i) {
       const int t0 = wk.part * kPart;
       const int nblk = min(kPart / kBS, (wk.L - t0 + kBS - 1) / kBS);
       int blk = -1;
-      if (j < nblk) {
-        blk = p.block_tables[(size_t)wk.b * p.max_blocks + wk.part * (kPart / kBS) + j];
+      if (lane < nblk) {
+        blk = p.block_tables[(size_t)wk.b * p.max_blocks + wk.part * (kPart / kBS) + lane];
         if (blk < 0 || blk >= p.num_blocks) {
           record_error(2);
           blk = -1;
         }
       }
-      const bool page_ok = lane < 16 && blk >= 0;
-      const bool scale_ok = lane >= 16 && blk >= 0;
-      const uint32_t n_pages = __popc(__ballot_sync(0xffffffffu, page_ok));
-      const uint32_t n_srows = __popc(__ballot_sync(0xffffffffu, scale_ok));
-      const uint32_t srow_bytes = kBS * Hkv * sizeof(float);
-      // K item (+ both scale rows)
-      {
-        const int item = 2 * i, slot = item % nslots;
-        if (item >= nslots) pipe_wait(&empty[slot], ((item / nslots) - 1) & 1, abort_flag);
-        if (lane == 0) mbar_expect_tx(&full[slot], n_pages * kPage + n_srows * 2 * srow_bytes);
-        __syncwarp();
-        if (page_ok)
-          bulk_g2s_hint(ring + (size_t)slot * kItem + (size_t)j * kPage, kc + ((size_t)blk * Hkv + wk.kvh) * kPage,
-                        kPage, &full[slot], pol);
-        if (scale_ok) {
-          float* ss = scales + (size_t)(i % lay.nsslots) * 2 * scale_floats;
-          bulk_g2s_hint(ss + j * kBS * Hkv, p.k_scale + (size_t)blk * kBS * Hkv, srow_bytes, &full[slot], pol);
-          bulk_g2s_hint(ss + scale_floats + j * kBS * Hkv, p.v_scale + (size_t)blk * kBS * Hkv, srow_bytes,
-                        &full[slot], pol);
-        }
-        mbar_arrive(&full[slot]);
-      }
-      // V item
-      {
-        const int item = 2 * i + 1, slot = item % nslots;
+      const bool ok = lane < 16 && blk >= 0;
+      const uint32_t n_pages = __popc(__ballot_sync(0xffffffffu, ok));
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        const int item = 2 * i + kv, slot = item % nslots;
         if (item >= nslots) pipe_wait(&empty[slot], ((item / nslots) - 1) & 1, abort_flag);
         if (lane == 0) mbar_expect_tx(&full[slot], n_pages * kPage);
         __syncwarp();
-        if (page_ok)
-          bulk_g2s_hint(ring + (size_t)slot * kItem + (size_t)j * kPage, vc + ((size_t)blk * Hkv + wk.kvh) * kPage,
-                        kPage, &full[slot], pol);
+        if (ok)
+          bulk_g2s_hint(ring + (size_t)slot * kItem + (size_t)lane * kPage,
+                        (kv == 0 ? kc : vc) + ((size_t)blk * Hkv + wk.kvh) * kPage, kPage, &full[slot], pol);
         mbar_arrive(&full[slot]);
       }
       walk_next(wk, p.seq_lens, B, Hkv, maxL);
@@ -325,12 +344,36 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
   // ================= consumer warps =================
   const int g = lane >> 2, t = lane & 3;
   const float c_scale = p.sm_scale;
+  int8_t* wqw = wqs + warp * (kRows * kGroup);
   Walk wk = w0;
   int cur_pair = -1;
-  uint32_t qf[D / 32][2];
+  uint32_t qf[D / 32][4];
   float sq[2] = {0.f, 0.f};
   float o[NDT][4];
-  float Mrun[2], Lrun[2];
+  float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
+  // this thread's scales for tokens {g, g+8} of blocks 2w and 2w+1 of a unit
+  float sk[4], sv[4], sk_n[4], sv_n[4];
+  auto load_scales = [&](const Walk& u, float (&k4)[4], float (&v4)[4]) {
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const int lb = u.part * (kPart / kBS) + 2 * warp + m;  // logical block in the sequence
+      const int tok0 = lb * kBS;
+      int blk = -1;
+      if (tok0 < u.L) {
+        blk = __ldg(p.block_tables + (size_t)u.b * p.max_blocks + lb);
+        if (blk < 0 || blk >= p.num_blocks) blk = -1;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int off = g + 8 * h;
+        const bool v = blk >= 0 && tok0 + off < u.L;
+        const size_t si = ((size_t)(v ? blk : 0) * kBS + off) * Hkv + u.kvh;
+        k4[2 * m + h] = v ? __ldg(p.k_scale + si) : 0.f;
+        v4[2 * m + h] = v ? __ldg(p.v_scale + si) : 0.f;
+      }
+    }
+  };
+  load_scales(wk, sk, sv);
   for (int i = 0; i < n_units; ++i) {
     const int pair = wk.b * Hkv + wk.kvh;
     if (pair != cur_pair) {
@@ -340,203 +383,211 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
       for (int r = 0; r < 2; ++r) {
         const int row = 2 * t + r;
         sq[r] = row < G ? p.q_scale[(size_t)wk.b * Hq + wk.kvh * G + row] : 0.f;
-        Mrun[r] = -INFINITY;
-        Lrun[r] = 0.f;
+        mrun[r] = -INFINITY;
+        lrun[r] = 0.f;
       }
 #pragma unroll
       for (int dt = 0; dt < NDT; ++dt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[dt][e] = 0.f;
     }
+    Walk nx = wk;
+    walk_next(nx, p.seq_lens, B, Hkv, maxL);
+    if (i + 1 < n_units) load_scales(nx, sk_n, sv_n);  // the next unit's scales, in flight meanwhile
     const int t0 = wk.part * kPart;
     const int ntok = min(kPart, wk.L - t0);
-    const float* sks = scales + (size_t)(i % lay.nsslots) * 2 * scale_floats;
-    const float* svs = sks + scale_floats;
+    const bool active = warp * kGroup < ntok;
 
-    // ---- K item: QK, scores, partition max ----
+    // ---- K item: QK for this warp's group ----
     const int kitem = 2 * i, kslot = kitem % nslots;
     pipe_wait(&full[kslot], (kitem / nslots) & 1, abort_flag);
-    int acc[2][4];
-    if (warp * kGroup < ntok) {
+    float acc[2][4];
+    if (active) {
       qk_warp<D>(ring + (size_t)kslot * kItem, warp, lane, qf, acc);
     } else {
 #pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[m][e] = 0;
+        for (int e = 0; e < 4; ++e) acc[m][e] = 0.f;
     }
-    float s[2][4], sv[2][4];
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int tok = warp * kGroup + 16 * m + g + 8 * (e >> 1);
-        const bool valid = tok < ntok;
-        float sc = -INFINITY, vsc = 0.f;
-        if (valid) {
-          const float sk = sks[tok * Hkv + wk.kvh];
-          vsc = svs[tok * Hkv + wk.kvh];
-          sc = __fmul_rn(__fmul_rn(__fmul_rn((float)acc[m][e], sq[e & 1]), sk), c_scale);
-        }
-        s[m][e] = sc;
-        sv[m][e] = vsc;
-        mx[e & 1] = fmaxf(mx[e & 1], sc);
-      }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[kslot]);
-#pragma unroll
-    for (int r = 0; r < 2; ++r)
-#pragma unroll
-      for (int off = 4; off <= 16; off <<= 1) mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], off));
-    if (g == 0) {
-      redmax[warp * kRows + 2 * t] = mx[0];
-      redmax[warp * kRows + 2 * t + 1] = mx[1];
-    }
-    named_bar_sync(1, kCWarps * 32);
 
-    // ---- partition softmax: m_g, l_g, P, W = P * sV ----
-    float mg[2], lg[2];
+    // ---- scores, online softmax over this warp's group, W = p~ * sV, quantize ----
+    float alpha[2] = {1.f, 1.f}, sw[2] = {0.f, 0.f};
+    if (active) {
+      float s[2][4];
+      float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      float m_ = -INFINITY;
+      for (int m = 0; m < 2; ++m)
 #pragma unroll
-      for (int w2 = 0; w2 < kCWarps; ++w2) m_ = fmaxf(m_, redmax[w2 * kRows + 2 * t + r]);
-      mg[r] = m_;
-    }
-    float ps[2][4];
-    float sum[2] = {0.f, 0.f};
+        for (int e = 0; e < 4; ++e) {
+          const int tok = warp * kGroup + 16 * m + g + 8 * (e >> 1);
+          float sc = -INFINITY;
+          if (tok < ntok) sc = __fmul_rn(__fmul_rn(__fmul_rn(acc[m][e], sq[e & 1]), sk[2 * m + (e >> 1)]), c_scale);
+          s[m][e] = sc;
+          mx[e & 1] = fmaxf(mx[e & 1], sc);
+        }
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
+      for (int r = 0; r < 2; ++r)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float pe = (s[m][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[m][e], mg[e & 1]));
-        ps[m][e] = pe;
-        sum[e & 1] += pe;
+        for (int off = 4; off <= 16; off <<= 1) mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], off));
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float mn = fmaxf(mrun[r], mx[r]);
+        alpha[r] = (mrun[r] == -INFINITY) ? 0.f : expf(mrun[r] - mn);
+        mrun[r] = mn;
+        lrun[r] *= alpha[r];
       }
+      float A[2] = {0.f, 0.f}, w[2][4];
 #pragma unroll
-    for (int r = 0; r < 2; ++r)
+      for (int m = 0; m < 2; ++m)
 #pragma unroll
-      for (int off = 4; off <= 16; off <<= 1) sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], off);
-    if (g == 0) {
-      redsum[warp * kRows + 2 * t] = sum[0];
-      redsum[warp * kRows + 2 * t + 1] = sum[1];
-    }
-    named_bar_sync(1, kCWarps * 32);
+        for (int e = 0; e < 4; ++e) {
+          const float pe = (s[m][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[m][e], mrun[e & 1]));
+          lrun[e & 1] += pe;
+          w[m][e] = __fmul_rn(pe, sv[2 * m + (e >> 1)]);
+          A[e & 1] = fmaxf(A[e & 1], w[m][e]);
+        }
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      float l_ = 0.f;
+      for (int r = 0; r < 2; ++r)
 #pragma unroll
-      for (int w2 = 0; w2 < kCWarps; ++w2) l_ += redsum[w2 * kRows + 2 * t + r];
-      lg[r] = l_;
-    }
-    float* wb = wbuf + (size_t)warp * kRows * kWStride;
+        for (int off = 4; off <= 16; off <<= 1) A[r] = fmaxf(A[r], __shfl_xor_sync(0xffffffffu, A[r], off));
+      float inv[2];
 #pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int row = 2 * t + (e & 1);
-        const int tg = 16 * m + g + 8 * (e >> 1);
-        const float P = __fdiv_rn(ps[m][e], lg[e & 1]);
-        wb[row * kWStride + tg] = (ps[m][e] > 0.f) ? __fmul_rn(P, sv[m][e]) : 0.f;
+      for (int r = 0; r < 2; ++r) {
+        sw[r] = __fdiv_rn(A[r], 127.0f);
+        inv[r] = A[r] > 0.f ? __fdiv_rn(127.0f, A[r]) : 0.f;
       }
+      // codes -> this warp's [row][token] bytes, read back below as PV B fragments
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int q = min(127, __float2int_rn(w[m][e] * inv[e & 1]));
+          wqw[(2 * t + (e & 1)) * kGroup + 16 * m + g + 8 * (e >> 1)] = (int8_t)q;
+        }
+    }
     __syncwarp();
-    // ---- W quantization of this warp's group, row g ----
-    {
-      const float4 w0v = *reinterpret_cast<const float4*>(wb + g * kWStride + 4 * t);
-      const float4 w1v = *reinterpret_cast<const float4*>(wb + g * kWStride + 16 + 4 * t);
-      const float wv[8] = {w0v.x, w0v.y, w0v.z, w0v.w, w1v.x, w1v.y, w1v.z, w1v.w};
-      float A = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) A = fmaxf(A, wv[e]);
-      A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, 1));
-      A = fmaxf(A, __shfl_xor_sync(0xffffffffu, A, 2));
-      const float sW = __fdiv_rn(A, 127.0f);
-      int qv[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) qv[e] = (A > 0.f) ? min(127, max(-127, __float2int_rn(__fdiv_rn(wv[e], sW)))) : 0;
-      wqf[warp * 32 + lane] = make_uint2(pack_s8x4(qv[0], qv[1], qv[2], qv[3]), pack_s8x4(qv[4], qv[5], qv[6], qv[7]));
-      if (t == 0) swr[warp * kRows + g] = (A > 0.f) ? sW : 0.f;
-    }
-    // ---- running merge of this partition into the CTA's state ----
-    float wg[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const float Mn = fmaxf(Mrun[r], mg[r]);
-      const float a = (Mrun[r] == -INFINITY) ? 0.f : expf(Mrun[r] - Mn);
-      wg[r] = lg[r] * expf(mg[r] - Mn);
-      Lrun[r] = Lrun[r] * a + wg[r];
-      Mrun[r] = Mn;
+    uint32_t bq[4];
+    s8b_to_f16(*reinterpret_cast<const uint32_t*>(wqw + g * kGroup + 4 * t),
+               *reinterpret_cast<const uint32_t*>(wqw + g * kGroup + 16 + 4 * t), bq);
+    if (alpha[0] != 1.f || alpha[1] != 1.f) {
 #pragma unroll
       for (int dt = 0; dt < NDT; ++dt) {
-        o[dt][r] *= a;
-        o[dt][2 + r] *= a;
+        o[dt][0] *= alpha[0];
+        o[dt][1] *= alpha[1];
+        o[dt][2] *= alpha[0];
+        o[dt][3] *= alpha[1];
       }
     }
-    named_bar_sync(1, kCWarps * 32);
 
-    // ---- V item: INT8 PV per group, rescaled by sW * merge weight ----
+    // ---- V item: exact INT8 PV of this warp's group, scaled by sW ----
     const int vitem = 2 * i + 1, vslot = vitem % nslots;
     pipe_wait(&full[vslot], (vitem / nslots) & 1, abort_flag);
-    {
-      const int ngroups = (ntok + kGroup - 1) / kGroup;
-      const int8_t* vpages = ring + (size_t)vslot * kItem;
+    if (active) {
       const int mi = lane >> 3, ri = lane & 7;
-      for (int jg = 0; jg < ngroups; ++jg) {
-        const uint2 bq = wqf[jg * 32 + lane];
-        const float sc0 = swr[jg * kRows + 2 * t] * wg[0];
-        const float sc1 = swr[jg * kRows + 2 * t + 1] * wg[1];
-        const int8_t* vrow = vpages + (size_t)(2 * jg + (mi >> 1)) * kPage + (ri + 8 * (mi & 1)) * 16;
+      const int8_t* vrow =
+          ring + (size_t)vslot * kItem + (size_t)(2 * warp + (mi >> 1)) * kPage + (ri + 8 * (mi & 1)) * 16;
 #pragma unroll
-        for (int dt = 0; dt < NDT; ++dt) {
-          const int dtile = warp * NDT + dt;
-          uint32_t a[4];
-          ldmatrix_x4(a, vrow + dtile * 16 * 16);
-          int pv[4] = {0, 0, 0, 0};
-          mma_s8_16832(pv, a, bq.x, bq.y);
-          o[dt][0] += (float)pv[0] * sc0;
-          o[dt][1] += (float)pv[1] * sc1;
-          o[dt][2] += (float)pv[2] * sc0;
-          o[dt][3] += (float)pv[3] * sc1;
-        }
+      for (int dt = 0; dt < NDT; ++dt) {
+        uint32_t a[4];
+        ldmatrix_x4(a, vrow + dt * 16 * 16);
+        float pv[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_s8a_f16b(pv, a, bq);
+        o[dt][0] = fmaf(pv[0], sw[0], o[dt][0]);
+        o[dt][1] = fmaf(pv[1], sw[1], o[dt][1]);
+        o[dt][2] = fmaf(pv[2], sw[0], o[dt][2]);
+        o[dt][3] = fmaf(pv[3], sw[1], o[dt][3]);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[vslot]);
 
-    // ---- end of this CTA's segment of the (sequence, KV head) pair? ----
-    Walk nx = wk;
-    walk_next(nx, p.seq_lens, B, Hkv, maxL);
+    // ---- end of this CTA's share of the (sequence, KV head) pair? ----
     const bool seg_end = (i == n_units - 1) || (nx.b * Hkv + nx.kvh != pair);
     if (seg_end) {
+      // full row sums of this warp (the 8 threads with one t hold one row's tokens)
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int off = 4; off <= 16; off <<= 1) lrun[r] += __shfl_xor_sync(0xffffffffu, lrun[r], off);
+      // common max over the 8 warps, then a tree sum in a fixed order
+      float* mw = mbuf + 4 * kWS;  // [8 warps][8 rows] maxima
+      if (g == 0) {
+        mw[warp * kRows + 2 * t] = mrun[0];
+        mw[warp * kRows + 2 * t + 1] = mrun[1];
+      }
+      named_bar_sync(1, kCWarps * 32);
+      float M[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float mm = -INFINITY;
+#pragma unroll
+        for (int w2 = 0; w2 < kCWarps; ++w2) mm = fmaxf(mm, mw[w2 * kRows + 2 * t + r]);
+        M[r] = mm;
+        const float f = (mrun[r] == -INFINITY) ? 0.f : expf(mrun[r] - mm);
+        lrun[r] *= f;
+#pragma unroll
+        for (int dt = 0; dt < NDT; ++dt) {
+          o[dt][r] *= f;
+          o[dt][2 + r] *= f;
+        }
+      }
+#pragma unroll
+      for (int half = 4; half >= 1; half >>= 1) {
+        if (warp >= half && warp < 2 * half) {
+          float* buf = mbuf + (size_t)(warp - half) * kWS;
+#pragma unroll
+          for (int dt = 0; dt < NDT; ++dt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) buf[(2 * t + (e & 1)) * D + dt * 16 + g + 8 * (e >> 1)] = o[dt][e];
+          if (g == 0) {
+            buf[kRows * D + 2 * t] = lrun[0];
+            buf[kRows * D + 2 * t + 1] = lrun[1];
+          }
+        }
+        named_bar_sync(1, kCWarps * 32);
+        if (warp < half) {
+          const float* buf = mbuf + (size_t)warp * kWS;
+#pragma unroll
+          for (int dt = 0; dt < NDT; ++dt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[dt][e] += buf[(2 * t + (e & 1)) * D + dt * 16 + g + 8 * (e >> 1)];
+          lrun[0] += buf[kRows * D + 2 * t];
+          lrun[1] += buf[kRows * D + 2 * t + 1];
+        }
+        named_bar_sync(1, kCWarps * 32);
+      }
+      // warp 0 now holds this CTA's (M, L, O) for the pair
       const long long Up = wk.ub + (long long)wk.kvh * wk.np;
       const int cf = cta_of(Up, U, Nw), cl = cta_of(Up + wk.np - 1, U, Nw);
       if (cf == cl) {
+        if (warp == 0) {
 #pragma unroll
-        for (int dt = 0; dt < NDT; ++dt)
+          for (int dt = 0; dt < NDT; ++dt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int row = 2 * t + (e & 1);
-            const int d = (warp * NDT + dt) * 16 + g + 8 * (e >> 1);
-            if (row < G) p.out[((size_t)wk.b * Hq + wk.kvh * G + row) * D + d] = o[dt][e] / Lrun[e & 1];
-          }
+            for (int e = 0; e < 4; ++e) {
+              const int row = 2 * t + (e & 1);
+              const int d = dt * 16 + g + 8 * (e >> 1);
+              if (row < G) p.out[((size_t)wk.b * Hq + wk.kvh * G + row) * D + d] = o[dt][e] / lrun[e & 1];
+            }
+        }
       } else {
         float* part = p.ws_part + (size_t)(pair + c) * kSlotFloats(D);
+        if (warp == 0) {
 #pragma unroll
-        for (int dt = 0; dt < NDT; ++dt)
+          for (int dt = 0; dt < NDT; ++dt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int row = 2 * t + (e & 1);
-            const int d = (warp * NDT + dt) * 16 + g + 8 * (e >> 1);
-            part[row * D + d] = o[dt][e];
+            for (int e = 0; e < 4; ++e) part[(2 * t + (e & 1)) * D + dt * 16 + g + 8 * (e >> 1)] = o[dt][e];
+          if (g == 0) {
+            part[kRows * D + 2 * t] = M[0];
+            part[kRows * D + 2 * t + 1] = M[1];
+            part[kRows * D + kRows + 2 * t] = lrun[0];
+            part[kRows * D + kRows + 2 * t + 1] = lrun[1];
           }
-        if (warp == 0 && g == 0) {
-          part[kRows * D + 2 * t] = Mrun[0];
-          part[kRows * D + 2 * t + 1] = Mrun[1];
-          part[kRows * D + kRows + 2 * t] = Lrun[0];
-          part[kRows * D + kRows + 2 * t + 1] = Lrun[1];
+          __threadfence();
         }
-        __threadfence();
         named_bar_sync(1, kCWarps * 32);
         if (tid == 0) {
           const int old = atomicAdd(&p.ws_count[pair], 1);
@@ -544,32 +595,64 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
         }
         named_bar_sync(1, kCWarps * 32);
         if (ctrl[9]) {
+          // last CTA of the pair: log-sum-exp merge of the nseg partials
           __threadfence();
-          for (int idx = tid; idx < G * D; idx += kCWarps * 32) {
-            const int row = idx / D, d = idx % D;
-            float M = -INFINITY;
-            for (int cc = cf; cc <= cl; ++cc)
-              M = fmaxf(M, __ldcg(p.ws_part + (size_t)(pair + cc) * kSlotFloats(D) + kRows * D + row));
-            float num = 0.f, den = 0.f;
-            for (int cc = cf; cc <= cl; ++cc) {
-              const float* ps2 = p.ws_part + (size_t)(pair + cc) * kSlotFloats(D);
-              const float e = expf(__ldcg(ps2 + kRows * D + row) - M);
-              num += e * __ldcg(ps2 + row * D + d);
-              den += e * __ldcg(ps2 + kRows * D + kRows + row);
+          const int nseg = cl - cf + 1;
+          const float* part0 = p.ws_part + (size_t)(pair + cf) * kSlotFloats(D);
+          float* Ms = mbuf;               // [8]
+          float* den = mbuf + kRows;      // [8]
+          float* wts = mbuf + 2 * kRows;  // [nseg][8]
+          if (tid < kRows) {
+            float mm = -INFINITY;
+            for (int sgi = 0; sgi < nseg; ++sgi) mm = fmaxf(mm, __ldcg(part0 + (size_t)sgi * kWS + kRows * D + tid));
+            Ms[tid] = mm;
+          }
+          named_bar_sync(1, kCWarps * 32);
+          for (int idx = tid; idx < nseg * kRows; idx += kCWarps * 32) {
+            const int sgi = idx / kRows, row = idx % kRows;
+            wts[idx] = (row < G) ? expf(__ldcg(part0 + (size_t)sgi * kWS + kRows * D + row) - Ms[row]) : 0.f;
+          }
+          named_bar_sync(1, kCWarps * 32);
+          if (tid < kRows) {
+            float dd = 0.f;
+            for (int sgi = 0; sgi < nseg; ++sgi)
+              dd += wts[sgi * kRows + tid] * __ldcg(part0 + (size_t)sgi * kWS + kRows * D + kRows + tid);
+            den[tid] = dd;
+          }
+          named_bar_sync(1, kCWarps * 32);
+          for (int idx = tid; idx < G * (D / 4); idx += kCWarps * 32) {
+            const int row = idx / (D / 4), d4 = idx % (D / 4);
+            float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int sgi = 0; sgi < nseg; ++sgi) {
+              const float4 v4 = __ldcg(reinterpret_cast<const float4*>(part0 + (size_t)sgi * kWS + row * D) + d4);
+              const float wgt = wts[sgi * kRows + row];
+              a4.x = fmaf(wgt, v4.x, a4.x);
+              a4.y = fmaf(wgt, v4.y, a4.y);
+              a4.z = fmaf(wgt, v4.z, a4.z);
+              a4.w = fmaf(wgt, v4.w, a4.w);
             }
-            p.out[((size_t)wk.b * Hq + wk.kvh * G + row) * D + d] = num / den;
+            const float inv = 1.0f / den[row];
+            *reinterpret_cast<float4*>(p.out + ((size_t)wk.b * Hq + wk.kvh * G + row) * D + 4 * d4) =
+                make_float4(a4.x * inv, a4.y * inv, a4.z * inv, a4.w * inv);
           }
           if (tid == 0) p.ws_count[pair] = 0;
+          named_bar_sync(1, kCWarps * 32);
         }
       }
     }
     wk = nx;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      sk[k] = sk_n[k];
+      sv[k] = sv_n[k];
+    }
   }
 }
 
 // Debug QK: one CTA per (sequence, KV head, 256-token partition); K pages are
 // staged with plain 16-byte loads and the decode kernel's qk_warp computes the
-// int32 accumulators.
+// accumulators (exact integers in fp32), written as int32.
 template <int D>
 __global__ void __launch_bounds__(256) debug_qk_kernel(DebugQKParams p) {
   constexpr int kPage = D * kBS;
@@ -595,9 +678,9 @@ __global__ void __launch_bounds__(256) debug_qk_kernel(DebugQKParams p) {
     reinterpret_cast<uint4*>(kp)[i] = val;
   }
   __syncthreads();
-  uint32_t qf[D / 32][2];
+  uint32_t qf[D / 32][4];
   load_q_frags<D>(p.q, b, p.Hq, kvh, p.G, lane, qf);
-  int acc[2][4];
+  float acc[2][4];
   qk_warp<D>(kp, warp, lane, qf, acc);
   const int g = lane >> 2, t = lane & 3;
 #pragma unroll
@@ -607,7 +690,7 @@ __global__ void __launch_bounds__(256) debug_qk_kernel(DebugQKParams p) {
       const int tok = t0 + warp * kGroup + 16 * m + g + 8 * (e >> 1);
       const int row = 2 * t + (e & 1);
       if (row < p.G && tok < p.max_len)
-        p.acc[((size_t)b * p.Hq + kvh * p.G + row) * p.max_len + tok] = tok < L ? acc[m][e] : 0;
+        p.acc[((size_t)b * p.Hq + kvh * p.G + row) * p.max_len + tok] = tok < L ? __float2int_rn(acc[m][e]) : 0;
     }
 }
 
@@ -637,9 +720,9 @@ int max_smem_optin(int device) {
 }
 
 // Deepest ring that fits.
-int pick_slots(int D, int Hkv, int smem_limit) {
+int pick_slots(int D, int smem_limit) {
   for (int ns = 8; ns >= 2; --ns)
-    if (decode_layout(D, Hkv, ns).total <= (size_t)smem_limit) return ns;
+    if (decode_layout(D, ns).total <= (size_t)smem_limit) return ns;
   return 0;
 }
 
@@ -647,9 +730,9 @@ template <int D>
 cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  const int ns = pick_slots(D, p.Hkv, max_smem_optin(dev));
+  const int ns = pick_slots(D, max_smem_optin(dev));
   if (ns == 0) return cudaErrorInvalidConfiguration;
-  const size_t smem = decode_layout(D, p.Hkv, ns).total;
+  const size_t smem = decode_layout(D, ns).total;
   // Raise the dynamic shared-memory limit once per device (to the opt-in
   // maximum), so that launches captured into a CUDA graph make no attribute call.
   static int attr_set[64] = {0};
@@ -665,6 +748,8 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+I8KV_DEFINE_ERROR_ACCESSOR(read_error_decode)
+
 int decode_grid(int device, int B, int Hkv, int max_blocks) {
   const long long max_units = (long long)B * Hkv * (((long long)max_blocks * kBS + kPart - 1) / kPart);
   long long g = num_sms(device);
@@ -677,8 +762,6 @@ size_t decode_workspace_bytes(int B, int Hkv, int D, int grid) {
   size_t bytes = slots * kSlotFloats(D) * sizeof(float) + (size_t)B * Hkv * sizeof(int);
   return (bytes + 255) / 256 * 256;
 }
-
-I8KV_DEFINE_ERROR_ACCESSOR(read_error_decode)
 
 cudaError_t launch_int8_decode(const DecodeParams& p, cudaStream_t stream) {
   if (p.D == 256) return launch_decode_d<256>(p, stream);
