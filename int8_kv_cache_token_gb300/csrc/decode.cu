@@ -595,46 +595,71 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
         }
         named_bar_sync(1, kCWarps * 32);
         if (ctrl[9]) {
-          // last CTA of the pair: log-sum-exp merge of the nseg partials
+          // last CTA of the pair: log-sum-exp merge of the nseg partials.  Every
+          // load is issued by its own thread (no thread walks a chain of L2 loads).
           __threadfence();
           const int nseg = cl - cf + 1;
           const float* part0 = p.ws_part + (size_t)(pair + cf) * kSlotFloats(D);
-          float* Ms = mbuf;               // [8]
-          float* den = mbuf + kRows;      // [8]
-          float* wts = mbuf + 2 * kRows;  // [nseg][8]
+          float* Ms = mbuf;                      // [8] common max per row
+          float* den = mbuf + kRows;             // [8] denominators
+          float* wts = mbuf + 2 * kRows;         // [nseg][8] segment weights (after: exp(M_s - M))
+          float* ls = wts + (size_t)nseg * kRows;  // [nseg][8] segment sums
+          for (int idx = tid; idx < nseg * kRows; idx += kCWarps * 32) {
+            const int sgi = idx / kRows, row = idx % kRows;
+            const float* ps = part0 + (size_t)sgi * kWS + kRows * D;
+            wts[idx] = __ldcg(ps + row);
+            ls[idx] = __ldcg(ps + kRows + row);
+          }
+          named_bar_sync(1, kCWarps * 32);
           if (tid < kRows) {
             float mm = -INFINITY;
-            for (int sgi = 0; sgi < nseg; ++sgi) mm = fmaxf(mm, __ldcg(part0 + (size_t)sgi * kWS + kRows * D + tid));
+            for (int sgi = 0; sgi < nseg; ++sgi) mm = fmaxf(mm, wts[sgi * kRows + tid]);
             Ms[tid] = mm;
           }
           named_bar_sync(1, kCWarps * 32);
           for (int idx = tid; idx < nseg * kRows; idx += kCWarps * 32) {
-            const int sgi = idx / kRows, row = idx % kRows;
-            wts[idx] = (row < G) ? expf(__ldcg(part0 + (size_t)sgi * kWS + kRows * D + row) - Ms[row]) : 0.f;
+            const int row = idx % kRows;
+            wts[idx] = (row < G) ? expf(wts[idx] - Ms[row]) : 0.f;
           }
           named_bar_sync(1, kCWarps * 32);
           if (tid < kRows) {
             float dd = 0.f;
-            for (int sgi = 0; sgi < nseg; ++sgi)
-              dd += wts[sgi * kRows + tid] * __ldcg(part0 + (size_t)sgi * kWS + kRows * D + kRows + tid);
+            for (int sgi = 0; sgi < nseg; ++sgi) dd += wts[sgi * kRows + tid] * ls[sgi * kRows + tid];
             den[tid] = dd;
           }
           named_bar_sync(1, kCWarps * 32);
           for (int idx = tid; idx < G * (D / 4); idx += kCWarps * 32) {
             const int row = idx / (D / 4), d4 = idx % (D / 4);
-            float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int sgi = 0; sgi < nseg; ++sgi) {
-              const float4 v4 = __ldcg(reinterpret_cast<const float4*>(part0 + (size_t)sgi * kWS + row * D) + d4);
+            const float4* col = reinterpret_cast<const float4*>(part0 + row * D) + d4;
+            float4 a4[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) a4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            int sgi = 0;
+            for (; sgi + 8 <= nseg; sgi += 8) {
+              float4 v8[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) v8[k] = __ldcg(col + (size_t)(sgi + k) * (kWS / 4));
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const float wgt = wts[(sgi + k) * kRows + row];
+                a4[k & 3].x = fmaf(wgt, v8[k].x, a4[k & 3].x);
+                a4[k & 3].y = fmaf(wgt, v8[k].y, a4[k & 3].y);
+                a4[k & 3].z = fmaf(wgt, v8[k].z, a4[k & 3].z);
+                a4[k & 3].w = fmaf(wgt, v8[k].w, a4[k & 3].w);
+              }
+            }
+            for (; sgi < nseg; ++sgi) {
+              const float4 v4 = __ldcg(col + (size_t)sgi * (kWS / 4));
               const float wgt = wts[sgi * kRows + row];
-              a4.x = fmaf(wgt, v4.x, a4.x);
-              a4.y = fmaf(wgt, v4.y, a4.y);
-              a4.z = fmaf(wgt, v4.z, a4.z);
-              a4.w = fmaf(wgt, v4.w, a4.w);
+              a4[0].x = fmaf(wgt, v4.x, a4[0].x);
+              a4[0].y = fmaf(wgt, v4.y, a4[0].y);
+              a4[0].z = fmaf(wgt, v4.z, a4[0].z);
+              a4[0].w = fmaf(wgt, v4.w, a4[0].w);
             }
             const float inv = 1.0f / den[row];
             *reinterpret_cast<float4*>(p.out + ((size_t)wk.b * Hq + wk.kvh * G + row) * D + 4 * d4) =
-                make_float4(a4.x * inv, a4.y * inv, a4.z * inv, a4.w * inv);
+                make_float4((a4[0].x + a4[1].x + a4[2].x + a4[3].x) * inv, (a4[0].y + a4[1].y + a4[2].y + a4[3].y) * inv,
+                            (a4[0].z + a4[1].z + a4[2].z + a4[3].z) * inv, (a4[0].w + a4[1].w + a4[2].w + a4[3].w) * inv);
           }
           if (tid == 0) p.ws_count[pair] = 0;
           named_bar_sync(1, kCWarps * 32);
