@@ -120,6 +120,33 @@ i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const fl
                                         int partition, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Allocation-free variant of i8kv_int8_paged_decode_attn.  The pages have   */
+/* no counterpart: this entry point exists for callers that cannot allocate   */
+/* device memory when they run a decode step -- for example a plugin inside  */
+/* another inference runtime, or a server whose memory planner reserved all  */
+/* device memory at start-up -- and so cannot provide a workspace.           */
+/* Same arguments and result as i8kv_int8_paged_decode_attn without the      */
+/* workspace: the merge scratch is a fixed 8 MiB array inside the library    */
+/* (8,388,608 bytes; every GPU that loads the library holds it until the     */
+/* process exits).  It calls no cudaMalloc or cudaFree.                      */
+/* Limit: i8kv_decode_workspace_bytes(B, Hq, Hkv, D, ...) must not exceed     */
+/* 8 MiB (about (B*Hkv + number of SMs) * (32*D + 64) bytes), else the call   */
+/* returns I8KV_ERR_WORKSPACE and launches nothing.                          */
+/* The first call on a device looks up the scratch's device address (with   */
+/* that device current), so make the first call on each device before any   */
+/* stream capture.  Each call clears the scratch's ticket counters on        */
+/* `stream` before the kernel.  All calls share the one scratch area: calls  */
+/* that overlap on the GPU (other streams, other host threads) race and give */
+/* wrong results -- serialize them, e.g. on one stream.                      */
+/* ------------------------------------------------------------------------ */
+i8kv_status i8kv_int8_paged_decode_attn_noalloc(float* out, const int8_t* q_i8, const float* q_scale,
+                                                const int8_t* k_cache, const int8_t* v_cache, const float* k_scale,
+                                                const float* v_scale, const int32_t* block_tables,
+                                                const int32_t* seq_lens, int B, int Hq, int Hkv, int D,
+                                                int block_size, int max_blocks, int num_blocks, float softmax_scale,
+                                                int partition, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* INT8 prefix-prefill chunk ([PV] §2.1, [KV] §3.2): one online softmax over */
 /* the cached history and the chunk itself.  Chunk query j (absolute         */
 /* position history_len + j) attends to cache positions 0..history_len + j   */

@@ -174,6 +174,39 @@ i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const fl
   return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "int8 decode launch");
 }
 
+i8kv_status i8kv_int8_paged_decode_attn_noalloc(float* out, const int8_t* q_i8, const float* q_scale,
+                                                const int8_t* k_cache, const int8_t* v_cache, const float* k_scale,
+                                                const float* v_scale, const int32_t* block_tables,
+                                                const int32_t* seq_lens, int B, int Hq, int Hkv, int D,
+                                                int block_size, int max_blocks, int num_blocks, float softmax_scale,
+                                                int partition, void* stream) {
+  // Same checks and the same kernel as i8kv_int8_paged_decode_attn; only the
+  // workspace comes from the library's fixed device scratch instead of the caller.
+  i8kv_status s = check_heads(Hq, Hkv, D);
+  if (s != I8KV_OK) return s;
+  REQUIRE(B >= 0 && max_blocks > 0, I8KV_ERR_INVALID_ARG, "B=%d max_blocks=%d", B, max_blocks);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e, "noalloc decode: cudaGetDevice");
+  const int grid = i8kv::decode_grid(dev, B, Hkv, max_blocks);
+  const size_t need = i8kv::decode_workspace_bytes(B, Hkv, D, grid);
+  REQUIRE(need <= i8kv::noalloc_scratch_bytes(), I8KV_ERR_WORKSPACE,
+          "noalloc decode needs %zu bytes of scratch for B=%d Hkv=%d D=%d; the fixed scratch holds %zu bytes "
+          "(use i8kv_int8_paged_decode_attn with a caller workspace)",
+          need, B, Hkv, D, i8kv::noalloc_scratch_bytes());
+  void* scratch = nullptr;
+  e = i8kv::noalloc_scratch_address(dev, &scratch);
+  if (e != cudaSuccess) return from_cuda(e, "noalloc decode: cudaGetSymbolAddress");
+  i8kv::DecodeParams p{};
+  s = decode_common(p, q_i8, q_scale, true, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, B, Hq, Hkv,
+                    D, block_size, max_blocks, num_blocks, softmax_scale, partition, scratch, need, out);
+  if (s != I8KV_OK || B == 0) return s;
+  // The merge tickets must start at zero; the scratch keeps whatever the last call left.
+  e = cudaMemsetAsync(p.ws_count, 0, (size_t)B * Hkv * sizeof(int), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return from_cuda(e, "noalloc decode: clear tickets");
+  return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "noalloc int8 decode launch");
+}
+
 i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
                                   const int8_t* v_cache, const float* k_scale, const float* v_scale,
                                   const int32_t* block_table, int history_len, int chunk_len, int Hq, int Hkv, int D,

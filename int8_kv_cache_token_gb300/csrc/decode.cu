@@ -36,6 +36,8 @@
 //    <= 516,128), so the fp32 accumulator holds the exact int32 result.  On
 //    sm_103a this path has about 4x the throughput of mma.sync s8; the debug QK
 //    entry point checks the accumulators bit for bit against integer QK.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -791,6 +793,38 @@ size_t decode_workspace_bytes(int B, int Hkv, int D, int grid) {
 cudaError_t launch_int8_decode(const DecodeParams& p, cudaStream_t stream) {
   if (p.D == 256) return launch_decode_d<256>(p, stream);
   return launch_decode_d<128>(p, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Fixed scratch for the allocation-free decode entry point.  Some callers cannot
+// call cudaMalloc when they run a decode step (for example a plugin inside
+// another inference runtime whose memory planner owns every byte, or a server
+// that reserves all device memory at start-up), so this file keeps one
+// device-resident scratch area of kNoAllocScratchBytes.  Every GPU that loads
+// the library holds it until the process exits.  In host code the array's name
+// is only a host-side stand-in, so its device address is taken once per device
+// with cudaGetSymbolAddress (with that device current) and passed to the kernel.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+}  // namespace
+
+size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+cudaError_t noalloc_scratch_address(int device, void** addr) {
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[device] == nullptr) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_addr[device] = ptr;
+  }
+  *addr = g_noalloc_addr[device];
+  return cudaSuccess;
 }
 
 cudaError_t launch_debug_qk(const DebugQKParams& p, cudaStream_t stream) {

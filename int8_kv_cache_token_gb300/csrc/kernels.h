@@ -78,6 +78,10 @@ size_t decode_workspace_bytes(int B, int Hkv, int D, int grid);
 cudaError_t launch_int8_decode(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_bf16_decode(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_debug_qk(const DebugQKParams& p, cudaStream_t stream);
+
+// Fixed device scratch of the allocation-free decode entry point (decode.cu).
+size_t noalloc_scratch_bytes();
+cudaError_t noalloc_scratch_address(int device, void** addr);
 cudaError_t launch_int8_prefix(const PrefixParams& p, cudaStream_t stream);
 
 }  // namespace i8kv
