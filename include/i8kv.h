@@ -12,7 +12,10 @@
  *    a per-thread last-error string and one device-side error word.
  *  - bf16 tensors are passed as `const uint16_t*` (raw bf16 bit patterns).
  *  - All launches are asynchronous on `stream` (a cudaStream_t passed as void*;
- *    NULL is the legacy default stream).  Nothing synchronizes.
+ *    NULL is the legacy default stream).  Nothing synchronizes.  Kernels are
+ *    launched with programmatic dependent launch: a kernel may be scheduled
+ *    while the previous kernel on the stream is still running, but it reads
+ *    no global memory before that kernel has finished.
  *  - Argument errors are reported synchronously through the status code, before
  *    anything is launched; i8kv_last_error() gives a one-line reason.  A launch
  *    failure reported by the CUDA runtime maps to I8KV_ERR_CUDA.
@@ -106,10 +109,11 @@ i8kv_status i8kv_kv_quant_write(const uint16_t* k, const uint16_t* v, const int3
 /* block_tables: int32 [B, max_blocks]; entries past ceil(L/bs) are unused.  */
 /* softmax_scale <= 0 selects 1/sqrt(D).  partition must be 256.             */
 /* workspace: device memory of at least i8kv_decode_workspace_bytes(...)     */
-/*   bytes, ZERO-FILLED ONCE before its first use.  Every call leaves its    */
-/*   counters at zero again, so it may be reused by later calls on the same  */
-/*   stream; calls that overlap in time need separate workspaces.  After a   */
-/*   call that returned an error, zero-fill it again.                        */
+/*   bytes; it needs no initialization (every record the call reads is      */
+/*   written earlier in the same call).  Reuse it for later calls on the     */
+/*   same stream; calls that overlap in time need separate workspaces.       */
+/* The call launches two kernels (the attention and a merge of the pairs    */
+/* whose history spans several CTAs).                                       */
 /* ------------------------------------------------------------------------ */
 size_t i8kv_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_blocks, int block_size, int partition);
 

@@ -156,7 +156,7 @@ static i8kv_status decode_common(i8kv::DecodeParams& p, const void* q, const flo
   p.num_blocks = num_blocks;
   p.sm_scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
   p.ws_part = ws;
-  p.ws_count = reinterpret_cast<int*>(ws + slots * (8 * (size_t)D + 16));
+  p.ws_info = reinterpret_cast<int*>(ws + slots * (8 * (size_t)D + 16));
   p.grid = grid;
   return I8KV_OK;
 }
@@ -201,9 +201,10 @@ i8kv_status i8kv_int8_paged_decode_attn_noalloc(float* out, const int8_t* q_i8, 
   s = decode_common(p, q_i8, q_scale, true, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, B, Hq, Hkv,
                     D, block_size, max_blocks, num_blocks, softmax_scale, partition, scratch, need, out);
   if (s != I8KV_OK || B == 0) return s;
-  // The merge tickets must start at zero; the scratch keeps whatever the last call left.
-  e = cudaMemsetAsync(p.ws_count, 0, (size_t)B * Hkv * sizeof(int), static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return from_cuda(e, "noalloc decode: clear tickets");
+  // The per-pair merge records are rewritten by every call before they are read;
+  // clearing them anyway keeps a call independent of what the last one left.
+  e = cudaMemsetAsync(p.ws_info, 0xff, (size_t)B * Hkv * sizeof(int), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return from_cuda(e, "noalloc decode: clear merge records");
   return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "noalloc int8 decode launch");
 }
 

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace i8kv {
 
 // Device error word: 0 = fine; the first failure wins.
@@ -117,6 +119,14 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream is still
+// running; griddep_wait() blocks until that kernel has finished and its memory
+// is visible (a no-op for an ordinary launch).  griddep_launch_dependents()
+// lets the next kernel on the stream start its own launch early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Named barrier among `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -147,6 +157,58 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// ----------------------------------------------------------------- exact INT8 on the f16 tensor path
+// Four int8 codes (little-endian) -> f16x2 {c0, c1} and {c2, c3}, exactly:
+// byte b becomes the f16 1024 + (b ^ 0x80) = 1152 + c, then 1152 is subtracted.
+__device__ __forceinline__ void s8x4_to_f16(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = x ^ 0x80808080u;
+  lo = __byte_perm(u, 0x64646464u, 0x5140);
+  hi = __byte_perm(u, 0x64646464u, 0x7362);
+  const uint32_t bias = 0x64806480u;  // f16x2 (1152, 1152)
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(bias));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(bias));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One exact INT8 m16n8k32 step on the f16 tensor path.  The s8 A fragment
+// (rows g / g+8 x k 4t..4t+3 and 16+4t..16+4t+3, as ldmatrix delivers it) is
+// split into two k16 MMAs over k {0..15} and {16..31}; inside each the f16
+// fragment order pairs logical k (2t, 2t+1 | 2t+8, 2t+9) with physical k
+// (4t, 4t+1 | 4t+2, 4t+3).  b[0..3] is B in the matching f16 form (b[0], b[1]
+// for k 0..15, b[2], b[3] for k 16..31).  The same permutation on both
+// operands leaves the sum unchanged.
+__device__ __forceinline__ void mma_s8a_f16b(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+  uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
+  s8x4_to_f16(a[0], a0l, a0h);
+  s8x4_to_f16(a[1], a1l, a1h);
+  s8x4_to_f16(a[2], a2l, a2h);
+  s8x4_to_f16(a[3], a3l, a3h);
+  mma_f16_16816(d, a0l, a1l, a0h, a1h, b[0], b[1]);
+  mma_f16_16816(d, a2l, a3l, a2h, a3h, b[2], b[3]);
+}
+
+// Two small integers (|x| <= 2048) as an exact f16x2 {lo, hi}.
+__device__ __forceinline__ uint32_t f16x2_of(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// s8 B fragment (k 4t..4t+3 and 16+4t..16+4t+3 of column g) -> the f16 form above.
+__device__ __forceinline__ void s8b_to_f16(uint32_t x0, uint32_t x1, uint32_t (&b)[4]) {
+  s8x4_to_f16(x0, b[0], b[1]);
+  s8x4_to_f16(x1, b[2], b[3]);
+}
+
+
 // ----------------------------------------------------------------- numerics
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
@@ -154,6 +216,25 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __
 __device__ __forceinline__ uint32_t pack_s8x4(int a, int b, int c, int d) {
   return (uint32_t)(a & 0xff) | ((uint32_t)(b & 0xff) << 8) | ((uint32_t)(c & 0xff) << 16) |
          ((uint32_t)(d & 0xff) << 24);
+}
+
+// Host: launch `kernel` with programmatic stream serialization allowed, so its
+// launch overlaps the tail of the previous kernel on `stream` (the kernel must
+// call griddep_wait() before it touches memory the previous kernel writes).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace i8kv

@@ -65,8 +65,8 @@ __host__ __device__ inline SmemLayout decode_layout(int D, int nslots) {
   size_t off = 0;
   L.ring = off;
   off += (size_t)nslots * item;
-  L.merge = off;  // 4 warp states [8 rows][D] + l [8] (+ maxima [8 warps][8 rows])
-  off += (size_t)(4 * (kRows * D + 2 * kRows) + kCWarps * kRows) * sizeof(float);
+  L.merge = off;  // 4 warp states [8 rows][D + 4] + l [8] (+ maxima [8 warps][8 rows])
+  off += (size_t)(4 * (kRows * (D + 4) + 2 * kRows) + kCWarps * kRows) * sizeof(float);
   L.wq = off;     // per-warp transpose of the quantized W: [8 rows][32 tokens] int8
   off += (size_t)kCWarps * kRows * kGroup;
   L.bars = off;
@@ -123,49 +123,6 @@ __device__ __forceinline__ void pipe_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// Four int8 codes (little-endian) -> f16x2 {c0, c1} and {c2, c3}, exactly:
-// byte b becomes the f16 1024 + (b ^ 0x80) = 1152 + c, then 1152 is subtracted.
-__device__ __forceinline__ void s8x4_to_f16(uint32_t x, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = x ^ 0x80808080u;
-  lo = __byte_perm(u, 0x64646464u, 0x5140);
-  hi = __byte_perm(u, 0x64646464u, 0x7362);
-  const uint32_t bias = 0x64806480u;  // f16x2 (1152, 1152)
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(bias));
-  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(bias));
-}
-
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// One exact INT8 m16n8k32 step on the f16 tensor path.  The s8 A fragment
-// (rows g / g+8 x k 4t..4t+3 and 16+4t..16+4t+3, as ldmatrix delivers it) is
-// split into two k16 MMAs over k {0..15} and {16..31}; inside each the f16
-// fragment order pairs logical k (2t, 2t+1 | 2t+8, 2t+9) with physical k
-// (4t, 4t+1 | 4t+2, 4t+3).  b[0..3] is B in the matching f16 form (b[0], b[1]
-// for k 0..15, b[2], b[3] for k 16..31).  The same permutation on both
-// operands leaves the sum unchanged.
-__device__ __forceinline__ void mma_s8a_f16b(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[4]) {
-  uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
-  s8x4_to_f16(a[0], a0l, a0h);
-  s8x4_to_f16(a[1], a1l, a1h);
-  s8x4_to_f16(a[2], a2l, a2h);
-  s8x4_to_f16(a[3], a3l, a3h);
-  mma_f16_16816(d, a0l, a1l, a0h, a1h, b[0], b[1]);
-  mma_f16_16816(d, a2l, a3l, a2h, a3h, b[2], b[3]);
-}
-
-// s8 B fragment (k 4t..4t+3 and 16+4t..16+4t+3 of column g) -> the f16 form above.
-__device__ __forceinline__ void s8b_to_f16(uint32_t x0, uint32_t x1, uint32_t (&b)[4]) {
-  s8x4_to_f16(x0, b[0], b[1]);
-  s8x4_to_f16(x1, b[2], b[3]);
-}
-
 // Query fragments (B operand of QK, f16 form) of the GQA-packed rows: column g of
 // the N-tile is query head kvh*G + g; per 32-dim step s the s8 fragment holds
 // dims 32s + {4t..4t+3} and 32s + 16 + {4t..4t+3}.
@@ -209,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
   constexpr int NDT = D / 16;  // PV head-dim tiles (every warp covers all of D for its group)
   constexpr int kPage = D * kBS;
   constexpr int kItem = kPart * D;
-  constexpr int kWS = kRows * D + 2 * kRows;  // one warp state in the merge buffer
+  constexpr int kRS = D + 4;                   // row stride of a warp state (conflict-free stores)
+  constexpr int kWS = kRows * kRS + 2 * kRows;  // one warp state in the merge buffer
   extern __shared__ __align__(1024) uint8_t smem[];
   const SmemLayout lay = decode_layout(D, nslots);
   int8_t* ring = reinterpret_cast<int8_t*>(smem + lay.ring);
@@ -225,6 +183,18 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
   const int N = gridDim.x, c = blockIdx.x;
   const int maxL = p.max_blocks * kBS;
 
+  if (tid == 0) {
+    for (int s = 0; s < nslots; ++s) {
+      mbar_init(&full[s], 32);
+      mbar_init(&empty[s], kCWarps);
+    }
+    fence_mbar_init();
+  }
+  // Everything above touches only shared memory; from here on the kernel reads
+  // what earlier work on the stream wrote.
+  griddep_wait();
+  griddep_launch_dependents();
+
   // ---- work split: every CTA scans seq_lens (warp 0) ----
   if (warp == 0) {
     long long total = 0;
@@ -236,9 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
         if (raw > maxL) record_error(2);
         const int L = clamp_len(raw, maxL);
         u = (L + kPart - 1) / kPart * Hkv;
-        if (L == 0 && b % N == c) {  // empty sequence: zero rows
+        if (L == 0 && b % N == c) {  // empty sequence: zero rows, nothing to merge
           float* o = p.out + (size_t)b * Hq * D;
           for (int i = 0; i < Hq * D; ++i) o[i] = 0.f;
+          for (int h = 0; h < Hkv; ++h) p.ws_info[b * Hkv + h] = -1;
         }
       }
       for (int o = 16; o >= 1; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
@@ -287,13 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
         ctrl[7] = (int)(U >> 31);
       }
     }
-  }
-  if (tid == 0) {
-    for (int s = 0; s < nslots; ++s) {
-      mbar_init(&full[s], 32);
-      mbar_init(&empty[s], kCWarps);
-    }
-    fence_mbar_init();
   }
   __syncthreads();
   const int n_units = ctrl[0];
@@ -543,10 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
 #pragma unroll
           for (int dt = 0; dt < NDT; ++dt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) buf[(2 * t + (e & 1)) * D + dt * 16 + g + 8 * (e >> 1)] = o[dt][e];
+            for (int e = 0; e < 4; ++e) buf[(2 * t + (e & 1)) * kRS + dt * 16 + g + 8 * (e >> 1)] = o[dt][e];
           if (g == 0) {
-            buf[kRows * D + 2 * t] = lrun[0];
-            buf[kRows * D + 2 * t + 1] = lrun[1];
+            buf[kRows * kRS + 2 * t] = lrun[0];
+            buf[kRows * kRS + 2 * t + 1] = lrun[1];
           }
         }
         named_bar_sync(1, kCWarps * 32);
@@ -555,15 +519,17 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
 #pragma unroll
           for (int dt = 0; dt < NDT; ++dt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[dt][e] += buf[(2 * t + (e & 1)) * D + dt * 16 + g + 8 * (e >> 1)];
-          lrun[0] += buf[kRows * D + 2 * t];
-          lrun[1] += buf[kRows * D + 2 * t + 1];
+            for (int e = 0; e < 4; ++e) o[dt][e] += buf[(2 * t + (e & 1)) * kRS + dt * 16 + g + 8 * (e >> 1)];
+          lrun[0] += buf[kRows * kRS + 2 * t];
+          lrun[1] += buf[kRows * kRS + 2 * t + 1];
         }
         named_bar_sync(1, kCWarps * 32);
       }
       // warp 0 now holds this CTA's (M, L, O) for the pair
       const long long Up = wk.ub + (long long)wk.kvh * wk.np;
       const int cf = cta_of(Up, U, Nw), cl = cta_of(Up + wk.np - 1, U, Nw);
+      // the CTA holding the pair's first unit records whether a merge is needed
+      if (c == cf && tid == 0) p.ws_info[pair] = (cf == cl) ? -1 : ((cf << 16) | cl);
       if (cf == cl) {
         if (warp == 0) {
 #pragma unroll
@@ -575,96 +541,18 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
               if (row < G) p.out[((size_t)wk.b * Hq + wk.kvh * G + row) * D + d] = o[dt][e] / lrun[e & 1];
             }
         }
-      } else {
+      } else if (warp == 0) {
+        // one partial per CTA; decode_merge_kernel combines them after this kernel
         float* part = p.ws_part + (size_t)(pair + c) * kSlotFloats(D);
-        if (warp == 0) {
 #pragma unroll
-          for (int dt = 0; dt < NDT; ++dt)
+        for (int dt = 0; dt < NDT; ++dt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) part[(2 * t + (e & 1)) * D + dt * 16 + g + 8 * (e >> 1)] = o[dt][e];
-          if (g == 0) {
-            part[kRows * D + 2 * t] = M[0];
-            part[kRows * D + 2 * t + 1] = M[1];
-            part[kRows * D + kRows + 2 * t] = lrun[0];
-            part[kRows * D + kRows + 2 * t + 1] = lrun[1];
-          }
-          __threadfence();
-        }
-        named_bar_sync(1, kCWarps * 32);
-        if (tid == 0) {
-          const int old = atomicAdd(&p.ws_count[pair], 1);
-          ctrl[9] = (old == cl - cf) ? 1 : 0;
-        }
-        named_bar_sync(1, kCWarps * 32);
-        if (ctrl[9]) {
-          // last CTA of the pair: log-sum-exp merge of the nseg partials.  Every
-          // load is issued by its own thread (no thread walks a chain of L2 loads).
-          __threadfence();
-          const int nseg = cl - cf + 1;
-          const float* part0 = p.ws_part + (size_t)(pair + cf) * kSlotFloats(D);
-          float* Ms = mbuf;                      // [8] common max per row
-          float* den = mbuf + kRows;             // [8] denominators
-          float* wts = mbuf + 2 * kRows;         // [nseg][8] segment weights (after: exp(M_s - M))
-          float* ls = wts + (size_t)nseg * kRows;  // [nseg][8] segment sums
-          for (int idx = tid; idx < nseg * kRows; idx += kCWarps * 32) {
-            const int sgi = idx / kRows, row = idx % kRows;
-            const float* ps = part0 + (size_t)sgi * kWS + kRows * D;
-            wts[idx] = __ldcg(ps + row);
-            ls[idx] = __ldcg(ps + kRows + row);
-          }
-          named_bar_sync(1, kCWarps * 32);
-          if (tid < kRows) {
-            float mm = -INFINITY;
-            for (int sgi = 0; sgi < nseg; ++sgi) mm = fmaxf(mm, wts[sgi * kRows + tid]);
-            Ms[tid] = mm;
-          }
-          named_bar_sync(1, kCWarps * 32);
-          for (int idx = tid; idx < nseg * kRows; idx += kCWarps * 32) {
-            const int row = idx % kRows;
-            wts[idx] = (row < G) ? expf(wts[idx] - Ms[row]) : 0.f;
-          }
-          named_bar_sync(1, kCWarps * 32);
-          if (tid < kRows) {
-            float dd = 0.f;
-            for (int sgi = 0; sgi < nseg; ++sgi) dd += wts[sgi * kRows + tid] * ls[sgi * kRows + tid];
-            den[tid] = dd;
-          }
-          named_bar_sync(1, kCWarps * 32);
-          for (int idx = tid; idx < G * (D / 4); idx += kCWarps * 32) {
-            const int row = idx / (D / 4), d4 = idx % (D / 4);
-            const float4* col = reinterpret_cast<const float4*>(part0 + row * D) + d4;
-            float4 a4[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) a4[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            int sgi = 0;
-            for (; sgi + 8 <= nseg; sgi += 8) {
-              float4 v8[8];
-#pragma unroll
-              for (int k = 0; k < 8; ++k) v8[k] = __ldcg(col + (size_t)(sgi + k) * (kWS / 4));
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const float wgt = wts[(sgi + k) * kRows + row];
-                a4[k & 3].x = fmaf(wgt, v8[k].x, a4[k & 3].x);
-                a4[k & 3].y = fmaf(wgt, v8[k].y, a4[k & 3].y);
-                a4[k & 3].z = fmaf(wgt, v8[k].z, a4[k & 3].z);
-                a4[k & 3].w = fmaf(wgt, v8[k].w, a4[k & 3].w);
-              }
-            }
-            for (; sgi < nseg; ++sgi) {
-              const float4 v4 = __ldcg(col + (size_t)sgi * (kWS / 4));
-              const float wgt = wts[sgi * kRows + row];
-              a4[0].x = fmaf(wgt, v4.x, a4[0].x);
-              a4[0].y = fmaf(wgt, v4.y, a4[0].y);
-              a4[0].z = fmaf(wgt, v4.z, a4[0].z);
-              a4[0].w = fmaf(wgt, v4.w, a4[0].w);
-            }
-            const float inv = 1.0f / den[row];
-            *reinterpret_cast<float4*>(p.out + ((size_t)wk.b * Hq + wk.kvh * G + row) * D + 4 * d4) =
-                make_float4((a4[0].x + a4[1].x + a4[2].x + a4[3].x) * inv, (a4[0].y + a4[1].y + a4[2].y + a4[3].y) * inv,
-                            (a4[0].z + a4[1].z + a4[2].z + a4[3].z) * inv, (a4[0].w + a4[1].w + a4[2].w + a4[3].w) * inv);
-          }
-          if (tid == 0) p.ws_count[pair] = 0;
-          named_bar_sync(1, kCWarps * 32);
+          for (int e = 0; e < 4; ++e) part[(2 * t + (e & 1)) * D + dt * 16 + g + 8 * (e >> 1)] = o[dt][e];
+        if (g == 0) {
+          part[kRows * D + 2 * t] = M[0];
+          part[kRows * D + 2 * t + 1] = M[1];
+          part[kRows * D + kRows + 2 * t] = lrun[0];
+          part[kRows * D + kRows + 2 * t + 1] = lrun[1];
         }
       }
     }
@@ -674,6 +562,79 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
       sk[k] = sk_n[k];
       sv[k] = sv_n[k];
     }
+  }
+}
+
+// Log-sum-exp merge of the partials of pairs that span CTAs: one CTA per
+// (pair, query row).  Thread (slice, column) sums every SL-th segment of one
+// float4 column; the slices are then added in a fixed order.
+constexpr int kMaxSeg = 1024;
+
+template <int D>
+__global__ void __launch_bounds__(256) decode_merge_kernel(DecodeParams p) {
+  constexpr int COLS = D / 4, SL = 256 / COLS;
+  __shared__ float wsh[kMaxSeg], lsh[kMaxSeg];
+  __shared__ float4 red[SL][COLS];
+  __shared__ float Msh, den;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int tid = threadIdx.x;
+  const int pair = blockIdx.x / p.G, row = blockIdx.x % p.G;
+  const int info = p.ws_info[pair];
+  if (info < 0) return;
+  const int cf = info >> 16, cl = info & 0xffff, nseg = cl - cf + 1;
+  if (nseg > kMaxSeg) {
+    record_error(2);
+    return;
+  }
+  const float* part0 = p.ws_part + (size_t)(pair + cf) * kSlotFloats(D);
+  for (int s = tid; s < nseg; s += 256) {
+    wsh[s] = part0[(size_t)s * kSlotFloats(D) + kRows * D + row];
+    lsh[s] = part0[(size_t)s * kSlotFloats(D) + kRows * D + kRows + row];
+  }
+  __syncthreads();
+  if (tid < 32) {
+    float m = -INFINITY;
+    for (int s = tid; s < nseg; s += 32) m = fmaxf(m, wsh[s]);
+    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (tid == 0) Msh = m;
+  }
+  __syncthreads();
+  for (int s = tid; s < nseg; s += 256) wsh[s] = expf(wsh[s] - Msh);
+  __syncthreads();
+  if (tid < 32) {
+    float dd = 0.f;
+    for (int s = tid; s < nseg; s += 32) dd += wsh[s] * lsh[s];
+    for (int off = 16; off >= 1; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
+    if (tid == 0) den = dd;
+  }
+  const int slice = tid / COLS, col = tid % COLS;
+  const float4* base = reinterpret_cast<const float4*>(part0 + row * D) + col;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int s = slice; s < nseg; s += SL) {
+    const float4 v = base[(size_t)s * (kSlotFloats(D) / 4)];
+    const float w = wsh[s];
+    a.x = fmaf(w, v.x, a.x);
+    a.y = fmaf(w, v.y, a.y);
+    a.z = fmaf(w, v.z, a.z);
+    a.w = fmaf(w, v.w, a.w);
+  }
+  red[slice][col] = a;
+  __syncthreads();
+  if (tid < COLS) {
+    float4 r = red[0][tid];
+#pragma unroll
+    for (int k = 1; k < SL; ++k) {
+      r.x += red[k][tid].x;
+      r.y += red[k][tid].y;
+      r.z += red[k][tid].z;
+      r.w += red[k][tid].w;
+    }
+    const float inv = 1.0f / den;
+    const int b = pair / p.Hkv, kvh = pair % p.Hkv;
+    *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + kvh * p.G + row) * D + 4 * tid) =
+        make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv);
   }
 }
 
@@ -769,8 +730,9 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
-  int8_decode_kernel<D><<<p.grid, kThreads, smem, stream>>>(p, ns);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(int8_decode_kernel<D>, dim3(p.grid), dim3(kThreads), smem, stream, p, ns);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_merge_kernel<D>, dim3(p.B * p.Hkv * p.G), dim3(256), 0, stream, p);
 }
 
 }  // namespace

@@ -37,7 +37,7 @@ struct DecodeParams {
   int B, Hq, Hkv, G, D, max_blocks, num_blocks;
   float sm_scale;
   float* ws_part;             // [(B*Hkv + grid) slots][8 rows * D + 16]
-  int* ws_count;              // [B*Hkv]
+  int* ws_info;               // [B*Hkv] per pair: -1 (no merge) or first CTA << 16 | last CTA
   int grid;                   // CTAs launched (the work split depends on it)
 };
 

@@ -43,7 +43,7 @@ struct PrefixSmem {
   // per stage: K tile, V tile, K-scale rows, V-scale rows (Hkv <= 8)
   static constexpr int kScaleBytes = kBlocksPerStage * kBS * 8 * 4;
   static constexpr int kStageBytes = 2 * kTileBytes + 2 * kScaleBytes;
-  static constexpr int kQBytes = kRowsPerCTA * D;  // query tile, 16-byte chunks XOR-swizzled by row
+  static constexpr int kQBytes = kRowsPerCTA * D * 2;  // f16 query tile, 16-byte chunks XOR-swizzled by row
   static constexpr int kTotal = kStages * kStageBytes + kQBytes + 64;
 };
 
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
   constexpr int KS = D / 32;  // k-steps of QK
   constexpr int ND = D / 8;   // n-tiles of PV
   extern __shared__ __align__(1024) uint8_t smem[];
-  int8_t* qs = reinterpret_cast<int8_t*>(smem + kStages * S::kStageBytes);
+  uint8_t* qs = smem + kStages * S::kStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * S::kStageBytes + S::kQBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kStages);
 
@@ -120,16 +120,26 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
     for (int st = 0; st < kStages && st < n_stages; ++st) issue(st);
   }
 
-  // ---- query tile -> shared memory (16-byte chunk c of row r stored at chunk c ^ (r & 7)) ----
-  for (int i = tid; i < kRowsPerCTA * (D / 16); i += kWarps * 32) {
-    const int rr = i / (D / 16), ch = i % (D / 16);
+  // ---- query tile -> shared memory as exact f16 ----
+  // Head-dims are stored in the order the k16 MMAs consume them next to K
+  // fragments converted by s8b_to_f16: inside each 16-dim half of a 32-dim
+  // step, logical positions 0..7 hold physical dims {0,1,4,5,8,9,12,13} and
+  // 8..15 hold {2,3,6,7,10,11,14,15}.  Logical 16-byte chunk c (8 f16) of row r
+  // is stored at chunk c ^ (r & 7).
+  for (int i = tid; i < kRowsPerCTA * (D / 8); i += kWarps * 32) {
+    const int rr = i / (D / 8), ch = i % (D / 8);
     const int r = r0 + rr;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (r < R) {
       const int j = r / G, hq = kvh * G + r % G;
-      v = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)j * Hq + hq) * D) + ch);
+      v = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)j * Hq + hq) * D) + (ch >> 1));
     }
-    *reinterpret_cast<uint4*>(qs + (size_t)rr * D + ((ch ^ (rr & 7)) * 16)) = v;
+    const uint32_t sel = (ch & 1) ? 0x7632u : 0x5410u;
+    const uint32_t x0 = __byte_perm(v.x, v.y, sel), x1 = __byte_perm(v.z, v.w, sel);
+    uint4 h;
+    s8x4_to_f16(x0, h.x, h.y);
+    s8x4_to_f16(x1, h.z, h.w);
+    *reinterpret_cast<uint4*>(qs + (size_t)rr * (2 * D) + ((ch ^ (rr & 7)) * 16)) = h;
   }
   // ---- this warp's 16 rows: (token, head), causal limit, query scale ----
   int row_lim[2];
@@ -177,17 +187,17 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
     for (int grp = 0; grp < kKeysPerStage / 32; ++grp) {
       const int key0 = st * kKeysPerStage + grp * 32;  // absolute position of the group's first key
       if (key0 > warp_lim) break;                       // every row of this warp is past its causal limit
-      // ---- QK: 4 n-tiles of 8 permuted keys ----
-      int acc[4][4];
+      // ---- QK: 4 n-tiles of 8 permuted keys, exact on the f16 tensor path ----
+      float acc[4][4];
 #pragma unroll
       for (int n = 0; n < 4; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[n][e] = 0;
+        for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
       {
-        // A (query rows) from the swizzled tile: matrices (rows 0-7 | 8-15) x (chunk 2s | 2s+1)
+        // A (query rows, f16): matrices (rows 0-7 | 8-15) x (logical chunk c | c+1)
         const int qr = warp * 16 + ri + 8 * (mi & 1);
-        const int8_t* qrow = qs + (size_t)qr * D;
-        // B (keys): lanes 0-7 n-tile 2*np2 chunk 2s, 8-15 chunk 2s+1, 16-31 n-tile 2*np2+1
+        const uint8_t* qrow = qs + (size_t)qr * (2 * D);
+        // B (keys, s8): lanes 0-7 n-tile 2*np2 chunk 2s, 8-15 chunk 2s+1, 16-31 n-tile 2*np2+1
         const int8_t* krow[2];
 #pragma unroll
         for (int np2 = 0; np2 < 2; ++np2) {
@@ -196,14 +206,19 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
         }
 #pragma unroll
         for (int s = 0; s < KS; ++s) {
-          uint32_t a[4];
-          ldmatrix_x4(a, qrow + (((2 * s + (mi >> 1)) ^ (qr & 7)) * 16));
+          uint32_t a1[4], a2[4];
+          ldmatrix_x4(a1, qrow + (((4 * s + (mi >> 1)) ^ (qr & 7)) * 16));
+          ldmatrix_x4(a2, qrow + (((4 * s + 2 + (mi >> 1)) ^ (qr & 7)) * 16));
 #pragma unroll
           for (int np2 = 0; np2 < 2; ++np2) {
-            uint32_t bb[4];
+            uint32_t bb[4], f0[4], f1[4];
             ldmatrix_x4(bb, krow[np2] + (size_t)(2 * s) * (kBS * 16));
-            mma_s8_16832(acc[2 * np2], a, bb[0], bb[1]);
-            mma_s8_16832(acc[2 * np2 + 1], a, bb[2], bb[3]);
+            s8b_to_f16(bb[0], bb[1], f0);
+            s8b_to_f16(bb[2], bb[3], f1);
+            mma_f16_16816(acc[2 * np2], a1[0], a1[1], a1[2], a1[3], f0[0], f0[1]);
+            mma_f16_16816(acc[2 * np2], a2[0], a2[1], a2[2], a2[3], f0[2], f0[3]);
+            mma_f16_16816(acc[2 * np2 + 1], a1[0], a1[1], a1[2], a1[3], f1[0], f1[1]);
+            mma_f16_16816(acc[2 * np2 + 1], a2[0], a2[1], a2[2], a2[3], f1[2], f1[3]);
           }
         }
       }
@@ -220,7 +235,7 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
           float s = -INFINITY;
           if (key <= row_lim[h2] && key < total_keys) {
             const int kl = grp * 32 + kg;
-            s = __fmul_rn(__fmul_rn(__fmul_rn((float)acc[n][e], sq[h2]), sks[kl * Hkv + kvh]), csc);
+            s = __fmul_rn(__fmul_rn(__fmul_rn(acc[n][e], sq[h2]), sks[kl * Hkv + kvh]), csc);
           }
           sc[n][e] = s;
           mx[h2] = fmaxf(mx[h2], s);
@@ -260,23 +275,29 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
         A[h2] = fmaxf(A[h2], __shfl_xor_sync(0xffffffffu, A[h2], 1));
         A[h2] = fmaxf(A[h2], __shfl_xor_sync(0xffffffffu, A[h2], 2));
       }
-      float sW[2];
-      int q[4][4];
+      float sW[2], inv[2];
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) sW[h2] = __fdiv_rn(A[h2], 127.0f);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        sW[h2] = __fdiv_rn(A[h2], 127.0f);
+        inv[h2] = A[h2] > 0.f ? __fdiv_rn(127.0f, A[h2]) : 0.f;
+      }
+      float q[4][4];
 #pragma unroll
       for (int n = 0; n < 4; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int h2 = e >> 1;
-          q[n][e] = A[h2] > 0.f ? min(127, __float2int_rn(__fdiv_rn(w[n][e], sW[h2]))) : 0;
-        }
-      // A operand of PV: (row g | g+8) x (keys 4t..4t+3 | 16+4t..16+4t+3)
-      uint32_t pa[4];
-      pa[0] = pack_s8x4(q[0][0], q[0][1], q[1][0], q[1][1]);
-      pa[1] = pack_s8x4(q[0][2], q[0][3], q[1][2], q[1][3]);
-      pa[2] = pack_s8x4(q[2][0], q[2][1], q[3][0], q[3][1]);
-      pa[3] = pack_s8x4(q[2][2], q[2][3], q[3][2], q[3][3]);
+        for (int e = 0; e < 4; ++e) q[n][e] = fminf(127.f, rintf(w[n][e] * inv[e >> 1]));
+      // A operand of PV in f16 (exact integers): k16 MMA 1 takes the group's keys
+      // 0..15, MMA 2 keys 16..31, with logical k (2t, 2t+1 | 2t+8, 2t+9) holding
+      // keys (4t, 4t+1 | 4t+2, 4t+3) -- the order s8b_to_f16 gives the V fragments.
+      uint32_t pa1[4], pa2[4];
+      pa1[0] = f16x2_of(q[0][0], q[0][1]);
+      pa1[1] = f16x2_of(q[0][2], q[0][3]);
+      pa1[2] = f16x2_of(q[1][0], q[1][1]);
+      pa1[3] = f16x2_of(q[1][2], q[1][3]);
+      pa2[0] = f16x2_of(q[2][0], q[2][1]);
+      pa2[1] = f16x2_of(q[2][2], q[2][3]);
+      pa2[2] = f16x2_of(q[3][0], q[3][1]);
+      pa2[3] = f16x2_of(q[3][2], q[3][3]);
       if (alpha[0] != 1.f || alpha[1] != 1.f) {
 #pragma unroll
         for (int n = 0; n < ND; ++n) {
@@ -290,19 +311,23 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
       const int8_t* vb = vt + (size_t)(2 * grp + (mi & 1)) * S::kPage + ri * 16 + (mi >> 1) * (8 * 16);
 #pragma unroll
       for (int n = 0; n < ND; n += 2) {
-        uint32_t bb[4];
+        uint32_t bb[4], f0[4], f1[4];
         ldmatrix_x4(bb, vb + (size_t)n * (8 * 16));
-        int c0[4] = {0, 0, 0, 0}, c1[4] = {0, 0, 0, 0};
-        mma_s8_16832(c0, pa, bb[0], bb[1]);
-        mma_s8_16832(c1, pa, bb[2], bb[3]);
-        o[n][0] += (float)c0[0] * sW[0];
-        o[n][1] += (float)c0[1] * sW[0];
-        o[n][2] += (float)c0[2] * sW[1];
-        o[n][3] += (float)c0[3] * sW[1];
-        o[n + 1][0] += (float)c1[0] * sW[0];
-        o[n + 1][1] += (float)c1[1] * sW[0];
-        o[n + 1][2] += (float)c1[2] * sW[1];
-        o[n + 1][3] += (float)c1[3] * sW[1];
+        s8b_to_f16(bb[0], bb[1], f0);
+        s8b_to_f16(bb[2], bb[3], f1);
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16_16816(c0, pa1[0], pa1[1], pa1[2], pa1[3], f0[0], f0[1]);
+        mma_f16_16816(c0, pa2[0], pa2[1], pa2[2], pa2[3], f0[2], f0[3]);
+        mma_f16_16816(c1, pa1[0], pa1[1], pa1[2], pa1[3], f1[0], f1[1]);
+        mma_f16_16816(c1, pa2[0], pa2[1], pa2[2], pa2[3], f1[2], f1[3]);
+        o[n][0] += c0[0] * sW[0];
+        o[n][1] += c0[1] * sW[0];
+        o[n][2] += c0[2] * sW[1];
+        o[n][3] += c0[3] * sW[1];
+        o[n + 1][0] += c1[0] * sW[0];
+        o[n + 1][1] += c1[1] * sW[0];
+        o[n + 1][2] += c1[2] * sW[1];
+        o[n + 1][3] += c1[3] * sW[1];
       }
     }
     __syncthreads();  // stage buffer b is free

@@ -26,25 +26,30 @@ namespace {
 constexpr int kTileTokens = 16;
 constexpr int kMaxHkvProducer = 8;
 
+// x / s correctly rounded (the IEEE quotient), for one divisor s shared by many
+// x: Markstein's method.  With y = RN(1/s), q = RN(x * y) and the residual
+// r = x - s * q (exact in one FMA), RN(q + r * y) is the correctly rounded
+// quotient provided nothing overflows or underflows; divisors below 2^-100 use
+// the plain division instead.
+__device__ __forceinline__ float div_shared(float x, float s, float y, bool tiny) {
+  if (tiny) return __fdiv_rn(x, s);
+  const float q = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-s, q, x);
+  return __fmaf_rn(r, y, q);
+}
+
 // Quantize the vector whose 16-element slice this lane holds (lane c of a group
-// of LPV lanes holds elements 16c .. 16c+15).  Every lane of the warp must call
-// this (the absmax reduction shuffles across the whole warp).  Returns the
-// vector's scale; writes this lane's 16 codes to `codes`.
+// of LPV lanes holds elements 16c .. 16c+15, as raw bf16 words in `raw`).
+// Every lane of the warp must call this (the absmax reduction shuffles across
+// the whole warp).  Returns the vector's scale; writes this lane's 16 codes.
 template <int LPV>
-__device__ __forceinline__ float quantize_slice(const uint16_t* src, bool active, uint4& codes) {
+__device__ __forceinline__ float quantize_slice(const uint4 (&raw)[2], bool active, uint4& codes) {
   float x[16];
-  if (active) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
-    const uint4 b = __ldg(reinterpret_cast<const uint4*>(src + 8));
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const uint32_t w[8] = {raw[0].x, raw[0].y, raw[0].z, raw[0].w, raw[1].x, raw[1].y, raw[1].z, raw[1].w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      x[2 * i] = bf16_bits_to_float(w[i] & 0xffffu);
-      x[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = 0.f;
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = active ? bf16_bits_to_float(w[i] & 0xffffu) : 0.f;
+    x[2 * i + 1] = active ? bf16_bits_to_float(w[i] >> 16) : 0.f;
   }
   float amax = 0.f;
 #pragma unroll
@@ -52,12 +57,14 @@ __device__ __forceinline__ float quantize_slice(const uint16_t* src, bool active
 #pragma unroll
   for (int o = LPV / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float scale = __fdiv_rn(amax, 127.0f);
+  const float y = __frcp_rn(scale);
+  const bool tiny = scale < 7.8886091e-31f;  // 2^-100
   int q[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     int qi = 0;
     if (amax > 0.f) {
-      qi = __float2int_rn(__fdiv_rn(x[i], scale));
+      qi = __float2int_rn(div_shared(x[i], scale, y, tiny));
       qi = max(-127, min(127, qi));
     }
     q[i] = qi;
@@ -77,6 +84,8 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(ProducerParams p) {
   __shared__ __align__(16) int8_t vstage[kMaxHkvProducer][kTileTokens][D];
   __shared__ int s_slot[kTileTokens];
 
+  griddep_wait();
+  griddep_launch_dependents();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kTileTokens;
   const int ntok = min(kTileTokens, p.T - t0);
@@ -99,59 +108,70 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(ProducerParams p) {
   for (int i = 1; i < kTileTokens; ++i) aligned = aligned && (s_slot[i] == s_slot[0] + i);
 
   const int Hkv = p.Hkv, Hq = p.q ? p.Hq : 0;
-  const int nvec = kTileTokens * (2 * Hkv + Hq);
+  // Only the tile's real tokens: vector vi is (token vi / per_tok, entry vi % per_tok),
+  // entries 0..Hkv-1 = K heads, Hkv..2Hkv-1 = V heads, then the query heads.
+  const int per_tok = 2 * Hkv + Hq;
+  const int nvec = ntok * per_tok;
   const int gi = lane / LPV, c = lane % LPV;
-  for (int base = warp * VPW; base < nvec; base += 8 * VPW) {
-    const int vi = base + gi;
-    int kind = 0, tok = 0, h = 0;  // kind 0 = K, 1 = V, 2 = Q
-    if (vi < kTileTokens * Hkv) {
-      kind = 0;
-      tok = vi / Hkv;
-      h = vi % Hkv;
-    } else if (vi < 2 * kTileTokens * Hkv) {
-      kind = 1;
-      tok = (vi - kTileTokens * Hkv) / Hkv;
-      h = (vi - kTileTokens * Hkv) % Hkv;
-    } else {
-      kind = 2;
-      const int r = vi - 2 * kTileTokens * Hkv;
-      tok = r / (Hq > 0 ? Hq : 1);
-      h = r % (Hq > 0 ? Hq : 1);
-    }
-    bool active = vi < nvec && tok < ntok;
-    const int slot = active ? s_slot[tok] : -1;
-    if (kind != 2) active = active && slot >= 0;
-    const int t = t0 + tok;
-    const uint16_t* src = nullptr;
-    if (active) {
-      if (kind == 0) src = p.k + ((size_t)t * Hkv + h) * D;
-      else if (kind == 1) src = p.v + ((size_t)t * Hkv + h) * D;
-      else src = p.q + ((size_t)t * Hq + h) * D;
-      src += 16 * c;
-    }
-    uint4 codes;
-    const float scale = quantize_slice<LPV>(src, active, codes);
-    if (!active) continue;
-    if (kind == 2) {
-      *reinterpret_cast<uint4*>(p.q_i8 + ((size_t)t * Hq + h) * D + 16 * c) = codes;
-      if (c == 0) p.q_scale[(size_t)t * Hq + h] = scale;
-      continue;
-    }
-    const int blk = slot / BS, off = slot % BS;
-    const size_t sidx = ((size_t)blk * BS + off) * Hkv + h;
-    if (kind == 0) {
-      *reinterpret_cast<uint4*>(p.k_cache + ((((size_t)blk * Hkv + h) * (D / 16) + c) * BS + off) * 16) = codes;
-      if (c == 0) p.k_scale[sidx] = scale;
-    } else {
-      if (aligned) {
-        *reinterpret_cast<uint4*>(&vstage[h][tok][16 * c]) = codes;
-      } else {
-        int8_t* dst = p.v_cache + (((size_t)blk * Hkv + h) * D + 16 * c) * BS + off;
-        const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+  // U warp passes at a time: all their loads are issued before any is used, so
+  // several global-load latencies overlap instead of queuing one per pass.
+  constexpr int U = 4;
+  for (int base0 = warp * VPW; base0 < nvec; base0 += 8 * VPW * U) {
+    bool act[U];
+    int kinds[U], toks[U], hs[U], slots[U];
+    uint4 raw[U][2];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) dst[(size_t)i * BS] = (int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
+    for (int u = 0; u < U; ++u) {
+      const int vi = base0 + u * 8 * VPW + gi;
+      const int tok = vi / per_tok, r = vi % per_tok;
+      const int kind = r < Hkv ? 0 : (r < 2 * Hkv ? 1 : 2);  // 0 = K, 1 = V, 2 = Q
+      const int h = kind == 0 ? r : (kind == 1 ? r - Hkv : r - 2 * Hkv);
+      bool active = vi < nvec;
+      const int slot = active ? s_slot[tok] : -1;
+      if (kind != 2) active = active && slot >= 0;
+      act[u] = active;
+      kinds[u] = kind;
+      toks[u] = tok;
+      hs[u] = h;
+      slots[u] = slot;
+      raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
+      if (active) {
+        const int t = t0 + tok;
+        const uint16_t* src = (kind == 0 ? p.k + ((size_t)t * Hkv + h) * D
+                               : kind == 1 ? p.v + ((size_t)t * Hkv + h) * D
+                                           : p.q + ((size_t)t * Hq + h) * D) + 16 * c;
+        raw[u][0] = __ldg(reinterpret_cast<const uint4*>(src));
+        raw[u][1] = __ldg(reinterpret_cast<const uint4*>(src + 8));
       }
-      if (c == 0) p.v_scale[sidx] = scale;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      uint4 codes;
+      const float scale = quantize_slice<LPV>(raw[u], act[u], codes);
+      if (!act[u]) continue;
+      const int kind = kinds[u], tok = toks[u], h = hs[u], slot = slots[u];
+      const int t = t0 + tok;
+      if (kind == 2) {
+        *reinterpret_cast<uint4*>(p.q_i8 + ((size_t)t * Hq + h) * D + 16 * c) = codes;
+        if (c == 0) p.q_scale[(size_t)t * Hq + h] = scale;
+        continue;
+      }
+      const int blk = slot / BS, off = slot % BS;
+      const size_t sidx = ((size_t)blk * BS + off) * Hkv + h;
+      if (kind == 0) {
+        *reinterpret_cast<uint4*>(p.k_cache + ((((size_t)blk * Hkv + h) * (D / 16) + c) * BS + off) * 16) = codes;
+        if (c == 0) p.k_scale[sidx] = scale;
+      } else {
+        if (aligned) {
+          *reinterpret_cast<uint4*>(&vstage[h][tok][16 * c]) = codes;
+        } else {
+          int8_t* dst = p.v_cache + (((size_t)blk * Hkv + h) * D + 16 * c) * BS + off;
+          const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+          for (int i = 0; i < 16; ++i) dst[(size_t)i * BS] = (int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
+        }
+        if (c == 0) p.v_scale[sidx] = scale;
+      }
     }
   }
   if (aligned) {
@@ -213,9 +233,8 @@ I8KV_DEFINE_ERROR_ACCESSOR(read_error_producer)
 cudaError_t launch_kv_quant_write(const ProducerParams& p, cudaStream_t stream) {
   const int grid = (p.T + kTileTokens - 1) / kTileTokens;
   if (grid == 0) return cudaSuccess;
-  if (p.D == 256) kv_quant_write_kernel<256><<<grid, 256, 0, stream>>>(p);
-  else kv_quant_write_kernel<128><<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  if (p.D == 256) return launch_pdl(kv_quant_write_kernel<256>, dim3(grid), dim3(256), 0, stream, p);
+  return launch_pdl(kv_quant_write_kernel<128>, dim3(grid), dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_bf16_kv_write(const ProducerParams& p, uint16_t* k_cache, uint16_t* v_cache, cudaStream_t stream) {
