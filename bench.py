@@ -378,6 +378,11 @@ def run_ours(args):
             for L, v in by_len.items()}
         if not args.quick:
             secondary.update(run_secondary(torch, i8, hbm_peak))
+            try:
+                secondary["bf16_kv_decode_by_history"] = run_bf16_comparison(
+                    torch, i8, hbm_peak, {L: v * 1e3 for L, v in by_len.items()})
+            except Exception as e:  # pragma: no cover - report, do not hide
+                secondary["bf16_kv_decode_by_history"] = {"error": str(e)[:200]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -474,6 +479,38 @@ def time_graph(torch, fn, reps: int):
     b.record()
     torch.cuda.synchronize()
     return a.elapsed_time(b) / reps
+
+
+def time_rotating(torch, calls, reps: int):
+    """Average ms per call of `calls` (a list of closures over distinct caches whose
+    total size exceeds L2), replayed round-robin `reps` times in one graph."""
+    return time_graph(torch, lambda: [c() for c in calls], reps) / len(calls)
+
+
+def run_bf16_comparison(torch, i8, hbm_peak, int8_us: dict):
+    """BF16-KV decode over the same histories (the pages' BF16 control): µs, GB/s
+    at 4096 B per cached token, and the INT8 speedup over it."""
+    res = {}
+    for L in HISTORIES:
+        w = wl.decode_outlier(L)
+        k, v = w.kv(0)
+        base = i8.alloc_bf16_cache(w.num_blocks, w.Hkv, w.D)
+        i8.bf16_kv_write(to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.slots(0)), **base)
+        copies = max(2, int(np.ceil(400e6 / w.kv_bytes_bf16())))
+        caches = [{n: t.clone() for n, t in base.items()} for _ in range(copies)]
+        del base
+        q = to_dev(torch, w.q())
+        out = torch.empty((1, w.Hq, w.D), dtype=torch.float32, device="cuda")
+        ws = i8.decode_workspace(1, w.Hq, w.Hkv, w.D, w.block_tables.shape[1])
+        bt, sl = to_dev(torch, w.block_tables), to_dev(torch, w.seq_lens)
+        calls = [(lambda c=c: i8.bf16_paged_decode_attn(out, q, c["k_cache"], c["v_cache"], bt, sl, ws)) for c in caches]
+        ms = time_rotating(torch, calls, 20)
+        gbs = w.kv_bytes_bf16() / (ms / 1e3) / 1e9
+        res[str(L)] = {"us": ms * 1e3, "gb_s": gbs, "frac_hbm": gbs / hbm_peak,
+                       "int8_speedup": (ms * 1e3) / int8_us[L] if L in int8_us else None}
+        del caches
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_secondary(torch, i8, hbm_peak):

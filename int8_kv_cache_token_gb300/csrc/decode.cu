@@ -36,6 +36,8 @@
 //    <= 516,128), so the fp32 accumulator holds the exact int32 result.  On
 //    sm_103a this path has about 4x the throughput of mma.sync s8; the debug QK
 //    entry point checks the accumulators bit for bit against integer QK.
+#include <cuda_bf16.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -88,7 +90,7 @@ __device__ __forceinline__ int clamp_len(int L, int maxL) {
   return L > maxL ? maxL : L;
 }
 
-__device__ __forceinline__ void walk_next(Walk& w, const int32_t* seq_lens, int B, int Hkv, int maxL) {
+__device__ __forceinline__ void walk_next(Walk& w, const int32_t* seq_lens, int B, int Hkv, int maxL, int unit) {
   if (++w.part < w.np) return;
   w.part = 0;
   if (++w.kvh < Hkv) return;
@@ -97,7 +99,7 @@ __device__ __forceinline__ void walk_next(Walk& w, const int32_t* seq_lens, int 
   for (;;) {
     if (++w.b >= B) return;
     w.L = clamp_len(seq_lens[w.b], maxL);
-    w.np = (w.L + kPart - 1) / kPart;
+    w.np = (w.L + unit - 1) / unit;
     if (w.np > 0) return;
   }
 }
@@ -146,26 +148,75 @@ template <int D>
 __device__ __forceinline__ void qk_warp(const int8_t* kpages, int warp, int lane, const uint32_t (&qf)[D / 32][4],
                                         float (&acc)[2][4]) {
   const int mi = lane >> 3, ri = lane & 7;
+  // Even and odd 32-dim steps accumulate separately (two independent MMA chains
+  // per block instead of one); the two partial sums are exact integers, so
+  // adding them at the end changes nothing.
+  float acc2[2][4];
 #pragma unroll
-  for (int m = 0; m < 2; ++m) {
+  for (int m = 0; m < 2; ++m)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
-    const int8_t* row =
-        kpages + (size_t)(2 * warp + m) * (D * kBS) + (mi >> 1) * (kBS * 16) + (ri + 8 * (mi & 1)) * 16;
+    for (int i = 0; i < 4; ++i) acc[m][i] = acc2[m][i] = 0.f;
 #pragma unroll
-    for (int s = 0; s < D / 32; ++s) {
+  for (int s = 0; s < D / 32; ++s) {
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const int8_t* row =
+          kpages + (size_t)(2 * warp + m) * (D * kBS) + (mi >> 1) * (kBS * 16) + (ri + 8 * (mi & 1)) * 16;
       uint32_t a[4];
       ldmatrix_x4(a, row + (size_t)(2 * s) * (kBS * 16));
-      mma_s8a_f16b(acc[m], a, qf[s]);
+      mma_s8a_f16b((s & 1) ? acc2[m] : acc[m], a, qf[s]);
     }
+  }
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[m][i] += acc2[m][i];
+}
+
+// BF16-KV comparison path: query fragments (B operand of QK) straight from the
+// bf16 query, qf[s] = dims 16s + {2t, 2t+1} and 16s + 8 + {2t, 2t+1} of row g.
+template <int D>
+__device__ __forceinline__ void load_q_frags_bf16(const uint16_t* q, int b, int Hq, int kvh, int G, int lane,
+                                                  uint32_t (&qf)[D / 16][2]) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint16_t* row = q + ((size_t)b * Hq + kvh * G + g) * D;
+#pragma unroll
+  for (int s = 0; s < D / 16; ++s) {
+    qf[s][0] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(row + 16 * s + 2 * t)) : 0u;
+    qf[s][1] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(row + 16 * s + 8 + 2 * t)) : 0u;
   }
 }
 
+// BF16-KV QK for warp w's 16-token block: acc = (token g | g+8) x (row 2t, 2t+1).
+// kpages holds 8 bf16 K pages [D/8][16 tokens][8 dims].
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p, int nslots) {
+__device__ __forceinline__ void qk_warp_bf16(const uint8_t* kpages, int warp, int lane,
+                                             const uint32_t (&qf)[D / 16][2], float (&acc)[4]) {
+  const int mi = lane >> 3, ri = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+  const uint8_t* row = kpages + (size_t)warp * (D * kBS * 2) + (mi >> 1) * (kBS * 16) + (ri + 8 * (mi & 1)) * 16;
+#pragma unroll
+  for (int s = 0; s < D / 16; ++s) {
+    uint32_t a[4];
+    ldmatrix_x4(a, row + (size_t)(2 * s) * (kBS * 16));
+    mma_bf16_16816(acc, a, qf[s][0], qf[s][1]);
+  }
+}
+
+// One kernel body for both caches.  BF16 = false: the INT8 method.  BF16 = true:
+// the BF16-KV comparison (plain softmax, bf16 P x V, no scales), with 128-token
+// units so that a ring item (8 bf16 pages) has the same 64 KB at D = 256.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int nslots) {
   constexpr int NDT = D / 16;  // PV head-dim tiles (every warp covers all of D for its group)
-  constexpr int kPage = D * kBS;
-  constexpr int kItem = kPart * D;
+  constexpr int EB = BF16 ? 2 : 1;              // bytes per cache element
+  constexpr int kUnit = BF16 ? 128 : kPart;     // tokens per work unit
+  constexpr int kBlocksU = kUnit / kBS;         // pages per ring item
+  constexpr int kWTok = kUnit / kCWarps;        // tokens per warp per unit (32 = one probability group)
+  constexpr int MT = kWTok / 16;                // 16-token blocks per warp per unit
+  constexpr int kPage = D * kBS * EB;
+  constexpr int kItem = kBlocksU * kPage;
   constexpr int kRS = D + 4;                   // row stride of a warp state (conflict-free stores)
   constexpr int kWS = kRows * kRS + 2 * kRows;  // one warp state in the merge buffer
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -183,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
   const int N = gridDim.x, c = blockIdx.x;
   const int maxL = p.max_blocks * kBS;
 
-  if (tid == 0) {
+  if (warp == kCWarps && lane == 0) {
     for (int s = 0; s < nslots; ++s) {
       mbar_init(&full[s], 32);
       mbar_init(&empty[s], kCWarps);
@@ -195,25 +246,46 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
   griddep_wait();
   griddep_launch_dependents();
 
-  // ---- work split: every CTA scans seq_lens (warp 0) ----
-  if (warp == 0) {
+  // ---- work split, by the producer warp (the consumers wait at the barrier
+  // below; they have nothing to do before it) ----
+  // One sequence in the batch (the long-context decode case): guess the first
+  // unit from max_blocks and load its block-table row together with seq_lens,
+  // so the two dependent loads overlap; the guess is checked below.
+  int spec_part = -1, spec_blk = -1;
+  if (warp == kCWarps && B == 1) {
+    const int np_g = (maxL + kUnit - 1) / kUnit;
+    const long long U_g = (long long)np_g * Hkv;
+    const int Nw_g = (int)(U_g < N ? U_g : N);
+    if (c < Nw_g) {
+      spec_part = (int)((U_g * c / Nw_g) % np_g);
+      if (lane < kBlocksU && spec_part * kBlocksU + lane < p.max_blocks)
+        spec_blk = __ldg(p.block_tables + spec_part * kBlocksU + lane);
+    }
+  }
+  if (warp == kCWarps) {
+    constexpr int kKeep = 8;  // chunks of 32 sequences whose unit counts stay in registers
+    int ukeep[kKeep];
     long long total = 0;
-    for (int b0 = 0; b0 < B; b0 += 32) {
+    for (int b0 = 0, ck = 0; b0 < B; b0 += 32, ++ck) {
       const int b = b0 + lane;
       int u = 0;
       if (b < B) {
         const int raw = p.seq_lens[b];
         if (raw > maxL) record_error(2);
         const int L = clamp_len(raw, maxL);
-        u = (L + kPart - 1) / kPart * Hkv;
+        u = (L + kUnit - 1) / kUnit * Hkv;
         if (L == 0 && b % N == c) {  // empty sequence: zero rows, nothing to merge
           float* o = p.out + (size_t)b * Hq * D;
           for (int i = 0; i < Hq * D; ++i) o[i] = 0.f;
           for (int h = 0; h < Hkv; ++h) p.ws_info[b * Hkv + h] = -1;
         }
       }
-      for (int o = 16; o >= 1; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
-      total += u;
+#pragma unroll
+      for (int k = 0; k < kKeep; ++k)
+        if (k == ck) ukeep[k] = u;
+      int su = u;
+      for (int o = 16; o >= 1; o >>= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
+      total += su;
     }
     const long long U = total;
     // Only the first min(N, U) CTAs take units, so every working CTA has at
@@ -224,13 +296,21 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
       ctrl[0] = (int)(ue - ub);
       ctrl[8] = 0;
       ctrl[10] = Nw;
+      ctrl[6] = (int)(U & 0x7fffffff);
+      ctrl[7] = (int)(U >> 31);
     }
     if (ue > ub) {
       long long run = 0;
-      for (int b0 = 0; b0 < B; b0 += 32) {
+      for (int b0 = 0, ck = 0; b0 < B; b0 += 32, ++ck) {
         const int b = b0 + lane;
         int u = 0;
-        if (b < B) u = (clamp_len(p.seq_lens[b], maxL) + kPart - 1) / kPart * Hkv;
+        if (ck < kKeep) {
+#pragma unroll
+          for (int k = 0; k < kKeep; ++k)
+            if (k == ck) u = ukeep[k];
+        } else if (b < B) {
+          u = (clamp_len(p.seq_lens[b], maxL) + kUnit - 1) / kUnit * Hkv;
+        }
         int incl = u;
         for (int o = 1; o < 32; o <<= 1) {
           const int y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -240,8 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
         const unsigned hit = __ballot_sync(0xffffffffu, u > 0 && ex <= ub && ub < in);
         if (hit) {
           if (lane == __ffs(hit) - 1) {
-            const int L = clamp_len(p.seq_lens[b], maxL);
-            const int np = (L + kPart - 1) / kPart;
+            const int np = u / Hkv;
             const long long local = ub - ex;
             ctrl[1] = b;
             ctrl[2] = (int)(local / np);
@@ -253,13 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
         }
         run += __shfl_sync(0xffffffffu, incl, 31);
       }
-      if (lane == 0) {
-        ctrl[6] = (int)(U & 0x7fffffff);
-        ctrl[7] = (int)(U >> 31);
-      }
     }
   }
-  __syncthreads();
+  __syncthreads();  // the split in ctrl[] is visible to every warp
   const int n_units = ctrl[0];
   if (n_units <= 0) return;
   Walk w0;
@@ -268,28 +343,30 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
   w0.part = ctrl[3];
   w0.ub = (long long)ctrl[4] | ((long long)ctrl[5] << 31);
   w0.L = clamp_len(p.seq_lens[w0.b], maxL);
-  w0.np = (w0.L + kPart - 1) / kPart;
+  w0.np = (w0.L + kUnit - 1) / kUnit;
   const long long U = (long long)ctrl[6] | ((long long)ctrl[7] << 31);
   const int Nw = ctrl[10];
 
   if (warp == kCWarps) {
     // ================= producer warp =================
-    const int8_t* kc = static_cast<const int8_t*>(p.k_cache);
-    const int8_t* vc = static_cast<const int8_t*>(p.v_cache);
+    const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
+    const uint8_t* vc = static_cast<const uint8_t*>(p.v_cache);
     const uint64_t pol = policy_evict_first();
     Walk wk = w0;
     for (int i = 0; i < n_units; ++i) {
-      const int t0 = wk.part * kPart;
-      const int nblk = min(kPart / kBS, (wk.L - t0 + kBS - 1) / kBS);
+      const int t0 = wk.part * kUnit;
+      const int nblk = min(kBlocksU, (wk.L - t0 + kBS - 1) / kBS);
       int blk = -1;
       if (lane < nblk) {
-        blk = p.block_tables[(size_t)wk.b * p.max_blocks + wk.part * (kPart / kBS) + lane];
+        blk = (i == 0 && B == 1 && wk.part == spec_part)
+                  ? spec_blk
+                  : p.block_tables[(size_t)wk.b * p.max_blocks + wk.part * kBlocksU + lane];
         if (blk < 0 || blk >= p.num_blocks) {
           record_error(2);
           blk = -1;
         }
       }
-      const bool ok = lane < 16 && blk >= 0;
+      const bool ok = lane < kBlocksU && blk >= 0;
       const uint32_t n_pages = __popc(__ballot_sync(0xffffffffu, ok));
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv) {
@@ -302,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
                         (kv == 0 ? kc : vc) + ((size_t)blk * Hkv + wk.kvh) * kPage, kPage, &full[slot], pol);
         mbar_arrive(&full[slot]);
       }
-      walk_next(wk, p.seq_lens, B, Hkv, maxL);
+      walk_next(wk, p.seq_lens, B, Hkv, maxL, kUnit);
     }
     return;
   }
@@ -313,7 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
   int8_t* wqw = wqs + warp * (kRows * kGroup);
   Walk wk = w0;
   int cur_pair = -1;
-  uint32_t qf[D / 32][4];
+  uint32_t qf[D / 32][4];    // INT8: converted query fragments
+  uint32_t qfb[D / 16][2];   // BF16: query fragments
   float sq[2] = {0.f, 0.f};
   float o[NDT][4];
   float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
@@ -322,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
   auto load_scales = [&](const Walk& u, float (&k4)[4], float (&v4)[4]) {
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
-      const int lb = u.part * (kPart / kBS) + 2 * warp + m;  // logical block in the sequence
+      const int lb = u.part * kBlocksU + 2 * warp + m;  // logical block in the sequence
       const int tok0 = lb * kBS;
       int blk = -1;
       if (tok0 < u.L) {
@@ -339,16 +417,20 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
       }
     }
   };
-  load_scales(wk, sk, sv);
+  if constexpr (!BF16) load_scales(wk, sk, sv);
   for (int i = 0; i < n_units; ++i) {
     const int pair = wk.b * Hkv + wk.kvh;
     if (pair != cur_pair) {
       cur_pair = pair;
-      load_q_frags<D>(static_cast<const int8_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qf);
+      if constexpr (BF16) {
+        load_q_frags_bf16<D>(static_cast<const uint16_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qfb);
+      } else {
+        load_q_frags<D>(static_cast<const int8_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qf);
+      }
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int row = 2 * t + r;
-        sq[r] = row < G ? p.q_scale[(size_t)wk.b * Hq + wk.kvh * G + row] : 0.f;
+        if constexpr (!BF16) sq[r] = row < G ? p.q_scale[(size_t)wk.b * Hq + wk.kvh * G + row] : 0.f;
         mrun[r] = -INFINITY;
         lrun[r] = 0.f;
       }
@@ -358,18 +440,22 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
         for (int e = 0; e < 4; ++e) o[dt][e] = 0.f;
     }
     Walk nx = wk;
-    walk_next(nx, p.seq_lens, B, Hkv, maxL);
-    if (i + 1 < n_units) load_scales(nx, sk_n, sv_n);  // the next unit's scales, in flight meanwhile
-    const int t0 = wk.part * kPart;
-    const int ntok = min(kPart, wk.L - t0);
-    const bool active = warp * kGroup < ntok;
+    walk_next(nx, p.seq_lens, B, Hkv, maxL, kUnit);
+    if constexpr (!BF16)
+      if (i + 1 < n_units) load_scales(nx, sk_n, sv_n);  // the next unit's scales, in flight meanwhile
+    const int t0 = wk.part * kUnit;
+    const int ntok = min(kUnit, wk.L - t0);
+    const bool active = warp * kWTok < ntok;
 
     // ---- K item: QK for this warp's group ----
     const int kitem = 2 * i, kslot = kitem % nslots;
     pipe_wait(&full[kslot], (kitem / nslots) & 1, abort_flag);
     float acc[2][4];
     if (active) {
-      qk_warp<D>(ring + (size_t)kslot * kItem, warp, lane, qf, acc);
+      if constexpr (BF16)
+        qk_warp_bf16<D>(reinterpret_cast<const uint8_t*>(ring) + (size_t)kslot * kItem, warp, lane, qfb, acc[0]);
+      else
+        qk_warp<D>(ring + (size_t)kslot * kItem, warp, lane, qf, acc);
     } else {
 #pragma unroll
       for (int m = 0; m < 2; ++m)
@@ -385,12 +471,17 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
       float s[2][4];
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int m = 0; m < 2; ++m)
+      for (int m = 0; m < MT; ++m)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int tok = warp * kGroup + 16 * m + g + 8 * (e >> 1);
+          const int tok = warp * kWTok + 16 * m + g + 8 * (e >> 1);
           float sc = -INFINITY;
-          if (tok < ntok) sc = __fmul_rn(__fmul_rn(__fmul_rn(acc[m][e], sq[e & 1]), sk[2 * m + (e >> 1)]), c_scale);
+          if (tok < ntok) {
+            if constexpr (BF16)
+              sc = __fmul_rn(acc[m][e], c_scale);
+            else
+              sc = __fmul_rn(__fmul_rn(__fmul_rn(acc[m][e], sq[e & 1]), sk[2 * m + (e >> 1)]), c_scale);
+          }
           s[m][e] = sc;
           mx[e & 1] = fmaxf(mx[e & 1], sc);
         }
@@ -405,39 +496,55 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
         mrun[r] = mn;
         lrun[r] *= alpha[r];
       }
-      float A[2] = {0.f, 0.f}, w[2][4];
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
+      if constexpr (BF16) {
+        // plain softmax weights p~ in bf16 -> this warp's [row][16 tokens] staging
+        uint16_t* pw = reinterpret_cast<uint16_t*>(wqw);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float pe = (s[m][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[m][e], mrun[e & 1]));
+          const float pe = (s[0][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[0][e], mrun[e & 1]));
           lrun[e & 1] += pe;
-          w[m][e] = __fmul_rn(pe, sv[2 * m + (e >> 1)]);
-          A[e & 1] = fmaxf(A[e & 1], w[m][e]);
+          pw[(2 * t + (e & 1)) * 16 + g + 8 * (e >> 1)] = __bfloat16_as_ushort(__float2bfloat16_rn(pe));
         }
+      } else {
+        float A[2] = {0.f, 0.f}, w[2][4];
 #pragma unroll
-      for (int r = 0; r < 2; ++r)
+        for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int off = 4; off <= 16; off <<= 1) A[r] = fmaxf(A[r], __shfl_xor_sync(0xffffffffu, A[r], off));
-      float inv[2];
+          for (int e = 0; e < 4; ++e) {
+            const float pe = (s[m][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[m][e], mrun[e & 1]));
+            lrun[e & 1] += pe;
+            w[m][e] = __fmul_rn(pe, sv[2 * m + (e >> 1)]);
+            A[e & 1] = fmaxf(A[e & 1], w[m][e]);
+          }
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        sw[r] = __fdiv_rn(A[r], 127.0f);
-        inv[r] = A[r] > 0.f ? __fdiv_rn(127.0f, A[r]) : 0.f;
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int off = 4; off <= 16; off <<= 1) A[r] = fmaxf(A[r], __shfl_xor_sync(0xffffffffu, A[r], off));
+        float inv[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          sw[r] = __fdiv_rn(A[r], 127.0f);
+          inv[r] = A[r] > 0.f ? __fdiv_rn(127.0f, A[r]) : 0.f;
+        }
+        // codes -> this warp's [row][token] bytes, read back below as PV B fragments
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int q = min(127, __float2int_rn(w[m][e] * inv[e & 1]));
+            wqw[(2 * t + (e & 1)) * kGroup + 16 * m + g + 8 * (e >> 1)] = (int8_t)q;
+          }
       }
-      // codes -> this warp's [row][token] bytes, read back below as PV B fragments
-#pragma unroll
-      for (int m = 0; m < 2; ++m)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int q = min(127, __float2int_rn(w[m][e] * inv[e & 1]));
-          wqw[(2 * t + (e & 1)) * kGroup + 16 * m + g + 8 * (e >> 1)] = (int8_t)q;
-        }
     }
     __syncwarp();
     uint32_t bq[4];
-    s8b_to_f16(*reinterpret_cast<const uint32_t*>(wqw + g * kGroup + 4 * t),
-               *reinterpret_cast<const uint32_t*>(wqw + g * kGroup + 16 + 4 * t), bq);
+    if constexpr (BF16) {
+      bq[0] = *reinterpret_cast<const uint32_t*>(wqw + g * 32 + 4 * t);
+      bq[1] = *reinterpret_cast<const uint32_t*>(wqw + g * 32 + 16 + 4 * t);
+    } else {
+      s8b_to_f16(*reinterpret_cast<const uint32_t*>(wqw + g * kGroup + 4 * t),
+                 *reinterpret_cast<const uint32_t*>(wqw + g * kGroup + 16 + 4 * t), bq);
+    }
     if (alpha[0] != 1.f || alpha[1] != 1.f) {
 #pragma unroll
       for (int dt = 0; dt < NDT; ++dt) {
@@ -453,18 +560,30 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
     pipe_wait(&full[vslot], (vitem / nslots) & 1, abort_flag);
     if (active) {
       const int mi = lane >> 3, ri = lane & 7;
-      const int8_t* vrow =
-          ring + (size_t)vslot * kItem + (size_t)(2 * warp + (mi >> 1)) * kPage + (ri + 8 * (mi & 1)) * 16;
+      if constexpr (BF16) {
+        // A = V^T from the warp's bf16 page [D][16 tokens]: matrices (dims 0-7 | 8-15) x (tokens 0-7 | 8-15)
+        const uint8_t* vrow = reinterpret_cast<const uint8_t*>(ring) + (size_t)vslot * kItem + (size_t)warp * kPage +
+                              (ri + 8 * (mi & 1)) * 32 + (mi >> 1) * 16;
 #pragma unroll
-      for (int dt = 0; dt < NDT; ++dt) {
-        uint32_t a[4];
-        ldmatrix_x4(a, vrow + dt * 16 * 16);
-        float pv[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_s8a_f16b(pv, a, bq);
-        o[dt][0] = fmaf(pv[0], sw[0], o[dt][0]);
-        o[dt][1] = fmaf(pv[1], sw[1], o[dt][1]);
-        o[dt][2] = fmaf(pv[2], sw[0], o[dt][2]);
-        o[dt][3] = fmaf(pv[3], sw[1], o[dt][3]);
+        for (int dt = 0; dt < NDT; ++dt) {
+          uint32_t a[4];
+          ldmatrix_x4(a, vrow + dt * 16 * 32);
+          mma_bf16_16816(o[dt], a, bq[0], bq[1]);
+        }
+      } else {
+        const int8_t* vrow =
+            ring + (size_t)vslot * kItem + (size_t)(2 * warp + (mi >> 1)) * kPage + (ri + 8 * (mi & 1)) * 16;
+#pragma unroll
+        for (int dt = 0; dt < NDT; ++dt) {
+          uint32_t a[4];
+          ldmatrix_x4(a, vrow + dt * 16 * 16);
+          float pv[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_s8a_f16b(pv, a, bq);
+          o[dt][0] = fmaf(pv[0], sw[0], o[dt][0]);
+          o[dt][1] = fmaf(pv[1], sw[1], o[dt][1]);
+          o[dt][2] = fmaf(pv[2], sw[0], o[dt][2]);
+          o[dt][3] = fmaf(pv[3], sw[1], o[dt][3]);
+        }
       }
     }
     __syncwarp();
@@ -500,67 +619,76 @@ __global__ void __launch_bounds__(kThreads, 1) int8_decode_kernel(DecodeParams p
           o[dt][2 + r] *= f;
         }
       }
+      // Two rounds (warps 0-3, then 4-7) through 4 shared buffers; each thread
+      // then owns one row and D/32 head-dims of the CTA's state and adds the
+      // 8 warps' values in warp order (deterministic).
+      constexpr int DPT = D / 32;
+      const int orow = tid >> 5;  // 0..7
+      float Mrow = -INFINITY;  // read before the rounds' barriers, so a later segment cannot overwrite it first
 #pragma unroll
-      for (int half = 4; half >= 1; half >>= 1) {
-        if (warp >= half && warp < 2 * half) {
-          float* buf = mbuf + (size_t)(warp - half) * kWS;
+      for (int w2 = 0; w2 < kCWarps; ++w2) Mrow = fmaxf(Mrow, mw[w2 * kRows + orow]);
+      float acc_o[DPT];
+      float acc_l = 0.f;
+#pragma unroll
+      for (int k = 0; k < DPT; ++k) acc_o[k] = 0.f;
+#pragma unroll
+      for (int round = 0; round < 2; ++round) {
+        if ((warp >> 2) == round) {
+          float* buf = mbuf + (size_t)(warp & 3) * kWS;
 #pragma unroll
           for (int dt = 0; dt < NDT; ++dt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) buf[(2 * t + (e & 1)) * kRS + dt * 16 + g + 8 * (e >> 1)] = o[dt][e];
+            for (int e = 0; e < 4; ++e)
+              if (2 * t + (e & 1) < G) buf[(2 * t + (e & 1)) * kRS + dt * 16 + g + 8 * (e >> 1)] = o[dt][e];
           if (g == 0) {
             buf[kRows * kRS + 2 * t] = lrun[0];
             buf[kRows * kRS + 2 * t + 1] = lrun[1];
           }
         }
         named_bar_sync(1, kCWarps * 32);
-        if (warp < half) {
-          const float* buf = mbuf + (size_t)warp * kWS;
+        if (orow < G) {
 #pragma unroll
-          for (int dt = 0; dt < NDT; ++dt)
+          for (int wb = 0; wb < 4; ++wb) {
+            const float* buf = mbuf + (size_t)wb * kWS;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[dt][e] += buf[(2 * t + (e & 1)) * kRS + dt * 16 + g + 8 * (e >> 1)];
-          lrun[0] += buf[kRows * kRS + 2 * t];
-          lrun[1] += buf[kRows * kRS + 2 * t + 1];
+            for (int k = 0; k < DPT; ++k) acc_o[k] += buf[orow * kRS + lane + 32 * k];
+            acc_l += buf[kRows * kRS + orow];
+          }
         }
         named_bar_sync(1, kCWarps * 32);
       }
-      // warp 0 now holds this CTA's (M, L, O) for the pair
+      (void)M;
       const long long Up = wk.ub + (long long)wk.kvh * wk.np;
       const int cf = cta_of(Up, U, Nw), cl = cta_of(Up + wk.np - 1, U, Nw);
       // the CTA holding the pair's first unit records whether a merge is needed
       if (c == cf && tid == 0) p.ws_info[pair] = (cf == cl) ? -1 : ((cf << 16) | cl);
       if (cf == cl) {
-        if (warp == 0) {
+        if (orow < G) {
+          float* dst = p.out + ((size_t)wk.b * Hq + wk.kvh * G + orow) * D;
+          const float inv = 1.0f / acc_l;
 #pragma unroll
-          for (int dt = 0; dt < NDT; ++dt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int row = 2 * t + (e & 1);
-              const int d = dt * 16 + g + 8 * (e >> 1);
-              if (row < G) p.out[((size_t)wk.b * Hq + wk.kvh * G + row) * D + d] = o[dt][e] / lrun[e & 1];
-            }
+          for (int k = 0; k < DPT; ++k) dst[lane + 32 * k] = acc_o[k] * inv;
         }
-      } else if (warp == 0) {
+      } else {
         // one partial per CTA; decode_merge_kernel combines them after this kernel
         float* part = p.ws_part + (size_t)(pair + c) * kSlotFloats(D);
+        if (orow < G) {
 #pragma unroll
-        for (int dt = 0; dt < NDT; ++dt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) part[(2 * t + (e & 1)) * D + dt * 16 + g + 8 * (e >> 1)] = o[dt][e];
-        if (g == 0) {
-          part[kRows * D + 2 * t] = M[0];
-          part[kRows * D + 2 * t + 1] = M[1];
-          part[kRows * D + kRows + 2 * t] = lrun[0];
-          part[kRows * D + kRows + 2 * t + 1] = lrun[1];
+          for (int k = 0; k < DPT; ++k) part[orow * D + lane + 32 * k] = acc_o[k];
+        }
+        if (lane == 0) {
+          part[kRows * D + orow] = Mrow;
+          part[kRows * D + kRows + orow] = acc_l;
         }
       }
     }
     wk = nx;
+    if constexpr (!BF16) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      sk[k] = sk_n[k];
-      sv[k] = sv_n[k];
+      for (int k = 0; k < 4; ++k) {
+        sk[k] = sk_n[k];
+        sv[k] = sv_n[k];
+      }
     }
   }
 }
@@ -714,7 +842,7 @@ int pick_slots(int D, int smem_limit) {
   return 0;
 }
 
-template <int D>
+template <int D, bool BF16>
 cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -725,12 +853,12 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   // maximum), so that launches captured into a CUDA graph make no attribute call.
   static int attr_set[64] = {0};
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(int8_decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          max_smem_optin(dev));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
-  cudaError_t e = launch_pdl(int8_decode_kernel<D>, dim3(p.grid), dim3(kThreads), smem, stream, p, ns);
+  cudaError_t e = launch_pdl(decode_kernel<D, BF16>, dim3(p.grid), dim3(kThreads), smem, stream, p, ns);
   if (e != cudaSuccess) return e;
   return launch_pdl(decode_merge_kernel<D>, dim3(p.B * p.Hkv * p.G), dim3(256), 0, stream, p);
 }
@@ -753,8 +881,13 @@ size_t decode_workspace_bytes(int B, int Hkv, int D, int grid) {
 }
 
 cudaError_t launch_int8_decode(const DecodeParams& p, cudaStream_t stream) {
-  if (p.D == 256) return launch_decode_d<256>(p, stream);
-  return launch_decode_d<128>(p, stream);
+  if (p.D == 256) return launch_decode_d<256, false>(p, stream);
+  return launch_decode_d<128, false>(p, stream);
+}
+
+cudaError_t launch_bf16_decode(const DecodeParams& p, cudaStream_t stream) {
+  if (p.D == 256) return launch_decode_d<256, true>(p, stream);
+  return launch_decode_d<128, true>(p, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -375,6 +375,5 @@ cudaError_t launch_int8_prefix(const PrefixParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_bf16_decode(const DecodeParams&, cudaStream_t) { return cudaErrorNotSupported; }
 
 }  // namespace i8kv

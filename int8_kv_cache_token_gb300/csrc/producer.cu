@@ -59,20 +59,22 @@ __device__ __forceinline__ float quantize_slice(const uint4 (&raw)[2], bool acti
   const float scale = __fdiv_rn(amax, 127.0f);
   const float y = __frcp_rn(scale);
   const bool tiny = scale < 7.8886091e-31f;  // 2^-100
-  int q[16];
+  // Codes: round half to even by adding 1.5 * 2^23 (the fp32 sum keeps the
+  // integer part of x / scale in its low mantissa bits, so its low byte is the
+  // two's-complement code).  |x / scale| <= amax / RN(amax / 127) < 127.5, so no
+  // code ever needs clamping to [-127, 127].
+  uint32_t q[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    int qi = 0;
-    if (amax > 0.f) {
-      qi = __float2int_rn(div_shared(x[i], scale, y, tiny));
-      qi = max(-127, min(127, qi));
-    }
-    q[i] = qi;
+    const float qf = (amax > 0.f) ? div_shared(x[i], scale, y, tiny) : 0.f;
+    q[i] = __float_as_uint(__fadd_rn(qf, 12582912.0f));
   }
-  codes.x = pack_s8x4(q[0], q[1], q[2], q[3]);
-  codes.y = pack_s8x4(q[4], q[5], q[6], q[7]);
-  codes.z = pack_s8x4(q[8], q[9], q[10], q[11]);
-  codes.w = pack_s8x4(q[12], q[13], q[14], q[15]);
+  uint32_t pk[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    pk[j] = __byte_perm(__byte_perm(q[4 * j], q[4 * j + 1], 0x0040), __byte_perm(q[4 * j + 2], q[4 * j + 3], 0x0040),
+                        0x5410);
+  codes = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   return amax > 0.f ? scale : 0.f;
 }
 
@@ -113,9 +115,9 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(ProducerParams p) {
   const int per_tok = 2 * Hkv + Hq;
   const int nvec = ntok * per_tok;
   const int gi = lane / LPV, c = lane % LPV;
-  // U warp passes at a time: all their loads are issued before any is used, so
-  // several global-load latencies overlap instead of queuing one per pass.
-  constexpr int U = 4;
+  // U warp passes at a time: their loads are issued before either is used, so
+  // two global-load latencies overlap instead of queuing one per pass.
+  constexpr int U = 2;
   for (int base0 = warp * VPW; base0 < nvec; base0 += 8 * VPW * U) {
     bool act[U];
     int kinds[U], toks[U], hs[U], slots[U];
