@@ -142,6 +142,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(mhz), "window": window}
 
 
+def max_over_ranks(torch, dist, ms: float, device) -> float:
+    """The slowest rank's time: the whole job ends when it does."""
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(world: int, steps: int, bytes_per_step: int, ms: float) -> float:
+    """Replicas (weak scaling): every rank streams bytes_per_step per step."""
+    return world * steps * bytes_per_step / (ms / 1e3) / 1e9
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -338,12 +350,10 @@ def run_ours(args):
         sampler.stop()
     ms = t_start.elapsed_time(t_end)
     if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(torch, dist, ms, "cuda")
     err = i8.device_error()
     assert err == 0, f"kernel error {err} in the timed region"
-    value = world * args.steps * bytes_per_step / (ms / 1e3) / 1e9
+    value = whole_job_gbs(world, args.steps, bytes_per_step, ms)
 
     # ---- the dominant kernel alone: the same K x 48 decode calls back to back ----
     # (one graph, events around it; a decode call is the attention kernel plus
@@ -436,12 +446,18 @@ def run_e2e(args, torch, i8, layers, ws, bytes_per_step, world):
     g.replay()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
     a.record()
     g.replay()
     b.record()
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
-    return {"value": world * args.steps * bytes_per_step / (ms / 1e3) / 1e9, "unit": "GB/s",
+    if world > 1:
+        ms = max_over_ranks(torch, dist, ms, "cuda")
+    return {"value": whole_job_gbs(world, args.steps, bytes_per_step, ms), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps}
 
 
@@ -554,31 +570,37 @@ def run_secondary(torch, i8, hbm_peak):
 
 
 def run_profile(args):
-    """Decode launches only, for profilers: `--layers` copies of the 32768-token
-    history (each its own cache, 68 MB, so the set exceeds L2), launched round-robin
-    eagerly: `--warmup` then `--steps` launches."""
+    """Decode launches only, for profilers: `--layers` copies of each history (each
+    its own cache; the set exceeds L2), launched eagerly in the order 8192, 16384,
+    32768, 8192, ...: `--warmup` then `--steps` launches."""
     import torch
 
     from int8_kv_cache_token_gb300 import build as ibuild
     ibuild.build()
     import int8_kv_cache_token_gb300 as i8
-    L = HISTORIES[-1]
-    w = wl.decode_outlier(L)
-    k, v = w.kv(0)
-    base = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
-    i8.kv_quant_write(to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.slots(0)), **base)
-    k_new, v_new, q_new = to_dev(torch, k[L - 1:L]), to_dev(torch, v[L - 1:L]), to_dev(torch, w.q())
-    layers = [DecodeLayer(i8, torch, base, w, k_new, v_new, q_new) for _ in range(args.layers)]
-    for ly in layers:
-        ly.produce(i8)
-    ws = i8.decode_workspace(1, 24, 4, 256, w.block_tables.shape[1])
+    rounds = []
+    ws = {}
+    for L in HISTORIES:
+        w = wl.decode_outlier(L)
+        k, v = w.kv(0)
+        base = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+        i8.kv_quant_write(to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.slots(0)), **base)
+        k_new, v_new, q_new = to_dev(torch, k[L - 1:L]), to_dev(torch, v[L - 1:L]), to_dev(torch, w.q())
+        rounds.append([DecodeLayer(i8, torch, base, w, k_new, v_new, q_new) for _ in range(args.layers)])
+        ws[L] = i8.decode_workspace(1, 24, 4, 256, w.block_tables.shape[1])
+        del base
+    for grp in rounds:
+        for ly in grp:
+            ly.produce(i8)
     torch.cuda.synchronize()
-    for i in range(args.warmup + args.steps):
-        layers[i % len(layers)].decode(i8, ws)
+    order = [rounds[j % len(HISTORIES)][(j // len(HISTORIES)) % args.layers]
+             for j in range(args.warmup + args.steps)]
+    for ly in order:
+        ly.decode(i8, ws[int(ly.w.seq_lens[0])])
     torch.cuda.synchronize()
     assert i8.device_error() == 0
-    print(json.dumps({"profile": "int8_decode", "history": L, "launches": args.warmup + args.steps,
-                      "bytes_per_launch": w.kv_bytes_int8()}))
+    print(json.dumps({"profile": "int8_decode", "histories": list(HISTORIES), "launches": len(order),
+                      "bytes_per_launch": {str(L): wl.decode_outlier(L).kv_bytes_int8() for L in HISTORIES}}))
     return 0
 
 
@@ -593,7 +615,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",
-                    help="decode launches only (32768 history, --layers caches round-robin) for ncu")
+                    help="decode launches only (the three histories round-robin, --layers caches each) for ncu")
     args = ap.parse_args()
     if args.profile:
         return run_profile(args)

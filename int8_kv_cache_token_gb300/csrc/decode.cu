@@ -7,29 +7,31 @@
 // MMA; int32 bound 32 x 127 x 127 per group) and "gfx936 DCU上实现INT8 KV与
 // INT8 MMAC Attention推理优化" §3.3 (the decode data flow) and §2.3 (layouts).
 //
-// GB300 design (not the pages' gfx936 one):
-//  * Work unit = (sequence, KV head, 256-token partition).  A persistent grid of
-//    one CTA per SM takes a contiguous range of units; pairs (sequence, KV head)
-//    that span CTAs leave one partial per CTA in the workspace and the last CTA
-//    to finish a pair (an atomic ticket, no waiting) merges them by
-//    log-sum-exp.
-//  * Warp 8 is a TMA producer: per unit it issues 16 bulk copies of K pages (one
-//    ring item) and 16 of V pages (a second item) into a ring of shared-memory
-//    slots guarded by full/empty mbarriers.
-//  * Warps 0-7 consume, each on its own 32-token group of every partition
-//    (warp w: tokens 32w .. 32w+31), with no CTA barrier per partition: every
-//    warp runs its own online softmax (m, l, o) over its groups.  The pages
-//    normalize P inside a 256-token partition before quantizing W; here the
-//    normalization of each group is carried in the running state instead.  The
-//    group quantization Wq = round(W / (max W / 127)) does not change when all
-//    W of a group are scaled by one positive factor, so the codes are the
-//    pages' codes and the output is the same up to fp32 rounding.  At the end of
-//    a CTA's share of a pair the 8 warps' states merge deterministically
-//    (log-sum-exp, tree order) through shared memory.
-//  * GQA packs the G <= 8 query heads of one KV head into the N = 8 side of the
-//    MMAs.  QK: M = 16 tokens (one block), K = head-dims.  PV: M = 16 head-dims,
-//    N = 8 query rows, K = the tokens of one probability group, so each group's
-//    contraction is one accumulator and its sW scales exactly that result.
+// GB300 design (not the pages' gfx936 one): a persistent, warp-specialized CTA.
+//  * Work unit = (sequence, KV head, 128-token chunk).  The grid has one CTA per
+//    SM; CTA c takes the contiguous unit range [c U / N, (c+1) U / N).  A pair
+//    (sequence, KV head) that spans CTAs leaves one partial (o, m, l) per CTA in
+//    the workspace, and decode_merge_kernel combines them by log-sum-exp.  A
+//    unit is only a work granule: the pages' 256-token partition fixes no
+//    arithmetic here, because the group quantization below does not depend on
+//    where the softmax normalization is applied.
+//  * Producer warp: per unit, bulk copies (TMA) of the 8 K pages into one ring
+//    slot, together with the unit's K and V scales (plain loads, stored next to
+//    the pages), then the 8 V pages into the next slot.  Full/empty mbarriers
+//    guard the slots; even slots hold K items, odd slots V items.
+//  * 4 QK warps: warp w owns tokens 32w .. 32w+31 of every unit, i.e. one
+//    probability group.  QK (M = 16 tokens, N = 8 GQA-packed query rows), the
+//    score recovery, a CTA-wide running row maximum (one named barrier per
+//    unit), p~ = exp(s - m), W = p~ x sV, the group scale sW = max W / 127 and
+//    the codes Wq = round(W / sW).  The codes go to a double-buffered handoff
+//    area as ready-made f16 B fragments, with sW and the rescale factor.
+//  * 8 PV warps: warp v owns head-dims [D/8 v, D/8 (v+1)) of the output.  Per
+//    unit it rescales its accumulator once, then for each group runs the exact
+//    INT8 product Wq x Vq (K = the group's 32 tokens) and adds sW x that
+//    result.  Its accumulator covers disjoint dims, so the end of a segment
+//    needs no cross-warp reduction: the QK warps hand over (m, l) and each PV
+//    warp writes its own dims (final output or partial).
+//  * QK of unit i+1 overlaps PV of unit i (the handoff area has two buffers).
 //  * The INT8 x INT8 contractions run on the f16 tensor path: every int8 code is
 //    exact in f16, every product (<= 127^2) is exact, and every partial sum is
 //    an integer below 2^22 (QK over 256 dims: <= 4,129,024; PV over one group:
@@ -47,32 +49,63 @@ namespace i8kv {
 
 namespace {
 
-constexpr int kPart = 256;   // partition (tokens) -- the pages' decode partition
+constexpr int kPart = 256;   // the pages' decode partition (debug QK tiles)
 constexpr int kBS = 16;      // block size
 constexpr int kGroup = 32;   // probability group
-constexpr int kCWarps = 8;   // consumer warps (one per group of a partition)
-constexpr int kThreads = (kCWarps + 1) * 32;
+constexpr int kQW = 4;       // QK / softmax warps
+constexpr int kPW = 8;       // PV warps
+constexpr int kProdWarp = kQW + kPW;
+constexpr int kThreads = (kQW + kPW + 1) * 32;
 constexpr int kRows = 8;     // query rows in the MMA N dimension
+constexpr int kMinUnit = 64; // smallest work unit of any variant (grid sizing)
 __host__ __device__ constexpr int kSlotFloats(int D) { return kRows * D + 2 * kRows; }
 
-struct SmemLayout {
-  int nslots;
-  size_t ring, merge, wq, bars, ctrl, total;
+// Geometry of one variant.  INT8: 128-token units, one 32-token group per QK
+// warp.  BF16-KV comparison: 64-token units (the same 32 KB per ring item at
+// D = 256), one 16-token block per QK warp, plain softmax weights.
+template <int D, bool BF16>
+struct Geo {
+  static constexpr int EB = BF16 ? 2 : 1;                       // bytes per cache element
+  static constexpr int kUnit = BF16 ? 64 : 128;                 // tokens per unit
+  static constexpr int kBlocksU = kUnit / kBS;                  // pages per ring item
+  static constexpr int kPage = D * kBS * EB;                    // one (block, KV head) page
+  static constexpr int kPages = kBlocksU * kPage;
+  static constexpr int kSlot = kPages + (BF16 ? 0 : kUnit * 8); // + float2 (sK, sV) per token
+  static constexpr int kWTok = kUnit / kQW;                     // tokens per QK warp
+  static constexpr int MT = kWTok / 16;                         // 16-token blocks per QK warp
+  static constexpr int kDimsPW = D / kPW;                       // head-dims per PV warp
+  static constexpr int NDT = kDimsPW / 16;                      // 16-dim MMA tiles per PV warp
+  static constexpr int kFrag = BF16 ? 8 : 16;                   // B-fragment bytes per lane
+  // handoff buffer: [kQW][32 lanes] B fragments | sW [kQW][8] | alpha [8] | m [8] | l [kQW][8]
+  static constexpr int kHSw = kQW * 32 * kFrag;
+  static constexpr int kHAlpha = kHSw + kQW * kRows * 4;
+  static constexpr int kHM = kHAlpha + kRows * 4;
+  static constexpr int kHL = kHM + kRows * 4;
+  static constexpr int kHand = kHL + kQW * kRows * 4;
+  static constexpr int kStage = kRows * kWTok * EB;             // per-QK-warp code/weight transpose
+  static_assert(kGroup == kWTok || BF16, "an INT8 QK warp owns exactly one probability group");
+  static_assert(kSlot % 1024 == 0 && kHand % 16 == 0, "alignment");
 };
 
-__host__ __device__ inline SmemLayout decode_layout(int D, int nslots) {
+struct SmemLayout {
+  size_t ring, hand, mx, stage, bars, ctrl, total;
+};
+
+template <int D, bool BF16>
+__host__ __device__ inline SmemLayout decode_layout(int nslots) {
+  using Gm = Geo<D, BF16>;
   SmemLayout L;
-  L.nslots = nslots;
-  const size_t item = (size_t)kPart * D;
   size_t off = 0;
   L.ring = off;
-  off += (size_t)nslots * item;
-  L.merge = off;  // 4 warp states [8 rows][D + 4] + l [8] (+ maxima [8 warps][8 rows])
-  off += (size_t)(4 * (kRows * (D + 4) + 2 * kRows) + kCWarps * kRows) * sizeof(float);
-  L.wq = off;     // per-warp transpose of the quantized W: [8 rows][32 tokens] int8
-  off += (size_t)kCWarps * kRows * kGroup;
-  L.bars = off;
-  off += (size_t)2 * nslots * sizeof(uint64_t);
+  off += (size_t)nslots * Gm::kSlot;
+  L.hand = off;
+  off += 2 * (size_t)Gm::kHand;
+  L.mx = off;  // [2][kQW][8] unit row maxima
+  off += 2 * kQW * kRows * sizeof(float);
+  L.stage = off;
+  off += (size_t)kQW * Gm::kStage;
+  L.bars = off;  // full[nslots], empty[nslots], hfull[2], hempty[2]
+  off += (size_t)(2 * nslots + 4) * sizeof(uint64_t);
   L.ctrl = off;
   off += 16 * sizeof(int);
   L.total = off;
@@ -204,28 +237,24 @@ __device__ __forceinline__ void qk_warp_bf16(const uint8_t* kpages, int warp, in
   }
 }
 
+
 // One kernel body for both caches.  BF16 = false: the INT8 method.  BF16 = true:
-// the BF16-KV comparison (plain softmax, bf16 P x V, no scales), with 128-token
-// units so that a ring item (8 bf16 pages) has the same 64 KB at D = 256.
+// the BF16-KV comparison (plain softmax, bf16 P x V, no scales).
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int nslots) {
-  constexpr int NDT = D / 16;  // PV head-dim tiles (every warp covers all of D for its group)
-  constexpr int EB = BF16 ? 2 : 1;              // bytes per cache element
-  constexpr int kUnit = BF16 ? 128 : kPart;     // tokens per work unit
-  constexpr int kBlocksU = kUnit / kBS;         // pages per ring item
-  constexpr int kWTok = kUnit / kCWarps;        // tokens per warp per unit (32 = one probability group)
-  constexpr int MT = kWTok / 16;                // 16-token blocks per warp per unit
-  constexpr int kPage = D * kBS * EB;
-  constexpr int kItem = kBlocksU * kPage;
-  constexpr int kRS = D + 4;                   // row stride of a warp state (conflict-free stores)
-  constexpr int kWS = kRows * kRS + 2 * kRows;  // one warp state in the merge buffer
+  using Gm = Geo<D, BF16>;
+  constexpr int kUnit = Gm::kUnit, kBlocksU = Gm::kBlocksU, kPage = Gm::kPage, kSlot = Gm::kSlot;
+  constexpr int kWTok = Gm::kWTok, MT = Gm::MT, NDT = Gm::NDT;
   extern __shared__ __align__(1024) uint8_t smem[];
-  const SmemLayout lay = decode_layout(D, nslots);
-  int8_t* ring = reinterpret_cast<int8_t*>(smem + lay.ring);
-  float* mbuf = reinterpret_cast<float*>(smem + lay.merge);
-  int8_t* wqs = reinterpret_cast<int8_t*>(smem + lay.wq);
+  const SmemLayout lay = decode_layout<D, BF16>(nslots);
+  uint8_t* ring = smem + lay.ring;
+  uint8_t* hand = smem + lay.hand;
+  float* mxb = reinterpret_cast<float*>(smem + lay.mx);
+  uint8_t* stage = smem + lay.stage;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
   uint64_t* empty = full + nslots;
+  uint64_t* hfull = empty + nslots;
+  uint64_t* hempty = hfull + 2;
   int* ctrl = reinterpret_cast<int*>(smem + lay.ctrl);
   volatile int* abort_flag = ctrl + 8;
 
@@ -234,10 +263,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   const int N = gridDim.x, c = blockIdx.x;
   const int maxL = p.max_blocks * kBS;
 
-  if (warp == kCWarps && lane == 0) {
+  if (warp == kProdWarp && lane == 0) {
     for (int s = 0; s < nslots; ++s) {
       mbar_init(&full[s], 32);
-      mbar_init(&empty[s], kCWarps);
+      mbar_init(&empty[s], (s & 1) ? kPW : kQW);  // nslots is even: K items in even slots
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&hfull[j], kQW * 32);
+      mbar_init(&hempty[j], kPW);
     }
     fence_mbar_init();
   }
@@ -246,13 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   griddep_wait();
   griddep_launch_dependents();
 
-  // ---- work split, by the producer warp (the consumers wait at the barrier
+  // ---- work split, by the producer warp (the others wait at the barrier
   // below; they have nothing to do before it) ----
   // One sequence in the batch (the long-context decode case): guess the first
   // unit from max_blocks and load its block-table row together with seq_lens,
   // so the two dependent loads overlap; the guess is checked below.
   int spec_part = -1, spec_blk = -1;
-  if (warp == kCWarps && B == 1) {
+  if (warp == kProdWarp && B == 1) {
     const int np_g = (maxL + kUnit - 1) / kUnit;
     const long long U_g = (long long)np_g * Hkv;
     const int Nw_g = (int)(U_g < N ? U_g : N);
@@ -262,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         spec_blk = __ldg(p.block_tables + spec_part * kBlocksU + lane);
     }
   }
-  if (warp == kCWarps) {
+  if (warp == kProdWarp) {
     constexpr int kKeep = 8;  // chunks of 32 sequences whose unit counts stay in registers
     int ukeep[kKeep];
     long long total = 0;
@@ -346,8 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   w0.np = (w0.L + kUnit - 1) / kUnit;
   const long long U = (long long)ctrl[6] | ((long long)ctrl[7] << 31);
   const int Nw = ctrl[10];
+  const int g = lane >> 2, t = lane & 3;
 
-  if (warp == kCWarps) {
+  if (warp == kProdWarp) {
     // ================= producer warp =================
     const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
     const uint8_t* vc = static_cast<const uint8_t*>(p.v_cache);
@@ -355,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     Walk wk = w0;
     for (int i = 0; i < n_units; ++i) {
       const int t0 = wk.part * kUnit;
-      const int nblk = min(kBlocksU, (wk.L - t0 + kBS - 1) / kBS);
+      const int ntok = min(kUnit, wk.L - t0);
+      const int nblk = (ntok + kBS - 1) / kBS;
       int blk = -1;
       if (lane < nblk) {
         blk = (i == 0 && B == 1 && wk.part == spec_part)
@@ -366,115 +401,120 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
           blk = -1;
         }
       }
-      const bool ok = lane < kBlocksU && blk >= 0;
+      const bool ok = blk >= 0;
       const uint32_t n_pages = __popc(__ballot_sync(0xffffffffu, ok));
+      // K item: pages by bulk copy ...
+      const int kitem = 2 * i, kslot = kitem % nslots;
+      if (kitem >= nslots) pipe_wait(&empty[kslot], ((kitem / nslots) - 1) & 1, abort_flag);
+      if (lane == 0) mbar_expect_tx(&full[kslot], n_pages * kPage);
+      __syncwarp();
+      if (ok)
+        bulk_g2s_hint(ring + (size_t)kslot * kSlot + (size_t)lane * kPage,
+                      kc + ((size_t)blk * Hkv + wk.kvh) * kPage, kPage, &full[kslot], pol);
+      // ... and the unit's (sK, sV) per token, loaded now and stored below
+      float2 sc[kUnit / 32];
+      if constexpr (!BF16) {
 #pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-        const int item = 2 * i + kv, slot = item % nslots;
-        if (item >= nslots) pipe_wait(&empty[slot], ((item / nslots) - 1) & 1, abort_flag);
-        if (lane == 0) mbar_expect_tx(&full[slot], n_pages * kPage);
-        __syncwarp();
-        if (ok)
-          bulk_g2s_hint(ring + (size_t)slot * kItem + (size_t)lane * kPage,
-                        (kv == 0 ? kc : vc) + ((size_t)blk * Hkv + wk.kvh) * kPage, kPage, &full[slot], pol);
-        mbar_arrive(&full[slot]);
+        for (int r = 0; r < kUnit / 32; ++r) {
+          const int tok = lane + 32 * r;
+          const int bj = __shfl_sync(0xffffffffu, blk, tok / kBS);
+          const bool v = tok < ntok && bj >= 0;
+          const size_t si = ((size_t)(v ? bj : 0) * kBS + tok % kBS) * Hkv + wk.kvh;
+          sc[r] = v ? make_float2(__ldg(p.k_scale + si), __ldg(p.v_scale + si)) : make_float2(0.f, 0.f);
+        }
       }
+      // V item
+      const int vitem = kitem + 1, vslot = vitem % nslots;
+      if (vitem >= nslots) pipe_wait(&empty[vslot], ((vitem / nslots) - 1) & 1, abort_flag);
+      if (lane == 0) mbar_expect_tx(&full[vslot], n_pages * kPage);
+      __syncwarp();
+      if (ok)
+        bulk_g2s_hint(ring + (size_t)vslot * kSlot + (size_t)lane * kPage,
+                      vc + ((size_t)blk * Hkv + wk.kvh) * kPage, kPage, &full[vslot], pol);
+      mbar_arrive(&full[vslot]);
+      if constexpr (!BF16) {
+        float2* dst = reinterpret_cast<float2*>(ring + (size_t)kslot * kSlot + Gm::kPages);
+#pragma unroll
+        for (int r = 0; r < kUnit / 32; ++r) dst[lane + 32 * r] = sc[r];
+      }
+      mbar_arrive(&full[kslot]);  // releases the scale stores together with the page bytes
       walk_next(wk, p.seq_lens, B, Hkv, maxL, kUnit);
     }
     return;
   }
 
-  // ================= consumer warps =================
-  const int g = lane >> 2, t = lane & 3;
-  const float c_scale = p.sm_scale;
-  int8_t* wqw = wqs + warp * (kRows * kGroup);
-  Walk wk = w0;
-  int cur_pair = -1;
-  uint32_t qf[D / 32][4];    // INT8: converted query fragments
-  uint32_t qfb[D / 16][2];   // BF16: query fragments
-  float sq[2] = {0.f, 0.f};
-  float o[NDT][4];
-  float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
-  // this thread's scales for tokens {g, g+8} of blocks 2w and 2w+1 of a unit
-  float sk[4], sv[4], sk_n[4], sv_n[4];
-  auto load_scales = [&](const Walk& u, float (&k4)[4], float (&v4)[4]) {
+  if (warp < kQW) {
+    // ================= QK / softmax warps =================
+    const float c_scale = p.sm_scale;
+    const int tok0 = warp * kWTok;  // this warp's tokens within a unit
+    uint8_t* stg = stage + warp * Gm::kStage;
+    Walk wk = w0;
+    int cur_pair = -1;
+    uint32_t qf[D / 32][4];    // INT8: converted query fragments
+    uint32_t qfb[D / 16][2];   // BF16: query fragments
+    float sq[2] = {0.f, 0.f};
+    float mrun[2] = {-INFINITY, -INFINITY}, lw[2] = {0.f, 0.f};
+    for (int i = 0; i < n_units; ++i) {
+      const int pair = wk.b * Hkv + wk.kvh;
+      if (pair != cur_pair) {
+        cur_pair = pair;
+        if constexpr (BF16) {
+          load_q_frags_bf16<D>(static_cast<const uint16_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qfb);
+        } else {
+          load_q_frags<D>(static_cast<const int8_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qf);
+        }
 #pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      const int lb = u.part * kBlocksU + 2 * warp + m;  // logical block in the sequence
-      const int tok0 = lb * kBS;
-      int blk = -1;
-      if (tok0 < u.L) {
-        blk = __ldg(p.block_tables + (size_t)u.b * p.max_blocks + lb);
-        if (blk < 0 || blk >= p.num_blocks) blk = -1;
+        for (int r = 0; r < 2; ++r) {
+          const int row = 2 * t + r;
+          if constexpr (!BF16) sq[r] = row < G ? p.q_scale[(size_t)wk.b * Hq + wk.kvh * G + row] : 0.f;
+          mrun[r] = -INFINITY;
+          lw[r] = 0.f;
+        }
       }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int off = g + 8 * h;
-        const bool v = blk >= 0 && tok0 + off < u.L;
-        const size_t si = ((size_t)(v ? blk : 0) * kBS + off) * Hkv + u.kvh;
-        k4[2 * m + h] = v ? __ldg(p.k_scale + si) : 0.f;
-        v4[2 * m + h] = v ? __ldg(p.v_scale + si) : 0.f;
-      }
-    }
-  };
-  if constexpr (!BF16) load_scales(wk, sk, sv);
-  for (int i = 0; i < n_units; ++i) {
-    const int pair = wk.b * Hkv + wk.kvh;
-    if (pair != cur_pair) {
-      cur_pair = pair;
-      if constexpr (BF16) {
-        load_q_frags_bf16<D>(static_cast<const uint16_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qfb);
-      } else {
-        load_q_frags<D>(static_cast<const int8_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qf);
-      }
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int row = 2 * t + r;
-        if constexpr (!BF16) sq[r] = row < G ? p.q_scale[(size_t)wk.b * Hq + wk.kvh * G + row] : 0.f;
-        mrun[r] = -INFINITY;
-        lrun[r] = 0.f;
-      }
-#pragma unroll
-      for (int dt = 0; dt < NDT; ++dt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o[dt][e] = 0.f;
-    }
-    Walk nx = wk;
-    walk_next(nx, p.seq_lens, B, Hkv, maxL, kUnit);
-    if constexpr (!BF16)
-      if (i + 1 < n_units) load_scales(nx, sk_n, sv_n);  // the next unit's scales, in flight meanwhile
-    const int t0 = wk.part * kUnit;
-    const int ntok = min(kUnit, wk.L - t0);
-    const bool active = warp * kWTok < ntok;
+      Walk nx = wk;
+      walk_next(nx, p.seq_lens, B, Hkv, maxL, kUnit);
+      const bool seg_end = (i == n_units - 1) || (nx.b * Hkv + nx.kvh != pair);
+      const int ntok = min(kUnit, wk.L - wk.part * kUnit);
+      const bool active = tok0 < ntok;
 
-    // ---- K item: QK for this warp's group ----
-    const int kitem = 2 * i, kslot = kitem % nslots;
-    pipe_wait(&full[kslot], (kitem / nslots) & 1, abort_flag);
-    float acc[2][4];
-    if (active) {
-      if constexpr (BF16)
-        qk_warp_bf16<D>(reinterpret_cast<const uint8_t*>(ring) + (size_t)kslot * kItem, warp, lane, qfb, acc[0]);
-      else
-        qk_warp<D>(ring + (size_t)kslot * kItem, warp, lane, qf, acc);
-    } else {
+      // ---- K item: QK of this warp's tokens, and their scales ----
+      const int kitem = 2 * i, kslot = kitem % nslots;
+      pipe_wait(&full[kslot], (kitem / nslots) & 1, abort_flag);
+      const uint8_t* kb = ring + (size_t)kslot * kSlot;
+      float acc[2][4];
 #pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[m][e] = 0.f;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[kslot]);
+      if (active) {
+        if constexpr (BF16)
+          qk_warp_bf16<D>(kb, warp, lane, qfb, acc[0]);
+        else
+          qk_warp<D>(reinterpret_cast<const int8_t*>(kb), warp, lane, qf, acc);
+      }
+      float sk[4], sv[4];  // tokens g, g+8 of this warp's blocks 0 and 1
+      if constexpr (!BF16) {
+        const float2* scl = reinterpret_cast<const float2*>(kb + Gm::kPages);
+#pragma unroll
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float2 v = scl[tok0 + 16 * m + g + 8 * h];
+            sk[2 * m + h] = v.x;
+            sv[2 * m + h] = v.y;
+          }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[kslot]);
 
-    // ---- scores, online softmax over this warp's group, W = p~ * sV, quantize ----
-    float alpha[2] = {1.f, 1.f}, sw[2] = {0.f, 0.f};
-    if (active) {
-      float s[2][4];
-      float mx[2] = {-INFINITY, -INFINITY};
+      // ---- scores and the CTA-wide running row maximum ----
+      float s[MT][4];
+      float lmax[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int m = 0; m < MT; ++m)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int tok = warp * kWTok + 16 * m + g + 8 * (e >> 1);
+          const int tok = tok0 + 16 * m + g + 8 * (e >> 1);
           float sc = -INFINITY;
           if (tok < ntok) {
             if constexpr (BF16)
@@ -483,26 +523,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
               sc = __fmul_rn(__fmul_rn(__fmul_rn(acc[m][e], sq[e & 1]), sk[2 * m + (e >> 1)]), c_scale);
           }
           s[m][e] = sc;
-          mx[e & 1] = fmaxf(mx[e & 1], sc);
+          lmax[e & 1] = fmaxf(lmax[e & 1], sc);
         }
 #pragma unroll
       for (int r = 0; r < 2; ++r)
 #pragma unroll
-        for (int off = 4; off <= 16; off <<= 1) mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], off));
+        for (int off = 4; off <= 16; off <<= 1)
+          lmax[r] = fmaxf(lmax[r], __shfl_xor_sync(0xffffffffu, lmax[r], off));
+      float* mxu = mxb + (i & 1) * (kQW * kRows);
+      if (g == 0) {
+        mxu[warp * kRows + 2 * t] = lmax[0];
+        mxu[warp * kRows + 2 * t + 1] = lmax[1];
+      }
+      named_bar_sync(1, kQW * 32);
+      float alpha[2];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const float mn = fmaxf(mrun[r], mx[r]);
+        float um = -INFINITY;
+#pragma unroll
+        for (int w2 = 0; w2 < kQW; ++w2) um = fmaxf(um, mxu[w2 * kRows + 2 * t + r]);
+        const float mn = fmaxf(mrun[r], um);
         alpha[r] = (mrun[r] == -INFINITY) ? 0.f : expf(mrun[r] - mn);
         mrun[r] = mn;
-        lrun[r] *= alpha[r];
+        lw[r] *= alpha[r];
       }
+
+      // ---- weights: BF16 p~; INT8 W = p~ sV, sW, codes ----
+      float swv[2] = {0.f, 0.f};
       if constexpr (BF16) {
-        // plain softmax weights p~ in bf16 -> this warp's [row][16 tokens] staging
-        uint16_t* pw = reinterpret_cast<uint16_t*>(wqw);
+        uint16_t* pw = reinterpret_cast<uint16_t*>(stg);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float pe = (s[0][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[0][e], mrun[e & 1]));
-          lrun[e & 1] += pe;
+          lw[e & 1] += pe;
           pw[(2 * t + (e & 1)) * 16 + g + 8 * (e >> 1)] = __bfloat16_as_ushort(__float2bfloat16_rn(pe));
         }
       } else {
@@ -512,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float pe = (s[m][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[m][e], mrun[e & 1]));
-            lrun[e & 1] += pe;
+            lw[e & 1] += pe;
             w[m][e] = __fmul_rn(pe, sv[2 * m + (e >> 1)]);
             A[e & 1] = fmaxf(A[e & 1], w[m][e]);
           }
@@ -523,187 +576,206 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         float inv[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          sw[r] = __fdiv_rn(A[r], 127.0f);
+          swv[r] = __fdiv_rn(A[r], 127.0f);
           inv[r] = A[r] > 0.f ? __fdiv_rn(127.0f, A[r]) : 0.f;
         }
-        // codes -> this warp's [row][token] bytes, read back below as PV B fragments
+        // codes -> [row][token] bytes, read back below as PV B fragments
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int q = min(127, __float2int_rn(w[m][e] * inv[e & 1]));
-            wqw[(2 * t + (e & 1)) * kGroup + 16 * m + g + 8 * (e >> 1)] = (int8_t)q;
+            stg[(2 * t + (e & 1)) * kGroup + 16 * m + g + 8 * (e >> 1)] = (uint8_t)(int8_t)q;
           }
       }
+      __syncwarp();
+
+      // ---- hand the unit over to the PV warps ----
+      if (i >= 2) pipe_wait(&hempty[i & 1], ((i >> 1) - 1) & 1, abort_flag);
+      uint8_t* hb = hand + (size_t)(i & 1) * Gm::kHand;
+      if constexpr (BF16) {
+        uint2 f;
+        f.x = *reinterpret_cast<const uint32_t*>(stg + g * 32 + 4 * t);
+        f.y = *reinterpret_cast<const uint32_t*>(stg + g * 32 + 16 + 4 * t);
+        reinterpret_cast<uint2*>(hb)[warp * 32 + lane] = f;
+      } else {
+        uint32_t b4[4];
+        s8b_to_f16(*reinterpret_cast<const uint32_t*>(stg + g * kGroup + 4 * t),
+                   *reinterpret_cast<const uint32_t*>(stg + g * kGroup + 16 + 4 * t), b4);
+        reinterpret_cast<uint4*>(hb)[warp * 32 + lane] = make_uint4(b4[0], b4[1], b4[2], b4[3]);
+      }
+      float* hsw = reinterpret_cast<float*>(hb + Gm::kHSw);
+      float* hal = reinterpret_cast<float*>(hb + Gm::kHAlpha);
+      float* hm = reinterpret_cast<float*>(hb + Gm::kHM);
+      float* hl = reinterpret_cast<float*>(hb + Gm::kHL);
+      if (g == 0) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          hsw[warp * kRows + 2 * t + r] = swv[r];
+          if (warp == 0) hal[2 * t + r] = alpha[r];
+        }
+      }
+      if (seg_end) {
+        float ls[2] = {lw[0], lw[1]};
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int off = 4; off <= 16; off <<= 1) ls[r] += __shfl_xor_sync(0xffffffffu, ls[r], off);
+        if (g == 0) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            hl[warp * kRows + 2 * t + r] = ls[r];
+            if (warp == 0) hm[2 * t + r] = mrun[r];
+          }
+        }
+      }
+      mbar_arrive(&hfull[i & 1]);  // every thread: releases its own stores
+      wk = nx;
     }
-    __syncwarp();
-    uint32_t bq[4];
-    if constexpr (BF16) {
-      bq[0] = *reinterpret_cast<const uint32_t*>(wqw + g * 32 + 4 * t);
-      bq[1] = *reinterpret_cast<const uint32_t*>(wqw + g * 32 + 16 + 4 * t);
-    } else {
-      s8b_to_f16(*reinterpret_cast<const uint32_t*>(wqw + g * kGroup + 4 * t),
-                 *reinterpret_cast<const uint32_t*>(wqw + g * kGroup + 16 + 4 * t), bq);
+    return;
+  }
+
+  // ================= PV warps =================
+  const int pv_w = warp - kQW;
+  const int mi = lane >> 3, ri = lane & 7;
+  Walk wk = w0;
+  int cur_pair = -1;
+  float o[NDT][4];
+  for (int i = 0; i < n_units; ++i) {
+    const int pair = wk.b * Hkv + wk.kvh;
+    if (pair != cur_pair) {
+      cur_pair = pair;
+#pragma unroll
+      for (int dt = 0; dt < NDT; ++dt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[dt][e] = 0.f;
     }
-    if (alpha[0] != 1.f || alpha[1] != 1.f) {
+    Walk nx = wk;
+    walk_next(nx, p.seq_lens, B, Hkv, maxL, kUnit);
+    const bool seg_end = (i == n_units - 1) || (nx.b * Hkv + nx.kvh != pair);
+    const int ntok = min(kUnit, wk.L - wk.part * kUnit);
+
+    const uint8_t* hb = hand + (size_t)(i & 1) * Gm::kHand;
+    pipe_wait(&hfull[i & 1], (i >> 1) & 1, abort_flag);
+    const float* hsw = reinterpret_cast<const float*>(hb + Gm::kHSw);
+    const float* hal = reinterpret_cast<const float*>(hb + Gm::kHAlpha);
+    const float a0 = hal[2 * t], a1 = hal[2 * t + 1];
+    if (a0 != 1.f || a1 != 1.f) {
 #pragma unroll
       for (int dt = 0; dt < NDT; ++dt) {
-        o[dt][0] *= alpha[0];
-        o[dt][1] *= alpha[1];
-        o[dt][2] *= alpha[0];
-        o[dt][3] *= alpha[1];
+        o[dt][0] *= a0;
+        o[dt][1] *= a1;
+        o[dt][2] *= a0;
+        o[dt][3] *= a1;
       }
     }
 
-    // ---- V item: exact INT8 PV of this warp's group, scaled by sW ----
+    // ---- V item: this warp's head-dims, every group of the unit ----
     const int vitem = 2 * i + 1, vslot = vitem % nslots;
     pipe_wait(&full[vslot], (vitem / nslots) & 1, abort_flag);
-    if (active) {
-      const int mi = lane >> 3, ri = lane & 7;
+    const uint8_t* vb = ring + (size_t)vslot * kSlot;
+#pragma unroll
+    for (int q = 0; q < kQW; ++q) {
+      if (q * kWTok >= ntok) break;
       if constexpr (BF16) {
-        // A = V^T from the warp's bf16 page [D][16 tokens]: matrices (dims 0-7 | 8-15) x (tokens 0-7 | 8-15)
-        const uint8_t* vrow = reinterpret_cast<const uint8_t*>(ring) + (size_t)vslot * kItem + (size_t)warp * kPage +
-                              (ri + 8 * (mi & 1)) * 32 + (mi >> 1) * 16;
+        // A = V^T of page q [D][16 tokens]: matrices (dims 0-7 | 8-15) x (tokens 0-7 | 8-15)
+        const uint2 f = reinterpret_cast<const uint2*>(hb)[q * 32 + lane];
+        const uint8_t* vrow = vb + (size_t)q * kPage + (size_t)(pv_w * Gm::kDimsPW) * 32 + (ri + 8 * (mi & 1)) * 32 +
+                              (mi >> 1) * 16;
 #pragma unroll
         for (int dt = 0; dt < NDT; ++dt) {
           uint32_t a[4];
           ldmatrix_x4(a, vrow + dt * 16 * 32);
-          mma_bf16_16816(o[dt], a, bq[0], bq[1]);
+          mma_bf16_16816(o[dt], a, f.x, f.y);
         }
       } else {
-        const int8_t* vrow =
-            ring + (size_t)vslot * kItem + (size_t)(2 * warp + (mi >> 1)) * kPage + (ri + 8 * (mi & 1)) * 16;
+        // A = V^T of the group's pages 2q, 2q+1: (dims 0-7 | 8-15) x (page 2q | 2q+1)
+        const uint4 f = reinterpret_cast<const uint4*>(hb)[q * 32 + lane];
+        const uint32_t bq[4] = {f.x, f.y, f.z, f.w};
+        const float s0 = hsw[q * kRows + 2 * t], s1 = hsw[q * kRows + 2 * t + 1];
+        const uint8_t* vrow = vb + (size_t)(2 * q + (mi >> 1)) * kPage + (size_t)(pv_w * Gm::kDimsPW) * 16 +
+                              (ri + 8 * (mi & 1)) * 16;
 #pragma unroll
         for (int dt = 0; dt < NDT; ++dt) {
           uint32_t a[4];
           ldmatrix_x4(a, vrow + dt * 16 * 16);
           float pv[4] = {0.f, 0.f, 0.f, 0.f};
           mma_s8a_f16b(pv, a, bq);
-          o[dt][0] = fmaf(pv[0], sw[0], o[dt][0]);
-          o[dt][1] = fmaf(pv[1], sw[1], o[dt][1]);
-          o[dt][2] = fmaf(pv[2], sw[0], o[dt][2]);
-          o[dt][3] = fmaf(pv[3], sw[1], o[dt][3]);
+          o[dt][0] = fmaf(pv[0], s0, o[dt][0]);
+          o[dt][1] = fmaf(pv[1], s1, o[dt][1]);
+          o[dt][2] = fmaf(pv[2], s0, o[dt][2]);
+          o[dt][3] = fmaf(pv[3], s1, o[dt][3]);
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[vslot]);
 
-    // ---- end of this CTA's share of the (sequence, KV head) pair? ----
-    const bool seg_end = (i == n_units - 1) || (nx.b * Hkv + nx.kvh != pair);
+    // ---- end of this CTA's share of the (sequence, KV head) pair ----
     if (seg_end) {
-      // full row sums of this warp (the 8 threads with one t hold one row's tokens)
-#pragma unroll
-      for (int r = 0; r < 2; ++r)
-#pragma unroll
-        for (int off = 4; off <= 16; off <<= 1) lrun[r] += __shfl_xor_sync(0xffffffffu, lrun[r], off);
-      // common max over the 8 warps, then a tree sum in a fixed order
-      float* mw = mbuf + 4 * kWS;  // [8 warps][8 rows] maxima
-      if (g == 0) {
-        mw[warp * kRows + 2 * t] = mrun[0];
-        mw[warp * kRows + 2 * t + 1] = mrun[1];
-      }
-      named_bar_sync(1, kCWarps * 32);
-      float M[2];
+      const float* hm = reinterpret_cast<const float*>(hb + Gm::kHM);
+      const float* hl = reinterpret_cast<const float*>(hb + Gm::kHL);
+      float lsum[2], mrow[2];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        float mm = -INFINITY;
+        float l = 0.f;
 #pragma unroll
-        for (int w2 = 0; w2 < kCWarps; ++w2) mm = fmaxf(mm, mw[w2 * kRows + 2 * t + r]);
-        M[r] = mm;
-        const float f = (mrun[r] == -INFINITY) ? 0.f : expf(mrun[r] - mm);
-        lrun[r] *= f;
-#pragma unroll
-        for (int dt = 0; dt < NDT; ++dt) {
-          o[dt][r] *= f;
-          o[dt][2 + r] *= f;
-        }
+        for (int w2 = 0; w2 < kQW; ++w2) l += hl[w2 * kRows + 2 * t + r];  // fixed order
+        lsum[r] = l;
+        mrow[r] = hm[2 * t + r];
       }
-      // Two rounds (warps 0-3, then 4-7) through 4 shared buffers; each thread
-      // then owns one row and D/32 head-dims of the CTA's state and adds the
-      // 8 warps' values in warp order (deterministic).
-      constexpr int DPT = D / 32;
-      const int orow = tid >> 5;  // 0..7
-      float Mrow = -INFINITY;  // read before the rounds' barriers, so a later segment cannot overwrite it first
-#pragma unroll
-      for (int w2 = 0; w2 < kCWarps; ++w2) Mrow = fmaxf(Mrow, mw[w2 * kRows + orow]);
-      float acc_o[DPT];
-      float acc_l = 0.f;
-#pragma unroll
-      for (int k = 0; k < DPT; ++k) acc_o[k] = 0.f;
-#pragma unroll
-      for (int round = 0; round < 2; ++round) {
-        if ((warp >> 2) == round) {
-          float* buf = mbuf + (size_t)(warp & 3) * kWS;
-#pragma unroll
-          for (int dt = 0; dt < NDT; ++dt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if (2 * t + (e & 1) < G) buf[(2 * t + (e & 1)) * kRS + dt * 16 + g + 8 * (e >> 1)] = o[dt][e];
-          if (g == 0) {
-            buf[kRows * kRS + 2 * t] = lrun[0];
-            buf[kRows * kRS + 2 * t + 1] = lrun[1];
-          }
-        }
-        named_bar_sync(1, kCWarps * 32);
-        if (orow < G) {
-#pragma unroll
-          for (int wb = 0; wb < 4; ++wb) {
-            const float* buf = mbuf + (size_t)wb * kWS;
-#pragma unroll
-            for (int k = 0; k < DPT; ++k) acc_o[k] += buf[orow * kRS + lane + 32 * k];
-            acc_l += buf[kRows * kRS + orow];
-          }
-        }
-        named_bar_sync(1, kCWarps * 32);
-      }
-      (void)M;
       const long long Up = wk.ub + (long long)wk.kvh * wk.np;
       const int cf = cta_of(Up, U, Nw), cl = cta_of(Up + wk.np - 1, U, Nw);
       // the CTA holding the pair's first unit records whether a merge is needed
-      if (c == cf && tid == 0) p.ws_info[pair] = (cf == cl) ? -1 : ((cf << 16) | cl);
+      if (c == cf && pv_w == 0 && lane == 0) p.ws_info[pair] = (cf == cl) ? -1 : ((cf << 16) | cl);
+      const int d0 = pv_w * Gm::kDimsPW;
       if (cf == cl) {
-        if (orow < G) {
-          float* dst = p.out + ((size_t)wk.b * Hq + wk.kvh * G + orow) * D;
-          const float inv = 1.0f / acc_l;
+        float* dst = p.out + ((size_t)wk.b * Hq + wk.kvh * G) * D;
+        const float inv0 = 1.0f / lsum[0], inv1 = 1.0f / lsum[1];
 #pragma unroll
-          for (int k = 0; k < DPT; ++k) dst[lane + 32 * k] = acc_o[k] * inv;
-        }
+        for (int dt = 0; dt < NDT; ++dt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = 2 * t + (e & 1);
+            if (row < G) dst[(size_t)row * D + d0 + dt * 16 + g + 8 * (e >> 1)] = o[dt][e] * ((e & 1) ? inv1 : inv0);
+          }
       } else {
         // one partial per CTA; decode_merge_kernel combines them after this kernel
         float* part = p.ws_part + (size_t)(pair + c) * kSlotFloats(D);
-        if (orow < G) {
 #pragma unroll
-          for (int k = 0; k < DPT; ++k) part[orow * D + lane + 32 * k] = acc_o[k];
-        }
-        if (lane == 0) {
-          part[kRows * D + orow] = Mrow;
-          part[kRows * D + kRows + orow] = acc_l;
+        for (int dt = 0; dt < NDT; ++dt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = 2 * t + (e & 1);
+            if (row < G) part[row * D + d0 + dt * 16 + g + 8 * (e >> 1)] = o[dt][e];
+          }
+        if (pv_w == 0 && g == 0) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            part[kRows * D + 2 * t + r] = mrow[r];
+            part[kRows * D + kRows + 2 * t + r] = lsum[r];
+          }
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&hempty[i & 1]);
     wk = nx;
-    if constexpr (!BF16) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        sk[k] = sk_n[k];
-        sv[k] = sv_n[k];
-      }
-    }
   }
 }
 
 // Log-sum-exp merge of the partials of pairs that span CTAs: one CTA per
-// (pair, query row).  Thread (slice, column) sums every SL-th segment of one
-// float4 column; the slices are then added in a fixed order.
+// (pair, query row).  Thread (slice, column) walks every SL-th segment of one
+// float4 column and keeps its own running (max, denominator, sum) -- all its
+// loads are independent, so they are in flight together -- then the slices are
+// combined in a fixed order.
 constexpr int kMaxSeg = 1024;
 
 template <int D>
 __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeParams p) {
   constexpr int COLS = D / 4, SL = 256 / COLS;
-  __shared__ float wsh[kMaxSeg], lsh[kMaxSeg];
   __shared__ float4 red[SL][COLS];
-  __shared__ float Msh, den;
+  __shared__ float msh[SL], dsh[SL];
   griddep_wait();
   griddep_launch_dependents();
   const int tid = threadIdx.x;
@@ -715,51 +787,46 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeParams p) {
     record_error(2);
     return;
   }
-  const float* part0 = p.ws_part + (size_t)(pair + cf) * kSlotFloats(D);
-  for (int s = tid; s < nseg; s += 256) {
-    wsh[s] = part0[(size_t)s * kSlotFloats(D) + kRows * D + row];
-    lsh[s] = part0[(size_t)s * kSlotFloats(D) + kRows * D + kRows + row];
-  }
-  __syncthreads();
-  if (tid < 32) {
-    float m = -INFINITY;
-    for (int s = tid; s < nseg; s += 32) m = fmaxf(m, wsh[s]);
-    for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (tid == 0) Msh = m;
-  }
-  __syncthreads();
-  for (int s = tid; s < nseg; s += 256) wsh[s] = expf(wsh[s] - Msh);
-  __syncthreads();
-  if (tid < 32) {
-    float dd = 0.f;
-    for (int s = tid; s < nseg; s += 32) dd += wsh[s] * lsh[s];
-    for (int off = 16; off >= 1; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
-    if (tid == 0) den = dd;
-  }
   const int slice = tid / COLS, col = tid % COLS;
-  const float4* base = reinterpret_cast<const float4*>(part0 + row * D) + col;
+  const float* part0 = p.ws_part + (size_t)(pair + cf) * kSlotFloats(D);
+  float m = -INFINITY, den = 0.f;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+#pragma unroll 8
   for (int s = slice; s < nseg; s += SL) {
-    const float4 v = base[(size_t)s * (kSlotFloats(D) / 4)];
-    const float w = wsh[s];
-    a.x = fmaf(w, v.x, a.x);
-    a.y = fmaf(w, v.y, a.y);
-    a.z = fmaf(w, v.z, a.z);
-    a.w = fmaf(w, v.w, a.w);
+    const float* ps = part0 + (size_t)s * kSlotFloats(D);
+    const float ms = ps[kRows * D + row], ls = ps[kRows * D + kRows + row];
+    const float4 v = *reinterpret_cast<const float4*>(ps + row * D + 4 * col);
+    const float mn = fmaxf(m, ms);
+    const float f = expf(m - mn), e = expf(ms - mn);
+    a.x = fmaf(v.x, e, a.x * f);
+    a.y = fmaf(v.y, e, a.y * f);
+    a.z = fmaf(v.z, e, a.z * f);
+    a.w = fmaf(v.w, e, a.w * f);
+    den = fmaf(ls, e, den * f);
+    m = mn;
   }
   red[slice][col] = a;
+  if (col == 0) {
+    msh[slice] = m;
+    dsh[slice] = den;
+  }
   __syncthreads();
   if (tid < COLS) {
-    float4 r = red[0][tid];
+    float M = -INFINITY;
 #pragma unroll
-    for (int k = 1; k < SL; ++k) {
-      r.x += red[k][tid].x;
-      r.y += red[k][tid].y;
-      r.z += red[k][tid].z;
-      r.w += red[k][tid].w;
+    for (int k = 0; k < SL; ++k) M = fmaxf(M, msh[k]);
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+    float dd = 0.f;
+#pragma unroll
+    for (int k = 0; k < SL; ++k) {
+      const float w = expf(msh[k] - M);  // 0 for a slice without segments
+      r.x = fmaf(red[k][tid].x, w, r.x);
+      r.y = fmaf(red[k][tid].y, w, r.y);
+      r.z = fmaf(red[k][tid].z, w, r.z);
+      r.w = fmaf(red[k][tid].w, w, r.w);
+      dd = fmaf(dsh[k], w, dd);
     }
-    const float inv = 1.0f / den;
+    const float inv = 1.0f / dd;
     const int b = pair / p.Hkv, kvh = pair % p.Hkv;
     *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + kvh * p.G + row) * D + 4 * tid) =
         make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv);
@@ -835,10 +902,11 @@ int max_smem_optin(int device) {
   return g_max_smem[device];
 }
 
-// Deepest ring that fits.
-int pick_slots(int D, int smem_limit) {
-  for (int ns = 8; ns >= 2; --ns)
-    if (decode_layout(D, ns).total <= (size_t)smem_limit) return ns;
+// Deepest ring that fits (an even number of slots: K items in even slots).
+template <int D, bool BF16>
+int pick_slots(int smem_limit) {
+  for (int ns = 12; ns >= 2; ns -= 2)
+    if (decode_layout<D, BF16>(ns).total <= (size_t)smem_limit) return ns;
   return 0;
 }
 
@@ -846,9 +914,9 @@ template <int D, bool BF16>
 cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
-  const int ns = pick_slots(D, max_smem_optin(dev));
+  const int ns = pick_slots<D, BF16>(max_smem_optin(dev));
   if (ns == 0) return cudaErrorInvalidConfiguration;
-  const size_t smem = decode_layout(D, ns).total;
+  const size_t smem = decode_layout<D, BF16>(ns).total;
   // Raise the dynamic shared-memory limit once per device (to the opt-in
   // maximum), so that launches captured into a CUDA graph make no attribute call.
   static int attr_set[64] = {0};
@@ -868,7 +936,7 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
 I8KV_DEFINE_ERROR_ACCESSOR(read_error_decode)
 
 int decode_grid(int device, int B, int Hkv, int max_blocks) {
-  const long long max_units = (long long)B * Hkv * (((long long)max_blocks * kBS + kPart - 1) / kPart);
+  const long long max_units = (long long)B * Hkv * (((long long)max_blocks * kBS + kMinUnit - 1) / kMinUnit);
   long long g = num_sms(device);
   if (max_units < g) g = max_units;
   return (int)(g < 1 ? 1 : g);

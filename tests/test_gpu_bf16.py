@@ -1,6 +1,13 @@
 """GPU parity of the BF16-KV comparison path: the bf16 paged cache write is a
 byte-exact scatter, and the decode matches fp64 softmax attention over the same
-bf16 cache (the oracle) within 2e-3."""
+bf16 cache (the oracle).
+
+Tolerance, from the arithmetic: the kernel rounds each softmax weight
+p~ = exp(s - m) to bf16 (8 significant bits, relative error <= 2^-8) before the
+bf16 P x V product, while l sums the unrounded fp32 weights.  So output element
+(h, j) is off by at most 2^-8 * sum_t (p_t / l) |v_tj| (the softmax-weighted
+mean of |v|), plus fp32 rounding of the scores, exp and accumulation (bounded
+here by 2e-4).  The bound is computed per element from the inputs in fp64."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +18,6 @@ from oracle import oracle as orc
 from tests.gpu_helpers import dev, host
 
 pytestmark = pytest.mark.gpu
-TOL = 2e-3
 
 
 def _caches(w):
@@ -22,6 +28,26 @@ def _caches(w):
         i8.bf16_kv_write(dev(k), dev(v), dev(w.slots(b)), **gc)
         oc = orc.bf16_kv_write(k, v, w.slots(b), w.num_blocks, w.block_size, **({} if oc is None else oc))
     return gc, oc
+
+
+def _f32(bits):
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _tol(w, q):
+    """[B, Hq, D] per-element bound 2^-8 * sum_t (p_t / l) |v_tj| + 2e-4."""
+    G = w.Hq // w.Hkv
+    tol = np.full((w.B, w.Hq, w.D), 2e-4)
+    for b in range(w.B):
+        L = int(w.seq_lens[b])
+        if L == 0:
+            continue
+        k, v = (_f32(x) for x in w.kv(b))
+        for h in range(w.Hq):
+            s = k[:, h // G, :] @ _f32(q[b, h]) / np.sqrt(w.D)
+            p = np.exp(s - s.max())
+            tol[b, h] += 2.0 ** -8 * (p / p.sum()) @ np.abs(v[:, h // G, :])
+    return tol
 
 
 @pytest.mark.parametrize("lens,Hq,Hkv,D", [([1], 24, 4, 256), ([300, 17], 24, 4, 256), ([129, 0, 1000], 32, 8, 128),
@@ -38,8 +64,9 @@ def test_bf16_write_and_decode(lens, Hq, Hkv, D):
     got = host(out)
     assert i8.device_error() == 0
     ref = orc.bf16_decode_attn(q, oc, w.block_tables, w.seq_lens, w.block_size)
-    err = np.abs(got - ref).max()
-    assert err <= TOL, f"max-abs {err:.3e}"
+    err = np.abs(got - ref)
+    tol = _tol(w, q)
+    assert (err <= tol).all(), f"max-abs {err.max():.3e}, worst err/bound {(err / tol).max():.2f}"
     for b, L in enumerate(lens):
         if L == 0:
             assert not got[b].any()
@@ -53,4 +80,4 @@ def test_bf16_decode_long_outlier_history():
     ws = i8.decode_workspace(1, 24, 4, 256, w.block_tables.shape[1])
     i8.bf16_paged_decode_attn(out, dev(q), gc["k_cache"], gc["v_cache"], dev(w.block_tables), dev(w.seq_lens), ws)
     ref = orc.bf16_decode_attn(q, oc, w.block_tables, w.seq_lens, w.block_size)
-    assert np.abs(host(out) - ref).max() <= TOL
+    assert (np.abs(host(out) - ref) <= _tol(w, q)).all()
