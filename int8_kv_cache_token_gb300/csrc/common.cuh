@@ -119,6 +119,20 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
       : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (cp.async); src_bytes = 0 writes
+// zeros without reading src.  Both addresses 4-byte aligned.
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+// The mbarrier's current phase also waits for every cp.async this thread has
+// issued so far (the pending count is raised by one now and lowered when the
+// copies land, so the barrier's expected arrival count is unchanged).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialization may start while the previous kernel on the stream is still
 // running; griddep_wait() blocks until that kernel has finished and its memory
@@ -210,6 +224,19 @@ __device__ __forceinline__ void s8b_to_f16(uint32_t x0, uint32_t x1, uint32_t (&
 
 
 // ----------------------------------------------------------------- numerics
+// x / s correctly rounded (the IEEE quotient) for one divisor s shared by many
+// x, by Markstein's method: with y = RN(1/s), q = RN(x * y) and the exact
+// residual r = x - s * q (one FMA), RN(q + r * y) is the correctly rounded
+// quotient while nothing overflows or underflows.  `tiny` (s below 2^-100)
+// selects the plain division instead.
+__device__ __forceinline__ float div_shared(float x, float s, float y, bool tiny) {
+  if (tiny) return __fdiv_rn(x, s);
+  const float q = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-s, q, x);
+  return __fmaf_rn(r, y, q);
+}
+constexpr float kTinyDivisor = 7.8886091e-31f;  // 2^-100
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
 // Four int8 codes packed little-endian into one register.

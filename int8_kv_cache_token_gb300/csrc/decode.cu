@@ -16,22 +16,30 @@
 //    arithmetic here, because the group quantization below does not depend on
 //    where the softmax normalization is applied.
 //  * Producer warp: per unit, bulk copies (TMA) of the 8 K pages into one ring
-//    slot, together with the unit's K and V scales (plain loads, stored next to
-//    the pages), then the 8 V pages into the next slot.  Full/empty mbarriers
+//    slot, together with the unit's K and V scales (cp.async, next to the
+//    pages), then the 8 V pages into the next slot.  Block-table entries are
+//    read one unit ahead.  Full/empty mbarriers
 //    guard the slots; even slots hold K items, odd slots V items.
-//  * 4 QK warps: warp w owns tokens 32w .. 32w+31 of every unit, i.e. one
+//  * 8 QK warps in two streams (warps 0-3 take the even units, 4-7 the odd
+//    ones); in a unit, warp w of a stream owns tokens 32w .. 32w+31, one
 //    probability group.  QK (M = 16 tokens, N = 8 GQA-packed query rows), the
-//    score recovery, a CTA-wide running row maximum (one named barrier per
-//    unit), p~ = exp(s - m), W = p~ x sV, the group scale sW = max W / 127 and
-//    the codes Wq = round(W / sW).  The codes go to a double-buffered handoff
-//    area as ready-made f16 B fragments, with sW and the rescale factor.
-//  * 8 PV warps: warp v owns head-dims [D/8 v, D/8 (v+1)) of the output.  Per
-//    unit it rescales its accumulator once, then for each group runs the exact
-//    INT8 product Wq x Vq (K = the group's 32 tokens) and adds sW x that
-//    result.  Its accumulator covers disjoint dims, so the end of a segment
-//    needs no cross-warp reduction: the QK warps hand over (m, l) and each PV
-//    warp writes its own dims (final output or partial).
-//  * QK of unit i+1 overlaps PV of unit i (the handoff area has two buffers).
+//    score recovery, the group's row maximum m_g, p~ = exp(s - m_g),
+//    W = p~ x sV, sW = max W / 127 and the codes Wq = round(W / sW).  The
+//    codes go to a handoff buffer (unit i uses buffer i % 4) as ready-made f16
+//    B fragments, with sW, m_g and the group's row sums l_g.  No QK warp waits
+//    for another: the group quantization gives the same codes for W scaled
+//    by any positive factor, so each group is quantized against its own
+//    maximum and brought to the common one afterwards.
+//  * 8 PV warps: warp v owns head-dims [D/8 v, D/8 (v+1)) of the output and
+//    keeps the pair's running maximum m.  Per unit, m_new = max(m, m_g), the
+//    accumulator and l are rescaled once by exp(m - m_new), and group g adds
+//    exp(m_g - m_new) sW_g (Wq x Vq) (the exact INT8 product, K = the group's
+//    32 tokens) and exp(m_g - m_new) l_g.  The accumulator covers disjoint
+//    dims, so the end of a segment needs no cross-warp reduction: each PV warp
+//    writes its own dims (final output or partial).
+//  * Ring slots: each QK stream has its own K slot(s), consumed in order, and
+//    the other slots carry V items in unit order, so every slot is refilled
+//    only after its previous item was consumed.
 //  * The INT8 x INT8 contractions run on the f16 tensor path: every int8 code is
 //    exact in f16, every product (<= 127^2) is exact, and every partial sum is
 //    an integer below 2^22 (QK over 256 dims: <= 4,129,024; PV over one group:
@@ -52,10 +60,13 @@ namespace {
 constexpr int kPart = 256;   // the pages' decode partition (debug QK tiles)
 constexpr int kBS = 16;      // block size
 constexpr int kGroup = 32;   // probability group
-constexpr int kQW = 4;       // QK / softmax warps
+constexpr int kQW = 4;       // QK / softmax warps per stream (one unit at a time)
+constexpr int kStreams = 2;  // QK streams: stream s takes the units i with i % 2 == s
 constexpr int kPW = 8;       // PV warps
-constexpr int kProdWarp = kQW + kPW;
-constexpr int kThreads = (kQW + kPW + 1) * 32;
+constexpr int kPVWarp0 = kStreams * kQW;
+constexpr int kProdWarp = kPVWarp0 + kPW;
+constexpr int kThreads = (kProdWarp + 1) * 32;
+constexpr int kHandBufs = 2 * kStreams;  // handoff buffers, unit i uses buffer i % 4
 constexpr int kRows = 8;     // query rows in the MMA N dimension
 constexpr int kMinUnit = 64; // smallest work unit of any variant (grid sizing)
 __host__ __device__ constexpr int kSlotFloats(int D) { return kRows * D + 2 * kRows; }
@@ -76,11 +87,11 @@ struct Geo {
   static constexpr int kDimsPW = D / kPW;                       // head-dims per PV warp
   static constexpr int NDT = kDimsPW / 16;                      // 16-dim MMA tiles per PV warp
   static constexpr int kFrag = BF16 ? 8 : 16;                   // B-fragment bytes per lane
-  // handoff buffer: [kQW][32 lanes] B fragments | sW [kQW][8] | alpha [8] | m [8] | l [kQW][8]
+  // handoff buffer, per group (QK warp) q and row r:
+  // [kQW][32 lanes] B fragments | sW [kQW][8] | m [kQW][8] | l [kQW][8]
   static constexpr int kHSw = kQW * 32 * kFrag;
-  static constexpr int kHAlpha = kHSw + kQW * kRows * 4;
-  static constexpr int kHM = kHAlpha + kRows * 4;
-  static constexpr int kHL = kHM + kRows * 4;
+  static constexpr int kHM = kHSw + kQW * kRows * 4;
+  static constexpr int kHL = kHM + kQW * kRows * 4;
   static constexpr int kHand = kHL + kQW * kRows * 4;
   static constexpr int kStage = kRows * kWTok * EB;             // per-QK-warp code/weight transpose
   static_assert(kGroup == kWTok || BF16, "an INT8 QK warp owns exactly one probability group");
@@ -88,7 +99,7 @@ struct Geo {
 };
 
 struct SmemLayout {
-  size_t ring, hand, mx, stage, bars, ctrl, total;
+  size_t ring, hand, stage, bars, ctrl, total;
 };
 
 template <int D, bool BF16>
@@ -99,13 +110,11 @@ __host__ __device__ inline SmemLayout decode_layout(int nslots) {
   L.ring = off;
   off += (size_t)nslots * Gm::kSlot;
   L.hand = off;
-  off += 2 * (size_t)Gm::kHand;
-  L.mx = off;  // [2][kQW][8] unit row maxima
-  off += 2 * kQW * kRows * sizeof(float);
+  off += (size_t)kHandBufs * Gm::kHand;
   L.stage = off;
-  off += (size_t)kQW * Gm::kStage;
-  L.bars = off;  // full[nslots], empty[nslots], hfull[2], hempty[2]
-  off += (size_t)(2 * nslots + 4) * sizeof(uint64_t);
+  off += (size_t)kStreams * kQW * Gm::kStage;
+  L.bars = off;  // full[nslots], empty[nslots], hfull[4], hempty[4]
+  off += (size_t)(2 * nslots + 2 * kHandBufs) * sizeof(uint64_t);
   L.ctrl = off;
   off += 16 * sizeof(int);
   L.total = off;
@@ -141,6 +150,25 @@ __device__ __forceinline__ void walk_next(Walk& w, const int32_t* seq_lens, int 
 __device__ __forceinline__ int cta_of(long long u, long long U, int N) {
   return (int)(((u + 1) * N + U - 1) / U - 1);
 }
+
+// Ring slots.  Slots [0, 2 kK) hold K items: stream s owns [s kK, (s+1) kK) and
+// fills them with its own units in order (j = i / 2 is unit i's index within
+// its stream), so each K slot is consumed by one stream, in order.  Slots
+// [2 kK, nslots) hold the V items of all units, in order.  Every slot is
+// therefore reused only after its previous item was consumed, which keeps each
+// mbarrier within one phase of its waiters.
+struct Ring {
+  int kK, nV;
+  // A stream releases its K slot right after its QK MMAs, long before its unit
+  // is done, so one K slot per stream (two at 12 slots) keeps it fed; the rest
+  // of the ring holds V items, which wait for the QK warps' handoff.
+  __host__ __device__ explicit Ring(int nslots)
+      : kK(nslots / 6 > 0 ? nslots / 6 : 1), nV(nslots - 2 * (nslots / 6 > 0 ? nslots / 6 : 1)) {}
+  __device__ int kslot(int i) const { return (i % 2) * kK + (i / 2) % kK; }
+  __device__ int kuse(int i) const { return (i / 2) / kK; }  // earlier uses of the slot
+  __device__ int vslot(int i) const { return 2 * kK + i % nV; }
+  __device__ int vuse(int i) const { return i / nV; }
+};
 
 // Bounded pipeline wait.  After a timeout (error 1) or once the CTA aborted,
 // it returns without waiting so every thread still reaches the same barriers.
@@ -249,12 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   const SmemLayout lay = decode_layout<D, BF16>(nslots);
   uint8_t* ring = smem + lay.ring;
   uint8_t* hand = smem + lay.hand;
-  float* mxb = reinterpret_cast<float*>(smem + lay.mx);
   uint8_t* stage = smem + lay.stage;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bars);
   uint64_t* empty = full + nslots;
   uint64_t* hfull = empty + nslots;
-  uint64_t* hempty = hfull + 2;
+  uint64_t* hempty = hfull + kHandBufs;
   int* ctrl = reinterpret_cast<int*>(smem + lay.ctrl);
   volatile int* abort_flag = ctrl + 8;
 
@@ -264,11 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   const int maxL = p.max_blocks * kBS;
 
   if (warp == kProdWarp && lane == 0) {
+    const Ring rg(nslots);
     for (int s = 0; s < nslots; ++s) {
       mbar_init(&full[s], 32);
-      mbar_init(&empty[s], (s & 1) ? kPW : kQW);  // nslots is even: K items in even slots
+      mbar_init(&empty[s], s < kStreams * rg.kK ? kQW : kPW);
     }
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < kHandBufs; ++j) {
       mbar_init(&hfull[j], kQW * 32);
       mbar_init(&hempty[j], kPW);
     }
@@ -297,15 +325,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   }
   if (warp == kProdWarp) {
     constexpr int kKeep = 8;  // chunks of 32 sequences whose unit counts stay in registers
-    int ukeep[kKeep];
+    int ukeep[kKeep], lkeep[kKeep];
     long long total = 0;
     for (int b0 = 0, ck = 0; b0 < B; b0 += 32, ++ck) {
       const int b = b0 + lane;
-      int u = 0;
+      int u = 0, L = 0;
       if (b < B) {
         const int raw = p.seq_lens[b];
         if (raw > maxL) record_error(2);
-        const int L = clamp_len(raw, maxL);
+        L = clamp_len(raw, maxL);
         u = (L + kUnit - 1) / kUnit * Hkv;
         if (L == 0 && b % N == c) {  // empty sequence: zero rows, nothing to merge
           float* o = p.out + (size_t)b * Hq * D;
@@ -315,7 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       }
 #pragma unroll
       for (int k = 0; k < kKeep; ++k)
-        if (k == ck) ukeep[k] = u;
+        if (k == ck) {
+          ukeep[k] = u;
+          lkeep[k] = L;
+        }
       int su = u;
       for (int o = 16; o >= 1; o >>= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
       total += su;
@@ -336,13 +367,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       long long run = 0;
       for (int b0 = 0, ck = 0; b0 < B; b0 += 32, ++ck) {
         const int b = b0 + lane;
-        int u = 0;
+        int u = 0, L = 0;
         if (ck < kKeep) {
 #pragma unroll
           for (int k = 0; k < kKeep; ++k)
-            if (k == ck) u = ukeep[k];
+            if (k == ck) {
+              u = ukeep[k];
+              L = lkeep[k];
+            }
         } else if (b < B) {
-          u = (clamp_len(p.seq_lens[b], maxL) + kUnit - 1) / kUnit * Hkv;
+          L = clamp_len(p.seq_lens[b], maxL);
+          u = (L + kUnit - 1) / kUnit * Hkv;
         }
         int incl = u;
         for (int o = 1; o < 32; o <<= 1) {
@@ -360,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
             ctrl[3] = (int)(local % np);
             ctrl[4] = (int)(ex & 0x7fffffff);
             ctrl[5] = (int)(ex >> 31);
+            ctrl[9] = L;
           }
           break;
         }
@@ -375,86 +411,124 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   w0.kvh = ctrl[2];
   w0.part = ctrl[3];
   w0.ub = (long long)ctrl[4] | ((long long)ctrl[5] << 31);
-  w0.L = clamp_len(p.seq_lens[w0.b], maxL);
+  w0.L = ctrl[9];
   w0.np = (w0.L + kUnit - 1) / kUnit;
   const long long U = (long long)ctrl[6] | ((long long)ctrl[7] << 31);
   const int Nw = ctrl[10];
   const int g = lane >> 2, t = lane & 3;
+  const Ring rg(nslots);
 
   if (warp == kProdWarp) {
     // ================= producer warp =================
     const uint8_t* kc = static_cast<const uint8_t*>(p.k_cache);
     const uint8_t* vc = static_cast<const uint8_t*>(p.v_cache);
     const uint64_t pol = policy_evict_first();
-    Walk wk = w0;
+    // This lane's page of a unit (lanes below the unit's page count), read from
+    // the block table one unit ahead of its use.
+    auto load_blk = [&](const Walk& u, int i) {
+      const int nb = (min(kUnit, u.L - u.part * kUnit) + kBS - 1) / kBS;
+      if (lane >= nb) return -1;
+      if (i == 0 && B == 1 && u.part == spec_part) return spec_blk;
+      return p.block_tables[(size_t)u.b * p.max_blocks + u.part * kBlocksU + lane];
+    };
+    Walk wk = w0, wn = w0;
+    walk_next(wn, p.seq_lens, B, Hkv, maxL, kUnit);
+    int blk_cur = load_blk(wk, 0);
+    int n_k = 0, n_v = 0;  // K and V items issued
     for (int i = 0; i < n_units; ++i) {
+      if (*abort_flag) break;
+      const int blk_nx = (i + 1 < n_units) ? load_blk(wn, i + 1) : -1;  // in flight meanwhile
       const int t0 = wk.part * kUnit;
       const int ntok = min(kUnit, wk.L - t0);
       const int nblk = (ntok + kBS - 1) / kBS;
-      int blk = -1;
-      if (lane < nblk) {
-        blk = (i == 0 && B == 1 && wk.part == spec_part)
-                  ? spec_blk
-                  : p.block_tables[(size_t)wk.b * p.max_blocks + wk.part * kBlocksU + lane];
-        if (blk < 0 || blk >= p.num_blocks) {
-          record_error(2);
-          blk = -1;
-        }
+      int blk = blk_cur;
+      if (lane < nblk && (blk < 0 || blk >= p.num_blocks)) {
+        record_error(2);
+        blk = -1;
       }
       const bool ok = blk >= 0;
       const uint32_t n_pages = __popc(__ballot_sync(0xffffffffu, ok));
-      // K item: pages by bulk copy ...
-      const int kitem = 2 * i, kslot = kitem % nslots;
-      if (kitem >= nslots) pipe_wait(&empty[kslot], ((kitem / nslots) - 1) & 1, abort_flag);
+      // K item: the pages by bulk copy, the unit's (sK, sV) per token by cp.async;
+      // the slot's full barrier waits for both.
+      const int kslot = rg.kslot(i), ku = rg.kuse(i);
+      if (ku > 0) pipe_wait(&empty[kslot], (ku - 1) & 1, abort_flag);
+      if (*abort_flag) break;  // never refill a slot whose previous item was not consumed
       if (lane == 0) mbar_expect_tx(&full[kslot], n_pages * kPage);
       __syncwarp();
+      uint8_t* kdst = ring + (size_t)kslot * kSlot;
       if (ok)
-        bulk_g2s_hint(ring + (size_t)kslot * kSlot + (size_t)lane * kPage,
-                      kc + ((size_t)blk * Hkv + wk.kvh) * kPage, kPage, &full[kslot], pol);
-      // ... and the unit's (sK, sV) per token, loaded now and stored below
-      float2 sc[kUnit / 32];
+        bulk_g2s_hint(kdst + (size_t)lane * kPage, kc + ((size_t)blk * Hkv + wk.kvh) * kPage, kPage, &full[kslot],
+                      pol);
       if constexpr (!BF16) {
+        float* sdst = reinterpret_cast<float*>(kdst + Gm::kPages);
 #pragma unroll
         for (int r = 0; r < kUnit / 32; ++r) {
           const int tok = lane + 32 * r;
           const int bj = __shfl_sync(0xffffffffu, blk, tok / kBS);
           const bool v = tok < ntok && bj >= 0;
           const size_t si = ((size_t)(v ? bj : 0) * kBS + tok % kBS) * Hkv + wk.kvh;
-          sc[r] = v ? make_float2(__ldg(p.k_scale + si), __ldg(p.v_scale + si)) : make_float2(0.f, 0.f);
+          cp_async_4(sdst + 2 * tok, p.k_scale + si, v ? 4u : 0u);
+          cp_async_4(sdst + 2 * tok + 1, p.v_scale + si, v ? 4u : 0u);
         }
+        cp_async_mbar_arrive(&full[kslot]);
       }
+      mbar_arrive(&full[kslot]);
+      ++n_k;
       // V item
-      const int vitem = kitem + 1, vslot = vitem % nslots;
-      if (vitem >= nslots) pipe_wait(&empty[vslot], ((vitem / nslots) - 1) & 1, abort_flag);
+      const int vslot = rg.vslot(i), vu = rg.vuse(i);
+      if (vu > 0) pipe_wait(&empty[vslot], (vu - 1) & 1, abort_flag);
+      if (*abort_flag) break;
       if (lane == 0) mbar_expect_tx(&full[vslot], n_pages * kPage);
       __syncwarp();
       if (ok)
         bulk_g2s_hint(ring + (size_t)vslot * kSlot + (size_t)lane * kPage,
                       vc + ((size_t)blk * Hkv + wk.kvh) * kPage, kPage, &full[vslot], pol);
       mbar_arrive(&full[vslot]);
-      if constexpr (!BF16) {
-        float2* dst = reinterpret_cast<float2*>(ring + (size_t)kslot * kSlot + Gm::kPages);
-#pragma unroll
-        for (int r = 0; r < kUnit / 32; ++r) dst[lane + 32 * r] = sc[r];
+      ++n_v;
+      blk_cur = blk_nx;
+      wk = wn;
+      walk_next(wn, p.seq_lens, B, Hkv, maxL, kUnit);
+    }
+    if (*abort_flag) {
+      // The consumers stopped waiting: hold the CTA (and its shared memory)
+      // until every copy issued into it has landed.  Each slot has at most one
+      // item in flight (a slot is refilled only after its consumers released it),
+      // so waiting for the last phase issued into each slot covers them all.
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      for (int sl = 0; sl < nslots; ++sl) {
+        int uses;
+        if (sl < kStreams * rg.kK) {
+          const int st = sl / rg.kK, r = sl % rg.kK;
+          const int js = n_k > st ? (n_k - st + 1) / 2 : 0;  // this stream's K items issued
+          uses = js > r ? (js - r + rg.kK - 1) / rg.kK : 0;
+        } else {
+          const int v = sl - kStreams * rg.kK;
+          uses = n_v > v ? (n_v - v + rg.nV - 1) / rg.nV : 0;
+        }
+        if (uses > 0) mbar_wait(&full[sl], (uses - 1) & 1);
       }
-      mbar_arrive(&full[kslot]);  // releases the scale stores together with the page bytes
-      walk_next(wk, p.seq_lens, B, Hkv, maxL, kUnit);
     }
     return;
   }
 
-  if (warp < kQW) {
-    // ================= QK / softmax warps =================
+  if (warp < kPVWarp0) {
+    // ================= QK / softmax warps (two streams) =================
+    // Each warp quantizes its group against the group's own row maximum m_g:
+    // p~ = exp(s - m_g), W = p~ sV, sW = max W / 127, Wq = round(W / sW).  The
+    // codes do not depend on a per-group scale factor, so the PV warps bring
+    // every group to the common running maximum later, by exp(m_g - m) folded
+    // into sW; no QK warp waits for another.
+    const int st = warp / kQW, qw = warp % kQW;  // stream; group within the unit
     const float c_scale = p.sm_scale;
-    const int tok0 = warp * kWTok;  // this warp's tokens within a unit
+    const int tok0 = qw * kWTok;  // this warp's tokens within a unit
     uint8_t* stg = stage + warp * Gm::kStage;
     Walk wk = w0;
+    if (st == 1) walk_next(wk, p.seq_lens, B, Hkv, maxL, kUnit);
     int cur_pair = -1;
     uint32_t qf[D / 32][4];    // INT8: converted query fragments
     uint32_t qfb[D / 16][2];   // BF16: query fragments
     float sq[2] = {0.f, 0.f};
-    float mrun[2] = {-INFINITY, -INFINITY}, lw[2] = {0.f, 0.f};
-    for (int i = 0; i < n_units; ++i) {
+    for (int i = st; i < n_units; i += kStreams) {
       const int pair = wk.b * Hkv + wk.kvh;
       if (pair != cur_pair) {
         cur_pair = pair;
@@ -462,24 +536,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
           load_q_frags_bf16<D>(static_cast<const uint16_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qfb);
         } else {
           load_q_frags<D>(static_cast<const int8_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qf);
-        }
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int row = 2 * t + r;
-          if constexpr (!BF16) sq[r] = row < G ? p.q_scale[(size_t)wk.b * Hq + wk.kvh * G + row] : 0.f;
-          mrun[r] = -INFINITY;
-          lw[r] = 0.f;
+          for (int r = 0; r < 2; ++r) {
+            const int row = 2 * t + r;
+            sq[r] = row < G ? p.q_scale[(size_t)wk.b * Hq + wk.kvh * G + row] : 0.f;
+          }
         }
       }
-      Walk nx = wk;
-      walk_next(nx, p.seq_lens, B, Hkv, maxL, kUnit);
-      const bool seg_end = (i == n_units - 1) || (nx.b * Hkv + nx.kvh != pair);
       const int ntok = min(kUnit, wk.L - wk.part * kUnit);
       const bool active = tok0 < ntok;
 
       // ---- K item: QK of this warp's tokens, and their scales ----
-      const int kitem = 2 * i, kslot = kitem % nslots;
-      pipe_wait(&full[kslot], (kitem / nslots) & 1, abort_flag);
+      const int kslot = rg.kslot(i);
+      pipe_wait(&full[kslot], rg.kuse(i) & 1, abort_flag);
       const uint8_t* kb = ring + (size_t)kslot * kSlot;
       float acc[2][4];
 #pragma unroll
@@ -488,9 +557,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         for (int e = 0; e < 4; ++e) acc[m][e] = 0.f;
       if (active) {
         if constexpr (BF16)
-          qk_warp_bf16<D>(kb, warp, lane, qfb, acc[0]);
+          qk_warp_bf16<D>(kb, qw, lane, qfb, acc[0]);
         else
-          qk_warp<D>(reinterpret_cast<const int8_t*>(kb), warp, lane, qf, acc);
+          qk_warp<D>(reinterpret_cast<const int8_t*>(kb), qw, lane, qf, acc);
       }
       float sk[4], sv[4];  // tokens g, g+8 of this warp's blocks 0 and 1
       if constexpr (!BF16) {
@@ -507,9 +576,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[kslot]);
 
-      // ---- scores and the CTA-wide running row maximum ----
+      // ---- scores and the group's row maximum ----
       float s[MT][4];
-      float lmax[2] = {-INFINITY, -INFINITY};
+      float gm[2] = {-INFINITY, -INFINITY};
 #pragma unroll
       for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -523,39 +592,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
               sc = __fmul_rn(__fmul_rn(__fmul_rn(acc[m][e], sq[e & 1]), sk[2 * m + (e >> 1)]), c_scale);
           }
           s[m][e] = sc;
-          lmax[e & 1] = fmaxf(lmax[e & 1], sc);
+          gm[e & 1] = fmaxf(gm[e & 1], sc);
         }
 #pragma unroll
       for (int r = 0; r < 2; ++r)
 #pragma unroll
-        for (int off = 4; off <= 16; off <<= 1)
-          lmax[r] = fmaxf(lmax[r], __shfl_xor_sync(0xffffffffu, lmax[r], off));
-      float* mxu = mxb + (i & 1) * (kQW * kRows);
-      if (g == 0) {
-        mxu[warp * kRows + 2 * t] = lmax[0];
-        mxu[warp * kRows + 2 * t + 1] = lmax[1];
-      }
-      named_bar_sync(1, kQW * 32);
-      float alpha[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float um = -INFINITY;
-#pragma unroll
-        for (int w2 = 0; w2 < kQW; ++w2) um = fmaxf(um, mxu[w2 * kRows + 2 * t + r]);
-        const float mn = fmaxf(mrun[r], um);
-        alpha[r] = (mrun[r] == -INFINITY) ? 0.f : expf(mrun[r] - mn);
-        mrun[r] = mn;
-        lw[r] *= alpha[r];
-      }
+        for (int off = 4; off <= 16; off <<= 1) gm[r] = fmaxf(gm[r], __shfl_xor_sync(0xffffffffu, gm[r], off));
 
       // ---- weights: BF16 p~; INT8 W = p~ sV, sW, codes ----
-      float swv[2] = {0.f, 0.f};
+      float swv[2] = {0.f, 0.f}, lg[2] = {0.f, 0.f};
       if constexpr (BF16) {
         uint16_t* pw = reinterpret_cast<uint16_t*>(stg);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float pe = (s[0][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[0][e], mrun[e & 1]));
-          lw[e & 1] += pe;
+          const float pe = (s[0][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[0][e], gm[e & 1]));
+          lg[e & 1] += pe;
           pw[(2 * t + (e & 1)) * 16 + g + 8 * (e >> 1)] = __bfloat16_as_ushort(__float2bfloat16_rn(pe));
         }
       } else {
@@ -564,8 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         for (int m = 0; m < 2; ++m)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float pe = (s[m][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[m][e], mrun[e & 1]));
-            lw[e & 1] += pe;
+            const float pe = (s[m][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[m][e], gm[e & 1]));
+            lg[e & 1] += pe;
             w[m][e] = __fmul_rn(pe, sv[2 * m + (e >> 1)]);
             A[e & 1] = fmaxf(A[e & 1], w[m][e]);
           }
@@ -573,74 +624,79 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         for (int r = 0; r < 2; ++r)
 #pragma unroll
           for (int off = 4; off <= 16; off <<= 1) A[r] = fmaxf(A[r], __shfl_xor_sync(0xffffffffu, A[r], off));
-        float inv[2];
+        // sW = A / 127 and the codes round(W / sW), both IEEE fp32 quotients
+        // (W / sW by Markstein's method, one reciprocal per row)
+        float ysw[2];
+        bool tiny[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           swv[r] = __fdiv_rn(A[r], 127.0f);
-          inv[r] = A[r] > 0.f ? __fdiv_rn(127.0f, A[r]) : 0.f;
+          ysw[r] = __frcp_rn(swv[r]);
+          tiny[r] = swv[r] < kTinyDivisor;
         }
-        // codes -> [row][token] bytes, read back below as PV B fragments
+        // codes -> [row][token] bytes, read back below as PV B fragments.
+        // W / sW <= A / RN(A / 127) < 127.5, so no code needs clamping.
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int q = min(127, __float2int_rn(w[m][e] * inv[e & 1]));
-            stg[(2 * t + (e & 1)) * kGroup + 16 * m + g + 8 * (e >> 1)] = (uint8_t)(int8_t)q;
+            const int r = e & 1;
+            const int q = A[r] > 0.f ? __float2int_rn(div_shared(w[m][e], swv[r], ysw[r], tiny[r])) : 0;
+            stg[(2 * t + r) * kGroup + 16 * m + g + 8 * (e >> 1)] = (uint8_t)(int8_t)q;
           }
       }
       __syncwarp();
 
-      // ---- hand the unit over to the PV warps ----
-      if (i >= 2) pipe_wait(&hempty[i & 1], ((i >> 1) - 1) & 1, abort_flag);
-      uint8_t* hb = hand + (size_t)(i & 1) * Gm::kHand;
+      // ---- hand the group over to the PV warps ----
+      const int hbi = i % kHandBufs;
+      if (i >= kHandBufs) pipe_wait(&hempty[hbi], ((i / kHandBufs) - 1) & 1, abort_flag);
+      uint8_t* hb = hand + (size_t)hbi * Gm::kHand;
       if constexpr (BF16) {
         uint2 f;
         f.x = *reinterpret_cast<const uint32_t*>(stg + g * 32 + 4 * t);
         f.y = *reinterpret_cast<const uint32_t*>(stg + g * 32 + 16 + 4 * t);
-        reinterpret_cast<uint2*>(hb)[warp * 32 + lane] = f;
+        reinterpret_cast<uint2*>(hb)[qw * 32 + lane] = f;
       } else {
         uint32_t b4[4];
         s8b_to_f16(*reinterpret_cast<const uint32_t*>(stg + g * kGroup + 4 * t),
                    *reinterpret_cast<const uint32_t*>(stg + g * kGroup + 16 + 4 * t), b4);
-        reinterpret_cast<uint4*>(hb)[warp * 32 + lane] = make_uint4(b4[0], b4[1], b4[2], b4[3]);
+        reinterpret_cast<uint4*>(hb)[qw * 32 + lane] = make_uint4(b4[0], b4[1], b4[2], b4[3]);
       }
-      float* hsw = reinterpret_cast<float*>(hb + Gm::kHSw);
-      float* hal = reinterpret_cast<float*>(hb + Gm::kHAlpha);
-      float* hm = reinterpret_cast<float*>(hb + Gm::kHM);
-      float* hl = reinterpret_cast<float*>(hb + Gm::kHL);
+      // the group's row sums of p~ (relative to m_g)
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int off = 4; off <= 16; off <<= 1) lg[r] += __shfl_xor_sync(0xffffffffu, lg[r], off);
       if (g == 0) {
+        float* hsw = reinterpret_cast<float*>(hb + Gm::kHSw);
+        float* hm = reinterpret_cast<float*>(hb + Gm::kHM);
+        float* hl = reinterpret_cast<float*>(hb + Gm::kHL);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          hsw[warp * kRows + 2 * t + r] = swv[r];
-          if (warp == 0) hal[2 * t + r] = alpha[r];
+          hsw[qw * kRows + 2 * t + r] = swv[r];
+          hm[qw * kRows + 2 * t + r] = gm[r];
+          hl[qw * kRows + 2 * t + r] = lg[r];
         }
       }
-      if (seg_end) {
-        float ls[2] = {lw[0], lw[1]};
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int off = 4; off <= 16; off <<= 1) ls[r] += __shfl_xor_sync(0xffffffffu, ls[r], off);
-        if (g == 0) {
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            hl[warp * kRows + 2 * t + r] = ls[r];
-            if (warp == 0) hm[2 * t + r] = mrun[r];
-          }
-        }
-      }
-      mbar_arrive(&hfull[i & 1]);  // every thread: releases its own stores
-      wk = nx;
+      mbar_arrive(&hfull[hbi]);  // every thread: releases its own stores
+      walk_next(wk, p.seq_lens, B, Hkv, maxL, kUnit);
+      walk_next(wk, p.seq_lens, B, Hkv, maxL, kUnit);
     }
     return;
   }
 
   // ================= PV warps =================
-  const int pv_w = warp - kQW;
+  // One running maximum m per pair, advanced in unit order: per unit,
+  // m_new = max(m, m_g over the unit's groups), o and l are rescaled by
+  // exp(m - m_new), and group q adds exp(m_g - m_new) * sW_g * (Wq x Vq) to o and
+  // exp(m_g - m_new) * l_g to l.
+  const int pv_w = warp - kPVWarp0;
   const int mi = lane >> 3, ri = lane & 7;
-  Walk wk = w0;
+  Walk wk = w0, w1 = w0;
+  walk_next(w1, p.seq_lens, B, Hkv, maxL, kUnit);
   int cur_pair = -1;
   float o[NDT][4];
+  float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
   for (int i = 0; i < n_units; ++i) {
     const int pair = wk.b * Hkv + wk.kvh;
     if (pair != cur_pair) {
@@ -649,34 +705,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       for (int dt = 0; dt < NDT; ++dt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) o[dt][e] = 0.f;
-    }
-    Walk nx = wk;
-    walk_next(nx, p.seq_lens, B, Hkv, maxL, kUnit);
-    const bool seg_end = (i == n_units - 1) || (nx.b * Hkv + nx.kvh != pair);
-    const int ntok = min(kUnit, wk.L - wk.part * kUnit);
-
-    const uint8_t* hb = hand + (size_t)(i & 1) * Gm::kHand;
-    pipe_wait(&hfull[i & 1], (i >> 1) & 1, abort_flag);
-    const float* hsw = reinterpret_cast<const float*>(hb + Gm::kHSw);
-    const float* hal = reinterpret_cast<const float*>(hb + Gm::kHAlpha);
-    const float a0 = hal[2 * t], a1 = hal[2 * t + 1];
-    if (a0 != 1.f || a1 != 1.f) {
 #pragma unroll
-      for (int dt = 0; dt < NDT; ++dt) {
-        o[dt][0] *= a0;
-        o[dt][1] *= a1;
-        o[dt][2] *= a0;
-        o[dt][3] *= a1;
+      for (int r = 0; r < 2; ++r) {
+        mrun[r] = -INFINITY;
+        lrun[r] = 0.f;
+      }
+    }
+    const bool seg_end = (i == n_units - 1) || (w1.b * Hkv + w1.kvh != pair);
+    const int ntok = min(kUnit, wk.L - wk.part * kUnit);
+    const int ng = (ntok + kWTok - 1) / kWTok;  // groups holding tokens
+
+    const int hbi = i % kHandBufs;
+    const uint8_t* hb = hand + (size_t)hbi * Gm::kHand;
+    pipe_wait(&hfull[hbi], (i / kHandBufs) & 1, abort_flag);
+    const float* hsw = reinterpret_cast<const float*>(hb + Gm::kHSw);
+    const float* hm = reinterpret_cast<const float*>(hb + Gm::kHM);
+    const float* hl = reinterpret_cast<const float*>(hb + Gm::kHL);
+    // ---- the unit's running maximum and the groups' factors ----
+    float fs[kQW][2];  // exp(m_g - m_new) * sW_g (INT8) or exp(m_g - m_new) (BF16)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float mg[kQW];
+      float mn = mrun[r];
+#pragma unroll
+      for (int q = 0; q < kQW; ++q) {
+        mg[q] = q < ng ? hm[q * kRows + 2 * t + r] : -INFINITY;
+        mn = fmaxf(mn, mg[q]);
+      }
+      const float alpha = (mrun[r] == -INFINITY) ? 0.f : expf(mrun[r] - mn);
+      float l = lrun[r] * alpha;
+#pragma unroll
+      for (int q = 0; q < kQW; ++q) {
+        const float f = (mg[q] == -INFINITY) ? 0.f : expf(mg[q] - mn);
+        if (q < ng) l = fmaf(hl[q * kRows + 2 * t + r], f, l);
+        fs[q][r] = BF16 ? f : f * (q < ng ? hsw[q * kRows + 2 * t + r] : 0.f);
+      }
+      lrun[r] = l;
+      mrun[r] = mn;
+      if (alpha != 1.f) {
+#pragma unroll
+        for (int dt = 0; dt < NDT; ++dt) {
+          o[dt][r] *= alpha;
+          o[dt][2 + r] *= alpha;
+        }
       }
     }
 
     // ---- V item: this warp's head-dims, every group of the unit ----
-    const int vitem = 2 * i + 1, vslot = vitem % nslots;
-    pipe_wait(&full[vslot], (vitem / nslots) & 1, abort_flag);
+    const int vslot = rg.vslot(i);
+    pipe_wait(&full[vslot], rg.vuse(i) & 1, abort_flag);
     const uint8_t* vb = ring + (size_t)vslot * kSlot;
 #pragma unroll
     for (int q = 0; q < kQW; ++q) {
-      if (q * kWTok >= ntok) break;
+      if (q >= ng) break;
       if constexpr (BF16) {
         // A = V^T of page q [D][16 tokens]: matrices (dims 0-7 | 8-15) x (tokens 0-7 | 8-15)
         const uint2 f = reinterpret_cast<const uint2*>(hb)[q * 32 + lane];
@@ -686,13 +767,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         for (int dt = 0; dt < NDT; ++dt) {
           uint32_t a[4];
           ldmatrix_x4(a, vrow + dt * 16 * 32);
-          mma_bf16_16816(o[dt], a, f.x, f.y);
+          float pv[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_bf16_16816(pv, a, f.x, f.y);
+          o[dt][0] = fmaf(pv[0], fs[q][0], o[dt][0]);
+          o[dt][1] = fmaf(pv[1], fs[q][1], o[dt][1]);
+          o[dt][2] = fmaf(pv[2], fs[q][0], o[dt][2]);
+          o[dt][3] = fmaf(pv[3], fs[q][1], o[dt][3]);
         }
       } else {
         // A = V^T of the group's pages 2q, 2q+1: (dims 0-7 | 8-15) x (page 2q | 2q+1)
         const uint4 f = reinterpret_cast<const uint4*>(hb)[q * 32 + lane];
         const uint32_t bq[4] = {f.x, f.y, f.z, f.w};
-        const float s0 = hsw[q * kRows + 2 * t], s1 = hsw[q * kRows + 2 * t + 1];
         const uint8_t* vrow = vb + (size_t)(2 * q + (mi >> 1)) * kPage + (size_t)(pv_w * Gm::kDimsPW) * 16 +
                               (ri + 8 * (mi & 1)) * 16;
 #pragma unroll
@@ -701,10 +786,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
           ldmatrix_x4(a, vrow + dt * 16 * 16);
           float pv[4] = {0.f, 0.f, 0.f, 0.f};
           mma_s8a_f16b(pv, a, bq);
-          o[dt][0] = fmaf(pv[0], s0, o[dt][0]);
-          o[dt][1] = fmaf(pv[1], s1, o[dt][1]);
-          o[dt][2] = fmaf(pv[2], s0, o[dt][2]);
-          o[dt][3] = fmaf(pv[3], s1, o[dt][3]);
+          o[dt][0] = fmaf(pv[0], fs[q][0], o[dt][0]);
+          o[dt][1] = fmaf(pv[1], fs[q][1], o[dt][1]);
+          o[dt][2] = fmaf(pv[2], fs[q][0], o[dt][2]);
+          o[dt][3] = fmaf(pv[3], fs[q][1], o[dt][3]);
         }
       }
     }
@@ -713,17 +798,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
 
     // ---- end of this CTA's share of the (sequence, KV head) pair ----
     if (seg_end) {
-      const float* hm = reinterpret_cast<const float*>(hb + Gm::kHM);
-      const float* hl = reinterpret_cast<const float*>(hb + Gm::kHL);
-      float lsum[2], mrow[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        float l = 0.f;
-#pragma unroll
-        for (int w2 = 0; w2 < kQW; ++w2) l += hl[w2 * kRows + 2 * t + r];  // fixed order
-        lsum[r] = l;
-        mrow[r] = hm[2 * t + r];
-      }
       const long long Up = wk.ub + (long long)wk.kvh * wk.np;
       const int cf = cta_of(Up, U, Nw), cl = cta_of(Up + wk.np - 1, U, Nw);
       // the CTA holding the pair's first unit records whether a merge is needed
@@ -731,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       const int d0 = pv_w * Gm::kDimsPW;
       if (cf == cl) {
         float* dst = p.out + ((size_t)wk.b * Hq + wk.kvh * G) * D;
-        const float inv0 = 1.0f / lsum[0], inv1 = 1.0f / lsum[1];
+        const float inv0 = 1.0f / lrun[0], inv1 = 1.0f / lrun[1];
 #pragma unroll
         for (int dt = 0; dt < NDT; ++dt)
 #pragma unroll
@@ -752,28 +826,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         if (pv_w == 0 && g == 0) {
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            part[kRows * D + 2 * t + r] = mrow[r];
-            part[kRows * D + kRows + 2 * t + r] = lsum[r];
+            part[kRows * D + 2 * t + r] = mrun[r];
+            part[kRows * D + kRows + 2 * t + r] = lrun[r];
           }
         }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&hempty[i & 1]);
-    wk = nx;
+    if (lane == 0) mbar_arrive(&hempty[hbi]);
+    wk = w1;
+    walk_next(w1, p.seq_lens, B, Hkv, maxL, kUnit);
   }
 }
 
-// Log-sum-exp merge of the partials of pairs that span CTAs: one CTA per
-// (pair, query row).  Thread (slice, column) walks every SL-th segment of one
-// float4 column and keeps its own running (max, denominator, sum) -- all its
-// loads are independent, so they are in flight together -- then the slices are
-// combined in a fixed order.
+// Log-sum-exp merge of the partials of pairs that span CTAs: one CTA of 512
+// threads per (pair, query row).  Thread (slice, column) owns every SL-th
+// segment of one float4 column.  It loads a batch of kMB segments (value, m, l)
+// at once -- independent loads, all in flight together -- then folds them into
+// its running (max, denominator, sum); the slices are combined in a fixed order.
 constexpr int kMaxSeg = 1024;
+constexpr int kMergeThreads = 512;
+constexpr int kMB = 8;
 
 template <int D>
-__global__ void __launch_bounds__(256) decode_merge_kernel(DecodeParams p) {
-  constexpr int COLS = D / 4, SL = 256 / COLS;
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
+  constexpr int COLS = D / 4, SL = kMergeThreads / COLS;
   __shared__ float4 red[SL][COLS];
   __shared__ float msh[SL], dsh[SL];
   griddep_wait();
@@ -791,19 +868,43 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeParams p) {
   const float* part0 = p.ws_part + (size_t)(pair + cf) * kSlotFloats(D);
   float m = -INFINITY, den = 0.f;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int s = slice; s < nseg; s += SL) {
-    const float* ps = part0 + (size_t)s * kSlotFloats(D);
-    const float ms = ps[kRows * D + row], ls = ps[kRows * D + kRows + row];
-    const float4 v = *reinterpret_cast<const float4*>(ps + row * D + 4 * col);
-    const float mn = fmaxf(m, ms);
-    const float f = expf(m - mn), e = expf(ms - mn);
-    a.x = fmaf(v.x, e, a.x * f);
-    a.y = fmaf(v.y, e, a.y * f);
-    a.z = fmaf(v.z, e, a.z * f);
-    a.w = fmaf(v.w, e, a.w * f);
-    den = fmaf(ls, e, den * f);
-    m = mn;
+  for (int s0 = slice; s0 < nseg; s0 += SL * kMB) {
+    float4 v[kMB];
+    float ms[kMB], ls[kMB];
+#pragma unroll
+    for (int j = 0; j < kMB; ++j) {
+      const int s = s0 + j * SL;
+      if (s < nseg) {
+        const float* ps = part0 + (size_t)s * kSlotFloats(D);
+        v[j] = *reinterpret_cast<const float4*>(ps + row * D + 4 * col);
+        ms[j] = ps[kRows * D + row];
+        ls[j] = ps[kRows * D + kRows + row];
+      } else {
+        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        ms[j] = -INFINITY;
+        ls[j] = 0.f;
+      }
+    }
+    float mb = m;
+#pragma unroll
+    for (int j = 0; j < kMB; ++j) mb = fmaxf(mb, ms[j]);
+    if (mb == -INFINITY) continue;
+    const float f = expf(m - mb);
+    a.x *= f;
+    a.y *= f;
+    a.z *= f;
+    a.w *= f;
+    den *= f;
+#pragma unroll
+    for (int j = 0; j < kMB; ++j) {
+      const float e = expf(ms[j] - mb);  // 0 for the padding entries
+      a.x = fmaf(v[j].x, e, a.x);
+      a.y = fmaf(v[j].y, e, a.y);
+      a.z = fmaf(v[j].z, e, a.z);
+      a.w = fmaf(v[j].w, e, a.w);
+      den = fmaf(ls[j], e, den);
+    }
+    m = mb;
   }
   red[slice][col] = a;
   if (col == 0) {
@@ -902,10 +1003,10 @@ int max_smem_optin(int device) {
   return g_max_smem[device];
 }
 
-// Deepest ring that fits (an even number of slots: K items in even slots).
+// Deepest ring that fits (at least one K slot per stream and two V slots).
 template <int D, bool BF16>
 int pick_slots(int smem_limit) {
-  for (int ns = 12; ns >= 2; ns -= 2)
+  for (int ns = 12; ns >= 4; ns -= 2)
     if (decode_layout<D, BF16>(ns).total <= (size_t)smem_limit) return ns;
   return 0;
 }
@@ -928,7 +1029,7 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   }
   cudaError_t e = launch_pdl(decode_kernel<D, BF16>, dim3(p.grid), dim3(kThreads), smem, stream, p, ns);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_merge_kernel<D>, dim3(p.B * p.Hkv * p.G), dim3(256), 0, stream, p);
+  return launch_pdl(decode_merge_kernel<D>, dim3(p.B * p.Hkv * p.G), dim3(kMergeThreads), 0, stream, p);
 }
 
 }  // namespace

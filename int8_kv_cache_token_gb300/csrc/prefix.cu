@@ -275,17 +275,24 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
         A[h2] = fmaxf(A[h2], __shfl_xor_sync(0xffffffffu, A[h2], 1));
         A[h2] = fmaxf(A[h2], __shfl_xor_sync(0xffffffffu, A[h2], 2));
       }
-      float sW[2], inv[2];
+      // sW = A / 127 and the codes round(W / sW), both IEEE fp32 quotients (W / sW
+      // by Markstein's method); W / sW <= A / RN(A / 127) < 127.5, no clamp needed
+      float sW[2], ysw[2];
+      bool tiny[2];
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         sW[h2] = __fdiv_rn(A[h2], 127.0f);
-        inv[h2] = A[h2] > 0.f ? __fdiv_rn(127.0f, A[h2]) : 0.f;
+        ysw[h2] = __frcp_rn(sW[h2]);
+        tiny[h2] = sW[h2] < kTinyDivisor;
       }
       float q[4][4];
 #pragma unroll
       for (int n = 0; n < 4; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) q[n][e] = fminf(127.f, rintf(w[n][e] * inv[e >> 1]));
+        for (int e = 0; e < 4; ++e) {
+          const int h2 = e >> 1;
+          q[n][e] = A[h2] > 0.f ? rintf(div_shared(w[n][e], sW[h2], ysw[h2], tiny[h2])) : 0.f;
+        }
       // A operand of PV in f16 (exact integers): k16 MMA 1 takes the group's keys
       // 0..15, MMA 2 keys 16..31, with logical k (2t, 2t+1 | 2t+8, 2t+9) holding
       // keys (4t, 4t+1 | 4t+2, 4t+3) -- the order s8b_to_f16 gives the V fragments.

@@ -26,18 +26,6 @@ namespace {
 constexpr int kTileTokens = 16;
 constexpr int kMaxHkvProducer = 8;
 
-// x / s correctly rounded (the IEEE quotient), for one divisor s shared by many
-// x: Markstein's method.  With y = RN(1/s), q = RN(x * y) and the residual
-// r = x - s * q (exact in one FMA), RN(q + r * y) is the correctly rounded
-// quotient provided nothing overflows or underflows; divisors below 2^-100 use
-// the plain division instead.
-__device__ __forceinline__ float div_shared(float x, float s, float y, bool tiny) {
-  if (tiny) return __fdiv_rn(x, s);
-  const float q = __fmul_rn(x, y);
-  const float r = __fmaf_rn(-s, q, x);
-  return __fmaf_rn(r, y, q);
-}
-
 // Quantize the vector whose 16-element slice this lane holds (lane c of a group
 // of LPV lanes holds elements 16c .. 16c+15, as raw bf16 words in `raw`).
 // Every lane of the warp must call this (the absmax reduction shuffles across
@@ -58,7 +46,7 @@ __device__ __forceinline__ float quantize_slice(const uint4 (&raw)[2], bool acti
   for (int o = LPV / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float scale = __fdiv_rn(amax, 127.0f);
   const float y = __frcp_rn(scale);
-  const bool tiny = scale < 7.8886091e-31f;  // 2^-100
+  const bool tiny = scale < kTinyDivisor;
   // Codes: round half to even by adding 1.5 * 2^23 (the fp32 sum keeps the
   // integer part of x / scale in its low mantissa bits, so its low byte is the
   // two's-complement code).  |x / scale| <= amax / RN(amax / 127) < 127.5, so no
@@ -92,34 +80,6 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(ProducerParams p) {
   const int t0 = blockIdx.x * kTileTokens;
   const int ntok = min(kTileTokens, p.T - t0);
   const long long pool_slots = (long long)p.num_blocks * BS;
-  const int Hkv = p.Hkv, Hq = p.q ? p.Hq : 0;
-  // Only the tile's real tokens: vector vi is (token vi / per_tok, entry vi % per_tok),
-  // entries 0..Hkv-1 = K heads, Hkv..2Hkv-1 = V heads, then the query heads.
-  const int per_tok = 2 * Hkv + Hq;
-  const int nvec = ntok * per_tok;
-  const int gi = lane / LPV, c = lane % LPV;
-  // U warp passes at a time: their loads are issued before either is used, so
-  // two global-load latencies overlap instead of queuing one per pass.
-  constexpr int U = 2;
-  auto load_batch = [&](int base0, uint4 (&raw)[U][2]) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int vi = base0 + u * 8 * VPW + gi;
-      raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
-      if (vi < nvec) {  // the input rows exist whatever the slot; the slot only gates the stores
-        const int tok = vi / per_tok, r = vi % per_tok;
-        const int t = t0 + tok;
-        const uint16_t* src = (r < Hkv       ? p.k + ((size_t)t * Hkv + r) * D
-                               : r < 2 * Hkv ? p.v + ((size_t)t * Hkv + (r - Hkv)) * D
-                                             : p.q + ((size_t)t * Hq + (r - 2 * Hkv)) * D) + 16 * c;
-        raw[u][0] = __ldg(reinterpret_cast<const uint4*>(src));
-        raw[u][1] = __ldg(reinterpret_cast<const uint4*>(src + 8));
-      }
-    }
-  };
-  // The first batch's loads go out before the slot indices are known.
-  uint4 raw[U][2];
-  load_batch(warp * VPW, raw);
   if (tid < kTileTokens) {
     int s = -1;
     if (tid < ntok) {
@@ -137,10 +97,19 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(ProducerParams p) {
 #pragma unroll
   for (int i = 1; i < kTileTokens; ++i) aligned = aligned && (s_slot[i] == s_slot[0] + i);
 
+  const int Hkv = p.Hkv, Hq = p.q ? p.Hq : 0;
+  // Only the tile's real tokens: vector vi is (token vi / per_tok, entry vi % per_tok),
+  // entries 0..Hkv-1 = K heads, Hkv..2Hkv-1 = V heads, then the query heads.
+  const int per_tok = 2 * Hkv + Hq;
+  const int nvec = ntok * per_tok;
+  const int gi = lane / LPV, c = lane % LPV;
+  // U warp passes at a time: their loads are issued before either is used, so
+  // two global-load latencies overlap instead of queuing one per pass.
+  constexpr int U = 2;
   for (int base0 = warp * VPW; base0 < nvec; base0 += 8 * VPW * U) {
-    if (base0 != warp * VPW) load_batch(base0, raw);
     bool act[U];
     int kinds[U], toks[U], hs[U], slots[U];
+    uint4 raw[U][2];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int vi = base0 + u * 8 * VPW + gi;
@@ -155,6 +124,15 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(ProducerParams p) {
       toks[u] = tok;
       hs[u] = h;
       slots[u] = slot;
+      raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
+      if (active) {
+        const int t = t0 + tok;
+        const uint16_t* src = (kind == 0 ? p.k + ((size_t)t * Hkv + h) * D
+                               : kind == 1 ? p.v + ((size_t)t * Hkv + h) * D
+                                           : p.q + ((size_t)t * Hq + h) * D) + 16 * c;
+        raw[u][0] = __ldg(reinterpret_cast<const uint4*>(src));
+        raw[u][1] = __ldg(reinterpret_cast<const uint4*>(src + 8));
+      }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {

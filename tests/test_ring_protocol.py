@@ -1,0 +1,127 @@
+"""The decode kernel's shared-memory ring protocol, checked on the CPU.
+
+The decode kernel moves K/V items through ring slots guarded by mbarriers
+whose waits see only the parity of a phase.  A waiter that falls two phases
+behind a barrier would pass on an old phase and read a slot whose copy has not
+landed.  This model replays the protocol with randomized agent speeds and
+out-of-order copy completion:
+  * a producer fills K and V slots (refilling a slot only after its previous
+    item was released);
+  * two QK streams take the even and odd units, each through its own K slots;
+  * the PV warps take every unit's V slot and its handoff buffer (unit i uses
+    buffer i % 4).
+The slot and phase formulas are the kernel's (struct Ring in decode.cu).  The
+model also shows that one ring whose K slots alternate between the two streams
+does fail (a stream reads a slot before its copy lands), which is why each
+stream has its own K slots.
+"""
+import random
+
+import pytest
+
+
+class Bar:
+    def __init__(self):
+        self.n = 0  # completed phases (one arrival completes a phase in this model)
+
+    def arrive(self):
+        self.n += 1
+
+    def passes(self, phase):  # try_wait.parity(phase & 1)
+        return (self.n & 1) != (phase & 1)
+
+
+def kernel_ring(nslots):
+    kK = max(1, nslots // 6)
+    nV = nslots - 2 * kK
+    return dict(kslot=lambda i: (i % 2) * kK + (i // 2) % kK, kuse=lambda i: (i // 2) // kK,
+                vslot=lambda i: 2 * kK + i % nV, vuse=lambda i: i // nV)
+
+
+def shared_ring(nslots):
+    return dict(kslot=lambda i: (2 * i) % nslots, kuse=lambda i: (2 * i) // nslots,
+                vslot=lambda i: (2 * i + 1) % nslots, vuse=lambda i: (2 * i + 1) // nslots)
+
+
+def simulate(n_units, nslots, ring, seed, nhb=4):
+    rnd = random.Random(seed)
+    kslot, kuse, vslot, vuse = ring["kslot"], ring["kuse"], ring["vslot"], ring["vuse"]
+    full = [Bar() for _ in range(nslots)]
+    empty = [Bar() for _ in range(nslots)]
+    hfull = [Bar() for _ in range(nhb)]
+    hempty = [Bar() for _ in range(nhb)]
+    content, hand, pending = [None] * nslots, [None] * nhb, []
+
+    def producer():
+        for i in range(n_units):
+            for kind, s, u in (("K", kslot(i), kuse(i)), ("V", vslot(i), vuse(i))):
+                if u > 0:
+                    while not empty[s].passes(u - 1):
+                        yield
+                pending.append((s, (kind, i)))
+                yield
+
+    def qk(st):
+        for i in range(st, n_units, 2):
+            s, u = kslot(i), kuse(i)
+            while not full[s].passes(u):
+                yield
+            assert content[s] == ("K", i), f"QK stream {st}, unit {i} read {content[s]} from slot {s}"
+            yield
+            empty[s].arrive()
+            hb = i % nhb
+            if i >= nhb:
+                while not hempty[hb].passes(i // nhb - 1):
+                    yield
+            hand[hb] = i
+            hfull[hb].arrive()
+            yield
+
+    def pv():
+        for i in range(n_units):
+            hb = i % nhb
+            while not hfull[hb].passes(i // nhb):
+                yield
+            assert hand[hb] == i, f"PV unit {i} read handoff {hand[hb]}"
+            s, u = vslot(i), vuse(i)
+            while not full[s].passes(u):
+                yield
+            assert content[s] == ("V", i), f"PV unit {i} read {content[s]} from slot {s}"
+            yield
+            empty[s].arrive()
+            hempty[hb].arrive()
+            yield
+
+    agents = {"producer": producer(), "qk0": qk(0), "qk1": qk(1), "pv": pv()}
+    speed = {k: rnd.uniform(0.1, 1.0) for k in agents}
+    for _ in range(200000):
+        if not agents and not pending:
+            return
+        if pending and rnd.random() < 0.3:  # some issued copy lands (any order)
+            s, item = pending.pop(rnd.randrange(len(pending)))
+            content[s] = item
+            full[s].arrive()
+            continue
+        names = list(agents)
+        k = rnd.choices(names, weights=[speed[n] for n in names])[0]
+        try:
+            next(agents[k])
+        except StopIteration:
+            del agents[k]
+    raise AssertionError("deadlock")
+
+
+@pytest.mark.parametrize("nslots", [4, 6, 8, 12])
+def test_kernel_ring_never_reads_an_unlanded_slot(nslots):
+    for seed in range(400):
+        simulate(random.Random(seed).randint(1, 30), nslots, kernel_ring(nslots), seed)
+
+
+def test_alternating_k_slots_do_race():
+    failures = 0
+    for seed in range(1500):
+        try:
+            simulate(random.Random(seed).randint(1, 20), 6, shared_ring(6), seed)
+        except AssertionError:
+            failures += 1
+    assert failures > 0
