@@ -172,11 +172,13 @@ struct Ring {
 
 // Bounded pipeline wait.  After a timeout (error 1) or once the CTA aborted,
 // it returns without waiting so every thread still reaches the same barriers.
+// A waiting warp sleeps inside try_wait (up to 20 us per try) instead of
+// spinning, so it takes no issue slots from the warps that have work.
 __device__ __forceinline__ void pipe_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return;
   if (*abort_flag) return;
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (*abort_flag) return;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       record_error(1);
