@@ -5,13 +5,15 @@ Workload (N = 1): single-sequence decode with 24 query / 4 KV heads, head_dim
 256, block size 16, histories 8192, 16384 and 32768 (K with 4 outlier channels
 per KV head x20, V N(0,1), seeded), i.e. the long-history decode configuration.
 One step = one new token through the 16 full-attention layers of the pages'
-model: for every (layer, history) the producer quantizes the new token's K/V
-into that layer's paged INT8 cache and quantizes its query, then the INT8
-decode kernel attends over the whole history.  Each layer owns its cache, so a
-step streams 16 x 56K tokens x 2080 B = 1.9 GB and L2 (129 MB) holds none of
-it between steps.  All K timed steps run as one CUDA graph with timing events
-around it.  The decode kernel's own average duration comes from a second graph
-of the same K x 48 decode calls back to back (no producer in between).
+model: for every (layer, history) the producer (i8kv_kv_quant_write) quantizes
+the new token's K/V into that layer's paged INT8 cache and quantizes its query,
+then the INT8 decode kernel attends over the whole history.  Each layer owns
+its cache, so a step streams 16 x 56K tokens x 2080 B = 1.9 GB and L2 (129 MB)
+holds none of it between steps.  All K timed steps run as one CUDA graph with
+timing events around it.  The decode kernel's own average duration comes from a
+second graph of the same K x 48 decode calls back to back (no producer in
+between).  The one-launch decode step (i8kv_int8_decode_step, producer work
+inside the attention kernel) is timed per history among the secondary results.
 
   value     = KV bytes read by the decode launches / timed wall time (GB/s)
   roofline  = same bytes / the decode calls' own time (second graph), against the
@@ -263,6 +265,12 @@ class DecodeLayer:
         self.bt = torch.from_numpy(w.block_tables).cuda()
         self.sl = torch.from_numpy(w.seq_lens).cuda()
 
+    def step(self, i8, ws):
+        """Producer + attention for the new token in one call (the timed path)."""
+        c = self.cache
+        i8.int8_decode_step(self.out, self.q, self.k.view(1, *self.k.shape[1:]), self.v.view(1, *self.v.shape[1:]),
+                            c["k_cache"], c["v_cache"], c["k_scale"], c["v_scale"], self.bt, self.sl, ws)
+
     def produce(self, i8):
         i8.kv_quant_write(self.k, self.v, self.slot, **self.cache, q=self.q, q_i8=self.q_i8, q_scale=self.q_scale)
 
@@ -362,11 +370,13 @@ def run_ours(args):
     n_dec = len(layers)
     achieved = bytes_per_step / (dec_ms / 1e3) / 1e9
     avg_launch_us = dec_ms / n_dec * 1e3
-    by_len = {}
+    by_len, step_by_len = {}, {}
     for L in HISTORIES:
         sub = [ly for ly in layers if int(ly.w.seq_lens[0]) == L]
         ms_l = time_graph(torch, lambda: [ly.decode(i8, ws[L]) for ly in sub], args.steps)
         by_len[L] = ms_l / len(sub)
+        ms_s = time_graph(torch, lambda: [ly.step(i8, ws[L]) for ly in sub], args.steps)
+        step_by_len[L] = ms_s / len(sub)
     src = kernel_hash("int8_kv_cache_token_gb300/csrc/decode.cu", "int8_kv_cache_token_gb300/csrc/common.cuh")
     traffic = recorded_traffic("int8_decode", src)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
@@ -386,6 +396,8 @@ def run_ours(args):
             str(L): {"us": v * 1e3, "gb_s": wl.decode_outlier(L).kv_bytes_int8() / (v / 1e3) / 1e9,
                      "frac_hbm": wl.decode_outlier(L).kv_bytes_int8() / (v / 1e3) / 1e9 / hbm_peak}
             for L, v in by_len.items()}
+        secondary["decode_step_by_history"] = {
+            str(L): {"us": v * 1e3} for L, v in step_by_len.items()}
         if not args.quick:
             secondary.update(run_secondary(torch, i8, hbm_peak))
             try:

@@ -151,6 +151,30 @@ i8kv_status i8kv_int8_paged_decode_attn_noalloc(float* out, const int8_t* q_i8, 
                                                 int partition, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* INT8 decode step: i8kv_kv_quant_write of every sequence's newest token    */
+/* followed by i8kv_int8_paged_decode_attn, in one attention launch (plus    */
+/* the merge).  The pages run the fused producer and the attention as two    */
+/* kernels ([KV] §2.2, §3.3); here the attention kernel also does the        */
+/* producer's work for the one new token per sequence:                       */
+/*   k_new, v_new: bf16 [B, Hkv, D], the K/V of position L - 1 of sequence b */
+/*   (L = seq_lens[b], which counts the new token).  They are quantized by    */
+/*   the producer's rule (the same codes and scales, bit for bit) and written */
+/*   into k_cache / v_cache / k_scale / v_scale at that position's slot       */
+/*   (block block_tables[b][(L-1)/16], offset (L-1) % 16); the attention      */
+/*   uses them as well.                                                       */
+/*   q: bf16 [B, Hq, D], quantized per (sequence, q-head) by the producer's  */
+/*   rule inside the kernel (the int8 query is not written out).             */
+/* Everything else as i8kv_int8_paged_decode_attn.  seq_lens[b] == 0 means  */
+/* no new token: a zero row and no write.  The output and the cache equal    */
+/* those of the two calls bit for bit.  q, k_new, v_new: 16-byte aligned.    */
+/* ------------------------------------------------------------------------ */
+i8kv_status i8kv_int8_decode_step(float* out, const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                                  int8_t* k_cache, int8_t* v_cache, float* k_scale, float* v_scale,
+                                  const int32_t* block_tables, const int32_t* seq_lens, int B, int Hq, int Hkv, int D,
+                                  int block_size, int max_blocks, int num_blocks, float softmax_scale, int partition,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* INT8 prefix-prefill chunk ([PV] §2.1, [KV] §3.2): one online softmax over */
 /* the cached history and the chunk itself.  Chunk query j (absolute         */
 /* position history_len + j) attends to cache positions 0..history_len + j   */

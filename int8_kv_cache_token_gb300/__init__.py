@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     decode_workspace_bytes,
     device_error,
     int8_paged_decode_attn,
+    int8_decode_step,
     int8_paged_decode_attn_noalloc,
     int8_prefix_attn,
     kv_quant_write,

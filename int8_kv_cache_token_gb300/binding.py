@@ -41,6 +41,7 @@ _SIGS = {
     "i8kv_decode_workspace_bytes": [_I, _I, _I, _I, _I, _I, _I],
     "i8kv_int8_paged_decode_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z,
                                     _P],
+    "i8kv_int8_decode_step": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P],
     "i8kv_int8_paged_decode_attn_noalloc": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                             _P],
     "i8kv_int8_prefix_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P],
@@ -188,6 +189,22 @@ def int8_paged_decode_attn(out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scal
     B, Hq, _ = q_i8.shape
     _check(lib().i8kv_int8_paged_decode_attn(
         _ptr(out, torch.float32, "out"), _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
+        _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
+        _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
+        _ptr(block_tables, torch.int32, "block_tables"), _ptr(seq_lens, torch.int32, "seq_lens"),
+        B, Hq, Hkv, D, BLOCK_SIZE, block_tables.shape[1], NB, float(softmax_scale), partition,
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def int8_decode_step(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, workspace,
+                     softmax_scale: float = 0.0, partition: int = PARTITION, stream=None):
+    """One decode step in one launch: quantize and write each sequence's newest
+    token (k_new, v_new bf16 [B, Hkv, D], at position seq_lens[b] - 1) into the
+    cache, quantize q (bf16 [B, Hq, D]) and attend; out [B, Hq, D] fp32."""
+    NB, Hkv, D = _cache_geom(k_cache, 16)
+    B, Hq, _ = q.shape
+    _check(lib().i8kv_int8_decode_step(
+        _ptr(out, torch.float32, "out"), _bf16(q, "q"), _bf16(k_new, "k_new"), _bf16(v_new, "v_new"),
         _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
         _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
         _ptr(block_tables, torch.int32, "block_tables"), _ptr(seq_lens, torch.int32, "seq_lens"),

@@ -125,7 +125,7 @@ static i8kv_status decode_common(i8kv::DecodeParams& p, const void* q, const flo
   REQUIRE(max_blocks > 0 && num_blocks > 0, I8KV_ERR_INVALID_ARG, "max_blocks=%d num_blocks=%d", max_blocks,
           num_blocks);
   REQUIRE(out && q && k_cache && v_cache && block_tables && seq_lens, I8KV_ERR_INVALID_ARG, "null pointer");
-  if (int8) REQUIRE(q_scale && k_scale && v_scale, I8KV_ERR_INVALID_ARG, "null scale pointer");
+  if (int8) REQUIRE(k_scale && v_scale, I8KV_ERR_INVALID_ARG, "null scale pointer");
   REQUIRE(aligned16(k_cache) && aligned16(v_cache) && aligned16(q), I8KV_ERR_INVALID_ARG,
           "caches and q must be 16-byte aligned");
   if (int8) REQUIRE(aligned16(k_scale) && aligned16(v_scale), I8KV_ERR_INVALID_ARG, "scales must be 16-byte aligned");
@@ -166,12 +166,36 @@ i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const fl
                                         const int32_t* block_tables, const int32_t* seq_lens, int B, int Hq, int Hkv,
                                         int D, int block_size, int max_blocks, int num_blocks, float softmax_scale,
                                         int partition, void* workspace, size_t workspace_bytes, void* stream) {
+  REQUIRE(q_scale != nullptr, I8KV_ERR_INVALID_ARG, "q_scale is NULL");
   i8kv::DecodeParams p{};
   i8kv_status s = decode_common(p, q_i8, q_scale, true, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
                                 B, Hq, Hkv, D, block_size, max_blocks, num_blocks, softmax_scale, partition,
                                 workspace, workspace_bytes, out);
   if (s != I8KV_OK || B == 0) return s;
   return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "int8 decode launch");
+}
+
+i8kv_status i8kv_int8_decode_step(float* out, const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+                                  int8_t* k_cache, int8_t* v_cache, float* k_scale, float* v_scale,
+                                  const int32_t* block_tables, const int32_t* seq_lens, int B, int Hq, int Hkv, int D,
+                                  int block_size, int max_blocks, int num_blocks, float softmax_scale, int partition,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  REQUIRE(k_new && v_new, I8KV_ERR_INVALID_ARG, "k_new / v_new is NULL");
+  REQUIRE(aligned16(k_new) && aligned16(v_new), I8KV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+  i8kv::DecodeParams p{};
+  i8kv_status s = decode_common(p, q, nullptr, true, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, B,
+                                Hq, Hkv, D, block_size, max_blocks, num_blocks, softmax_scale, partition, workspace,
+                                workspace_bytes, out);
+  if (s != I8KV_OK || B == 0) return s;
+  p.step = 1;
+  p.q_bf16 = q;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.k_cache_w = k_cache;
+  p.v_cache_w = v_cache;
+  p.k_scale_w = k_scale;
+  p.v_scale_w = v_scale;
+  return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "int8 decode step launch");
 }
 
 i8kv_status i8kv_int8_paged_decode_attn_noalloc(float* out, const int8_t* q_i8, const float* q_scale,

@@ -251,6 +251,18 @@ __device__ __forceinline__ float div_shared(float x, float s, float y, bool tiny
 }
 constexpr float kTinyDivisor = 7.8886091e-31f;  // 2^-100
 
+// a / 127 correctly rounded, by the same method with the constant RN(1/127).
+// Checked exhaustively against IEEE division for every float in [1, 4), in the
+// two lowest normal binades and in the top binade (the rounding pattern
+// repeats in every binade); inputs below 2^-100 use the plain division.
+__device__ __forceinline__ float div127(float a) {
+  if (a < kTinyDivisor) return __fdiv_rn(a, 127.0f);
+  const float y = 0.0078740157f;  // RN(1/127)
+  const float q = __fmul_rn(a, y);
+  const float r = __fmaf_rn(-127.0f, q, a);
+  return __fmaf_rn(r, y, q);
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
 // Four int8 codes packed little-endian into one register.

@@ -68,7 +68,6 @@ constexpr int kProdWarp = kPVWarp0 + kPW;
 constexpr int kThreads = (kProdWarp + 1) * 32;
 constexpr int kHandBufs = 2 * kStreams;  // handoff buffers, unit i uses buffer i % 4
 constexpr int kRows = 8;     // query rows in the MMA N dimension
-constexpr int kMinUnit = 64; // smallest work unit of any variant (grid sizing)
 __host__ __device__ constexpr int kSlotFloats(int D) { return kRows * D + 2 * kRows; }
 
 // Geometry of one variant.  INT8: 128-token units, one 32-token group per QK
@@ -81,25 +80,29 @@ struct Geo {
   static constexpr int kBlocksU = kUnit / kBS;                  // pages per ring item
   static constexpr int kPage = D * kBS * EB;                    // one (block, KV head) page
   static constexpr int kPages = kBlocksU * kPage;
-  static constexpr int kSlot = kPages + (BF16 ? 0 : kUnit * 8); // + float2 (sK, sV) per token
+  static constexpr int kScales = kPages;                         // INT8: float2 (sK, sV) per token (K items)
+  static constexpr int kPatch = kPages + kUnit * 8;             // decode step: the new token's codes [D]
+  static constexpr int kSlot = (kPages + (BF16 ? 0 : kUnit * 8 + D) + 127) / 128 * 128;
+  static constexpr int kQBuf = BF16 ? 0 : kRows * D + kRows * 4;  // decode step: a stream's query codes, scales
   static constexpr int kWTok = kUnit / kQW;                     // tokens per QK warp
+  static constexpr int kGran = kWTok;                           // work-split granule (one QK warp's tokens)
   static constexpr int MT = kWTok / 16;                         // 16-token blocks per QK warp
   static constexpr int kDimsPW = D / kPW;                       // head-dims per PV warp
   static constexpr int NDT = kDimsPW / 16;                      // 16-dim MMA tiles per PV warp
   static constexpr int kFrag = BF16 ? 8 : 16;                   // B-fragment bytes per lane
-  // handoff buffer, per group (QK warp) q and row r:
-  // [kQW][32 lanes] B fragments | sW [kQW][8] | m [kQW][8] | l [kQW][8]
+  // handoff buffer: [kQW][32 lanes] B fragments, then per row r and group q
+  // (QK warp): sW [8][kQW] | m [8][kQW] | l [8][kQW] (a row's 4 groups in 16 bytes)
   static constexpr int kHSw = kQW * 32 * kFrag;
   static constexpr int kHM = kHSw + kQW * kRows * 4;
   static constexpr int kHL = kHM + kQW * kRows * 4;
   static constexpr int kHand = kHL + kQW * kRows * 4;
   static constexpr int kStage = kRows * kWTok * EB;             // per-QK-warp code/weight transpose
   static_assert(kGroup == kWTok || BF16, "an INT8 QK warp owns exactly one probability group");
-  static_assert(kSlot % 1024 == 0 && kHand % 16 == 0, "alignment");
+  static_assert(kSlot % 128 == 0 && kHand % 16 == 0, "alignment");
 };
 
 struct SmemLayout {
-  size_t ring, hand, stage, bars, ctrl, total;
+  size_t ring, hand, stage, qbuf, bars, ctrl, total;
 };
 
 template <int D, bool BF16>
@@ -113,6 +116,8 @@ __host__ __device__ inline SmemLayout decode_layout(int nslots) {
   off += (size_t)kHandBufs * Gm::kHand;
   L.stage = off;
   off += (size_t)kStreams * kQW * Gm::kStage;
+  L.qbuf = off;  // [stream] query codes [8][D] and scales [8] (decode step)
+  off += (size_t)kStreams * Gm::kQBuf;
   L.bars = off;  // full[nslots], empty[nslots], hfull[4], hempty[4]
   off += (size_t)(2 * nslots + 2 * kHandBufs) * sizeof(uint64_t);
   L.ctrl = off;
@@ -121,10 +126,15 @@ __host__ __device__ inline SmemLayout decode_layout(int nslots) {
   return L;
 }
 
-// Position in the (sequence, KV head, partition) unit order.
+// Position in the CTA's sequence of units.  The work is split over granules
+// (one QK warp's tokens: a 32-token probability group, or a 16-token block for
+// the BF16 comparison) in (sequence, KV head, token) order; a unit is up to kQW
+// consecutive granules of one (sequence, KV head) pair inside the CTA's range.
 struct Walk {
-  int b, kvh, part, L, np;
-  long long ub;  // global index of the first unit of sequence b
+  int b, kvh, gi, ngp, L, n;  // sequence, KV head, first granule in the pair, granules per pair, length,
+                              // granules in this unit (0 = past the CTA's range)
+  long long gb;               // global index of sequence b's first granule
+  long long gc;               // global index of this unit's first granule
 };
 
 __device__ __forceinline__ int clamp_len(int L, int maxL) {
@@ -132,21 +142,48 @@ __device__ __forceinline__ int clamp_len(int L, int maxL) {
   return L > maxL ? maxL : L;
 }
 
-__device__ __forceinline__ void walk_next(Walk& w, const int32_t* seq_lens, int B, int Hkv, int maxL, int unit) {
-  if (++w.part < w.np) return;
-  w.part = 0;
-  if (++w.kvh < Hkv) return;
-  w.kvh = 0;
-  w.ub += (long long)w.np * Hkv;
-  for (;;) {
-    if (++w.b >= B) return;
-    w.L = clamp_len(seq_lens[w.b], maxL);
-    w.np = (w.L + unit - 1) / unit;
-    if (w.np > 0) return;
-  }
+__device__ __forceinline__ int unit_granules(const Walk& w, long long g_end) {
+  if (w.gc >= g_end) return 0;
+  const long long left = g_end - w.gc;
+  const int in_pair = w.ngp - w.gi;
+  const int n = in_pair < kQW ? in_pair : kQW;
+  return left < n ? (int)left : n;
 }
 
-// CTA whose unit range [c*U/N, (c+1)*U/N) holds unit u (N <= U: no empty ranges).
+__device__ __forceinline__ void walk_next(Walk& w, const int32_t* seq_lens, int B, int Hkv, int maxL, int gran,
+                                          long long g_end) {
+  w.gc += w.n;
+  w.gi += w.n;
+  if (w.gi >= w.ngp) {
+    w.gi = 0;
+    if (++w.kvh >= Hkv) {
+      w.kvh = 0;
+      w.gb += (long long)w.ngp * Hkv;
+      for (;;) {
+        if (++w.b >= B) {
+          w.n = 0;
+          return;
+        }
+        w.L = clamp_len(seq_lens[w.b], maxL);
+        w.ngp = (w.L + gran - 1) / gran;
+        if (w.ngp > 0) break;
+      }
+    }
+  }
+  w.n = unit_granules(w, g_end);
+}
+
+// floor(U * c / N), in 32-bit arithmetic when U fits (the 64-bit division is a
+// long instruction sequence on the kernel's start-up path).
+__device__ __forceinline__ long long split_point(long long U, int c, int N) {
+  if (U < (1ll << 31)) {
+    const unsigned u = (unsigned)U, q = u / (unsigned)N, r = u % (unsigned)N;
+    return (long long)q * c + (r * (unsigned)c) / (unsigned)N;
+  }
+  return U * c / N;
+}
+
+// CTA whose granule range [c*U/N, (c+1)*U/N) holds granule u (N <= U: no empty ranges).
 __device__ __forceinline__ int cta_of(long long u, long long U, int N) {
   return (int)(((u + 1) * N + U - 1) / U - 1);
 }
@@ -268,12 +305,88 @@ __device__ __forceinline__ void qk_warp_bf16(const uint8_t* kpages, int warp, in
 }
 
 
+// ---- the decode step's quantization (the producer's rule, inside the kernel) ----
+// scale = amax / 127 (IEEE), code = round-half-even(x / scale) with the IEEE
+// quotient (Markstein's method, one reciprocal per vector), all codes 0 and
+// scale 0 for a zero vector -- the same arithmetic as kv_quant_write_kernel,
+// so the codes and scales are bit-identical to the two-kernel path.
+__device__ __forceinline__ uint32_t quant4(const float (&x)[4], float scale, float y, bool tiny, bool nz) {
+  int c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = nz ? __float2int_rn(div_shared(x[i], scale, y, tiny)) : 0;
+  return pack_s8x4(c[0], c[1], c[2], c[3]);
+}
+
+__device__ __forceinline__ void unpack_bf16x4(uint2 r, float (&x)[4]) {
+  x[0] = bf16_bits_to_float(r.x & 0xffffu);
+  x[1] = bf16_bits_to_float(r.x >> 16);
+  x[2] = bf16_bits_to_float(r.y & 0xffffu);
+  x[3] = bf16_bits_to_float(r.y >> 16);
+}
+
+// One D-vector quantized by a whole warp: lane l holds elements l*E .. l*E+E-1
+// (E = D / 32) and gets their codes packed 4 per word.  Loading is split from
+// quantizing so that a caller issues the loads of all its rows first (one
+// global round trip for the batch, not one per row).
+template <int D>
+struct RowRaw {
+  uint2 w[D / 128];
+};
+
+template <int D>
+__device__ __forceinline__ RowRaw<D> load_row_warp(const uint16_t* row, int lane) {
+  RowRaw<D> r;
+#pragma unroll
+  for (int j = 0; j < D / 128; ++j) r.w[j] = __ldg(reinterpret_cast<const uint2*>(row + lane * (D / 32)) + j);
+  return r;
+}
+
+// Returns the scale.
+template <int D>
+__device__ __forceinline__ float quant_row_warp(const RowRaw<D>& raw, uint32_t (&packed)[D / 128]) {
+  float x[D / 128][4];
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < D / 128; ++j) {
+    unpack_bf16x4(raw.w[j], x[j]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(x[j][i]));
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float scale = __fdiv_rn(amax, 127.0f);
+  const float y = __frcp_rn(scale);
+  const bool tiny = scale < kTinyDivisor, nz = amax > 0.f;
+#pragma unroll
+  for (int j = 0; j < D / 128; ++j) packed[j] = quant4(x[j], scale, y, tiny, nz);
+  return nz ? scale : 0.f;
+}
+
+// Query fragments (B operand of QK, f16 form) from int8 codes in shared memory,
+// rows [8][D] (the decode step's query buffer); same layout as load_q_frags.
+template <int D>
+__device__ __forceinline__ void load_q_frags_smem(const uint8_t* qa, int G, int lane, uint32_t (&qf)[D / 32][4]) {
+  const int g = lane >> 2, t = lane & 3;
+  const uint8_t* row = qa + g * D;
+#pragma unroll
+  for (int s = 0; s < D / 32; ++s) {
+    const uint32_t x0 = g < G ? *reinterpret_cast<const uint32_t*>(row + 32 * s + 4 * t) : 0u;
+    const uint32_t x1 = g < G ? *reinterpret_cast<const uint32_t*>(row + 32 * s + 16 + 4 * t) : 0u;
+    s8b_to_f16(x0, x1, qf[s]);
+  }
+}
+
 // One kernel body for both caches.  BF16 = false: the INT8 method.  BF16 = true:
-// the BF16-KV comparison (plain softmax, bf16 P x V, no scales).
-template <int D, bool BF16>
+// the BF16-KV comparison (plain softmax, bf16 P x V, no scales).  STEP (INT8
+// only): the decode step, which also quantizes and writes each sequence's new
+// token and quantizes the query; a separate instantiation, so the plain decode
+// carries none of that code.
+template <int D, bool BF16, bool STEP = false>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int nslots) {
+  static_assert(!(STEP && BF16), "the decode step is INT8 only");
   using Gm = Geo<D, BF16>;
   constexpr int kUnit = Gm::kUnit, kBlocksU = Gm::kBlocksU, kPage = Gm::kPage, kSlot = Gm::kSlot;
+  constexpr int kGran = Gm::kGran;
   constexpr int kWTok = Gm::kWTok, MT = Gm::MT, NDT = Gm::NDT;
   extern __shared__ __align__(1024) uint8_t smem[];
   const SmemLayout lay = decode_layout<D, BF16>(nslots);
@@ -314,15 +427,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   // One sequence in the batch (the long-context decode case): guess the first
   // unit from max_blocks and load its block-table row together with seq_lens,
   // so the two dependent loads overlap; the guess is checked below.
-  int spec_part = -1, spec_blk = -1;
+  int spec_gi = -1, spec_blk = -1;
   if (warp == kProdWarp && B == 1) {
-    const int np_g = (maxL + kUnit - 1) / kUnit;
-    const long long U_g = (long long)np_g * Hkv;
+    const int ngp_g = (maxL + kGran - 1) / kGran;
+    const long long U_g = (long long)ngp_g * Hkv;
     const int Nw_g = (int)(U_g < N ? U_g : N);
     if (c < Nw_g) {
-      spec_part = (int)((U_g * c / Nw_g) % np_g);
-      if (lane < kBlocksU && spec_part * kBlocksU + lane < p.max_blocks)
-        spec_blk = __ldg(p.block_tables + spec_part * kBlocksU + lane);
+      spec_gi = (int)(split_point(U_g, c, Nw_g) % ngp_g);
+      const int pg = spec_gi * kGran / kBS + lane;
+      if (lane < kBlocksU && pg < p.max_blocks) spec_blk = __ldg(p.block_tables + pg);
     }
   }
   if (warp == kProdWarp) {
@@ -336,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         const int raw = p.seq_lens[b];
         if (raw > maxL) record_error(2);
         L = clamp_len(raw, maxL);
-        u = (L + kUnit - 1) / kUnit * Hkv;
+        u = (L + kGran - 1) / kGran * Hkv;
         if (L == 0 && b % N == c) {  // empty sequence: zero rows, nothing to merge
           float* o = p.out + (size_t)b * Hq * D;
           for (int i = 0; i < Hq * D; ++i) o[i] = 0.f;
@@ -354,10 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       total += su;
     }
     const long long U = total;
-    // Only the first min(N, U) CTAs take units, so every working CTA has at
+    // Only the first min(N, U) CTAs take granules, so every working CTA has at
     // least one and the CTAs covering a pair are consecutive.
     const int Nw = (int)(U < N ? U : N);
-    const long long ub = c < Nw ? U * c / Nw : 0, ue = c < Nw ? U * (c + 1) / Nw : 0;
+    const long long ub = c < Nw ? split_point(U, c, Nw) : 0, ue = c < Nw ? split_point(U, c + 1, Nw) : 0;
     if (lane == 0) {
       ctrl[0] = (int)(ue - ub);
       ctrl[8] = 0;
@@ -379,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
             }
         } else if (b < B) {
           L = clamp_len(p.seq_lens[b], maxL);
-          u = (L + kUnit - 1) / kUnit * Hkv;
+          u = (L + kGran - 1) / kGran * Hkv;
         }
         int incl = u;
         for (int o = 1; o < 32; o <<= 1) {
@@ -391,10 +504,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         if (hit) {
           if (lane == __ffs(hit) - 1) {
             const int np = u / Hkv;
-            const long long local = ub - ex;
+            const int local = (int)(ub - ex);  // < np * Hkv
             ctrl[1] = b;
-            ctrl[2] = (int)(local / np);
-            ctrl[3] = (int)(local % np);
+            ctrl[2] = local / np;
+            ctrl[3] = local % np;
             ctrl[4] = (int)(ex & 0x7fffffff);
             ctrl[5] = (int)(ex >> 31);
             ctrl[9] = L;
@@ -406,15 +519,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     }
   }
   __syncthreads();  // the split in ctrl[] is visible to every warp
-  const int n_units = ctrl[0];
-  if (n_units <= 0) return;
+  const int n_gran = ctrl[0];
+  if (n_gran <= 0) return;
   Walk w0;
   w0.b = ctrl[1];
   w0.kvh = ctrl[2];
-  w0.part = ctrl[3];
-  w0.ub = (long long)ctrl[4] | ((long long)ctrl[5] << 31);
+  w0.gi = ctrl[3];
+  w0.gb = (long long)ctrl[4] | ((long long)ctrl[5] << 31);
   w0.L = ctrl[9];
-  w0.np = (w0.L + kUnit - 1) / kUnit;
+  w0.ngp = (w0.L + kGran - 1) / kGran;
+  w0.gc = w0.gb + (long long)w0.kvh * w0.ngp + w0.gi;
+  const long long g_end = w0.gc + n_gran;  // end of this CTA's granule range
+  w0.n = unit_granules(w0, g_end);
   const long long U = (long long)ctrl[6] | ((long long)ctrl[7] << 31);
   const int Nw = ctrl[10];
   const int g = lane >> 2, t = lane & 3;
@@ -428,20 +544,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     // This lane's page of a unit (lanes below the unit's page count), read from
     // the block table one unit ahead of its use.
     auto load_blk = [&](const Walk& u, int i) {
-      const int nb = (min(kUnit, u.L - u.part * kUnit) + kBS - 1) / kBS;
+      const int t0 = u.gi * kGran;
+      const int nb = (min(u.n * kGran, u.L - t0) + kBS - 1) / kBS;
       if (lane >= nb) return -1;
-      if (i == 0 && B == 1 && u.part == spec_part) return spec_blk;
-      return p.block_tables[(size_t)u.b * p.max_blocks + u.part * kBlocksU + lane];
+      if (i == 0 && B == 1 && u.gi == spec_gi) return spec_blk;
+      return p.block_tables[(size_t)u.b * p.max_blocks + t0 / kBS + lane];
     };
     Walk wk = w0, wn = w0;
-    walk_next(wn, p.seq_lens, B, Hkv, maxL, kUnit);
+    walk_next(wn, p.seq_lens, B, Hkv, maxL, kGran, g_end);
     int blk_cur = load_blk(wk, 0);
     int n_k = 0, n_v = 0;  // K and V items issued
-    for (int i = 0; i < n_units; ++i) {
+    uint32_t nt_k[D / 128], nt_v[D / 128];  // decode step: the new token's codes
+    for (int i = 0; wk.n > 0; ++i) {
       if (*abort_flag) break;
-      const int blk_nx = (i + 1 < n_units) ? load_blk(wn, i + 1) : -1;  // in flight meanwhile
-      const int t0 = wk.part * kUnit;
-      const int ntok = min(kUnit, wk.L - t0);
+      const int blk_nx = wn.n > 0 ? load_blk(wn, i + 1) : -1;  // in flight meanwhile
+      const int t0 = wk.gi * kGran;
+      const int ntok = min(wk.n * kGran, wk.L - t0);
       const int nblk = (ntok + kBS - 1) / kBS;
       int blk = blk_cur;
       if (lane < nblk && (blk < 0 || blk >= p.num_blocks)) {
@@ -461,16 +579,58 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       if (ok)
         bulk_g2s_hint(kdst + (size_t)lane * kPage, kc + ((size_t)blk * Hkv + wk.kvh) * kPage, kPage, &full[kslot],
                       pol);
+      // Decode step: this unit holds the pair's newest token (position L - 1).
+      // Quantize its K/V here, write them into the cache for later steps, and
+      // stage them in the slots' patch areas; the consumers patch their
+      // shared-memory copy of the page (which may predate the write).
+      const bool patched = STEP && (wk.gi + wk.n == wk.ngp);
+      const int pos = wk.L - 1 - t0;  // the new token within the unit
       if constexpr (!BF16) {
-        float* sdst = reinterpret_cast<float*>(kdst + Gm::kPages);
+        float sk_new = 0.f, sv_new = 0.f;
+        if (patched) {
+          const size_t ri = ((size_t)wk.b * Hkv + wk.kvh) * D;
+          const RowRaw<D> kr = load_row_warp<D>(p.k_new + ri, lane), vr = load_row_warp<D>(p.v_new + ri, lane);
+          sk_new = quant_row_warp<D>(kr, nt_k);
+          sv_new = quant_row_warp<D>(vr, nt_v);
+          const uint32_t(&kcodes)[D / 128] = nt_k;
+          const int blk_new = __shfl_sync(0xffffffffu, blk, pos / kBS), off_new = (wk.L - 1) % kBS;
+          constexpr int E = D / 32;
+          const int d0 = lane * E;
+          if (blk_new >= 0) {
+            int8_t* kg = p.k_cache_w + ((((size_t)blk_new * Hkv + wk.kvh) * (D / 16) + d0 / 16) * kBS + off_new) * 16 +
+                         d0 % 16;
+            if constexpr (E == 8)
+              *reinterpret_cast<uint2*>(kg) = make_uint2(kcodes[0], kcodes[1]);
+            else
+              *reinterpret_cast<uint32_t*>(kg) = kcodes[0];
+            int8_t* vg = p.v_cache_w + (((size_t)blk_new * Hkv + wk.kvh) * D + d0) * kBS + off_new;
+#pragma unroll
+            for (int e = 0; e < E; ++e) vg[(size_t)e * kBS] = (int8_t)((nt_v[e >> 2] >> (8 * (e & 3))) & 0xff);
+            if (lane == 0) {
+              const size_t si = ((size_t)blk_new * kBS + off_new) * Hkv + wk.kvh;
+              p.k_scale_w[si] = sk_new;
+              p.v_scale_w[si] = sv_new;
+            }
+          }
+          if constexpr (E == 8)
+            *reinterpret_cast<uint2*>(kdst + Gm::kPatch + d0) = make_uint2(kcodes[0], kcodes[1]);
+          else
+            *reinterpret_cast<uint32_t*>(kdst + Gm::kPatch + d0) = kcodes[0];
+        }
+        float* sdst = reinterpret_cast<float*>(kdst + Gm::kScales);
 #pragma unroll
         for (int r = 0; r < kUnit / 32; ++r) {
           const int tok = lane + 32 * r;
-          const int bj = __shfl_sync(0xffffffffu, blk, tok / kBS);
-          const bool v = tok < ntok && bj >= 0;
-          const size_t si = ((size_t)(v ? bj : 0) * kBS + tok % kBS) * Hkv + wk.kvh;
-          cp_async_4(sdst + 2 * tok, p.k_scale + si, v ? 4u : 0u);
-          cp_async_4(sdst + 2 * tok + 1, p.v_scale + si, v ? 4u : 0u);
+          const int bj = __shfl_sync(0xffffffffu, blk, tok / kBS);  // every lane takes part in the shuffle
+          if (patched && tok == pos) {  // the new token's scales come from this warp, not the cache
+            sdst[2 * tok] = sk_new;
+            sdst[2 * tok + 1] = sv_new;
+          } else {
+            const bool v = tok < ntok && bj >= 0;
+            const size_t si = ((size_t)(v ? bj : 0) * kBS + tok % kBS) * Hkv + wk.kvh;
+            cp_async_4(sdst + 2 * tok, p.k_scale + si, v ? 4u : 0u);
+            cp_async_4(sdst + 2 * tok + 1, p.v_scale + si, v ? 4u : 0u);
+          }
         }
         cp_async_mbar_arrive(&full[kslot]);
       }
@@ -485,11 +645,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       if (ok)
         bulk_g2s_hint(ring + (size_t)vslot * kSlot + (size_t)lane * kPage,
                       vc + ((size_t)blk * Hkv + wk.kvh) * kPage, kPage, &full[vslot], pol);
+      if constexpr (!BF16) {
+        if (patched) {
+          constexpr int E = D / 32;
+          uint8_t* vpatch = ring + (size_t)vslot * kSlot + Gm::kPatch + lane * E;
+          if constexpr (E == 8)
+            *reinterpret_cast<uint2*>(vpatch) = make_uint2(nt_v[0], nt_v[1]);
+          else
+            *reinterpret_cast<uint32_t*>(vpatch) = nt_v[0];
+        }
+      }
       mbar_arrive(&full[vslot]);
       ++n_v;
       blk_cur = blk_nx;
       wk = wn;
-      walk_next(wn, p.seq_lens, B, Hkv, maxL, kUnit);
+      walk_next(wn, p.seq_lens, B, Hkv, maxL, kGran, g_end);
     }
     if (*abort_flag) {
       // The consumers stopped waiting: hold the CTA (and its shared memory)
@@ -525,17 +695,48 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     const int tok0 = qw * kWTok;  // this warp's tokens within a unit
     uint8_t* stg = stage + warp * Gm::kStage;
     Walk wk = w0;
-    if (st == 1) walk_next(wk, p.seq_lens, B, Hkv, maxL, kUnit);
+    if (st == 1) walk_next(wk, p.seq_lens, B, Hkv, maxL, kGran, g_end);
     int cur_pair = -1;
     uint32_t qf[D / 32][4];    // INT8: converted query fragments
     uint32_t qfb[D / 16][2];   // BF16: query fragments
     float sq[2] = {0.f, 0.f};
-    for (int i = st; i < n_units; i += kStreams) {
+    for (int i = st; wk.n > 0; i += kStreams) {
       const int pair = wk.b * Hkv + wk.kvh;
       if (pair != cur_pair) {
         cur_pair = pair;
         if constexpr (BF16) {
           load_q_frags_bf16<D>(static_cast<const uint16_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qfb);
+        } else if constexpr (STEP) {
+          // Decode step: the stream's 4 warps quantize the pair's query rows
+          // (warp w: rows w and w + 4) by the producer's rule into the stream's
+          // buffer, then each builds its fragments from it.
+          uint8_t* qb = smem + lay.qbuf + (size_t)st * Gm::kQBuf;
+          RowRaw<D> qr[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int r = qw + kQW * h;
+            if (r < G) qr[h] = load_row_warp<D>(p.q_bf16 + ((size_t)wk.b * Hq + wk.kvh * G + r) * D, lane);
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int r = qw + kQW * h;
+            if (r < G) {
+              uint32_t codes[D / 128];
+              const float sc = quant_row_warp<D>(qr[h], codes);
+              constexpr int E = D / 32;
+              if constexpr (E == 8)
+                *reinterpret_cast<uint2*>(qb + r * D + lane * E) = make_uint2(codes[0], codes[1]);
+              else
+                *reinterpret_cast<uint32_t*>(qb + r * D + lane * E) = codes[0];
+              if (lane == 0) reinterpret_cast<float*>(qb + kRows * D)[r] = sc;
+            }
+          }
+          named_bar_sync(1 + st, kQW * 32);  // the rows are in the buffer
+          load_q_frags_smem<D>(qb, G, lane, qf);
+          const float* qsc = reinterpret_cast<const float*>(qb + kRows * D);
+          sq[0] = 2 * t < G ? qsc[2 * t] : 0.f;
+          sq[1] = 2 * t + 1 < G ? qsc[2 * t + 1] : 0.f;
+          named_bar_sync(1 + st, kQW * 32);  // every warp has read it before it is reused
         } else {
           load_q_frags<D>(static_cast<const int8_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qf);
 #pragma unroll
@@ -545,13 +746,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
           }
         }
       }
-      const int ntok = min(kUnit, wk.L - wk.part * kUnit);
-      const bool active = tok0 < ntok;
+      const int ntok = min(wk.n * kGran, wk.L - wk.gi * kGran);
+      const bool active = qw < wk.n;  // every granule of the unit holds tokens
 
       // ---- K item: QK of this warp's tokens, and their scales ----
       const int kslot = rg.kslot(i);
       pipe_wait(&full[kslot], rg.kuse(i) & 1, abort_flag);
       const uint8_t* kb = ring + (size_t)kslot * kSlot;
+      if constexpr (!BF16) {
+        // decode step: the warp whose granule holds the new token patches its K row
+        const int pos = wk.L - 1 - wk.gi * kGran;
+        if (STEP && wk.gi + wk.n == wk.ngp && pos / kGran == qw) {
+          if (lane < D / 16) {
+            uint8_t* page = ring + (size_t)kslot * kSlot + (size_t)(pos / kBS) * kPage;
+            *reinterpret_cast<uint4*>(page + (size_t)lane * (kBS * 16) + (pos % kBS) * 16) =
+                *reinterpret_cast<const uint4*>(kb + Gm::kPatch + lane * 16);
+          }
+          __syncwarp();
+        }
+      }
       float acc[2][4];
 #pragma unroll
       for (int m = 0; m < 2; ++m)
@@ -565,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       }
       float sk[4], sv[4];  // tokens g, g+8 of this warp's blocks 0 and 1
       if constexpr (!BF16) {
-        const float2* scl = reinterpret_cast<const float2*>(kb + Gm::kPages);
+        const float2* scl = reinterpret_cast<const float2*>(kb + Gm::kScales);
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
@@ -602,12 +815,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         for (int off = 4; off <= 16; off <<= 1) gm[r] = fmaxf(gm[r], __shfl_xor_sync(0xffffffffu, gm[r], off));
 
       // ---- weights: BF16 p~; INT8 W = p~ sV, sW, codes ----
+      // In an active warp every row maximum is finite and masked scores are
+      // -inf, so exp(s - m_g) is 0 there without a test.  An inactive warp
+      // (no tokens of its group in the unit) publishes zeros.
       float swv[2] = {0.f, 0.f}, lg[2] = {0.f, 0.f};
       if constexpr (BF16) {
         uint16_t* pw = reinterpret_cast<uint16_t*>(stg);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float pe = (s[0][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[0][e], gm[e & 1]));
+          const float pe = active ? expf(__fsub_rn(s[0][e], gm[e & 1])) : 0.f;
           lg[e & 1] += pe;
           pw[(2 * t + (e & 1)) * 16 + g + 8 * (e >> 1)] = __bfloat16_as_ushort(__float2bfloat16_rn(pe));
         }
@@ -617,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         for (int m = 0; m < 2; ++m)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float pe = (s[m][e] == -INFINITY) ? 0.f : expf(__fsub_rn(s[m][e], gm[e & 1]));
+            const float pe = active ? expf(__fsub_rn(s[m][e], gm[e & 1])) : 0.f;
             lg[e & 1] += pe;
             w[m][e] = __fmul_rn(pe, sv[2 * m + (e >> 1)]);
             A[e & 1] = fmaxf(A[e & 1], w[m][e]);
@@ -632,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         bool tiny[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          swv[r] = __fdiv_rn(A[r], 127.0f);
+          swv[r] = div127(A[r]);
           ysw[r] = __frcp_rn(swv[r]);
           tiny[r] = swv[r] < kTinyDivisor;
         }
@@ -675,14 +891,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         float* hl = reinterpret_cast<float*>(hb + Gm::kHL);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          hsw[qw * kRows + 2 * t + r] = swv[r];
-          hm[qw * kRows + 2 * t + r] = gm[r];
-          hl[qw * kRows + 2 * t + r] = lg[r];
+          hsw[(2 * t + r) * kQW + qw] = swv[r];
+          hm[(2 * t + r) * kQW + qw] = active ? gm[r] : -INFINITY;
+          hl[(2 * t + r) * kQW + qw] = lg[r];
         }
       }
       mbar_arrive(&hfull[hbi]);  // every thread: releases its own stores
-      walk_next(wk, p.seq_lens, B, Hkv, maxL, kUnit);
-      walk_next(wk, p.seq_lens, B, Hkv, maxL, kUnit);
+      walk_next(wk, p.seq_lens, B, Hkv, maxL, kGran, g_end);
+      if (wk.n > 0) walk_next(wk, p.seq_lens, B, Hkv, maxL, kGran, g_end);
     }
     return;
   }
@@ -695,11 +911,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   const int pv_w = warp - kPVWarp0;
   const int mi = lane >> 3, ri = lane & 7;
   Walk wk = w0, w1 = w0;
-  walk_next(w1, p.seq_lens, B, Hkv, maxL, kUnit);
+  walk_next(w1, p.seq_lens, B, Hkv, maxL, kGran, g_end);
   int cur_pair = -1;
   float o[NDT][4];
   float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
-  for (int i = 0; i < n_units; ++i) {
+  for (int i = 0; wk.n > 0; ++i) {
     const int pair = wk.b * Hkv + wk.kvh;
     if (pair != cur_pair) {
       cur_pair = pair;
@@ -713,34 +929,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         lrun[r] = 0.f;
       }
     }
-    const bool seg_end = (i == n_units - 1) || (w1.b * Hkv + w1.kvh != pair);
-    const int ntok = min(kUnit, wk.L - wk.part * kUnit);
-    const int ng = (ntok + kWTok - 1) / kWTok;  // groups holding tokens
+    const bool seg_end = (w1.n == 0) || (w1.b * Hkv + w1.kvh != pair);
+    const int ng = wk.n;  // granules (groups) of the unit, all holding tokens
 
     const int hbi = i % kHandBufs;
     const uint8_t* hb = hand + (size_t)hbi * Gm::kHand;
     pipe_wait(&hfull[hbi], (i / kHandBufs) & 1, abort_flag);
-    const float* hsw = reinterpret_cast<const float*>(hb + Gm::kHSw);
-    const float* hm = reinterpret_cast<const float*>(hb + Gm::kHM);
-    const float* hl = reinterpret_cast<const float*>(hb + Gm::kHL);
     // ---- the unit's running maximum and the groups' factors ----
+    static_assert(kQW == 4, "a row's group values are read as one float4");
     float fs[kQW][2];  // exp(m_g - m_new) * sW_g (INT8) or exp(m_g - m_new) (BF16)
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      float mg[kQW];
-      float mn = mrun[r];
-#pragma unroll
-      for (int q = 0; q < kQW; ++q) {
-        mg[q] = q < ng ? hm[q * kRows + 2 * t + r] : -INFINITY;
-        mn = fmaxf(mn, mg[q]);
-      }
+      const int row = 2 * t + r;
+      const float4 m4 = reinterpret_cast<const float4*>(hb + Gm::kHM)[row];
+      const float4 l4 = reinterpret_cast<const float4*>(hb + Gm::kHL)[row];
+      const float4 s4 = reinterpret_cast<const float4*>(hb + Gm::kHSw)[row];
+      // groups past the unit's tokens published m = -inf, l = 0, sW = 0
+      const float mg[4] = {m4.x, m4.y, m4.z, m4.w}, lgv[4] = {l4.x, l4.y, l4.z, l4.w},
+                  sg[4] = {s4.x, s4.y, s4.z, s4.w};
+      const float mn = fmaxf(fmaxf(mrun[r], fmaxf(mg[0], mg[1])), fmaxf(mg[2], mg[3]));
       const float alpha = (mrun[r] == -INFINITY) ? 0.f : expf(mrun[r] - mn);
       float l = lrun[r] * alpha;
 #pragma unroll
       for (int q = 0; q < kQW; ++q) {
         const float f = (mg[q] == -INFINITY) ? 0.f : expf(mg[q] - mn);
-        if (q < ng) l = fmaf(hl[q * kRows + 2 * t + r], f, l);
-        fs[q][r] = BF16 ? f : f * (q < ng ? hsw[q * kRows + 2 * t + r] : 0.f);
+        l = fmaf(lgv[q], f, l);
+        fs[q][r] = BF16 ? f : f * sg[q];
       }
       lrun[r] = l;
       mrun[r] = mn;
@@ -757,6 +971,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     const int vslot = rg.vslot(i);
     pipe_wait(&full[vslot], rg.vuse(i) & 1, abort_flag);
     const uint8_t* vb = ring + (size_t)vslot * kSlot;
+    if constexpr (!BF16) {
+      // decode step: every PV warp patches its own head-dims of the new token's V column
+      if (STEP && wk.gi + wk.n == wk.ngp) {
+        const int pos = wk.L - 1 - wk.gi * kGran;
+        if (lane < Gm::kDimsPW) {
+          const int d = pv_w * Gm::kDimsPW + lane;
+          uint8_t* vp = ring + (size_t)vslot * kSlot;
+          vp[(size_t)(pos / kBS) * kPage + (size_t)d * kBS + pos % kBS] = vp[Gm::kPatch + d];
+        }
+        __syncwarp();
+      }
+    }
 #pragma unroll
     for (int q = 0; q < kQW; ++q) {
       if (q >= ng) break;
@@ -800,8 +1026,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
 
     // ---- end of this CTA's share of the (sequence, KV head) pair ----
     if (seg_end) {
-      const long long Up = wk.ub + (long long)wk.kvh * wk.np;
-      const int cf = cta_of(Up, U, Nw), cl = cta_of(Up + wk.np - 1, U, Nw);
+      const long long Up = wk.gb + (long long)wk.kvh * wk.ngp;  // the pair's first granule
+      const int cf = cta_of(Up, U, Nw), cl = cta_of(Up + wk.ngp - 1, U, Nw);
       // the CTA holding the pair's first unit records whether a merge is needed
       if (c == cf && pv_w == 0 && lane == 0) p.ws_info[pair] = (cf == cl) ? -1 : ((cf << 16) | cl);
       const int d0 = pv_w * Gm::kDimsPW;
@@ -837,7 +1063,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     __syncwarp();
     if (lane == 0) mbar_arrive(&hempty[hbi]);
     wk = w1;
-    walk_next(w1, p.seq_lens, B, Hkv, maxL, kUnit);
+    walk_next(w1, p.seq_lens, B, Hkv, maxL, kGran, g_end);
   }
 }
 
@@ -1013,7 +1239,7 @@ int pick_slots(int smem_limit) {
   return 0;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool STEP>
 cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1024,12 +1250,12 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   // maximum), so that launches captured into a CUDA graph make no attribute call.
   static int attr_set[64] = {0};
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16, STEP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          max_smem_optin(dev));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
-  cudaError_t e = launch_pdl(decode_kernel<D, BF16>, dim3(p.grid), dim3(kThreads), smem, stream, p, ns);
+  cudaError_t e = launch_pdl(decode_kernel<D, BF16, STEP>, dim3(p.grid), dim3(kThreads), smem, stream, p, ns);
   if (e != cudaSuccess) return e;
   return launch_pdl(decode_merge_kernel<D>, dim3(p.B * p.Hkv * p.G), dim3(kMergeThreads), 0, stream, p);
 }
@@ -1039,7 +1265,7 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
 I8KV_DEFINE_ERROR_ACCESSOR(read_error_decode)
 
 int decode_grid(int device, int B, int Hkv, int max_blocks) {
-  const long long max_units = (long long)B * Hkv * (((long long)max_blocks * kBS + kMinUnit - 1) / kMinUnit);
+  const long long max_units = (long long)B * Hkv * max_blocks;  // granules are at least one block
   long long g = num_sms(device);
   if (max_units < g) g = max_units;
   return (int)(g < 1 ? 1 : g);
@@ -1052,13 +1278,17 @@ size_t decode_workspace_bytes(int B, int Hkv, int D, int grid) {
 }
 
 cudaError_t launch_int8_decode(const DecodeParams& p, cudaStream_t stream) {
-  if (p.D == 256) return launch_decode_d<256, false>(p, stream);
-  return launch_decode_d<128, false>(p, stream);
+  if (p.step) {
+    if (p.D == 256) return launch_decode_d<256, false, true>(p, stream);
+    return launch_decode_d<128, false, true>(p, stream);
+  }
+  if (p.D == 256) return launch_decode_d<256, false, false>(p, stream);
+  return launch_decode_d<128, false, false>(p, stream);
 }
 
 cudaError_t launch_bf16_decode(const DecodeParams& p, cudaStream_t stream) {
-  if (p.D == 256) return launch_decode_d<256, true>(p, stream);
-  return launch_decode_d<128, true>(p, stream);
+  if (p.D == 256) return launch_decode_d<256, true, false>(p, stream);
+  return launch_decode_d<128, true, false>(p, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -39,6 +39,18 @@ struct DecodeParams {
   float* ws_part;             // [(B*Hkv + grid) slots][8 rows * D + 16]
   int* ws_info;               // [B*Hkv] per pair: -1 (no merge) or first CTA << 16 | last CTA
   int grid;                   // CTAs launched (the work split depends on it)
+  // Decode step (INT8 path, step != 0): the newest token of each sequence
+  // (position seq_lens[b] - 1) arrives as bf16 and is quantized inside the
+  // kernel -- K/V written into the cache, Q quantized per warp -- instead of
+  // being read from q / the cache.
+  int step;
+  const uint16_t* q_bf16;     // [B, Hq, D]
+  const uint16_t* k_new;      // [B, Hkv, D]
+  const uint16_t* v_new;      // [B, Hkv, D]
+  int8_t* k_cache_w;          // the caches again, written at the new token's slot
+  int8_t* v_cache_w;
+  float* k_scale_w;
+  float* v_scale_w;
 };
 
 // Debug QK: int32 accumulators through the decode kernel's QK fragments.

@@ -62,6 +62,18 @@ def test_argument_checks_without_gpu(lib):
     assert d(*args, 1, 72, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20, None) == 2
     assert d(*args, 1, 24, 4, 256, 16, 8, 10, 0.0, 512, P(16), 1 << 20, None) == 2
     assert "partition" in _last_error(lib)
+    # decode step: the new token's K/V are required and 16-byte aligned
+    st = lib.i8kv_int8_decode_step
+    st.restype = ctypes.c_int
+    st.argtypes = [P] * 10 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int, P, ctypes.c_size_t, P]
+    base = [P(16)] * 10
+    assert st(P(16), P(16), None, P(16), *([P(16)] * 6), 1, 24, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20,
+              None) == 1
+    assert "k_new" in _last_error(lib)
+    assert st(P(16), P(16), P(24), P(16), *([P(16)] * 6), 1, 24, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20,
+              None) == 1
+    assert "aligned" in _last_error(lib)
+    assert st(*base, 1, 24, 4, 64, 16, 8, 10, 0.0, 256, P(16), 1 << 20, None) == 2
     # prefix: chunk_len == 0 is a no-op; negative history rejected
     pf = lib.i8kv_int8_prefix_attn
     pf.restype = ctypes.c_int
