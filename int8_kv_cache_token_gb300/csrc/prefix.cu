@@ -8,19 +8,21 @@
 // INT8 MMAC Attention推理优化" §3.2 (history and the chunk's own K/V in one
 // online softmax, never two attentions merged afterwards).
 //
-// GB300 shape.  A CTA owns 64 query rows of one KV head (4 warps x 16 rows);
+// GB300 shape.  A CTA owns 128 query rows of one KV head (8 warps x 16 rows);
 // the rows are (chunk token, query head) pairs of that KV head's GQA group,
-// token-major, so the 6 query heads sharing K/V read the same shared-memory
-// tiles.  K/V pages of 64 keys per stage arrive by bulk copy (thread 0 issues,
-// mbarrier completes), double-buffered.  Each warp keeps its rows' softmax
-// state and the FP32 output in registers (FlashAttention-2 style).  Per
-// 32-key group: QK with mma.sync m16n8k32 s8 whose B fragments are loaded with
-// a key order permuted inside the group, so the score fragments land exactly
-// where the PV A operand needs the 32 codes of the group (the group's set of
-// tokens is unchanged; only the order inside the MMA's K dimension differs);
-// then scores, causal mask, online softmax, W = p~ x sV, per-row group absmax,
-// quantize, and PV with mma.sync s8 (B = V pages via ldmatrix), the int32
-// result scaled by the row's sW into the FP32 accumulators.
+// token-major, so the query heads sharing K/V read the same tiles.  K/V pages
+// of 64 keys per stage arrive by bulk copy into a double-buffered int8 staging
+// area.  Each stage is then converted once, by all warps together, into f16
+// tiles in shared memory: K as [key][dim] and V as [dim][key], 16-byte chunks
+// XOR-swizzled so that ldmatrix reads them without bank conflicts.  The int8
+// values are exact in f16, every product is exact and every partial sum stays
+// below 2^22, so the f16 tensor-core MMAs with fp32 accumulation give the exact
+// int32 results of the INT8 contractions (QK over D dims; PV over one 32-key
+// group).  Each warp keeps its rows' softmax state and FP32 output in registers
+// (FlashAttention-2 style).  Per 32-key group: QK, scores, causal mask, online
+// softmax, W = p~ x sV, per-row group absmax, sW = A / 127 and the codes
+// round(W / sW) (IEEE quotients, as the oracle), then PV with the codes as the
+// A operand and sW x (the exact product) added to the output.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -30,37 +32,51 @@ I8KV_DEFINE_ERROR_ACCESSOR(read_error_prefix)
 namespace {
 
 constexpr int kBS = 16;
-constexpr int kRowsPerCTA = 64;
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
+constexpr int kRowsPerCTA = kWarps * 16;
 constexpr int kKeysPerStage = 64;  // 4 blocks
 constexpr int kBlocksPerStage = kKeysPerStage / kBS;
-constexpr int kStages = 2;
+constexpr int kStages = 2;         // int8 staging buffers
+constexpr int kMaxHkv = 8;
 
 template <int D>
 struct PrefixSmem {
-  static constexpr int kPage = D * kBS;
-  static constexpr int kTileBytes = kBlocksPerStage * kPage;
-  // per stage: K tile, V tile, K-scale rows, V-scale rows (Hkv <= 8)
-  static constexpr int kScaleBytes = kBlocksPerStage * kBS * 8 * 4;
+  static constexpr int kPage = D * kBS;                           // int8 page
+  static constexpr int kTileBytes = kBlocksPerStage * kPage;      // int8 K (or V) tile of a stage
+  static constexpr int kScaleBytes = kBlocksPerStage * kBS * kMaxHkv * 4;
   static constexpr int kStageBytes = 2 * kTileBytes + 2 * kScaleBytes;
-  static constexpr int kQBytes = kRowsPerCTA * D * 2;  // f16 query tile, 16-byte chunks XOR-swizzled by row
-  static constexpr int kTotal = kStages * kStageBytes + kQBytes + 64;
+  static constexpr int kK16 = kKeysPerStage * D * 2;              // f16 K [64 keys][D]
+  static constexpr int kV16 = D * kKeysPerStage * 2;              // f16 V [D][64 keys]
+  static constexpr int kQ16 = kRowsPerCTA * D * 2;                // f16 Q [128 rows][D]
+  static constexpr int kSc = kKeysPerStage * 2 * 4;               // the stage's (sK, sV) per key
+  static constexpr int kOffK16 = kStages * kStageBytes;
+  static constexpr int kOffV16 = kOffK16 + kK16;
+  static constexpr int kOffQ16 = kOffV16 + kV16;
+  static constexpr int kOffSc = kOffQ16 + kQ16;
+  static constexpr int kOffBar = kOffSc + kSc;
+  static constexpr int kTotal = kOffBar + 64;
 };
 
-// Key offset (within a 32-key group) of column c of QK n-tile nn (0..3).
-__device__ __forceinline__ int group_key(int nn, int c) {
-  const int base = (nn & 1) * 2 + (nn >> 1) * 16;
-  return base + 4 * (c >> 1) + (c & 1);
+// 16 int8 codes (one 16-byte chunk) -> 16 exact f16 values, natural order.
+__device__ __forceinline__ void s8x16_to_f16(const uint4& v, uint4& h0, uint4& h1) {
+  s8x4_to_f16(v.x, h0.x, h0.y);
+  s8x4_to_f16(v.y, h0.z, h0.w);
+  s8x4_to_f16(v.z, h1.x, h1.y);
+  s8x4_to_f16(v.w, h1.z, h1.w);
 }
 
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p) {
+__global__ void __launch_bounds__(kWarps * 32, 1) int8_prefix_kernel(PrefixParams p) {
   using S = PrefixSmem<D>;
-  constexpr int KS = D / 32;  // k-steps of QK
+  constexpr int KS = D / 16;  // k16 steps of QK
   constexpr int ND = D / 8;   // n-tiles of PV
+  constexpr int KC = (D / 16) * kBS;  // int8 chunks of one K page
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* qs = smem + kStages * S::kStageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * S::kStageBytes + S::kQBytes);
+  uint8_t* k16 = smem + S::kOffK16;
+  uint8_t* v16 = smem + S::kOffV16;
+  uint8_t* q16 = smem + S::kOffQ16;
+  float* scs = reinterpret_cast<float*>(smem + S::kOffSc);  // [64 keys][sK, sV]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kStages);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -120,26 +136,21 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
     for (int st = 0; st < kStages && st < n_stages; ++st) issue(st);
   }
 
-  // ---- query tile -> shared memory as exact f16 ----
-  // Head-dims are stored in the order the k16 MMAs consume them next to K
-  // fragments converted by s8b_to_f16: inside each 16-dim half of a 32-dim
-  // step, logical positions 0..7 hold physical dims {0,1,4,5,8,9,12,13} and
-  // 8..15 hold {2,3,6,7,10,11,14,15}.  Logical 16-byte chunk c (8 f16) of row r
-  // is stored at chunk c ^ (r & 7).
-  for (int i = tid; i < kRowsPerCTA * (D / 8); i += kWarps * 32) {
-    const int rr = i / (D / 8), ch = i % (D / 8);
+  // ---- query tile -> shared memory as exact f16, natural dim order; 16-byte
+  // chunk c of row r is stored at chunk c ^ (r & 7) ----
+  for (int i = tid; i < kRowsPerCTA * (D / 16); i += kWarps * 32) {
+    const int rr = i / (D / 16), c16 = i % (D / 16);
     const int r = r0 + rr;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (r < R) {
       const int j = r / G, hq = kvh * G + r % G;
-      v = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)j * Hq + hq) * D) + (ch >> 1));
+      v = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)j * Hq + hq) * D) + c16);
     }
-    const uint32_t sel = (ch & 1) ? 0x7632u : 0x5410u;
-    const uint32_t x0 = __byte_perm(v.x, v.y, sel), x1 = __byte_perm(v.z, v.w, sel);
-    uint4 h;
-    s8x4_to_f16(x0, h.x, h.y);
-    s8x4_to_f16(x1, h.z, h.w);
-    *reinterpret_cast<uint4*>(qs + (size_t)rr * (2 * D) + ((ch ^ (rr & 7)) * 16)) = h;
+    uint4 h0, h1;
+    s8x16_to_f16(v, h0, h1);
+    uint8_t* row = q16 + (size_t)rr * (2 * D);
+    *reinterpret_cast<uint4*>(row + (((2 * c16) ^ (rr & 7)) * 16)) = h0;
+    *reinterpret_cast<uint4*>(row + (((2 * c16 + 1) ^ (rr & 7)) * 16)) = h1;
   }
   // ---- this warp's 16 rows: (token, head), causal limit, query scale ----
   int row_lim[2];
@@ -154,7 +165,6 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
     sq[h2] = ok ? p.q_scale[(size_t)j * Hq + hq] : 0.f;
   }
   const int warp_lim = __shfl_sync(0xffffffffu, row_lim[1], 31);  // rows are token-major: last row sees most
-  __syncthreads();
 
   float o[ND][4];
 #pragma unroll
@@ -179,46 +189,76 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
         }
       }
     }
-    const int8_t* kt = reinterpret_cast<const int8_t*>(stage_base(b));
-    const int8_t* vt = kt + S::kTileBytes;
-    const float* sks = reinterpret_cast<const float*>(kt + 2 * S::kTileBytes);
-    const float* svs = sks + S::kScaleBytes / 4;
+    __syncthreads();  // every warp is done with the previous stage's f16 tiles
+    // ---- convert the stage once: int8 pages -> f16 tiles, scales -> scs ----
+    {
+      const uint8_t* kt = stage_base(b);
+      const uint8_t* vt = kt + S::kTileBytes;
+      const float* sks = reinterpret_cast<const float*>(kt + 2 * S::kTileBytes);
+      const float* svs = sks + S::kScaleBytes / 4;
+      // K page [D/16][16 tokens][16 B] -> K16 [key][D]
+      for (int i = tid; i < kBlocksPerStage * KC; i += kWarps * 32) {
+        const int pg = i / KC, rem = i % KC;
+        const int c16 = rem / kBS, tk = rem % kBS;
+        const uint4 v = *reinterpret_cast<const uint4*>(kt + (size_t)pg * S::kPage + (size_t)rem * 16);
+        const int key = pg * kBS + tk;
+        uint4 h0, h1;
+        s8x16_to_f16(v, h0, h1);
+        uint8_t* row = k16 + (size_t)key * (2 * D);
+        *reinterpret_cast<uint4*>(row + (((2 * c16) ^ (key & 7)) * 16)) = h0;
+        *reinterpret_cast<uint4*>(row + (((2 * c16 + 1) ^ (key & 7)) * 16)) = h1;
+      }
+      // V page [D][16 tokens] -> V16 [D][64 keys]
+      for (int i = tid; i < kBlocksPerStage * D; i += kWarps * 32) {
+        const int pg = i / D, d = i % D;
+        const uint4 v = *reinterpret_cast<const uint4*>(vt + (size_t)pg * S::kPage + (size_t)d * 16);
+        uint4 h0, h1;
+        s8x16_to_f16(v, h0, h1);
+        uint8_t* row = v16 + (size_t)d * (2 * kKeysPerStage);
+        *reinterpret_cast<uint4*>(row + (((2 * pg) ^ (d & 7)) * 16)) = h0;
+        *reinterpret_cast<uint4*>(row + (((2 * pg + 1) ^ (d & 7)) * 16)) = h1;
+      }
+      if (tid < kKeysPerStage) {
+        scs[2 * tid] = sks[tid * Hkv + kvh];
+        scs[2 * tid + 1] = svs[tid * Hkv + kvh];
+      }
+    }
+    __syncthreads();  // the f16 tiles are ready; the int8 buffer b is free
+    if (tid == 0 && st + kStages < n_stages) issue(st + kStages);
+
 #pragma unroll 1
     for (int grp = 0; grp < kKeysPerStage / 32; ++grp) {
       const int key0 = st * kKeysPerStage + grp * 32;  // absolute position of the group's first key
       if (key0 > warp_lim) break;                       // every row of this warp is past its causal limit
-      // ---- QK: 4 n-tiles of 8 permuted keys, exact on the f16 tensor path ----
+      // ---- QK: 4 n-tiles of 8 keys, exact on the f16 tensor path ----
       float acc[4][4];
 #pragma unroll
       for (int n = 0; n < 4; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
       {
-        // A (query rows, f16): matrices (rows 0-7 | 8-15) x (logical chunk c | c+1)
+        // A (query rows): matrices (rows 0-7 | 8-15) x (dim chunk 2kk | 2kk+1)
         const int qr = warp * 16 + ri + 8 * (mi & 1);
-        const uint8_t* qrow = qs + (size_t)qr * (2 * D);
-        // B (keys, s8): lanes 0-7 n-tile 2*np2 chunk 2s, 8-15 chunk 2s+1, 16-31 n-tile 2*np2+1
-        const int8_t* krow[2];
+        const uint8_t* qrow = q16 + (size_t)qr * (2 * D);
+        // B (keys): matrices (n-tile 2np2 | 2np2+1) x (dim chunk 2kk | 2kk+1)
+        const uint8_t* krow[2];
+        int kxor[2];
 #pragma unroll
         for (int np2 = 0; np2 < 2; ++np2) {
-          const int kl = grp * 32 + group_key(2 * np2 + (mi >> 1), ri);  // key within the stage
-          krow[np2] = kt + (kl >> 4) * S::kPage + (kl & 15) * 16 + (mi & 1) * (kBS * 16);
+          const int key = grp * 32 + 8 * (2 * np2 + (mi >> 1)) + ri;  // key within the stage
+          krow[np2] = k16 + (size_t)key * (2 * D);
+          kxor[np2] = key & 7;
         }
 #pragma unroll
-        for (int s = 0; s < KS; ++s) {
-          uint32_t a1[4], a2[4];
-          ldmatrix_x4(a1, qrow + (((4 * s + (mi >> 1)) ^ (qr & 7)) * 16));
-          ldmatrix_x4(a2, qrow + (((4 * s + 2 + (mi >> 1)) ^ (qr & 7)) * 16));
+        for (int kk = 0; kk < KS; ++kk) {
+          uint32_t a[4];
+          ldmatrix_x4(a, qrow + (((2 * kk + (mi >> 1)) ^ (qr & 7)) * 16));
 #pragma unroll
           for (int np2 = 0; np2 < 2; ++np2) {
-            uint32_t bb[4], f0[4], f1[4];
-            ldmatrix_x4(bb, krow[np2] + (size_t)(2 * s) * (kBS * 16));
-            s8b_to_f16(bb[0], bb[1], f0);
-            s8b_to_f16(bb[2], bb[3], f1);
-            mma_f16_16816(acc[2 * np2], a1[0], a1[1], a1[2], a1[3], f0[0], f0[1]);
-            mma_f16_16816(acc[2 * np2], a2[0], a2[1], a2[2], a2[3], f0[2], f0[3]);
-            mma_f16_16816(acc[2 * np2 + 1], a1[0], a1[1], a1[2], a1[3], f1[0], f1[1]);
-            mma_f16_16816(acc[2 * np2 + 1], a2[0], a2[1], a2[2], a2[3], f1[2], f1[3]);
+            uint32_t bb[4];
+            ldmatrix_x4(bb, krow[np2] + (((2 * kk + (mi & 1)) ^ kxor[np2]) * 16));
+            mma_f16_16816(acc[2 * np2], a[0], a[1], a[2], a[3], bb[0], bb[1]);
+            mma_f16_16816(acc[2 * np2 + 1], a[0], a[1], a[2], a[3], bb[2], bb[3]);
           }
         }
       }
@@ -229,14 +269,12 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
       for (int n = 0; n < 4; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int kg = group_key(n, 2 * t + (e & 1));
-          const int key = key0 + kg;
+          const int kl = grp * 32 + 8 * n + 2 * t + (e & 1);  // key within the stage
+          const int key = st * kKeysPerStage + kl;
           const int h2 = e >> 1;
           float s = -INFINITY;
-          if (key <= row_lim[h2] && key < total_keys) {
-            const int kl = grp * 32 + kg;
-            s = __fmul_rn(__fmul_rn(__fmul_rn(acc[n][e], sq[h2]), sks[kl * Hkv + kvh]), csc);
-          }
+          if (key <= row_lim[h2] && key < total_keys)
+            s = __fmul_rn(__fmul_rn(__fmul_rn(acc[n][e], sq[h2]), scs[2 * kl]), csc);
           sc[n][e] = s;
           mx[h2] = fmaxf(mx[h2], s);
         }
@@ -263,8 +301,7 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
           float pe = 0.f, we = 0.f;
           if (sc[n][e] != -INFINITY) {
             pe = expf(__fsub_rn(sc[n][e], mnew[h2]));
-            const int kl = grp * 32 + group_key(n, 2 * t + (e & 1));
-            we = __fmul_rn(pe, svs[kl * Hkv + kvh]);
+            we = __fmul_rn(pe, scs[2 * (grp * 32 + 8 * n + 2 * t + (e & 1)) + 1]);
           }
           l[h2] += pe;
           w[n][e] = we;
@@ -281,7 +318,7 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
       bool tiny[2];
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
-        sW[h2] = __fdiv_rn(A[h2], 127.0f);
+        sW[h2] = div127(A[h2]);
         ysw[h2] = __frcp_rn(sW[h2]);
         tiny[h2] = sW[h2] < kTinyDivisor;
       }
@@ -293,18 +330,17 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
           const int h2 = e >> 1;
           q[n][e] = A[h2] > 0.f ? rintf(div_shared(w[n][e], sW[h2], ysw[h2], tiny[h2])) : 0.f;
         }
-      // A operand of PV in f16 (exact integers): k16 MMA 1 takes the group's keys
-      // 0..15, MMA 2 keys 16..31, with logical k (2t, 2t+1 | 2t+8, 2t+9) holding
-      // keys (4t, 4t+1 | 4t+2, 4t+3) -- the order s8b_to_f16 gives the V fragments.
-      uint32_t pa1[4], pa2[4];
-      pa1[0] = f16x2_of(q[0][0], q[0][1]);
-      pa1[1] = f16x2_of(q[0][2], q[0][3]);
-      pa1[2] = f16x2_of(q[1][0], q[1][1]);
-      pa1[3] = f16x2_of(q[1][2], q[1][3]);
-      pa2[0] = f16x2_of(q[2][0], q[2][1]);
-      pa2[1] = f16x2_of(q[2][2], q[2][3]);
-      pa2[2] = f16x2_of(q[3][0], q[3][1]);
-      pa2[3] = f16x2_of(q[3][2], q[3][3]);
+      // A operand of PV (exact integers in f16): k16 step kk covers the group's
+      // keys 16kk .. 16kk+15 = score n-tiles 2kk (a0: row g, a1: row g+8) and
+      // 2kk+1 (a2, a3).
+      uint32_t pa[2][4];
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        pa[kk][0] = f16x2_of(q[2 * kk][0], q[2 * kk][1]);
+        pa[kk][1] = f16x2_of(q[2 * kk][2], q[2 * kk][3]);
+        pa[kk][2] = f16x2_of(q[2 * kk + 1][0], q[2 * kk + 1][1]);
+        pa[kk][3] = f16x2_of(q[2 * kk + 1][2], q[2 * kk + 1][3]);
+      }
       if (alpha[0] != 1.f || alpha[1] != 1.f) {
 #pragma unroll
         for (int n = 0; n < ND; ++n) {
@@ -314,31 +350,30 @@ __global__ void __launch_bounds__(kWarps * 32) int8_prefix_kernel(PrefixParams p
           o[n][3] *= alpha[1];
         }
       }
-      // ---- PV: B = V pages (rows = head-dims, 16 keys of one block per row) ----
-      const int8_t* vb = vt + (size_t)(2 * grp + (mi & 1)) * S::kPage + ri * 16 + (mi >> 1) * (8 * 16);
+      // ---- PV: B = V tile [dim][key]: matrices (dim n-tile dn | dn+1) x (key chunk c | c+1) ----
 #pragma unroll
-      for (int n = 0; n < ND; n += 2) {
-        uint32_t bb[4], f0[4], f1[4];
-        ldmatrix_x4(bb, vb + (size_t)n * (8 * 16));
-        s8b_to_f16(bb[0], bb[1], f0);
-        s8b_to_f16(bb[2], bb[3], f1);
+      for (int dn = 0; dn < ND; dn += 2) {
+        const int d = 8 * (dn + (mi >> 1)) + ri;
+        const uint8_t* vrow = v16 + (size_t)d * (2 * kKeysPerStage);
         float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f16_16816(c0, pa1[0], pa1[1], pa1[2], pa1[3], f0[0], f0[1]);
-        mma_f16_16816(c0, pa2[0], pa2[1], pa2[2], pa2[3], f0[2], f0[3]);
-        mma_f16_16816(c1, pa1[0], pa1[1], pa1[2], pa1[3], f1[0], f1[1]);
-        mma_f16_16816(c1, pa2[0], pa2[1], pa2[2], pa2[3], f1[2], f1[3]);
-        o[n][0] += c0[0] * sW[0];
-        o[n][1] += c0[1] * sW[0];
-        o[n][2] += c0[2] * sW[1];
-        o[n][3] += c0[3] * sW[1];
-        o[n + 1][0] += c1[0] * sW[0];
-        o[n + 1][1] += c1[1] * sW[0];
-        o[n + 1][2] += c1[2] * sW[1];
-        o[n + 1][3] += c1[3] * sW[1];
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const int chunk = 4 * grp + 2 * kk + (mi & 1);
+          uint32_t bb[4];
+          ldmatrix_x4(bb, vrow + ((chunk ^ (d & 7)) * 16));
+          mma_f16_16816(c0, pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], bb[0], bb[1]);
+          mma_f16_16816(c1, pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], bb[2], bb[3]);
+        }
+        o[dn][0] = fmaf(c0[0], sW[0], o[dn][0]);
+        o[dn][1] = fmaf(c0[1], sW[0], o[dn][1]);
+        o[dn][2] = fmaf(c0[2], sW[1], o[dn][2]);
+        o[dn][3] = fmaf(c0[3], sW[1], o[dn][3]);
+        o[dn + 1][0] = fmaf(c1[0], sW[0], o[dn + 1][0]);
+        o[dn + 1][1] = fmaf(c1[1], sW[0], o[dn + 1][1]);
+        o[dn + 1][2] = fmaf(c1[2], sW[1], o[dn + 1][2]);
+        o[dn + 1][3] = fmaf(c1[3], sW[1], o[dn + 1][3]);
       }
     }
-    __syncthreads();  // stage buffer b is free
-    if (tid == 0 && st + kStages < n_stages) issue(st + kStages);
   }
 
   // ---- finish: O = o / l ----
@@ -381,6 +416,5 @@ cudaError_t launch_int8_prefix(const PrefixParams& p, cudaStream_t stream) {
   }
   return cudaGetLastError();
 }
-
 
 }  // namespace i8kv
