@@ -616,6 +616,37 @@ def run_profile(args):
     return 0
 
 
+def run_profile_prefix(args):
+    """Prefix-chunk launches only, for profilers: the 16384 + 2048 chunk (24 q / 4 KV
+    heads, head_dim 256), `--warmup` then `--steps` launches."""
+    import torch
+
+    from int8_kv_cache_token_gb300 import build as ibuild
+    ibuild.build()
+    import int8_kv_cache_token_gb300 as i8
+    w = wl.prefix_chunk()
+    k, v = w.kv()
+    cache = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+    i8.kv_quant_write(to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.slots()), **cache)
+    qd = to_dev(torch, w.q())
+    q_i8 = torch.empty(qd.shape, dtype=torch.int8, device="cuda")
+    q_s = torch.empty(qd.shape[:2], dtype=torch.float32, device="cuda")
+    dummy = torch.zeros((w.chunk, w.Hkv, w.D), dtype=torch.bfloat16, device="cuda")
+    none = torch.full((w.chunk,), -1, dtype=torch.int32, device="cuda")
+    i8.kv_quant_write(dummy, dummy, none, **cache, q=qd, q_i8=q_i8, q_scale=q_s)
+    out = torch.empty((w.chunk, w.Hq, w.D), dtype=torch.float32, device="cuda")
+    bt = to_dev(torch, w.block_table)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup + args.steps):
+        i8.int8_prefix_attn(out, q_i8, q_s, cache["k_cache"], cache["v_cache"], cache["k_scale"], cache["v_scale"],
+                            bt, w.history)
+    torch.cuda.synchronize()
+    assert i8.device_error() == 0
+    print(json.dumps({"profile": "int8_prefix", "history": w.history, "chunk": w.chunk,
+                      "launches": args.warmup + args.steps, "int8_ops_per_launch": w.int8_ops()}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -628,9 +659,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",
                     help="decode launches only (the three histories round-robin, --layers caches each) for ncu")
+    ap.add_argument("--profile-prefix", action="store_true",
+                    help="prefix-chunk launches only (16384 + 2048 chunk) for ncu")
     args = ap.parse_args()
     if args.profile:
         return run_profile(args)
+    if args.profile_prefix:
+        return run_profile_prefix(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

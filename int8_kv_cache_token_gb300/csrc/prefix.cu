@@ -84,7 +84,10 @@ __global__ void __launch_bounds__(kWarps * 32, 1) int8_prefix_kernel(PrefixParam
   const int kvh = blockIdx.y;
   const int G = p.G, Hkv = p.Hkv, Hq = p.Hq, H = p.H, C = p.C;
   const int R = C * G;
-  const int r0 = blockIdx.x * kRowsPerCTA;
+  // Row blocks in reverse: later chunk tokens see more keys, and CTAs start in
+  // index order, so the heaviest blocks run first and the partial last wave
+  // holds the lightest ones.
+  const int r0 = (gridDim.x - 1 - blockIdx.x) * kRowsPerCTA;
   const int total_keys = H + C;
   const int j_hi = min(C - 1, (r0 + kRowsPerCTA - 1) / G);
   const int n_keys = H + j_hi + 1;
