@@ -15,7 +15,12 @@
  *    NULL is the legacy default stream).  Nothing synchronizes.  Kernels are
  *    launched with programmatic dependent launch: a kernel may be scheduled
  *    while the previous kernel on the stream is still running, but it reads
- *    no global memory before that kernel has finished.
+ *    no global memory before that kernel has finished -- with one exception:
+ *    the decode kernels read seq_lens and block_tables early (no kernel of
+ *    this library writes them), so these two inputs must not be written by
+ *    the kernel launched just before on the same stream (a host copy, or any
+ *    earlier kernel, is fine).  The decode kernels read them again after the
+ *    wait and record error 3 in the device error word if they changed.
  *  - Argument errors are reported synchronously through the status code, before
  *    anything is launched; i8kv_last_error() gives a one-line reason.  A launch
  *    failure reported by the CUDA runtime maps to I8KV_ERR_CUDA.
@@ -66,7 +71,9 @@ i8kv_status i8kv_last_error(char* buf, size_t n);
 /* Reads and clears the device error word (synchronizes the device).  *code is
  * 0 when no kernel recorded a failure; otherwise the first failure's code:
  * 1 = a pipeline wait exceeded its time limit, 2 = a block-table or slot entry
- * or sequence length out of range (the access was skipped).  Returns
+ * or sequence length out of range (the access was skipped), 3 = seq_lens or
+ * block_tables changed while a decode kernel was starting (they were written
+ * by the kernel just before it on the stream; the result is undefined).  Returns
  * I8KV_ERR_DEVICE if *code != 0. */
 i8kv_status i8kv_device_error(int* code);
 

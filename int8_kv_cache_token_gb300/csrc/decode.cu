@@ -173,15 +173,38 @@ __device__ __forceinline__ void walk_next(Walk& w, const int32_t* seq_lens, int 
   w.n = unit_granules(w, g_end);
 }
 
+// floor(a / d), d >= 1.  Below 2^22 the product of the exact operand a and a
+// reciprocal of d within one ulp, rounded toward zero, is within 2^-22 a / d < 1
+// of the quotient, so its integer part is off by at most one and one remainder
+// step corrects it: a few instructions where the integer division is a long
+// dependent sequence (the kernel's start-up path runs several in a row).
+__device__ __forceinline__ unsigned udiv_fast(unsigned a, unsigned d) {
+  if (a >= (1u << 22) || d >= (1u << 22)) return a / d;
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(__uint2float_rn(d)));
+  unsigned q = __float2uint_rz(__fmul_rz(__uint2float_rn(a), r));
+  const int rem = (int)(a - q * d);  // q * d <= a + d < 2^23
+  if (rem < 0)
+    --q;
+  else if (rem >= (int)d)
+    ++q;
+  return q;
+}
+
 // floor(U * c / N), in 32-bit arithmetic when U fits (the 64-bit division is a
 // long instruction sequence on the kernel's start-up path).
 __device__ __forceinline__ long long split_point(long long U, int c, int N) {
   if (U < (1ll << 31)) {
-    const unsigned u = (unsigned)U, q = u / (unsigned)N, r = u % (unsigned)N;
-    return (long long)q * c + (r * (unsigned)c) / (unsigned)N;
+    const unsigned u = (unsigned)U, q = udiv_fast(u, (unsigned)N), r = u - q * (unsigned)N;
+    return (long long)q * c + udiv_fast(r * (unsigned)c, (unsigned)N);
   }
   return U * c / N;
 }
+
+// Hash of the sequence lengths one lane reads (its lanes' entries in chunk
+// order), to see whether they changed between the read before griddep_wait()
+// and the one after it.
+__device__ __forceinline__ uint32_t len_hash(uint32_t h, int raw) { return h * 0x9E3779B1u + (uint32_t)raw; }
 
 // CTA whose granule range [c*U/N, (c+1)*U/N) holds granule u (N <= U: no empty ranges).
 __device__ __forceinline__ int cta_of(long long u, long long U, int N) {
@@ -201,10 +224,19 @@ struct Ring {
   // of the ring holds V items, which wait for the QK warps' handoff.
   __host__ __device__ explicit Ring(int nslots)
       : kK(nslots / 6 > 0 ? nslots / 6 : 1), nV(nslots - 2 * (nslots / 6 > 0 ? nslots / 6 : 1)) {}
-  __device__ int kslot(int i) const { return (i % 2) * kK + (i / 2) % kK; }
-  __device__ int kuse(int i) const { return (i / 2) / kK; }  // earlier uses of the slot
-  __device__ int vslot(int i) const { return 2 * kK + i % nV; }
-  __device__ int vuse(int i) const { return i / nV; }
+};
+
+// A position in a ring of n slots: the slot, and how many times the ring was
+// passed before it (whose parity is the phase to wait for).  It advances one
+// item at a time, so the pipeline loops do no division.
+struct RingPos {
+  int s = 0, use = 0;
+  __device__ void next(int n) {
+    if (++s == n) {
+      s = 0;
+      ++use;
+    }
+  }
 };
 
 // Bounded pipeline wait.  After a timeout (error 1) or once the CTA aborted,
@@ -417,25 +449,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     }
     fence_mbar_init();
   }
-  // Everything above touches only shared memory; from here on the kernel reads
-  // what earlier work on the stream wrote.
-  griddep_wait();
-  griddep_launch_dependents();
-
-  // ---- work split, by the producer warp (the others wait at the barrier
-  // below; they have nothing to do before it) ----
+  // ---- work split, by the producer warp, before the wait on earlier work ----
+  // seq_lens and block_tables are the only global memory read before
+  // griddep_wait(), and nothing is written before it.  No kernel of this
+  // library writes them, and reading them early overlaps their latency (and the
+  // split's arithmetic) with the end of the previous kernel on the stream.  They
+  // are read past L1 (ld.global.cg), so no stale line outlives the wait; after
+  // it the producer warp reads them again and records error 3 if they changed
+  // (the caller wrote them in the kernel just before this one).
+  //
   // One sequence in the batch (the long-context decode case): guess the first
   // unit from max_blocks and load its block-table row together with seq_lens,
   // so the two dependent loads overlap; the guess is checked below.
   int spec_gi = -1, spec_blk = -1;
+  uint32_t lhash = 0;  // this lane's sequence lengths, for the check after the wait
   if (warp == kProdWarp && B == 1) {
     const int ngp_g = (maxL + kGran - 1) / kGran;
     const long long U_g = (long long)ngp_g * Hkv;
     const int Nw_g = (int)(U_g < N ? U_g : N);
     if (c < Nw_g) {
-      spec_gi = (int)(split_point(U_g, c, Nw_g) % ngp_g);
+      const long long ub_g = split_point(U_g, c, Nw_g);  // < U_g
+      spec_gi = ub_g < (1ll << 31) ? (int)((unsigned)ub_g - udiv_fast((unsigned)ub_g, ngp_g) * ngp_g)
+                                   : (int)(ub_g % ngp_g);
       const int pg = spec_gi * kGran / kBS + lane;
-      if (lane < kBlocksU && pg < p.max_blocks) spec_blk = __ldg(p.block_tables + pg);
+      if (lane < kBlocksU && pg < p.max_blocks) spec_blk = __ldcg(p.block_tables + pg);
     }
   }
   if (warp == kProdWarp) {
@@ -446,15 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       const int b = b0 + lane;
       int u = 0, L = 0;
       if (b < B) {
-        const int raw = p.seq_lens[b];
-        if (raw > maxL) record_error(2);
+        const int raw = __ldcg(p.seq_lens + b);
+        lhash = len_hash(lhash, raw);
         L = clamp_len(raw, maxL);
         u = (L + kGran - 1) / kGran * Hkv;
-        if (L == 0 && b % N == c) {  // empty sequence: zero rows, nothing to merge
-          float* o = p.out + (size_t)b * Hq * D;
-          for (int i = 0; i < Hq * D; ++i) o[i] = 0.f;
-          for (int h = 0; h < Hkv; ++h) p.ws_info[b * Hkv + h] = -1;
-        }
       }
 #pragma unroll
       for (int k = 0; k < kKeep; ++k)
@@ -491,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
               L = lkeep[k];
             }
         } else if (b < B) {
-          L = clamp_len(p.seq_lens[b], maxL);
+          L = clamp_len(__ldcg(p.seq_lens + b), maxL);
           u = (L + kGran - 1) / kGran * Hkv;
         }
         int incl = u;
@@ -503,11 +535,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         const unsigned hit = __ballot_sync(0xffffffffu, u > 0 && ex <= ub && ub < in);
         if (hit) {
           if (lane == __ffs(hit) - 1) {
-            const int np = u / Hkv;
-            const int local = (int)(ub - ex);  // < np * Hkv
+            const unsigned np = (unsigned)((L + kGran - 1) / kGran);  // granules per pair
+            const unsigned local = (unsigned)(ub - ex);                // < np * Hkv
+            const unsigned kv = udiv_fast(local, np);
             ctrl[1] = b;
-            ctrl[2] = local / np;
-            ctrl[3] = local % np;
+            ctrl[2] = (int)kv;
+            ctrl[3] = (int)(local - kv * np);
             ctrl[4] = (int)(ex & 0x7fffffff);
             ctrl[5] = (int)(ex >> 31);
             ctrl[9] = L;
@@ -520,7 +553,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   }
   __syncthreads();  // the split in ctrl[] is visible to every warp
   const int n_gran = ctrl[0];
-  if (n_gran <= 0) return;
   Walk w0;
   w0.b = ctrl[1];
   w0.kvh = ctrl[2];
@@ -530,7 +562,48 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   w0.ngp = (w0.L + kGran - 1) / kGran;
   w0.gc = w0.gb + (long long)w0.kvh * w0.ngp + w0.gi;
   const long long g_end = w0.gc + n_gran;  // end of this CTA's granule range
-  w0.n = unit_granules(w0, g_end);
+  w0.n = n_gran > 0 ? unit_granules(w0, g_end) : 0;
+  // This lane's page of the first unit (lanes below the unit's page count).
+  auto first_blk_lanes = [&]() {
+    const int t0 = w0.gi * kGran;
+    return (min(w0.n * kGran, w0.L - t0) + kBS - 1) / kBS;
+  };
+  int blk_first = -1;
+  if (warp == kProdWarp && n_gran > 0 && lane < first_blk_lanes()) {
+    blk_first = (B == 1 && w0.gi == spec_gi)
+                    ? spec_blk
+                    : __ldcg(p.block_tables + (size_t)w0.b * p.max_blocks + w0.gi * kGran / kBS + lane);
+  }
+  // From here on the kernel reads and writes what earlier work on the stream uses.
+  griddep_wait();
+  griddep_launch_dependents();
+  // The producer warp, after the wait: sequence lengths above the table are
+  // recorded (error 2); empty sequences get zero rows and no merge; the inputs
+  // read before the wait must not have changed (error 3).
+  auto check_inputs = [&]() {
+    uint32_t h = 0;
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int b = b0 + lane;
+      if (b < B) {
+        const int raw = p.seq_lens[b];
+        h = len_hash(h, raw);
+        if (raw > maxL) record_error(2);
+        if (clamp_len(raw, maxL) == 0 && b % N == c) {
+          float* o = p.out + (size_t)b * Hq * D;
+          for (int i = 0; i < Hq * D; ++i) o[i] = 0.f;
+          for (int hh = 0; hh < Hkv; ++hh) p.ws_info[b * Hkv + hh] = -1;
+        }
+      }
+    }
+    bool changed = h != lhash;
+    if (n_gran > 0 && lane < first_blk_lanes())
+      changed |= p.block_tables[(size_t)w0.b * p.max_blocks + w0.gi * kGran / kBS + lane] != blk_first;
+    if (__any_sync(0xffffffffu, changed) && lane == 0) record_error(3);
+  };
+  if (n_gran <= 0) {
+    if (warp == kProdWarp) check_inputs();
+    return;
+  }
   const long long U = (long long)ctrl[6] | ((long long)ctrl[7] << 31);
   const int Nw = ctrl[10];
   const int g = lane >> 2, t = lane & 3;
@@ -543,21 +616,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     const uint64_t pol = policy_evict_first();
     // This lane's page of a unit (lanes below the unit's page count), read from
     // the block table one unit ahead of its use.
-    auto load_blk = [&](const Walk& u, int i) {
+    auto load_blk = [&](const Walk& u) {
       const int t0 = u.gi * kGran;
       const int nb = (min(u.n * kGran, u.L - t0) + kBS - 1) / kBS;
       if (lane >= nb) return -1;
-      if (i == 0 && B == 1 && u.gi == spec_gi) return spec_blk;
       return p.block_tables[(size_t)u.b * p.max_blocks + t0 / kBS + lane];
     };
     Walk wk = w0, wn = w0;
     walk_next(wn, p.seq_lens, B, Hkv, maxL, kGran, g_end);
-    int blk_cur = load_blk(wk, 0);
+    int blk_cur = blk_first;
     int n_k = 0, n_v = 0;  // K and V items issued
+    RingPos kp_cur, kp_oth, vp;  // K positions of this unit's stream and of the other; V position
     uint32_t nt_k[D / 128], nt_v[D / 128];  // decode step: the new token's codes
     for (int i = 0; wk.n > 0; ++i) {
       if (*abort_flag) break;
-      const int blk_nx = wn.n > 0 ? load_blk(wn, i + 1) : -1;  // in flight meanwhile
+      const int blk_nx = wn.n > 0 ? load_blk(wn) : -1;  // in flight meanwhile
       const int t0 = wk.gi * kGran;
       const int ntok = min(wk.n * kGran, wk.L - t0);
       const int nblk = (ntok + kBS - 1) / kBS;
@@ -570,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       const uint32_t n_pages = __popc(__ballot_sync(0xffffffffu, ok));
       // K item: the pages by bulk copy, the unit's (sK, sV) per token by cp.async;
       // the slot's full barrier waits for both.
-      const int kslot = rg.kslot(i), ku = rg.kuse(i);
+      const int kslot = (i & 1) * rg.kK + kp_cur.s, ku = kp_cur.use;
       if (ku > 0) pipe_wait(&empty[kslot], (ku - 1) & 1, abort_flag);
       if (*abort_flag) break;  // never refill a slot whose previous item was not consumed
       if (lane == 0) mbar_expect_tx(&full[kslot], n_pages * kPage);
@@ -637,7 +710,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       mbar_arrive(&full[kslot]);
       ++n_k;
       // V item
-      const int vslot = rg.vslot(i), vu = rg.vuse(i);
+      kp_cur.next(rg.kK);
+      {
+        const RingPos tmp = kp_cur;  // the next unit belongs to the other stream
+        kp_cur = kp_oth;
+        kp_oth = tmp;
+      }
+      const int vslot = 2 * rg.kK + vp.s, vu = vp.use;
       if (vu > 0) pipe_wait(&empty[vslot], (vu - 1) & 1, abort_flag);
       if (*abort_flag) break;
       if (lane == 0) mbar_expect_tx(&full[vslot], n_pages * kPage);
@@ -657,6 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       }
       mbar_arrive(&full[vslot]);
       ++n_v;
+      vp.next(rg.nV);
       blk_cur = blk_nx;
       wk = wn;
       walk_next(wn, p.seq_lens, B, Hkv, maxL, kGran, g_end);
@@ -680,6 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         if (uses > 0) mbar_wait(&full[sl], (uses - 1) & 1);
       }
     }
+    check_inputs();
     return;
   }
 
@@ -700,6 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     uint32_t qf[D / 32][4];    // INT8: converted query fragments
     uint32_t qfb[D / 16][2];   // BF16: query fragments
     float sq[2] = {0.f, 0.f};
+    RingPos kpos;  // this stream's K slots
     for (int i = st; wk.n > 0; i += kStreams) {
       const int pair = wk.b * Hkv + wk.kvh;
       if (pair != cur_pair) {
@@ -750,8 +832,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       const bool active = qw < wk.n;  // every granule of the unit holds tokens
 
       // ---- K item: QK of this warp's tokens, and their scales ----
-      const int kslot = rg.kslot(i);
-      pipe_wait(&full[kslot], rg.kuse(i) & 1, abort_flag);
+      const int kslot = st * rg.kK + kpos.s;
+      pipe_wait(&full[kslot], kpos.use & 1, abort_flag);
+      kpos.next(rg.kK);
       const uint8_t* kb = ring + (size_t)kslot * kSlot;
       if constexpr (!BF16) {
         // decode step: the warp whose granule holds the new token patches its K row
@@ -913,6 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   Walk wk = w0, w1 = w0;
   walk_next(w1, p.seq_lens, B, Hkv, maxL, kGran, g_end);
   int cur_pair = -1;
+  RingPos vpos;  // V slots
   float o[NDT][4];
   float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
   for (int i = 0; wk.n > 0; ++i) {
@@ -968,8 +1052,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     }
 
     // ---- V item: this warp's head-dims, every group of the unit ----
-    const int vslot = rg.vslot(i);
-    pipe_wait(&full[vslot], rg.vuse(i) & 1, abort_flag);
+    const int vslot = 2 * rg.kK + vpos.s;
+    pipe_wait(&full[vslot], vpos.use & 1, abort_flag);
+    vpos.next(rg.nV);
     const uint8_t* vb = ring + (size_t)vslot * kSlot;
     if constexpr (!BF16) {
       // decode step: every PV warp patches its own head-dims of the new token's V column

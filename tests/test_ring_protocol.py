@@ -10,7 +10,9 @@ out-of-order copy completion:
   * two QK streams take the even and odd units, each through its own K slots;
   * the PV warps take every unit's V slot and its handoff buffer (unit i uses
     buffer i % 4).
-The slot and phase formulas are the kernel's (struct Ring in decode.cu).  The
+The slot and phase formulas are the closed forms of the kernel's ring (struct
+Ring in decode.cu); the kernel reaches them by stepping a RingPos per item,
+and a test below checks that the stepping gives the closed forms.  The
 model also shows that one ring whose K slots alternate between the two streams
 does fail (a stream reads a slot before its copy lands), which is why each
 stream has its own K slots.
@@ -125,3 +127,38 @@ def test_alternating_k_slots_do_race():
         except AssertionError:
             failures += 1
     assert failures > 0
+
+
+class RingPos:
+    """The kernel's incremental ring position (slot, earlier passes)."""
+
+    def __init__(self):
+        self.s, self.use = 0, 0
+
+    def next(self, n):
+        self.s += 1
+        if self.s == n:
+            self.s, self.use = 0, self.use + 1
+
+
+@pytest.mark.parametrize("nslots", [4, 6, 8, 10, 12])
+def test_stepped_positions_equal_the_closed_forms(nslots):
+    kK = max(1, nslots // 6)
+    nV = nslots - 2 * kK
+    ring = kernel_ring(nslots)
+    # producer: one K position per stream, swapped after every unit; one V position
+    cur, oth, vp = RingPos(), RingPos(), RingPos()
+    # consumers: each QK stream steps its own K position; the PV warps step the V position
+    qk = [RingPos(), RingPos()]
+    pv = RingPos()
+    for i in range(200):
+        assert ((i & 1) * kK + cur.s, cur.use) == (ring["kslot"](i), ring["kuse"](i))
+        cur.next(kK)
+        cur, oth = oth, cur
+        assert (2 * kK + vp.s, vp.use) == (ring["vslot"](i), ring["vuse"](i))
+        vp.next(nV)
+        st = i % 2
+        assert (st * kK + qk[st].s, qk[st].use) == (ring["kslot"](i), ring["kuse"](i))
+        qk[st].next(kK)
+        assert (2 * kK + pv.s, pv.use) == (ring["vslot"](i), ring["vuse"](i))
+        pv.next(nV)
