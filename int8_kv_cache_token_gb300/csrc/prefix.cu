@@ -1,4 +1,5 @@
-// prefix.cu -- INT8 prefix-prefill chunk attention.
+// prefix.cu -- INT8 prefix-prefill chunk attention on the 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory).
 //
 // Source: "gfx936 DCU上实现INT8 PV MMAC：V Scale融合、概率量化与Fragment分组"
 // §2.1 (the prefix keeps one online softmax (m, l, o); alpha = exp(m - m'),
@@ -8,21 +9,29 @@
 // INT8 MMAC Attention推理优化" §3.2 (history and the chunk's own K/V in one
 // online softmax, never two attentions merged afterwards).
 //
-// GB300 shape.  A CTA owns 128 query rows of one KV head (8 warps x 16 rows);
-// the rows are (chunk token, query head) pairs of that KV head's GQA group,
-// token-major, so the query heads sharing K/V read the same tiles.  K/V pages
-// of 64 keys per stage arrive by bulk copy into a double-buffered int8 staging
-// area.  Each stage is then converted once, by all warps together, into f16
-// tiles in shared memory: K as [key][dim] and V as [dim][key], 16-byte chunks
-// XOR-swizzled so that ldmatrix reads them without bank conflicts.  The int8
-// values are exact in f16, every product is exact and every partial sum stays
-// below 2^22, so the f16 tensor-core MMAs with fp32 accumulation give the exact
-// int32 results of the INT8 contractions (QK over D dims; PV over one 32-key
-// group).  Each warp keeps its rows' softmax state and FP32 output in registers
-// (FlashAttention-2 style).  Per 32-key group: QK, scores, causal mask, online
-// softmax, W = p~ x sV, per-row group absmax, sW = A / 127 and the codes
-// round(W / sW) (IEEE quotients, as the oracle), then PV with the codes as the
-// A operand and sW x (the exact product) added to the output.
+// GB300 shape.  A CTA owns 128 query rows of one KV head -- (chunk token, query
+// head) pairs of that head's GQA group, token-major, so the query heads sharing
+// K/V read the same tiles -- and walks the keys in 32-key probability groups:
+//   S  = Qq x Kq^T        tcgen05, M = 128, N = 32, K = D, into TMEM
+//   scores, causal mask, online softmax, W = p~ sV, sW = max W / 127,
+//   Wq = round(W / sW)    CUDA cores, one thread per (row, half of the keys)
+//   PV = Wq x Vq          tcgen05, M = 128, N = D, K = 32, into TMEM
+//   o  = alpha o + sW PV  CUDA cores, o in registers (half of D per thread)
+// The int8 codes are exact in f16, every product (<= 127^2) is exact and every
+// partial sum stays below 2^22, so f16 MMAs with fp32 accumulation give the
+// INT8 contractions' exact integer results.
+//
+// Warps.  Warp 0 lane 0 issues the bulk copies of each group's int8 pages and
+// scale rows (three groups in flight); warps 0, 2 and 3 convert each group
+// once into f16 operand tiles (K-major, 16-byte chunks XOR-swizzled: K as
+// [key][dim] in 128-byte rows, V as [dim][key] in 64-byte rows).  Warp 1 owns
+// the TMEM allocation; its lane 0 issues every MMA.  Warps 4-7 and 8-11 are two
+// halves: thread (half, row) takes keys 16 half .. 16 half + 15 of each group
+// for its row's softmax (the halves exchange the row's group maximum and
+// absmax through shared memory) and output dims [half D/2, (half + 1) D/2).
+// S is double-buffered in TMEM, so the QK of the next group runs during a
+// softmax; the PV of group g runs during the softmax of g + 1, after which the
+// output takes group g's product.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -32,30 +41,51 @@ I8KV_DEFINE_ERROR_ACCESSOR(read_error_prefix)
 namespace {
 
 constexpr int kBS = 16;
-constexpr int kWarps = 8;
-constexpr int kRowsPerCTA = kWarps * 16;
-constexpr int kKeysPerStage = 64;  // 4 blocks
-constexpr int kBlocksPerStage = kKeysPerStage / kBS;
-constexpr int kStages = 2;         // int8 staging buffers
+constexpr int kRows = 128;       // query rows per CTA: the MMA's M, one TMEM lane each
+constexpr int kGroup = 32;       // keys per probability group
+constexpr int kPagesPG = kGroup / kBS;
+constexpr int kStages = 3;       // int8 staging buffers (groups in flight)
 constexpr int kMaxHkv = 8;
+constexpr int kThreads = 384;
+constexpr int kMmaWarp = 1;
+constexpr int kCompWarp0 = 4;    // warps 4..11
+constexpr int kConvThreads = 96; // warps 0, 2, 3
+constexpr int kCompThreads = 256;
 
 template <int D>
-struct PrefixSmem {
-  static constexpr int kPage = D * kBS;                           // int8 page
-  static constexpr int kTileBytes = kBlocksPerStage * kPage;      // int8 K (or V) tile of a stage
-  static constexpr int kScaleBytes = kBlocksPerStage * kBS * kMaxHkv * 4;
-  static constexpr int kStageBytes = 2 * kTileBytes + 2 * kScaleBytes;
-  static constexpr int kK16 = kKeysPerStage * D * 2;              // f16 K [64 keys][D]
-  static constexpr int kV16 = D * kKeysPerStage * 2;              // f16 V [D][64 keys]
-  static constexpr int kQ16 = kRowsPerCTA * D * 2;                // f16 Q [128 rows][D]
-  static constexpr int kSc = kKeysPerStage * 2 * 4;               // the stage's (sK, sV) per key
-  static constexpr int kOffK16 = kStages * kStageBytes;
-  static constexpr int kOffV16 = kOffK16 + kK16;
-  static constexpr int kOffQ16 = kOffV16 + kV16;
-  static constexpr int kOffSc = kOffQ16 + kQ16;
-  static constexpr int kOffBar = kOffSc + kSc;
-  static constexpr int kTotal = kOffBar + 64;
+struct Lay {
+  static constexpr int kQ16 = kRows * D * 2;          // f16 Q, D/64 atoms of [128 rows][128 B]
+  static constexpr int kK16 = kGroup * D * 2;         // f16 K, D/64 atoms of [32 keys][128 B]
+  static constexpr int kV16 = D * kGroup * 2;         // f16 V, [D][64 B]
+  static constexpr int kP16 = kRows * kGroup * 2;     // f16 Wq, [128][64 B]
+  static constexpr int kPage = D * kBS;               // one int8 K or V page
+  static constexpr int kSRow = kBS * kMaxHkv * 4;     // one block's scale rows (room for kMaxHkv heads)
+  static constexpr int kStage = 2 * kPagesPG * kPage + 2 * kPagesPG * kSRow;
+  static constexpr int oQ = 0;
+  static constexpr int oK = oQ + kQ16;                // two slots
+  static constexpr int oV = oK + 2 * kK16;            // two slots
+  static constexpr int oP = oV + 2 * kV16;            // two slots
+  static constexpr int oStage = oP + 2 * kP16;        // kStages
+  static constexpr int oSc = oStage + kStages * kStage;  // two slots of [32 keys][sK, sV]
+  static constexpr int oX = oSc + 2 * kGroup * 8;     // exchange: [3 values][2 halves][128 rows] floats
+  static constexpr int oBar = oX + 3 * 2 * kRows * 4;
+  // barriers: stage_full[3], conv_full[2], s_full[2], s_free[2], p_full[2], mma_done[2], pv_free
+  static constexpr int kBars = kStages + 2 + 2 + 2 + 2 + 2 + 1;
+  static constexpr int oCtl = oBar + kBars * 8;       // TMEM base, abort flag
+  static constexpr int kTotal = oCtl + 16;
+  // TMEM: S in columns [0, 64) (two slots of 32), PV in [kPVCol, kPVCol + D)
+  static constexpr uint32_t kPVCol = D == 256 ? 256 : 128;
+  static constexpr uint32_t kTmemCols = D == 256 ? 512 : 256;
 };
+
+// Byte offset of 16-byte chunk `chunk16` of row r in a K-major tile with
+// SWZ-byte rows, the chunk index XOR-swizzled by the row's place in its
+// 8-row (SWZ = 128) or 8-row-pair (SWZ = 64) pattern, as the tensor cores read it.
+template <int SWZ>
+__device__ __forceinline__ uint32_t swz_chunk(int r, int chunk16) {
+  constexpr int mask = SWZ == 128 ? 7 : 3;
+  return (uint32_t)(r * SWZ + ((chunk16 ^ ((r * SWZ >> 7) & mask)) << 4));
+}
 
 // 16 int8 codes (one 16-byte chunk) -> 16 exact f16 values, natural order.
 __device__ __forceinline__ void s8x16_to_f16(const uint4& v, uint4& h0, uint4& h1) {
@@ -65,338 +95,369 @@ __device__ __forceinline__ void s8x16_to_f16(const uint4& v, uint4& h0, uint4& h
   s8x4_to_f16(v.w, h1.z, h1.w);
 }
 
+// Bounded wait that gives up at once when the CTA has aborted (error 1 after
+// the time limit); every thread still runs the same loop and the same named
+// barriers, so no thread waits on a barrier another one skipped.
+__device__ __forceinline__ void pwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return;
+  if (*abort_flag) return;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+    if (*abort_flag) return;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      record_error(1);
+      *abort_flag = 1;
+      return;
+    }
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32, 1) int8_prefix_kernel(PrefixParams p) {
-  using S = PrefixSmem<D>;
-  constexpr int KS = D / 16;  // k16 steps of QK
-  constexpr int ND = D / 8;   // n-tiles of PV
-  constexpr int KC = (D / 16) * kBS;  // int8 chunks of one K page
+__global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p) {
+  using Ly = Lay<D>;
+  constexpr int DH = D / 2;  // output dims per half
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* k16 = smem + S::kOffK16;
-  uint8_t* v16 = smem + S::kOffV16;
-  uint8_t* q16 = smem + S::kOffQ16;
-  float* scs = reinterpret_cast<float*>(smem + S::kOffSc);  // [64 keys][sK, sV]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kOffBar);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kStages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::oBar);
+  uint64_t* stage_full = bars;
+  uint64_t* conv_full = stage_full + kStages;
+  uint64_t* s_full = conv_full + 2;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* mma_done = p_full + 2;  // PV of group g done: its slots and the PV accumulator are readable/free
+  uint64_t* pv_free = mma_done + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::oCtl);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::oCtl + 4);
+  float* xch = reinterpret_cast<float*>(smem + Ly::oX);  // [value][half][row]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t = lane & 3;
   const int kvh = blockIdx.y;
   const int G = p.G, Hkv = p.Hkv, Hq = p.Hq, H = p.H, C = p.C;
   const int R = C * G;
   // Row blocks in reverse: later chunk tokens see more keys, and CTAs start in
-  // index order, so the heaviest blocks run first and the partial last wave
-  // holds the lightest ones.
-  const int r0 = (gridDim.x - 1 - blockIdx.x) * kRowsPerCTA;
-  const int total_keys = H + C;
-  const int j_hi = min(C - 1, (r0 + kRowsPerCTA - 1) / G);
+  // index order, so the heaviest blocks run first and the last wave holds the
+  // lightest ones.
+  const int r0 = (gridDim.x - 1 - blockIdx.x) * kRows;
+  const int j_hi = min(C - 1, (r0 + kRows - 1) / G);
   const int n_keys = H + j_hi + 1;
-  const int n_stages = (n_keys + kKeysPerStage - 1) / kKeysPerStage;
-  const int max_blk = (total_keys + kBS - 1) / kBS;
-
-  auto stage_base = [&](int b) { return smem + (size_t)b * S::kStageBytes; };
-  auto issue = [&](int st) {
-    const int b = st % kStages;
-    uint8_t* base = stage_base(b);
-    int nb = 0;
-    int blks[kBlocksPerStage];
-#pragma unroll
-    for (int i = 0; i < kBlocksPerStage; ++i) {
-      const int lb = st * kBlocksPerStage + i;
-      int blk = -1;
-      if (lb < max_blk) {
-        blk = p.block_table[lb];
-        if (blk < 0 || blk >= p.num_blocks) {
-          record_error(2);
-          blk = -1;
-        }
-      }
-      blks[i] = blk;
-      nb += blk >= 0;
-    }
-    const uint32_t srow = kBS * Hkv * 4;
-    mbar_expect_tx(&full[b], nb * (2 * S::kPage + 2 * srow));
-#pragma unroll
-    for (int i = 0; i < kBlocksPerStage; ++i) {
-      if (blks[i] < 0) continue;
-      const size_t page = ((size_t)blks[i] * Hkv + kvh) * S::kPage;
-      bulk_g2s(base + i * S::kPage, p.k_cache + page, S::kPage, &full[b]);
-      bulk_g2s(base + S::kTileBytes + i * S::kPage, p.v_cache + page, S::kPage, &full[b]);
-      bulk_g2s(base + 2 * S::kTileBytes + i * srow, p.k_scale + (size_t)blks[i] * kBS * Hkv, srow, &full[b]);
-      bulk_g2s(base + 2 * S::kTileBytes + S::kScaleBytes + i * srow, p.v_scale + (size_t)blks[i] * kBS * Hkv, srow,
-               &full[b]);
-    }
-    mbar_arrive(&full[b]);
-  };
+  const int ng = (n_keys + kGroup - 1) / kGroup;
+  const int max_blk = (H + C + kBS - 1) / kBS;
 
   if (tid == 0) {
-    for (int b = 0; b < kStages; ++b) mbar_init(&full[b], 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&stage_full[s], 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&conv_full[s], kConvThreads);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], kCompThreads);
+      mbar_init(&p_full[s], kCompThreads);
+      mbar_init(&mma_done[s], 1);
+    }
+    mbar_init(pv_free, kCompThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, Ly::kTmemCols);
+  tc_fence_before();
   __syncthreads();
-  if (tid == 0) {
-    for (int st = 0; st < kStages && st < n_stages; ++st) issue(st);
-  }
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // From here on the kernel reads what earlier work on the stream wrote.
+  griddep_wait();
+  griddep_launch_dependents();
 
-  // ---- query tile -> shared memory as exact f16, natural dim order; 16-byte
-  // chunk c of row r is stored at chunk c ^ (r & 7) ----
-  for (int i = tid; i < kRowsPerCTA * (D / 16); i += kWarps * 32) {
-    const int rr = i / (D / 16), c16 = i % (D / 16);
-    const int r = r0 + rr;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r < R) {
-      const int j = r / G, hq = kvh * G + r % G;
-      v = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)j * Hq + hq) * D) + c16);
+  // ---- Q tile -> f16 (all threads), K-major SW128 ----
+  {
+    uint8_t* q16 = smem + Ly::oQ;
+    constexpr int CH = D / 16;  // int8 chunks per row
+    for (int i = tid; i < kRows * CH; i += kThreads) {
+      const int rr = i / CH, dc = i % CH;
+      const int r = r0 + rr;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < R) {
+        const int j = r / G, hq = kvh * G + r % G;
+        v = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)j * Hq + hq) * D) + dc);
+      }
+      uint4 h0, h1;
+      s8x16_to_f16(v, h0, h1);
+      uint8_t* atom = q16 + (size_t)(dc / 4) * (kRows * 128);
+      *reinterpret_cast<uint4*>(atom + swz_chunk<128>(rr, 2 * (dc % 4))) = h0;
+      *reinterpret_cast<uint4*>(atom + swz_chunk<128>(rr, 2 * (dc % 4) + 1)) = h1;
     }
-    uint4 h0, h1;
-    s8x16_to_f16(v, h0, h1);
-    uint8_t* row = q16 + (size_t)rr * (2 * D);
-    *reinterpret_cast<uint4*>(row + (((2 * c16) ^ (rr & 7)) * 16)) = h0;
-    *reinterpret_cast<uint4*>(row + (((2 * c16 + 1) ^ (rr & 7)) * 16)) = h1;
+    fence_async_smem();
   }
-  // ---- this warp's 16 rows: (token, head), causal limit, query scale ----
-  int row_lim[2];
-  float sq[2];
-#pragma unroll
-  for (int h2 = 0; h2 < 2; ++h2) {
-    const int r = r0 + warp * 16 + g + 8 * h2;
-    const bool ok = r < R;
-    const int j = ok ? r / G : C - 1;
-    const int hq = kvh * G + (ok ? r % G : 0);
-    row_lim[h2] = H + j;  // last visible key
-    sq[h2] = ok ? p.q_scale[(size_t)j * Hq + hq] : 0.f;
-  }
-  const int warp_lim = __shfl_sync(0xffffffffu, row_lim[1], 31);  // rows are token-major: last row sees most
+  __syncthreads();
 
-  float o[ND][4];
+  if (warp < kCompWarp0) {
+    regs_dec<56>();  // warpgroup 0 hands registers to the softmax/output warpgroups
+    if (warp != kMmaWarp) {
+      // ================= copies and conversion (warps 0, 2, 3) =================
+      const int ct = warp == 0 ? lane : tid - 32;  // 0 .. 95
+      const uint32_t srow = kBS * Hkv * 4;
+      auto issue = [&](int g) {  // warp 0 lane 0
+        const int st = g % kStages;
+        uint8_t* base = smem + Ly::oStage + (size_t)st * Ly::kStage;
+        int blks[kPagesPG];
+        int nb = 0;
 #pragma unroll
-  for (int n = 0; n < ND; ++n)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) o[n][e] = 0.f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-  const float csc = p.sm_scale;
-  const int mi = lane >> 3, ri = lane & 7;
-
-  for (int st = 0; st < n_stages; ++st) {
-    const int b = st % kStages;
-    // bounded wait (see common.cuh); every thread passes the same barriers
-    if (!mbar_try_wait(&full[b], (st / kStages) & 1)) {
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(&full[b], (st / kStages) & 1)) {
-        if (*abort_flag) break;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-          record_error(1);
-          *abort_flag = 1;
-          break;
+        for (int i = 0; i < kPagesPG; ++i) {
+          const int lb = g * kPagesPG + i;
+          int blk = -1;
+          if (lb < max_blk) {
+            blk = p.block_table[lb];
+            if (blk < 0 || blk >= p.num_blocks) {
+              record_error(2);
+              blk = -1;
+            }
+          }
+          blks[i] = blk;
+          nb += blk >= 0;
         }
-      }
-    }
-    __syncthreads();  // every warp is done with the previous stage's f16 tiles
-    // ---- convert the stage once: int8 pages -> f16 tiles, scales -> scs ----
-    {
-      const uint8_t* kt = stage_base(b);
-      const uint8_t* vt = kt + S::kTileBytes;
-      const float* sks = reinterpret_cast<const float*>(kt + 2 * S::kTileBytes);
-      const float* svs = sks + S::kScaleBytes / 4;
-      // K page [D/16][16 tokens][16 B] -> K16 [key][D]
-      for (int i = tid; i < kBlocksPerStage * KC; i += kWarps * 32) {
-        const int pg = i / KC, rem = i % KC;
-        const int c16 = rem / kBS, tk = rem % kBS;
-        const uint4 v = *reinterpret_cast<const uint4*>(kt + (size_t)pg * S::kPage + (size_t)rem * 16);
-        const int key = pg * kBS + tk;
-        uint4 h0, h1;
-        s8x16_to_f16(v, h0, h1);
-        uint8_t* row = k16 + (size_t)key * (2 * D);
-        *reinterpret_cast<uint4*>(row + (((2 * c16) ^ (key & 7)) * 16)) = h0;
-        *reinterpret_cast<uint4*>(row + (((2 * c16 + 1) ^ (key & 7)) * 16)) = h1;
-      }
-      // V page [D][16 tokens] -> V16 [D][64 keys]
-      for (int i = tid; i < kBlocksPerStage * D; i += kWarps * 32) {
-        const int pg = i / D, d = i % D;
-        const uint4 v = *reinterpret_cast<const uint4*>(vt + (size_t)pg * S::kPage + (size_t)d * 16);
-        uint4 h0, h1;
-        s8x16_to_f16(v, h0, h1);
-        uint8_t* row = v16 + (size_t)d * (2 * kKeysPerStage);
-        *reinterpret_cast<uint4*>(row + (((2 * pg) ^ (d & 7)) * 16)) = h0;
-        *reinterpret_cast<uint4*>(row + (((2 * pg + 1) ^ (d & 7)) * 16)) = h1;
-      }
-      if (tid < kKeysPerStage) {
-        scs[2 * tid] = sks[tid * Hkv + kvh];
-        scs[2 * tid + 1] = svs[tid * Hkv + kvh];
-      }
-    }
-    __syncthreads();  // the f16 tiles are ready; the int8 buffer b is free
-    if (tid == 0 && st + kStages < n_stages) issue(st + kStages);
-
-#pragma unroll 1
-    for (int grp = 0; grp < kKeysPerStage / 32; ++grp) {
-      const int key0 = st * kKeysPerStage + grp * 32;  // absolute position of the group's first key
-      if (key0 > warp_lim) break;                       // every row of this warp is past its causal limit
-      // ---- QK: 4 n-tiles of 8 keys, exact on the f16 tensor path ----
-      float acc[4][4];
+        mbar_expect_tx(&stage_full[st], nb * (2 * Ly::kPage + 2 * srow));
 #pragma unroll
-      for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
-      {
-        // A (query rows): matrices (rows 0-7 | 8-15) x (dim chunk 2kk | 2kk+1)
-        const int qr = warp * 16 + ri + 8 * (mi & 1);
-        const uint8_t* qrow = q16 + (size_t)qr * (2 * D);
-        // B (keys): matrices (n-tile 2np2 | 2np2+1) x (dim chunk 2kk | 2kk+1)
-        const uint8_t* krow[2];
-        int kxor[2];
-#pragma unroll
-        for (int np2 = 0; np2 < 2; ++np2) {
-          const int key = grp * 32 + 8 * (2 * np2 + (mi >> 1)) + ri;  // key within the stage
-          krow[np2] = k16 + (size_t)key * (2 * D);
-          kxor[np2] = key & 7;
+        for (int i = 0; i < kPagesPG; ++i) {
+          if (blks[i] < 0) continue;
+          const size_t page = ((size_t)blks[i] * Hkv + kvh) * Ly::kPage;
+          bulk_g2s(base + i * Ly::kPage, p.k_cache + page, Ly::kPage, &stage_full[st]);
+          bulk_g2s(base + (kPagesPG + i) * Ly::kPage, p.v_cache + page, Ly::kPage, &stage_full[st]);
+          const size_t so = (size_t)blks[i] * kBS * Hkv;
+          bulk_g2s(base + 2 * kPagesPG * Ly::kPage + i * Ly::kSRow, p.k_scale + so, srow, &stage_full[st]);
+          bulk_g2s(base + 2 * kPagesPG * Ly::kPage + (kPagesPG + i) * Ly::kSRow, p.v_scale + so, srow,
+                   &stage_full[st]);
         }
+        mbar_arrive(&stage_full[st]);
+      };
+      int issued = 0;  // groups whose copies were issued (warp 0 lane 0)
+      if (warp == 0 && lane == 0)
+        for (; issued < kStages && issued < ng; ++issued) issue(issued);
+      for (int g = 0; g < ng; ++g) {
+        const int st = g % kStages, sl = g & 1;
+        pwait(&stage_full[st], (g / kStages) & 1, abort_flag);
+        if (g >= 2) pwait(&mma_done[sl], ((g - 2) >> 1) & 1, abort_flag);  // PV(g-2) has read the slot
+        const uint8_t* kt = smem + Ly::oStage + (size_t)st * Ly::kStage;
+        const uint8_t* vt = kt + kPagesPG * Ly::kPage;
+        const float* sks = reinterpret_cast<const float*>(kt + 2 * kPagesPG * Ly::kPage);
+        const float* svs = sks + kPagesPG * Ly::kSRow / 4;
+        uint8_t* k16 = smem + Ly::oK + (size_t)sl * Ly::kK16;
+        uint8_t* v16 = smem + Ly::oV + (size_t)sl * Ly::kV16;
+        // K page [D/16][16 tokens][16 B] -> [key][D]: chunk i = (page, dim chunk, token)
+        constexpr int KC = kPagesPG * (D / 16) * kBS;
+        for (int i = ct; i < KC; i += kConvThreads) {
+          const int pg = i / ((D / 16) * kBS), rem = i % ((D / 16) * kBS);
+          const int dc = rem / kBS, tk = rem % kBS;
+          const uint4 v = *reinterpret_cast<const uint4*>(kt + (size_t)pg * Ly::kPage + (size_t)rem * 16);
+          uint4 h0, h1;
+          s8x16_to_f16(v, h0, h1);
+          const int key = pg * kBS + tk;
+          uint8_t* atom = k16 + (size_t)(dc / 4) * (kGroup * 128);
+          *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4))) = h0;
+          *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4) + 1)) = h1;
+        }
+        // V page [D][16 tokens] -> [D][32 keys]: chunk i = (page, dim)
+        for (int i = ct; i < kPagesPG * D; i += kConvThreads) {
+          const int pg = i / D, d = i % D;
+          const uint4 v = *reinterpret_cast<const uint4*>(vt + (size_t)pg * Ly::kPage + (size_t)d * 16);
+          uint4 h0, h1;
+          s8x16_to_f16(v, h0, h1);
+          *reinterpret_cast<uint4*>(v16 + swz_chunk<64>(d, 2 * pg)) = h0;
+          *reinterpret_cast<uint4*>(v16 + swz_chunk<64>(d, 2 * pg + 1)) = h1;
+        }
+        if (ct < kGroup) {
+          float2* sc = reinterpret_cast<float2*>(smem + Ly::oSc) + sl * kGroup;
+          const int pg = ct / kBS, tk = ct % kBS;
+          sc[ct] = make_float2(sks[pg * (Ly::kSRow / 4) + tk * Hkv + kvh], svs[pg * (Ly::kSRow / 4) + tk * Hkv + kvh]);
+        }
+        fence_async_smem();
+        mbar_arrive(&conv_full[sl]);
+        named_bar_sync(5, kConvThreads);  // every converter is done with staging buffer st
+        if (warp == 0 && lane == 0 && issued < ng && !*abort_flag) issue(issued++);
+      }
+      if (warp == 0 && lane == 0) {
+        // copies issued but never waited for (after an abort) land before the CTA exits
+        for (int g = max(0, issued - kStages); g < issued; ++g) mbar_wait(&stage_full[g % kStages], (g / kStages) & 1);
+      }
+    } else {
+      // ================= MMA issue (warp 1, lane 0) =================
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = umma_idesc_f16(kRows, kGroup);
+        constexpr uint32_t idesc_pv = umma_idesc_f16(kRows, D);
+        const uint32_t q16 = smem_u32(smem + Ly::oQ);
+        for (int g = 0; g <= ng; ++g) {
+          if (g < ng) {
+            const int sl = g & 1;
+            pwait(&conv_full[sl], (g >> 1) & 1, abort_flag);
+            if (g >= 2) pwait(&s_free[sl], ((g - 2) >> 1) & 1, abort_flag);
+            tc_fence_after();
+            const uint32_t k16 = smem_u32(smem + Ly::oK + (size_t)sl * Ly::kK16);
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-          uint32_t a[4];
-          ldmatrix_x4(a, qrow + (((2 * kk + (mi >> 1)) ^ (qr & 7)) * 16));
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t a = q16 + (kk / 4) * (kRows * 128) + (kk % 4) * 32;
+              const uint32_t b = k16 + (kk / 4) * (kGroup * 128) + (kk % 4) * 32;
+              umma_f16(tmem + 32 * sl, umma_desc(a, 128), umma_desc(b, 128), idesc_qk, kk > 0);
+            }
+            umma_commit(&s_full[sl]);
+          }
+          if (g >= 1) {
+            const int h = g - 1, sl = h & 1;
+            pwait(&p_full[sl], (h >> 1) & 1, abort_flag);
+            if (h >= 1) pwait(pv_free, (h - 1) & 1, abort_flag);
+            tc_fence_after();
+            const uint32_t p16 = smem_u32(smem + Ly::oP + (size_t)sl * Ly::kP16);
+            const uint32_t v16 = smem_u32(smem + Ly::oV + (size_t)sl * Ly::kV16);
 #pragma unroll
-          for (int np2 = 0; np2 < 2; ++np2) {
-            uint32_t bb[4];
-            ldmatrix_x4(bb, krow[np2] + (((2 * kk + (mi & 1)) ^ kxor[np2]) * 16));
-            mma_f16_16816(acc[2 * np2], a[0], a[1], a[2], a[3], bb[0], bb[1]);
-            mma_f16_16816(acc[2 * np2 + 1], a[0], a[1], a[2], a[3], bb[2], bb[3]);
+            for (int kk = 0; kk < kGroup / 16; ++kk)
+              umma_f16(tmem + Ly::kPVCol, umma_desc(p16 + kk * 32, 64), umma_desc(v16 + kk * 32, 64), idesc_pv,
+                       kk > 0);
+            umma_commit(&mma_done[sl]);
           }
         }
+        // every MMA has completed before TMEM is released (the last commit covers all)
+        if (ng >= 1) mbar_wait(&mma_done[(ng - 1) & 1], ((ng - 1) >> 1) & 1);
       }
-      // ---- scores, mask, online softmax ----
-      float sc[4][4];
-      float mx[2] = {-INFINITY, -INFINITY};
+      __syncwarp();
+    }
+  } else {
+    // ================= softmax and output (warps 4..11) =================
+    regs_inc<216>();
+    const int half = (warp - kCompWarp0) >> 2, quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const int r = r0 + row;
+    const bool valid = r < R;
+    const int j = valid ? r / G : 0, hq = kvh * G + (valid ? r % G : 0);
+    const int lim = valid ? H + j : -1;  // last visible key
+    const float sq = valid ? p.q_scale[(size_t)j * Hq + hq] : 0.f;
+    const float csc = p.sm_scale;
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int pair_bar = 1 + quarter;  // named barrier of warps quarter + 4 and quarter + 8
+    float* xm = xch;                   // [half][row] group maxima
+    float* xa = xch + 2 * kRows;       // [half][row] group absmax of W
+    float* xl = xch + 4 * kRows;       // [half][row] final row sums
+    float o[DH];
 #pragma unroll
-      for (int n = 0; n < 4; ++n)
+    for (int i = 0; i < DH; ++i) o[i] = 0.f;
+    float m = -INFINITY, l = 0.f;
+    float prev_alpha = 1.f, prev_sw = 0.f;
+
+    // o = alpha o + sW (Wq x Vq) of group h, read from TMEM
+    auto update = [&](int h, float alpha, float sw) {
+      pwait(&mma_done[h & 1], (h >> 1) & 1, abort_flag);
+      tc_fence_after();
+      const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int kl = grp * 32 + 8 * n + 2 * t + (e & 1);  // key within the stage
-          const int key = st * kKeysPerStage + kl;
-          const int h2 = e >> 1;
-          float s = -INFINITY;
-          if (key <= row_lim[h2] && key < total_keys)
-            s = __fmul_rn(__fmul_rn(__fmul_rn(acc[n][e], sq[h2]), scs[2 * kl]), csc);
-          sc[n][e] = s;
-          mx[h2] = fmaxf(mx[h2], s);
+      for (int c = 0; c < DH / 32; ++c) {
+        float v[32];
+        tmem_ld32(trow + Ly::kPVCol + half * DH + 32 * c, v);
+        tmem_wait_ld();
+        if (c == DH / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(pv_free);
         }
+        if (rescale) {
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        mx[h2] = fmaxf(mx[h2], __shfl_xor_sync(0xffffffffu, mx[h2], 1));
-        mx[h2] = fmaxf(mx[h2], __shfl_xor_sync(0xffffffffu, mx[h2], 2));
-      }
-      float alpha[2], mnew[2];
+          for (int i = 0; i < 32; ++i) o[32 * c + i] = __fmaf_rn(v[i], sw, __fmul_rn(o[32 * c + i], alpha));
+        } else {
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        mnew[h2] = fmaxf(m[h2], mx[h2]);
-        alpha[h2] = (m[h2] == -INFINITY) ? 0.f : expf(m[h2] - mnew[h2]);
-        m[h2] = mnew[h2];
-        l[h2] *= alpha[h2];
-      }
-      float w[4][4];
-      float A[2] = {0.f, 0.f};
-#pragma unroll
-      for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int h2 = e >> 1;
-          float pe = 0.f, we = 0.f;
-          if (sc[n][e] != -INFINITY) {
-            pe = expf(__fsub_rn(sc[n][e], mnew[h2]));
-            we = __fmul_rn(pe, scs[2 * (grp * 32 + 8 * n + 2 * t + (e & 1)) + 1]);
-          }
-          l[h2] += pe;
-          w[n][e] = we;
-          A[h2] = fmaxf(A[h2], we);
+          for (int i = 0; i < 32; ++i) o[32 * c + i] = __fmaf_rn(v[i], sw, o[32 * c + i]);
         }
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        A[h2] = fmaxf(A[h2], __shfl_xor_sync(0xffffffffu, A[h2], 1));
-        A[h2] = fmaxf(A[h2], __shfl_xor_sync(0xffffffffu, A[h2], 2));
       }
+    };
+
+    for (int g = 0; g < ng; ++g) {
+      const int sl = g & 1;
+      pwait(&s_full[sl], (g >> 1) & 1, abort_flag);
+      tc_fence_after();
+      float s[16];
+      tmem_ld16(trow + 32 * sl + 16 * half, s);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s_free[sl]);
+      pwait(&conv_full[sl], (g >> 1) & 1, abort_flag);  // the group's scales (already complete)
+      const float4* sc4 = reinterpret_cast<const float4*>(smem + Ly::oSc) + sl * (kGroup / 2) + half * 8;
+      float sk[16], sv[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 f = sc4[i];
+        sk[2 * i] = f.x;
+        sv[2 * i] = f.y;
+        sk[2 * i + 1] = f.z;
+        sv[2 * i + 1] = f.w;
+      }
+      // ---- scores (acc x sQ x sK x scale), causal mask, the group's row maximum ----
+      const int key0 = g * kGroup + half * 16;
+      float gmh = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        s[i] = key0 + i <= lim ? __fmul_rn(__fmul_rn(__fmul_rn(s[i], sq), sk[i]), csc) : -INFINITY;
+        gmh = fmaxf(gmh, s[i]);
+      }
+      xm[half * kRows + row] = gmh;
+      named_bar_sync(pair_bar, 64);
+      const float gm = fmaxf(xm[row], xm[kRows + row]);
+      // ---- online softmax: m' = max(m, gm), alpha = exp(m - m'), p~ = exp(s - m') ----
+      const float mn = fmaxf(m, gm);
+      float alpha = 1.f;
+      float w[16];
+      float ah = 0.f, lsum = 0.f;
+      if (mn != -INFINITY) {
+        alpha = m == -INFINITY ? 0.f : expf(__fsub_rn(m, mn));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float pe = expf(__fsub_rn(s[i], mn));  // 0 for masked keys
+          lsum += pe;
+          w[i] = pe != 0.f ? __fmul_rn(pe, sv[i]) : 0.f;
+          ah = fmaxf(ah, w[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = 0.f;
+      }
+      m = mn;
+      l = __fmaf_rn(l, alpha, lsum);
+      xa[half * kRows + row] = ah;
+      named_bar_sync(pair_bar, 64);
+      const float A = fmaxf(xa[row], xa[kRows + row]);
       // sW = A / 127 and the codes round(W / sW), both IEEE fp32 quotients (W / sW
       // by Markstein's method); W / sW <= A / RN(A / 127) < 127.5, no clamp needed
-      float sW[2], ysw[2];
-      bool tiny[2];
+      const float sw = div127(A);
+      const float ysw = __frcp_rn(sw);
+      const bool tiny = sw < kTinyDivisor;
+      uint32_t pk[8];
 #pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        sW[h2] = div127(A[h2]);
-        ysw[h2] = __frcp_rn(sW[h2]);
-        tiny[h2] = sW[h2] < kTinyDivisor;
+      for (int i = 0; i < 8; ++i) {
+        const float c0 = A > 0.f ? rintf(div_shared(w[2 * i], sw, ysw, tiny)) : 0.f;
+        const float c1 = A > 0.f ? rintf(div_shared(w[2 * i + 1], sw, ysw, tiny)) : 0.f;
+        pk[i] = f16x2_of(c0, c1);
       }
-      float q[4][4];
+      // ---- Wq (f16) -> the PV A tile: row `row`, keys 16 half .. 16 half + 15 ----
+      if (g >= 2) pwait(&mma_done[sl], ((g - 2) >> 1) & 1, abort_flag);  // PV(g-2) has read the slot
+      uint8_t* p16 = smem + Ly::oP + (size_t)sl * Ly::kP16;
+      *reinterpret_cast<uint4*>(p16 + swz_chunk<64>(row, 2 * half)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<uint4*>(p16 + swz_chunk<64>(row, 2 * half + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      fence_async_smem();
+      mbar_arrive(&p_full[sl]);
+      // ---- the previous group's product joins the output ----
+      if (g >= 1) update(g - 1, prev_alpha, prev_sw);
+      prev_alpha = alpha;
+      prev_sw = sw;
+    }
+    if (ng >= 1) update(ng - 1, prev_alpha, prev_sw);
+
+    // ---- finish: O = o / l ----
+    xl[half * kRows + row] = l;
+    named_bar_sync(pair_bar, 64);
+    const float lt = xl[row] + xl[kRows + row];
+    if (valid) {
+      const float inv = 1.0f / lt;
+      float4* orow = reinterpret_cast<float4*>(p.out + ((size_t)j * Hq + hq) * D + half * DH);
 #pragma unroll
-      for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int h2 = e >> 1;
-          q[n][e] = A[h2] > 0.f ? rintf(div_shared(w[n][e], sW[h2], ysw[h2], tiny[h2])) : 0.f;
-        }
-      // A operand of PV (exact integers in f16): k16 step kk covers the group's
-      // keys 16kk .. 16kk+15 = score n-tiles 2kk (a0: row g, a1: row g+8) and
-      // 2kk+1 (a2, a3).
-      uint32_t pa[2][4];
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        pa[kk][0] = f16x2_of(q[2 * kk][0], q[2 * kk][1]);
-        pa[kk][1] = f16x2_of(q[2 * kk][2], q[2 * kk][3]);
-        pa[kk][2] = f16x2_of(q[2 * kk + 1][0], q[2 * kk + 1][1]);
-        pa[kk][3] = f16x2_of(q[2 * kk + 1][2], q[2 * kk + 1][3]);
-      }
-      if (alpha[0] != 1.f || alpha[1] != 1.f) {
-#pragma unroll
-        for (int n = 0; n < ND; ++n) {
-          o[n][0] *= alpha[0];
-          o[n][1] *= alpha[0];
-          o[n][2] *= alpha[1];
-          o[n][3] *= alpha[1];
-        }
-      }
-      // ---- PV: B = V tile [dim][key]: matrices (dim n-tile dn | dn+1) x (key chunk c | c+1) ----
-#pragma unroll
-      for (int dn = 0; dn < ND; dn += 2) {
-        const int d = 8 * (dn + (mi >> 1)) + ri;
-        const uint8_t* vrow = v16 + (size_t)d * (2 * kKeysPerStage);
-        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-          const int chunk = 4 * grp + 2 * kk + (mi & 1);
-          uint32_t bb[4];
-          ldmatrix_x4(bb, vrow + ((chunk ^ (d & 7)) * 16));
-          mma_f16_16816(c0, pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], bb[0], bb[1]);
-          mma_f16_16816(c1, pa[kk][0], pa[kk][1], pa[kk][2], pa[kk][3], bb[2], bb[3]);
-        }
-        o[dn][0] = fmaf(c0[0], sW[0], o[dn][0]);
-        o[dn][1] = fmaf(c0[1], sW[0], o[dn][1]);
-        o[dn][2] = fmaf(c0[2], sW[1], o[dn][2]);
-        o[dn][3] = fmaf(c0[3], sW[1], o[dn][3]);
-        o[dn + 1][0] = fmaf(c1[0], sW[0], o[dn + 1][0]);
-        o[dn + 1][1] = fmaf(c1[1], sW[0], o[dn + 1][1]);
-        o[dn + 1][2] = fmaf(c1[2], sW[1], o[dn + 1][2]);
-        o[dn + 1][3] = fmaf(c1[3], sW[1], o[dn + 1][3]);
-      }
+      for (int i = 0; i < DH / 4; ++i)
+        orow[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
     }
   }
 
-  // ---- finish: O = o / l ----
-#pragma unroll
-  for (int h2 = 0; h2 < 2; ++h2) {
-    l[h2] += __shfl_xor_sync(0xffffffffu, l[h2], 1);
-    l[h2] += __shfl_xor_sync(0xffffffffu, l[h2], 2);
-  }
-#pragma unroll
-  for (int h2 = 0; h2 < 2; ++h2) {
-    const int r = r0 + warp * 16 + g + 8 * h2;
-    if (r >= R) continue;
-    const int j = r / G, hq = kvh * G + r % G;
-    float* orow = p.out + ((size_t)j * Hq + hq) * D;
-    const float inv = 1.0f / l[h2];
-#pragma unroll
-    for (int n = 0; n < ND; ++n) {
-      float2 v2 = make_float2(o[n][2 * h2] * inv, o[n][2 * h2 + 1] * inv);
-      *reinterpret_cast<float2*>(orow + 8 * n + 2 * t) = v2;
-    }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Ly::kTmemCols);
   }
 }
 
@@ -404,20 +465,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1) int8_prefix_kernel(PrefixParam
 
 cudaError_t launch_int8_prefix(const PrefixParams& p, cudaStream_t stream) {
   const int R = p.C * p.G;
-  dim3 grid((R + kRowsPerCTA - 1) / kRowsPerCTA, p.Hkv);
+  dim3 grid((R + kRows - 1) / kRows, p.Hkv);
   cudaError_t e;
   if (p.D == 256) {
-    e = cudaFuncSetAttribute(int8_prefix_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PrefixSmem<256>::kTotal);
+    e = cudaFuncSetAttribute(int8_prefix_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<256>::kTotal);
     if (e != cudaSuccess) return e;
-    int8_prefix_kernel<256><<<grid, kWarps * 32, PrefixSmem<256>::kTotal, stream>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(int8_prefix_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PrefixSmem<128>::kTotal);
-    if (e != cudaSuccess) return e;
-    int8_prefix_kernel<128><<<grid, kWarps * 32, PrefixSmem<128>::kTotal, stream>>>(p);
+    return launch_pdl(int8_prefix_kernel<256>, grid, dim3(kThreads), Lay<256>::kTotal, stream, p);
   }
-  return cudaGetLastError();
+  e = cudaFuncSetAttribute(int8_prefix_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<128>::kTotal);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(int8_prefix_kernel<128>, grid, dim3(kThreads), Lay<128>::kTotal, stream, p);
 }
 
 }  // namespace i8kv
