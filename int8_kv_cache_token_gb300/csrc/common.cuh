@@ -336,15 +336,35 @@ __device__ __forceinline__ void regs_dec() {
 // x / s correctly rounded (the IEEE quotient) for one divisor s shared by many
 // x, by Markstein's method: with y = RN(1/s), q = RN(x * y) and the exact
 // residual r = x - s * q (one FMA), RN(q + r * y) is the correctly rounded
-// quotient while nothing overflows or underflows.  `tiny` (s below 2^-100)
-// selects the plain division instead.
-__device__ __forceinline__ float div_shared(float x, float s, float y, bool tiny) {
-  if (tiny) return __fdiv_rn(x, s);
+// quotient while nothing overflows or underflows (s >= 2^-100 here).
+__device__ __forceinline__ float div_markstein(float x, float s, float y) {
   const float q = __fmul_rn(x, y);
   const float r = __fmaf_rn(-s, q, x);
   return __fmaf_rn(r, y, q);
 }
 constexpr float kTinyDivisor = 7.8886091e-31f;  // 2^-100
+
+// x[i] / s, correctly rounded, for the N values of one row sharing the divisor
+// s > 0: Markstein's step when s >= 2^-100, the plain division below.  The test
+// on s is made once for the row, so the N quotients are independent chains of
+// three FMA-pipe operations (a test inside each quotient would split them into
+// N serial blocks).  y = RN(1/s) is computed by the caller when it serves
+// several rows' calls.
+template <int N>
+__device__ __forceinline__ void div_row(float (&x)[N], float s, float y) {
+  if (s < kTinyDivisor) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = __fdiv_rn(x[i], s);
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = div_markstein(x[i], s, y);
+  }
+}
+
+// round-half-even(x) for |x| < 2^21, as the low bits of the fp32 sum
+// x + 1.5 * 2^23 (whose unit in the last place is 1): the low byte is the
+// integer's two's-complement byte.
+__device__ __forceinline__ uint32_t rne_bits(float x) { return __float_as_uint(__fadd_rn(x, 12582912.0f)); }
 
 // a / 127 correctly rounded, by the same method with the constant RN(1/127).
 // Checked exhaustively against IEEE division for every float in [1, 4), in the
@@ -359,12 +379,6 @@ __device__ __forceinline__ float div127(float a) {
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
-
-// Four int8 codes packed little-endian into one register.
-__device__ __forceinline__ uint32_t pack_s8x4(int a, int b, int c, int d) {
-  return (uint32_t)(a & 0xff) | ((uint32_t)(b & 0xff) << 8) | ((uint32_t)(c & 0xff) << 16) |
-         ((uint32_t)(d & 0xff) << 24);
-}
 
 // Host: launch `kernel` with programmatic stream serialization allowed, so its
 // launch overlaps the tail of the previous kernel on `stream` (the kernel must

@@ -342,11 +342,13 @@ __device__ __forceinline__ void qk_warp_bf16(const uint8_t* kpages, int warp, in
 // quotient (Markstein's method, one reciprocal per vector), all codes 0 and
 // scale 0 for a zero vector -- the same arithmetic as kv_quant_write_kernel,
 // so the codes and scales are bit-identical to the two-kernel path.
-__device__ __forceinline__ uint32_t quant4(const float (&x)[4], float scale, float y, bool tiny, bool nz) {
-  int c[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) c[i] = nz ? __float2int_rn(div_shared(x[i], scale, y, tiny)) : 0;
-  return pack_s8x4(c[0], c[1], c[2], c[3]);
+__device__ __forceinline__ uint32_t quant4(const float (&x)[4], float scale, float y, bool nz) {
+  if (!nz) return 0u;
+  float q[4] = {x[0], x[1], x[2], x[3]};
+  div_row(q, scale, y);
+  const uint32_t lo = __byte_perm(rne_bits(q[0]), rne_bits(q[1]), 0x0040);
+  const uint32_t hi = __byte_perm(rne_bits(q[2]), rne_bits(q[3]), 0x0040);
+  return __byte_perm(lo, hi, 0x5410);
 }
 
 __device__ __forceinline__ void unpack_bf16x4(uint2 r, float (&x)[4]) {
@@ -388,9 +390,9 @@ __device__ __forceinline__ float quant_row_warp(const RowRaw<D>& raw, uint32_t (
   for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   const float scale = __fdiv_rn(amax, 127.0f);
   const float y = __frcp_rn(scale);
-  const bool tiny = scale < kTinyDivisor, nz = amax > 0.f;
+  const bool nz = amax > 0.f;
 #pragma unroll
-  for (int j = 0; j < D / 128; ++j) packed[j] = quant4(x[j], scale, y, tiny, nz);
+  for (int j = 0; j < D / 128; ++j) packed[j] = quant4(x[j], scale, y, nz);
   return nz ? scale : 0.f;
 }
 
@@ -926,25 +928,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
 #pragma unroll
           for (int off = 4; off <= 16; off <<= 1) A[r] = fmaxf(A[r], __shfl_xor_sync(0xffffffffu, A[r], off));
         // sW = A / 127 and the codes round(W / sW), both IEEE fp32 quotients
-        // (W / sW by Markstein's method, one reciprocal per row)
-        float ysw[2];
-        bool tiny[2];
+        // (W / sW by Markstein's method, one reciprocal per row); codes ->
+        // [row][token] bytes, read back below as PV B fragments.
+        // W / sW <= A / RN(A / 127) < 127.5, so no code needs clamping.
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           swv[r] = div127(A[r]);
-          ysw[r] = __frcp_rn(swv[r]);
-          tiny[r] = swv[r] < kTinyDivisor;
-        }
-        // codes -> [row][token] bytes, read back below as PV B fragments.
-        // W / sW <= A / RN(A / 127) < 127.5, so no code needs clamping.
+          // this lane's values of row 2t + r: (block m, token g + 8 h) at e = r + 2 h
+          float x[4] = {w[0][r], w[0][r + 2], w[1][r], w[1][r + 2]};
+          if (A[r] > 0.f) {
+            div_row(x, swv[r], __frcp_rn(swv[r]));
+          } else {
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int r = e & 1;
-            const int q = A[r] > 0.f ? __float2int_rn(div_shared(w[m][e], swv[r], ysw[r], tiny[r])) : 0;
-            stg[(2 * t + r) * kGroup + 16 * m + g + 8 * (e >> 1)] = (uint8_t)(int8_t)q;
+            for (int i = 0; i < 4; ++i) x[i] = 0.f;
           }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            stg[(2 * t + r) * kGroup + 16 * (i >> 1) + g + 8 * (i & 1)] = (uint8_t)rne_bits(x[i]);
+        }
       }
       __syncwarp();
 

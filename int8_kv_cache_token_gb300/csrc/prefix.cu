@@ -13,25 +13,31 @@
 // head) pairs of that head's GQA group, token-major, so the query heads sharing
 // K/V read the same tiles -- and walks the keys in 32-key probability groups:
 //   S  = Qq x Kq^T        tcgen05, M = 128, N = 32, K = D, into TMEM
-//   scores, causal mask, online softmax, W = p~ sV, sW = max W / 127,
-//   Wq = round(W / sW)    CUDA cores, one thread per (row, half of the keys)
+//   scores, causal mask, p~ = exp(s - m_g) against the group's own row
+//   maximum m_g, W = p~ sV, sW = max W / 127, Wq = round(W / sW)
+//                         CUDA cores, one thread per row
 //   PV = Wq x Vq          tcgen05, M = 128, N = D, K = 32, into TMEM
-//   o  = alpha o + sW PV  CUDA cores, o in registers (half of D per thread)
+//   o  = alpha o + exp(m_g - m') sW PV,  l = alpha l + exp(m_g - m') l_g
+//                         CUDA cores, o in registers (half of D per thread)
+// with m' = max(m, m_g) and alpha = exp(m - m').  The codes round(W / sW) do
+// not change when W is scaled, so quantizing each group against m_g and
+// bringing it to the running maximum in the output update is the pages' online
+// softmax, reordered; it lets the softmax of a group start before the previous
+// group's maximum is known.  Scores are kept in log2 units (the scale folds in
+// log2 e) so every exponential is one ex2.
+//
 // The int8 codes are exact in f16, every product (<= 127^2) is exact and every
 // partial sum stays below 2^22, so f16 MMAs with fp32 accumulation give the
 // INT8 contractions' exact integer results.
 //
 // Warps.  Warp 0 lane 0 issues the bulk copies of each group's int8 pages and
-// scale rows (three groups in flight); warps 0, 2 and 3 convert each group
-// once into f16 operand tiles (K-major, 16-byte chunks XOR-swizzled: K as
-// [key][dim] in 128-byte rows, V as [dim][key] in 64-byte rows).  Warp 1 owns
-// the TMEM allocation; its lane 0 issues every MMA.  Warps 4-7 and 8-11 are two
-// halves: thread (half, row) takes keys 16 half .. 16 half + 15 of each group
-// for its row's softmax (the halves exchange the row's group maximum and
-// absmax through shared memory) and output dims [half D/2, (half + 1) D/2).
-// S is double-buffered in TMEM, so the QK of the next group runs during a
-// softmax; the PV of group g runs during the softmax of g + 1, after which the
-// output takes group g's product.
+// scale rows (three groups in flight); warps 0, 2 and 3 convert each group once
+// into f16 operand tiles (K-major, 16-byte chunks XOR-swizzled: K as [key][dim]
+// in 128-byte rows, V as [dim][key] in 64-byte rows), K one group ahead of V.
+// Warp 1 owns the TMEM allocation; its lane 0 issues every MMA, the QK two
+// groups ahead of the PV.  Warpgroups 1 and 2 (warps 4-7, 8-11) take the
+// softmax of the even and the odd groups, thread = row, so the two run side by
+// side; both apply every group's product to their half of the output dims.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -50,7 +56,8 @@ constexpr int kThreads = 384;
 constexpr int kMmaWarp = 1;
 constexpr int kCompWarp0 = 4;    // warps 4..11
 constexpr int kConvThreads = 96; // warps 0, 2, 3
-constexpr int kCompThreads = 256;
+constexpr int kWGThreads = 128;
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct Lay {
@@ -66,11 +73,11 @@ struct Lay {
   static constexpr int oV = oK + 2 * kK16;            // two slots
   static constexpr int oP = oV + 2 * kV16;            // two slots
   static constexpr int oStage = oP + 2 * kP16;        // kStages
-  static constexpr int oSc = oStage + kStages * kStage;  // two slots of [32 keys][sK, sV]
-  static constexpr int oX = oSc + 2 * kGroup * 8;     // exchange: [3 values][2 halves][128 rows] floats
-  static constexpr int oBar = oX + 3 * 2 * kRows * 4;
-  // barriers: stage_full[3], conv_full[2], s_full[2], s_free[2], p_full[2], mma_done[2], pv_free
-  static constexpr int kBars = kStages + 2 + 2 + 2 + 2 + 2 + 1;
+  static constexpr int oSc = oStage + kStages * kStage;  // four slots of sK[32], sV[32]
+  static constexpr int oSt = oSc + 4 * 2 * kGroup * 4;   // four slots of m_g[128], sW[128], l_g[128]
+  static constexpr int oBar = oSt + 4 * 3 * kRows * 4;
+  // stage_full[3], k_full[4], v_full[2], qk_done[2], s_free[2], p_full[2], pv_done[2], pv_free, st_full[4]
+  static constexpr int kBars = kStages + 4 + 2 + 2 + 2 + 2 + 2 + 1 + 4;
   static constexpr int oCtl = oBar + kBars * 8;       // TMEM base, abort flag
   static constexpr int kTotal = oCtl + 16;
   // TMEM: S in columns [0, 64) (two slots of 32), PV in [kPVCol, kPVCol + D)
@@ -95,9 +102,38 @@ __device__ __forceinline__ void s8x16_to_f16(const uint4& v, uint4& h0, uint4& h
   s8x4_to_f16(v.w, h1.z, h1.w);
 }
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Maximum and sum of 32 values as balanced trees (depth 5 instead of a
+// 31-step chain); the sum's order is fixed, so every thread rounds alike.
+__device__ __forceinline__ float tree_max(const float (&a)[32]) {
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = fmaxf(a[i], a[i + 16]);
+#pragma unroll
+  for (int n = 8; n >= 1; n >>= 1)
+#pragma unroll
+    for (int i = 0; i < n; ++i) t[i] = fmaxf(t[i], t[i + n]);
+  return t[0];
+}
+__device__ __forceinline__ float tree_sum(const float (&a)[32]) {
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = __fadd_rn(a[i], a[i + 16]);
+#pragma unroll
+  for (int n = 8; n >= 1; n >>= 1)
+#pragma unroll
+    for (int i = 0; i < n; ++i) t[i] = __fadd_rn(t[i], t[i + n]);
+  return t[0];
+}
+
 // Bounded wait that gives up at once when the CTA has aborted (error 1 after
-// the time limit); every thread still runs the same loop and the same named
-// barriers, so no thread waits on a barrier another one skipped.
+// the time limit); every thread still runs the same loop and barriers, so no
+// thread waits on a barrier another one skipped.
 __device__ __forceinline__ void pwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return;
   if (*abort_flag) return;
@@ -115,19 +151,19 @@ __device__ __forceinline__ void pwait(uint64_t* bar, uint32_t parity, volatile i
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p) {
   using Ly = Lay<D>;
-  constexpr int DH = D / 2;  // output dims per half
+  constexpr int DH = D / 2;  // output dims per warpgroup
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::oBar);
-  uint64_t* stage_full = bars;
-  uint64_t* conv_full = stage_full + kStages;
-  uint64_t* s_full = conv_full + 2;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* mma_done = p_full + 2;  // PV of group g done: its slots and the PV accumulator are readable/free
-  uint64_t* pv_free = mma_done + 2;
+  uint64_t* stage_full = reinterpret_cast<uint64_t*>(smem + Ly::oBar);
+  uint64_t* k_full = stage_full + kStages;  // [g & 3]: K(g) in its f16 slot, the group's scales
+  uint64_t* v_full = k_full + 4;            // [g & 1]: V(g) in its f16 slot
+  uint64_t* qk_done = v_full + 2;           // [g & 1]: S(g) in TMEM; K slot free
+  uint64_t* s_free = qk_done + 2;           // [g & 1]: S(g) read
+  uint64_t* p_full = s_free + 2;            // [g & 1]: Wq(g) in its slot
+  uint64_t* pv_done = p_full + 2;           // [g & 1]: PV(g) in TMEM; V and Wq slots free
+  uint64_t* pv_free = pv_done + 2;          // PV accumulator read by both warpgroups
+  uint64_t* st_full = pv_free + 1;          // [g & 3]: the group's row statistics
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::oCtl);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::oCtl + 4);
-  float* xch = reinterpret_cast<float*>(smem + Ly::oX);  // [value][half][row]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kvh = blockIdx.y;
@@ -144,14 +180,18 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&stage_full[s], 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&conv_full[s], kConvThreads);
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], kCompThreads);
-      mbar_init(&p_full[s], kCompThreads);
-      mbar_init(&mma_done[s], 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&k_full[s], kConvThreads);
+      mbar_init(&st_full[s], kWGThreads);
     }
-    mbar_init(pv_free, kCompThreads);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&v_full[s], kConvThreads);
+      mbar_init(&qk_done[s], 1);
+      mbar_init(&s_free[s], kWGThreads);
+      mbar_init(&p_full[s], kWGThreads);
+      mbar_init(&pv_done[s], 1);
+    }
+    mbar_init(pv_free, 2 * kWGThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -228,51 +268,62 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
       int issued = 0;  // groups whose copies were issued (warp 0 lane 0)
       if (warp == 0 && lane == 0)
         for (; issued < kStages && issued < ng; ++issued) issue(issued);
-      for (int g = 0; g < ng; ++g) {
-        const int st = g % kStages, sl = g & 1;
-        pwait(&stage_full[st], (g / kStages) & 1, abort_flag);
-        if (g >= 2) pwait(&mma_done[sl], ((g - 2) >> 1) & 1, abort_flag);  // PV(g-2) has read the slot
-        const uint8_t* kt = smem + Ly::oStage + (size_t)st * Ly::kStage;
-        const uint8_t* vt = kt + kPagesPG * Ly::kPage;
-        const float* sks = reinterpret_cast<const float*>(kt + 2 * kPagesPG * Ly::kPage);
-        const float* svs = sks + kPagesPG * Ly::kSRow / 4;
-        uint8_t* k16 = smem + Ly::oK + (size_t)sl * Ly::kK16;
-        uint8_t* v16 = smem + Ly::oV + (size_t)sl * Ly::kV16;
-        // K page [D/16][16 tokens][16 B] -> [key][D]: chunk i = (page, dim chunk, token)
-        constexpr int KC = kPagesPG * (D / 16) * kBS;
-        for (int i = ct; i < KC; i += kConvThreads) {
-          const int pg = i / ((D / 16) * kBS), rem = i % ((D / 16) * kBS);
-          const int dc = rem / kBS, tk = rem % kBS;
-          const uint4 v = *reinterpret_cast<const uint4*>(kt + (size_t)pg * Ly::kPage + (size_t)rem * 16);
-          uint4 h0, h1;
-          s8x16_to_f16(v, h0, h1);
-          const int key = pg * kBS + tk;
-          uint8_t* atom = k16 + (size_t)(dc / 4) * (kGroup * 128);
-          *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4))) = h0;
-          *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4) + 1)) = h1;
+      // step t converts K(t) and V(t - 1)
+      for (int t = 0; t <= ng; ++t) {
+        if (t < ng) {
+          const int st = t % kStages;
+          pwait(&stage_full[st], (t / kStages) & 1, abort_flag);
+          if (t >= 2) pwait(&qk_done[t & 1], ((t - 2) >> 1) & 1, abort_flag);  // QK(t-2) has read the K slot
+          const uint8_t* kt = smem + Ly::oStage + (size_t)st * Ly::kStage;
+          uint8_t* k16 = smem + Ly::oK + (size_t)(t & 1) * Ly::kK16;
+          // K page [D/16][16 tokens][16 B] -> [key][D]: chunk i = (page, dim chunk, token)
+          constexpr int KC = kPagesPG * (D / 16) * kBS;
+          for (int i = ct; i < KC; i += kConvThreads) {
+            const int pg = i / ((D / 16) * kBS), rem = i % ((D / 16) * kBS);
+            const int dc = rem / kBS, tk = rem % kBS;
+            const uint4 v = *reinterpret_cast<const uint4*>(kt + (size_t)pg * Ly::kPage + (size_t)rem * 16);
+            uint4 h0, h1;
+            s8x16_to_f16(v, h0, h1);
+            const int key = pg * kBS + tk;
+            uint8_t* atom = k16 + (size_t)(dc / 4) * (kGroup * 128);
+            *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4))) = h0;
+            *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4) + 1)) = h1;
+          }
+          if (ct < kGroup) {
+            const float* sks = reinterpret_cast<const float*>(kt + 2 * kPagesPG * Ly::kPage);
+            const float* svs = sks + kPagesPG * Ly::kSRow / 4;
+            float* sc = reinterpret_cast<float*>(smem + Ly::oSc) + (t & 3) * 2 * kGroup;
+            const int si = (ct / kBS) * (Ly::kSRow / 4) + (ct % kBS) * Hkv + kvh;
+            sc[ct] = sks[si];
+            sc[kGroup + ct] = svs[si];
+          }
+          fence_async_smem();
+          mbar_arrive(&k_full[t & 3]);
         }
-        // V page [D][16 tokens] -> [D][32 keys]: chunk i = (page, dim)
-        for (int i = ct; i < kPagesPG * D; i += kConvThreads) {
-          const int pg = i / D, d = i % D;
-          const uint4 v = *reinterpret_cast<const uint4*>(vt + (size_t)pg * Ly::kPage + (size_t)d * 16);
-          uint4 h0, h1;
-          s8x16_to_f16(v, h0, h1);
-          *reinterpret_cast<uint4*>(v16 + swz_chunk<64>(d, 2 * pg)) = h0;
-          *reinterpret_cast<uint4*>(v16 + swz_chunk<64>(d, 2 * pg + 1)) = h1;
+        if (t >= 1) {
+          const int h = t - 1, st = h % kStages;
+          if (h >= 2) pwait(&pv_done[h & 1], ((h - 2) >> 1) & 1, abort_flag);  // PV(h-2) has read the V slot
+          const uint8_t* vt = smem + Ly::oStage + (size_t)st * Ly::kStage + kPagesPG * Ly::kPage;
+          uint8_t* v16 = smem + Ly::oV + (size_t)(h & 1) * Ly::kV16;
+          // V page [D][16 tokens] -> [D][32 keys]: chunk i = (page, dim)
+          for (int i = ct; i < kPagesPG * D; i += kConvThreads) {
+            const int pg = i / D, d = i % D;
+            const uint4 v = *reinterpret_cast<const uint4*>(vt + (size_t)pg * Ly::kPage + (size_t)d * 16);
+            uint4 h0, h1;
+            s8x16_to_f16(v, h0, h1);
+            *reinterpret_cast<uint4*>(v16 + swz_chunk<64>(d, 2 * pg)) = h0;
+            *reinterpret_cast<uint4*>(v16 + swz_chunk<64>(d, 2 * pg + 1)) = h1;
+          }
+          fence_async_smem();
+          mbar_arrive(&v_full[h & 1]);
+          named_bar_sync(5, kConvThreads);  // every converter is done with staging buffer st
+          if (warp == 0 && lane == 0 && issued < ng && !*abort_flag) issue(issued++);
         }
-        if (ct < kGroup) {
-          float2* sc = reinterpret_cast<float2*>(smem + Ly::oSc) + sl * kGroup;
-          const int pg = ct / kBS, tk = ct % kBS;
-          sc[ct] = make_float2(sks[pg * (Ly::kSRow / 4) + tk * Hkv + kvh], svs[pg * (Ly::kSRow / 4) + tk * Hkv + kvh]);
-        }
-        fence_async_smem();
-        mbar_arrive(&conv_full[sl]);
-        named_bar_sync(5, kConvThreads);  // every converter is done with staging buffer st
-        if (warp == 0 && lane == 0 && issued < ng && !*abort_flag) issue(issued++);
       }
       if (warp == 0 && lane == 0) {
         // copies issued but never waited for (after an abort) land before the CTA exits
-        for (int g = max(0, issued - kStages); g < issued; ++g) mbar_wait(&stage_full[g % kStages], (g / kStages) & 1);
+        for (int g = max(0, issued - kStages); g < issued; ++g)
+          mbar_wait(&stage_full[g % kStages], (g / kStages) & 1);
       }
     } else {
       // ================= MMA issue (warp 1, lane 0) =================
@@ -280,71 +331,169 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
         constexpr uint32_t idesc_qk = umma_idesc_f16(kRows, kGroup);
         constexpr uint32_t idesc_pv = umma_idesc_f16(kRows, D);
         const uint32_t q16 = smem_u32(smem + Ly::oQ);
-        for (int g = 0; g <= ng; ++g) {
-          if (g < ng) {
-            const int sl = g & 1;
-            pwait(&conv_full[sl], (g >> 1) & 1, abort_flag);
-            if (g >= 2) pwait(&s_free[sl], ((g - 2) >> 1) & 1, abort_flag);
-            tc_fence_after();
-            const uint32_t k16 = smem_u32(smem + Ly::oK + (size_t)sl * Ly::kK16);
+        auto qk = [&](int g) {
+          const int sl = g & 1;
+          pwait(&k_full[g & 3], (g >> 2) & 1, abort_flag);
+          if (g >= 2) pwait(&s_free[sl], ((g - 2) >> 1) & 1, abort_flag);
+          tc_fence_after();
+          const uint32_t k16 = smem_u32(smem + Ly::oK + (size_t)sl * Ly::kK16);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t a = q16 + (kk / 4) * (kRows * 128) + (kk % 4) * 32;
-              const uint32_t b = k16 + (kk / 4) * (kGroup * 128) + (kk % 4) * 32;
-              umma_f16(tmem + 32 * sl, umma_desc(a, 128), umma_desc(b, 128), idesc_qk, kk > 0);
-            }
-            umma_commit(&s_full[sl]);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t a = q16 + (kk / 4) * (kRows * 128) + (kk % 4) * 32;
+            const uint32_t b = k16 + (kk / 4) * (kGroup * 128) + (kk % 4) * 32;
+            umma_f16(tmem + 32 * sl, umma_desc(a, 128), umma_desc(b, 128), idesc_qk, kk > 0);
           }
-          if (g >= 1) {
-            const int h = g - 1, sl = h & 1;
-            pwait(&p_full[sl], (h >> 1) & 1, abort_flag);
-            if (h >= 1) pwait(pv_free, (h - 1) & 1, abort_flag);
-            tc_fence_after();
-            const uint32_t p16 = smem_u32(smem + Ly::oP + (size_t)sl * Ly::kP16);
-            const uint32_t v16 = smem_u32(smem + Ly::oV + (size_t)sl * Ly::kV16);
+          umma_commit(&qk_done[sl]);
+        };
+        for (int g = 0; g < 2 && g < ng; ++g) qk(g);
+        for (int h = 0; h < ng; ++h) {
+          if (h + 2 < ng) qk(h + 2);
+          const int sl = h & 1;
+          pwait(&v_full[sl], (h >> 1) & 1, abort_flag);
+          pwait(&p_full[sl], (h >> 1) & 1, abort_flag);
+          if (h >= 1) pwait(pv_free, (h - 1) & 1, abort_flag);
+          tc_fence_after();
+          const uint32_t p16 = smem_u32(smem + Ly::oP + (size_t)sl * Ly::kP16);
+          const uint32_t v16 = smem_u32(smem + Ly::oV + (size_t)sl * Ly::kV16);
 #pragma unroll
-            for (int kk = 0; kk < kGroup / 16; ++kk)
-              umma_f16(tmem + Ly::kPVCol, umma_desc(p16 + kk * 32, 64), umma_desc(v16 + kk * 32, 64), idesc_pv,
-                       kk > 0);
-            umma_commit(&mma_done[sl]);
-          }
+          for (int kk = 0; kk < kGroup / 16; ++kk)
+            umma_f16(tmem + Ly::kPVCol, umma_desc(p16 + kk * 32, 64), umma_desc(v16 + kk * 32, 64), idesc_pv,
+                     kk > 0);
+          umma_commit(&pv_done[sl]);
         }
         // every MMA has completed before TMEM is released (the last commit covers all)
-        if (ng >= 1) mbar_wait(&mma_done[(ng - 1) & 1], ((ng - 1) >> 1) & 1);
+        if (ng >= 1) mbar_wait(&pv_done[(ng - 1) & 1], ((ng - 1) >> 1) & 1);
       }
       __syncwarp();
     }
   } else {
-    // ================= softmax and output (warps 4..11) =================
+    // ================= softmax and output (warpgroups 1, 2) =================
     regs_inc<216>();
-    const int half = (warp - kCompWarp0) >> 2, quarter = warp & 3;
+    const int wg = (warp - kCompWarp0) >> 2, quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int r = r0 + row;
     const bool valid = r < R;
     const int j = valid ? r / G : 0, hq = kvh * G + (valid ? r % G : 0);
     const int lim = valid ? H + j : -1;  // last visible key
-    const float sq = valid ? p.q_scale[(size_t)j * Hq + hq] : 0.f;
-    const float csc = p.sm_scale;
+    // score in log2 units: acc x sQ x scale x log2(e) x sK
+    const float c2 = valid ? __fmul_rn(__fmul_rn(p.q_scale[(size_t)j * Hq + hq], p.sm_scale), kLog2e) : 0.f;
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const int pair_bar = 1 + quarter;  // named barrier of warps quarter + 4 and quarter + 8
-    float* xm = xch;                   // [half][row] group maxima
-    float* xa = xch + 2 * kRows;       // [half][row] group absmax of W
-    float* xl = xch + 4 * kRows;       // [half][row] final row sums
+    float* stats = reinterpret_cast<float*>(smem + Ly::oSt);  // [slot][m_g | sW | l_g][row]
     float o[DH];
 #pragma unroll
     for (int i = 0; i < DH; ++i) o[i] = 0.f;
     float m = -INFINITY, l = 0.f;
-    float prev_alpha = 1.f, prev_sw = 0.f;
 
-    // o = alpha o + sW (Wq x Vq) of group h, read from TMEM
-    auto update = [&](int h, float alpha, float sw) {
-      pwait(&mma_done[h & 1], (h >> 1) & 1, abort_flag);
+    // softmax of group g (this warpgroup's parity): codes into the Wq slot,
+    // (m_g, sW, l_g) into the statistics slot
+    auto softmax = [&](int g) {
+      const int sl = g & 1;
+      pwait(&qk_done[sl], (g >> 1) & 1, abort_flag);
+      tc_fence_after();
+      float s[32];
+      tmem_ld32(trow + 32 * sl, s);
+      pwait(&k_full[g & 3], (g >> 2) & 1, abort_flag);  // the group's scales (already complete)
+      const float4* sk4 = reinterpret_cast<const float4*>(smem + Ly::oSc) + (g & 3) * (2 * kGroup / 4);
+      const float4* sv4 = sk4 + kGroup / 4;
+      tmem_wait_ld();
+      const int key0 = g * kGroup;
+      const bool full = __all_sync(0xffffffffu, key0 + kGroup - 1 <= lim);  // no key of the warp is masked
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 k4 = sk4[i];
+        s[4 * i] = __fmul_rn(__fmul_rn(s[4 * i], k4.x), c2);
+        s[4 * i + 1] = __fmul_rn(__fmul_rn(s[4 * i + 1], k4.y), c2);
+        s[4 * i + 2] = __fmul_rn(__fmul_rn(s[4 * i + 2], k4.z), c2);
+        s[4 * i + 3] = __fmul_rn(__fmul_rn(s[4 * i + 3], k4.w), c2);
+      }
+      if (!full) {
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (key0 + t > lim) s[t] = -INFINITY;
+      }
+      const float mg = tree_max(s);
+      float lg = 0.f, A = 0.f;
+      if (mg != -INFINITY) {
+#pragma unroll
+        for (int t = 0; t < 32; ++t) s[t] = ex2(__fsub_rn(s[t], mg));  // p~; 0 for a masked key
+        lg = tree_sum(s);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 v4 = sv4[i];
+          s[4 * i] = __fmul_rn(s[4 * i], v4.x);
+          s[4 * i + 1] = __fmul_rn(s[4 * i + 1], v4.y);
+          s[4 * i + 2] = __fmul_rn(s[4 * i + 2], v4.z);
+          s[4 * i + 3] = __fmul_rn(s[4 * i + 3], v4.w);
+        }
+        if (!full) {
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            if (key0 + t > lim) s[t] = 0.f;  // a masked key's scale may be stale
+        }
+        A = tree_max(s);
+      }
+      // S and the group's scales are read: the S slot and (two groups later, after
+      // QK(g + 2)) the scale slot may be refilled
+      tc_fence_before();
+      mbar_arrive(&s_free[sl]);
+      // sW = A / 127 and the codes round(W / sW), both IEEE fp32 quotients (W / sW
+      // by Markstein's method); W / sW <= A / RN(A / 127) < 127.5, no clamp needed
+      const float sw = div127(A);
+      uint32_t pk[16];
+      if (A > 0.f) {
+        div_row(s, sw, __frcp_rn(sw));
+        // round-half-even(q) + 1024 as the f16 bit pattern 0x6400 + code, from the
+        // low bits of the fp32 sum q + 1.5 * 2^23 + 0x6400; two per register, then
+        // 1024 subtracted (exact)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t lo = __float_as_uint(__fadd_rn(s[2 * i], 12608512.0f));
+          const uint32_t hi = __float_as_uint(__fadd_rn(s[2 * i + 1], 12608512.0f));
+          uint32_t h = __byte_perm(lo, hi, 0x5410);
+          asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(h) : "r"(0x64006400u));
+          pk[i] = h;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = 0u;
+      }
+      // Wq (f16) -> the PV A tile, row `row`; then the row statistics
+      if (g >= 2) pwait(&pv_done[sl], ((g - 2) >> 1) & 1, abort_flag);  // PV(g-2) has read the slot
+      uint8_t* p16 = smem + Ly::oP + (size_t)sl * Ly::kP16;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(p16 + swz_chunk<64>(row, c)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_async_smem();
+      mbar_arrive(&p_full[sl]);
+      float* st = stats + (g & 3) * 3 * kRows;
+      st[row] = mg;
+      st[kRows + row] = sw;
+      st[2 * kRows + row] = lg;
+      mbar_arrive(&st_full[g & 3]);
+    };
+
+    // o = alpha o + exp(m_g - m') sW (Wq x Vq), l = alpha l + exp(m_g - m') l_g
+    auto update = [&](int h) {
+      pwait(&pv_done[h & 1], (h >> 1) & 1, abort_flag);
+      pwait(&st_full[h & 3], (h >> 2) & 1, abort_flag);
+      const float* st = stats + (h & 3) * 3 * kRows;
+      const float mg = st[row], sw = st[kRows + row], lg = st[2 * kRows + row];
+      float alpha = 1.f, e = 0.f;
+      if (mg != -INFINITY) {
+        const float mn = fmaxf(m, mg);
+        alpha = m == -INFINITY ? 0.f : ex2(__fsub_rn(m, mn));
+        const float f = ex2(__fsub_rn(mg, mn));
+        e = __fmul_rn(f, sw);
+        l = __fmaf_rn(l, alpha, __fmul_rn(f, lg));
+        m = mn;
+      }
       tc_fence_after();
       const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
 #pragma unroll
       for (int c = 0; c < DH / 32; ++c) {
         float v[32];
-        tmem_ld32(trow + Ly::kPVCol + half * DH + 32 * c, v);
+        tmem_ld32(trow + Ly::kPVCol + wg * DH + 32 * c, v);
         tmem_wait_ld();
         if (c == DH / 32 - 1) {
           tc_fence_before();
@@ -352,101 +501,24 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
         }
         if (rescale) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[32 * c + i] = __fmaf_rn(v[i], sw, __fmul_rn(o[32 * c + i], alpha));
+          for (int i = 0; i < 32; ++i) o[32 * c + i] = __fmaf_rn(v[i], e, __fmul_rn(o[32 * c + i], alpha));
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[32 * c + i] = __fmaf_rn(v[i], sw, o[32 * c + i]);
+          for (int i = 0; i < 32; ++i) o[32 * c + i] = __fmaf_rn(v[i], e, o[32 * c + i]);
         }
       }
     };
 
     for (int g = 0; g < ng; ++g) {
-      const int sl = g & 1;
-      pwait(&s_full[sl], (g >> 1) & 1, abort_flag);
-      tc_fence_after();
-      float s[16];
-      tmem_ld16(trow + 32 * sl + 16 * half, s);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&s_free[sl]);
-      pwait(&conv_full[sl], (g >> 1) & 1, abort_flag);  // the group's scales (already complete)
-      const float4* sc4 = reinterpret_cast<const float4*>(smem + Ly::oSc) + sl * (kGroup / 2) + half * 8;
-      float sk[16], sv[16];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 f = sc4[i];
-        sk[2 * i] = f.x;
-        sv[2 * i] = f.y;
-        sk[2 * i + 1] = f.z;
-        sv[2 * i + 1] = f.w;
-      }
-      // ---- scores (acc x sQ x sK x scale), causal mask, the group's row maximum ----
-      const int key0 = g * kGroup + half * 16;
-      float gmh = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        s[i] = key0 + i <= lim ? __fmul_rn(__fmul_rn(__fmul_rn(s[i], sq), sk[i]), csc) : -INFINITY;
-        gmh = fmaxf(gmh, s[i]);
-      }
-      xm[half * kRows + row] = gmh;
-      named_bar_sync(pair_bar, 64);
-      const float gm = fmaxf(xm[row], xm[kRows + row]);
-      // ---- online softmax: m' = max(m, gm), alpha = exp(m - m'), p~ = exp(s - m') ----
-      const float mn = fmaxf(m, gm);
-      float alpha = 1.f;
-      float w[16];
-      float ah = 0.f, lsum = 0.f;
-      if (mn != -INFINITY) {
-        alpha = m == -INFINITY ? 0.f : expf(__fsub_rn(m, mn));
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float pe = expf(__fsub_rn(s[i], mn));  // 0 for masked keys
-          lsum += pe;
-          w[i] = pe != 0.f ? __fmul_rn(pe, sv[i]) : 0.f;
-          ah = fmaxf(ah, w[i]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = 0.f;
-      }
-      m = mn;
-      l = __fmaf_rn(l, alpha, lsum);
-      xa[half * kRows + row] = ah;
-      named_bar_sync(pair_bar, 64);
-      const float A = fmaxf(xa[row], xa[kRows + row]);
-      // sW = A / 127 and the codes round(W / sW), both IEEE fp32 quotients (W / sW
-      // by Markstein's method); W / sW <= A / RN(A / 127) < 127.5, no clamp needed
-      const float sw = div127(A);
-      const float ysw = __frcp_rn(sw);
-      const bool tiny = sw < kTinyDivisor;
-      uint32_t pk[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float c0 = A > 0.f ? rintf(div_shared(w[2 * i], sw, ysw, tiny)) : 0.f;
-        const float c1 = A > 0.f ? rintf(div_shared(w[2 * i + 1], sw, ysw, tiny)) : 0.f;
-        pk[i] = f16x2_of(c0, c1);
-      }
-      // ---- Wq (f16) -> the PV A tile: row `row`, keys 16 half .. 16 half + 15 ----
-      if (g >= 2) pwait(&mma_done[sl], ((g - 2) >> 1) & 1, abort_flag);  // PV(g-2) has read the slot
-      uint8_t* p16 = smem + Ly::oP + (size_t)sl * Ly::kP16;
-      *reinterpret_cast<uint4*>(p16 + swz_chunk<64>(row, 2 * half)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<uint4*>(p16 + swz_chunk<64>(row, 2 * half + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      fence_async_smem();
-      mbar_arrive(&p_full[sl]);
-      // ---- the previous group's product joins the output ----
-      if (g >= 1) update(g - 1, prev_alpha, prev_sw);
-      prev_alpha = alpha;
-      prev_sw = sw;
+      if ((g & 1) == wg) softmax(g);
+      if (g >= 1) update(g - 1);
     }
-    if (ng >= 1) update(ng - 1, prev_alpha, prev_sw);
+    if (ng >= 1) update(ng - 1);
 
-    // ---- finish: O = o / l ----
-    xl[half * kRows + row] = l;
-    named_bar_sync(pair_bar, 64);
-    const float lt = xl[row] + xl[kRows + row];
+    // ---- finish: O = o / l (both warpgroups hold the same l) ----
     if (valid) {
-      const float inv = 1.0f / lt;
-      float4* orow = reinterpret_cast<float4*>(p.out + ((size_t)j * Hq + hq) * D + half * DH);
+      const float inv = 1.0f / l;
+      float4* orow = reinterpret_cast<float4*>(p.out + ((size_t)j * Hq + hq) * D + wg * DH);
 #pragma unroll
       for (int i = 0; i < DH / 4; ++i)
         orow[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);

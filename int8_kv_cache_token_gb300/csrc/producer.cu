@@ -45,18 +45,19 @@ __device__ __forceinline__ float quantize_slice(const uint4 (&raw)[2], bool acti
 #pragma unroll
   for (int o = LPV / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float scale = __fdiv_rn(amax, 127.0f);
-  const float y = __frcp_rn(scale);
-  const bool tiny = scale < kTinyDivisor;
   // Codes: round half to even by adding 1.5 * 2^23 (the fp32 sum keeps the
   // integer part of x / scale in its low mantissa bits, so its low byte is the
   // two's-complement code).  |x / scale| <= amax / RN(amax / 127) < 127.5, so no
   // code ever needs clamping to [-127, 127].
+  if (amax > 0.f) {
+    div_row(x, scale, __frcp_rn(scale));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = 0.f;
+  }
   uint32_t q[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float qf = (amax > 0.f) ? div_shared(x[i], scale, y, tiny) : 0.f;
-    q[i] = __float_as_uint(__fadd_rn(qf, 12582912.0f));
-  }
+  for (int i = 0; i < 16; ++i) q[i] = rne_bits(x[i]);
   uint32_t pk[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j)
