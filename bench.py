@@ -572,8 +572,10 @@ def run_secondary(torch, i8, hbm_peak):
         i8.kv_quant_write(dummy, dummy, none, **cache, q=qd, q_i8=q_i8, q_scale=q_s)
         out = torch.empty((w.chunk, w.Hq, w.D), dtype=torch.float32, device="cuda")
         bt = to_dev(torch, w.block_table)
+        pws = i8.prefix_workspace(w.history, w.chunk, w.Hkv, w.D)
         ms = time_graph(torch, lambda: i8.int8_prefix_attn(out, q_i8, q_s, cache["k_cache"], cache["v_cache"],
-                                                           cache["k_scale"], cache["v_scale"], bt, w.history), 5)
+                                                           cache["k_scale"], cache["v_scale"], bt, w.history,
+                                                           workspace=pws), 5)
         res["prefix_16384+2048"] = {"ms": ms, "int8_tops": w.int8_ops() / (ms / 1e3) / 1e12,
                                     "pairs": w.pairs(), "ops": w.int8_ops()}
     except Exception as e:  # pragma: no cover
@@ -636,10 +638,11 @@ def run_profile_prefix(args):
     i8.kv_quant_write(dummy, dummy, none, **cache, q=qd, q_i8=q_i8, q_scale=q_s)
     out = torch.empty((w.chunk, w.Hq, w.D), dtype=torch.float32, device="cuda")
     bt = to_dev(torch, w.block_table)
+    pws = i8.prefix_workspace(w.history, w.chunk, w.Hkv, w.D)
     torch.cuda.synchronize()
     for _ in range(args.warmup + args.steps):
         i8.int8_prefix_attn(out, q_i8, q_s, cache["k_cache"], cache["v_cache"], cache["k_scale"], cache["v_scale"],
-                            bt, w.history)
+                            bt, w.history, workspace=pws)
     torch.cuda.synchronize()
     assert i8.device_error() == 0
     print(json.dumps({"profile": "int8_prefix", "history": w.history, "chunk": w.chunk,

@@ -194,11 +194,21 @@ i8kv_status i8kv_int8_decode_step(float* out, const uint16_t* q, const uint16_t*
 /*   O = o / l.                                                               */
 /* q_i8: int8 [chunk_len, Hq, D], q_scale: fp32 [chunk_len, Hq].             */
 /* out: fp32 [chunk_len, Hq, D].  softmax_scale <= 0 selects 1/sqrt(D).      */
+/* workspace: device memory of at least i8kv_prefix_workspace_bytes(...)    */
+/*   bytes, 16-byte aligned, no initialization needed.  The call first      */
+/*   writes into it the sequence's K/V codes as f16 (exact) operand tiles,  */
+/*   one per (KV head, 32-key group), then runs the attention from them;    */
+/*   about 4.1 bytes per cached (token, KV head, head dim).  Calls that     */
+/*   overlap in time need separate workspaces.                              */
+/* The call launches two kernels (the tiles and the attention).             */
 /* ------------------------------------------------------------------------ */
+size_t i8kv_prefix_workspace_bytes(int history_len, int chunk_len, int Hkv, int D);
+
 i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
                                   const int8_t* v_cache, const float* k_scale, const float* v_scale,
                                   const int32_t* block_table, int history_len, int chunk_len, int Hq, int Hkv, int D,
-                                  int block_size, int num_blocks, float softmax_scale, void* stream);
+                                  int block_size, int num_blocks, float softmax_scale, void* workspace,
+                                  size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Debug: raw int32 QK accumulators acc[b, h, t] = sum_d q_i8[b,h,d] *        */

@@ -23,5 +23,7 @@ from .binding import (  # noqa: F401
     last_error,
     lib,
     library_path,
+    prefix_workspace,
+    prefix_workspace_bytes,
     version,
 )

@@ -44,7 +44,8 @@ _SIGS = {
     "i8kv_int8_decode_step": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P],
     "i8kv_int8_paged_decode_attn_noalloc": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                             _P],
-    "i8kv_int8_prefix_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P],
+    "i8kv_prefix_workspace_bytes": [_I, _I, _I, _I],
+    "i8kv_int8_prefix_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _Z, _P],
     "i8kv_debug_qk_i32": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
     "i8kv_bf16_kv_write": [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P],
     "i8kv_bf16_paged_decode_attn": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P],
@@ -68,6 +69,7 @@ def lib():
             fn.argtypes = args
             fn.restype = _I
         L.i8kv_decode_workspace_bytes.restype = _Z
+        L.i8kv_prefix_workspace_bytes.restype = _Z
         _lib = L
     return _lib
 
@@ -249,14 +251,28 @@ def debug_qk_i32(acc, q_i8, k_cache, block_tables, seq_lens, stream=None):
 
 
 # ----------------------------------------------------------------------------- prefix
+def prefix_workspace_bytes(history_len: int, chunk_len: int, Hkv: int, D: int) -> int:
+    return int(lib().i8kv_prefix_workspace_bytes(history_len, chunk_len, Hkv, D))
+
+
+def prefix_workspace(history_len: int, chunk_len: int, Hkv: int, D: int, device="cuda") -> torch.Tensor:
+    """A prefix workspace (the f16 operand tiles; reusable by later calls on the same stream)."""
+    n = prefix_workspace_bytes(history_len, chunk_len, Hkv, D)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
 def int8_prefix_attn(out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, history_len: int,
-                     softmax_scale: float = 0.0, stream=None):
-    """out [C, Hq, D] fp32 <- INT8 prefix-chunk attention of q_i8 [C, Hq, D] over history + chunk."""
+                     workspace=None, softmax_scale: float = 0.0, stream=None):
+    """out [C, Hq, D] fp32 <- INT8 prefix-chunk attention of q_i8 [C, Hq, D] over history + chunk.
+
+    workspace: a prefix_workspace(...) tensor; when None one is allocated for this call."""
     NB, Hkv, D = _cache_geom(k_cache, 16)
     C, Hq, _ = q_i8.shape
+    if workspace is None:
+        workspace = prefix_workspace(int(history_len), C, Hkv, D, device=out.device)
     _check(lib().i8kv_int8_prefix_attn(
         _ptr(out, torch.float32, "out"), _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
         _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
         _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
         _ptr(block_table, torch.int32, "block_table"), int(history_len), C, Hq, Hkv, D, BLOCK_SIZE, NB,
-        float(softmax_scale), _stream(stream)))
+        float(softmax_scale), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))

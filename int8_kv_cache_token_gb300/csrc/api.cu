@@ -232,10 +232,16 @@ i8kv_status i8kv_int8_paged_decode_attn_noalloc(float* out, const int8_t* q_i8, 
   return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "noalloc int8 decode launch");
 }
 
+size_t i8kv_prefix_workspace_bytes(int history_len, int chunk_len, int Hkv, int D) {
+  if (history_len < 0 || chunk_len <= 0 || Hkv <= 0 || (D != 128 && D != 256)) return 0;
+  return i8kv::prefix_workspace_bytes(history_len, chunk_len, Hkv, D);
+}
+
 i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
                                   const int8_t* v_cache, const float* k_scale, const float* v_scale,
                                   const int32_t* block_table, int history_len, int chunk_len, int Hq, int Hkv, int D,
-                                  int block_size, int num_blocks, float softmax_scale, void* stream) {
+                                  int block_size, int num_blocks, float softmax_scale, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
   REQUIRE(history_len >= 0 && chunk_len >= 0, I8KV_ERR_INVALID_ARG, "history_len=%d chunk_len=%d", history_len,
           chunk_len);
   i8kv_status s = check_heads(Hq, Hkv, D);
@@ -247,8 +253,13 @@ i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q
           "null pointer");
   REQUIRE(aligned16(k_cache) && aligned16(v_cache) && aligned16(q_i8) && aligned16(k_scale) && aligned16(v_scale),
           I8KV_ERR_INVALID_ARG, "caches, scales and q must be 16-byte aligned");
+  const size_t need = i8kv::prefix_workspace_bytes(history_len, chunk_len, Hkv, D);
+  REQUIRE(workspace != nullptr && workspace_bytes >= need, I8KV_ERR_WORKSPACE,
+          "prefix workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+  REQUIRE(aligned16(workspace), I8KV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   i8kv::PrefixParams p{out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, history_len, chunk_len,
-                       Hq, Hkv, Hq / Hkv, D, num_blocks, softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D)};
+                       Hq, Hkv, Hq / Hkv, D, num_blocks, softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D),
+                       static_cast<uint8_t*>(workspace)};
   return from_cuda(i8kv::launch_int8_prefix(p, static_cast<cudaStream_t>(stream)), "int8 prefix launch");
 }
 

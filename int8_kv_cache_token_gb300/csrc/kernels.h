@@ -74,6 +74,7 @@ struct PrefixParams {
   const int32_t* block_table;
   int H, C, Hq, Hkv, G, D, num_blocks;
   float sm_scale;
+  uint8_t* tiles;  // workspace: f16 operand tiles per (KV head, 32-key group)
 };
 
 // Per-translation-unit device error words (read and cleared).
@@ -82,6 +83,7 @@ cudaError_t read_error_decode(int* value);
 cudaError_t read_error_prefix(int* value);
 
 cudaError_t launch_kv_quant_write(const ProducerParams& p, cudaStream_t stream);
+size_t prefix_workspace_bytes(int H, int C, int Hkv, int D);
 cudaError_t launch_bf16_kv_write(const ProducerParams& p, uint16_t* k_cache, uint16_t* v_cache, cudaStream_t stream);
 
 // Per-device decode geometry: CTAs per launch and dynamic shared memory.

@@ -30,14 +30,20 @@
 // partial sum stays below 2^22, so f16 MMAs with fp32 accumulation give the
 // INT8 contractions' exact integer results.
 //
-// Warps.  Warp 0 lane 0 issues the bulk copies of each group's int8 pages and
-// scale rows (three groups in flight); warps 0, 2 and 3 convert each group once
-// into f16 operand tiles (K-major, 16-byte chunks XOR-swizzled: K as [key][dim]
-// in 128-byte rows, V as [dim][key] in 64-byte rows), K one group ahead of V.
-// Warp 1 owns the TMEM allocation; its lane 0 issues every MMA, the QK two
-// groups ahead of the PV.  Warpgroups 1 and 2 (warps 4-7, 8-11) take the
-// softmax of the even and the odd groups, thread = row, so the two run side by
-// side; both apply every group's product to their half of the output dims.
+// Operand tiles.  Every one of the row blocks of a KV head multiplies the same
+// keys, so the int8 -> f16 conversion (exact) is done once per (KV head,
+// 32-key group) by prefix_tiles_kernel, into a workspace tile laid out exactly
+// as the MMAs read it in shared memory (K-major, 16-byte chunks XOR-swizzled:
+// K as [key][dim] in 128-byte rows, V as [dim][key] in 64-byte rows) followed
+// by the group's sK and sV.  The attention kernel moves each tile with one
+// bulk copy.
+//
+// Warps of the attention kernel.  Warp 0 lane 0 issues the tiles' bulk copies
+// (a ring of four); warp 1 owns the TMEM allocation and its lane 0 issues every
+// MMA, each QK or PV as soon as its operands are ready.  Warpgroups 1 and 2
+// (warps 4-7, 8-11) take the softmax of the even and the odd groups, thread =
+// row, so the two run side by side; both apply every group's product to their
+// half of the output dims.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -50,34 +56,37 @@ constexpr int kBS = 16;
 constexpr int kRows = 128;       // query rows per CTA: the MMA's M, one TMEM lane each
 constexpr int kGroup = 32;       // keys per probability group
 constexpr int kPagesPG = kGroup / kBS;
-constexpr int kStages = 3;       // int8 staging buffers (groups in flight)
-constexpr int kMaxHkv = 8;
+constexpr int kStages = 4;       // operand tiles in flight
 constexpr int kThreads = 384;
+constexpr int kLoadWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kCompWarp0 = 4;    // warps 4..11
-constexpr int kConvThreads = 96; // warps 0, 2, 3
 constexpr int kWGThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
+
+// One (KV head, group) operand tile, in global memory and in shared memory.
+template <int D>
+struct Tile {
+  static constexpr int kK16 = kGroup * D * 2;           // f16 K, D/64 atoms of [32 keys][128 B] (SW128)
+  static constexpr int kV16 = D * kGroup * 2;           // f16 V, [D][64 B] (SW64)
+  static constexpr int oK = 0;
+  static constexpr int oV = kK16;
+  static constexpr int oSk = kK16 + kV16;               // sK[32], then sV[32]
+  static constexpr int kBytes = oSk + 2 * kGroup * 4;   // one bulk copy
+  static constexpr int kSlot = (kBytes + 1023) / 1024 * 1024;  // shared-memory stride (SW128 needs 1024-byte bases)
+};
 
 template <int D>
 struct Lay {
   static constexpr int kQ16 = kRows * D * 2;          // f16 Q, D/64 atoms of [128 rows][128 B]
-  static constexpr int kK16 = kGroup * D * 2;         // f16 K, D/64 atoms of [32 keys][128 B]
-  static constexpr int kV16 = D * kGroup * 2;         // f16 V, [D][64 B]
   static constexpr int kP16 = kRows * kGroup * 2;     // f16 Wq, [128][64 B]
-  static constexpr int kPage = D * kBS;               // one int8 K or V page
-  static constexpr int kSRow = kBS * kMaxHkv * 4;     // one block's scale rows (room for kMaxHkv heads)
-  static constexpr int kStage = 2 * kPagesPG * kPage + 2 * kPagesPG * kSRow;
   static constexpr int oQ = 0;
-  static constexpr int oK = oQ + kQ16;                // two slots
-  static constexpr int oV = oK + 2 * kK16;            // two slots
-  static constexpr int oP = oV + 2 * kV16;            // two slots
-  static constexpr int oStage = oP + 2 * kP16;        // kStages
-  static constexpr int oSc = oStage + kStages * kStage;  // four slots of sK[32], sV[32]
-  static constexpr int oSt = oSc + 4 * 2 * kGroup * 4;   // four slots of m_g[128], sW[128], l_g[128]
+  static constexpr int oTile = oQ + kQ16;             // kStages tiles
+  static constexpr int oP = oTile + kStages * Tile<D>::kSlot;  // two slots
+  static constexpr int oSt = oP + 2 * kP16;           // four slots of m_g[128], sW[128], l_g[128]
   static constexpr int oBar = oSt + 4 * 3 * kRows * 4;
-  // stage_full[3], k_full[4], v_full[2], qk_done[2], s_free[2], p_full[2], pv_done[2], pv_free, st_full[4]
-  static constexpr int kBars = kStages + 4 + 2 + 2 + 2 + 2 + 2 + 1 + 4;
+  // tile_full[4], tile_free[4], qk_done[2], s_free[2], p_full[2], pv_done[2], pv_free, st_full[4]
+  static constexpr int kBars = kStages + kStages + 2 + 2 + 2 + 2 + 1 + 4;
   static constexpr int oCtl = oBar + kBars * 8;       // TMEM base, abort flag
   static constexpr int kTotal = oCtl + 16;
   // TMEM: S in columns [0, 64) (two slots of 32), PV in [kPVCol, kPVCol + D)
@@ -148,26 +157,89 @@ __device__ __forceinline__ void pwait(uint64_t* bar, uint32_t parity, volatile i
   }
 }
 
+// ---- operand tiles: one CTA per (group, KV head); the int8 pages and scales
+// of the group's 32 keys -> the f16 tile (exact codes) and sK, sV.  Keys past
+// the sequence (the last group's tail) get zero codes and scales; the
+// attention masks them anyway.
+template <int D>
+__global__ void __launch_bounds__(256) prefix_tiles_kernel(PrefixParams p) {
+  using T = Tile<D>;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int g = blockIdx.x, kvh = blockIdx.y, tid = threadIdx.x;
+  const int Hkv = p.Hkv;
+  const int ngt = gridDim.x;
+  const int max_blk = (p.H + p.C + kBS - 1) / kBS;
+  uint8_t* tile = p.tiles + ((size_t)kvh * ngt + g) * T::kBytes;
+  int blk[kPagesPG];
+#pragma unroll
+  for (int i = 0; i < kPagesPG; ++i) {
+    const int lb = g * kPagesPG + i;
+    blk[i] = lb < max_blk ? p.block_table[lb] : -1;
+    if (lb < max_blk && (blk[i] < 0 || blk[i] >= p.num_blocks)) {
+      if (tid == 0) record_error(2);
+      blk[i] = -1;
+    }
+  }
+  // K page [D/16][16 tokens][16 B] -> [key][D] (SW128 atoms): chunk i = (page, dim chunk, token)
+  constexpr int KC = kPagesPG * (D / 16) * kBS;
+  for (int i = tid; i < KC; i += 256) {
+    const int pg = i / ((D / 16) * kBS), rem = i % ((D / 16) * kBS);
+    const int dc = rem / kBS, key = pg * kBS + rem % kBS;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (blk[pg] >= 0)
+      v = __ldg(reinterpret_cast<const uint4*>(p.k_cache + ((size_t)blk[pg] * Hkv + kvh) * (D * kBS)) + rem);
+    uint4 h0, h1;
+    s8x16_to_f16(v, h0, h1);
+    uint8_t* atom = tile + T::oK + (size_t)(dc / 4) * (kGroup * 128);
+    *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4))) = h0;
+    *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4) + 1)) = h1;
+  }
+  // V page [D][16 tokens] -> [D][32 keys] (SW64): chunk i = (page, dim)
+  for (int i = tid; i < kPagesPG * D; i += 256) {
+    const int pg = i / D, d = i % D;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (blk[pg] >= 0)
+      v = __ldg(reinterpret_cast<const uint4*>(p.v_cache + ((size_t)blk[pg] * Hkv + kvh) * (D * kBS)) + d);
+    uint4 h0, h1;
+    s8x16_to_f16(v, h0, h1);
+    *reinterpret_cast<uint4*>(tile + T::oV + swz_chunk<64>(d, 2 * pg)) = h0;
+    *reinterpret_cast<uint4*>(tile + T::oV + swz_chunk<64>(d, 2 * pg + 1)) = h1;
+  }
+  if (tid < kGroup) {
+    const int pg = tid / kBS;
+    float sk = 0.f, sv = 0.f;
+    if (blk[pg] >= 0) {
+      const size_t si = ((size_t)blk[pg] * kBS + tid % kBS) * Hkv + kvh;
+      sk = p.k_scale[si];
+      sv = p.v_scale[si];
+    }
+    float* sc = reinterpret_cast<float*>(tile + T::oSk);
+    sc[tid] = sk;
+    sc[kGroup + tid] = sv;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p) {
   using Ly = Lay<D>;
+  using T = Tile<D>;
   constexpr int DH = D / 2;  // output dims per warpgroup
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* stage_full = reinterpret_cast<uint64_t*>(smem + Ly::oBar);
-  uint64_t* k_full = stage_full + kStages;  // [g & 3]: K(g) in its f16 slot, the group's scales
-  uint64_t* v_full = k_full + 4;            // [g & 1]: V(g) in its f16 slot
-  uint64_t* qk_done = v_full + 2;           // [g & 1]: S(g) in TMEM; K slot free
-  uint64_t* s_free = qk_done + 2;           // [g & 1]: S(g) read
-  uint64_t* p_full = s_free + 2;            // [g & 1]: Wq(g) in its slot
-  uint64_t* pv_done = p_full + 2;           // [g & 1]: PV(g) in TMEM; V and Wq slots free
-  uint64_t* pv_free = pv_done + 2;          // PV accumulator read by both warpgroups
-  uint64_t* st_full = pv_free + 1;          // [g & 3]: the group's row statistics
+  uint64_t* tile_full = reinterpret_cast<uint64_t*>(smem + Ly::oBar);  // [g % kStages]: tile g landed
+  uint64_t* tile_free = tile_full + kStages;  // [g % kStages]: PV(g) done, the tile slot may be refilled
+  uint64_t* qk_done = tile_free + kStages;    // [g & 1]: S(g) in TMEM
+  uint64_t* s_free = qk_done + 2;             // [g & 1]: S(g) read
+  uint64_t* p_full = s_free + 2;              // [g & 1]: Wq(g) in its slot
+  uint64_t* pv_done = p_full + 2;             // [g & 1]: PV(g) in TMEM; the Wq slot free
+  uint64_t* pv_free = pv_done + 2;            // PV accumulator read by both warpgroups
+  uint64_t* st_full = pv_free + 1;            // [g & 3]: the group's row statistics
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::oCtl);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::oCtl + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kvh = blockIdx.y;
-  const int G = p.G, Hkv = p.Hkv, Hq = p.Hq, H = p.H, C = p.C;
+  const int G = p.G, Hq = p.Hq, H = p.H, C = p.C;
   const int R = C * G;
   // Row blocks in reverse: later chunk tokens see more keys, and CTAs start in
   // index order, so the heaviest blocks run first and the last wave holds the
@@ -176,16 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
   const int j_hi = min(C - 1, (r0 + kRows - 1) / G);
   const int n_keys = H + j_hi + 1;
   const int ng = (n_keys + kGroup - 1) / kGroup;
-  const int max_blk = (H + C + kBS - 1) / kBS;
+  const int ngt = (H + C + kGroup - 1) / kGroup;  // groups of the whole sequence (tiles per KV head)
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&stage_full[s], 1);
-    for (int s = 0; s < 4; ++s) {
-      mbar_init(&k_full[s], kConvThreads);
-      mbar_init(&st_full[s], kWGThreads);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&tile_full[s], 1);
+      mbar_init(&tile_free[s], 1);
     }
+    for (int s = 0; s < 4; ++s) mbar_init(&st_full[s], kWGThreads);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&v_full[s], kConvThreads);
       mbar_init(&qk_done[s], 1);
       mbar_init(&s_free[s], kWGThreads);
       mbar_init(&p_full[s], kWGThreads);
@@ -200,7 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // From here on the kernel reads what earlier work on the stream wrote.
+  // From here on the kernel reads what earlier work on the stream wrote (the
+  // query and the operand tiles).
   griddep_wait();
   griddep_launch_dependents();
 
@@ -228,144 +300,82 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
 
   if (warp < kCompWarp0) {
     regs_dec<56>();  // warpgroup 0 hands registers to the softmax/output warpgroups
-    if (warp != kMmaWarp) {
-      // ================= copies and conversion (warps 0, 2, 3) =================
-      const int ct = warp == 0 ? lane : tid - 32;  // 0 .. 95
-      const uint32_t srow = kBS * Hkv * 4;
-      auto issue = [&](int g) {  // warp 0 lane 0
+    if (warp == kLoadWarp && lane == 0) {
+      // ================= tile copies (warp 0, lane 0) =================
+      const uint8_t* src = p.tiles + (size_t)kvh * ngt * T::kBytes;
+      int g = 0;
+      for (; g < ng; ++g) {
         const int st = g % kStages;
-        uint8_t* base = smem + Ly::oStage + (size_t)st * Ly::kStage;
-        int blks[kPagesPG];
-        int nb = 0;
-#pragma unroll
-        for (int i = 0; i < kPagesPG; ++i) {
-          const int lb = g * kPagesPG + i;
-          int blk = -1;
-          if (lb < max_blk) {
-            blk = p.block_table[lb];
-            if (blk < 0 || blk >= p.num_blocks) {
-              record_error(2);
-              blk = -1;
-            }
-          }
-          blks[i] = blk;
-          nb += blk >= 0;
-        }
-        mbar_expect_tx(&stage_full[st], nb * (2 * Ly::kPage + 2 * srow));
-#pragma unroll
-        for (int i = 0; i < kPagesPG; ++i) {
-          if (blks[i] < 0) continue;
-          const size_t page = ((size_t)blks[i] * Hkv + kvh) * Ly::kPage;
-          bulk_g2s(base + i * Ly::kPage, p.k_cache + page, Ly::kPage, &stage_full[st]);
-          bulk_g2s(base + (kPagesPG + i) * Ly::kPage, p.v_cache + page, Ly::kPage, &stage_full[st]);
-          const size_t so = (size_t)blks[i] * kBS * Hkv;
-          bulk_g2s(base + 2 * kPagesPG * Ly::kPage + i * Ly::kSRow, p.k_scale + so, srow, &stage_full[st]);
-          bulk_g2s(base + 2 * kPagesPG * Ly::kPage + (kPagesPG + i) * Ly::kSRow, p.v_scale + so, srow,
-                   &stage_full[st]);
-        }
-        mbar_arrive(&stage_full[st]);
-      };
-      int issued = 0;  // groups whose copies were issued (warp 0 lane 0)
-      if (warp == 0 && lane == 0)
-        for (; issued < kStages && issued < ng; ++issued) issue(issued);
-      // step t converts K(t) and V(t - 1)
-      for (int t = 0; t <= ng; ++t) {
-        if (t < ng) {
-          const int st = t % kStages;
-          pwait(&stage_full[st], (t / kStages) & 1, abort_flag);
-          if (t >= 2) pwait(&qk_done[t & 1], ((t - 2) >> 1) & 1, abort_flag);  // QK(t-2) has read the K slot
-          const uint8_t* kt = smem + Ly::oStage + (size_t)st * Ly::kStage;
-          uint8_t* k16 = smem + Ly::oK + (size_t)(t & 1) * Ly::kK16;
-          // K page [D/16][16 tokens][16 B] -> [key][D]: chunk i = (page, dim chunk, token)
-          constexpr int KC = kPagesPG * (D / 16) * kBS;
-          for (int i = ct; i < KC; i += kConvThreads) {
-            const int pg = i / ((D / 16) * kBS), rem = i % ((D / 16) * kBS);
-            const int dc = rem / kBS, tk = rem % kBS;
-            const uint4 v = *reinterpret_cast<const uint4*>(kt + (size_t)pg * Ly::kPage + (size_t)rem * 16);
-            uint4 h0, h1;
-            s8x16_to_f16(v, h0, h1);
-            const int key = pg * kBS + tk;
-            uint8_t* atom = k16 + (size_t)(dc / 4) * (kGroup * 128);
-            *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4))) = h0;
-            *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4) + 1)) = h1;
-          }
-          if (ct < kGroup) {
-            const float* sks = reinterpret_cast<const float*>(kt + 2 * kPagesPG * Ly::kPage);
-            const float* svs = sks + kPagesPG * Ly::kSRow / 4;
-            float* sc = reinterpret_cast<float*>(smem + Ly::oSc) + (t & 3) * 2 * kGroup;
-            const int si = (ct / kBS) * (Ly::kSRow / 4) + (ct % kBS) * Hkv + kvh;
-            sc[ct] = sks[si];
-            sc[kGroup + ct] = svs[si];
-          }
-          fence_async_smem();
-          mbar_arrive(&k_full[t & 3]);
-        }
-        if (t >= 1) {
-          const int h = t - 1, st = h % kStages;
-          if (h >= 2) pwait(&pv_done[h & 1], ((h - 2) >> 1) & 1, abort_flag);  // PV(h-2) has read the V slot
-          const uint8_t* vt = smem + Ly::oStage + (size_t)st * Ly::kStage + kPagesPG * Ly::kPage;
-          uint8_t* v16 = smem + Ly::oV + (size_t)(h & 1) * Ly::kV16;
-          // V page [D][16 tokens] -> [D][32 keys]: chunk i = (page, dim)
-          for (int i = ct; i < kPagesPG * D; i += kConvThreads) {
-            const int pg = i / D, d = i % D;
-            const uint4 v = *reinterpret_cast<const uint4*>(vt + (size_t)pg * Ly::kPage + (size_t)d * 16);
-            uint4 h0, h1;
-            s8x16_to_f16(v, h0, h1);
-            *reinterpret_cast<uint4*>(v16 + swz_chunk<64>(d, 2 * pg)) = h0;
-            *reinterpret_cast<uint4*>(v16 + swz_chunk<64>(d, 2 * pg + 1)) = h1;
-          }
-          fence_async_smem();
-          mbar_arrive(&v_full[h & 1]);
-          named_bar_sync(5, kConvThreads);  // every converter is done with staging buffer st
-          if (warp == 0 && lane == 0 && issued < ng && !*abort_flag) issue(issued++);
-        }
+        if (g >= kStages) pwait(&tile_free[st], ((g - kStages) / kStages) & 1, abort_flag);
+        if (*abort_flag) break;
+        mbar_expect_tx(&tile_full[st], T::kBytes);
+        bulk_g2s(smem + Ly::oTile + (size_t)st * T::kSlot, src + (size_t)g * T::kBytes, T::kBytes, &tile_full[st]);
+        mbar_arrive(&tile_full[st]);
       }
-      if (warp == 0 && lane == 0) {
-        // copies issued but never waited for (after an abort) land before the CTA exits
-        for (int g = max(0, issued - kStages); g < issued; ++g)
-          mbar_wait(&stage_full[g % kStages], (g / kStages) & 1);
-      }
-    } else {
+      // copies issued but never waited for (after an abort) land before the CTA exits
+      for (int k = max(0, g - kStages); k < g; ++k) mbar_wait(&tile_full[k % kStages], (k / kStages) & 1);
+    } else if (warp == kMmaWarp && lane == 0) {
       // ================= MMA issue (warp 1, lane 0) =================
-      if (lane == 0) {
-        constexpr uint32_t idesc_qk = umma_idesc_f16(kRows, kGroup);
-        constexpr uint32_t idesc_pv = umma_idesc_f16(kRows, D);
-        const uint32_t q16 = smem_u32(smem + Ly::oQ);
-        auto qk = [&](int g) {
-          const int sl = g & 1;
-          pwait(&k_full[g & 3], (g >> 2) & 1, abort_flag);
-          if (g >= 2) pwait(&s_free[sl], ((g - 2) >> 1) & 1, abort_flag);
+      // Whichever of the next QK and the next PV has its operands first is
+      // issued; the checks never suspend (test_wait), a pass with nothing to
+      // issue sleeps briefly, and the same time limit as pwait applies.
+      constexpr uint32_t idesc_qk = umma_idesc_f16(kRows, kGroup);
+      constexpr uint32_t idesc_pv = umma_idesc_f16(kRows, D);
+      const uint32_t q16 = smem_u32(smem + Ly::oQ);
+      const uint32_t tiles = smem_u32(smem + Ly::oTile);
+      int nq = 0, np = 0;  // next QK, next PV
+      uint64_t t_idle = 0;
+      while (np < ng) {
+        bool did = false;
+        if (nq < ng && mbar_test(&tile_full[nq % kStages], (nq / kStages) & 1) &&
+            (nq < 2 || mbar_test(&s_free[nq & 1], ((nq - 2) >> 1) & 1))) {
+          const uint32_t k16 = tiles + (nq % kStages) * T::kSlot + T::oK;
           tc_fence_after();
-          const uint32_t k16 = smem_u32(smem + Ly::oK + (size_t)sl * Ly::kK16);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t a = q16 + (kk / 4) * (kRows * 128) + (kk % 4) * 32;
             const uint32_t b = k16 + (kk / 4) * (kGroup * 128) + (kk % 4) * 32;
-            umma_f16(tmem + 32 * sl, umma_desc(a, 128), umma_desc(b, 128), idesc_qk, kk > 0);
+            umma_f16(tmem + 32 * (nq & 1), umma_desc(a, 128), umma_desc(b, 128), idesc_qk, kk > 0);
           }
-          umma_commit(&qk_done[sl]);
-        };
-        for (int g = 0; g < 2 && g < ng; ++g) qk(g);
-        for (int h = 0; h < ng; ++h) {
-          if (h + 2 < ng) qk(h + 2);
-          const int sl = h & 1;
-          pwait(&v_full[sl], (h >> 1) & 1, abort_flag);
-          pwait(&p_full[sl], (h >> 1) & 1, abort_flag);
-          if (h >= 1) pwait(pv_free, (h - 1) & 1, abort_flag);
+          umma_commit(&qk_done[nq & 1]);
+          ++nq;
+          did = true;
+        }
+        if (np < nq && mbar_test(&p_full[np & 1], (np >> 1) & 1) &&
+            (np < 1 || mbar_test(pv_free, (np - 1) & 1))) {
+          const uint32_t p16 = smem_u32(smem + Ly::oP + (size_t)(np & 1) * Ly::kP16);
+          const uint32_t v16 = tiles + (np % kStages) * T::kSlot + T::oV;
           tc_fence_after();
-          const uint32_t p16 = smem_u32(smem + Ly::oP + (size_t)sl * Ly::kP16);
-          const uint32_t v16 = smem_u32(smem + Ly::oV + (size_t)sl * Ly::kV16);
 #pragma unroll
           for (int kk = 0; kk < kGroup / 16; ++kk)
             umma_f16(tmem + Ly::kPVCol, umma_desc(p16 + kk * 32, 64), umma_desc(v16 + kk * 32, 64), idesc_pv,
                      kk > 0);
-          umma_commit(&pv_done[sl]);
+          umma_commit(&pv_done[np & 1]);
+          umma_commit(&tile_free[np % kStages]);
+          ++np;
+          did = true;
         }
-        // every MMA has completed before TMEM is released (the last commit covers all)
-        if (ng >= 1) mbar_wait(&pv_done[(ng - 1) & 1], ((ng - 1) >> 1) & 1);
+        if (did) {
+          t_idle = 0;
+        } else {
+          if (*abort_flag) break;
+          const uint64_t now = global_timer_ns();
+          if (t_idle == 0) {
+            t_idle = now;
+          } else if (now - t_idle > kWaitLimitNs) {
+            record_error(1);
+            *abort_flag = 1;
+            break;
+          }
+          __nanosleep(32);
+        }
       }
-      __syncwarp();
+      // every MMA issued has completed before TMEM is released (the last commit
+      // covers all earlier MMAs)
+      if (np >= 1) mbar_wait(&pv_done[(np - 1) & 1], ((np - 1) >> 1) & 1);
+      if (nq > np) mbar_wait(&qk_done[(nq - 1) & 1], ((nq - 1) >> 1) & 1);
     }
+    __syncwarp();
   } else {
     // ================= softmax and output (warpgroups 1, 2) =================
     regs_inc<216>();
@@ -392,8 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
       tc_fence_after();
       float s[32];
       tmem_ld32(trow + 32 * sl, s);
-      pwait(&k_full[g & 3], (g >> 2) & 1, abort_flag);  // the group's scales (already complete)
-      const float4* sk4 = reinterpret_cast<const float4*>(smem + Ly::oSc) + (g & 3) * (2 * kGroup / 4);
+      pwait(&tile_full[g % kStages], (g / kStages) & 1, abort_flag);  // the group's scales (already landed)
+      const float4* sk4 =
+          reinterpret_cast<const float4*>(smem + Ly::oTile + (size_t)(g % kStages) * T::kSlot + T::oSk);
       const float4* sv4 = sk4 + kGroup / 4;
       tmem_wait_ld();
       const int key0 = g * kGroup;
@@ -428,14 +439,12 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
         if (!full) {
 #pragma unroll
           for (int t = 0; t < 32; ++t)
-            if (key0 + t > lim) s[t] = 0.f;  // a masked key's scale may be stale
+            if (key0 + t > lim) s[t] = 0.f;
         }
         A = tree_max(s);
       }
-      // S and the group's scales are read: the S slot and (two groups later, after
-      // QK(g + 2)) the scale slot may be refilled
       tc_fence_before();
-      mbar_arrive(&s_free[sl]);
+      mbar_arrive(&s_free[sl]);  // S is read; QK(g + 2) may overwrite it
       // sW = A / 127 and the codes round(W / sW), both IEEE fp32 quotients (W / sW
       // by Markstein's method); W / sW <= A / RN(A / 127) < 127.5, no clamp needed
       const float sw = div127(A);
@@ -533,20 +542,27 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
   }
 }
 
+template <int D>
+cudaError_t launch_prefix_d(const PrefixParams& p, cudaStream_t stream) {
+  const int ngt = (p.H + p.C + kGroup - 1) / kGroup;
+  cudaError_t e = launch_pdl(prefix_tiles_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(int8_prefix_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kTotal);
+  if (e != cudaSuccess) return e;
+  const int R = p.C * p.G;
+  return launch_pdl(int8_prefix_kernel<D>, dim3((R + kRows - 1) / kRows, p.Hkv), dim3(kThreads), Lay<D>::kTotal,
+                    stream, p);
+}
+
 }  // namespace
 
+size_t prefix_workspace_bytes(int H, int C, int Hkv, int D) {
+  const size_t ngt = ((size_t)H + C + kGroup - 1) / kGroup;
+  return ngt * Hkv * (D == 256 ? Tile<256>::kBytes : Tile<128>::kBytes);
+}
+
 cudaError_t launch_int8_prefix(const PrefixParams& p, cudaStream_t stream) {
-  const int R = p.C * p.G;
-  dim3 grid((R + kRows - 1) / kRows, p.Hkv);
-  cudaError_t e;
-  if (p.D == 256) {
-    e = cudaFuncSetAttribute(int8_prefix_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<256>::kTotal);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(int8_prefix_kernel<256>, grid, dim3(kThreads), Lay<256>::kTotal, stream, p);
-  }
-  e = cudaFuncSetAttribute(int8_prefix_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<128>::kTotal);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(int8_prefix_kernel<128>, grid, dim3(kThreads), Lay<128>::kTotal, stream, p);
+  return p.D == 256 ? launch_prefix_d<256>(p, stream) : launch_prefix_d<128>(p, stream);
 }
 
 }  // namespace i8kv

@@ -77,6 +77,17 @@ def test_argument_checks_without_gpu(lib):
     # prefix: chunk_len == 0 is a no-op; negative history rejected
     pf = lib.i8kv_int8_prefix_attn
     pf.restype = ctypes.c_int
-    pf.argtypes = [P] * 8 + [ctypes.c_int] * 7 + [ctypes.c_float, P]
-    assert pf(*([P(16)] * 8), 100, 0, 24, 4, 256, 16, 10, 0.0, None) == 0
-    assert pf(*([P(16)] * 8), -1, 5, 24, 4, 256, 16, 10, 0.0, None) == 1
+    pf.argtypes = [P] * 8 + [ctypes.c_int] * 7 + [ctypes.c_float, P, ctypes.c_size_t, P]
+    assert pf(*([P(16)] * 8), 100, 0, 24, 4, 256, 16, 10, 0.0, None, 0, None) == 0
+    assert pf(*([P(16)] * 8), -1, 5, 24, 4, 256, 16, 10, 0.0, P(16), 1 << 30, None) == 1
+    # the workspace: size from i8kv_prefix_workspace_bytes, checked before any launch
+    wb = lib.i8kv_prefix_workspace_bytes
+    wb.restype = ctypes.c_size_t
+    wb.argtypes = [ctypes.c_int] * 4
+    need = wb(100, 5, 4, 256)
+    assert need == 4 * ((100 + 5 + 31) // 32) * (2 * 32 * 256 * 2 + 256)
+    assert wb(100, 5, 4, 64) == 0
+    assert pf(*([P(16)] * 8), 100, 5, 24, 4, 256, 16, 10, 0.0, None, need, None) == 3
+    assert pf(*([P(16)] * 8), 100, 5, 24, 4, 256, 16, 10, 0.0, P(16), need - 1, None) == 3
+    assert "workspace" in _last_error(lib)
+    assert pf(*([P(16)] * 8), 100, 5, 24, 4, 256, 16, 10, 0.0, P(24), need, None) == 1
