@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
   __syncthreads();
 
   if (warp < kCompWarp0) {
-    regs_dec<56>();  // warpgroup 0 hands registers to the softmax/output warpgroups
+    regs_dec<64>();  // warpgroup 0 hands registers to the softmax/output warpgroups
     if (warp == kLoadWarp && lane == 0) {
       // ================= tile copies (warp 0, lane 0) =================
       const uint8_t* src = p.tiles + (size_t)kvh * ngt * T::kBytes;
@@ -499,21 +499,27 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
       }
       tc_fence_after();
       const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
+      // 32-column chunks, two in flight: chunk c + 1 is loading while chunk c
+      // joins the output (tcgen05.wait::ld waits for every load issued so far)
+      const uint32_t src = trow + Ly::kPVCol + wg * DH;
+      float v[2][32];
+      tmem_ld32(src, v[0]);
 #pragma unroll
       for (int c = 0; c < DH / 32; ++c) {
-        float v[32];
-        tmem_ld32(trow + Ly::kPVCol + wg * DH + 32 * c, v);
         tmem_wait_ld();
-        if (c == DH / 32 - 1) {
+        if (c + 1 < DH / 32) {
+          tmem_ld32(src + 32 * (c + 1), v[(c + 1) & 1]);
+        } else {
           tc_fence_before();
-          mbar_arrive(pv_free);
+          mbar_arrive(pv_free);  // every column of the accumulator is read
         }
+        const float(&x)[32] = v[c & 1];
         if (rescale) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[32 * c + i] = __fmaf_rn(v[i], e, __fmul_rn(o[32 * c + i], alpha));
+          for (int i = 0; i < 32; ++i) o[32 * c + i] = __fmaf_rn(x[i], e, __fmul_rn(o[32 * c + i], alpha));
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[32 * c + i] = __fmaf_rn(v[i], e, o[32 * c + i]);
+          for (int i = 0; i < 32; ++i) o[32 * c + i] = __fmaf_rn(x[i], e, o[32 * c + i]);
         }
       }
     };
