@@ -257,37 +257,33 @@ __device__ __forceinline__ void pipe_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// Query fragments (B operand of QK, f16 form) of the GQA-packed rows: column g of
-// the N-tile is query head kvh*G + g; per 32-dim step s the s8 fragment holds
-// dims 32s + {4t..4t+3} and 32s + 16 + {4t..4t+3}.
+// Query fragments (B operand of the s8 QK MMA) of the GQA-packed rows: column g
+// of the N-tile is query head kvh*G + g; per 32-dim step s the fragment holds
+// dims 32s + {4t..4t+3} and 32s + 16 + {4t..4t+3} as raw int8.
 template <int D>
 __device__ __forceinline__ void load_q_frags(const int8_t* q, int b, int Hq, int kvh, int G, int lane,
-                                             uint32_t (&qf)[D / 32][4]) {
+                                             uint32_t (&qf)[D / 32][2]) {
   const int g = lane >> 2, t = lane & 3;
   const int8_t* row = q + ((size_t)b * Hq + kvh * G + g) * D;
 #pragma unroll
   for (int s = 0; s < D / 32; ++s) {
-    const uint32_t x0 = g < G ? __ldg(reinterpret_cast<const uint32_t*>(row + 32 * s + 4 * t)) : 0u;
-    const uint32_t x1 = g < G ? __ldg(reinterpret_cast<const uint32_t*>(row + 32 * s + 16 + 4 * t)) : 0u;
-    s8b_to_f16(x0, x1, qf[s]);
+    qf[s][0] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(row + 32 * s + 4 * t)) : 0u;
+    qf[s][1] = g < G ? __ldg(reinterpret_cast<const uint32_t*>(row + 32 * s + 16 + 4 * t)) : 0u;
   }
 }
 
-// QK for the two 16-token blocks (2w, 2w+1) of warp w's group:
+// QK for the two 16-token blocks (2w, 2w+1) of warp w's group on the INT8 tensor
+// path (mma.sync m16n8k32, s8 x s8 -> s32: exact):
 // acc[m][0..3] = (token g, row 2t), (token g, row 2t+1), (token g+8, row 2t),
-// (token g+8, row 2t+1) of block 2w+m.  kpages holds 16 K pages [D/16][16][16 B].
+// (token g+8, row 2t+1) of block 2w+m.  kpages holds 16 K pages [D/16][16][16 B];
+// ldmatrix of (tokens 0-7 | 8-15) x (dim chunk 2s | 2s+1) of a page is the s8 A
+// fragment of dims 32s .. 32s + 31 as it is, so K is never converted.
 template <int D>
-__device__ __forceinline__ void qk_warp(const int8_t* kpages, int warp, int lane, const uint32_t (&qf)[D / 32][4],
+__device__ __forceinline__ void qk_warp(const int8_t* kpages, int warp, int lane, const uint32_t (&qf)[D / 32][2],
                                         float (&acc)[2][4]) {
   const int mi = lane >> 3, ri = lane & 7;
-  // Even and odd 32-dim steps accumulate separately (two independent MMA chains
-  // per block instead of one); the two partial sums are exact integers, so
-  // adding them at the end changes nothing.
-  float acc2[2][4];
-#pragma unroll
-  for (int m = 0; m < 2; ++m)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[m][i] = acc2[m][i] = 0.f;
+  // even and odd 32-dim steps accumulate separately: two independent MMA chains per block
+  int ae[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}}, ao[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
 #pragma unroll
   for (int s = 0; s < D / 32; ++s) {
 #pragma unroll
@@ -296,13 +292,13 @@ __device__ __forceinline__ void qk_warp(const int8_t* kpages, int warp, int lane
           kpages + (size_t)(2 * warp + m) * (D * kBS) + (mi >> 1) * (kBS * 16) + (ri + 8 * (mi & 1)) * 16;
       uint32_t a[4];
       ldmatrix_x4(a, row + (size_t)(2 * s) * (kBS * 16));
-      mma_s8a_f16b((s & 1) ? acc2[m] : acc[m], a, qf[s]);
+      mma_s8_16832((s & 1) ? ao[m] : ae[m], a, qf[s][0], qf[s][1]);
     }
   }
 #pragma unroll
   for (int m = 0; m < 2; ++m)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[m][i] += acc2[m][i];
+    for (int i = 0; i < 4; ++i) acc[m][i] = (float)(ae[m][i] + ao[m][i]);  // |sum| < 2^23: exact
 }
 
 // BF16-KV comparison path: query fragments (B operand of QK) straight from the
@@ -396,17 +392,16 @@ __device__ __forceinline__ float quant_row_warp(const RowRaw<D>& raw, uint32_t (
   return nz ? scale : 0.f;
 }
 
-// Query fragments (B operand of QK, f16 form) from int8 codes in shared memory,
+// Query fragments (B operand of the s8 QK MMA) from int8 codes in shared memory,
 // rows [8][D] (the decode step's query buffer); same layout as load_q_frags.
 template <int D>
-__device__ __forceinline__ void load_q_frags_smem(const uint8_t* qa, int G, int lane, uint32_t (&qf)[D / 32][4]) {
+__device__ __forceinline__ void load_q_frags_smem(const uint8_t* qa, int G, int lane, uint32_t (&qf)[D / 32][2]) {
   const int g = lane >> 2, t = lane & 3;
   const uint8_t* row = qa + g * D;
 #pragma unroll
   for (int s = 0; s < D / 32; ++s) {
-    const uint32_t x0 = g < G ? *reinterpret_cast<const uint32_t*>(row + 32 * s + 4 * t) : 0u;
-    const uint32_t x1 = g < G ? *reinterpret_cast<const uint32_t*>(row + 32 * s + 16 + 4 * t) : 0u;
-    s8b_to_f16(x0, x1, qf[s]);
+    qf[s][0] = g < G ? *reinterpret_cast<const uint32_t*>(row + 32 * s + 4 * t) : 0u;
+    qf[s][1] = g < G ? *reinterpret_cast<const uint32_t*>(row + 32 * s + 16 + 4 * t) : 0u;
   }
 }
 
@@ -780,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     Walk wk = w0;
     if (st == 1) walk_next(wk, p.seq_lens, B, Hkv, maxL, kGran, g_end);
     int cur_pair = -1;
-    uint32_t qf[D / 32][4];    // INT8: converted query fragments
+    uint32_t qf[D / 32][2];    // INT8: query fragments (raw s8)
     uint32_t qfb[D / 16][2];   // BF16: query fragments
     float sq[2] = {0.f, 0.f};
     RingPos kpos;  // this stream's K slots
@@ -1276,7 +1271,7 @@ __global__ void __launch_bounds__(256) debug_qk_kernel(DebugQKParams p) {
     reinterpret_cast<uint4*>(kp)[i] = val;
   }
   __syncthreads();
-  uint32_t qf[D / 32][4];
+  uint32_t qf[D / 32][2];
   load_q_frags<D>(p.q, b, p.Hq, kvh, p.G, lane, qf);
   float acc[2][4];
   qk_warp<D>(kp, warp, lane, qf, acc);
