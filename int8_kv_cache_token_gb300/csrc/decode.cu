@@ -89,7 +89,7 @@ struct Geo {
   static constexpr int MT = kWTok / 16;                         // 16-token blocks per QK warp
   static constexpr int kDimsPW = D / kPW;                       // head-dims per PV warp
   static constexpr int NDT = kDimsPW / 16;                      // 16-dim MMA tiles per PV warp
-  static constexpr int kFrag = BF16 ? 8 : 16;                   // B-fragment bytes per lane
+  static constexpr int kFrag = 8;                               // B-fragment bytes per lane (bf16 p~ or s8 codes)
   // handoff buffer: [kQW][32 lanes] B fragments, then per row r and group q
   // (QK warp): sW [8][kQW] | m [8][kQW] | l [8][kQW] (a row's 4 groups in 16 bytes)
   static constexpr int kHSw = kQW * 32 * kFrag;
@@ -954,10 +954,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         f.y = *reinterpret_cast<const uint32_t*>(stg + g * 32 + 16 + 4 * t);
         reinterpret_cast<uint2*>(hb)[qw * 32 + lane] = f;
       } else {
-        uint32_t b4[4];
-        s8b_to_f16(*reinterpret_cast<const uint32_t*>(stg + g * kGroup + 4 * t),
-                   *reinterpret_cast<const uint32_t*>(stg + g * kGroup + 16 + 4 * t), b4);
-        reinterpret_cast<uint4*>(hb)[qw * 32 + lane] = make_uint4(b4[0], b4[1], b4[2], b4[3]);
+        // the s8 B fragment of PV: codes of row g, tokens 4t..4t+3 and 16+4t..16+4t+3
+        reinterpret_cast<uint2*>(hb)[qw * 32 + lane] =
+            make_uint2(*reinterpret_cast<const uint32_t*>(stg + g * kGroup + 4 * t),
+                       *reinterpret_cast<const uint32_t*>(stg + g * kGroup + 16 + 4 * t));
       }
       // the group's row sums of p~ (relative to m_g)
 #pragma unroll
@@ -1084,21 +1084,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
           o[dt][3] = fmaf(pv[3], fs[q][1], o[dt][3]);
         }
       } else {
-        // A = V^T of the group's pages 2q, 2q+1: (dims 0-7 | 8-15) x (page 2q | 2q+1)
-        const uint4 f = reinterpret_cast<const uint4*>(hb)[q * 32 + lane];
-        const uint32_t bq[4] = {f.x, f.y, f.z, f.w};
+        // PV on the INT8 tensor path (mma.sync m16n8k32, s8 x s8 -> s32: exact).
+        // A = V^T of the group's pages 2q, 2q+1: ldmatrix of (dims 0-7 | 8-15) x
+        // (page 2q | 2q+1) is the s8 A fragment (16 dims x 32 tokens) as it is.
+        const uint2 f = reinterpret_cast<const uint2*>(hb)[q * 32 + lane];
         const uint8_t* vrow = vb + (size_t)(2 * q + (mi >> 1)) * kPage + (size_t)(pv_w * Gm::kDimsPW) * 16 +
                               (ri + 8 * (mi & 1)) * 16;
 #pragma unroll
         for (int dt = 0; dt < NDT; ++dt) {
           uint32_t a[4];
           ldmatrix_x4(a, vrow + dt * 16 * 16);
-          float pv[4] = {0.f, 0.f, 0.f, 0.f};
-          mma_s8a_f16b(pv, a, bq);
-          o[dt][0] = fmaf(pv[0], fs[q][0], o[dt][0]);
-          o[dt][1] = fmaf(pv[1], fs[q][1], o[dt][1]);
-          o[dt][2] = fmaf(pv[2], fs[q][0], o[dt][2]);
-          o[dt][3] = fmaf(pv[3], fs[q][1], o[dt][3]);
+          int pv[4] = {0, 0, 0, 0};
+          mma_s8_16832(pv, a, f.x, f.y);
+          o[dt][0] = fmaf((float)pv[0], fs[q][0], o[dt][0]);  // |pv| <= 32 * 127^2: exact in fp32
+          o[dt][1] = fmaf((float)pv[1], fs[q][1], o[dt][1]);
+          o[dt][2] = fmaf((float)pv[2], fs[q][0], o[dt][2]);
+          o[dt][3] = fmaf((float)pv[3], fs[q][1], o[dt][3]);
         }
       }
     }
