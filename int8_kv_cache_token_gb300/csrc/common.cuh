@@ -374,6 +374,16 @@ __device__ __forceinline__ void div_row(float (&x)[N], float s, float y) {
   }
 }
 
+// 2^x by the hardware approximation (ex2.approx: relative error about 2^-22;
+// -inf gives 0).  The kernels keep softmax scores in log2 units (their scale
+// folds in log2 e), so every exponential of the softmax is one ex2.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
 // round-half-even(x) for |x| < 2^21, as the low bits of the fp32 sum
 // x + 1.5 * 2^23 (whose unit in the last place is 1): the low byte is the
 // integer's two's-complement byte.

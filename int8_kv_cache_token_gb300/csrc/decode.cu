@@ -619,15 +619,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       if (lane >= nb) return -1;
       return p.block_tables[(size_t)u.b * p.max_blocks + t0 / kBS + lane];
     };
-    Walk wk = w0, wn = w0;
+    // The block-table entries of the next two units are in flight while a unit is
+    // issued (one unit ahead left the producer waiting on the load whenever a
+    // unit's slots freed up sooner than the load returned).
+    Walk wk = w0, wn = w0, wnn;
     walk_next(wn, p.seq_lens, B, Hkv, maxL, kGran, g_end);
+    wnn = wn;
+    if (wnn.n > 0) walk_next(wnn, p.seq_lens, B, Hkv, maxL, kGran, g_end);
     int blk_cur = blk_first;
+    int blk_n = wn.n > 0 ? load_blk(wn) : -1;
     int n_k = 0, n_v = 0;  // K and V items issued
     RingPos kp_cur, kp_oth, vp;  // K positions of this unit's stream and of the other; V position
     uint32_t nt_k[D / 128], nt_v[D / 128];  // decode step: the new token's codes
     for (int i = 0; wk.n > 0; ++i) {
       if (*abort_flag) break;
-      const int blk_nx = wn.n > 0 ? load_blk(wn) : -1;  // in flight meanwhile
+      const int blk_nn = wnn.n > 0 ? load_blk(wnn) : -1;  // in flight meanwhile
       const int t0 = wk.gi * kGran;
       const int ntok = min(wk.n * kGran, wk.L - t0);
       const int nblk = (ntok + kBS - 1) / kBS;
@@ -734,9 +740,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       mbar_arrive(&full[vslot]);
       ++n_v;
       vp.next(rg.nV);
-      blk_cur = blk_nx;
+      blk_cur = blk_n;
+      blk_n = blk_nn;
       wk = wn;
-      walk_next(wn, p.seq_lens, B, Hkv, maxL, kGran, g_end);
+      wn = wnn;
+      if (wnn.n > 0) walk_next(wnn, p.seq_lens, B, Hkv, maxL, kGran, g_end);
     }
     if (*abort_flag) {
       // The consumers stopped waiting: hold the CTA (and its shared memory)
@@ -769,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     // every group to the common running maximum later, by exp(m_g - m) folded
     // into sW; no QK warp waits for another.
     const int st = warp / kQW, qw = warp % kQW;  // stream; group within the unit
-    const float c_scale = p.sm_scale;
+    const float c_scale = __fmul_rn(p.sm_scale, kLog2e);  // scores in log2 units: every exponential is one ex2
     const int tok0 = qw * kWTok;  // this warp's tokens within a unit
     uint8_t* stg = stage + warp * Gm::kStage;
     Walk wk = w0;
@@ -903,7 +911,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         uint16_t* pw = reinterpret_cast<uint16_t*>(stg);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float pe = active ? expf(__fsub_rn(s[0][e], gm[e & 1])) : 0.f;
+          const float pe = active ? ex2(__fsub_rn(s[0][e], gm[e & 1])) : 0.f;
           lg[e & 1] += pe;
           pw[(2 * t + (e & 1)) * 16 + g + 8 * (e >> 1)] = __bfloat16_as_ushort(__float2bfloat16_rn(pe));
         }
@@ -913,7 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         for (int m = 0; m < 2; ++m)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float pe = active ? expf(__fsub_rn(s[m][e], gm[e & 1])) : 0.f;
+            const float pe = active ? ex2(__fsub_rn(s[m][e], gm[e & 1])) : 0.f;
             lg[e & 1] += pe;
             w[m][e] = __fmul_rn(pe, sv[2 * m + (e >> 1)]);
             A[e & 1] = fmaxf(A[e & 1], w[m][e]);
@@ -1028,11 +1036,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       const float mg[4] = {m4.x, m4.y, m4.z, m4.w}, lgv[4] = {l4.x, l4.y, l4.z, l4.w},
                   sg[4] = {s4.x, s4.y, s4.z, s4.w};
       const float mn = fmaxf(fmaxf(mrun[r], fmaxf(mg[0], mg[1])), fmaxf(mg[2], mg[3]));
-      const float alpha = (mrun[r] == -INFINITY) ? 0.f : expf(mrun[r] - mn);
+      const float alpha = (mrun[r] == -INFINITY) ? 0.f : ex2(mrun[r] - mn);
       float l = lrun[r] * alpha;
 #pragma unroll
       for (int q = 0; q < kQW; ++q) {
-        const float f = (mg[q] == -INFINITY) ? 0.f : expf(mg[q] - mn);
+        const float f = (mg[q] == -INFINITY) ? 0.f : ex2(mg[q] - mn);
         l = fmaf(lgv[q], f, l);
         fs[q][r] = BF16 ? f : f * sg[q];
       }
@@ -1199,7 +1207,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
 #pragma unroll
     for (int j = 0; j < kMB; ++j) mb = fmaxf(mb, ms[j]);
     if (mb == -INFINITY) continue;
-    const float f = expf(m - mb);
+    const float f = ex2(m - mb);  // the partials' maxima are in log2 units
     a.x *= f;
     a.y *= f;
     a.z *= f;
@@ -1207,7 +1215,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
     den *= f;
 #pragma unroll
     for (int j = 0; j < kMB; ++j) {
-      const float e = expf(ms[j] - mb);  // 0 for the padding entries
+      const float e = ex2(ms[j] - mb);  // 0 for the padding entries
       a.x = fmaf(v[j].x, e, a.x);
       a.y = fmaf(v[j].y, e, a.y);
       a.z = fmaf(v[j].z, e, a.z);
@@ -1230,7 +1238,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
     float dd = 0.f;
 #pragma unroll
     for (int k = 0; k < SL; ++k) {
-      const float w = expf(msh[k] - M);  // 0 for a slice without segments
+      const float w = ex2(msh[k] - M);  // 0 for a slice without segments
       r.x = fmaf(red[k][tid].x, w, r.x);
       r.y = fmaf(red[k][tid].y, w, r.y);
       r.z = fmaf(red[k][tid].z, w, r.z);

@@ -62,7 +62,6 @@ constexpr int kLoadWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kCompWarp0 = 4;    // warps 4..11
 constexpr int kWGThreads = 128;
-constexpr float kLog2e = 1.4426950408889634f;
 
 // One (KV head, group) operand tile, in global memory and in shared memory.
 template <int D>
@@ -109,12 +108,6 @@ __device__ __forceinline__ void s8x16_to_f16(const uint4& v, uint4& h0, uint4& h
   s8x4_to_f16(v.y, h0.z, h0.w);
   s8x4_to_f16(v.z, h1.x, h1.y);
   s8x4_to_f16(v.w, h1.z, h1.w);
-}
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 
 // Maximum and sum of 32 values as balanced trees (depth 5 instead of a
