@@ -145,8 +145,7 @@ i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const fl
 /* returns I8KV_ERR_WORKSPACE and launches nothing.                          */
 /* The first call on a device looks up the scratch's device address (with   */
 /* that device current), so make the first call on each device before any   */
-/* stream capture.  Each call clears the scratch's ticket counters on        */
-/* `stream` before the kernel.  All calls share the one scratch area: calls  */
+/* stream capture.  All calls share the one scratch area: calls            */
 /* that overlap on the GPU (other streams, other host threads) race and give */
 /* wrong results -- serialize them, e.g. on one stream.                      */
 /* ------------------------------------------------------------------------ */

@@ -136,7 +136,6 @@ static i8kv_status decode_common(i8kv::DecodeParams& p, const void* q, const flo
   REQUIRE(workspace != nullptr && workspace_bytes >= need, I8KV_ERR_WORKSPACE,
           "workspace of %zu bytes given, %zu needed", workspace_bytes, need);
   REQUIRE(aligned16(workspace), I8KV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-  const size_t slots = (size_t)B * Hkv + grid;
   float* ws = static_cast<float*>(workspace);
   p.out = out;
   p.q = q;
@@ -156,7 +155,6 @@ static i8kv_status decode_common(i8kv::DecodeParams& p, const void* q, const flo
   p.num_blocks = num_blocks;
   p.sm_scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
   p.ws_part = ws;
-  p.ws_info = reinterpret_cast<int*>(ws + slots * (8 * (size_t)D + 16));
   p.grid = grid;
   return I8KV_OK;
 }
@@ -225,10 +223,6 @@ i8kv_status i8kv_int8_paged_decode_attn_noalloc(float* out, const int8_t* q_i8, 
   s = decode_common(p, q_i8, q_scale, true, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, B, Hq, Hkv,
                     D, block_size, max_blocks, num_blocks, softmax_scale, partition, scratch, need, out);
   if (s != I8KV_OK || B == 0) return s;
-  // The per-pair merge records are rewritten by every call before they are read;
-  // clearing them anyway keeps a call independent of what the last one left.
-  e = cudaMemsetAsync(p.ws_info, 0xff, (size_t)B * Hkv * sizeof(int), static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return from_cuda(e, "noalloc decode: clear merge records");
   return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "noalloc int8 decode launch");
 }
 

@@ -588,7 +588,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         if (clamp_len(raw, maxL) == 0 && b % N == c) {
           float* o = p.out + (size_t)b * Hq * D;
           for (int i = 0; i < Hq * D; ++i) o[i] = 0.f;
-          for (int hh = 0; hh < Hkv; ++hh) p.ws_info[b * Hkv + hh] = -1;
         }
       }
     }
@@ -1118,8 +1117,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     if (seg_end) {
       const long long Up = wk.gb + (long long)wk.kvh * wk.ngp;  // the pair's first granule
       const int cf = cta_of(Up, U, Nw), cl = cta_of(Up + wk.ngp - 1, U, Nw);
-      // the CTA holding the pair's first unit records whether a merge is needed
-      if (c == cf && pv_w == 0 && lane == 0) p.ws_info[pair] = (cf == cl) ? -1 : ((cf << 16) | cl);
       const int d0 = pv_w * Gm::kDimsPW;
       if (cf == cl) {
         float* dst = p.out + ((size_t)wk.b * Hq + wk.kvh * G) * D;
@@ -1162,22 +1159,64 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
 // segment of one float4 column.  It loads a batch of kMB segments (value, m, l)
 // at once -- independent loads, all in flight together -- then folds them into
 // its running (max, denominator, sum); the slices are combined in a fixed order.
+//
+// Which CTAs hold the pair's partials follows from the attention kernel's work
+// split, so warp 0 recomputes it from seq_lens (the same arithmetic) before the
+// grid-dependency wait, while the attention kernel still runs; after the wait
+// the partials' loads go out at once.
 constexpr int kMaxSeg = 1024;
 constexpr int kMergeThreads = 512;
 constexpr int kMB = 8;
 
-template <int D>
+template <int D, bool BF16>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
   constexpr int COLS = D / 4, SL = kMergeThreads / COLS;
+  constexpr int kGran = Geo<D, BF16>::kGran;
   __shared__ float4 red[SL][COLS];
   __shared__ float msh[SL], dsh[SL];
-  griddep_wait();
-  griddep_launch_dependents();
+  __shared__ int s_seg[2];
   const int tid = threadIdx.x;
   const int pair = blockIdx.x / p.G, row = blockIdx.x % p.G;
-  const int info = p.ws_info[pair];
-  if (info < 0) return;
-  const int cf = info >> 16, cl = info & 0xffff, nseg = cl - cf + 1;
+  if (tid < 32) {
+    const int lane = tid, Hkv = p.Hkv, maxL = p.max_blocks * kBS;
+    const int bp = pair / Hkv, kvh = pair % Hkv;
+    long long total = 0, before = 0;  // granules of all sequences; of the sequences before bp
+    int Lp = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int b = b0 + lane;
+      int u = 0, L = 0;
+      if (b < p.B) {
+        L = clamp_len(__ldcg(p.seq_lens + b), maxL);
+        u = (L + kGran - 1) / kGran * Hkv;
+      }
+      int su = u, sb = b < bp ? u : 0, lp = b == bp ? L : 0;
+      for (int o = 16; o >= 1; o >>= 1) {
+        su += __shfl_xor_sync(0xffffffffu, su, o);
+        sb += __shfl_xor_sync(0xffffffffu, sb, o);
+        lp += __shfl_xor_sync(0xffffffffu, lp, o);
+      }
+      total += su;
+      before += sb;
+      Lp += lp;
+    }
+    if (lane == 0) {
+      const int ngp = (Lp + kGran - 1) / kGran;
+      int cf = -1, cl = -1;
+      if (ngp > 0) {  // an empty sequence has zero rows and no partials
+        const long long U = total, Up = before + (long long)kvh * ngp;
+        const int Nw = (int)(U < p.grid ? U : p.grid);
+        cf = cta_of(Up, U, Nw);
+        cl = cta_of(Up + ngp - 1, U, Nw);
+      }
+      s_seg[0] = cf;
+      s_seg[1] = cl;
+    }
+  }
+  __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();
+  const int cf = s_seg[0], cl = s_seg[1], nseg = cl - cf + 1;
+  if (cf == cl) return;  // no partials: the attention kernel wrote the rows (or the sequence is empty)
   if (nseg > kMaxSeg) {
     record_error(2);
     return;
@@ -1347,7 +1386,7 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   }
   cudaError_t e = launch_pdl(decode_kernel<D, BF16, STEP>, dim3(p.grid), dim3(kThreads), smem, stream, p, ns);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_merge_kernel<D>, dim3(p.B * p.Hkv * p.G), dim3(kMergeThreads), 0, stream, p);
+  return launch_pdl(decode_merge_kernel<D, BF16>, dim3(p.B * p.Hkv * p.G), dim3(kMergeThreads), 0, stream, p);
 }
 
 }  // namespace
@@ -1363,7 +1402,7 @@ int decode_grid(int device, int B, int Hkv, int max_blocks) {
 
 size_t decode_workspace_bytes(int B, int Hkv, int D, int grid) {
   const size_t slots = (size_t)B * Hkv + (size_t)grid;
-  size_t bytes = slots * kSlotFloats(D) * sizeof(float) + (size_t)B * Hkv * sizeof(int);
+  size_t bytes = slots * kSlotFloats(D) * sizeof(float);
   return (bytes + 255) / 256 * 256;
 }
 

@@ -37,7 +37,6 @@ struct DecodeParams {
   int B, Hq, Hkv, G, D, max_blocks, num_blocks;
   float sm_scale;
   float* ws_part;             // [(B*Hkv + grid) slots][8 rows * D + 16]
-  int* ws_info;               // [B*Hkv] per pair: -1 (no merge) or first CTA << 16 | last CTA
   int grid;                   // CTAs launched (the work split depends on it)
   // Decode step (INT8 path, step != 0): the newest token of each sequence
   // (position seq_lens[b] - 1) arrives as bf16 and is quantized inside the
