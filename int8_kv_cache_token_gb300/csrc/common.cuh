@@ -358,21 +358,29 @@ __device__ __forceinline__ float div_markstein(float x, float s, float y) {
 constexpr float kTinyDivisor = 7.8886091e-31f;  // 2^-100
 
 // x[i] / s, correctly rounded, for the N values of one row sharing the divisor
-// s > 0: Markstein's step when s >= 2^-100, the plain division below.  The test
-// on s is made once for the row, so the N quotients are independent chains of
-// three FMA-pipe operations (a test inside each quotient would split them into
-// N serial blocks).  y = RN(1/s) is computed by the caller when it serves
-// several rows' calls.
+// s > 0, by Markstein's step.  Below 2^-100 both operands are first scaled by
+// 2^100 (exact: x <= 127.5 s < 2^-93 cannot overflow, a subnormal keeps its
+// bits, and the quotient does not change), which keeps every intermediate of
+// the step in the normal range; so no IEEE division routine is inlined at any
+// call site (those made the kernels' code far larger than their hot loops).
+// The test on s is made once for the row, and the N quotients are independent
+// chains of FMA-pipe operations.  y = RN(1/s) is passed in when the caller has
+// it; for s below 2^-100 it is recomputed for the scaled divisor.
 template <int N>
 __device__ __forceinline__ void div_row(float (&x)[N], float s, float y) {
   if (s < kTinyDivisor) {
+    const float s2 = __fmul_rn(s, 0x1p100f), y2 = __frcp_rn(s2);
 #pragma unroll
-    for (int i = 0; i < N; ++i) x[i] = __fdiv_rn(x[i], s);
+    for (int i = 0; i < N; ++i) x[i] = div_markstein(__fmul_rn(x[i], 0x1p100f), s2, y2);
   } else {
 #pragma unroll
     for (int i = 0; i < N; ++i) x[i] = div_markstein(x[i], s, y);
   }
 }
+
+// a / 127 correctly rounded below 2^-100 (the rare tiny-absmax case of div127),
+// kept out of line so its division routine is compiled once per kernel.
+static __device__ __noinline__ float div127_tiny(float a) { return __fdiv_rn(a, 127.0f); }
 
 // 2^x by the hardware approximation (ex2.approx: relative error about 2^-22;
 // -inf gives 0).  The kernels keep softmax scores in log2 units (their scale
@@ -394,7 +402,7 @@ __device__ __forceinline__ uint32_t rne_bits(float x) { return __float_as_uint(_
 // two lowest normal binades and in the top binade (the rounding pattern
 // repeats in every binade); inputs below 2^-100 use the plain division.
 __device__ __forceinline__ float div127(float a) {
-  if (a < kTinyDivisor) return __fdiv_rn(a, 127.0f);
+  if (a < kTinyDivisor) return div127_tiny(a);
   const float y = 0.0078740157f;  // RN(1/127)
   const float q = __fmul_rn(a, y);
   const float r = __fmaf_rn(-127.0f, q, a);

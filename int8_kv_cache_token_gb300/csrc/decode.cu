@@ -384,7 +384,7 @@ __device__ __forceinline__ float quant_row_warp(const RowRaw<D>& raw, uint32_t (
   }
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const float scale = __fdiv_rn(amax, 127.0f);
+  const float scale = div127(amax);  // amax / 127, correctly rounded
   const float y = __frcp_rn(scale);
   const bool nz = amax > 0.f;
 #pragma unroll

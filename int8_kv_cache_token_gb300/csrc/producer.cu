@@ -44,7 +44,7 @@ __device__ __forceinline__ float quantize_slice(const uint4 (&raw)[2], bool acti
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
 #pragma unroll
   for (int o = LPV / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float scale = __fdiv_rn(amax, 127.0f);
+  const float scale = div127(amax);  // amax / 127, correctly rounded
   // Codes: round half to even by adding 1.5 * 2^23 (the fp32 sum keeps the
   // integer part of x / scale in its low mantissa bits, so its low byte is the
   // two's-complement code).  |x / scale| <= amax / RN(amax / 127) < 127.5, so no
