@@ -84,10 +84,10 @@ static inline size_t s_index(int blk, int h, int off, int Hkv, int bs) {
 /*   amax = max|x|, scale = amax/127, q = clamp(round(x/scale), -127, 127).   */
 /* The producer's arithmetic is fp32 (bit-exact target), whatever the mode.  */
 /* ------------------------------------------------------------------------- */
-void orc_quantize_vector(const uint16_t* x, int n, int8_t* q, float* scale) {
+static void quantize_f32(const float* x, int n, int8_t* q, float* scale) {
   double amax = 0.0;
   for (int i = 0; i < n; ++i) {
-    double a = fabs((double)bf16_to_f32(x[i]));
+    double a = fabs((double)x[i]);
     if (a > amax) amax = a;
   }
   if (amax == 0.0) {
@@ -98,11 +98,18 @@ void orc_quantize_vector(const uint16_t* x, int n, int8_t* q, float* scale) {
   double s = R(amax / 127.0, 1);
   *scale = (float)s;
   for (int i = 0; i < n; ++i) {
-    double r = rne(R((double)bf16_to_f32(x[i]) / s, 1));
+    double r = rne(R((double)x[i] / s, 1));
     if (r > 127.0) r = 127.0;
     if (r < -127.0) r = -127.0;
     q[i] = (int8_t)r;
   }
+}
+
+void orc_quantize_vector(const uint16_t* x, int n, int8_t* q, float* scale) {
+  float* f = (float*)malloc((size_t)n * sizeof(float));
+  for (int i = 0; i < n; ++i) f[i] = bf16_to_f32(x[i]);
+  quantize_f32(f, n, q, scale);
+  free(f);
 }
 
 /* KV producer ([KV] §2.2 steps 3-6, without RoPE): quantize K and V of every
@@ -136,6 +143,133 @@ int orc_kv_quant_write(const uint16_t* k, const uint16_t* v, const int32_t* slot
   }
   free(tmp);
   return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Fused producer with Q/K RMSNorm and RoPE.  [KV] §2.2 lists RoPE on Q and K  */
+/* as the producer's second step, before the absmax, scale and quantization;  */
+/* [KV] §5.3 notes that the served model applies a per-head RMSNorm to Q and  */
+/* K before RoPE.  The pages give neither formula, so the plain readings:     */
+/*   RMSNorm   y_i = (x_i * (1 / sqrt(mean_j x_j^2 + eps))) * w_i             */
+/*   RoPE      rotate-half on the first rd dims with h = rd/2 and a table     */
+/*             row cs = cos_sin[position] = (cos_0..cos_{h-1}, sin_0..sin_{h-1}):*/
+/*             y_i = a c_i - b s_i,  y_{i+h} = b c_i + a s_i,  a = x_i, b = x_{i+h}*/
+/*   then the quantization rule of [KV] §2.1 on the fp32 result.              */
+/* Every step is one correctly rounded fp32 operation in the order written    */
+/* (the file is built without FP contraction): the sum of squares is a        */
+/* balanced binary tree in index order, mean = sum * (1/D) (exact, D a power  */
+/* of two), then sqrt, the reciprocal, and the two products.  No bf16         */
+/* rounding happens between the steps; the optional bf16 copies (q_out,       */
+/* k_out) are the fp32 result rounded to nearest even.                        */
+/* ------------------------------------------------------------------------- */
+#define ORC_BAD_POSITION 2
+
+/* Sum of x_i^2 over n = 2^k elements: each half summed the same way, then added. */
+static float sum_sq_tree(const float* x, int n) {
+  if (n == 1) return x[0] * x[0];
+  float lo = sum_sq_tree(x, n / 2);
+  float hi = sum_sq_tree(x + n / 2, n / 2);
+  return lo + hi;
+}
+
+static void rms_norm_f32(float* x, int D, const uint16_t* w, float eps) {
+  float ss = sum_sq_tree(x, D);
+  float mean = ss * (1.0f / (float)D);
+  float var = mean + eps;
+  float rms = sqrtf(var);
+  float inv = 1.0f / rms;
+  for (int i = 0; i < D; ++i) {
+    float t = x[i] * inv;
+    x[i] = t * bf16_to_f32(w[i]);
+  }
+}
+
+static void rope_rotate_half(float* x, int rd, const float* cs) {
+  int h = rd / 2;
+  for (int i = 0; i < h; ++i) {
+    float c = cs[i], s = cs[h + i];
+    float a = x[i], b = x[i + h];
+    float ac = a * c, bsn = b * s, bc = b * c, asn = a * s;
+    x[i] = ac - bsn;
+    x[i + h] = bc + asn;
+  }
+}
+
+/* fp32 -> bf16 bits, round to nearest even (finite values). */
+static uint16_t f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+static int is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
+
+/* One Q or K head vector: bf16 -> fp32, optional RMSNorm, optional RoPE. */
+static void qk_transform(const uint16_t* src, int D, const uint16_t* norm_w, float eps, const float* cs, int rd,
+                         float* x) {
+  for (int i = 0; i < D; ++i) x[i] = bf16_to_f32(src[i]);
+  if (norm_w) rms_norm_f32(x, D, norm_w, eps);
+  if (rd > 0) rope_rotate_half(x, rd, cs);
+}
+
+/* The fused producer.  positions [T] and cos_sin [max_position, rd] fp32 are
+ * needed when rd > 0 (rd even, <= D); rd = 0 rotates nothing.  A null norm
+ * weight skips that RMSNorm.  K/V go to the cache for slot >= 0 exactly as in
+ * orc_kv_quant_write; q (nullable) is transformed and, when q_i8 is given,
+ * quantized into q_i8 / q_scale.  q_out / k_out (nullable) receive the
+ * transformed Q / K in bf16 for every token, whatever its slot.  A token whose
+ * position lies outside [0, max_position) is skipped entirely (nothing of it
+ * is written) and the call returns ORC_BAD_POSITION after the other tokens. */
+int orc_kv_rope_quant_write(const uint16_t* k, const uint16_t* v, const int32_t* slot_mapping, int T, int Hkv, int D,
+                            int bs, int8_t* k_cache, int8_t* v_cache, float* k_scale, float* v_scale,
+                            const uint16_t* q, int Hq, int8_t* q_i8, float* q_scale, const int32_t* positions,
+                            const float* cos_sin, int max_position, int rd, const uint16_t* q_norm_w,
+                            const uint16_t* k_norm_w, float eps, uint16_t* q_out, uint16_t* k_out) {
+  if (D % 16 != 0 || bs <= 0 || Hkv <= 0 || rd < 0 || rd % 2 != 0 || rd > D) return ORC_BAD_ARG;
+  if ((q_norm_w || k_norm_w) && !is_pow2(D)) return ORC_BAD_ARG;
+  if (rd > 0 && (positions == NULL || cos_sin == NULL || max_position <= 0)) return ORC_BAD_ARG;
+  int bad = 0;
+  float* x = (float*)malloc((size_t)D * sizeof(float));
+  int8_t* tmp = (int8_t*)malloc((size_t)D);
+  for (int t = 0; t < T; ++t) {
+    const float* cs = NULL;
+    if (rd > 0) {
+      int p = positions[t];
+      if (p < 0 || p >= max_position) {
+        bad = 1;
+        continue;
+      }
+      cs = cos_sin + (size_t)p * rd;
+    }
+    int slot = slot_mapping[t];
+    int blk = slot >= 0 ? slot / bs : 0, off = slot >= 0 ? slot % bs : 0;
+    for (int h = 0; h < Hkv; ++h) {
+      size_t row = ((size_t)t * Hkv + h) * D;
+      float s;
+      qk_transform(k + row, D, k_norm_w, eps, cs, rd, x);
+      if (k_out)
+        for (int d = 0; d < D; ++d) k_out[row + d] = f32_to_bf16(x[d]);
+      if (slot < 0) continue;
+      quantize_f32(x, D, tmp, &s);
+      for (int d = 0; d < D; ++d) k_cache[k_index(blk, h, d, off, Hkv, D, bs)] = tmp[d];
+      k_scale[s_index(blk, h, off, Hkv, bs)] = s;
+      orc_quantize_vector(v + row, D, tmp, &s);
+      for (int d = 0; d < D; ++d) v_cache[v_index(blk, h, d, off, Hkv, D, bs)] = tmp[d];
+      v_scale[s_index(blk, h, off, Hkv, bs)] = s;
+    }
+    if (q == NULL) continue;
+    for (int h = 0; h < Hq; ++h) {
+      size_t row = ((size_t)t * Hq + h) * D;
+      qk_transform(q + row, D, q_norm_w, eps, cs, rd, x);
+      if (q_out)
+        for (int d = 0; d < D; ++d) q_out[row + d] = f32_to_bf16(x[d]);
+      if (q_i8) quantize_f32(x, D, q_i8 + row, q_scale + (size_t)t * Hq + h);
+    }
+  }
+  free(tmp);
+  free(x);
+  return bad ? ORC_BAD_POSITION : ORC_OK;
 }
 
 /* ------------------------------------------------------------------------- */

@@ -66,6 +66,8 @@ def _load():
             lib.orc_quantize_vector.argtypes = [P, I, P, P]
             lib.orc_quantize_vector.restype = None
             lib.orc_kv_quant_write.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, I, P, P]
+            lib.orc_kv_rope_quant_write.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, I, P, P, P, P, I, I, P, P,
+                                                    ctypes.c_float, P, P]
             lib.orc_qk_i32.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I]
             lib.orc_decode_attn.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float,
                                             I, I, I, I, I, I, P, P, P, P]
@@ -73,7 +75,7 @@ def _load():
                                             P, I, I, I]
             lib.orc_bf16_kv_write.argtypes = [P, P, P, I, I, I, I, P, P]
             lib.orc_bf16_decode_attn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_double, I]
-            for name in ("orc_kv_quant_write", "orc_qk_i32", "orc_decode_attn", "orc_prefix_attn",
+            for name in ("orc_kv_quant_write", "orc_kv_rope_quant_write", "orc_qk_i32", "orc_decode_attn", "orc_prefix_attn",
                          "orc_bf16_kv_write", "orc_bf16_decode_attn", "orc_max_threads"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
@@ -141,6 +143,60 @@ def kv_quant_write(k, v, slot_mapping, num_blocks, block_size, q=None, k_cache=N
     rc = _load().orc_kv_quant_write(_p(k), _p(v), _p(slots), T, Hkv, D, bs, _p(k_cache), _p(v_cache),
                                     _p(k_scale), _p(v_scale), _p(q), Hq, _p(q_i8), _p(q_scale))
     _check(rc, "kv_quant_write")
+    return out
+
+
+BAD_POSITION = 2   # orc_kv_rope_quant_write: some token's position was outside the table
+
+
+def kv_rope_quant_write(k, v, slot_mapping, num_blocks, block_size, positions=None, cos_sin=None, rotary_dim=0,
+                        q=None, q_norm_weight=None, k_norm_weight=None, eps=1e-6, quantize_q=True,
+                        q_out=False, k_out=False):
+    """Fused producer: optional Q/K RMSNorm, RoPE (rotate-half on the first
+    ``rotary_dim`` dims, table ``cos_sin`` float32 [max_position, rotary_dim]),
+    then the [KV] §2.1 quantization and the paged scatter of kv_quant_write.
+
+    Returns the kv_quant_write dict plus ``q_out`` / ``k_out`` (bf16 bits of the
+    transformed Q / K) when asked, and ``status`` (0, or BAD_POSITION when some
+    token was skipped because its position lay outside the table)."""
+    k, v = _u16(k), _u16(v)
+    T, Hkv, D = k.shape
+    bs = block_size
+    out = dict(k_cache=np.zeros((num_blocks, Hkv, D // 16, bs, 16), np.int8),
+               v_cache=np.zeros((num_blocks, Hkv, D, bs), np.int8),
+               k_scale=np.zeros((num_blocks, bs, Hkv), np.float32),
+               v_scale=np.zeros((num_blocks, bs, Hkv), np.float32))
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int32)
+    pos = None if positions is None else np.ascontiguousarray(positions, dtype=np.int32)
+    cs = None if cos_sin is None else np.ascontiguousarray(cos_sin, dtype=np.float32)
+    max_pos = 0 if cs is None else cs.shape[0]
+    if cs is not None:
+        assert cs.shape[1] == rotary_dim, "cos_sin rows must hold rotary_dim values"
+    Hq = 0
+    q_i8 = q_scale = qo = None
+    if q is not None:
+        q = _u16(q)
+        Hq = q.shape[1]
+        if quantize_q:
+            q_i8 = np.zeros(q.shape, np.int8)
+            q_scale = np.zeros(q.shape[:2], np.float32)
+            out.update(q_i8=q_i8, q_scale=q_scale)
+        if q_out:
+            qo = np.zeros(q.shape, np.uint16)
+            out["q_out"] = qo
+    ko = None
+    if k_out:
+        ko = np.zeros(k.shape, np.uint16)
+        out["k_out"] = ko
+    qw = None if q_norm_weight is None else _u16(q_norm_weight)
+    kw = None if k_norm_weight is None else _u16(k_norm_weight)
+    rc = _load().orc_kv_rope_quant_write(_p(k), _p(v), _p(slots), T, Hkv, D, bs, _p(out["k_cache"]),
+                                         _p(out["v_cache"]), _p(out["k_scale"]), _p(out["v_scale"]), _p(q), Hq,
+                                         _p(q_i8), _p(q_scale), _p(pos), _p(cs), max_pos, rotary_dim, _p(qw),
+                                         _p(kw), float(eps), _p(qo), _p(ko))
+    if rc not in (0, BAD_POSITION):
+        _check(rc, "kv_rope_quant_write")
+    out["status"] = rc
     return out
 
 

@@ -42,6 +42,19 @@ MUTANTS = {
     # int32 QK accumulation truncated to 16 bits
     "qk_acc_int16": ("acc += (int32_t)qv[d] * (int32_t)k_cache[k_index(blk, kvh, d, off, Hkv, D, bs)];",
                      "acc = (int16_t)(acc + (int32_t)qv[d] * (int32_t)k_cache[k_index(blk, kvh, d, off, Hkv, D, bs)]);"),
+    # RoPE: sign of the sine term, cos/sin halves of the table row swapped
+    "rope_sign": ("    x[i] = ac - bsn;\n", "    x[i] = ac + bsn;\n"),
+    "rope_table_swap": ("float c = cs[i], s = cs[h + i];", "float c = cs[h + i], s = cs[i];"),
+    # RMSNorm: sum instead of mean, eps dropped, weight reversed, the query
+    # normalized with the key's weight, a left-to-right sum of squares
+    "rms_no_mean": ("float mean = ss * (1.0f / (float)D);", "float mean = ss;"),
+    "rms_no_eps": ("float var = mean + eps;", "float var = mean;"),
+    "rms_weight_reversed": ("x[i] = t * bf16_to_f32(w[i]);", "x[i] = t * bf16_to_f32(w[D - 1 - i]);"),
+    "q_norm_with_k_weight": ("qk_transform(q + row, D, q_norm_w, eps, cs, rd, x);",
+                             "qk_transform(q + row, D, k_norm_w, eps, cs, rd, x);"),
+    "rms_sequential_sum": ("  if (n == 1) return x[0] * x[0];\n",
+                           "  if (n > 1) {\n    float acc = 0.0f;\n    for (int i = 0; i < n; ++i) acc += x[i] * x[i];\n"
+                           "    return acc;\n  }\n  if (n == 1) return x[0] * x[0];\n"),
 }
 
 
@@ -57,6 +70,6 @@ def test_pins_catch_mutant(name, tmp_path):
                     str(mut), "-lm"], check=True)
     env = dict(os.environ, I8KV_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        "tests/test_oracle_quant.py", "tests/test_oracle_attention.py"],
+                        "tests/test_oracle_quant.py", "tests/test_oracle_rope.py", "tests/test_oracle_attention.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

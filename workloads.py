@@ -20,6 +20,9 @@ heads, head_dim 256, block size 16):
 * ``decode_batch``   64 sequences, lengths uniform in [1024, 32768].
 * ``producer_gqa``   8192 new tokens, 8 KV heads, head_dim 128, N(0,1) with 2%
   of elements x10; then batch-16 decode at 32768 with 32 / 8 heads.
+* ``producer_rope_tokens``  the same tokens with their positions, a RoPE
+  cos/sin table and per-head Q/K RMSNorm weights (model constants, drawn or
+  tabulated here like any other input).
 """
 from __future__ import annotations
 
@@ -220,3 +223,30 @@ def producer_tokens(T: int = 8192, Hq: int = 32, Hkv: int = 8, D: int = 128, see
     tables, num_blocks = paged_tables([T], BLOCK_SIZE, perm_seed=5)
     slots = slot_mapping(tables[0], np.arange(T))
     return dict(q=q, k=k, v=v, slots=slots, num_blocks=num_blocks, Hq=Hq, Hkv=Hkv, D=D)
+
+
+def rope_cos_sin(max_position: int, rotary_dim: int, base: float = 10000.0) -> np.ndarray:
+    """RoPE table float32 [max_position, rotary_dim]: row p holds cos(p f_i) for
+    i < rotary_dim/2, then sin(p f_i), with f_i = base^(-2i / rotary_dim).  The
+    angles and their cos/sin are taken in fp64 and rounded once to fp32; the
+    table is a model constant handed to both the oracle and the kernels."""
+    h = rotary_dim // 2
+    f = base ** (-2.0 * np.arange(h, dtype=np.float64) / rotary_dim)
+    ang = np.arange(max_position, dtype=np.float64)[:, None] * f[None, :]
+    return np.ascontiguousarray(np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32))
+
+
+def norm_weight_bf16(rng: np.random.Generator, D: int) -> np.ndarray:
+    """Per-head RMSNorm weight: 1 + 0.25 N(0,1), in bf16."""
+    return bf16_bits(np.float32(1.0) + np.float32(0.25) * rng.standard_normal(D, dtype=np.float32))
+
+
+def producer_rope_tokens(T: int = 8192, Hq: int = 32, Hkv: int = 8, D: int = 128, rotary_dim: int = 128,
+                         max_position: int = 32768, seed: int = 4):
+    """producer_tokens plus positions 0..T-1 (one sequence from its start), a
+    RoPE table for max_position positions and Q / K RMSNorm weights."""
+    p = producer_tokens(T, Hq, Hkv, D, seed)
+    rng = np.random.default_rng([seed, 22])
+    p.update(positions=np.arange(T, dtype=np.int32), cos_sin=rope_cos_sin(max_position, rotary_dim),
+             rotary_dim=rotary_dim, q_norm_weight=norm_weight_bf16(rng, D), k_norm_weight=norm_weight_bf16(rng, D))
+    return p
