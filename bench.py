@@ -558,6 +558,24 @@ def run_secondary(torch, i8, hbm_peak):
                                       "frac_hbm": moved / (ms / 1e3) / 1e9 / hbm_peak}
     except Exception as e:  # pragma: no cover - report, do not hide
         res["producer_8192x8x128"] = {"error": str(e)[:200]}
+    # fused producer: the same tokens at positions 0..8191 with Q/K RMSNorm and
+    # full-width RoPE (table rows read once per token, 512 B each)
+    try:
+        p = wl.producer_rope_tokens()
+        cache = i8.alloc_int8_cache(p["num_blocks"], p["Hkv"], p["D"])
+        k, v, q, s, pos, cs, qw, kw = (to_dev(torch, p[n]) for n in ("k", "v", "q", "slots", "positions", "cos_sin",
+                                                                  "q_norm_weight", "k_norm_weight"))
+        q_i8 = torch.empty(q.shape, dtype=torch.int8, device="cuda")
+        q_s = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+        ms = time_graph(torch, lambda: i8.kv_rope_quant_write(k, v, s, **cache, positions=pos, cos_sin=cs,
+                                                              rotary_dim=p["rotary_dim"], q=q, q_i8=q_i8, q_scale=q_s,
+                                                              q_norm_weight=qw, k_norm_weight=kw), 20)
+        T, Hkv, Hq, D, rd = 8192, p["Hkv"], p["Hq"], p["D"], p["rotary_dim"]
+        moved = (T * (2 * Hkv * D * 2 + 2 * Hkv * D + 2 * Hkv * 4) + T * Hq * (2 * D + D + 4) + T * (rd * 4 + 4))
+        res["producer_rope_norm_8192x8x128"] = {"us": ms * 1e3, "gb_s": moved / (ms / 1e3) / 1e9,
+                                                "frac_hbm": moved / (ms / 1e3) / 1e9 / hbm_peak}
+    except Exception as e:  # pragma: no cover
+        res["producer_rope_norm_8192x8x128"] = {"error": str(e)[:200]}
     # prefix chunk: 2048 queries after 16384 cached tokens, 24 q / 4 kv heads, head_dim 256
     try:
         w = wl.prefix_chunk()

@@ -73,7 +73,8 @@ i8kv_status i8kv_last_error(char* buf, size_t n);
  * 1 = a pipeline wait exceeded its time limit, 2 = a block-table or slot entry
  * or sequence length out of range (the access was skipped), 3 = seq_lens or
  * block_tables changed while a decode kernel was starting (they were written
- * by the kernel just before it on the stream; the result is undefined).  Returns
+ * by the kernel just before it on the stream; the result is undefined), 4 = a
+ * RoPE position outside the cos/sin table (the token was skipped).  Returns
  * I8KV_ERR_DEVICE if *code != 0. */
 i8kv_status i8kv_device_error(int* code);
 
@@ -100,6 +101,41 @@ i8kv_status i8kv_kv_quant_write(const uint16_t* k, const uint16_t* v, const int3
                                 int D, int block_size, int num_blocks, int8_t* k_cache, int8_t* v_cache,
                                 float* k_scale, float* v_scale, const uint16_t* q, int Hq, int8_t* q_i8,
                                 float* q_scale, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Fused KV producer with Q/K RMSNorm and RoPE ([KV] §2.2 steps 1-6: RoPE on */
+/* Q and K ahead of the absmax and the quantization; [KV] §5.3: the per-head */
+/* Q/K RMSNorm that precedes RoPE).  Same outputs, rules and error handling  */
+/* as i8kv_kv_quant_write, except that every Q and K vector x (bf16 -> fp32) */
+/* is first transformed in fp32, each step one correctly rounded operation   */
+/* in this order (no FMA contraction), so results are bit-reproducible:      */
+/*   RMSNorm (when the kind's weight is given, bf16 [D]):                    */
+/*     ss  = sum of x_i^2 as a balanced binary tree in index order           */
+/*           (pairs (0,1), (2,3), ..., then pairs of those, ...);             */
+/*     inv = 1 / sqrt(ss * (1/D) + norm_eps);   x_i = (x_i * inv) * w_i.      */
+/*   RoPE, rotate-half on the first rotary_dim dims (h = rotary_dim / 2),    */
+/*     with row r = cos_sin[positions[t]] (fp32 [max_position, rotary_dim]:  */
+/*     cos of the h frequencies, then their sin):                            */
+/*     a = x_i, b = x_{i+h}:  x_i = a*r[i] - b*r[h+i],  x_{i+h} = b*r[i] + a*r[h+i]*/
+/*     (products rounded, then the sum).  Dims >= rotary_dim are unchanged.   */
+/*   V is not transformed.                                                   */
+/* rotary_dim: 0 (no RoPE; positions and cos_sin may be NULL) or a multiple  */
+/*   of 32 up to D.  q_norm_weight / k_norm_weight: NULL skips that norm     */
+/*   (q_norm_weight is ignored without q); norm_eps > 0 when either is given.*/
+/* q_i8 / q_scale may both be NULL when q_out is given.                      */
+/* q_out (bf16 [T, Hq, D]) and k_out (bf16 [T, Hkv, D]), nullable, receive   */
+/*   the transformed Q / K rounded to nearest-even bf16, for every token     */
+/*   whatever its slot (k_out lets a high-precision path reuse the rotated K).*/
+/* A token whose position lies outside [0, max_position) is skipped entirely */
+/*   (none of its outputs is written) and the device error word records 4.   */
+/* cos_sin and the norm weights must be 16-byte aligned.                     */
+/* ------------------------------------------------------------------------ */
+i8kv_status i8kv_kv_rope_quant_write(const uint16_t* k, const uint16_t* v, const int32_t* slot_mapping, int T,
+                                     int Hkv, int D, int block_size, int num_blocks, int8_t* k_cache, int8_t* v_cache,
+                                     float* k_scale, float* v_scale, const uint16_t* q, int Hq, int8_t* q_i8,
+                                     float* q_scale, const int32_t* positions, const float* cos_sin, int max_position,
+                                     int rotary_dim, const uint16_t* q_norm_weight, const uint16_t* k_norm_weight,
+                                     float norm_eps, uint16_t* q_out, uint16_t* k_out, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* INT8 paged decode attention ([PV] §2-§3, [KV] §3.3).                     */

@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     int8_paged_decode_attn_noalloc,
     int8_prefix_attn,
     kv_quant_write,
+    kv_rope_quant_write,
     last_error,
     lib,
     library_path,

@@ -38,6 +38,8 @@ _SIGS = {
     "i8kv_device_error": [ctypes.POINTER(ctypes.c_int)],
     "i8kv_version": [],
     "i8kv_kv_quant_write": [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P],
+    "i8kv_kv_rope_quant_write": [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _P,
+                                 _P, _F, _P, _P, _P],
     "i8kv_decode_workspace_bytes": [_I, _I, _I, _I, _I, _I, _I],
     "i8kv_int8_paged_decode_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z,
                                     _P],
@@ -164,6 +166,31 @@ def kv_quant_write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, q=Non
         _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
         _bf16(q, "q"), Hq, _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
         _stream(stream)))
+
+
+def kv_rope_quant_write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, positions=None, cos_sin=None,
+                        rotary_dim: int = 0, q=None, q_i8=None, q_scale=None, q_norm_weight=None,
+                        k_norm_weight=None, norm_eps: float = 1e-6, q_out=None, k_out=None, stream=None):
+    """kv_quant_write with Q/K RMSNorm (optional bf16 weights [D]) and rotate-half
+    RoPE on the first rotary_dim dims (positions int32 [T], cos_sin float32
+    [max_position, rotary_dim]) applied before the quantization; q_out / k_out
+    (bf16, nullable) receive the transformed vectors."""
+    NB, Hkv, D = _cache_geom(k_cache, 16)
+    T = k.shape[0]
+    Hq = 0 if q is None else q.shape[1]
+    max_pos = 0
+    if cos_sin is not None:
+        if cos_sin.dim() != 2 or cos_sin.shape[1] != rotary_dim:
+            raise I8KVError(ERR_INVALID_ARG, "cos_sin must be [max_position, rotary_dim]")
+        max_pos = cos_sin.shape[0]
+    _check(lib().i8kv_kv_rope_quant_write(
+        _bf16(k, "k"), _bf16(v, "v"), _ptr(slot_mapping, torch.int32, "slot_mapping"), T, Hkv, D, BLOCK_SIZE, NB,
+        _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
+        _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
+        _bf16(q, "q"), Hq, _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
+        _ptr(positions, torch.int32, "positions"), _ptr(cos_sin, torch.float32, "cos_sin"), max_pos, rotary_dim,
+        _bf16(q_norm_weight, "q_norm_weight"), _bf16(k_norm_weight, "k_norm_weight"), float(norm_eps),
+        _bf16(q_out, "q_out"), _bf16(k_out, "k_out"), _stream(stream)))
 
 
 def bf16_kv_write(k, v, slot_mapping, k_cache, v_cache, stream=None):

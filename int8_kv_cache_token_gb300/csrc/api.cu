@@ -101,6 +101,57 @@ i8kv_status i8kv_kv_quant_write(const uint16_t* k, const uint16_t* v, const int3
   return from_cuda(i8kv::launch_kv_quant_write(p, static_cast<cudaStream_t>(stream)), "kv_quant_write launch");
 }
 
+i8kv_status i8kv_kv_rope_quant_write(const uint16_t* k, const uint16_t* v, const int32_t* slot_mapping, int T,
+                                     int Hkv, int D, int block_size, int num_blocks, int8_t* k_cache, int8_t* v_cache,
+                                     float* k_scale, float* v_scale, const uint16_t* q, int Hq, int8_t* q_i8,
+                                     float* q_scale, const int32_t* positions, const float* cos_sin, int max_position,
+                                     int rotary_dim, const uint16_t* q_norm_weight, const uint16_t* k_norm_weight,
+                                     float norm_eps, uint16_t* q_out, uint16_t* k_out, void* stream) {
+  REQUIRE(T >= 0, I8KV_ERR_INVALID_ARG, "T=%d < 0", T);
+  REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+  REQUIRE(D == 128 || D == 256, I8KV_ERR_UNSUPPORTED, "head_dim %d not supported (128 or 256)", D);
+  REQUIRE(Hkv > 0 && Hkv <= 8, I8KV_ERR_UNSUPPORTED, "Hkv=%d not in 1..8", Hkv);
+  REQUIRE(num_blocks > 0, I8KV_ERR_INVALID_ARG, "num_blocks=%d", num_blocks);
+  REQUIRE(rotary_dim >= 0 && rotary_dim <= D, I8KV_ERR_INVALID_ARG, "rotary_dim=%d not in 0..%d", rotary_dim, D);
+  REQUIRE(rotary_dim % 32 == 0, I8KV_ERR_UNSUPPORTED, "rotary_dim=%d not a multiple of 32", rotary_dim);
+  if (rotary_dim > 0) {
+    REQUIRE(positions && cos_sin, I8KV_ERR_INVALID_ARG, "rotary_dim > 0 needs positions and cos_sin");
+    REQUIRE(max_position > 0, I8KV_ERR_INVALID_ARG, "max_position=%d", max_position);
+    REQUIRE(aligned16(cos_sin), I8KV_ERR_INVALID_ARG, "cos_sin must be 16-byte aligned");
+  }
+  if (q_norm_weight || k_norm_weight) {
+    REQUIRE(norm_eps > 0.f && norm_eps < 3.0e38f, I8KV_ERR_INVALID_ARG, "norm_eps must be positive and finite");
+    REQUIRE(aligned16(q_norm_weight) && aligned16(k_norm_weight), I8KV_ERR_INVALID_ARG,
+            "norm weights must be 16-byte aligned");
+  }
+  if (T == 0) return I8KV_OK;
+  REQUIRE(k && v && slot_mapping && k_cache && v_cache && k_scale && v_scale, I8KV_ERR_INVALID_ARG,
+          "null K/V/slot/cache/scale pointer");
+  REQUIRE(aligned16(k) && aligned16(v) && aligned16(k_cache) && aligned16(v_cache) && aligned16(k_out),
+          I8KV_ERR_INVALID_ARG, "K/V inputs, caches and k_out must be 16-byte aligned");
+  REQUIRE(q || !q_out, I8KV_ERR_INVALID_ARG, "q_out given without q");
+  if (q) {
+    REQUIRE(Hq > 0, I8KV_ERR_INVALID_ARG, "Hq=%d with a query", Hq);
+    REQUIRE((q_i8 != nullptr) == (q_scale != nullptr), I8KV_ERR_INVALID_ARG, "q_i8 and q_scale go together");
+    REQUIRE(q_i8 || q_out, I8KV_ERR_INVALID_ARG, "q given without q_i8/q_scale or q_out");
+    REQUIRE(aligned16(q) && aligned16(q_i8) && aligned16(q_out), I8KV_ERR_INVALID_ARG,
+            "q, q_i8 and q_out must be 16-byte aligned");
+  }
+  i8kv::ProducerParams p{k, v, slot_mapping, T, Hkv, D, num_blocks, k_cache, v_cache, k_scale, v_scale,
+                         q, q ? Hq : 0, q_i8, q_scale};
+  p.positions = rotary_dim > 0 ? positions : nullptr;
+  p.cos_sin = rotary_dim > 0 ? cos_sin : nullptr;
+  p.max_pos = max_position;
+  p.rd = rotary_dim;
+  p.q_norm_w = q_norm_weight;
+  p.k_norm_w = k_norm_weight;
+  p.eps = norm_eps;
+  p.q_out = q_out;
+  p.k_out = k_out;
+  return from_cuda(i8kv::launch_kv_rope_quant_write(p, static_cast<cudaStream_t>(stream)),
+                   "kv_rope_quant_write launch");
+}
+
 size_t i8kv_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_blocks, int block_size, int partition) {
   (void)Hq;
   (void)block_size;

@@ -397,6 +397,64 @@ constexpr float kLog2e = 1.4426950408889634f;
 // integer's two's-complement byte.
 __device__ __forceinline__ uint32_t rne_bits(float x) { return __float_as_uint(__fadd_rn(x, 12582912.0f)); }
 
+// Packed fp32 pairs for the f32x2 instructions of sm_100-class GPUs: two
+// lanes in one 64-bit register pair, each lane an IEEE round-to-nearest
+// operation, so each result equals two scalar __fmul_rn / __fadd_rn /
+// __fmaf_rn calls bit for bit at half the instruction count.  One exception,
+// measured: ptxas fuses add2(mul2(a, b), c) into one multiply-add (the
+// product's rounding is lost), so where a product's rounding is part of the
+// definition its sum is taken with scalar __fadd_rn instead.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// rne_bits(x[i] / s) for the N (even) values of one row: div_row's quotient
+// then the round-half-even add, on packed pairs.  Same results as div_row
+// followed by rne_bits, element by element.
+template <int N>
+__device__ __forceinline__ void div_rne_row(const float (&x)[N], float s, float y, uint32_t (&q)[N]) {
+  if (s < kTinyDivisor) {
+    float t[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) t[i] = x[i];
+    div_row(t, s, y);
+#pragma unroll
+    for (int i = 0; i < N; ++i) q[i] = rne_bits(t[i]);
+    return;
+  }
+  const uint64_t y2 = f2(y, y), ns2 = f2(-s, -s), c2 = f2(12582912.0f, 12582912.0f);
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const uint64_t v = f2(x[2 * i], x[2 * i + 1]);
+    const uint64_t qq = mul2(v, y2);
+    const uint64_t r = fma2(ns2, qq, v);
+    float lo, hi;
+    f2_split(add2(fma2(r, y2, qq), c2), lo, hi);
+    q[2 * i] = __float_as_uint(lo);
+    q[2 * i + 1] = __float_as_uint(hi);
+  }
+}
+
 // a / 127 correctly rounded, by the same method with the constant RN(1/127).
 // Checked exhaustively against IEEE division for every float in [1, 4), in the
 // two lowest normal binades and in the top binade (the rounding pattern

@@ -19,8 +19,17 @@ struct ProducerParams {
   float* v_scale;
   const uint16_t* q;  // nullable
   int Hq;
-  int8_t* q_i8;
+  int8_t* q_i8;  // nullable in the fused variant (only q_out wanted)
   float* q_scale;
+  // Fused variant only (RMSNorm and RoPE on Q / K before the quantization).
+  const int32_t* positions;  // [T], needed when rd > 0
+  const float* cos_sin;      // [max_pos, rd]: cos of the rd/2 frequencies, then their sin
+  int max_pos, rd;           // rd = 0: no rotation
+  const uint16_t* q_norm_w;  // [D] bf16, nullable
+  const uint16_t* k_norm_w;  // [D] bf16, nullable
+  float eps;
+  uint16_t* q_out;  // [T, Hq, D] bf16, nullable
+  uint16_t* k_out;  // [T, Hkv, D] bf16, nullable
 };
 
 // Decode (INT8 and BF16-KV variants share the work split and the workspace).
@@ -82,6 +91,7 @@ cudaError_t read_error_decode(int* value);
 cudaError_t read_error_prefix(int* value);
 
 cudaError_t launch_kv_quant_write(const ProducerParams& p, cudaStream_t stream);
+cudaError_t launch_kv_rope_quant_write(const ProducerParams& p, cudaStream_t stream);
 size_t prefix_workspace_bytes(int H, int C, int Hkv, int D);
 cudaError_t launch_bf16_kv_write(const ProducerParams& p, uint16_t* k_cache, uint16_t* v_cache, cudaStream_t stream);
 
