@@ -551,6 +551,72 @@ int orc_bf16_kv_write(const uint16_t* k, const uint16_t* v, const int32_t* slot_
 
 /* Plain softmax attention in fp64 over the bf16 paged cache, for a bf16 query
  * [B, Hq, D]: O = sum_t softmax(q.k_t * scale) v_t.  out is [B, Hq, D]. */
+/* High-precision chunk attention, the first-chunk path of [KV] §3.1 (the
+ * first prefill chunk keeps a high-precision attention while the producer
+ * writes its K/V to the INT8 cache) and of the routing in [KV] §4 (chunks
+ * whose history is below the INT8 threshold stay high-precision).  Query row
+ * j of the chunk (position history_len + j) attends to keys 0 .. history_len
+ * + j: a history key t < history_len is read back from the INT8 cache as
+ * code * scale (the only copy the cache keeps), a chunk key from the bf16
+ * inputs k_chunk / v_chunk [chunk_len, Hkv, D].  Plain softmax attention in
+ * fp64: out = sum_t e^(s_t - m) V_t / sum_t e^(s_t - m), s_t = scale q.K_t.
+ * rows (nullable) selects chunk rows; out is [nrows, Hq, D]. */
+int orc_bf16_prefix_attn(double* out, const uint16_t* q, const uint16_t* k_chunk, const uint16_t* v_chunk,
+                         const int8_t* k_cache, const int8_t* v_cache, const float* k_scale, const float* v_scale,
+                         const int32_t* block_table, int history_len, int chunk_len, int Hq, int Hkv, int D, int bs,
+                         double softmax_scale, const int32_t* rows, int nrows, int nthreads) {
+  if (Hq % Hkv != 0 || D % 16 != 0 || history_len < 0 || chunk_len < 0) return ORC_BAD_ARG;
+  if (rows == NULL) nrows = chunk_len;
+  const int G = Hq / Hkv;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) num_threads(nthreads)
+#endif
+  for (int r = 0; r < nrows; ++r)
+    for (int h = 0; h < Hq; ++h) {
+      const int j = rows ? rows[r] : r;
+      const int n_keys = history_len + j + 1;
+      const int kvh = h / G;
+      const uint16_t* qv = q + ((size_t)j * Hq + h) * D;
+      double* O = out + ((size_t)r * Hq + h) * D;
+      double* s = (double*)malloc(sizeof(double) * (size_t)n_keys);
+      double* kx = (double*)malloc(sizeof(double) * (size_t)D);
+      double m = -INFINITY;
+      for (int t = 0; t < n_keys; ++t) {
+        if (t < history_len) {
+          const int blk = block_table[t / bs], off = t % bs;
+          const double sc = (double)k_scale[s_index(blk, kvh, off, Hkv, bs)];
+          for (int d = 0; d < D; ++d) kx[d] = (double)k_cache[k_index(blk, kvh, d, off, Hkv, D, bs)] * sc;
+        } else {
+          const uint16_t* kr = k_chunk + ((size_t)(t - history_len) * Hkv + kvh) * D;
+          for (int d = 0; d < D; ++d) kx[d] = (double)bf16_to_f32(kr[d]);
+        }
+        double a = 0.0;
+        for (int d = 0; d < D; ++d) a += (double)bf16_to_f32(qv[d]) * kx[d];
+        s[t] = a * softmax_scale;
+        if (s[t] > m) m = s[t];
+      }
+      double l = 0.0;
+      for (int d = 0; d < D; ++d) O[d] = 0.0;
+      for (int t = 0; t < n_keys; ++t) {
+        const double p = exp(s[t] - m);
+        l += p;
+        if (t < history_len) {
+          const int blk = block_table[t / bs], off = t % bs;
+          const double sc = (double)v_scale[s_index(blk, kvh, off, Hkv, bs)];
+          for (int d = 0; d < D; ++d) O[d] += p * (double)v_cache[v_index(blk, kvh, d, off, Hkv, D, bs)] * sc;
+        } else {
+          const uint16_t* vr = v_chunk + ((size_t)(t - history_len) * Hkv + kvh) * D;
+          for (int d = 0; d < D; ++d) O[d] += p * (double)bf16_to_f32(vr[d]);
+        }
+      }
+      for (int d = 0; d < D; ++d) O[d] /= l;
+      free(kx);
+      free(s);
+    }
+  return ORC_OK;
+}
+
 int orc_bf16_decode_attn(double* out, const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
                          const int32_t* block_tables, const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int bs,
                          int max_blocks, double softmax_scale, int nthreads) {

@@ -74,9 +74,11 @@ def _load():
             lib.orc_prefix_attn.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, I,
                                             P, I, I, I]
             lib.orc_bf16_kv_write.argtypes = [P, P, P, I, I, I, I, P, P]
+            lib.orc_bf16_prefix_attn.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, I,
+                                                 I]
             lib.orc_bf16_decode_attn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_double, I]
             for name in ("orc_kv_quant_write", "orc_kv_rope_quant_write", "orc_qk_i32", "orc_decode_attn", "orc_prefix_attn",
-                         "orc_bf16_kv_write", "orc_bf16_decode_attn", "orc_max_threads"):
+                         "orc_bf16_kv_write", "orc_bf16_decode_attn", "orc_bf16_prefix_attn", "orc_max_threads"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -268,6 +270,30 @@ def prefix_attn(q_i8, q_scale, cache, block_table, history_len, block_size, soft
                              block_size, softmax_scale, key_tile, group, _p(r), nrows, int(fp32_decisions),
                              nthreads)
     _check(rc, "prefix_attn")
+    return out
+
+
+def bf16_prefix_attn(q, k_chunk, v_chunk, cache, block_table, history_len, block_size, softmax_scale=None,
+                     rows=None, nthreads=0):
+    """High-precision chunk attention ([KV] §3.1, §4 routing): chunk rows of q
+    (uint16 bf16 [C,Hq,D]) over the INT8 history read back as code * scale and
+    the chunk's own bf16 k_chunk / v_chunk [C,Hkv,D], causal.  fp64 out
+    [len(rows) or C, Hq, D].  cache / block_table may be None when
+    history_len == 0."""
+    q, kc, vc = _u16(q), _u16(k_chunk), _u16(v_chunk)
+    C, Hq, D = q.shape
+    Hkv = kc.shape[1]
+    if softmax_scale is None:
+        softmax_scale = float(np.float32(1.0) / np.sqrt(np.float32(D)))
+    r = None if rows is None else np.ascontiguousarray(rows, np.int32)
+    nrows = C if r is None else r.size
+    out = np.empty((nrows, Hq, D), np.float64)
+    c = cache or {}
+    bt = None if block_table is None else np.ascontiguousarray(block_table, np.int32).ravel()
+    rc = _load().orc_bf16_prefix_attn(_p(out), _p(q), _p(kc), _p(vc), _p(c.get("k_cache")), _p(c.get("v_cache")),
+                                      _p(c.get("k_scale")), _p(c.get("v_scale")), _p(bt), history_len, C, Hq, Hkv,
+                                      D, block_size, float(softmax_scale), _p(r), nrows, nthreads)
+    _check(rc, "bf16_prefix_attn")
     return out
 
 

@@ -35,7 +35,8 @@ MUTANTS = {
     # online softmax forgets to rescale l
     "prefix_no_l_rescale": ("        l *= alpha;\n", "\n"),
     # causal mask off by one
-    "causal_off_by_one": ("const int n_keys = history_len + j + 1;", "const int n_keys = history_len + j;"),
+    "causal_off_by_one": ("const int n_keys = history_len + j + 1;\n      const int kvh = h / G;\n      const int8_t* qv",
+                          "const int n_keys = history_len + j;\n      const int kvh = h / G;\n      const int8_t* qv"),
     # K chunk layout with token and chunk swapped
     "k_layout_swap": ("return ((((size_t)blk * Hkv + h) * (D / 16) + d / 16) * bs + off) * 16 + (d % 16);",
                       "return ((((size_t)blk * Hkv + h) * bs + off) * (D / 16) + d / 16) * 16 + (d % 16);"),
@@ -55,6 +56,11 @@ MUTANTS = {
     "rms_sequential_sum": ("  if (n == 1) return x[0] * x[0];\n",
                            "  if (n > 1) {\n    float acc = 0.0f;\n    for (int i = 0; i < n; ++i) acc += x[i] * x[i];\n"
                            "    return acc;\n  }\n  if (n == 1) return x[0] * x[0];\n"),
+    # high-precision chunk: causal limit off by one, history K scaled by sV
+    "bf16_prefix_causal": ("const int n_keys = history_len + j + 1;\n      const int kvh = h / G;\n      const uint16_t* qv",
+                           "const int n_keys = history_len + j;\n      const int kvh = h / G;\n      const uint16_t* qv"),
+    "bf16_prefix_k_scale": ("const double sc = (double)k_scale[s_index(blk, kvh, off, Hkv, bs)];\n          for (int d = 0; d < D; ++d) kx[d]",
+                            "const double sc = (double)v_scale[s_index(blk, kvh, off, Hkv, bs)];\n          for (int d = 0; d < D; ++d) kx[d]"),
 }
 
 
@@ -70,6 +76,7 @@ def test_pins_catch_mutant(name, tmp_path):
                     str(mut), "-lm"], check=True)
     env = dict(os.environ, I8KV_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        "tests/test_oracle_quant.py", "tests/test_oracle_rope.py", "tests/test_oracle_attention.py"],
+                        "tests/test_oracle_quant.py", "tests/test_oracle_rope.py", "tests/test_oracle_bf16_prefix.py",
+                        "tests/test_oracle_attention.py"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
