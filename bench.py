@@ -598,6 +598,31 @@ def run_secondary(torch, i8, hbm_peak):
                                     "pairs": w.pairs(), "ops": w.int8_ops()}
     except Exception as e:  # pragma: no cover
         res["prefix_16384+2048"] = {"error": str(e)[:200]}
+    # first prefill chunk, 0 + 4096 tokens, 24 / 4 heads, head_dim 256: the routed
+    # entry on the high-precision path (producer + bf16 attention) and forced onto
+    # INT8 (producer with the query + INT8 attention), as the pages compare them
+    try:
+        w = wl.PrefixWorkload("first_chunk", 24, 4, 256, 0, 4096, seed=5)
+        k, v = w.kv()
+        kd, vd, qd, sd = to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.q()), to_dev(torch, w.slots())
+        cache = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+        out = torch.empty((w.chunk, w.Hq, w.D), dtype=torch.float32, device="cuda")
+        q_i8 = torch.empty((w.chunk, w.Hq, w.D), dtype=torch.int8, device="cuda")
+        q_s = torch.empty((w.chunk, w.Hq), dtype=torch.float32, device="cuda")
+        bt = to_dev(torch, w.block_table)
+        pws = i8.prefix_workspace(0, w.chunk, w.Hkv, w.D)
+        flops = w.int8_ops()
+        first = {}
+        for name, thr in (("bf16", 4096), ("int8", 0)):
+            ms = time_graph(torch, lambda thr=thr: i8.prefill_chunk(out, qd, kd, vd, sd, cache["k_cache"],
+                                                                    cache["v_cache"], cache["k_scale"],
+                                                                    cache["v_scale"], bt, 0, int8_min_history=thr,
+                                                                    q_i8=q_i8, q_scale=q_s, workspace=pws), 5)
+            first[name] = {"ms": ms, "tflops": flops / (ms / 1e3) / 1e12}
+        first["bf16_over_int8_time"] = first["bf16"]["ms"] / first["int8"]["ms"]
+        res["prefill_first_chunk_0+4096"] = first
+    except Exception as e:  # pragma: no cover
+        res["prefill_first_chunk_0+4096"] = {"error": str(e)[:200]}
     return res
 
 

@@ -246,6 +246,56 @@ i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q
                                   size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* High-precision chunk attention ([KV] §3.1: the first prefill chunk keeps  */
+/* a high-precision attention while the producer writes its K/V as INT8;     */
+/* [KV] §4: below the routing threshold chunks stay high-precision).  Query  */
+/* row j of the chunk (bf16 q [C, Hq, D], position history_len + j) attends  */
+/* to keys 0 .. history_len + j:                                             */
+/*   a history key t < history_len is read back from the INT8 cache as       */
+/*   bf16(code x scale) (the cache keeps no other copy), through block_table */
+/*   (entries for positions < history_len);                                  */
+/*   a chunk key comes from the chunk's own bf16 k_chunk / v_chunk           */
+/*   [C, Hkv, D], as given.                                                  */
+/* S = Q K^T on bf16 tensor-core MMAs with fp32 accumulation; online softmax */
+/* in fp32 over 32-key groups; P = p~ rounded to bf16 for the P V MMA; the   */
+/* row sums l use the fp32 p~.  out: fp32 [C, Hq, D].                        */
+/* history_len == 0 (a first chunk): the cache pointers, block_table and     */
+/* num_blocks are not used and may be NULL / 0.                              */
+/* workspace: as for i8kv_int8_prefix_attn (same size function; the tiles    */
+/*   hold bf16 values instead of f16 codes).  Launches two kernels.          */
+/* ------------------------------------------------------------------------ */
+i8kv_status i8kv_bf16_prefix_attn(float* out, const uint16_t* q, const uint16_t* k_chunk, const uint16_t* v_chunk,
+                                  const int8_t* k_cache, const int8_t* v_cache, const float* k_scale,
+                                  const float* v_scale, const int32_t* block_table, int history_len, int chunk_len,
+                                  int Hq, int Hkv, int D, int block_size, int num_blocks, float softmax_scale,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* One prefill chunk, routed ([KV] §3.1-§3.2 and §4: the first chunk on the  */
+/* high-precision attention, later chunks -- once the history reaches the    */
+/* threshold -- wholly INT8, history and chunk in one online softmax).       */
+/* Always: i8kv_kv_quant_write of the chunk's bf16 k, v [C, Hkv, D] to their */
+/* slots (slot_mapping [C]), so the INT8 cache holds the chunk afterwards.   */
+/* Then, with history_len >= int8_min_history: the query is quantized by the */
+/* same call into q_i8 [C, Hq, D] / q_scale [C, Hq] (caller-owned scratch)   */
+/* and i8kv_int8_prefix_attn runs over history + chunk; otherwise            */
+/* i8kv_bf16_prefix_attn runs on the bf16 q, k, v (q_i8 / q_scale unused and */
+/* may be NULL).  int8_min_history = 4096 is the pages' routing; 0 sends     */
+/* every chunk to INT8, INT_MAX none.  block_table must cover history_len +  */
+/* chunk_len positions.  *route (host int, nullable) receives the route      */
+/* taken.  Inputs are assumed rotated already (i8kv_kv_rope_quant_write with */
+/* q_out / k_out produces them).  Three launches: producer, tiles, attention.*/
+/* ------------------------------------------------------------------------ */
+#define I8KV_ROUTE_BF16 0
+#define I8KV_ROUTE_INT8 1
+i8kv_status i8kv_prefill_chunk(float* out, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               const int32_t* slot_mapping, int8_t* k_cache, int8_t* v_cache, float* k_scale,
+                               float* v_scale, const int32_t* block_table, int history_len, int chunk_len, int Hq,
+                               int Hkv, int D, int block_size, int num_blocks, int int8_min_history,
+                               float softmax_scale, int8_t* q_i8, float* q_scale, void* workspace,
+                               size_t workspace_bytes, int* route, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Debug: raw int32 QK accumulators acc[b, h, t] = sum_d q_i8[b,h,d] *        */
 /* K_i8[b, t, h / G, d] for t < seq_lens[b]; 0 for t in [seq_lens[b],        */
 /* max_len).  Uses the decode kernel's paged-K addressing and MMA fragments, */

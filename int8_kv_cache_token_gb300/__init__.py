@@ -6,11 +6,14 @@ thin ctypes binding (binding.py)."""
 from .binding import (  # noqa: F401
     BLOCK_SIZE,
     PARTITION,
+    ROUTE_BF16,
+    ROUTE_INT8,
     I8KVError,
     alloc_bf16_cache,
     alloc_int8_cache,
     bf16_kv_write,
     bf16_paged_decode_attn,
+    bf16_prefix_attn,
     debug_qk_i32,
     decode_workspace,
     decode_workspace_bytes,
@@ -24,6 +27,7 @@ from .binding import (  # noqa: F401
     last_error,
     lib,
     library_path,
+    prefill_chunk,
     prefix_workspace,
     prefix_workspace_bytes,
     version,

@@ -48,6 +48,9 @@ _SIGS = {
                                             _P],
     "i8kv_prefix_workspace_bytes": [_I, _I, _I, _I],
     "i8kv_int8_prefix_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _Z, _P],
+    "i8kv_bf16_prefix_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _Z, _P],
+    "i8kv_prefill_chunk": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _Z,
+                           _P, _P],
     "i8kv_debug_qk_i32": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
     "i8kv_bf16_kv_write": [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P],
     "i8kv_bf16_paged_decode_attn": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P],
@@ -303,3 +306,49 @@ def int8_prefix_attn(out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, blo
         _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
         _ptr(block_table, torch.int32, "block_table"), int(history_len), C, Hq, Hkv, D, BLOCK_SIZE, NB,
         float(softmax_scale), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+ROUTE_BF16, ROUTE_INT8 = 0, 1
+
+
+def bf16_prefix_attn(out, q, k_chunk, v_chunk, history_len: int = 0, k_cache=None, v_cache=None, k_scale=None,
+                     v_scale=None, block_table=None, workspace=None, softmax_scale: float = 0.0, stream=None):
+    """out [C, Hq, D] fp32 <- high-precision chunk attention: bf16 q [C, Hq, D] over the INT8
+    history (read back as code x scale) and the chunk's own bf16 k_chunk / v_chunk [C, Hkv, D]."""
+    C, Hq, D = q.shape
+    Hkv = k_chunk.shape[1]
+    NB = 0
+    if history_len > 0:
+        NB, Hkv_c, D_c = _cache_geom(k_cache, 16)
+        if (Hkv_c, D_c) != (Hkv, D):
+            raise I8KVError(ERR_INVALID_ARG, "cache geometry does not match k_chunk")
+    if workspace is None:
+        workspace = prefix_workspace(int(history_len), C, Hkv, D, device=out.device)
+    _check(lib().i8kv_bf16_prefix_attn(
+        _ptr(out, torch.float32, "out"), _bf16(q, "q"), _bf16(k_chunk, "k_chunk"), _bf16(v_chunk, "v_chunk"),
+        _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
+        _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
+        _ptr(block_table, torch.int32, "block_table"), int(history_len), C, Hq, Hkv, D, BLOCK_SIZE, NB,
+        float(softmax_scale), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def prefill_chunk(out, q, k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, block_table, history_len: int,
+                  int8_min_history: int = 4096, q_i8=None, q_scale=None, workspace=None, softmax_scale: float = 0.0,
+                  stream=None) -> int:
+    """One routed prefill chunk: the producer writes the chunk's K/V to the INT8 cache, then the
+    chunk runs on INT8 attention when history_len >= int8_min_history, else on the high-precision
+    path.  Returns the route taken (ROUTE_BF16 or ROUTE_INT8)."""
+    NB, Hkv, D = _cache_geom(k_cache, 16)
+    C, Hq, _ = q.shape
+    if workspace is None:
+        workspace = prefix_workspace(int(history_len), C, Hkv, D, device=out.device)
+    route = ctypes.c_int(-1)
+    _check(lib().i8kv_prefill_chunk(
+        _ptr(out, torch.float32, "out"), _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"),
+        _ptr(slot_mapping, torch.int32, "slot_mapping"), _ptr(k_cache, torch.int8, "k_cache"),
+        _ptr(v_cache, torch.int8, "v_cache"), _ptr(k_scale, torch.float32, "k_scale"),
+        _ptr(v_scale, torch.float32, "v_scale"), _ptr(block_table, torch.int32, "block_table"), int(history_len), C,
+        Hq, Hkv, D, BLOCK_SIZE, NB, int(int8_min_history), float(softmax_scale), _ptr(q_i8, torch.int8, "q_i8"),
+        _ptr(q_scale, torch.float32, "q_scale"), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        ctypes.byref(route), _stream(stream)))
+    return int(route.value)

@@ -308,6 +308,70 @@ i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q
   return from_cuda(i8kv::launch_int8_prefix(p, static_cast<cudaStream_t>(stream)), "int8 prefix launch");
 }
 
+i8kv_status i8kv_bf16_prefix_attn(float* out, const uint16_t* q, const uint16_t* k_chunk, const uint16_t* v_chunk,
+                                  const int8_t* k_cache, const int8_t* v_cache, const float* k_scale,
+                                  const float* v_scale, const int32_t* block_table, int history_len, int chunk_len,
+                                  int Hq, int Hkv, int D, int block_size, int num_blocks, float softmax_scale,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  REQUIRE(history_len >= 0 && chunk_len >= 0, I8KV_ERR_INVALID_ARG, "history_len=%d chunk_len=%d", history_len,
+          chunk_len);
+  i8kv_status s = check_heads(Hq, Hkv, D);
+  if (s != I8KV_OK) return s;
+  REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+  if (chunk_len == 0) return I8KV_OK;
+  REQUIRE(out && q && k_chunk && v_chunk, I8KV_ERR_INVALID_ARG, "null out/q/k_chunk/v_chunk pointer");
+  REQUIRE(aligned16(q) && aligned16(k_chunk) && aligned16(v_chunk) && aligned16(out), I8KV_ERR_INVALID_ARG,
+          "out, q, k_chunk and v_chunk must be 16-byte aligned");
+  if (history_len > 0) {
+    REQUIRE(num_blocks > 0, I8KV_ERR_INVALID_ARG, "num_blocks=%d", num_blocks);
+    REQUIRE(k_cache && v_cache && k_scale && v_scale && block_table, I8KV_ERR_INVALID_ARG,
+            "history_len > 0 needs the caches, scales and block_table");
+    REQUIRE(aligned16(k_cache) && aligned16(v_cache), I8KV_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+  }
+  const size_t need = i8kv::prefix_workspace_bytes(history_len, chunk_len, Hkv, D);
+  REQUIRE(workspace != nullptr && workspace_bytes >= need, I8KV_ERR_WORKSPACE,
+          "prefix workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+  REQUIRE(aligned16(workspace), I8KV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  i8kv::PrefixParams p{out, nullptr, nullptr, k_cache, v_cache, k_scale, v_scale, block_table, history_len, chunk_len,
+                       Hq, Hkv, Hq / Hkv, D, num_blocks, softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D),
+                       static_cast<uint8_t*>(workspace)};
+  p.qb = q;
+  p.k_chunk = k_chunk;
+  p.v_chunk = v_chunk;
+  return from_cuda(i8kv::launch_bf16_prefix(p, static_cast<cudaStream_t>(stream)), "bf16 prefix launch");
+}
+
+i8kv_status i8kv_prefill_chunk(float* out, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               const int32_t* slot_mapping, int8_t* k_cache, int8_t* v_cache, float* k_scale,
+                               float* v_scale, const int32_t* block_table, int history_len, int chunk_len, int Hq,
+                               int Hkv, int D, int block_size, int num_blocks, int int8_min_history,
+                               float softmax_scale, int8_t* q_i8, float* q_scale, void* workspace,
+                               size_t workspace_bytes, int* route, void* stream) {
+  REQUIRE(history_len >= 0 && chunk_len >= 0, I8KV_ERR_INVALID_ARG, "history_len=%d chunk_len=%d", history_len,
+          chunk_len);
+  i8kv_status s = check_heads(Hq, Hkv, D);
+  if (s != I8KV_OK) return s;
+  const bool int8 = history_len >= int8_min_history;
+  if (route) *route = int8 ? I8KV_ROUTE_INT8 : I8KV_ROUTE_BF16;
+  if (chunk_len == 0) return I8KV_OK;
+  REQUIRE(out && q && block_table && k_cache && v_cache && k_scale && v_scale, I8KV_ERR_INVALID_ARG,
+          "null out/q/block_table/cache pointer");
+  if (int8) REQUIRE(q_i8 && q_scale, I8KV_ERR_INVALID_ARG, "the INT8 route needs q_i8 and q_scale");
+  const size_t need = i8kv::prefix_workspace_bytes(history_len, chunk_len, Hkv, D);
+  REQUIRE(workspace != nullptr && workspace_bytes >= need, I8KV_ERR_WORKSPACE,
+          "prefix workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+  // the chunk's K/V (and, on the INT8 route, its query) through the producer
+  s = i8kv_kv_quant_write(k, v, slot_mapping, chunk_len, Hkv, D, block_size, num_blocks, k_cache, v_cache, k_scale,
+                          v_scale, int8 ? q : nullptr, Hq, q_i8, q_scale, stream);
+  if (s != I8KV_OK) return s;
+  if (int8)
+    return i8kv_int8_prefix_attn(out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, history_len,
+                                 chunk_len, Hq, Hkv, D, block_size, num_blocks, softmax_scale, workspace,
+                                 workspace_bytes, stream);
+  return i8kv_bf16_prefix_attn(out, q, k, v, k_cache, v_cache, k_scale, v_scale, block_table, history_len, chunk_len,
+                               Hq, Hkv, D, block_size, num_blocks, softmax_scale, workspace, workspace_bytes, stream);
+}
+
 i8kv_status i8kv_debug_qk_i32(int32_t* acc, const int8_t* q_i8, const int8_t* k_cache, const int32_t* block_tables,
                               const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size, int max_blocks,
                               int num_blocks, int max_len, void* stream) {

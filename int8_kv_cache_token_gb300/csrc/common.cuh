@@ -274,6 +274,11 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with bf16 A and B (A and B types sit in bits 7-9 and 10-12).
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+  return umma_idesc_f16(M, N) | (1u << 7) | (1u << 10);
+}
+
 // D[tmem] (+)= A * B^T, one K = 16 step (cta_group::1).
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          bool accumulate) {

@@ -82,7 +82,12 @@ struct PrefixParams {
   const int32_t* block_table;
   int H, C, Hq, Hkv, G, D, num_blocks;
   float sm_scale;
-  uint8_t* tiles;  // workspace: f16 operand tiles per (KV head, 32-key group)
+  uint8_t* tiles;  // workspace: f16 (bf16) operand tiles per (KV head, 32-key group)
+  // High-precision variant: bf16 query and the chunk's own bf16 K/V (the
+  // history still comes from the INT8 cache, read back as code x scale).
+  const uint16_t* qb;       // [C, Hq, D]
+  const uint16_t* k_chunk;  // [C, Hkv, D]
+  const uint16_t* v_chunk;  // [C, Hkv, D]
 };
 
 // Per-translation-unit device error words (read and cleared).
@@ -106,5 +111,6 @@ cudaError_t launch_debug_qk(const DebugQKParams& p, cudaStream_t stream);
 size_t noalloc_scratch_bytes();
 cudaError_t noalloc_scratch_address(int device, void** addr);
 cudaError_t launch_int8_prefix(const PrefixParams& p, cudaStream_t stream);
+cudaError_t launch_bf16_prefix(const PrefixParams& p, cudaStream_t stream);
 
 }  // namespace i8kv

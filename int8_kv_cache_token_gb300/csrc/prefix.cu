@@ -44,6 +44,8 @@
 // (warps 4-7, 8-11) take the softmax of the even and the odd groups, thread =
 // row, so the two run side by side; both apply every group's product to their
 // half of the output dims.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -213,8 +215,116 @@ __global__ void __launch_bounds__(256) prefix_tiles_kernel(PrefixParams p) {
   }
 }
 
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+__device__ __forceinline__ float s8_at(const uint32_t (&w)[4], int e) {
+  return (float)(int8_t)((w[e >> 2] >> (8 * (e & 3))) & 0xffu);
+}
+
+// ---- bf16 operand tiles for the high-precision variant: one CTA per (group,
+// KV head).  A history key (t < H) is read back from the INT8 cache as
+// bf16(code x scale); a chunk key comes from the bf16 k_chunk / v_chunk rows
+// as it is; keys past the sequence are zero.  Same tile layout as the f16
+// tiles (the scale slots are not used).
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p) {
+__global__ void __launch_bounds__(256) prefix_tiles_bf16_kernel(PrefixParams p) {
+  using T = Tile<D>;
+  __shared__ __align__(16) uint16_t vrows[kGroup][D + 8];  // the group's chunk V rows (padded rows)
+  __shared__ float s_sk[kGroup], s_sv[kGroup];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int g = blockIdx.x, kvh = blockIdx.y, tid = threadIdx.x;
+  const int Hkv = p.Hkv, H = p.H, C = p.C;
+  const int ngt = gridDim.x;
+  const int key0 = g * kGroup;
+  uint8_t* tile = p.tiles + ((size_t)kvh * ngt + g) * T::kBytes;
+  int blk[kPagesPG];
+#pragma unroll
+  for (int i = 0; i < kPagesPG; ++i) {
+    const int lb = g * kPagesPG + i;
+    blk[i] = -1;
+    if (lb * kBS < H) {
+      const int b = p.block_table[lb];
+      if (b < 0 || b >= p.num_blocks) {
+        if (tid == 0) record_error(2);
+      } else {
+        blk[i] = b;
+      }
+    }
+  }
+  if (tid < kGroup) {
+    const int t = key0 + tid, pg = tid / kBS;
+    float sk = 0.f, sv = 0.f;
+    if (t < H && blk[pg] >= 0) {
+      const size_t si = ((size_t)blk[pg] * kBS + t % kBS) * Hkv + kvh;
+      sk = p.k_scale[si];
+      sv = p.v_scale[si];
+    }
+    s_sk[tid] = sk;
+    s_sv[tid] = sv;
+  }
+  for (int i = tid; i < kGroup * (D / 8); i += 256) {
+    const int key = i / (D / 8), c8 = i % (D / 8), t = key0 + key;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (t >= H && t < H + C)
+      v = __ldg(reinterpret_cast<const uint4*>(p.v_chunk + ((size_t)(t - H) * Hkv + kvh) * D) + c8);
+    *reinterpret_cast<uint4*>(&vrows[key][8 * c8]) = v;
+  }
+  __syncthreads();
+  // K: (key, 16-dim chunk) -> [key][D] (SW128 atoms)
+  for (int i = tid; i < kGroup * (D / 16); i += 256) {
+    const int key = i / (D / 16), dc = i % (D / 16), t = key0 + key;
+    uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+    if (t < H) {
+      const int pg = key / kBS;
+      if (blk[pg] >= 0) {
+        const uint4 c = __ldg(reinterpret_cast<const uint4*>(p.k_cache + ((size_t)blk[pg] * Hkv + kvh) * (D * kBS)) +
+                              dc * kBS + t % kBS);
+        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+        const float sk = s_sk[key];
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = bf16x2_bits(__fmul_rn(s8_at(cw, 2 * e), sk), __fmul_rn(s8_at(cw, 2 * e + 1), sk));
+        h0 = make_uint4(w[0], w[1], w[2], w[3]);
+        h1 = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    } else if (t < H + C) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.k_chunk + ((size_t)(t - H) * Hkv + kvh) * D + 16 * dc);
+      h0 = __ldg(src);
+      h1 = __ldg(src + 1);
+    }
+    uint8_t* atom = tile + T::oK + (size_t)(dc / 4) * (kGroup * 128);
+    *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4))) = h0;
+    *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4) + 1)) = h1;
+  }
+  // V: (page, dim) -> 16 keys of [D][32 keys] (SW64)
+  for (int i = tid; i < kPagesPG * D; i += 256) {
+    const int pg = i / D, d = i % D;
+    uint4 c = make_uint4(0, 0, 0, 0);
+    if (blk[pg] >= 0) c = __ldg(reinterpret_cast<const uint4*>(p.v_cache + ((size_t)blk[pg] * Hkv + kvh) * (D * kBS)) + d);
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+    uint32_t w[8];
+#pragma unroll
+    for (int e2 = 0; e2 < 8; ++e2) {
+      uint32_t half[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int e = 2 * e2 + u, key = pg * kBS + e;
+        half[u] = key0 + key < H ? bf16x2_bits(__fmul_rn(s8_at(cw, e), s_sv[key]), 0.f) & 0xffffu : vrows[key][d];
+      }
+      w[e2] = half[0] | (half[1] << 16);
+    }
+    *reinterpret_cast<uint4*>(tile + T::oV + swz_chunk<64>(d, 2 * pg)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(tile + T::oV + swz_chunk<64>(d, 2 * pg + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// kBF: the high-precision variant -- bf16 query and tiles, no scales, and
+// the probabilities go to the PV MMA as bf16 p~ (no group quantization).
+template <int D, bool kBF>
+__global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p) {
   using Ly = Lay<D>;
   using T = Tile<D>;
   constexpr int DH = D / 2;  // output dims per warpgroup
@@ -276,13 +386,22 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
     for (int i = tid; i < kRows * CH; i += kThreads) {
       const int rr = i / CH, dc = i % CH;
       const int r = r0 + rr;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < R) {
-        const int j = r / G, hq = kvh * G + r % G;
-        v = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)j * Hq + hq) * D) + dc);
+      uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+      if constexpr (kBF) {
+        if (r < R) {
+          const int j = r / G, hq = kvh * G + r % G;
+          const uint4* src = reinterpret_cast<const uint4*>(p.qb + ((size_t)j * Hq + hq) * D) + 2 * dc;
+          h0 = __ldg(src);
+          h1 = __ldg(src + 1);
+        }
+      } else {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < R) {
+          const int j = r / G, hq = kvh * G + r % G;
+          v = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)j * Hq + hq) * D) + dc);
+        }
+        s8x16_to_f16(v, h0, h1);
       }
-      uint4 h0, h1;
-      s8x16_to_f16(v, h0, h1);
       uint8_t* atom = q16 + (size_t)(dc / 4) * (kRows * 128);
       *reinterpret_cast<uint4*>(atom + swz_chunk<128>(rr, 2 * (dc % 4))) = h0;
       *reinterpret_cast<uint4*>(atom + swz_chunk<128>(rr, 2 * (dc % 4) + 1)) = h1;
@@ -312,8 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
       // Whichever of the next QK and the next PV has its operands first is
       // issued; the checks never suspend (test_wait), a pass with nothing to
       // issue sleeps briefly, and the same time limit as pwait applies.
-      constexpr uint32_t idesc_qk = umma_idesc_f16(kRows, kGroup);
-      constexpr uint32_t idesc_pv = umma_idesc_f16(kRows, D);
+      constexpr uint32_t idesc_qk = kBF ? umma_idesc_bf16(kRows, kGroup) : umma_idesc_f16(kRows, kGroup);
+      constexpr uint32_t idesc_pv = kBF ? umma_idesc_bf16(kRows, D) : umma_idesc_f16(kRows, D);
       const uint32_t q16 = smem_u32(smem + Ly::oQ);
       const uint32_t tiles = smem_u32(smem + Ly::oTile);
       int nq = 0, np = 0;  // next QK, next PV
@@ -379,7 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
     const int j = valid ? r / G : 0, hq = kvh * G + (valid ? r % G : 0);
     const int lim = valid ? H + j : -1;  // last visible key
     // score in log2 units: acc x sQ x scale x log2(e) x sK
-    const float c2 = valid ? __fmul_rn(__fmul_rn(p.q_scale[(size_t)j * Hq + hq], p.sm_scale), kLog2e) : 0.f;
+    const float c2 = !valid ? 0.f
+                     : kBF  ? __fmul_rn(p.sm_scale, kLog2e)
+                            : __fmul_rn(__fmul_rn(p.q_scale[(size_t)j * Hq + hq], p.sm_scale), kLog2e);
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     float* stats = reinterpret_cast<float*>(smem + Ly::oSt);  // [slot][m_g | sW | l_g][row]
     float o[DH];
@@ -395,13 +516,40 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
       tc_fence_after();
       float s[32];
       tmem_ld32(trow + 32 * sl, s);
+      const int key0 = g * kGroup;
+      const bool full = __all_sync(0xffffffffu, key0 + kGroup - 1 <= lim);  // no key of the warp is masked
+      float mg, lg = 0.f, sw = 0.f;
+      uint32_t pk[16];
+      if constexpr (kBF) {
+        tmem_wait_ld();
+#pragma unroll
+        for (int t = 0; t < 32; ++t) s[t] = __fmul_rn(s[t], c2);
+        if (!full) {
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            if (key0 + t > lim) s[t] = -INFINITY;
+        }
+        mg = tree_max(s);
+        if (mg != -INFINITY) {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) s[t] = ex2(__fsub_rn(s[t], mg));  // p~; 0 for a masked key
+          lg = tree_sum(s);
+          sw = 1.f;
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) s[t] = 0.f;
+        }
+        tc_fence_before();
+        mbar_arrive(&s_free[sl]);  // S is read; QK(g + 2) may overwrite it
+        // p~ as bf16, two per register (low half = the even key)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = bf16x2_bits(s[2 * i], s[2 * i + 1]);
+      } else {
       pwait(&tile_full[g % kStages], (g / kStages) & 1, abort_flag);  // the group's scales (already landed)
       const float4* sk4 =
           reinterpret_cast<const float4*>(smem + Ly::oTile + (size_t)(g % kStages) * T::kSlot + T::oSk);
       const float4* sv4 = sk4 + kGroup / 4;
       tmem_wait_ld();
-      const int key0 = g * kGroup;
-      const bool full = __all_sync(0xffffffffu, key0 + kGroup - 1 <= lim);  // no key of the warp is masked
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float4 k4 = sk4[i];
@@ -415,8 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
         for (int t = 0; t < 32; ++t)
           if (key0 + t > lim) s[t] = -INFINITY;
       }
-      const float mg = tree_max(s);
-      float lg = 0.f, A = 0.f;
+      mg = tree_max(s);
+      float A = 0.f;
       if (mg != -INFINITY) {
 #pragma unroll
         for (int t = 0; t < 32; ++t) s[t] = ex2(__fsub_rn(s[t], mg));  // p~; 0 for a masked key
@@ -440,8 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
       mbar_arrive(&s_free[sl]);  // S is read; QK(g + 2) may overwrite it
       // sW = A / 127 and the codes round(W / sW), both IEEE fp32 quotients (W / sW
       // by Markstein's method); W / sW <= A / RN(A / 127) < 127.5, no clamp needed
-      const float sw = div127(A);
-      uint32_t pk[16];
+      sw = div127(A);
       if (A > 0.f) {
         div_row(s, sw, __frcp_rn(sw));
         // round-half-even(q) + 1024 as the f16 bit pattern 0x6400 + code, from the
@@ -459,7 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = 0u;
       }
-      // Wq (f16) -> the PV A tile, row `row`; then the row statistics
+      }
+      // Wq (f16) or p~ (bf16) -> the PV A tile, row `row`; then the row statistics
       if (g >= 2) pwait(&pv_done[sl], ((g - 2) >> 1) & 1, abort_flag);  // PV(g-2) has read the slot
       uint8_t* p16 = smem + Ly::oP + (size_t)sl * Ly::kP16;
 #pragma unroll
@@ -541,16 +689,17 @@ __global__ void __launch_bounds__(kThreads, 1) int8_prefix_kernel(PrefixParams p
   }
 }
 
-template <int D>
+template <int D, bool kBF>
 cudaError_t launch_prefix_d(const PrefixParams& p, cudaStream_t stream) {
   const int ngt = (p.H + p.C + kGroup - 1) / kGroup;
-  cudaError_t e = launch_pdl(prefix_tiles_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p);
+  cudaError_t e = kBF ? launch_pdl(prefix_tiles_bf16_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p)
+                      : launch_pdl(prefix_tiles_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(int8_prefix_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kTotal);
+  e = cudaFuncSetAttribute(prefix_attn_kernel<D, kBF>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kTotal);
   if (e != cudaSuccess) return e;
   const int R = p.C * p.G;
-  return launch_pdl(int8_prefix_kernel<D>, dim3((R + kRows - 1) / kRows, p.Hkv), dim3(kThreads), Lay<D>::kTotal,
-                    stream, p);
+  return launch_pdl(prefix_attn_kernel<D, kBF>, dim3((R + kRows - 1) / kRows, p.Hkv), dim3(kThreads),
+                    Lay<D>::kTotal, stream, p);
 }
 
 }  // namespace
@@ -561,7 +710,11 @@ size_t prefix_workspace_bytes(int H, int C, int Hkv, int D) {
 }
 
 cudaError_t launch_int8_prefix(const PrefixParams& p, cudaStream_t stream) {
-  return p.D == 256 ? launch_prefix_d<256>(p, stream) : launch_prefix_d<128>(p, stream);
+  return p.D == 256 ? launch_prefix_d<256, false>(p, stream) : launch_prefix_d<128, false>(p, stream);
+}
+
+cudaError_t launch_bf16_prefix(const PrefixParams& p, cudaStream_t stream) {
+  return p.D == 256 ? launch_prefix_d<256, true>(p, stream) : launch_prefix_d<128, true>(p, stream);
 }
 
 }  // namespace i8kv
