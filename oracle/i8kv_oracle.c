@@ -312,22 +312,25 @@ static inline double score_of(int32_t acc, float sq, float sk, double c, int fp3
 }
 
 /* One 32-token probability group ([PV] §1, §2.2, §3):
- *   A = max W over the group, sW = A / 127, Wq = round(W / sW),
- *   o[d] += sW * sum_t Wq_t * Vq_t[d]   (int32 contraction, rescaled to float).
- * W >= 0 here, so Wq lies in [0, 127].  A == 0 gives Wq = 0. */
+ *   A = max W over the group, sW = A / pmax, Wq = round(W / sW),
+ *   o[d] += sW * sum_t Wq_t * Vq_t[d]   (integer contraction, rescaled to float).
+ * W >= 0 here, so Wq lies in [0, pmax].  A == 0 gives Wq = 0.  pmax = 127 is
+ * the pages' signed INT8 probability code; pmax = 255 is the UINT8 code that
+ * [PV] §6 weighs (probabilities are non-negative, so 0..255 gains one bit)
+ * and leaves unbuilt for want of a mixed-sign MMA. */
 static void pv_group(const double* W, int n, const int8_t* const* vrows, int D, int fp32, double weight, double* o,
-                     int8_t* trace_wq, double* trace_sw) {
+                     int16_t* trace_wq, double* trace_sw, int pmax) {
   double A = 0.0;
   for (int i = 0; i < n; ++i)
     if (W[i] > A) A = W[i];
-  double sW = R(A / 127.0, fp32);
+  double sW = R(A / (double)pmax, fp32);
   int wq[64];
   for (int i = 0; i < n; ++i) {
     double r = (A > 0.0) ? rne(R(W[i] / sW, fp32)) : 0.0;
-    if (r > 127.0) r = 127.0;
-    if (r < -127.0) r = -127.0;
+    if (r > (double)pmax) r = (double)pmax;
+    if (r < 0.0) r = 0.0;
     wq[i] = (int)r;
-    if (trace_wq) trace_wq[i] = (int8_t)wq[i];
+    if (trace_wq) trace_wq[i] = (int16_t)wq[i];
     if (trace_sw) trace_sw[i] = sW;
   }
   for (int d = 0; d < D; ++d) {
@@ -358,8 +361,9 @@ int orc_decode_attn(double* out, const int8_t* q_i8, const float* q_scale, const
                     const int8_t* v_cache, const float* k_scale, const float* v_scale, const int32_t* block_tables,
                     const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int bs, int max_blocks,
                     float softmax_scale, int partition, int group, int fp32_decisions, int nthreads, int trace_b,
-                    int trace_h, double* tr_W, int8_t* tr_Wq, double* tr_sW, double* tr_c) {
-  if (Hq % Hkv != 0 || D % 16 != 0 || group <= 0 || group > 64 || partition <= 0 || partition % group != 0)
+                    int trace_h, double* tr_W, int16_t* tr_Wq, double* tr_sW, double* tr_c, int pmax) {
+  if (Hq % Hkv != 0 || D % 16 != 0 || group <= 0 || group > 64 || partition <= 0 || partition % group != 0 ||
+      (pmax != 127 && pmax != 255))
     return ORC_BAD_ARG;
   const int G = Hq / Hkv;
   const int fp32 = fp32_decisions;
@@ -419,7 +423,7 @@ int orc_decode_attn(double* out, const int8_t* q_i8, const float* q_scale, const
             vrows[i] = vbuf + (size_t)i * D;
           }
           pv_group(W + (j0 - t0), n, vrows, D, fp32, 1.0, o_g + (size_t)g * D, tracing ? tr_Wq + j0 : NULL,
-                   tracing ? tr_sW + j0 : NULL);
+                   tracing ? tr_sW + j0 : NULL, pmax);
           if (tracing)
             for (int i = 0; i < n; ++i) tr_W[j0 + i] = W[j0 - t0 + i];
         }
@@ -511,7 +515,7 @@ int orc_prefix_attn(double* out, const int8_t* q_i8, const float* q_scale, const
             gather_v(vbuf + (size_t)i * D, v_cache, block_table[t / bs], kvh, t % bs, Hkv, D, bs);
             vrows[i] = vbuf + (size_t)i * D;
           }
-          pv_group(W + (j0 - k0), n, vrows, D, fp32, 1.0, o, NULL, NULL);
+          pv_group(W + (j0 - k0), n, vrows, D, fp32, 1.0, o, NULL, NULL, 127);
         }
         m = m_new;
       }

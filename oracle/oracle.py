@@ -70,7 +70,7 @@ def _load():
                                                     ctypes.c_float, P, P]
             lib.orc_qk_i32.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I]
             lib.orc_decode_attn.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float,
-                                            I, I, I, I, I, I, P, P, P, P]
+                                            I, I, I, I, I, I, P, P, P, P, I]
             lib.orc_prefix_attn.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, I,
                                             P, I, I, I]
             lib.orc_bf16_kv_write.argtypes = [P, P, P, I, I, I, I, P, P]
@@ -220,9 +220,11 @@ def qk_i32(q_i8, k_cache, block_tables, seq_lens, Hkv, block_size, max_len=None)
 
 # --------------------------------------------------------------------------- decode
 def decode_attn(q_i8, q_scale, cache, block_tables, seq_lens, block_size, softmax_scale=None,
-                partition=PARTITION, group=GROUP, fp32_decisions=True, nthreads=0, trace=None):
+                partition=PARTITION, group=GROUP, fp32_decisions=True, nthreads=0, trace=None, pmax=127):
     """Literal decode ([PV] §2.2): 256-token partitions, LSE merge.  Returns out [B,Hq,D] fp64.
 
+    pmax: the probability code range, 127 (signed INT8, the pages' kernels) or
+    255 (UINT8 probabilities, [PV] §6).
     trace=(b, h) additionally returns per-token arrays W, Wq, sW, c (see the C file)."""
     lib = _load()
     q_i8 = np.ascontiguousarray(q_i8, np.int8)
@@ -238,12 +240,12 @@ def decode_attn(q_i8, q_scale, cache, block_tables, seq_lens, block_size, softma
     tr = None
     if trace is not None:
         L = int(sl[tb])
-        tr = dict(W=np.zeros(L), Wq=np.zeros(L, np.int8), sW=np.zeros(L), c=np.zeros(L))
+        tr = dict(W=np.zeros(L), Wq=np.zeros(L, np.int16), sW=np.zeros(L), c=np.zeros(L))
     rc = lib.orc_decode_attn(_p(out), _p(q_i8), _p(qs), _p(cache["k_cache"]), _p(cache["v_cache"]),
                              _p(cache["k_scale"]), _p(cache["v_scale"]), _p(bt), _p(sl), B, Hq, Hkv, D,
                              block_size, bt.shape[1], softmax_scale, partition, group, int(fp32_decisions),
                              nthreads, tb, th, _p(tr["W"]) if tr else None, _p(tr["Wq"]) if tr else None,
-                             _p(tr["sW"]) if tr else None, _p(tr["c"]) if tr else None)
+                             _p(tr["sW"]) if tr else None, _p(tr["c"]) if tr else None, int(pmax))
     _check(rc, "decode_attn")
     return (out, tr) if trace is not None else out
 
@@ -356,8 +358,9 @@ def attention_fp64(q, k, v, kv_lens, softmax_scale=None):
     return out
 
 
-def group_form(scores: np.ndarray, sV: np.ndarray, Vq: np.ndarray, group: int = GROUP) -> np.ndarray:
-    """Closed group form for one query row in fp64 (see module docstring).
+def group_form(scores: np.ndarray, sV: np.ndarray, Vq: np.ndarray, group: int = GROUP, pmax: int = 127) -> np.ndarray:
+    """Closed group form for one query row in fp64 (see module docstring; pmax
+    replaces 127 for the UINT8 probability codes).
 
     scores [L] fp64, sV [L], Vq [L, D] int -> O [D]."""
     c = scores.max()
@@ -369,6 +372,6 @@ def group_form(scores: np.ndarray, sV: np.ndarray, Vq: np.ndarray, group: int = 
         A = wj.max()
         if A == 0:
             continue
-        wq = np.rint(wj / (A / 127.0))
-        num += (A / 127.0) * (wq @ Vq[j0:j0 + group].astype(np.float64))
+        wq = np.rint(wj / (A / pmax))
+        num += (A / pmax) * (wq @ Vq[j0:j0 + group].astype(np.float64))
     return num / e.sum()

@@ -132,13 +132,15 @@ def test_decode_group_constant_scores_exact(fp32):
 
 
 # --------------------------------------------------------------------------- invariants
-def test_partition_merge_invariance():
+@pytest.mark.parametrize("pmax", [127, 255])
+def test_partition_merge_invariance(pmax):
     # fp64 decisions: partitioned decode + LSE merge == one pass == the closed group form
+    # (signed INT8 probability codes, and the UINT8 codes 0..255)
     w = _small_decode([1000, 777, 64, 5], Hq=6, Hkv=2, D=64, seed=7)
     cache = oracle_decode_cache(w)
     q_i8, q_s = oracle_query(w)
     outs = [orc.decode_attn(q_i8, q_s, cache, w.block_tables, w.seq_lens, w.block_size, partition=p,
-                            fp32_decisions=False) for p in (32, 64, 256, 512, 1024)]
+                            fp32_decisions=False, pmax=pmax) for p in (32, 64, 256, 512, 1024)]
     for o in outs[1:]:
         np.testing.assert_allclose(o, outs[0], rtol=0, atol=1e-12)
     c = 1.0 / np.sqrt(64.0)
@@ -147,11 +149,12 @@ def test_partition_merge_invariance():
         Kt, Vt, sK, sV = gather_int8(cache, w.block_tables[b], L, w.Hkv, w.D)
         for h in range(w.Hq):
             s = (Kt[:, h // 3].astype(np.int64) @ q_i8[b, h].astype(np.int64)) * float(q_s[b, h]) * sK[:, h // 3] * c
-            g = orc.group_form(s, sV[:, h // 3].astype(np.float64), Vt[:, h // 3])
+            g = orc.group_form(s, sV[:, h // 3].astype(np.float64), Vt[:, h // 3], pmax=pmax)
             np.testing.assert_allclose(outs[0][b, h], g, rtol=0, atol=1e-12)
 
 
-def test_decode_error_decomposition_and_bound():
+@pytest.mark.parametrize("pmax", [127, 255])
+def test_decode_error_decomposition_and_bound(pmax):
     # O - O_hat = sum_t P_t eV_t + sum_t c_g(t) eW_t Vq_t   with eV = V - sV Vq,
     # eW = W - sW Wq, P_t = c_g(t) * (partition-normalized P_t), for the oracle's
     # own W/Wq/sW trace; plus the a-priori bound |eV| <= sV/2, |eW| <= sW/2.
@@ -160,7 +163,7 @@ def test_decode_error_decomposition_and_bound():
     q_i8, q_s = oracle_query(w)
     b, h = 0, 3
     out, tr = orc.decode_attn(q_i8, q_s, cache, w.block_tables, w.seq_lens, w.block_size,
-                              fp32_decisions=True, trace=(b, h))
+                              fp32_decisions=True, trace=(b, h), pmax=pmax)
     L = 700
     kvh = h // 2
     Kt, Vq, sK, sV = gather_int8(cache, w.block_tables[b], L, w.Hkv, w.D)
@@ -189,7 +192,34 @@ def test_decode_error_decomposition_and_bound():
     for j0 in range(0, L, 32):
         assert np.unique(tr["sW"][j0:j0 + 32]).size == 1
         Wg = tr["W"][j0:j0 + 32]
-        assert tr["Wq"][j0 + int(np.argmax(Wg))] == 127
+        assert tr["Wq"][j0 + int(np.argmax(Wg))] == pmax
+        assert tr["Wq"][j0:j0 + 32].min() >= 0
+
+
+def test_uint8_codes_halve_the_probability_error():
+    # With V exact (integer V, sV = 1 so eV = 0) the only error left is the
+    # probability rounding, bounded by sW / 2 per token; sW = A / 255 is half of
+    # A / 127, so the UINT8 codes' error must come out clearly smaller.
+    L, Hq, Hkv, D = 2000, 4, 1, 64
+    w = _small_decode([L], Hq=Hq, Hkv=Hkv, D=D, seed=21)
+    rng = np.random.default_rng(22)
+    k, _ = w.kv(0)
+    v = _integer_v(rng, L, Hkv, D)
+    cache = orc.kv_quant_write(k, wl.bf16_bits(v), w.slots(0), w.num_blocks, w.block_size)
+    q_i8, q_s = oracle_query(w)
+    Kt, Vt, sK, sV = gather_int8(cache, w.block_tables[0], L, Hkv, D)
+    c = float(np.float32(1) / np.sqrt(np.float32(D)))
+    errs = {}
+    for pmax in (127, 255):
+        out = orc.decode_attn(q_i8, q_s, cache, w.block_tables, w.seq_lens, w.block_size, fp32_decisions=False,
+                              pmax=pmax)
+        e = []
+        for h in range(Hq):
+            s = (Kt[:, 0].astype(np.int64) @ q_i8[0, h].astype(np.int64)) * float(q_s[0, h]) * sK[:, 0] * c
+            p = np.exp(s - s.max())
+            e.append(np.abs(out[0, h] - (p / p.sum()) @ (Vt[:, 0] * sV[:, 0, None]).astype(np.float64)))
+        errs[pmax] = np.mean(e)
+    assert errs[255] < 0.7 * errs[127], errs
 
 
 # --------------------------------------------------------------------------- prefix
