@@ -401,6 +401,10 @@ def run_ours(args):
         if not args.quick:
             secondary.update(run_secondary(torch, i8, hbm_peak))
             try:
+                secondary["decode_u8_probs_by_history"] = run_u8p_comparison(torch, i8, hbm_peak)
+            except Exception as e:  # pragma: no cover - report, do not hide
+                secondary["decode_u8_probs_by_history"] = {"error": str(e)[:200]}
+            try:
                 secondary["bf16_kv_decode_by_history"] = run_bf16_comparison(
                     torch, i8, hbm_peak, {L: v * 1e3 for L, v in by_len.items()})
             except Exception as e:  # pragma: no cover - report, do not hide
@@ -536,6 +540,39 @@ def run_bf16_comparison(torch, i8, hbm_peak, int8_us: dict):
         gbs = w.kv_bytes_bf16() / (ms / 1e3) / 1e9
         res[str(L)] = {"us": ms * 1e3, "gb_s": gbs, "frac_hbm": gbs / hbm_peak,
                        "int8_speedup": (ms * 1e3) / int8_us[L] if L in int8_us else None}
+        del caches
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_u8p_comparison(torch, i8, hbm_peak):
+    """Decode with UINT8 probability codes against the signed codes, each timed
+    the same way (rotating cache copies past L2, one graph): µs and the ratio."""
+    res = {}
+    for L in HISTORIES:
+        w = wl.decode_outlier(L)
+        k, v = w.kv(0)
+        base = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+        i8.kv_quant_write(to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.slots(0)), **base)
+        copies = max(2, int(np.ceil(400e6 / w.kv_bytes_int8())))
+        caches = [{n: t.clone() for n, t in base.items()} for _ in range(copies)]
+        del base
+        q_i8 = torch.empty((1, w.Hq, w.D), dtype=torch.int8, device="cuda")
+        q_s = torch.empty((1, w.Hq), dtype=torch.float32, device="cuda")
+        dummy = torch.zeros((1, w.Hkv, w.D), dtype=torch.bfloat16, device="cuda")
+        i8.kv_quant_write(dummy, dummy, torch.full((1,), -1, dtype=torch.int32, device="cuda"), **caches[0],
+                          q=to_dev(torch, w.q()), q_i8=q_i8, q_scale=q_s)
+        out = torch.empty((1, w.Hq, w.D), dtype=torch.float32, device="cuda")
+        ws = i8.decode_workspace(1, w.Hq, w.Hkv, w.D, w.block_tables.shape[1])
+        bt, sl = to_dev(torch, w.block_tables), to_dev(torch, w.seq_lens)
+        r = {}
+        for name, u8 in (("s8_codes", False), ("u8_codes", True)):
+            calls = [(lambda c=c, u8=u8: i8.int8_paged_decode_attn(out, q_i8, q_s, c["k_cache"], c["v_cache"],
+                                                                   c["k_scale"], c["v_scale"], bt, sl, ws,
+                                                                   u8_probs=u8)) for c in caches]
+            r[name + "_us"] = time_rotating(torch, calls, 20) * 1e3
+        r["u8_over_s8_time"] = r["u8_codes_us"] / r["s8_codes_us"]
+        res[str(L)] = r
         del caches
         torch.cuda.empty_cache()
     return res

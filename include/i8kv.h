@@ -167,6 +167,21 @@ i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const fl
                                         int partition, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* The same decode with UINT8 probability codes ([PV] §6 weighs them: the   */
+/* weights W = P x sV are non-negative, so codes 0..255 carry one bit more   */
+/* than the signed 0..127; the pages leave the variant for want of a         */
+/* mixed-sign MMA).  Per 32-token group sW = fp32(A / 255) and              */
+/* Wq = round-half-even(W / sW) in 0..255; PV = Wq x Vq on the s8 x u8 MMA   */
+/* (exact int32).  Arguments, layouts and workspace as above.                */
+/* ------------------------------------------------------------------------ */
+i8kv_status i8kv_int8_paged_decode_attn_u8p(float* out, const int8_t* q_i8, const float* q_scale,
+                                            const int8_t* k_cache, const int8_t* v_cache, const float* k_scale,
+                                            const float* v_scale, const int32_t* block_tables,
+                                            const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
+                                            int max_blocks, int num_blocks, float softmax_scale, int partition,
+                                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Allocation-free variant of i8kv_int8_paged_decode_attn.  The pages have   */
 /* no counterpart: this entry point exists for callers that cannot allocate   */
 /* device memory when they run a decode step -- for example a plugin inside  */

@@ -43,6 +43,8 @@ _SIGS = {
     "i8kv_decode_workspace_bytes": [_I, _I, _I, _I, _I, _I, _I],
     "i8kv_int8_paged_decode_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z,
                                     _P],
+    "i8kv_int8_paged_decode_attn_u8p": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P,
+                                        _Z, _P],
     "i8kv_int8_decode_step": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P],
     "i8kv_int8_paged_decode_attn_noalloc": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                             _P],
@@ -215,11 +217,15 @@ def decode_workspace(B: int, Hq: int, Hkv: int, D: int, max_blocks: int, device=
 
 
 def int8_paged_decode_attn(out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
-                           workspace, softmax_scale: float = 0.0, partition: int = PARTITION, stream=None):
-    """out [B, Hq, D] fp32 <- INT8 paged decode attention of q_i8 [B, Hq, D] over the cache."""
+                           workspace, softmax_scale: float = 0.0, partition: int = PARTITION, stream=None,
+                           u8_probs: bool = False):
+    """out [B, Hq, D] fp32 <- INT8 paged decode attention of q_i8 [B, Hq, D] over the cache.
+
+    u8_probs: UINT8 probability codes (0..255, sW = A / 255, s8 x u8 MMA) instead of 0..127."""
     NB, Hkv, D = _cache_geom(k_cache, 16)
     B, Hq, _ = q_i8.shape
-    _check(lib().i8kv_int8_paged_decode_attn(
+    fn = lib().i8kv_int8_paged_decode_attn_u8p if u8_probs else lib().i8kv_int8_paged_decode_attn
+    _check(fn(
         _ptr(out, torch.float32, "out"), _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
         _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
         _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),

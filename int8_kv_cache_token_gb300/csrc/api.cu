@@ -224,6 +224,22 @@ i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const fl
   return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "int8 decode launch");
 }
 
+i8kv_status i8kv_int8_paged_decode_attn_u8p(float* out, const int8_t* q_i8, const float* q_scale,
+                                            const int8_t* k_cache, const int8_t* v_cache, const float* k_scale,
+                                            const float* v_scale, const int32_t* block_tables,
+                                            const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
+                                            int max_blocks, int num_blocks, float softmax_scale, int partition,
+                                            void* workspace, size_t workspace_bytes, void* stream) {
+  REQUIRE(q_scale != nullptr, I8KV_ERR_INVALID_ARG, "q_scale is NULL");
+  i8kv::DecodeParams p{};
+  i8kv_status s = decode_common(p, q_i8, q_scale, true, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
+                                B, Hq, Hkv, D, block_size, max_blocks, num_blocks, softmax_scale, partition,
+                                workspace, workspace_bytes, out);
+  if (s != I8KV_OK || B == 0) return s;
+  p.u8_probs = 1;
+  return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "int8 decode (u8 P) launch");
+}
+
 i8kv_status i8kv_int8_decode_step(float* out, const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
                                   int8_t* k_cache, int8_t* v_cache, float* k_scale, float* v_scale,
                                   const int32_t* block_tables, const int32_t* seq_lens, int B, int Hq, int Hkv, int D,

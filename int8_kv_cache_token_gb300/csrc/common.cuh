@@ -189,6 +189,15 @@ __device__ __forceinline__ void mma_s8_16832(int (&d)[4], const uint32_t (&a)[4]
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The same with unsigned 8-bit B (codes 0..255): s8 x u8 -> exact s32.
+__device__ __forceinline__ void mma_s8u8_16832(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.s8.u8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 // D = A(16x16 bf16, row) * B(16x8 bf16, col) + C, fp32 accumulate.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -469,6 +478,17 @@ __device__ __forceinline__ float div127(float a) {
   const float y = 0.0078740157f;  // RN(1/127)
   const float q = __fmul_rn(a, y);
   const float r = __fmaf_rn(-127.0f, q, a);
+  return __fmaf_rn(r, y, q);
+}
+
+// a / 255 correctly rounded, the same method with RN(1/255) (the UINT8
+// probability scale); the same exhaustive check covers it.
+static __device__ __noinline__ float div255_tiny(float a) { return __fdiv_rn(a, 255.0f); }
+__device__ __forceinline__ float div255(float a) {
+  if (a < kTinyDivisor) return div255_tiny(a);
+  const float y = 0x1.010102p-8f;  // RN(1/255)
+  const float q = __fmul_rn(a, y);
+  const float r = __fmaf_rn(-255.0f, q, a);
   return __fmaf_rn(r, y, q);
 }
 

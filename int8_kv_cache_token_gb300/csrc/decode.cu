@@ -409,10 +409,14 @@ __device__ __forceinline__ void load_q_frags_smem(const uint8_t* qa, int G, int 
 // the BF16-KV comparison (plain softmax, bf16 P x V, no scales).  STEP (INT8
 // only): the decode step, which also quantizes and writes each sequence's new
 // token and quantizes the query; a separate instantiation, so the plain decode
-// carries none of that code.
-template <int D, bool BF16, bool STEP = false>
+// carries none of that code.  U8P (INT8 only): UINT8 probability codes --
+// sW = A / 255, Wq in 0..255, PV on the s8 x u8 MMA (|PV| <= 32 x 255 x 127,
+// still exact in fp32); the pages' notes on PV weigh this variant and leave it
+// for want of a mixed-sign MMA, which sm_103a's mma.sync has.
+template <int D, bool BF16, bool STEP = false, bool U8P = false>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int nslots) {
   static_assert(!(STEP && BF16), "the decode step is INT8 only");
+  static_assert(!(U8P && (BF16 || STEP)), "UINT8 probabilities: plain INT8 decode only");
   using Gm = Geo<D, BF16>;
   constexpr int kUnit = Gm::kUnit, kBlocksU = Gm::kBlocksU, kPage = Gm::kPage, kSlot = Gm::kSlot;
   constexpr int kGran = Gm::kGran;
@@ -932,10 +936,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         // sW = A / 127 and the codes round(W / sW), both IEEE fp32 quotients
         // (W / sW by Markstein's method, one reciprocal per row); codes ->
         // [row][token] bytes, read back below as PV B fragments.
-        // W / sW <= A / RN(A / 127) < 127.5, so no code needs clamping.
+        // W / sW <= A / RN(A / 127) < 127.5 (A / RN(A / 255) < 255.5), so no
+        // code needs clamping; the low byte is the code either way.
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          swv[r] = div127(A[r]);
+          swv[r] = U8P ? div255(A[r]) : div127(A[r]);
           // this lane's values of row 2t + r: (block m, token g + 8 h) at e = r + 2 h
           float x[4] = {w[0][r], w[0][r + 2], w[1][r], w[1][r + 2]};
           if (A[r] > 0.f) {
@@ -1102,8 +1107,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
           uint32_t a[4];
           ldmatrix_x4(a, vrow + dt * 16 * 16);
           int pv[4] = {0, 0, 0, 0};
-          mma_s8_16832(pv, a, f.x, f.y);
-          o[dt][0] = fmaf((float)pv[0], fs[q][0], o[dt][0]);  // |pv| <= 32 * 127^2: exact in fp32
+          if constexpr (U8P)
+            mma_s8u8_16832(pv, a, f.x, f.y);
+          else
+            mma_s8_16832(pv, a, f.x, f.y);
+          o[dt][0] = fmaf((float)pv[0], fs[q][0], o[dt][0]);  // |pv| <= 32 * 255 * 127 < 2^24: exact in fp32
           o[dt][1] = fmaf((float)pv[1], fs[q][1], o[dt][1]);
           o[dt][2] = fmaf((float)pv[2], fs[q][0], o[dt][2]);
           o[dt][3] = fmaf((float)pv[3], fs[q][1], o[dt][3]);
@@ -1368,7 +1376,7 @@ int pick_slots(int smem_limit) {
   return 0;
 }
 
-template <int D, bool BF16, bool STEP>
+template <int D, bool BF16, bool STEP, bool U8P = false>
 cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1377,14 +1385,14 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   const size_t smem = decode_layout<D, BF16>(ns).total;
   // Raise the dynamic shared-memory limit once per device (to the opt-in
   // maximum), so that launches captured into a CUDA graph make no attribute call.
-  static int attr_set[64] = {0};
+  static int attr_set[64] = {0};  // per instantiation
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16, STEP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16, STEP, U8P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          max_smem_optin(dev));
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
-  cudaError_t e = launch_pdl(decode_kernel<D, BF16, STEP>, dim3(p.grid), dim3(kThreads), smem, stream, p, ns);
+  cudaError_t e = launch_pdl(decode_kernel<D, BF16, STEP, U8P>, dim3(p.grid), dim3(kThreads), smem, stream, p, ns);
   if (e != cudaSuccess) return e;
   return launch_pdl(decode_merge_kernel<D, BF16>, dim3(p.B * p.Hkv * p.G), dim3(kMergeThreads), 0, stream, p);
 }
@@ -1410,6 +1418,10 @@ cudaError_t launch_int8_decode(const DecodeParams& p, cudaStream_t stream) {
   if (p.step) {
     if (p.D == 256) return launch_decode_d<256, false, true>(p, stream);
     return launch_decode_d<128, false, true>(p, stream);
+  }
+  if (p.u8_probs) {
+    if (p.D == 256) return launch_decode_d<256, false, false, true>(p, stream);
+    return launch_decode_d<128, false, false, true>(p, stream);
   }
   if (p.D == 256) return launch_decode_d<256, false, false>(p, stream);
   return launch_decode_d<128, false, false>(p, stream);

@@ -52,6 +52,7 @@ struct DecodeParams {
   // kernel -- K/V written into the cache, Q quantized per warp -- instead of
   // being read from q / the cache.
   int step;
+  int u8_probs;               // INT8 path: probability codes 0..255 (sW = A / 255) instead of 0..127
   const uint16_t* q_bf16;     // [B, Hq, D]
   const uint16_t* k_new;      // [B, Hkv, D]
   const uint16_t* v_new;      // [B, Hkv, D]

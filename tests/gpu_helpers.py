@@ -50,11 +50,11 @@ def gpu_quantize_rows(q: np.ndarray, Hkv: int, cache):
     return q_i8, q_scale
 
 
-def gpu_decode(w: wl.DecodeWorkload, cache, q_i8, q_scale, workspace=None, out=None):
+def gpu_decode(w: wl.DecodeWorkload, cache, q_i8, q_scale, workspace=None, out=None, u8_probs=False):
     if out is None:
         out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.float32, device="cuda")
     if workspace is None:
         workspace = i8.decode_workspace(w.B, w.Hq, w.Hkv, w.D, w.block_tables.shape[1])
     i8.int8_paged_decode_attn(out, q_i8, q_scale, cache["k_cache"], cache["v_cache"], cache["k_scale"],
-                              cache["v_scale"], dev(w.block_tables), dev(w.seq_lens), workspace)
+                              cache["v_scale"], dev(w.block_tables), dev(w.seq_lens), workspace, u8_probs=u8_probs)
     return out
