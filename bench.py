@@ -730,6 +730,55 @@ def run_profile_prefix(args):
     return 0
 
 
+def run_profile_first_chunk(args):
+    """High-precision first-chunk launches only, for profilers: 0 + 4096 tokens (24 q /
+    4 KV heads, head_dim 256), `--warmup` then `--steps` calls (tiles + attention)."""
+    import torch
+
+    from int8_kv_cache_token_gb300 import build as ibuild
+    ibuild.build()
+    import int8_kv_cache_token_gb300 as i8
+    w = wl.PrefixWorkload("first_chunk", 24, 4, 256, 0, 4096, seed=5)
+    k, v = w.kv()
+    kd, vd, qd = to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.q())
+    out = torch.empty((w.chunk, w.Hq, w.D), dtype=torch.float32, device="cuda")
+    pws = i8.prefix_workspace(0, w.chunk, w.Hkv, w.D)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup + args.steps):
+        i8.bf16_prefix_attn(out, qd, kd, vd, workspace=pws)
+    torch.cuda.synchronize()
+    assert i8.device_error() == 0
+    print(json.dumps({"profile": "bf16_first_chunk", "chunk": w.chunk, "launches": args.warmup + args.steps,
+                      "flops_per_launch": w.int8_ops()}))
+    return 0
+
+
+def run_profile_producer(args):
+    """Producer launches only, for profilers: 8192 tokens, 32 q / 8 KV heads, head_dim
+    128; each round launches the plain producer, then the fused one (Q/K RMSNorm and
+    full-width RoPE); `--warmup` then `--steps` rounds."""
+    import torch
+
+    from int8_kv_cache_token_gb300 import build as ibuild
+    ibuild.build()
+    import int8_kv_cache_token_gb300 as i8
+    p = wl.producer_rope_tokens()
+    cache = i8.alloc_int8_cache(p["num_blocks"], p["Hkv"], p["D"])
+    k, v, q, s, pos, cs, qw, kw = (to_dev(torch, p[n]) for n in ("k", "v", "q", "slots", "positions", "cos_sin",
+                                                              "q_norm_weight", "k_norm_weight"))
+    q_i8 = torch.empty(q.shape, dtype=torch.int8, device="cuda")
+    q_s = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    for _ in range(args.warmup + args.steps):
+        i8.kv_quant_write(k, v, s, **cache, q=q, q_i8=q_i8, q_scale=q_s)
+        i8.kv_rope_quant_write(k, v, s, **cache, positions=pos, cos_sin=cs, rotary_dim=p["rotary_dim"], q=q,
+                               q_i8=q_i8, q_scale=q_s, q_norm_weight=qw, k_norm_weight=kw)
+    torch.cuda.synchronize()
+    assert i8.device_error() == 0
+    print(json.dumps({"profile": "producer", "tokens": 8192, "rounds": args.warmup + args.steps}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -744,7 +793,15 @@ def main():
                     help="decode launches only (the three histories round-robin, --layers caches each) for ncu")
     ap.add_argument("--profile-prefix", action="store_true",
                     help="prefix-chunk launches only (16384 + 2048 chunk) for ncu")
+    ap.add_argument("--profile-first-chunk", action="store_true",
+                    help="high-precision first-chunk launches only (0 + 4096) for ncu")
+    ap.add_argument("--profile-producer", action="store_true",
+                    help="plain and fused producer launches only (8192 tokens) for ncu")
     args = ap.parse_args()
+    if args.profile_first_chunk:
+        return run_profile_first_chunk(args)
+    if args.profile_producer:
+        return run_profile_producer(args)
     if args.profile:
         return run_profile(args)
     if args.profile_prefix:
