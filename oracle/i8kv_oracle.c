@@ -213,6 +213,21 @@ static void qk_transform(const uint16_t* src, int D, const uint16_t* norm_w, flo
   if (rd > 0) rope_rotate_half(x, rd, cs);
 }
 
+/* Per-channel K smoothing (the accuracy variant for stable channel outliers in
+ * K that [KV] §2.1 points to, KIVI's observation): with factors s [Hkv, D]
+ * (fp32, > 0), after RMSNorm and RoPE the K vector of KV head h becomes
+ * k_d * RN(1/s[h][d]) and the Q vector of query head hq becomes
+ * q_d * s[hq / G][d] (G = Hq / Hkv), each product rounded once.  q.k is
+ * unchanged in exact arithmetic, the same folding the PV page applies to sV,
+ * and the per-token scales no longer see K's channel outliers.  The bf16 copies
+ * q_out / k_out are taken before the smoothing. */
+static void smooth_vec(float* x, int D, const float* f, int invert) {
+  for (int d = 0; d < D; ++d) {
+    float m = invert ? 1.0f / f[d] : f[d];
+    x[d] = x[d] * m;
+  }
+}
+
 /* The fused producer.  positions [T] and cos_sin [max_position, rd] fp32 are
  * needed when rd > 0 (rd even, <= D); rd = 0 rotates nothing.  A null norm
  * weight skips that RMSNorm.  K/V go to the cache for slot >= 0 exactly as in
@@ -225,8 +240,10 @@ int orc_kv_rope_quant_write(const uint16_t* k, const uint16_t* v, const int32_t*
                             int bs, int8_t* k_cache, int8_t* v_cache, float* k_scale, float* v_scale,
                             const uint16_t* q, int Hq, int8_t* q_i8, float* q_scale, const int32_t* positions,
                             const float* cos_sin, int max_position, int rd, const uint16_t* q_norm_w,
-                            const uint16_t* k_norm_w, float eps, uint16_t* q_out, uint16_t* k_out) {
+                            const uint16_t* k_norm_w, float eps, uint16_t* q_out, uint16_t* k_out,
+                            const float* k_smooth) {
   if (D % 16 != 0 || bs <= 0 || Hkv <= 0 || rd < 0 || rd % 2 != 0 || rd > D) return ORC_BAD_ARG;
+  if (k_smooth && q != NULL && (Hq <= 0 || Hq % Hkv != 0)) return ORC_BAD_ARG;
   if ((q_norm_w || k_norm_w) && !is_pow2(D)) return ORC_BAD_ARG;
   if (rd > 0 && (positions == NULL || cos_sin == NULL || max_position <= 0)) return ORC_BAD_ARG;
   int bad = 0;
@@ -251,6 +268,7 @@ int orc_kv_rope_quant_write(const uint16_t* k, const uint16_t* v, const int32_t*
       if (k_out)
         for (int d = 0; d < D; ++d) k_out[row + d] = f32_to_bf16(x[d]);
       if (slot < 0) continue;
+      if (k_smooth) smooth_vec(x, D, k_smooth + (size_t)h * D, 1);
       quantize_f32(x, D, tmp, &s);
       for (int d = 0; d < D; ++d) k_cache[k_index(blk, h, d, off, Hkv, D, bs)] = tmp[d];
       k_scale[s_index(blk, h, off, Hkv, bs)] = s;
@@ -264,6 +282,7 @@ int orc_kv_rope_quant_write(const uint16_t* k, const uint16_t* v, const int32_t*
       qk_transform(q + row, D, q_norm_w, eps, cs, rd, x);
       if (q_out)
         for (int d = 0; d < D; ++d) q_out[row + d] = f32_to_bf16(x[d]);
+      if (k_smooth) smooth_vec(x, D, k_smooth + (size_t)(h / (Hq / Hkv)) * D, 0);
       if (q_i8) quantize_f32(x, D, q_i8 + row, q_scale + (size_t)t * Hq + h);
     }
   }

@@ -67,7 +67,7 @@ def _load():
             lib.orc_quantize_vector.restype = None
             lib.orc_kv_quant_write.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, I, P, P]
             lib.orc_kv_rope_quant_write.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, I, P, P, P, P, I, I, P, P,
-                                                    ctypes.c_float, P, P]
+                                                    ctypes.c_float, P, P, P]
             lib.orc_qk_i32.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I]
             lib.orc_decode_attn.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float,
                                             I, I, I, I, I, I, P, P, P, P, I]
@@ -153,14 +153,16 @@ BAD_POSITION = 2   # orc_kv_rope_quant_write: some token's position was outside 
 
 def kv_rope_quant_write(k, v, slot_mapping, num_blocks, block_size, positions=None, cos_sin=None, rotary_dim=0,
                         q=None, q_norm_weight=None, k_norm_weight=None, eps=1e-6, quantize_q=True,
-                        q_out=False, k_out=False):
+                        q_out=False, k_out=False, k_smooth=None):
     """Fused producer: optional Q/K RMSNorm, RoPE (rotate-half on the first
     ``rotary_dim`` dims, table ``cos_sin`` float32 [max_position, rotary_dim]),
     then the [KV] §2.1 quantization and the paged scatter of kv_quant_write.
 
     Returns the kv_quant_write dict plus ``q_out`` / ``k_out`` (bf16 bits of the
     transformed Q / K) when asked, and ``status`` (0, or BAD_POSITION when some
-    token was skipped because its position lay outside the table)."""
+    token was skipped because its position lay outside the table).  k_smooth
+    (float32 [Hkv, D], optional): per-channel K smoothing factors -- K is
+    multiplied by RN(1/s), Q by s of its KV head, before the quantization."""
     k, v = _u16(k), _u16(v)
     T, Hkv, D = k.shape
     bs = block_size
@@ -192,10 +194,11 @@ def kv_rope_quant_write(k, v, slot_mapping, num_blocks, block_size, positions=No
         out["k_out"] = ko
     qw = None if q_norm_weight is None else _u16(q_norm_weight)
     kw = None if k_norm_weight is None else _u16(k_norm_weight)
+    ks = None if k_smooth is None else np.ascontiguousarray(k_smooth, np.float32)
     rc = _load().orc_kv_rope_quant_write(_p(k), _p(v), _p(slots), T, Hkv, D, bs, _p(out["k_cache"]),
                                          _p(out["v_cache"]), _p(out["k_scale"]), _p(out["v_scale"]), _p(q), Hq,
                                          _p(q_i8), _p(q_scale), _p(pos), _p(cs), max_pos, rotary_dim, _p(qw),
-                                         _p(kw), float(eps), _p(qo), _p(ko))
+                                         _p(kw), float(eps), _p(qo), _p(ko), _p(ks))
     if rc not in (0, BAD_POSITION):
         _check(rc, "kv_rope_quant_write")
     out["status"] = rc

@@ -61,6 +61,11 @@ MUTANTS = {
                            "const int n_keys = history_len + j;\n      const int kvh = h / G;\n      const uint16_t* qv"),
     "bf16_prefix_k_scale": ("const double sc = (double)k_scale[s_index(blk, kvh, off, Hkv, bs)];\n          for (int d = 0; d < D; ++d) kx[d]",
                             "const double sc = (double)v_scale[s_index(blk, kvh, off, Hkv, bs)];\n          for (int d = 0; d < D; ++d) kx[d]"),
+    # K smoothing: K multiplied by s instead of 1/s; query head -> KV head by modulo
+    "smooth_k_not_inverted": ("if (k_smooth) smooth_vec(x, D, k_smooth + (size_t)h * D, 1);",
+                              "if (k_smooth) smooth_vec(x, D, k_smooth + (size_t)h * D, 0);"),
+    "smooth_q_head_modulo": ("smooth_vec(x, D, k_smooth + (size_t)(h / (Hq / Hkv)) * D, 0);",
+                             "smooth_vec(x, D, k_smooth + (size_t)(h % Hkv) * D, 0);"),
 }
 
 

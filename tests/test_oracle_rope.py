@@ -254,3 +254,55 @@ def test_bad_position_skips_only_that_token():
     for key in ("q_i8", "q_scale", "k_out"):
         assert np.array_equal(r[key][good], ok[key])
         assert not r[key][[2, 4]].any()
+
+
+# --------------------------------------------------------------------------- per-channel K smoothing
+def test_unit_smoothing_changes_nothing():
+    T, Hkv, D, Hq = 20, 2, 128, 6
+    k, v, q, slots, NB = _inputs(T, Hkv, D, Hq, seed=41)
+    a = orc.kv_rope_quant_write(k, v, slots, NB, BS, q=q)
+    b = orc.kv_rope_quant_write(k, v, slots, NB, BS, q=q, k_smooth=np.ones((Hkv, D), np.float32))
+    _same(a, b, ["k_cache", "v_cache", "k_scale", "v_scale", "q_i8", "q_scale"])
+
+
+@pytest.mark.parametrize("D,Hkv,Hq", [(128, 2, 6), (256, 4, 4)])
+def test_power_of_two_smoothing_is_exact_channel_scaling(D, Hkv, Hq):
+    # s = 2^e per (KV head, channel): K' = K 2^-e and Q' = Q 2^e exactly, so the
+    # caches must equal the plain producer's on bf16 inputs scaled channel-wise
+    # in numpy -- which fixes which factor meets which channel, that K takes 1/s
+    # and Q takes s, and that query head hq uses KV head hq / (Hq / Hkv).
+    T = 19
+    k, v, q, slots, NB = _inputs(T, Hkv, D, Hq, seed=D + Hkv)
+    e = np.random.default_rng(7).integers(-4, 5, size=(Hkv, D))
+    s = np.ldexp(np.ones((Hkv, D), np.float32), e).astype(np.float32)
+    G = Hq // Hkv
+    ks = wl.bf16_bits(wl.bf16_values(k) / s[None, :, :])
+    qs = wl.bf16_bits(wl.bf16_values(q) * np.repeat(s, G, axis=0)[None, :, :])
+    fused = orc.kv_rope_quant_write(k, v, slots, NB, BS, q=q, k_smooth=s)
+    plain = orc.kv_quant_write(ks, v, slots, NB, BS, q=qs)
+    _same(plain, fused, ["k_cache", "v_cache", "k_scale", "v_scale", "q_i8", "q_scale"])
+
+
+def test_smoothing_reduces_decode_error_on_channel_outliers():
+    # K with 4 outlier channels x20 per KV head (the decode_outlier recipe, at a
+    # shorter history): smoothing with s = sqrt(max |K_c|) per channel moves the
+    # outliers' range half into Q; the quantized decode must come out closer to
+    # fp64 attention on the unquantized values.
+    L, Hq, Hkv, D = 2048, 8, 2, 128
+    w = wl.DecodeWorkload("sm", Hq, Hkv, D, [L], seed=3, outlier_channels=4)
+    k, v = w.kv(0)
+    q = w.q()
+    slots = w.slots(0)
+    kf = wl.bf16_values(k).astype(np.float64)
+    s = np.sqrt(np.abs(kf).max(axis=0)).astype(np.float32)   # [Hkv, D]
+    errs = []
+    for ks in (None, s):
+        # history K/V through the producer; the query alone (slot -1 rows)
+        c = orc.kv_rope_quant_write(k, v, slots, w.num_blocks, BS, k_smooth=ks)
+        qq = orc.kv_rope_quant_write(np.zeros((1, Hkv, D), np.uint16), np.zeros((1, Hkv, D), np.uint16),
+                                     np.array([-1], np.int32), w.num_blocks, BS, q=q, k_smooth=ks)
+        out = orc.decode_attn(qq["q_i8"], qq["q_scale"], c, w.block_tables, w.seq_lens, BS)
+        ref = orc.attention_fp64(orc.bf16_to_f64(q), kf, wl.bf16_values(v).astype(np.float64), np.array([L]),
+                                 softmax_scale=float(np.float32(1) / np.sqrt(np.float32(D))))
+        errs.append(np.abs(out - ref).mean())
+    assert errs[1] < 0.8 * errs[0], errs
