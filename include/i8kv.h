@@ -128,14 +128,22 @@ i8kv_status i8kv_kv_quant_write(const uint16_t* k, const uint16_t* v, const int3
 /*   whatever its slot (k_out lets a high-precision path reuse the rotated K).*/
 /* A token whose position lies outside [0, max_position) is skipped entirely */
 /*   (none of its outputs is written) and the device error word records 4.   */
-/* cos_sin and the norm weights must be 16-byte aligned.                     */
+/* k_smooth (fp32 [Hkv, D], nullable, entries > 0 and finite): per-channel   */
+/*   K smoothing for stable channel outliers (KIVI's observation, cited in   */
+/*   [KV] §2.1).  After RMSNorm and RoPE, K of KV head h is multiplied by    */
+/*   RN(1/s[h][d]) and Q of query head hq by s[hq / G][d] (G = Hq / Hkv),    */
+/*   each product rounded once; q.k is unchanged in exact arithmetic (the    */
+/*   folding [PV] applies to sV), so the attention kernels need no change.   */
+/*   q_out / k_out are taken before the smoothing.                           */
+/* cos_sin, the norm weights and k_smooth must be 16-byte aligned.           */
 /* ------------------------------------------------------------------------ */
 i8kv_status i8kv_kv_rope_quant_write(const uint16_t* k, const uint16_t* v, const int32_t* slot_mapping, int T,
                                      int Hkv, int D, int block_size, int num_blocks, int8_t* k_cache, int8_t* v_cache,
                                      float* k_scale, float* v_scale, const uint16_t* q, int Hq, int8_t* q_i8,
                                      float* q_scale, const int32_t* positions, const float* cos_sin, int max_position,
                                      int rotary_dim, const uint16_t* q_norm_weight, const uint16_t* k_norm_weight,
-                                     float norm_eps, uint16_t* q_out, uint16_t* k_out, void* stream);
+                                     float norm_eps, uint16_t* q_out, uint16_t* k_out, const float* k_smooth,
+                                     void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* INT8 paged decode attention ([PV] §2-§3, [KV] §3.3).                     */

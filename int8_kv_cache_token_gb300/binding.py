@@ -39,7 +39,7 @@ _SIGS = {
     "i8kv_version": [],
     "i8kv_kv_quant_write": [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P],
     "i8kv_kv_rope_quant_write": [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _P,
-                                 _P, _F, _P, _P, _P],
+                                 _P, _F, _P, _P, _P, _P],
     "i8kv_decode_workspace_bytes": [_I, _I, _I, _I, _I, _I, _I],
     "i8kv_int8_paged_decode_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z,
                                     _P],
@@ -175,11 +175,13 @@ def kv_quant_write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, q=Non
 
 def kv_rope_quant_write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, positions=None, cos_sin=None,
                         rotary_dim: int = 0, q=None, q_i8=None, q_scale=None, q_norm_weight=None,
-                        k_norm_weight=None, norm_eps: float = 1e-6, q_out=None, k_out=None, stream=None):
+                        k_norm_weight=None, norm_eps: float = 1e-6, q_out=None, k_out=None, k_smooth=None,
+                        stream=None):
     """kv_quant_write with Q/K RMSNorm (optional bf16 weights [D]) and rotate-half
     RoPE on the first rotary_dim dims (positions int32 [T], cos_sin float32
     [max_position, rotary_dim]) applied before the quantization; q_out / k_out
-    (bf16, nullable) receive the transformed vectors."""
+    (bf16, nullable) receive the transformed vectors; k_smooth (float32 [Hkv, D],
+    nullable) smooths K's channels (K times 1/s, Q times s) before the quantization."""
     NB, Hkv, D = _cache_geom(k_cache, 16)
     T = k.shape[0]
     Hq = 0 if q is None else q.shape[1]
@@ -195,7 +197,7 @@ def kv_rope_quant_write(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, 
         _bf16(q, "q"), Hq, _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
         _ptr(positions, torch.int32, "positions"), _ptr(cos_sin, torch.float32, "cos_sin"), max_pos, rotary_dim,
         _bf16(q_norm_weight, "q_norm_weight"), _bf16(k_norm_weight, "k_norm_weight"), float(norm_eps),
-        _bf16(q_out, "q_out"), _bf16(k_out, "k_out"), _stream(stream)))
+        _bf16(q_out, "q_out"), _bf16(k_out, "k_out"), _ptr(k_smooth, torch.float32, "k_smooth"), _stream(stream)))
 
 
 def bf16_kv_write(k, v, slot_mapping, k_cache, v_cache, stream=None):

@@ -106,7 +106,8 @@ i8kv_status i8kv_kv_rope_quant_write(const uint16_t* k, const uint16_t* v, const
                                      float* k_scale, float* v_scale, const uint16_t* q, int Hq, int8_t* q_i8,
                                      float* q_scale, const int32_t* positions, const float* cos_sin, int max_position,
                                      int rotary_dim, const uint16_t* q_norm_weight, const uint16_t* k_norm_weight,
-                                     float norm_eps, uint16_t* q_out, uint16_t* k_out, void* stream) {
+                                     float norm_eps, uint16_t* q_out, uint16_t* k_out, const float* k_smooth,
+                                     void* stream) {
   REQUIRE(T >= 0, I8KV_ERR_INVALID_ARG, "T=%d < 0", T);
   REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
   REQUIRE(D == 128 || D == 256, I8KV_ERR_UNSUPPORTED, "head_dim %d not supported (128 or 256)", D);
@@ -123,6 +124,10 @@ i8kv_status i8kv_kv_rope_quant_write(const uint16_t* k, const uint16_t* v, const
     REQUIRE(norm_eps > 0.f && norm_eps < 3.0e38f, I8KV_ERR_INVALID_ARG, "norm_eps must be positive and finite");
     REQUIRE(aligned16(q_norm_weight) && aligned16(k_norm_weight), I8KV_ERR_INVALID_ARG,
             "norm weights must be 16-byte aligned");
+  }
+  if (k_smooth) {
+    REQUIRE(aligned16(k_smooth), I8KV_ERR_INVALID_ARG, "k_smooth must be 16-byte aligned");
+    REQUIRE(!q || (Hq > 0 && Hq % Hkv == 0), I8KV_ERR_INVALID_ARG, "k_smooth needs Hq a multiple of Hkv");
   }
   if (T == 0) return I8KV_OK;
   REQUIRE(k && v && slot_mapping && k_cache && v_cache && k_scale && v_scale, I8KV_ERR_INVALID_ARG,
@@ -148,6 +153,7 @@ i8kv_status i8kv_kv_rope_quant_write(const uint16_t* k, const uint16_t* v, const
   p.eps = norm_eps;
   p.q_out = q_out;
   p.k_out = k_out;
+  p.k_smooth = k_smooth;
   return from_cuda(i8kv::launch_kv_rope_quant_write(p, static_cast<cudaStream_t>(stream)),
                    "kv_rope_quant_write launch");
 }

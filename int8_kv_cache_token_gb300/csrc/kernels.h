@@ -30,6 +30,7 @@ struct ProducerParams {
   float eps;
   uint16_t* q_out;  // [T, Hq, D] bf16, nullable
   uint16_t* k_out;  // [T, Hkv, D] bf16, nullable
+  const float* k_smooth;  // [Hkv, D] per-channel K smoothing factors, nullable
 };
 
 // Decode (INT8 and BF16-KV variants share the work split and the workspace).

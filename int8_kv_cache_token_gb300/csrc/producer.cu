@@ -163,8 +163,10 @@ __device__ __forceinline__ void store_bf16x16(uint16_t* dst, const float (&x)[16
 }
 
 // kFused adds the RMSNorm / RoPE step on Q and K (and the optional bf16 copies
-// of the transformed vectors); it then takes its shared memory dynamically:
-// [16 tokens][rd] fp32 table rows, then the V staging tile [Hkv][16][D].
+// of the transformed vectors) and the optional per-channel K smoothing (K times
+// RN(1/s), Q times s of its KV head); it then takes its shared memory
+// dynamically: [16 tokens][rd] fp32 table rows, the smoothing factors [Hkv][D]
+// and their reciprocals [Hkv][D] (when given), then the V staging tile [Hkv][16][D].
 template <int D, bool kFused>
 __global__ void __launch_bounds__(256, 4) kv_quant_write_kernel(ProducerParams p) {
   constexpr int LPV = D / 16;    // lanes per vector
@@ -176,8 +178,12 @@ __global__ void __launch_bounds__(256, 4) kv_quant_write_kernel(ProducerParams p
   __shared__ __align__(16) float s_w[2][kFused ? D : 4];  // fused: Q, K norm weights (fp32)
   extern __shared__ __align__(16) uint8_t dsm[];
   const int rd = kFused ? p.rd : 0;
+  const bool smooth = kFused && p.k_smooth != nullptr;
   const float* s_cs = reinterpret_cast<const float*>(dsm);
-  int8_t* vstage = kFused ? reinterpret_cast<int8_t*>(dsm + (size_t)kTileTokens * rd * sizeof(float)) : vstage_s;
+  float* s_sm = reinterpret_cast<float*>(dsm + (size_t)kTileTokens * rd * sizeof(float));  // s, then RN(1/s)
+  const size_t sm_bytes = smooth ? (size_t)2 * p.Hkv * D * sizeof(float) : 0;
+  int8_t* vstage = kFused ? reinterpret_cast<int8_t*>(dsm + (size_t)kTileTokens * rd * sizeof(float) + sm_bytes)
+                          : vstage_s;
 
   griddep_wait();
   griddep_launch_dependents();
@@ -210,6 +216,13 @@ __global__ void __launch_bounds__(256, 4) kv_quant_write_kernel(ProducerParams p
     for (int i = tid; i < 2 * D; i += blockDim.x) {
       const uint16_t* w = i < D ? p.q_norm_w : p.k_norm_w;
       if (w) s_w[i / D][i % D] = bf16_bits_to_float(__ldg(w + i % D));
+    }
+    if (smooth) {
+      for (int i = tid; i < p.Hkv * D; i += blockDim.x) {
+        const float f = __ldg(p.k_smooth + i);
+        s_sm[i] = f;
+        s_sm[p.Hkv * D + i] = __frcp_rn(f);
+      }
     }
     if (rd > 0) {
       __syncthreads();  // s_pos
@@ -282,6 +295,17 @@ __global__ void __launch_bounds__(256, 4) kv_quant_write_kernel(ProducerParams p
         if (act) {
           if (kind == 0 && p.k_out) store_bf16x16(p.k_out + ((size_t)t * Hkv + h) * D + 16 * c, x);
           if (kind == 2 && p.q_out) store_bf16x16(p.q_out + ((size_t)t * Hq + h) * D + 16 * c, x);
+          if (smooth && kind != 1) {
+            // K: times RN(1/s[h]); Q: times s[h / G]
+            const float* f = s_sm + (kind == 0 ? (size_t)Hkv * D + (size_t)h * D : (size_t)(h / (Hq / Hkv)) * D) +
+                             16 * c;
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+              const float4 m = *reinterpret_cast<const float4*>(f + 4 * j4);
+              f2_split(mul2(f2(x[4 * j4], x[4 * j4 + 1]), f2(m.x, m.y)), x[4 * j4], x[4 * j4 + 1]);
+              f2_split(mul2(f2(x[4 * j4 + 2], x[4 * j4 + 3]), f2(m.z, m.w)), x[4 * j4 + 2], x[4 * j4 + 3]);
+            }
+          }
         }
       }
       uint4 codes;
@@ -379,15 +403,16 @@ cudaError_t launch_kv_quant_write(const ProducerParams& p, cudaStream_t stream) 
 
 // Dynamic shared memory: the tile's table rows, then the V staging tile.
 static size_t fused_smem_bytes(const ProducerParams& p) {
-  return (size_t)kTileTokens * p.rd * sizeof(float) + (size_t)p.Hkv * kTileTokens * p.D;
+  return (size_t)kTileTokens * p.rd * sizeof(float) + (p.k_smooth ? (size_t)2 * p.Hkv * p.D * sizeof(float) : 0) +
+         (size_t)p.Hkv * kTileTokens * p.D;
 }
 
 cudaError_t launch_kv_rope_quant_write(const ProducerParams& p, cudaStream_t stream) {
   const int grid = (p.T + kTileTokens - 1) / kTileTokens;
   if (grid == 0) return cudaSuccess;
   const size_t smem = fused_smem_bytes(p);
-  // At most 16 x 256 x 4 + 8 x 16 x 256 = 48 KB; allow it past the default cap.
-  constexpr int kMaxDyn = kTileTokens * 256 * 4 + kMaxHkvProducer * kTileTokens * 256;
+  // At most 16 x 256 x 4 + 2 x 8 x 256 x 4 + 8 x 16 x 256 = 64 KB; allow it past the default cap.
+  constexpr int kMaxDyn = kTileTokens * 256 * 4 + 2 * kMaxHkvProducer * 256 * 4 + kMaxHkvProducer * kTileTokens * 256;
   auto kernel = p.D == 256 ? kv_quant_write_kernel<256, true> : kv_quant_write_kernel<128, true>;
   static bool opted_in[2] = {false, false};  // per device process; setting it twice is harmless
   bool& done = opted_in[p.D == 256 ? 1 : 0];

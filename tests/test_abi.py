@@ -98,12 +98,12 @@ def test_rope_producer_argument_checks_without_gpu(lib):
     f = lib.i8kv_kv_rope_quant_write
     f.restype = ctypes.c_int
     f.argtypes = ([P, P, P] + [ctypes.c_int] * 5 + [P] * 5 + [ctypes.c_int] + [P] * 4 + [ctypes.c_int] * 2 +
-                  [P, P, ctypes.c_float, P, P, P])
+                  [P, P, ctypes.c_float, P, P, P, P])
 
     def call(rd=128, pos=P(16), cs=P(16), max_pos=64, qw=None, kw=None, eps=1e-6, q=None, q_i8=None, q_scale=None,
-             q_out=None, k_out=None, T=4):
-        return f(P(16), P(16), P(16), T, 4, 128, 16, 10, P(16), P(16), P(16), P(16), q, 8, q_i8, q_scale, pos, cs,
-                 max_pos, rd, qw, kw, eps, q_out, k_out, None)
+             q_out=None, k_out=None, T=4, Hq=8, smooth=None):
+        return f(P(16), P(16), P(16), T, 4, 128, 16, 10, P(16), P(16), P(16), P(16), q, Hq, q_i8, q_scale, pos, cs,
+                 max_pos, rd, qw, kw, eps, q_out, k_out, smooth, None)
 
     assert call(rd=48) == 2 and "multiple of 32" in _last_error(lib)
     assert call(rd=256) == 1 and "rotary_dim" in _last_error(lib)
@@ -116,5 +116,7 @@ def test_rope_producer_argument_checks_without_gpu(lib):
     assert call(q=P(16)) == 1 and "q_out" in _last_error(lib)
     assert call(q_out=P(16)) == 1 and "without q" in _last_error(lib)
     assert call(k_out=P(8)) == 1 and "aligned" in _last_error(lib)
+    assert call(smooth=P(20)) == 1 and "k_smooth" in _last_error(lib)
+    assert call(smooth=P(16), q=P(16), q_i8=P(16), q_scale=P(16), Hq=6) == 1 and "multiple" in _last_error(lib)
     # rotary_dim 0 needs no table; T == 0 is a no-op after the shape checks
     assert call(rd=0, pos=None, cs=None, max_pos=0, T=0) == 0

@@ -29,7 +29,7 @@ def _assert_same(gpu: dict, ref: dict, keys):
 
 
 def _run(k, v, slots, num_blocks, positions=None, cos_sin=None, rotary_dim=0, q=None, q_norm_weight=None,
-         k_norm_weight=None, eps=1e-6, quantize_q=True, q_out=False, k_out=False, expect_error=0):
+         k_norm_weight=None, eps=1e-6, quantize_q=True, q_out=False, k_out=False, expect_error=0, k_smooth=None):
     T, Hkv, D = k.shape
     gc = i8.alloc_int8_cache(num_blocks, Hkv, D)
     extra = {}
@@ -47,14 +47,14 @@ def _run(k, v, slots, num_blocks, positions=None, cos_sin=None, rotary_dim=0, q=
                            cos_sin=None if cos_sin is None else dev(cos_sin), rotary_dim=rotary_dim,
                            q_norm_weight=None if q_norm_weight is None else dev(q_norm_weight),
                            k_norm_weight=None if k_norm_weight is None else dev(k_norm_weight),
-                           norm_eps=eps, **extra)
+                           norm_eps=eps, k_smooth=None if k_smooth is None else dev(k_smooth), **extra)
     torch.cuda.synchronize()
     assert i8.device_error() == expect_error
     gc.update({kk: extra[kk] for kk in ("q_i8", "q_scale", "q_out", "k_out") if kk in extra})
     ref = orc.kv_rope_quant_write(k, v, slots, num_blocks, BS, positions=positions, cos_sin=cos_sin,
                                   rotary_dim=rotary_dim, q=q, q_norm_weight=q_norm_weight,
                                   k_norm_weight=k_norm_weight, eps=eps, quantize_q=quantize_q, q_out=q_out,
-                                  k_out=k_out)
+                                  k_out=k_out, k_smooth=k_smooth)
     return gc, ref
 
 
@@ -158,3 +158,21 @@ def test_rope_producer_identity_table_matches_plain_producer():
     for key in a:
         assert torch.equal(a[key], b[key]), key
     assert torch.equal(qa, qb) and torch.equal(sa, sb)
+
+
+@pytest.mark.parametrize("D,rd", [(128, 128), (256, 64)])
+def test_rope_producer_k_smoothing_bit_exact(D, rd):
+    # per-channel K smoothing after norm and rotation: factors sqrt(max |K_c|)
+    # of a channel-outlier K (not powers of two, so every product rounds)
+    T, Hkv, Hq = 40, 4, 12
+    w = wl.DecodeWorkload("sm", Hq, Hkv, D, [T], seed=D + rd, outlier_channels=4)
+    k, v = w.kv(0)
+    rng = np.random.default_rng(rd)
+    q = wl.randn_bf16(rng, (T, Hq, D))
+    smooth = np.sqrt(np.abs(wl.bf16_values(k)).max(axis=0)).astype(np.float32)
+    slots = w.slots(0).copy()
+    slots[5] = -1
+    gc, ref = _run(k, v, slots, w.num_blocks, positions=np.arange(T, dtype=np.int32) * 7,
+                   cos_sin=wl.rope_cos_sin(300, rd), rotary_dim=rd, q=q, q_norm_weight=wl.norm_weight_bf16(rng, D),
+                   k_norm_weight=wl.norm_weight_bf16(rng, D), q_out=True, k_out=True, k_smooth=smooth)
+    _assert_same(gc, ref, ALL)
