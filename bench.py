@@ -5,18 +5,18 @@ Workload (N = 1): single-sequence decode with 24 query / 4 KV heads, head_dim
 256, block size 16, histories 8192, 16384 and 32768 (K with 4 outlier channels
 per KV head x20, V N(0,1), seeded), i.e. the long-history decode configuration.
 One step = one new token through the 16 full-attention layers of the pages'
-model: for every (layer, history) the producer (i8kv_kv_quant_write) quantizes
-the new token's K/V into that layer's paged INT8 cache and quantizes its query,
-then the INT8 decode kernel attends over the whole history.  Each layer owns
-its cache, so a step streams 16 x 56K tokens x 2080 B = 1.9 GB and L2 (129 MB)
-holds none of it between steps.  All K timed steps run as one CUDA graph with
-timing events around it.  The decode kernel's own average duration comes from a
-second graph of the same K x 48 decode calls back to back (no producer in
-between).  The one-launch decode step (i8kv_int8_decode_step, producer work
-inside the attention kernel) is timed per history among the secondary results.
+model: for every (layer, history) one i8kv_int8_decode_step call quantizes the
+new token's K/V into that layer's paged INT8 cache (the producer's rule, bit for
+bit), quantizes its query and attends over the whole history, then its merge
+kernel runs.  Each layer owns its cache, so a step streams 16 x 56K tokens x
+2080 B = 1.9 GB and L2 (129 MB) holds none of it between steps.  All K timed
+steps run as one CUDA graph with timing events around it.  The dominant
+kernel's own average duration comes from a second graph of the same K x 48
+calls back to back.  The producer + plain decode pair (two calls) is timed per
+history among the secondary results.
 
   value     = KV bytes read by the decode launches / timed wall time (GB/s)
-  roofline  = same bytes / the decode calls' own time (second graph), against the
+  roofline  = same bytes / the decode-step calls' own time (second graph), against the
               measured HBM copy bandwidth (MEASURED_PEAKS.json)
   e2e       = the same step through the C ABI with pinned host buffers: the new
               tokens' q/k/v copied host->device and every output copied back,
@@ -318,12 +318,11 @@ def run_ours(args):
     torch.cuda.synchronize()
     ws = {L: i8.decode_workspace(1, 24, 4, 256, wl.decode_outlier(L).block_tables.shape[1]) for L in HISTORIES}
     bytes_per_step = sum(ly.w.kv_bytes_int8() for ly in layers)
-    launches_per_step = 3 * len(layers)  # producer, attention, merge
+    launches_per_step = 2 * len(layers)  # decode step (producer work + attention), merge
 
     def step():
         for ly in layers:
-            ly.produce(i8)
-            ly.decode(i8, ws[int(ly.w.seq_lens[0])])
+            ly.step(i8, ws[int(ly.w.seq_lens[0])])
 
     for _ in range(max(args.warmup, 1)):
         step()
@@ -363,10 +362,11 @@ def run_ours(args):
     assert err == 0, f"kernel error {err} in the timed region"
     value = whole_job_gbs(world, args.steps, bytes_per_step, ms)
 
-    # ---- the dominant kernel alone: the same K x 48 decode calls back to back ----
-    # (one graph, events around it; a decode call is the attention kernel plus
-    # its merge kernel).  Then per history, the 16 layers x K calls of that length.
-    dec_ms = time_graph(torch, lambda: [ly.decode(i8, ws[int(ly.w.seq_lens[0])]) for ly in layers], args.steps)
+    # ---- the dominant kernel alone: the same K x 48 decode-step calls back to back ----
+    # (one graph, events around it; a call is the decode-step attention kernel plus
+    # its merge kernel).  Then per history, the 16 layers x K calls of that length,
+    # for the step and for the plain decode (the producer run separately).
+    dec_ms = time_graph(torch, lambda: [ly.step(i8, ws[int(ly.w.seq_lens[0])]) for ly in layers], args.steps)
     n_dec = len(layers)
     achieved = bytes_per_step / (dec_ms / 1e3) / 1e9
     avg_launch_us = dec_ms / n_dec * 1e3
@@ -378,14 +378,15 @@ def run_ours(args):
         ms_s = time_graph(torch, lambda: [ly.step(i8, ws[L]) for ly in sub], args.steps)
         step_by_len[L] = ms_s / len(sub)
     src = kernel_hash("int8_kv_cache_token_gb300/csrc/decode.cu", "int8_kv_cache_token_gb300/csrc/common.cuh")
-    traffic = recorded_traffic("int8_decode", src)
+    traffic = recorded_traffic("int8_decode_step", src)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": (achieved / hbm_peak) if achieved else None, "traffic": traffic,
-                "kernel": "int8_decode_kernel", "peak_kind": f"of {peak_kind} (HBM copy bandwidth)",
+                "kernel": "decode_kernel<256, INT8, STEP> + decode_merge_kernel",
+                "peak_kind": f"of {peak_kind} (HBM copy bandwidth)",
                 "avg_launch_us": avg_launch_us,
                 "algorithmic_bytes_per_launch": bytes_per_step / len(layers),
-                "method": "K x 48 decode calls (attention + merge kernel) replayed back to back in one CUDA graph, "
-                          "CUDA events around the graph"}
+                "method": "K x 48 decode-step calls (attention + merge kernel) replayed back to back in one CUDA "
+                          "graph, CUDA events around the graph"}
 
     # ---- e2e: the same steps through the C ABI with pinned host buffers ----
     e2e = run_e2e(args, torch, i8, layers, ws, bytes_per_step, world)
@@ -436,8 +437,8 @@ def run_ours(args):
 
 
 def run_e2e(args, torch, i8, layers, ws, bytes_per_step, world):
-    """Per step: H2D of every layer's new q/k/v from pinned host memory, producer +
-    decode, D2H of every output; captured with the steps in one graph."""
+    """Per step: H2D of every layer's new q/k/v from pinned host memory, the decode
+    step, D2H of every output; captured with the steps in one graph."""
     host_in = []
     for ly in layers:
         host_in.append((ly.k.cpu().pin_memory(), ly.v.cpu().pin_memory(), ly.q.cpu().pin_memory()))
@@ -455,8 +456,7 @@ def run_e2e(args, torch, i8, layers, ws, bytes_per_step, world):
                     ly.k.copy_(hk, non_blocking=True)
                     ly.v.copy_(hv, non_blocking=True)
                     ly.q.copy_(hq, non_blocking=True)
-                    ly.produce(i8)
-                    ly.decode(i8, ws[int(ly.w.seq_lens[0])])
+                    ly.step(i8, ws[int(ly.w.seq_lens[0])])
                     ho.copy_(ly.out, non_blocking=True)
     stream.wait_stream(cap)
     g.replay()
@@ -690,10 +690,14 @@ def run_profile(args):
     order = [rounds[j % len(HISTORIES)][(j // len(HISTORIES)) % args.layers]
              for j in range(args.warmup + args.steps)]
     for ly in order:
-        ly.decode(i8, ws[int(ly.w.seq_lens[0])])
+        if args.profile_step:
+            ly.step(i8, ws[int(ly.w.seq_lens[0])])
+        else:
+            ly.decode(i8, ws[int(ly.w.seq_lens[0])])
     torch.cuda.synchronize()
     assert i8.device_error() == 0
-    print(json.dumps({"profile": "int8_decode", "histories": list(HISTORIES), "launches": len(order),
+    print(json.dumps({"profile": "int8_decode_step" if args.profile_step else "int8_decode",
+                      "histories": list(HISTORIES), "launches": len(order),
                       "bytes_per_launch": {str(L): wl.decode_outlier(L).kv_bytes_int8() for L in HISTORIES}}))
     return 0
 
@@ -791,6 +795,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile", action="store_true",
                     help="decode launches only (the three histories round-robin, --layers caches each) for ncu")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="with --profile: the one-launch decode step instead of the plain decode")
     ap.add_argument("--profile-prefix", action="store_true",
                     help="prefix-chunk launches only (16384 + 2048 chunk) for ncu")
     ap.add_argument("--profile-first-chunk", action="store_true",
