@@ -442,21 +442,23 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
   return r;
 }
 
-// rne_bits(x[i] / s) for the N (even) values of one row: div_row's quotient
-// then the round-half-even add, on packed pairs.  Same results as div_row
-// followed by rne_bits, element by element.
+// The bits of RN(x[i] / s + bias) for the N (even) values of one row: div_row's
+// quotient, then one add, on packed pairs.  With bias = 1.5 * 2^23 the low byte
+// is round-half-even(x / s) (rne_bits); the same results as div_row followed by
+// the scalar add, element by element.
 template <int N>
-__device__ __forceinline__ void div_rne_row(const float (&x)[N], float s, float y, uint32_t (&q)[N]) {
+__device__ __forceinline__ void div_rne_row(const float (&x)[N], float s, float y, uint32_t (&q)[N],
+                                            float bias = 12582912.0f) {
   if (s < kTinyDivisor) {
     float t[N];
 #pragma unroll
     for (int i = 0; i < N; ++i) t[i] = x[i];
     div_row(t, s, y);
 #pragma unroll
-    for (int i = 0; i < N; ++i) q[i] = rne_bits(t[i]);
+    for (int i = 0; i < N; ++i) q[i] = __float_as_uint(__fadd_rn(t[i], bias));
     return;
   }
-  const uint64_t y2 = f2(y, y), ns2 = f2(-s, -s), c2 = f2(12582912.0f, 12582912.0f);
+  const uint64_t y2 = f2(y, y), ns2 = f2(-s, -s), c2 = f2(bias, bias);
 #pragma unroll
   for (int i = 0; i < N / 2; ++i) {
     const uint64_t v = f2(x[2 * i], x[2 * i + 1]);

@@ -522,8 +522,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
       uint32_t pk[16];
       if constexpr (kBF) {
         tmem_wait_ld();
+        {
+          const uint64_t cc = f2(c2, c2);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) s[t] = __fmul_rn(s[t], c2);
+          for (int t = 0; t < 16; ++t) f2_split(mul2(f2(s[2 * t], s[2 * t + 1]), cc), s[2 * t], s[2 * t + 1]);
+        }
         if (!full) {
 #pragma unroll
           for (int t = 0; t < 32; ++t)
@@ -550,13 +553,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
           reinterpret_cast<const float4*>(smem + Ly::oTile + (size_t)(g % kStages) * T::kSlot + T::oSk);
       const float4* sv4 = sk4 + kGroup / 4;
       tmem_wait_ld();
+      {
+        const uint64_t cc = f2(c2, c2);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 k4 = sk4[i];
-        s[4 * i] = __fmul_rn(__fmul_rn(s[4 * i], k4.x), c2);
-        s[4 * i + 1] = __fmul_rn(__fmul_rn(s[4 * i + 1], k4.y), c2);
-        s[4 * i + 2] = __fmul_rn(__fmul_rn(s[4 * i + 2], k4.z), c2);
-        s[4 * i + 3] = __fmul_rn(__fmul_rn(s[4 * i + 3], k4.w), c2);
+        for (int i = 0; i < 8; ++i) {
+          const float4 k4 = sk4[i];
+          f2_split(mul2(mul2(f2(s[4 * i], s[4 * i + 1]), f2(k4.x, k4.y)), cc), s[4 * i], s[4 * i + 1]);
+          f2_split(mul2(mul2(f2(s[4 * i + 2], s[4 * i + 3]), f2(k4.z, k4.w)), cc), s[4 * i + 2], s[4 * i + 3]);
+        }
       }
       if (!full) {
 #pragma unroll
@@ -572,10 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float4 v4 = sv4[i];
-          s[4 * i] = __fmul_rn(s[4 * i], v4.x);
-          s[4 * i + 1] = __fmul_rn(s[4 * i + 1], v4.y);
-          s[4 * i + 2] = __fmul_rn(s[4 * i + 2], v4.z);
-          s[4 * i + 3] = __fmul_rn(s[4 * i + 3], v4.w);
+          f2_split(mul2(f2(s[4 * i], s[4 * i + 1]), f2(v4.x, v4.y)), s[4 * i], s[4 * i + 1]);
+          f2_split(mul2(f2(s[4 * i + 2], s[4 * i + 3]), f2(v4.z, v4.w)), s[4 * i + 2], s[4 * i + 3]);
         }
         if (!full) {
 #pragma unroll
@@ -590,14 +592,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
       // by Markstein's method); W / sW <= A / RN(A / 127) < 127.5, no clamp needed
       sw = div127(A);
       if (A > 0.f) {
-        div_row(s, sw, __frcp_rn(sw));
         // round-half-even(q) + 1024 as the f16 bit pattern 0x6400 + code, from the
         // low bits of the fp32 sum q + 1.5 * 2^23 + 0x6400; two per register, then
         // 1024 subtracted (exact)
+        uint32_t qb[32];
+        div_rne_row(s, sw, __frcp_rn(sw), qb, 12608512.0f);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint32_t lo = __float_as_uint(__fadd_rn(s[2 * i], 12608512.0f));
-          const uint32_t hi = __float_as_uint(__fadd_rn(s[2 * i + 1], 12608512.0f));
+          const uint32_t lo = qb[2 * i], hi = qb[2 * i + 1];
           uint32_t h = __byte_perm(lo, hi, 0x5410);
           asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(h) : "r"(0x64006400u));
           pk[i] = h;
@@ -655,12 +657,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
           mbar_arrive(pv_free);  // every column of the accumulator is read
         }
         const float(&x)[32] = v[c & 1];
+        const uint64_t e2 = f2(e, e);
         if (rescale) {
+          const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[32 * c + i] = __fmaf_rn(x[i], e, __fmul_rn(o[32 * c + i], alpha));
+          for (int i = 0; i < 16; ++i)
+            f2_split(fma2(f2(x[2 * i], x[2 * i + 1]), e2, mul2(f2(o[32 * c + 2 * i], o[32 * c + 2 * i + 1]), a2)),
+                     o[32 * c + 2 * i], o[32 * c + 2 * i + 1]);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[32 * c + i] = __fmaf_rn(x[i], e, o[32 * c + i]);
+          for (int i = 0; i < 16; ++i)
+            f2_split(fma2(f2(x[2 * i], x[2 * i + 1]), e2, f2(o[32 * c + 2 * i], o[32 * c + 2 * i + 1])),
+                     o[32 * c + 2 * i], o[32 * c + 2 * i + 1]);
         }
       }
     };
