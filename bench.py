@@ -402,6 +402,10 @@ def run_ours(args):
         if not args.quick:
             secondary.update(run_secondary(torch, i8, hbm_peak))
             try:
+                secondary["decode_other_configs"] = run_batch_decodes(torch, i8, hbm_peak)
+            except Exception as e:  # pragma: no cover - report, do not hide
+                secondary["decode_other_configs"] = {"error": str(e)[:200]}
+            try:
                 secondary["decode_u8_probs_by_history"] = run_u8p_comparison(torch, i8, hbm_peak)
             except Exception as e:  # pragma: no cover - report, do not hide
                 secondary["decode_u8_probs_by_history"] = {"error": str(e)[:200]}
@@ -589,6 +593,54 @@ def run_u8p_comparison(torch, i8, hbm_peak):
         res[str(L)] = r
         del caches
         torch.cuda.empty_cache()
+    return res
+
+
+def run_batch_decodes(torch, i8, hbm_peak):
+    """The other decode configurations, timed only (their parity is in the tests):
+    single sequence at 4096 (config 0), 64 sequences with lengths uniform in
+    [1024, 32768] (config 3) and batch 16 at 32768 with 32 q / 8 KV heads, head_dim
+    128 (config 4).  Shapes, lengths and paging come from workloads.py; the K/V
+    values are drawn on the device (torch generator, seed 0) and written through
+    the producer, the query quantized by its query path.  Each cache exceeds L2
+    except config 0's, which rotates copies."""
+    res = {}
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    for name, w in (("config0_decode_4k", wl.decode_4k()), ("config3_decode_batch64", wl.decode_batch()),
+                    ("config4_decode_gqa_b16_32k", wl.producer_gqa_decode())):
+        try:
+            cache = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+            for b in range(w.B):
+                L = int(w.seq_lens[b])
+                k = torch.randn((L, w.Hkv, w.D), generator=gen, device="cuda").to(torch.bfloat16)
+                v = torch.randn((L, w.Hkv, w.D), generator=gen, device="cuda").to(torch.bfloat16)
+                i8.kv_quant_write(k, v, to_dev(torch, w.slots(b)), **cache)
+                del k, v
+            q = torch.randn((w.B, w.Hq, w.D), generator=gen, device="cuda").to(torch.bfloat16)
+            q_i8 = torch.empty((w.B, w.Hq, w.D), dtype=torch.int8, device="cuda")
+            q_s = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+            dummy = torch.zeros((w.B, w.Hkv, w.D), dtype=torch.bfloat16, device="cuda")
+            i8.kv_quant_write(dummy, dummy, torch.full((w.B,), -1, dtype=torch.int32, device="cuda"), **cache, q=q,
+                              q_i8=q_i8, q_scale=q_s)
+            out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device="cuda")
+            ws = i8.decode_workspace(w.B, w.Hq, w.Hkv, w.D, w.block_tables.shape[1])
+            bt, sl = to_dev(torch, w.block_tables), to_dev(torch, w.seq_lens)
+            nbytes = w.kv_bytes_int8()
+            copies = max(1, int(np.ceil(400e6 / nbytes)))
+            caches = [cache] + [{n: t.clone() for n, t in cache.items()} for _ in range(copies - 1)]
+            calls = [(lambda c=c: i8.int8_paged_decode_attn(out, q_i8, q_s, c["k_cache"], c["v_cache"], c["k_scale"],
+                                                            c["v_scale"], bt, sl, ws)) for c in caches]
+            ms = time_rotating(torch, calls, 10 if nbytes > 1e9 else 20)
+            torch.cuda.synchronize()
+            assert i8.device_error() == 0
+            gbs = nbytes / (ms / 1e3) / 1e9
+            res[name] = {"us": ms * 1e3, "kv_bytes": nbytes, "gb_s": gbs, "frac_hbm": gbs / hbm_peak,
+                         "batch": w.B, "heads": f"{w.Hq}/{w.Hkv}/{w.D}"}
+            del caches, cache
+            torch.cuda.empty_cache()
+        except Exception as e:  # pragma: no cover - report, do not hide
+            res[name] = {"error": str(e)[:200]}
     return res
 
 
