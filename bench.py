@@ -800,6 +800,44 @@ def run_profile_prefix(args):
     return 0
 
 
+def run_profile_gqa128(args):
+    """Decode launches at head_dim 128 for profilers: batch 4 at 32768 with 32 q /
+    8 KV heads (config 4's shape at a quarter of its batch, 277 MB of cache, above
+    L2); device-drawn seeded values; `--warmup` then `--steps` launches."""
+    import torch
+
+    from int8_kv_cache_token_gb300 import build as ibuild
+    ibuild.build()
+    import int8_kv_cache_token_gb300 as i8
+    w = wl.producer_gqa_decode(B=4)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(0)
+    cache = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+    for b in range(w.B):
+        L = int(w.seq_lens[b])
+        k = torch.randn((L, w.Hkv, w.D), generator=gen, device="cuda").to(torch.bfloat16)
+        v = torch.randn((L, w.Hkv, w.D), generator=gen, device="cuda").to(torch.bfloat16)
+        i8.kv_quant_write(k, v, to_dev(torch, w.slots(b)), **cache)
+    q = torch.randn((w.B, w.Hq, w.D), generator=gen, device="cuda").to(torch.bfloat16)
+    q_i8 = torch.empty((w.B, w.Hq, w.D), dtype=torch.int8, device="cuda")
+    q_s = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+    dummy = torch.zeros((w.B, w.Hkv, w.D), dtype=torch.bfloat16, device="cuda")
+    i8.kv_quant_write(dummy, dummy, torch.full((w.B,), -1, dtype=torch.int32, device="cuda"), **cache, q=q,
+                      q_i8=q_i8, q_scale=q_s)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device="cuda")
+    ws = i8.decode_workspace(w.B, w.Hq, w.Hkv, w.D, w.block_tables.shape[1])
+    bt, sl = to_dev(torch, w.block_tables), to_dev(torch, w.seq_lens)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup + args.steps):
+        i8.int8_paged_decode_attn(out, q_i8, q_s, cache["k_cache"], cache["v_cache"], cache["k_scale"],
+                                  cache["v_scale"], bt, sl, ws)
+    torch.cuda.synchronize()
+    assert i8.device_error() == 0
+    print(json.dumps({"profile": "int8_decode_gqa128", "batch": w.B, "kv_bytes": w.kv_bytes_int8(),
+                      "launches": args.warmup + args.steps}))
+    return 0
+
+
 def run_profile_first_chunk(args):
     """High-precision first-chunk launches only, for profilers: 0 + 4096 tokens (24 q /
     4 KV heads, head_dim 256), `--warmup` then `--steps` calls (tiles + attention)."""
@@ -865,6 +903,8 @@ def main():
                     help="with --profile: the one-launch decode step instead of the plain decode")
     ap.add_argument("--profile-prefix", action="store_true",
                     help="prefix-chunk launches only (16384 + 2048 chunk) for ncu")
+    ap.add_argument("--profile-gqa128", action="store_true",
+                    help="decode launches at head_dim 128 (batch 4 x 32768, 32/8 heads) for ncu")
     ap.add_argument("--profile-first-chunk", action="store_true",
                     help="high-precision first-chunk launches only (0 + 4096) for ncu")
     ap.add_argument("--profile-producer", action="store_true",
@@ -872,6 +912,8 @@ def main():
     args = ap.parse_args()
     if args.profile_first_chunk:
         return run_profile_first_chunk(args)
+    if args.profile_gqa128:
+        return run_profile_gqa128(args)
     if args.profile_producer:
         return run_profile_producer(args)
     if args.profile:
