@@ -60,23 +60,29 @@ namespace {
 constexpr int kPart = 256;   // the pages' decode partition (debug QK tiles)
 constexpr int kBS = 16;      // block size
 constexpr int kGroup = 32;   // probability group
-constexpr int kQW = 4;       // QK / softmax warps per stream (one unit at a time)
-constexpr int kStreams = 2;  // QK streams: stream s takes the units i with i % 2 == s
+constexpr int kQKWarps = 8;  // QK / softmax warps, in kStreams streams of kQW (per variant, below)
 constexpr int kPW = 8;       // PV warps
-constexpr int kPVWarp0 = kStreams * kQW;
+constexpr int kPVWarp0 = kQKWarps;
 constexpr int kProdWarp = kPVWarp0 + kPW;
 constexpr int kThreads = (kProdWarp + 1) * 32;
-constexpr int kHandBufs = 2 * kStreams;  // handoff buffers, unit i uses buffer i % 4
+constexpr int kHandBufs = 4;  // handoff buffers, unit i uses buffer i % 4
 constexpr int kRows = 8;     // query rows in the MMA N dimension
 __host__ __device__ constexpr int kSlotFloats(int D) { return kRows * D + 2 * kRows; }
 
-// Geometry of one variant.  INT8: 128-token units, one 32-token group per QK
-// warp.  BF16-KV comparison: 64-token units (the same 32 KB per ring item at
-// D = 256), one 16-token block per QK warp, plain softmax weights.
+// Geometry of one variant.  The 8 QK warps form kStreams streams of kQW warps;
+// stream s takes the units i with i % kStreams == s, one granule per QK warp.
+// INT8: 32-token granules (one probability group per QK warp); BF16-KV
+// comparison: 16-token granules (one block per QK warp), plain softmax weights.
+// At D = 256 two streams of 4 warps: 128-token INT8 units of 66 KB of K and V.
+// At D = 128 one stream of 8 warps: 256-token units, the same bytes per ring
+// item, so the per-unit work (copies, handoff, rescale) is spread over as many
+// bytes as at D = 256.
 template <int D, bool BF16>
 struct Geo {
+  static constexpr int kStreams = D == 128 ? 1 : 2;             // QK streams
+  static constexpr int kQW = kQKWarps / kStreams;               // QK warps per stream = granules per unit
   static constexpr int EB = BF16 ? 2 : 1;                       // bytes per cache element
-  static constexpr int kUnit = BF16 ? 64 : 128;                 // tokens per unit
+  static constexpr int kUnit = kQW * (BF16 ? 16 : 32);          // tokens per unit
   static constexpr int kBlocksU = kUnit / kBS;                  // pages per ring item
   static constexpr int kPage = D * kBS * EB;                    // one (block, KV head) page
   static constexpr int kPages = kBlocksU * kPage;
@@ -115,9 +121,9 @@ __host__ __device__ inline SmemLayout decode_layout(int nslots) {
   L.hand = off;
   off += (size_t)kHandBufs * Gm::kHand;
   L.stage = off;
-  off += (size_t)kStreams * kQW * Gm::kStage;
+  off += (size_t)kQKWarps * Gm::kStage;
   L.qbuf = off;  // [stream] query codes [8][D] and scales [8] (decode step)
-  off += (size_t)kStreams * Gm::kQBuf;
+  off += (size_t)Gm::kStreams * Gm::kQBuf;
   L.bars = off;  // full[nslots], empty[nslots], hfull[4], hempty[4]
   off += (size_t)(2 * nslots + 2 * kHandBufs) * sizeof(uint64_t);
   L.ctrl = off;
@@ -142,16 +148,17 @@ __device__ __forceinline__ int clamp_len(int L, int maxL) {
   return L > maxL ? maxL : L;
 }
 
-__device__ __forceinline__ int unit_granules(const Walk& w, long long g_end) {
+// Granules of the unit that starts at w: up to maxg (one per QK warp of a stream).
+__device__ __forceinline__ int unit_granules(const Walk& w, long long g_end, int maxg) {
   if (w.gc >= g_end) return 0;
   const long long left = g_end - w.gc;
   const int in_pair = w.ngp - w.gi;
-  const int n = in_pair < kQW ? in_pair : kQW;
+  const int n = in_pair < maxg ? in_pair : maxg;
   return left < n ? (int)left : n;
 }
 
 __device__ __forceinline__ void walk_next(Walk& w, const int32_t* seq_lens, int B, int Hkv, int maxL, int gran,
-                                          long long g_end) {
+                                          long long g_end, int maxg) {
   w.gc += w.n;
   w.gi += w.n;
   if (w.gi >= w.ngp) {
@@ -170,7 +177,7 @@ __device__ __forceinline__ void walk_next(Walk& w, const int32_t* seq_lens, int 
       }
     }
   }
-  w.n = unit_granules(w, g_end);
+  w.n = unit_granules(w, g_end, maxg);
 }
 
 // floor(a / d), d >= 1.  Below 2^22 the product of the exact operand a and a
@@ -211,10 +218,10 @@ __device__ __forceinline__ int cta_of(long long u, long long U, int N) {
   return (int)(((u + 1) * N + U - 1) / U - 1);
 }
 
-// Ring slots.  Slots [0, 2 kK) hold K items: stream s owns [s kK, (s+1) kK) and
-// fills them with its own units in order (j = i / 2 is unit i's index within
-// its stream), so each K slot is consumed by one stream, in order.  Slots
-// [2 kK, nslots) hold the V items of all units, in order.  Every slot is
+// Ring slots.  Slots [0, kStreams kK) hold K items: stream s owns [s kK, (s+1) kK)
+// and fills them with its own units in order (j = i / kStreams is unit i's index
+// within its stream), so each K slot is consumed by one stream, in order.  Slots
+// [kStreams kK, nslots) hold the V items of all units, in order.  Every slot is
 // therefore reused only after its previous item was consumed, which keeps each
 // mbarrier within one phase of its waiters.
 struct Ring {
@@ -222,8 +229,8 @@ struct Ring {
   // A stream releases its K slot right after its QK MMAs, long before its unit
   // is done, so one K slot per stream (two at 12 slots) keeps it fed; the rest
   // of the ring holds V items, which wait for the QK warps' handoff.
-  __host__ __device__ explicit Ring(int nslots)
-      : kK(nslots / 6 > 0 ? nslots / 6 : 1), nV(nslots - 2 * (nslots / 6 > 0 ? nslots / 6 : 1)) {}
+  __host__ __device__ Ring(int nslots, int streams)
+      : kK(nslots / 6 > 0 ? nslots / 6 : 1), nV(nslots - streams * (nslots / 6 > 0 ? nslots / 6 : 1)) {}
 };
 
 // A position in a ring of n slots: the slot, and how many times the ring was
@@ -416,6 +423,7 @@ __device__ __forceinline__ void load_q_frags_smem(const uint8_t* qa, int G, int 
 template <int D, bool BF16, bool STEP = false, bool U8P = false>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int nslots) {
   static_assert(!(STEP && BF16), "the decode step is INT8 only");
+  constexpr int kQW = Geo<D, BF16>::kQW, kStreams = Geo<D, BF16>::kStreams;
   static_assert(!(U8P && (BF16 || STEP)), "UINT8 probabilities: plain INT8 decode only");
   using Gm = Geo<D, BF16>;
   constexpr int kUnit = Gm::kUnit, kBlocksU = Gm::kBlocksU, kPage = Gm::kPage, kSlot = Gm::kSlot;
@@ -439,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   const int maxL = p.max_blocks * kBS;
 
   if (warp == kProdWarp && lane == 0) {
-    const Ring rg(nslots);
+    const Ring rg(nslots, Gm::kStreams);
     for (int s = 0; s < nslots; ++s) {
       mbar_init(&full[s], 32);
       mbar_init(&empty[s], s < kStreams * rg.kK ? kQW : kPW);
@@ -563,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   w0.ngp = (w0.L + kGran - 1) / kGran;
   w0.gc = w0.gb + (long long)w0.kvh * w0.ngp + w0.gi;
   const long long g_end = w0.gc + n_gran;  // end of this CTA's granule range
-  w0.n = n_gran > 0 ? unit_granules(w0, g_end) : 0;
+  w0.n = n_gran > 0 ? unit_granules(w0, g_end, Gm::kQW) : 0;
   // This lane's page of the first unit (lanes below the unit's page count).
   auto first_blk_lanes = [&]() {
     const int t0 = w0.gi * kGran;
@@ -607,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   const long long U = (long long)ctrl[6] | ((long long)ctrl[7] << 31);
   const int Nw = ctrl[10];
   const int g = lane >> 2, t = lane & 3;
-  const Ring rg(nslots);
+  const Ring rg(nslots, Gm::kStreams);
 
   if (warp == kProdWarp) {
     // ================= producer warp =================
@@ -626,9 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     // issued (one unit ahead left the producer waiting on the load whenever a
     // unit's slots freed up sooner than the load returned).
     Walk wk = w0, wn = w0, wnn;
-    walk_next(wn, p.seq_lens, B, Hkv, maxL, kGran, g_end);
+    walk_next(wn, p.seq_lens, B, Hkv, maxL, kGran, g_end, Gm::kQW);
     wnn = wn;
-    if (wnn.n > 0) walk_next(wnn, p.seq_lens, B, Hkv, maxL, kGran, g_end);
+    if (wnn.n > 0) walk_next(wnn, p.seq_lens, B, Hkv, maxL, kGran, g_end, Gm::kQW);
     int blk_cur = blk_first;
     int blk_n = wn.n > 0 ? load_blk(wn) : -1;
     int n_k = 0, n_v = 0;  // K and V items issued
@@ -649,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       const uint32_t n_pages = __popc(__ballot_sync(0xffffffffu, ok));
       // K item: the pages by bulk copy, the unit's (sK, sV) per token by cp.async;
       // the slot's full barrier waits for both.
-      const int kslot = (i & 1) * rg.kK + kp_cur.s, ku = kp_cur.use;
+      const int kslot = (i % kStreams) * rg.kK + kp_cur.s, ku = kp_cur.use;
       if (ku > 0) pipe_wait(&empty[kslot], (ku - 1) & 1, abort_flag);
       if (*abort_flag) break;  // never refill a slot whose previous item was not consumed
       if (lane == 0) mbar_expect_tx(&full[kslot], n_pages * kPage);
@@ -717,12 +725,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       ++n_k;
       // V item
       kp_cur.next(rg.kK);
-      {
+      if constexpr (kStreams == 2) {
         const RingPos tmp = kp_cur;  // the next unit belongs to the other stream
         kp_cur = kp_oth;
         kp_oth = tmp;
       }
-      const int vslot = 2 * rg.kK + vp.s, vu = vp.use;
+      const int vslot = kStreams * rg.kK + vp.s, vu = vp.use;
       if (vu > 0) pipe_wait(&empty[vslot], (vu - 1) & 1, abort_flag);
       if (*abort_flag) break;
       if (lane == 0) mbar_expect_tx(&full[vslot], n_pages * kPage);
@@ -747,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       blk_n = blk_nn;
       wk = wn;
       wn = wnn;
-      if (wnn.n > 0) walk_next(wnn, p.seq_lens, B, Hkv, maxL, kGran, g_end);
+      if (wnn.n > 0) walk_next(wnn, p.seq_lens, B, Hkv, maxL, kGran, g_end, Gm::kQW);
     }
     if (*abort_flag) {
       // The consumers stopped waiting: hold the CTA (and its shared memory)
@@ -759,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         int uses;
         if (sl < kStreams * rg.kK) {
           const int st = sl / rg.kK, r = sl % rg.kK;
-          const int js = n_k > st ? (n_k - st + 1) / 2 : 0;  // this stream's K items issued
+          const int js = n_k > st ? (n_k - st + kStreams - 1) / kStreams : 0;  // this stream's K items issued
           uses = js > r ? (js - r + rg.kK - 1) / rg.kK : 0;
         } else {
           const int v = sl - kStreams * rg.kK;
@@ -784,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     const int tok0 = qw * kWTok;  // this warp's tokens within a unit
     uint8_t* stg = stage + warp * Gm::kStage;
     Walk wk = w0;
-    if (st == 1) walk_next(wk, p.seq_lens, B, Hkv, maxL, kGran, g_end);
+    if (st == 1) walk_next(wk, p.seq_lens, B, Hkv, maxL, kGran, g_end, Gm::kQW);
     int cur_pair = -1;
     uint32_t qf[D / 32][2];    // INT8: query fragments (raw s8)
     uint32_t qfb[D / 16][2];   // BF16: query fragments
@@ -988,8 +996,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         }
       }
       mbar_arrive(&hfull[hbi]);  // every thread: releases its own stores
-      walk_next(wk, p.seq_lens, B, Hkv, maxL, kGran, g_end);
-      if (wk.n > 0) walk_next(wk, p.seq_lens, B, Hkv, maxL, kGran, g_end);
+      // the next unit of this stream: skip the other streams' units
+#pragma unroll
+      for (int k = 0; k < kStreams; ++k)
+        if (k == 0 || wk.n > 0) walk_next(wk, p.seq_lens, B, Hkv, maxL, kGran, g_end, Gm::kQW);
     }
     return;
   }
@@ -1002,7 +1012,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   const int pv_w = warp - kPVWarp0;
   const int mi = lane >> 3, ri = lane & 7;
   Walk wk = w0, w1 = w0;
-  walk_next(w1, p.seq_lens, B, Hkv, maxL, kGran, g_end);
+  walk_next(w1, p.seq_lens, B, Hkv, maxL, kGran, g_end, Gm::kQW);
   int cur_pair = -1;
   RingPos vpos;  // V slots
   float o[NDT][4];
@@ -1028,18 +1038,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     const uint8_t* hb = hand + (size_t)hbi * Gm::kHand;
     pipe_wait(&hfull[hbi], (i / kHandBufs) & 1, abort_flag);
     // ---- the unit's running maximum and the groups' factors ----
-    static_assert(kQW == 4, "a row's group values are read as one float4");
+    static_assert(kQW % 4 == 0, "a row's group values are read as float4s");
     float fs[kQW][2];  // exp(m_g - m_new) * sW_g (INT8) or exp(m_g - m_new) (BF16)
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
       const int row = 2 * t + r;
-      const float4 m4 = reinterpret_cast<const float4*>(hb + Gm::kHM)[row];
-      const float4 l4 = reinterpret_cast<const float4*>(hb + Gm::kHL)[row];
-      const float4 s4 = reinterpret_cast<const float4*>(hb + Gm::kHSw)[row];
       // groups past the unit's tokens published m = -inf, l = 0, sW = 0
-      const float mg[4] = {m4.x, m4.y, m4.z, m4.w}, lgv[4] = {l4.x, l4.y, l4.z, l4.w},
-                  sg[4] = {s4.x, s4.y, s4.z, s4.w};
-      const float mn = fmaxf(fmaxf(mrun[r], fmaxf(mg[0], mg[1])), fmaxf(mg[2], mg[3]));
+      float mg[kQW], lgv[kQW], sg[kQW];
+#pragma unroll
+      for (int j = 0; j < kQW / 4; ++j) {
+        const float4 m4 = reinterpret_cast<const float4*>(hb + Gm::kHM)[row * (kQW / 4) + j];
+        const float4 l4 = reinterpret_cast<const float4*>(hb + Gm::kHL)[row * (kQW / 4) + j];
+        const float4 s4 = reinterpret_cast<const float4*>(hb + Gm::kHSw)[row * (kQW / 4) + j];
+        mg[4 * j] = m4.x, mg[4 * j + 1] = m4.y, mg[4 * j + 2] = m4.z, mg[4 * j + 3] = m4.w;
+        lgv[4 * j] = l4.x, lgv[4 * j + 1] = l4.y, lgv[4 * j + 2] = l4.z, lgv[4 * j + 3] = l4.w;
+        sg[4 * j] = s4.x, sg[4 * j + 1] = s4.y, sg[4 * j + 2] = s4.z, sg[4 * j + 3] = s4.w;
+      }
+      float mn = mrun[r];
+#pragma unroll
+      for (int q = 0; q < kQW; ++q) mn = fmaxf(mn, mg[q]);
       const float alpha = (mrun[r] == -INFINITY) ? 0.f : ex2(mrun[r] - mn);
       float l = lrun[r] * alpha;
 #pragma unroll
@@ -1060,7 +1077,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     }
 
     // ---- V item: this warp's head-dims, every group of the unit ----
-    const int vslot = 2 * rg.kK + vpos.s;
+    const int vslot = kStreams * rg.kK + vpos.s;
     pipe_wait(&full[vslot], vpos.use & 1, abort_flag);
     vpos.next(rg.nV);
     const uint8_t* vb = ring + (size_t)vslot * kSlot;
@@ -1158,7 +1175,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     __syncwarp();
     if (lane == 0) mbar_arrive(&hempty[hbi]);
     wk = w1;
-    walk_next(w1, p.seq_lens, B, Hkv, maxL, kGran, g_end);
+    walk_next(w1, p.seq_lens, B, Hkv, maxL, kGran, g_end, Gm::kQW);
   }
 }
 
