@@ -120,3 +120,29 @@ def test_rope_producer_argument_checks_without_gpu(lib):
     assert call(smooth=P(16), q=P(16), q_i8=P(16), q_scale=P(16), Hq=6) == 1 and "multiple" in _last_error(lib)
     # rotary_dim 0 needs no table; T == 0 is a no-op after the shape checks
     assert call(rd=0, pos=None, cs=None, max_pos=0, T=0) == 0
+
+
+def test_prefill_route_decision_without_gpu(lib):
+    # i8kv_prefill_chunk reports its route before any launch: INT8 once the
+    # history reaches int8_min_history, the high-precision path below it; a
+    # zero-length chunk then returns without touching the device.
+    P = ctypes.c_void_p
+    f = lib.i8kv_prefill_chunk
+    f.restype = ctypes.c_int
+    f.argtypes = ([P] * 10 + [ctypes.c_int] * 8 + [ctypes.c_float, P, P, P, ctypes.c_size_t,
+                                                    ctypes.POINTER(ctypes.c_int), P])
+
+    def route(history, threshold):
+        r = ctypes.c_int(-1)
+        st = f(*([P(16)] * 10), history, 0, 24, 4, 256, 16, 10, threshold, 0.0, None, None, None, 0,
+               ctypes.byref(r), None)
+        assert st == 0
+        return r.value
+
+    BF16, INT8 = 0, 1  # I8KV_ROUTE_BF16, I8KV_ROUTE_INT8
+    assert route(0, 4096) == BF16 and route(4095, 4096) == BF16
+    assert route(4096, 4096) == INT8 and route(20000, 4096) == INT8
+    assert route(0, 0) == INT8  # threshold 0: every chunk INT8
+    # bad shapes are rejected before the route is used
+    r = ctypes.c_int(-1)
+    assert f(*([P(16)] * 10), 10, 4, 24, 5, 256, 16, 10, 0, 0.0, None, None, None, 0, ctypes.byref(r), None) != 0
