@@ -703,8 +703,16 @@ cudaError_t launch_prefix_d(const PrefixParams& p, cudaStream_t stream) {
   cudaError_t e = kBF ? launch_pdl(prefix_tiles_bf16_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p)
                       : launch_pdl(prefix_tiles_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(prefix_attn_kernel<D, kBF>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<D>::kTotal);
-  if (e != cudaSuccess) return e;
+  // the shared-memory opt-in, once per device (graph captures then make no attribute call)
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool opted[64] = {false};
+  if (dev < 0 || dev >= 64 || !opted[dev]) {
+    e = cudaFuncSetAttribute(prefix_attn_kernel<D, kBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Lay<D>::kTotal);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) opted[dev] = true;
+  }
   const int R = p.C * p.G;
   return launch_pdl(prefix_attn_kernel<D, kBF>, dim3((R + kRows - 1) / kRows, p.Hkv), dim3(kThreads),
                     Lay<D>::kTotal, stream, p);

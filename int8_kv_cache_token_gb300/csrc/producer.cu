@@ -414,12 +414,15 @@ cudaError_t launch_kv_rope_quant_write(const ProducerParams& p, cudaStream_t str
   // At most 16 x 256 x 4 + 2 x 8 x 256 x 4 + 8 x 16 x 256 = 64 KB; allow it past the default cap.
   constexpr int kMaxDyn = kTileTokens * 256 * 4 + 2 * kMaxHkvProducer * 256 * 4 + kMaxHkvProducer * kTileTokens * 256;
   auto kernel = p.D == 256 ? kv_quant_write_kernel<256, true> : kv_quant_write_kernel<128, true>;
-  static bool opted_in[2] = {false, false};  // per device process; setting it twice is harmless
-  bool& done = opted_in[p.D == 256 ? 1 : 0];
-  if (!done) {
+  // the shared-memory opt-in, once per (device, head_dim); setting it twice is harmless
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool opted_in[64][2] = {};
+  const bool track = dev >= 0 && dev < 64;
+  if (!track || !opted_in[dev][p.D == 256 ? 1 : 0]) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDyn);
     if (e != cudaSuccess) return e;
-    done = true;
+    if (track) opted_in[dev][p.D == 256 ? 1 : 0] = true;
   }
   return launch_pdl(kernel, dim3(grid), dim3(256), smem, stream, p);
 }
