@@ -113,26 +113,34 @@ __device__ __forceinline__ void s8x16_to_f16(const uint4& v, uint4& h0, uint4& h
 }
 
 // Maximum and sum of 32 values as balanced trees (depth 5 instead of a
-// 31-step chain); the sum's order is fixed, so every thread rounds alike.
+// 31-step chain); the sum's order is fixed, so every thread rounds alike.  The
+// maximum uses the three-input max (exact, so the grouping does not matter);
+// the sum adds pairs of adjacent partial sums with one packed add, the same
+// additions in the same order as the scalar tree.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ float tree_max(const float (&a)[32]) {
-  float t[16];
+  float t[11];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = fmaxf(a[i], a[i + 16]);
-#pragma unroll
-  for (int n = 8; n >= 1; n >>= 1)
-#pragma unroll
-    for (int i = 0; i < n; ++i) t[i] = fmaxf(t[i], t[i + n]);
-  return t[0];
+  for (int i = 0; i < 10; ++i) t[i] = max3(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+  t[10] = fmaxf(a[30], a[31]);
+  const float u0 = max3(t[0], t[1], t[2]), u1 = max3(t[3], t[4], t[5]), u2 = max3(t[6], t[7], t[8]);
+  const float u3 = fmaxf(t[9], t[10]);
+  return fmaxf(max3(u0, u1, u2), u3);
 }
 __device__ __forceinline__ float tree_sum(const float (&a)[32]) {
   float t[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = __fadd_rn(a[i], a[i + 16]);
+  for (int i = 0; i < 16; i += 2)
+    f2_split(add2(f2(a[i], a[i + 1]), f2(a[i + 16], a[i + 17])), t[i], t[i + 1]);
 #pragma unroll
-  for (int n = 8; n >= 1; n >>= 1)
+  for (int n = 8; n >= 2; n >>= 1)
 #pragma unroll
-    for (int i = 0; i < n; ++i) t[i] = __fadd_rn(t[i], t[i + n]);
-  return t[0];
+    for (int i = 0; i < n; i += 2) f2_split(add2(f2(t[i], t[i + 1]), f2(t[i + n], t[i + n + 1])), t[i], t[i + 1]);
+  return __fadd_rn(t[0], t[1]);
 }
 
 // Bounded wait that gives up at once when the CTA has aborted (error 1 after
