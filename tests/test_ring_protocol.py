@@ -7,7 +7,8 @@ landed.  This model replays the protocol with randomized agent speeds and
 out-of-order copy completion:
   * a producer fills K and V slots (refilling a slot only after its previous
     item was released);
-  * two QK streams take the even and odd units, each through its own K slots;
+  * the QK streams (two at head_dim 256: the even and the odd units; one at
+    head_dim 128: every unit) each take their units through their own K slots;
   * the PV warps take every unit's V slot and its handoff buffer (unit i uses
     buffer i % 4).
 The slot and phase formulas are the closed forms of the kernel's ring (struct
@@ -33,11 +34,11 @@ class Bar:
         return (self.n & 1) != (phase & 1)
 
 
-def kernel_ring(nslots):
+def kernel_ring(nslots, streams=2):
     kK = max(1, nslots // 6)
-    nV = nslots - 2 * kK
-    return dict(kslot=lambda i: (i % 2) * kK + (i // 2) % kK, kuse=lambda i: (i // 2) // kK,
-                vslot=lambda i: 2 * kK + i % nV, vuse=lambda i: i // nV)
+    nV = nslots - streams * kK
+    return dict(kslot=lambda i: (i % streams) * kK + (i // streams) % kK, kuse=lambda i: (i // streams) // kK,
+                vslot=lambda i: streams * kK + i % nV, vuse=lambda i: i // nV)
 
 
 def shared_ring(nslots):
@@ -45,7 +46,7 @@ def shared_ring(nslots):
                 vslot=lambda i: (2 * i + 1) % nslots, vuse=lambda i: (2 * i + 1) // nslots)
 
 
-def simulate(n_units, nslots, ring, seed, nhb=4):
+def simulate(n_units, nslots, ring, seed, nhb=4, streams=2):
     rnd = random.Random(seed)
     kslot, kuse, vslot, vuse = ring["kslot"], ring["kuse"], ring["vslot"], ring["vuse"]
     full = [Bar() for _ in range(nslots)]
@@ -64,7 +65,7 @@ def simulate(n_units, nslots, ring, seed, nhb=4):
                 yield
 
     def qk(st):
-        for i in range(st, n_units, 2):
+        for i in range(st, n_units, streams):
             s, u = kslot(i), kuse(i)
             while not full[s].passes(u):
                 yield
@@ -94,7 +95,9 @@ def simulate(n_units, nslots, ring, seed, nhb=4):
             hempty[hb].arrive()
             yield
 
-    agents = {"producer": producer(), "qk0": qk(0), "qk1": qk(1), "pv": pv()}
+    agents = {"producer": producer(), "pv": pv()}
+    for st in range(streams):
+        agents[f"qk{st}"] = qk(st)
     speed = {k: rnd.uniform(0.1, 1.0) for k in agents}
     for _ in range(200000):
         if not agents and not pending:
@@ -113,10 +116,11 @@ def simulate(n_units, nslots, ring, seed, nhb=4):
     raise AssertionError("deadlock")
 
 
+@pytest.mark.parametrize("streams", [1, 2])
 @pytest.mark.parametrize("nslots", [4, 6, 8, 12])
-def test_kernel_ring_never_reads_an_unlanded_slot(nslots):
+def test_kernel_ring_never_reads_an_unlanded_slot(nslots, streams):
     for seed in range(400):
-        simulate(random.Random(seed).randint(1, 30), nslots, kernel_ring(nslots), seed)
+        simulate(random.Random(seed).randint(1, 30), nslots, kernel_ring(nslots, streams), seed, streams=streams)
 
 
 def test_alternating_k_slots_do_race():
@@ -141,24 +145,26 @@ class RingPos:
             self.s, self.use = 0, self.use + 1
 
 
+@pytest.mark.parametrize("streams", [1, 2])
 @pytest.mark.parametrize("nslots", [4, 6, 8, 10, 12])
-def test_stepped_positions_equal_the_closed_forms(nslots):
+def test_stepped_positions_equal_the_closed_forms(nslots, streams):
     kK = max(1, nslots // 6)
-    nV = nslots - 2 * kK
-    ring = kernel_ring(nslots)
-    # producer: one K position per stream, swapped after every unit; one V position
+    nV = nslots - streams * kK
+    ring = kernel_ring(nslots, streams)
+    # producer: one K position per stream, swapped after every unit (two streams); one V position
     cur, oth, vp = RingPos(), RingPos(), RingPos()
     # consumers: each QK stream steps its own K position; the PV warps step the V position
-    qk = [RingPos(), RingPos()]
+    qk = [RingPos() for _ in range(streams)]
     pv = RingPos()
     for i in range(200):
-        assert ((i & 1) * kK + cur.s, cur.use) == (ring["kslot"](i), ring["kuse"](i))
+        assert ((i % streams) * kK + cur.s, cur.use) == (ring["kslot"](i), ring["kuse"](i))
         cur.next(kK)
-        cur, oth = oth, cur
-        assert (2 * kK + vp.s, vp.use) == (ring["vslot"](i), ring["vuse"](i))
+        if streams == 2:
+            cur, oth = oth, cur
+        assert (streams * kK + vp.s, vp.use) == (ring["vslot"](i), ring["vuse"](i))
         vp.next(nV)
-        st = i % 2
+        st = i % streams
         assert (st * kK + qk[st].s, qk[st].use) == (ring["kslot"](i), ring["kuse"](i))
         qk[st].next(kK)
-        assert (2 * kK + pv.s, pv.use) == (ring["vslot"](i), ring["vuse"](i))
+        assert (streams * kK + pv.s, pv.use) == (ring["vslot"](i), ring["vuse"](i))
         pv.next(nV)
