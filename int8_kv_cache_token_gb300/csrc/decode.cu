@@ -8,44 +8,46 @@
 // INT8 MMAC Attention推理优化" §3.3 (the decode data flow) and §2.3 (layouts).
 //
 // GB300 design (not the pages' gfx936 one): a persistent, warp-specialized CTA.
-//  * Work unit = (sequence, KV head, 128-token chunk).  The grid has one CTA per
-//    SM; CTA c takes the contiguous unit range [c U / N, (c+1) U / N).  A pair
-//    (sequence, KV head) that spans CTAs leaves one partial (o, m, l) per CTA in
-//    the workspace, and decode_merge_kernel combines them by log-sum-exp.  A
-//    unit is only a work granule: the pages' 256-token partition fixes no
-//    arithmetic here, because the group quantization below does not depend on
-//    where the softmax normalization is applied.
-//  * Producer warp: per unit, bulk copies (TMA) of the 8 K pages into one ring
-//    slot, together with the unit's K and V scales (cp.async, next to the
-//    pages), then the 8 V pages into the next slot.  Block-table entries are
-//    read one unit ahead.  Full/empty mbarriers
-//    guard the slots; even slots hold K items, odd slots V items.
-//  * 8 QK warps in two streams (warps 0-3 take the even units, 4-7 the odd
-//    ones); in a unit, warp w of a stream owns tokens 32w .. 32w+31, one
-//    probability group.  QK (M = 16 tokens, N = 8 GQA-packed query rows), the
-//    score recovery, the group's row maximum m_g, p~ = exp(s - m_g),
-//    W = p~ x sV, sW = max W / 127 and the codes Wq = round(W / sW).  The
-//    codes go to a handoff buffer (unit i uses buffer i % 4) as ready-made f16
-//    B fragments, with sW, m_g and the group's row sums l_g.  No QK warp waits
-//    for another: the group quantization gives the same codes for W scaled
-//    by any positive factor, so each group is quantized against its own
-//    maximum and brought to the common one afterwards.
+//  * Work unit = (sequence, KV head, a run of 32-token granules): 128 tokens at
+//    head_dim 256, 256 tokens at head_dim 128 (the same bytes per ring item).
+//    The grid has one CTA per SM; CTA c takes the contiguous granule range
+//    [c U / N, (c+1) U / N).  A pair (sequence, KV head) that spans CTAs leaves
+//    one partial (o, m, l) per CTA in the workspace, and decode_merge_kernel
+//    combines them by log-sum-exp.  A unit is only a work granule: the pages'
+//    256-token partition fixes no arithmetic here, because the group
+//    quantization below does not depend on where the softmax normalization is
+//    applied.
+//  * Producer warp: per unit, bulk copies (TMA) of the unit's K pages into a K
+//    slot of the unit's QK stream, together with the unit's K and V scales
+//    (cp.async, next to the pages), then its V pages into the next V slot.
+//    Block-table entries are read two units ahead.  Full/empty mbarriers guard
+//    the slots.
+//  * 8 QK warps in streams (two streams of 4 at head_dim 256, taking the even
+//    and the odd units; one stream of 8 at head_dim 128); in a unit, warp w of a
+//    stream owns tokens 32w .. 32w+31, one probability group.  QK on mma.sync
+//    m16n8k32 s8 (exact int32; M = 16 tokens, N = 8 GQA-packed query rows), the
+//    score recovery in log2 units, the group's row maximum m_g,
+//    p~ = 2^(s - m_g), W = p~ x sV, sW = max W / 127 and the codes
+//    Wq = round(W / sW).  The raw codes go to a handoff buffer (unit i uses
+//    buffer i % 4) as the PV MMA's B fragments, with sW, m_g and the group's
+//    row sums l_g.  No QK warp waits for another: the group quantization gives
+//    the same codes for W scaled by any positive factor, so each group is
+//    quantized against its own maximum and brought to the common one afterwards.
 //  * 8 PV warps: warp v owns head-dims [D/8 v, D/8 (v+1)) of the output and
 //    keeps the pair's running maximum m.  Per unit, m_new = max(m, m_g), the
-//    accumulator and l are rescaled once by exp(m - m_new), and group g adds
-//    exp(m_g - m_new) sW_g (Wq x Vq) (the exact INT8 product, K = the group's
-//    32 tokens) and exp(m_g - m_new) l_g.  The accumulator covers disjoint
-//    dims, so the end of a segment needs no cross-warp reduction: each PV warp
-//    writes its own dims (final output or partial).
+//    accumulator and l are rescaled once by 2^(m - m_new), and group g adds
+//    2^(m_g - m_new) sW_g (Wq x Vq) (mma.sync m16n8k32 s8, exact int32, K = the
+//    group's 32 tokens; s8 x u8 for UINT8 probability codes) and
+//    2^(m_g - m_new) l_g.  The accumulator covers disjoint dims, so the end of a
+//    segment needs no cross-warp reduction: each PV warp writes its own dims
+//    (final output or partial).
 //  * Ring slots: each QK stream has its own K slot(s), consumed in order, and
 //    the other slots carry V items in unit order, so every slot is refilled
 //    only after its previous item was consumed.
-//  * The INT8 x INT8 contractions run on the f16 tensor path: every int8 code is
-//    exact in f16, every product (<= 127^2) is exact, and every partial sum is
-//    an integer below 2^22 (QK over 256 dims: <= 4,129,024; PV over one group:
-//    <= 516,128), so the fp32 accumulator holds the exact int32 result.  On
-//    sm_103a this path has about 4x the throughput of mma.sync s8; the debug QK
-//    entry point checks the accumulators bit for bit against integer QK.
+//  * Every product (<= 127^2, or 255 x 127) and every sum (QK over 256 dims:
+//    <= 4,129,024; PV over one group: <= 1,036,320) is exact in int32 and in the
+//    fp32 rescale; the debug QK entry point checks the accumulators bit for bit
+//    against integer QK.
 #include <cuda_bf16.h>
 
 #include <mutex>

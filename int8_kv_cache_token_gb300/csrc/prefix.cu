@@ -44,6 +44,13 @@
 // (warps 4-7, 8-11) take the softmax of the even and the odd groups, thread =
 // row, so the two run side by side; both apply every group's product to their
 // half of the output dims.
+//
+// The same kernel, instantiated with kBF, is the high-precision chunk path
+// ("gfx936 DCU上实现INT8 KV与INT8 MMAC Attention推理优化" §3.1: the first
+// prefill chunk keeps a high-precision attention): bf16 Q and operand tiles
+// (history keys read back from the INT8 cache as bf16(code x scale), the
+// chunk's own keys as given), bf16 MMAs, and p~ handed to the PV MMA as bf16
+// with no group quantization.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
