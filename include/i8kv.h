@@ -256,9 +256,13 @@ i8kv_status i8kv_int8_decode_step(float* out, const uint16_t* q, const uint16_t*
 /*   bytes, 16-byte aligned, no initialization needed.  The call first      */
 /*   writes into it the sequence's K/V codes as f16 (exact) operand tiles,  */
 /*   one per (KV head, 32-key group), then runs the attention from them;    */
-/*   about 4.1 bytes per cached (token, KV head, head dim).  Calls that     */
-/*   overlap in time need separate workspaces.                              */
-/* The call launches two kernels (the tiles and the attention).             */
+/*   about 4.1 bytes per cached (token, KV head, head dim), plus room for   */
+/*   the split row blocks' partial results (2 x #SM x 128 rows x (D + 4)    */
+/*   fp32, #SM of the current device).  Calls that overlap in time need     */
+/*   separate workspaces.                                                   */
+/* The call launches two kernels (the tiles and the attention), and a third */
+/* that merges partial results when the last wave of 128-row blocks is      */
+/* split over its keys (more row blocks than SMs, not a multiple of them).  */
 /* ------------------------------------------------------------------------ */
 size_t i8kv_prefix_workspace_bytes(int history_len, int chunk_len, int Hkv, int D);
 

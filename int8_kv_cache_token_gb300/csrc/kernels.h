@@ -90,6 +90,12 @@ struct PrefixParams {
   const uint16_t* qb;       // [C, Hq, D]
   const uint16_t* k_chunk;  // [C, Hkv, D]
   const uint16_t* v_chunk;  // [C, Hkv, D]
+  // Work items (set by the launcher): row blocks (128 rows of one KV head) in
+  // order of decreasing cost; the first full_items run whole, each of the rest
+  // is split into split_k parts over its key groups, whose (o, m, l) go to part
+  // and are merged by a second kernel.
+  int nrb, full_items, split_k;
+  float* part;  // [split items][128 rows][D + 2]
 };
 
 // Per-translation-unit device error words (read and cleared).

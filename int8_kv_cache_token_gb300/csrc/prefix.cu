@@ -356,16 +356,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::oCtl + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int kvh = blockIdx.y;
   const int G = p.G, Hq = p.Hq, H = p.H, C = p.C;
   const int R = C * G;
-  // Row blocks in reverse: later chunk tokens see more keys, and CTAs start in
+  // Work item -> (row block, KV head, part).  Row blocks in reverse order, the
+  // KV heads interleaved: later chunk tokens see more keys, and CTAs start in
   // index order, so the heaviest blocks run first and the last wave holds the
-  // lightest ones.
-  const int r0 = (gridDim.x - 1 - blockIdx.x) * kRows;
+  // lightest ones -- which are split over their key groups (split_k parts), so
+  // that the last wave's work spreads over the SMs instead of leaving them idle.
+  int blk = blockIdx.x, part = 0, nparts = 1;
+  if (blk >= p.full_items) {
+    const int t = blk - p.full_items;
+    blk = p.full_items + t / p.split_k;
+    part = t % p.split_k;
+    nparts = p.split_k;
+  }
+  const int kvh = blk % p.Hkv;
+  const int r0 = (p.nrb - 1 - blk / p.Hkv) * kRows;
   const int j_hi = min(C - 1, (r0 + kRows - 1) / G);
   const int n_keys = H + j_hi + 1;
-  const int ng = (n_keys + kGroup - 1) / kGroup;
+  const int ng_all = (n_keys + kGroup - 1) / kGroup;
+  // this part's key groups [g_begin, g_begin + ng); the pipeline counts from 0
+  const int g_begin = (int)((long long)ng_all * part / nparts);
+  const int ng = (int)((long long)ng_all * (part + 1) / nparts) - g_begin;
   const int ngt = (H + C + kGroup - 1) / kGroup;  // groups of the whole sequence (tiles per KV head)
 
   if (tid == 0) {
@@ -436,7 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
         if (g >= kStages) pwait(&tile_free[st], ((g - kStages) / kStages) & 1, abort_flag);
         if (*abort_flag) break;
         mbar_expect_tx(&tile_full[st], T::kBytes);
-        bulk_g2s(smem + Ly::oTile + (size_t)st * T::kSlot, src + (size_t)g * T::kBytes, T::kBytes, &tile_full[st]);
+        bulk_g2s(smem + Ly::oTile + (size_t)st * T::kSlot, src + (size_t)(g_begin + g) * T::kBytes, T::kBytes,
+                 &tile_full[st]);
         mbar_arrive(&tile_full[st]);
       }
       // copies issued but never waited for (after an abort) land before the CTA exits
@@ -531,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
       tc_fence_after();
       float s[32];
       tmem_ld32(trow + 32 * sl, s);
-      const int key0 = g * kGroup;
+      const int key0 = (g_begin + g) * kGroup;
       const bool full = __all_sync(0xffffffffu, key0 + kGroup - 1 <= lim);  // no key of the warp is masked
       float mg, lg = 0.f, sw = 0.f;
       uint32_t pk[16];
@@ -694,8 +707,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
     }
     if (ng >= 1) update(ng - 1);
 
-    // ---- finish: O = o / l (both warpgroups hold the same l) ----
-    if (valid) {
+    // ---- finish: O = o / l (both warpgroups hold the same l), or this part's
+    // unnormalized (o, m, l) for the merge ----
+    if (valid && nparts > 1) {
+      float* ps = p.part + ((size_t)(blockIdx.x - p.full_items) * kRows + row) * (D + 4);
+#pragma unroll
+      for (int i = 0; i < DH / 4; ++i)
+        reinterpret_cast<float4*>(ps + wg * DH)[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+      if (wg == 0) {
+        ps[D] = m;
+        ps[D + 1] = l;
+      }
+    } else if (valid) {
       const float inv = 1.0f / l;
       float4* orow = reinterpret_cast<float4*>(p.out + ((size_t)j * Hq + hq) * D + wg * DH);
 #pragma unroll
@@ -712,8 +735,88 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
   }
 }
 
+// The split row blocks' parts, merged by log-sum-exp: one CTA of D/4 threads
+// per (split block, row), each thread one float4 column.  A part's (o, m, l) is
+// unnormalized, m in log2 units; a part that saw no key of the row has
+// m = -inf, l = 0 and o = 0.
+template <int D>
+__global__ void __launch_bounds__(D / 4) prefix_merge_kernel(PrefixParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int tb = blockIdx.x / kRows, row = blockIdx.x % kRows;
+  const int blk = p.full_items + tb;
+  const int kvh = blk % p.Hkv;
+  const int r = (p.nrb - 1 - blk / p.Hkv) * kRows + row;
+  if (r >= p.C * p.G) return;
+  const int j = r / p.G, hq = kvh * p.G + r % p.G;
+  const int k = p.split_k, col = threadIdx.x;
+  const float* base = p.part + ((size_t)tb * k * kRows + row) * (D + 4);
+  constexpr int kMaxParts = 8;
+  float mp[kMaxParts], lp[kMaxParts];
+  float4 op[kMaxParts];
+  float M = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kMaxParts; ++q) {
+    if (q < k) {
+      const float* ps = base + (size_t)q * kRows * (D + 4);
+      op[q] = reinterpret_cast<const float4*>(ps)[col];
+      mp[q] = ps[D];
+      lp[q] = ps[D + 1];
+      M = fmaxf(M, mp[q]);
+    }
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+#pragma unroll
+  for (int q = 0; q < kMaxParts; ++q) {
+    if (q < k && mp[q] != -INFINITY) {
+      const float w = ex2(__fsub_rn(mp[q], M));
+      acc.x = __fmaf_rn(op[q].x, w, acc.x);
+      acc.y = __fmaf_rn(op[q].y, w, acc.y);
+      acc.z = __fmaf_rn(op[q].z, w, acc.z);
+      acc.w = __fmaf_rn(op[q].w, w, acc.w);
+      den = __fmaf_rn(lp[q], w, den);
+    }
+  }
+  const float inv = 1.0f / den;
+  reinterpret_cast<float4*>(p.out + ((size_t)j * p.Hq + hq) * D)[col] =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
+constexpr int kMaxSplit = 6;
+
+// The number of SMs of the current device (the work split depends on it).
+static int device_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  return n;
+}
+
+// The last wave's split: with RB row blocks (one CTA each, one CTA per SM)
+// and N SMs, the tail RB mod N blocks would run with the rest of the SMs idle.
+// Each tail block is split into k parts over its key groups, k <= kMaxSplit
+// and tail * k <= 2 N (the workspace bound), choosing the k that minimizes the
+// tail's waves of parts per part: ceil(tail k / N) / k.  k = 1: no split.
+static void choose_split(int RB, int nsm, int& full_items, int& k) {
+  const int tail = RB > nsm ? RB % nsm : 0;
+  k = 1;
+  if (tail > 0) {
+    double best = 1.0;
+    for (int kk = 2; kk <= kMaxSplit && tail * kk <= 2 * nsm; ++kk) {
+      const double cost = (double)((tail * kk + nsm - 1) / nsm) / kk;
+      if (cost < best - 1e-9) {
+        best = cost;
+        k = kk;
+      }
+    }
+  }
+  full_items = k > 1 ? RB - tail : RB;
+}
+
 template <int D, bool kBF>
-cudaError_t launch_prefix_d(const PrefixParams& p, cudaStream_t stream) {
+cudaError_t launch_prefix_d(const PrefixParams& p0, cudaStream_t stream) {
+  PrefixParams p = p0;
   const int ngt = (p.H + p.C + kGroup - 1) / kGroup;
   cudaError_t e = kBF ? launch_pdl(prefix_tiles_bf16_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p)
                       : launch_pdl(prefix_tiles_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p);
@@ -729,15 +832,24 @@ cudaError_t launch_prefix_d(const PrefixParams& p, cudaStream_t stream) {
     if (dev >= 0 && dev < 64) opted[dev] = true;
   }
   const int R = p.C * p.G;
-  return launch_pdl(prefix_attn_kernel<D, kBF>, dim3((R + kRows - 1) / kRows, p.Hkv), dim3(kThreads),
-                    Lay<D>::kTotal, stream, p);
+  p.nrb = (R + kRows - 1) / kRows;
+  const int RB = p.nrb * p.Hkv;
+  choose_split(RB, device_sms(), p.full_items, p.split_k);
+  const int tail = RB - p.full_items;
+  p.part = reinterpret_cast<float*>(p.tiles + (size_t)ngt * p.Hkv * Tile<D>::kBytes);
+  e = launch_pdl(prefix_attn_kernel<D, kBF>, dim3(p.full_items + tail * p.split_k), dim3(kThreads), Lay<D>::kTotal,
+                 stream, p);
+  if (e != cudaSuccess || tail == 0) return e;
+  return launch_pdl(prefix_merge_kernel<D>, dim3(tail * kRows), dim3(D / 4), 0, stream, p);
 }
 
 }  // namespace
 
 size_t prefix_workspace_bytes(int H, int C, int Hkv, int D) {
   const size_t ngt = ((size_t)H + C + kGroup - 1) / kGroup;
-  return ngt * Hkv * (D == 256 ? Tile<256>::kBytes : Tile<128>::kBytes);
+  const size_t tiles = ngt * Hkv * (D == 256 ? Tile<256>::kBytes : Tile<128>::kBytes);
+  // the split parts' (o, m, l): at most 2 x #SM parts of 128 rows
+  return tiles + (size_t)2 * device_sms() * kRows * (D + 4) * sizeof(float);
 }
 
 cudaError_t launch_int8_prefix(const PrefixParams& p, cudaStream_t stream) {

@@ -115,3 +115,8 @@ def test_prefill_chunk_routes(H, thr):
         assert np.abs(host(out) - ref).max() <= 2e-3  # the INT8 path's own tolerance
     else:
         _check_close(host(out), ref, np.abs(wl.bf16_values(v)).max(), "routed bf16")
+
+
+def test_bf16_prefix_split_tail_blocks():
+    # 176 row blocks (700 tokens, 32 / 8 heads, head_dim 128): the tail is split
+    _run_bf16(wl.PrefixWorkload("bsplit", 32, 8, 128, 300, 700, seed=11))

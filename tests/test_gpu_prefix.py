@@ -70,3 +70,11 @@ def test_prefix_chunk_pages_shape_sampled():
     w = wl.prefix_chunk()
     rows = np.array([0, 1, 63, 64, 1000, 2047], np.int32)
     _prefix_parity(w, rows=rows)
+
+
+@pytest.mark.parametrize("H", [100, 1000])
+def test_prefix_split_tail_blocks(H):
+    # 700 chunk tokens x 32 q-heads over 8 KV heads = 176 row blocks of 128 rows,
+    # more than the SMs: the last wave's blocks are split over their key groups
+    # and merged by log-sum-exp; the whole chunk is checked against the oracle.
+    _prefix_parity(wl.PrefixWorkload("split", 32, 8, 128, H, 700, seed=H + 7))
