@@ -156,6 +156,25 @@ def whole_job_gbs(world: int, steps: int, bytes_per_step: int, ms: float) -> flo
     return world * steps * bytes_per_step / (ms / 1e3) / 1e9
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU baseline."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "hardware", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -190,6 +209,49 @@ def time_oracle(budget_s: float, nthreads: int):
         reps += 1
     gbs = reps * w.kv_bytes_int8() / t_total / 1e9
     return gbs, reps, t_total
+
+
+def time_oracle_prefix(budget_s: float, nthreads: int):
+    """Oracle prefix chunk (16384 history + 2048 chunk, 24 q / 4 KV heads, head_dim
+    256) on a bounded sample of chunk rows (all 24 heads each, evenly spaced
+    over the chunk), repeated for about budget_s; returns INT8 TOPS over the
+    sampled rows' causal pairs (4 D ops each), the rows and the time."""
+    from oracle import oracle as orc
+    w = wl.prefix_chunk()
+    k, v = w.kv()
+    cache = orc.kv_quant_write(k, v, w.slots(), w.num_blocks, w.block_size)
+    q = w.q()
+    n_rows = max(1, min(w.chunk, 2 * nthreads))
+    rows = np.linspace(0, w.chunk - 1, n_rows).astype(np.int32)
+    q_i8 = np.empty(q.shape, np.int8)
+    q_s = np.empty(q.shape[:2], np.float32)
+    for j in rows:
+        for h in range(w.Hq):
+            q_i8[j, h], q_s[j, h] = orc.quantize_vector(q[j, h])
+    ops = sum(w.Hq * (w.history + int(j) + 1) * 4 * w.D for j in rows)
+    reps, t_total = 0, 0.0
+    while t_total < budget_s or reps == 0:
+        t0 = time.perf_counter()
+        orc.prefix_attn(q_i8, q_s, cache, w.block_table, w.history, w.block_size, rows=rows, nthreads=nthreads)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return reps * ops / t_total / 1e12, len(rows), reps, t_total
+
+
+def cpu_baseline(seconds: float):
+    """The oracle on this host: the decode sample on all cores and on one thread,
+    and a prefix-chunk sample on all cores."""
+    cores = cpu_cores()
+    gbs, reps, el = time_oracle(seconds, cores)
+    gbs1, reps1, el1 = time_oracle(seconds, 1)
+    tops, nrows, preps, pel = time_oracle_prefix(seconds, cores)
+    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
+            "sample": f"{reps} oracle decodes of the 8192-token history (24 heads) in {el:.1f} s on {cores} threads",
+            "single_thread": {"value": gbs1, "unit": "GB/s", "cores": 1,
+                              "sample": f"{reps1} oracle decodes of the same history in {el1:.1f} s on 1 thread"},
+            "prefix": {"value": tops, "unit": "INT8 TOPS", "cores": cores,
+                       "sample": f"{preps} x {nrows} chunk rows (24 heads each) of the 16384 + 2048 chunk in "
+                                 f"{pel:.1f} s on {cores} threads"}}
 
 
 def run_reference(args):
@@ -232,7 +294,8 @@ def run_reference(args):
             "config": {"workload": "decode_outlier single-sequence, 24q/4kv heads, head_dim 256, history 8192 "
                                    "(bounded CPU sample)", "global_batch": 1, "seq_len": HISTORIES[0],
                        "parallelism": "host cores"},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+                             "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -300,7 +363,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl")
-    hbm_peak, _, peak_kind = measured_peaks()
+    hbm_peak, tensor_peak, peak_kind = measured_peaks()
     stream = torch.cuda.current_stream()
 
     # ---- inputs: one seeded history per length, cloned into every layer ----
@@ -400,7 +463,7 @@ def run_ours(args):
         secondary["decode_step_by_history"] = {
             str(L): {"us": v * 1e3} for L, v in step_by_len.items()}
         if not args.quick:
-            secondary.update(run_secondary(torch, i8, hbm_peak))
+            secondary.update(run_secondary(torch, i8, hbm_peak, tensor_peak, peak_kind))
             try:
                 secondary["decode_other_configs"] = run_batch_decodes(torch, i8, hbm_peak)
             except Exception as e:  # pragma: no cover - report, do not hide
@@ -417,10 +480,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        cores = cpu_cores()
-        gbs, reps, el = time_oracle(args.cpu_seconds, cores)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": f"{reps} oracle decodes of the 8192-token history (24 heads) in {el:.1f} s"}
+        cpu = cpu_baseline(args.cpu_seconds)
 
     if rank == 0:
         clocks = sampler.summary(wall0, wall1) if sampler else None
@@ -644,7 +704,13 @@ def run_batch_decodes(torch, i8, hbm_peak):
     return res
 
 
-def run_secondary(torch, i8, hbm_peak):
+def hbm_roofline(moved: int, ms: float, peak: float, kind: str, kernel: str) -> dict:
+    gbs = moved / (ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+            "peak_kind": f"of {kind} (HBM copy bandwidth)", "kernel": kernel, "algorithmic_bytes_per_launch": moved}
+
+
+def run_secondary(torch, i8, hbm_peak, tensor_peak=0.0, peak_kind="measured"):
     """Other rows of the path, each timed on its own (after the main region)."""
     res = {}
     # producer: 8192 new tokens, 8 KV heads, head_dim 128, 32 query heads
@@ -658,7 +724,9 @@ def run_secondary(torch, i8, hbm_peak):
         T, Hkv, Hq, D = 8192, p["Hkv"], p["Hq"], p["D"]
         moved = T * (2 * Hkv * D * 2 + 2 * Hkv * D + 2 * Hkv * 4) + T * Hq * (2 * D + D + 4)
         res["producer_8192x8x128"] = {"us": ms * 1e3, "gb_s": moved / (ms / 1e3) / 1e9,
-                                      "frac_hbm": moved / (ms / 1e3) / 1e9 / hbm_peak}
+                                      "frac_hbm": moved / (ms / 1e3) / 1e9 / hbm_peak,
+                                      "roofline": hbm_roofline(moved, ms, hbm_peak, peak_kind,
+                                                               "kv_quant_write_kernel<128, plain>")}
     except Exception as e:  # pragma: no cover - report, do not hide
         res["producer_8192x8x128"] = {"error": str(e)[:200]}
     # fused producer: the same tokens at positions 0..8191 with Q/K RMSNorm and
@@ -676,29 +744,53 @@ def run_secondary(torch, i8, hbm_peak):
         T, Hkv, Hq, D, rd = 8192, p["Hkv"], p["Hq"], p["D"], p["rotary_dim"]
         moved = (T * (2 * Hkv * D * 2 + 2 * Hkv * D + 2 * Hkv * 4) + T * Hq * (2 * D + D + 4) + T * (rd * 4 + 4))
         res["producer_rope_norm_8192x8x128"] = {"us": ms * 1e3, "gb_s": moved / (ms / 1e3) / 1e9,
-                                                "frac_hbm": moved / (ms / 1e3) / 1e9 / hbm_peak}
+                                                "frac_hbm": moved / (ms / 1e3) / 1e9 / hbm_peak,
+                                                "roofline": hbm_roofline(moved, ms, hbm_peak, peak_kind,
+                                                                         "kv_quant_write_kernel<128, fused>")}
     except Exception as e:  # pragma: no cover
         res["producer_rope_norm_8192x8x128"] = {"error": str(e)[:200]}
-    # prefix chunk: 2048 queries after 16384 cached tokens, 24 q / 4 kv heads, head_dim 256
+    # prefix chunk: 2048 queries after 16384 cached tokens, 24 q / 4 kv heads, head_dim 256.
+    # Three copies of the whole call's state (cache, operand-tile workspace,
+    # query, output: about 150 MB each, 3x L2) rotate inside one graph, so no
+    # call finds its tiles in L2; the unit timed is the whole call (tiles,
+    # attention, merge of the split last wave).
     try:
         w = wl.prefix_chunk()
         k, v = w.kv()
-        cache = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
-        i8.kv_quant_write(to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.slots()), **cache)
+        base = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+        i8.kv_quant_write(to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.slots()), **base)
         qd = to_dev(torch, w.q())
-        q_i8 = torch.empty(qd.shape, dtype=torch.int8, device="cuda")
-        q_s = torch.empty(qd.shape[:2], dtype=torch.float32, device="cuda")
         dummy = torch.zeros((w.chunk, w.Hkv, w.D), dtype=torch.bfloat16, device="cuda")
         none = torch.full((w.chunk,), -1, dtype=torch.int32, device="cuda")
-        i8.kv_quant_write(dummy, dummy, none, **cache, q=qd, q_i8=q_i8, q_scale=q_s)
-        out = torch.empty((w.chunk, w.Hq, w.D), dtype=torch.float32, device="cuda")
         bt = to_dev(torch, w.block_table)
-        pws = i8.prefix_workspace(w.history, w.chunk, w.Hkv, w.D)
-        ms = time_graph(torch, lambda: i8.int8_prefix_attn(out, q_i8, q_s, cache["k_cache"], cache["v_cache"],
-                                                           cache["k_scale"], cache["v_scale"], bt, w.history,
-                                                           workspace=pws), 5)
-        res["prefix_16384+2048"] = {"ms": ms, "int8_tops": w.int8_ops() / (ms / 1e3) / 1e12,
-                                    "pairs": w.pairs(), "ops": w.int8_ops()}
+        sets = []
+        for _ in range(3):
+            cache = {n: t.clone() for n, t in base.items()}
+            q_i8 = torch.empty(qd.shape, dtype=torch.int8, device="cuda")
+            q_s = torch.empty(qd.shape[:2], dtype=torch.float32, device="cuda")
+            i8.kv_quant_write(dummy, dummy, none, **cache, q=qd, q_i8=q_i8, q_scale=q_s)
+            out = torch.empty((w.chunk, w.Hq, w.D), dtype=torch.float32, device="cuda")
+            sets.append((cache, q_i8, q_s, out, i8.prefix_workspace(w.history, w.chunk, w.Hkv, w.D)))
+        del base
+        calls = [(lambda c=c, qi=qi, qs=qs, o=o, ws=ws: i8.int8_prefix_attn(
+            o, qi, qs, c["k_cache"], c["v_cache"], c["k_scale"], c["v_scale"], bt, w.history, workspace=ws))
+            for (c, qi, qs, o, ws) in sets]
+        ms = time_rotating(torch, calls, 4)
+        torch.cuda.synchronize()
+        assert i8.device_error() == 0
+        tops = w.int8_ops() / (ms / 1e3) / 1e12
+        res["prefix_16384+2048"] = {
+            "ms": ms, "int8_tops": tops, "pairs": w.pairs(), "ops": w.int8_ops(),
+            "roofline": {"bound": "tensor", "achieved": tops, "peak": tensor_peak, "unit": "TFLOP/s",
+                         "frac": tops / tensor_peak if tensor_peak else None,
+                         "peak_kind": f"of {peak_kind} dense bf16 (burst): the INT8 codes run exactly on the "
+                                      "tcgen05 f16 path, which has the bf16 rate",
+                         "kernel": "prefix_tiles_kernel + prefix_attn_kernel<256, INT8> + prefix_merge_kernel",
+                         "algorithmic_ops_per_launch": w.int8_ops(),
+                         "method": "3 rotating copies of cache + workspace + query + output (3x L2), 12 calls in "
+                                   "one CUDA graph, CUDA events around it"}}
+        del sets, calls
+        torch.cuda.empty_cache()
     except Exception as e:  # pragma: no cover
         res["prefix_16384+2048"] = {"error": str(e)[:200]}
     # first prefill chunk, 0 + 4096 tokens, 24 / 4 heads, head_dim 256: the routed
@@ -896,7 +988,8 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS)
     ap.add_argument("--quick", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="seconds of each of the three CPU oracle samples")
     ap.add_argument("--profile", action="store_true",
                     help="decode launches only (the three histories round-robin, --layers caches each) for ncu")
     ap.add_argument("--profile-step", action="store_true",

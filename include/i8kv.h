@@ -64,6 +64,12 @@ typedef enum {
   I8KV_ERR_DEVICE = 5       /* a kernel recorded a failure in the device error word */
 } i8kv_status;
 
+/* Element type of an attention output ([KV] §3.3: the decode merges its      */
+/* partitions and writes BF16).  I8KV_OUT_F32: fp32.  I8KV_OUT_BF16: the same  */
+/* fp32 results rounded to nearest-even bf16 (raw bit patterns), half the     */
+/* bytes.  Every attention entry point takes `void* out, int out_dtype`.      */
+typedef enum { I8KV_OUT_F32 = 0, I8KV_OUT_BF16 = 1 } i8kv_out_dtype;
+
 /* One-line description of the last non-OK status returned on this host thread.
  * Copies at most n-1 bytes plus a terminating NUL into buf (host memory). */
 i8kv_status i8kv_last_error(char* buf, size_t n);
@@ -156,7 +162,8 @@ i8kv_status i8kv_kv_rope_quant_write(const uint16_t* k, const uint16_t* v, const
 /*   query row is quantized with sW = max W / 127, Wq = round(W / sW), and   */
 /*   o_g += sW * (Wq x Vq) with an int32 contraction; partitions are merged   */
 /*   by log-sum-exp: O = sum_g l_g e^(m_g-M) o_g / sum_g l_g e^(m_g-M).      */
-/* out: fp32 [B, Hq, D].  seq_lens[b] == 0 gives a zero row.                 */
+/* out: [B, Hq, D] of out_dtype (fp32, or bf16 = RNE of the fp32 result),    */
+/*   16-byte aligned.  seq_lens[b] == 0 gives a zero row.                     */
 /* block_tables: int32 [B, max_blocks]; entries past ceil(L/bs) are unused.  */
 /* softmax_scale <= 0 selects 1/sqrt(D).  partition must be 256.             */
 /* workspace: device memory of at least i8kv_decode_workspace_bytes(...)     */
@@ -168,7 +175,8 @@ i8kv_status i8kv_kv_rope_quant_write(const uint16_t* k, const uint16_t* v, const
 /* ------------------------------------------------------------------------ */
 size_t i8kv_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int max_blocks, int block_size, int partition);
 
-i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
+i8kv_status i8kv_int8_paged_decode_attn(void* out, int out_dtype, const int8_t* q_i8, const float* q_scale,
+                                        const int8_t* k_cache,
                                         const int8_t* v_cache, const float* k_scale, const float* v_scale,
                                         const int32_t* block_tables, const int32_t* seq_lens, int B, int Hq, int Hkv,
                                         int D, int block_size, int max_blocks, int num_blocks, float softmax_scale,
@@ -182,7 +190,7 @@ i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const fl
 /* Wq = round-half-even(W / sW) in 0..255; PV = Wq x Vq on the s8 x u8 MMA   */
 /* (exact int32).  Arguments, layouts and workspace as above.                */
 /* ------------------------------------------------------------------------ */
-i8kv_status i8kv_int8_paged_decode_attn_u8p(float* out, const int8_t* q_i8, const float* q_scale,
+i8kv_status i8kv_int8_paged_decode_attn_u8p(void* out, int out_dtype, const int8_t* q_i8, const float* q_scale,
                                             const int8_t* k_cache, const int8_t* v_cache, const float* k_scale,
                                             const float* v_scale, const int32_t* block_tables,
                                             const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
@@ -195,16 +203,20 @@ i8kv_status i8kv_int8_paged_decode_attn_u8p(float* out, const int8_t* q_i8, cons
 /* device memory when they run a decode step -- for example a plugin inside  */
 /* another inference runtime, or a server whose memory planner reserved all  */
 /* device memory at start-up -- and so cannot provide a workspace.           */
-/* Same arguments and result as i8kv_int8_paged_decode_attn without the      */
-/* workspace: the merge scratch is a fixed 8 MiB array inside the library    */
+/* Same arguments and result as i8kv_int8_paged_decode_attn with an fp32 out  */
+/* and without the workspace: the merge scratch is a fixed 8 MiB array inside the library    */
 /* (8,388,608 bytes; every GPU that loads the library holds it until the     */
 /* process exits).  It calls no cudaMalloc or cudaFree.                      */
 /* Limit: i8kv_decode_workspace_bytes(B, Hq, Hkv, D, ...) must not exceed     */
 /* 8 MiB (about (B*Hkv + number of SMs) * (32*D + 64) bytes), else the call   */
 /* returns I8KV_ERR_WORKSPACE and launches nothing.                          */
-/* The first call on a device looks up the scratch's device address (with   */
-/* that device current), so make the first call on each device before any   */
-/* stream capture.  All calls share the one scratch area: calls            */
+/* The scratch's device address belongs to the CUDA context that loaded the */
+/* library's code: the first call in each context (the device's primary     */
+/* context, or a context the caller made current) looks it up and caches it */
+/* under that context's id, so make the first call in each context before   */
+/* any stream capture.  A device reset destroys the primary context; the    */
+/* first call after it looks the address up again, for the new context.     */
+/* All calls share the one scratch area: calls                              */
 /* that overlap on the GPU (other streams, other host threads) race and give */
 /* wrong results -- serialize them, e.g. on one stream.                      */
 /* ------------------------------------------------------------------------ */
@@ -233,7 +245,8 @@ i8kv_status i8kv_int8_paged_decode_attn_noalloc(float* out, const int8_t* q_i8, 
 /* no new token: a zero row and no write.  The output and the cache equal    */
 /* those of the two calls bit for bit.  q, k_new, v_new: 16-byte aligned.    */
 /* ------------------------------------------------------------------------ */
-i8kv_status i8kv_int8_decode_step(float* out, const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+i8kv_status i8kv_int8_decode_step(void* out, int out_dtype, const uint16_t* q, const uint16_t* k_new,
+                                  const uint16_t* v_new,
                                   int8_t* k_cache, int8_t* v_cache, float* k_scale, float* v_scale,
                                   const int32_t* block_tables, const int32_t* seq_lens, int B, int Hq, int Hkv, int D,
                                   int block_size, int max_blocks, int num_blocks, float softmax_scale, int partition,
@@ -251,7 +264,8 @@ i8kv_status i8kv_int8_decode_step(float* out, const uint16_t* q, const uint16_t*
 /*   Wq = round(W / sW), o = alpha o + sum sW (Wq x Vq), l = alpha l + sum p~,*/
 /*   O = o / l.                                                               */
 /* q_i8: int8 [chunk_len, Hq, D], q_scale: fp32 [chunk_len, Hq].             */
-/* out: fp32 [chunk_len, Hq, D].  softmax_scale <= 0 selects 1/sqrt(D).      */
+/* out: [chunk_len, Hq, D] of out_dtype, 16-byte aligned.                     */
+/* softmax_scale <= 0 selects 1/sqrt(D).                                     */
 /* workspace: device memory of at least i8kv_prefix_workspace_bytes(...)    */
 /*   bytes, 16-byte aligned, no initialization needed.  The call first      */
 /*   writes into it the sequence's K/V codes as f16 (exact) operand tiles,  */
@@ -266,7 +280,8 @@ i8kv_status i8kv_int8_decode_step(float* out, const uint16_t* q, const uint16_t*
 /* ------------------------------------------------------------------------ */
 size_t i8kv_prefix_workspace_bytes(int history_len, int chunk_len, int Hkv, int D);
 
-i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
+i8kv_status i8kv_int8_prefix_attn(void* out, int out_dtype, const int8_t* q_i8, const float* q_scale,
+                                  const int8_t* k_cache,
                                   const int8_t* v_cache, const float* k_scale, const float* v_scale,
                                   const int32_t* block_table, int history_len, int chunk_len, int Hq, int Hkv, int D,
                                   int block_size, int num_blocks, float softmax_scale, void* workspace,
@@ -285,13 +300,14 @@ i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q
 /*   [C, Hkv, D], as given.                                                  */
 /* S = Q K^T on bf16 tensor-core MMAs with fp32 accumulation; online softmax */
 /* in fp32 over 32-key groups; P = p~ rounded to bf16 for the P V MMA; the   */
-/* row sums l use the fp32 p~.  out: fp32 [C, Hq, D].                        */
+/* row sums l use the fp32 p~.  out: [C, Hq, D] of out_dtype.                */
 /* history_len == 0 (a first chunk): the cache pointers, block_table and     */
 /* num_blocks are not used and may be NULL / 0.                              */
 /* workspace: as for i8kv_int8_prefix_attn (same size function; the tiles    */
 /*   hold bf16 values instead of f16 codes).  Launches two kernels.          */
 /* ------------------------------------------------------------------------ */
-i8kv_status i8kv_bf16_prefix_attn(float* out, const uint16_t* q, const uint16_t* k_chunk, const uint16_t* v_chunk,
+i8kv_status i8kv_bf16_prefix_attn(void* out, int out_dtype, const uint16_t* q, const uint16_t* k_chunk,
+                                  const uint16_t* v_chunk,
                                   const int8_t* k_cache, const int8_t* v_cache, const float* k_scale,
                                   const float* v_scale, const int32_t* block_table, int history_len, int chunk_len,
                                   int Hq, int Hkv, int D, int block_size, int num_blocks, float softmax_scale,
@@ -315,7 +331,7 @@ i8kv_status i8kv_bf16_prefix_attn(float* out, const uint16_t* q, const uint16_t*
 /* ------------------------------------------------------------------------ */
 #define I8KV_ROUTE_BF16 0
 #define I8KV_ROUTE_INT8 1
-i8kv_status i8kv_prefill_chunk(float* out, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+i8kv_status i8kv_prefill_chunk(void* out, int out_dtype, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                const int32_t* slot_mapping, int8_t* k_cache, int8_t* v_cache, float* k_scale,
                                float* v_scale, const int32_t* block_table, int history_len, int chunk_len, int Hq,
                                int Hkv, int D, int block_size, int num_blocks, int int8_min_history,
@@ -334,6 +350,30 @@ i8kv_status i8kv_debug_qk_i32(int32_t* acc, const int8_t* q_i8, const int8_t* k_
                               int num_blocks, int max_len, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Debug: the prefix kernel's raw integer contractions ([PV] §3: INT8 Wq x   */
+/* Vq accumulated in int32, at most 32 x 127 x 127 per group; [PV] §2: INT8  */
+/* QK in int32).  Runs i8kv_int8_prefix_attn's kernels -- the same operand   */
+/* tiles, tensor-core descriptors and tensor-memory reads -- on the same     */
+/* arguments, writes the same fp32 out, and also records, for chunk row j    */
+/* (position H + j) and query head h, with NG = ceil((H + C) / 32):         */
+/*   s_acc  int32 [C, Hq, H + C]: S[t] = sum_d q_i8 * K_code[t] for every    */
+/*          visible key t <= H + j, 0 for the others;                        */
+/*   wq     uint8 [C, Hq, NG * 32]: the probability code Wq of each visible  */
+/*          key (0..127), 0 for the others;                                  */
+/*   pv_acc int32 [C, Hq, NG, D]: per 32-key group g the contraction         */
+/*          sum_{t in g} Wq[t] * V_code[t][d] as the kernel read it from     */
+/*          tensor memory; 0 for groups the row's block never reaches.       */
+/* The records are cleared on the stream first (cudaMemsetAsync).  Meant for */
+/* tests: the stores make it slow.                                          */
+/* ------------------------------------------------------------------------ */
+i8kv_status i8kv_debug_prefix_i32(int32_t* s_acc, uint8_t* wq, int32_t* pv_acc, float* out, const int8_t* q_i8,
+                                  const float* q_scale, const int8_t* k_cache, const int8_t* v_cache,
+                                  const float* k_scale, const float* v_scale, const int32_t* block_table,
+                                  int history_len, int chunk_len, int Hq, int Hkv, int D, int block_size,
+                                  int num_blocks, float softmax_scale, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* BF16-KV comparison path (the pages' BF16 control: same paging, bf16      */
 /* elements, bf16 tensor-core contractions, fp32 softmax; [KV] §4.2).       */
 /*   K cache bf16 [NB, Hkv, D/8, bs, 8], V cache bf16 [NB, Hkv, D, bs].      */
@@ -343,9 +383,10 @@ i8kv_status i8kv_bf16_kv_write(const uint16_t* k, const uint16_t* v, const int32
                                void* stream);
 
 /* Plain softmax decode attention over the bf16 cache with the same 256-token
- * partitions and log-sum-exp merge.  q: bf16 [B, Hq, D]; out: fp32 [B, Hq, D].
+ * partitions and log-sum-exp merge.  q: bf16 [B, Hq, D]; out: [B, Hq, D] of
+ * out_dtype.
  * The workspace follows the same rules and size as the INT8 decode's. */
-i8kv_status i8kv_bf16_paged_decode_attn(float* out, const uint16_t* q, const uint16_t* k_cache,
+i8kv_status i8kv_bf16_paged_decode_attn(void* out, int out_dtype, const uint16_t* q, const uint16_t* k_cache,
                                         const uint16_t* v_cache, const int32_t* block_tables,
                                         const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
                                         int max_blocks, int num_blocks, float softmax_scale, int partition,

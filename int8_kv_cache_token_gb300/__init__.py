@@ -5,6 +5,8 @@ this package holds its sources (csrc/), the in-tree build (build.py) and the
 thin ctypes binding (binding.py)."""
 from .binding import (  # noqa: F401
     BLOCK_SIZE,
+    OUT_BF16,
+    OUT_F32,
     PARTITION,
     ROUTE_BF16,
     ROUTE_INT8,
@@ -14,6 +16,7 @@ from .binding import (  # noqa: F401
     bf16_kv_write,
     bf16_paged_decode_attn,
     bf16_prefix_attn,
+    debug_prefix_i32,
     debug_qk_i32,
     decode_workspace,
     decode_workspace_bytes,

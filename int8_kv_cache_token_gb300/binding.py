@@ -16,6 +16,7 @@ import torch
 from . import build as _build
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE = range(6)
+OUT_F32, OUT_BF16 = 0, 1
 BLOCK_SIZE = 16
 PARTITION = 256
 
@@ -41,21 +42,23 @@ _SIGS = {
     "i8kv_kv_rope_quant_write": [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I, _P,
                                  _P, _F, _P, _P, _P, _P],
     "i8kv_decode_workspace_bytes": [_I, _I, _I, _I, _I, _I, _I],
-    "i8kv_int8_paged_decode_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z,
+    "i8kv_int8_paged_decode_attn": [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z,
                                     _P],
-    "i8kv_int8_paged_decode_attn_u8p": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P,
+    "i8kv_int8_paged_decode_attn_u8p": [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P,
                                         _Z, _P],
-    "i8kv_int8_decode_step": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P],
+    "i8kv_int8_decode_step": [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P],
     "i8kv_int8_paged_decode_attn_noalloc": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                             _P],
     "i8kv_prefix_workspace_bytes": [_I, _I, _I, _I],
-    "i8kv_int8_prefix_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _Z, _P],
-    "i8kv_bf16_prefix_attn": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _Z, _P],
-    "i8kv_prefill_chunk": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _Z,
+    "i8kv_int8_prefix_attn": [_P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _Z, _P],
+    "i8kv_bf16_prefix_attn": [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _Z, _P],
+    "i8kv_prefill_chunk": [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P, _Z,
                            _P, _P],
+    "i8kv_debug_prefix_i32": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _Z,
+                              _P],
     "i8kv_debug_qk_i32": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
     "i8kv_bf16_kv_write": [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P],
-    "i8kv_bf16_paged_decode_attn": [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P],
+    "i8kv_bf16_paged_decode_attn": [_P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P],
 }
 
 
@@ -115,6 +118,16 @@ def _ptr(t: torch.Tensor | None, dtype=None, name="tensor"):
     if dtype is not None and t.dtype != dtype:
         raise I8KVError(ERR_INVALID_ARG, f"{name} must be {dtype}, got {t.dtype}")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _out(t: torch.Tensor):
+    """An attention output: fp32, or bf16 (the fp32 result rounded to nearest even).
+    Returns (pointer, out_dtype code)."""
+    if t.dtype == torch.float32:
+        return _ptr(t, None, "out"), OUT_F32
+    if t.dtype == torch.bfloat16:
+        return _ptr(t, None, "out"), OUT_BF16
+    raise I8KVError(ERR_INVALID_ARG, f"out must be float32 or bfloat16, got {t.dtype}")
 
 
 def _stream(stream) -> ctypes.c_void_p:
@@ -221,14 +234,15 @@ def decode_workspace(B: int, Hq: int, Hkv: int, D: int, max_blocks: int, device=
 def int8_paged_decode_attn(out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
                            workspace, softmax_scale: float = 0.0, partition: int = PARTITION, stream=None,
                            u8_probs: bool = False):
-    """out [B, Hq, D] fp32 <- INT8 paged decode attention of q_i8 [B, Hq, D] over the cache.
+    """out [B, Hq, D] (float32, or bfloat16 = the fp32 result rounded to nearest even) <- INT8
+    paged decode attention of q_i8 [B, Hq, D] over the cache.
 
     u8_probs: UINT8 probability codes (0..255, sW = A / 255, s8 x u8 MMA) instead of 0..127."""
     NB, Hkv, D = _cache_geom(k_cache, 16)
     B, Hq, _ = q_i8.shape
     fn = lib().i8kv_int8_paged_decode_attn_u8p if u8_probs else lib().i8kv_int8_paged_decode_attn
     _check(fn(
-        _ptr(out, torch.float32, "out"), _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
+        *_out(out), _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
         _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
         _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
         _ptr(block_tables, torch.int32, "block_tables"), _ptr(seq_lens, torch.int32, "seq_lens"),
@@ -244,7 +258,7 @@ def int8_decode_step(out, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, b
     NB, Hkv, D = _cache_geom(k_cache, 16)
     B, Hq, _ = q.shape
     _check(lib().i8kv_int8_decode_step(
-        _ptr(out, torch.float32, "out"), _bf16(q, "q"), _bf16(k_new, "k_new"), _bf16(v_new, "v_new"),
+        *_out(out), _bf16(q, "q"), _bf16(k_new, "k_new"), _bf16(v_new, "v_new"),
         _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
         _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
         _ptr(block_tables, torch.int32, "block_tables"), _ptr(seq_lens, torch.int32, "seq_lens"),
@@ -272,7 +286,7 @@ def bf16_paged_decode_attn(out, q, k_cache, v_cache, block_tables, seq_lens, wor
     NB, Hkv, D = _cache_geom(k_cache, 8)
     B, Hq, _ = q.shape
     _check(lib().i8kv_bf16_paged_decode_attn(
-        _ptr(out, torch.float32, "out"), _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"),
+        *_out(out), _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"),
         _ptr(block_tables, torch.int32, "block_tables"), _ptr(seq_lens, torch.int32, "seq_lens"),
         B, Hq, Hkv, D, BLOCK_SIZE, block_tables.shape[1], NB, float(softmax_scale), partition,
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream)))
@@ -309,11 +323,37 @@ def int8_prefix_attn(out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, blo
     if workspace is None:
         workspace = prefix_workspace(int(history_len), C, Hkv, D, device=out.device)
     _check(lib().i8kv_int8_prefix_attn(
-        _ptr(out, torch.float32, "out"), _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
+        *_out(out), _ptr(q_i8, torch.int8, "q_i8"), _ptr(q_scale, torch.float32, "q_scale"),
         _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
         _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
         _ptr(block_table, torch.int32, "block_table"), int(history_len), C, Hq, Hkv, D, BLOCK_SIZE, NB,
         float(softmax_scale), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
+
+
+def debug_prefix_i32(q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, history_len: int,
+                     workspace=None, softmax_scale: float = 0.0, stream=None):
+    """The prefix kernel's raw integer contractions on int8_prefix_attn's arguments.
+    Returns (s_acc int32 [C, Hq, H + C], wq uint8 [C, Hq, NG * 32], pv_acc int32
+    [C, Hq, NG, D], out float32 [C, Hq, D]) with NG = ceil((H + C) / 32)."""
+    NB, Hkv, D = _cache_geom(k_cache, 16)
+    C, Hq, _ = q_i8.shape
+    H = int(history_len)
+    ng = (H + C + 31) // 32
+    dev = q_i8.device
+    s_acc = torch.empty((C, Hq, H + C), dtype=torch.int32, device=dev)
+    wq = torch.empty((C, Hq, ng * 32), dtype=torch.uint8, device=dev)
+    pv = torch.empty((C, Hq, ng, D), dtype=torch.int32, device=dev)
+    out = torch.empty((C, Hq, D), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = prefix_workspace(H, C, Hkv, D, device=dev)
+    _check(lib().i8kv_debug_prefix_i32(
+        _ptr(s_acc), _ptr(wq), _ptr(pv), _ptr(out), _ptr(q_i8, torch.int8, "q_i8"),
+        _ptr(q_scale, torch.float32, "q_scale"), _ptr(k_cache, torch.int8, "k_cache"),
+        _ptr(v_cache, torch.int8, "v_cache"), _ptr(k_scale, torch.float32, "k_scale"),
+        _ptr(v_scale, torch.float32, "v_scale"), _ptr(block_table, torch.int32, "block_table"), H, C, Hq, Hkv, D,
+        BLOCK_SIZE, NB, float(softmax_scale), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _stream(stream)))
+    return s_acc, wq, pv, out
 
 
 ROUTE_BF16, ROUTE_INT8 = 0, 1
@@ -333,7 +373,7 @@ def bf16_prefix_attn(out, q, k_chunk, v_chunk, history_len: int = 0, k_cache=Non
     if workspace is None:
         workspace = prefix_workspace(int(history_len), C, Hkv, D, device=out.device)
     _check(lib().i8kv_bf16_prefix_attn(
-        _ptr(out, torch.float32, "out"), _bf16(q, "q"), _bf16(k_chunk, "k_chunk"), _bf16(v_chunk, "v_chunk"),
+        *_out(out), _bf16(q, "q"), _bf16(k_chunk, "k_chunk"), _bf16(v_chunk, "v_chunk"),
         _ptr(k_cache, torch.int8, "k_cache"), _ptr(v_cache, torch.int8, "v_cache"),
         _ptr(k_scale, torch.float32, "k_scale"), _ptr(v_scale, torch.float32, "v_scale"),
         _ptr(block_table, torch.int32, "block_table"), int(history_len), C, Hq, Hkv, D, BLOCK_SIZE, NB,
@@ -352,7 +392,7 @@ def prefill_chunk(out, q, k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale
         workspace = prefix_workspace(int(history_len), C, Hkv, D, device=out.device)
     route = ctypes.c_int(-1)
     _check(lib().i8kv_prefill_chunk(
-        _ptr(out, torch.float32, "out"), _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"),
+        *_out(out), _bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"),
         _ptr(slot_mapping, torch.int32, "slot_mapping"), _ptr(k_cache, torch.int8, "k_cache"),
         _ptr(v_cache, torch.int8, "v_cache"), _ptr(k_scale, torch.float32, "k_scale"),
         _ptr(v_scale, torch.float32, "v_scale"), _ptr(block_table, torch.int32, "block_table"), int(history_len), C,

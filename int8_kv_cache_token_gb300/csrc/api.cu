@@ -46,6 +46,14 @@ i8kv_status check_heads(int Hq, int Hkv, int D) {
   return I8KV_OK;
 }
 
+i8kv_status check_out(const void* out, int out_dtype) {
+  REQUIRE(out_dtype == I8KV_OUT_F32 || out_dtype == I8KV_OUT_BF16, I8KV_ERR_INVALID_ARG,
+          "out_dtype=%d (I8KV_OUT_F32 or I8KV_OUT_BF16)", out_dtype);
+  REQUIRE(out != nullptr, I8KV_ERR_INVALID_ARG, "out is NULL");
+  REQUIRE(aligned16(out), I8KV_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  return I8KV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -173,9 +181,11 @@ static i8kv_status decode_common(i8kv::DecodeParams& p, const void* q, const flo
                                  const float* v_scale, const int32_t* block_tables, const int32_t* seq_lens, int B,
                                  int Hq, int Hkv, int D, int block_size, int max_blocks, int num_blocks,
                                  float softmax_scale, int partition, void* workspace, size_t workspace_bytes,
-                                 float* out) {
+                                 void* out, int out_dtype) {
   REQUIRE(B >= 0, I8KV_ERR_INVALID_ARG, "B=%d < 0", B);
   i8kv_status s = check_heads(Hq, Hkv, D);
+  if (s != I8KV_OK) return s;
+  s = check_out(out, out_dtype);
   if (s != I8KV_OK) return s;
   REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
   REQUIRE(partition == 256, I8KV_ERR_UNSUPPORTED, "partition %d not supported (256)", partition);
@@ -195,6 +205,7 @@ static i8kv_status decode_common(i8kv::DecodeParams& p, const void* q, const flo
   REQUIRE(aligned16(workspace), I8KV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   float* ws = static_cast<float*>(workspace);
   p.out = out;
+  p.out_bf16 = out_dtype == I8KV_OUT_BF16;
   p.q = q;
   p.q_scale = q_scale;
   p.k_cache = k_cache;
@@ -216,7 +227,8 @@ static i8kv_status decode_common(i8kv::DecodeParams& p, const void* q, const flo
   return I8KV_OK;
 }
 
-i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
+i8kv_status i8kv_int8_paged_decode_attn(void* out, int out_dtype, const int8_t* q_i8, const float* q_scale,
+                                        const int8_t* k_cache,
                                         const int8_t* v_cache, const float* k_scale, const float* v_scale,
                                         const int32_t* block_tables, const int32_t* seq_lens, int B, int Hq, int Hkv,
                                         int D, int block_size, int max_blocks, int num_blocks, float softmax_scale,
@@ -225,12 +237,12 @@ i8kv_status i8kv_int8_paged_decode_attn(float* out, const int8_t* q_i8, const fl
   i8kv::DecodeParams p{};
   i8kv_status s = decode_common(p, q_i8, q_scale, true, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
                                 B, Hq, Hkv, D, block_size, max_blocks, num_blocks, softmax_scale, partition,
-                                workspace, workspace_bytes, out);
+                                workspace, workspace_bytes, out, out_dtype);
   if (s != I8KV_OK || B == 0) return s;
   return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "int8 decode launch");
 }
 
-i8kv_status i8kv_int8_paged_decode_attn_u8p(float* out, const int8_t* q_i8, const float* q_scale,
+i8kv_status i8kv_int8_paged_decode_attn_u8p(void* out, int out_dtype, const int8_t* q_i8, const float* q_scale,
                                             const int8_t* k_cache, const int8_t* v_cache, const float* k_scale,
                                             const float* v_scale, const int32_t* block_tables,
                                             const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
@@ -240,13 +252,14 @@ i8kv_status i8kv_int8_paged_decode_attn_u8p(float* out, const int8_t* q_i8, cons
   i8kv::DecodeParams p{};
   i8kv_status s = decode_common(p, q_i8, q_scale, true, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
                                 B, Hq, Hkv, D, block_size, max_blocks, num_blocks, softmax_scale, partition,
-                                workspace, workspace_bytes, out);
+                                workspace, workspace_bytes, out, out_dtype);
   if (s != I8KV_OK || B == 0) return s;
   p.u8_probs = 1;
   return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "int8 decode (u8 P) launch");
 }
 
-i8kv_status i8kv_int8_decode_step(float* out, const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new,
+i8kv_status i8kv_int8_decode_step(void* out, int out_dtype, const uint16_t* q, const uint16_t* k_new,
+                                  const uint16_t* v_new,
                                   int8_t* k_cache, int8_t* v_cache, float* k_scale, float* v_scale,
                                   const int32_t* block_tables, const int32_t* seq_lens, int B, int Hq, int Hkv, int D,
                                   int block_size, int max_blocks, int num_blocks, float softmax_scale, int partition,
@@ -256,7 +269,7 @@ i8kv_status i8kv_int8_decode_step(float* out, const uint16_t* q, const uint16_t*
   i8kv::DecodeParams p{};
   i8kv_status s = decode_common(p, q, nullptr, true, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, B,
                                 Hq, Hkv, D, block_size, max_blocks, num_blocks, softmax_scale, partition, workspace,
-                                workspace_bytes, out);
+                                workspace_bytes, out, out_dtype);
   if (s != I8KV_OK || B == 0) return s;
   p.step = 1;
   p.q_bf16 = q;
@@ -290,11 +303,12 @@ i8kv_status i8kv_int8_paged_decode_attn_noalloc(float* out, const int8_t* q_i8, 
           "(use i8kv_int8_paged_decode_attn with a caller workspace)",
           need, B, Hkv, D, i8kv::noalloc_scratch_bytes());
   void* scratch = nullptr;
-  e = i8kv::noalloc_scratch_address(dev, &scratch);
+  e = i8kv::noalloc_scratch_address(&scratch);
   if (e != cudaSuccess) return from_cuda(e, "noalloc decode: cudaGetSymbolAddress");
   i8kv::DecodeParams p{};
   s = decode_common(p, q_i8, q_scale, true, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, B, Hq, Hkv,
-                    D, block_size, max_blocks, num_blocks, softmax_scale, partition, scratch, need, out);
+                    D, block_size, max_blocks, num_blocks, softmax_scale, partition, scratch, need, out,
+                    I8KV_OUT_F32);
   if (s != I8KV_OK || B == 0) return s;
   return from_cuda(i8kv::launch_int8_decode(p, static_cast<cudaStream_t>(stream)), "noalloc int8 decode launch");
 }
@@ -304,7 +318,8 @@ size_t i8kv_prefix_workspace_bytes(int history_len, int chunk_len, int Hkv, int 
   return i8kv::prefix_workspace_bytes(history_len, chunk_len, Hkv, D);
 }
 
-i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q_scale, const int8_t* k_cache,
+i8kv_status i8kv_int8_prefix_attn(void* out, int out_dtype, const int8_t* q_i8, const float* q_scale,
+                                  const int8_t* k_cache,
                                   const int8_t* v_cache, const float* k_scale, const float* v_scale,
                                   const int32_t* block_table, int history_len, int chunk_len, int Hq, int Hkv, int D,
                                   int block_size, int num_blocks, float softmax_scale, void* workspace,
@@ -316,7 +331,9 @@ i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q
   REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
   REQUIRE(num_blocks > 0, I8KV_ERR_INVALID_ARG, "num_blocks=%d", num_blocks);
   if (chunk_len == 0) return I8KV_OK;
-  REQUIRE(out && q_i8 && q_scale && k_cache && v_cache && k_scale && v_scale && block_table, I8KV_ERR_INVALID_ARG,
+  s = check_out(out, out_dtype);
+  if (s != I8KV_OK) return s;
+  REQUIRE(q_i8 && q_scale && k_cache && v_cache && k_scale && v_scale && block_table, I8KV_ERR_INVALID_ARG,
           "null pointer");
   REQUIRE(aligned16(k_cache) && aligned16(v_cache) && aligned16(q_i8) && aligned16(k_scale) && aligned16(v_scale),
           I8KV_ERR_INVALID_ARG, "caches, scales and q must be 16-byte aligned");
@@ -327,10 +344,12 @@ i8kv_status i8kv_int8_prefix_attn(float* out, const int8_t* q_i8, const float* q
   i8kv::PrefixParams p{out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, history_len, chunk_len,
                        Hq, Hkv, Hq / Hkv, D, num_blocks, softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D),
                        static_cast<uint8_t*>(workspace)};
+  p.out_bf16 = out_dtype == I8KV_OUT_BF16;
   return from_cuda(i8kv::launch_int8_prefix(p, static_cast<cudaStream_t>(stream)), "int8 prefix launch");
 }
 
-i8kv_status i8kv_bf16_prefix_attn(float* out, const uint16_t* q, const uint16_t* k_chunk, const uint16_t* v_chunk,
+i8kv_status i8kv_bf16_prefix_attn(void* out, int out_dtype, const uint16_t* q, const uint16_t* k_chunk,
+                                  const uint16_t* v_chunk,
                                   const int8_t* k_cache, const int8_t* v_cache, const float* k_scale,
                                   const float* v_scale, const int32_t* block_table, int history_len, int chunk_len,
                                   int Hq, int Hkv, int D, int block_size, int num_blocks, float softmax_scale,
@@ -341,9 +360,11 @@ i8kv_status i8kv_bf16_prefix_attn(float* out, const uint16_t* q, const uint16_t*
   if (s != I8KV_OK) return s;
   REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
   if (chunk_len == 0) return I8KV_OK;
-  REQUIRE(out && q && k_chunk && v_chunk, I8KV_ERR_INVALID_ARG, "null out/q/k_chunk/v_chunk pointer");
-  REQUIRE(aligned16(q) && aligned16(k_chunk) && aligned16(v_chunk) && aligned16(out), I8KV_ERR_INVALID_ARG,
-          "out, q, k_chunk and v_chunk must be 16-byte aligned");
+  s = check_out(out, out_dtype);
+  if (s != I8KV_OK) return s;
+  REQUIRE(q && k_chunk && v_chunk, I8KV_ERR_INVALID_ARG, "null q/k_chunk/v_chunk pointer");
+  REQUIRE(aligned16(q) && aligned16(k_chunk) && aligned16(v_chunk), I8KV_ERR_INVALID_ARG,
+          "q, k_chunk and v_chunk must be 16-byte aligned");
   if (history_len > 0) {
     REQUIRE(num_blocks > 0, I8KV_ERR_INVALID_ARG, "num_blocks=%d", num_blocks);
     REQUIRE(k_cache && v_cache && k_scale && v_scale && block_table, I8KV_ERR_INVALID_ARG,
@@ -360,10 +381,11 @@ i8kv_status i8kv_bf16_prefix_attn(float* out, const uint16_t* q, const uint16_t*
   p.qb = q;
   p.k_chunk = k_chunk;
   p.v_chunk = v_chunk;
+  p.out_bf16 = out_dtype == I8KV_OUT_BF16;
   return from_cuda(i8kv::launch_bf16_prefix(p, static_cast<cudaStream_t>(stream)), "bf16 prefix launch");
 }
 
-i8kv_status i8kv_prefill_chunk(float* out, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+i8kv_status i8kv_prefill_chunk(void* out, int out_dtype, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                const int32_t* slot_mapping, int8_t* k_cache, int8_t* v_cache, float* k_scale,
                                float* v_scale, const int32_t* block_table, int history_len, int chunk_len, int Hq,
                                int Hkv, int D, int block_size, int num_blocks, int int8_min_history,
@@ -376,8 +398,10 @@ i8kv_status i8kv_prefill_chunk(float* out, const uint16_t* q, const uint16_t* k,
   const bool int8 = history_len >= int8_min_history;
   if (route) *route = int8 ? I8KV_ROUTE_INT8 : I8KV_ROUTE_BF16;
   if (chunk_len == 0) return I8KV_OK;
-  REQUIRE(out && q && block_table && k_cache && v_cache && k_scale && v_scale, I8KV_ERR_INVALID_ARG,
-          "null out/q/block_table/cache pointer");
+  s = check_out(out, out_dtype);
+  if (s != I8KV_OK) return s;
+  REQUIRE(q && block_table && k_cache && v_cache && k_scale && v_scale, I8KV_ERR_INVALID_ARG,
+          "null q/block_table/cache pointer");
   if (int8) REQUIRE(q_i8 && q_scale, I8KV_ERR_INVALID_ARG, "the INT8 route needs q_i8 and q_scale");
   const size_t need = i8kv::prefix_workspace_bytes(history_len, chunk_len, Hkv, D);
   REQUIRE(workspace != nullptr && workspace_bytes >= need, I8KV_ERR_WORKSPACE,
@@ -387,11 +411,43 @@ i8kv_status i8kv_prefill_chunk(float* out, const uint16_t* q, const uint16_t* k,
                           v_scale, int8 ? q : nullptr, Hq, q_i8, q_scale, stream);
   if (s != I8KV_OK) return s;
   if (int8)
-    return i8kv_int8_prefix_attn(out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, history_len,
+    return i8kv_int8_prefix_attn(out, out_dtype, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, history_len,
                                  chunk_len, Hq, Hkv, D, block_size, num_blocks, softmax_scale, workspace,
                                  workspace_bytes, stream);
-  return i8kv_bf16_prefix_attn(out, q, k, v, k_cache, v_cache, k_scale, v_scale, block_table, history_len, chunk_len,
+  return i8kv_bf16_prefix_attn(out, out_dtype, q, k, v, k_cache, v_cache, k_scale, v_scale, block_table, history_len, chunk_len,
                                Hq, Hkv, D, block_size, num_blocks, softmax_scale, workspace, workspace_bytes, stream);
+}
+
+i8kv_status i8kv_debug_prefix_i32(int32_t* s_acc, uint8_t* wq, int32_t* pv_acc, float* out, const int8_t* q_i8,
+                                  const float* q_scale, const int8_t* k_cache, const int8_t* v_cache,
+                                  const float* k_scale, const float* v_scale, const int32_t* block_table,
+                                  int history_len, int chunk_len, int Hq, int Hkv, int D, int block_size,
+                                  int num_blocks, float softmax_scale, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  REQUIRE(history_len >= 0 && chunk_len >= 0, I8KV_ERR_INVALID_ARG, "history_len=%d chunk_len=%d", history_len,
+          chunk_len);
+  i8kv_status s = check_heads(Hq, Hkv, D);
+  if (s != I8KV_OK) return s;
+  REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+  REQUIRE(num_blocks > 0, I8KV_ERR_INVALID_ARG, "num_blocks=%d", num_blocks);
+  if (chunk_len == 0) return I8KV_OK;
+  s = check_out(out, I8KV_OUT_F32);
+  if (s != I8KV_OK) return s;
+  REQUIRE(s_acc && wq && pv_acc && q_i8 && q_scale && k_cache && v_cache && k_scale && v_scale && block_table,
+          I8KV_ERR_INVALID_ARG, "null pointer");
+  REQUIRE(aligned16(k_cache) && aligned16(v_cache) && aligned16(q_i8) && aligned16(k_scale) && aligned16(v_scale),
+          I8KV_ERR_INVALID_ARG, "caches, scales and q must be 16-byte aligned");
+  const size_t need = i8kv::prefix_workspace_bytes(history_len, chunk_len, Hkv, D);
+  REQUIRE(workspace != nullptr && workspace_bytes >= need, I8KV_ERR_WORKSPACE,
+          "prefix workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+  REQUIRE(aligned16(workspace), I8KV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  i8kv::PrefixParams p{out, q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, history_len, chunk_len,
+                       Hq, Hkv, Hq / Hkv, D, num_blocks, softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D),
+                       static_cast<uint8_t*>(workspace)};
+  p.dbg_s = s_acc;
+  p.dbg_wq = wq;
+  p.dbg_pv = pv_acc;
+  return from_cuda(i8kv::launch_debug_prefix(p, static_cast<cudaStream_t>(stream)), "debug prefix launch");
 }
 
 i8kv_status i8kv_debug_qk_i32(int32_t* acc, const int8_t* q_i8, const int8_t* k_cache, const int32_t* block_tables,
@@ -429,7 +485,7 @@ i8kv_status i8kv_bf16_kv_write(const uint16_t* k, const uint16_t* v, const int32
                    "bf16 kv write launch");
 }
 
-i8kv_status i8kv_bf16_paged_decode_attn(float* out, const uint16_t* q, const uint16_t* k_cache,
+i8kv_status i8kv_bf16_paged_decode_attn(void* out, int out_dtype, const uint16_t* q, const uint16_t* k_cache,
                                         const uint16_t* v_cache, const int32_t* block_tables,
                                         const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
                                         int max_blocks, int num_blocks, float softmax_scale, int partition,
@@ -437,7 +493,7 @@ i8kv_status i8kv_bf16_paged_decode_attn(float* out, const uint16_t* q, const uin
   i8kv::DecodeParams p{};
   i8kv_status s = decode_common(p, q, nullptr, false, k_cache, v_cache, nullptr, nullptr, block_tables, seq_lens, B,
                                 Hq, Hkv, D, block_size, max_blocks, num_blocks, softmax_scale, partition, workspace,
-                                workspace_bytes, out);
+                                workspace_bytes, out, out_dtype);
   if (s != I8KV_OK || B == 0) return s;
   return from_cuda(i8kv::launch_bf16_decode(p, static_cast<cudaStream_t>(stream)), "bf16 decode launch");
 }

@@ -496,6 +496,30 @@ __device__ __forceinline__ float div255(float a) {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
+// Two fp32 values rounded to nearest-even bf16, packed {lo, hi} (cvt.rn.bf16x2).
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Attention outputs are fp32 or, when out_bf16 is set, the same fp32 values
+// rounded to nearest-even bf16 (the pages' decode writes BF16 after the
+// partition merge).  `i` is an element index into [rows, D].
+__device__ __forceinline__ void store_out1(void* out, int out_bf16, size_t i, float v) {
+  if (out_bf16)
+    static_cast<uint16_t*>(out)[i] = (uint16_t)(bf16x2_rn(v, 0.f) & 0xffffu);
+  else
+    static_cast<float*>(out)[i] = v;
+}
+// Four consecutive elements, i a multiple of 4 (16-byte fp32 or 8-byte bf16 store).
+__device__ __forceinline__ void store_out4(void* out, int out_bf16, size_t i, float4 v) {
+  if (out_bf16)
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + i) = make_uint2(bf16x2_rn(v.x, v.y), bf16x2_rn(v.z, v.w));
+  else
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + i) = v;
+}
+
 // Host: launch `kernel` with programmatic stream serialization allowed, so its
 // launch overlaps the tail of the previous kernel on `stream` (the kernel must
 // call griddep_wait() before it touches memory the previous kernel writes).

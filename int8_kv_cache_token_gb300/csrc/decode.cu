@@ -600,8 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         h = len_hash(h, raw);
         if (raw > maxL) record_error(2);
         if (clamp_len(raw, maxL) == 0 && b % N == c) {
-          float* o = p.out + (size_t)b * Hq * D;
-          for (int i = 0; i < Hq * D; ++i) o[i] = 0.f;
+          for (int i = 0; i < Hq * D; i += 4)
+            store_out4(p.out, p.out_bf16, (size_t)b * Hq * D + i, make_float4(0.f, 0.f, 0.f, 0.f));
         }
       }
     }
@@ -1146,14 +1146,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       const int cf = cta_of(Up, U, Nw), cl = cta_of(Up + wk.ngp - 1, U, Nw);
       const int d0 = pv_w * Gm::kDimsPW;
       if (cf == cl) {
-        float* dst = p.out + ((size_t)wk.b * Hq + wk.kvh * G) * D;
+        const size_t dst = ((size_t)wk.b * Hq + wk.kvh * G) * D;
         const float inv0 = 1.0f / lrun[0], inv1 = 1.0f / lrun[1];
 #pragma unroll
         for (int dt = 0; dt < NDT; ++dt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int row = 2 * t + (e & 1);
-            if (row < G) dst[(size_t)row * D + d0 + dt * 16 + g + 8 * (e >> 1)] = o[dt][e] * ((e & 1) ? inv1 : inv0);
+            if (row < G)
+              store_out1(p.out, p.out_bf16, dst + (size_t)row * D + d0 + dt * 16 + g + 8 * (e >> 1),
+                         o[dt][e] * ((e & 1) ? inv1 : inv0));
           }
       } else {
         // one partial per CTA; decode_merge_kernel combines them after this kernel
@@ -1313,8 +1315,8 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
     }
     const float inv = 1.0f / dd;
     const int b = pair / p.Hkv, kvh = pair % p.Hkv;
-    *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + kvh * p.G + row) * D + 4 * tid) =
-        make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv);
+    store_out4(p.out, p.out_bf16, ((size_t)b * p.Hq + kvh * p.G + row) * D + 4 * tid,
+               make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv));
   }
 }
 
@@ -1464,22 +1466,75 @@ constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace {
+// The array's device address belongs to the CUDA context that loaded this
+// module: another context on the same device (a plugin's own context), or the
+// new primary context after a device reset, has its own copy at another
+// address.  So the address is cached per context, keyed by the context's
+// unique id (cuCtxGetId; ids are never reused within a process).  The driver
+// calls are reached through the runtime's entry-point lookup, so the library
+// needs no link-time dependency on the driver library.
+typedef int (*CtxGetCurrentFn)(void** ctx);
+typedef int (*CtxGetIdFn)(void* ctx, unsigned long long* id);
+
+struct NoAllocEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+constexpr int kNoAllocContexts = 32;
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64] = {};
+NoAllocEntry g_noalloc_cache[kNoAllocContexts] = {};
+int g_noalloc_next = 0;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+bool g_ctx_fns_looked_up = false;
+
+// Id of the calling thread's current context; 0 when it cannot be told (then
+// the address is looked up on every call).  Called with g_noalloc_mu held.
+unsigned long long current_context_id() {
+  if (!g_ctx_fns_looked_up) {
+    g_ctx_fns_looked_up = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+  }
+  if (!g_ctx_get_current || !g_ctx_get_id) return 0;
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (g_ctx_get_current(&ctx) != 0 || ctx == nullptr) return 0;
+  if (g_ctx_get_id(ctx, &id) != 0) return 0;
+  return id;
+}
 }  // namespace
 
 size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 
-cudaError_t noalloc_scratch_address(int device, void** addr) {
-  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+cudaError_t noalloc_scratch_address(void** addr) {
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_addr[device] == nullptr) {
-    void* ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_noalloc_addr[device] = ptr;
+  unsigned long long id = current_context_id();
+  if (id != 0) {
+    for (const NoAllocEntry& en : g_noalloc_cache)
+      if (en.ctx_id == id) {
+        *addr = en.addr;
+        return cudaSuccess;
+      }
   }
-  *addr = g_noalloc_addr[device];
+  // Not cached for this context (or no context is current yet: the runtime
+  // then makes the device's primary context current here).
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  if (id == 0) id = current_context_id();
+  if (id != 0) {
+    g_noalloc_cache[g_noalloc_next] = NoAllocEntry{id, ptr};
+    g_noalloc_next = (g_noalloc_next + 1) % kNoAllocContexts;
+  }
+  *addr = ptr;
   return cudaSuccess;
 }
 

@@ -35,7 +35,8 @@ struct ProducerParams {
 
 // Decode (INT8 and BF16-KV variants share the work split and the workspace).
 struct DecodeParams {
-  float* out;                 // [B, Hq, D]
+  void* out;                  // [B, Hq, D], fp32 or (out_bf16) bf16
+  int out_bf16;
   const void* q;              // int8 [B, Hq, D] (INT8 path) or bf16 [B, Hq, D] (BF16 path)
   const float* q_scale;       // [B, Hq] (INT8 path)
   const void* k_cache;
@@ -74,7 +75,7 @@ struct DebugQKParams {
 };
 
 struct PrefixParams {
-  float* out;                 // [C, Hq, D]
+  void* out;                  // [C, Hq, D], fp32 or (out_bf16) bf16
   const int8_t* q;            // [C, Hq, D]
   const float* q_scale;       // [C, Hq]
   const int8_t* k_cache;
@@ -96,6 +97,12 @@ struct PrefixParams {
   // and are merged by a second kernel.
   int nrb, full_items, split_k;
   float* part;  // [split items][128 rows][D + 2]
+  int out_bf16;
+  // Debug record (i8kv_debug_prefix_i32): S [C, Hq, H + C], Wq [C, Hq, NG * 32]
+  // and PV [C, Hq, NG, D] with NG = ceil((H + C) / 32).
+  int32_t* dbg_s;
+  uint8_t* dbg_wq;
+  int32_t* dbg_pv;
 };
 
 // Per-translation-unit device error words (read and cleared).
@@ -117,8 +124,11 @@ cudaError_t launch_debug_qk(const DebugQKParams& p, cudaStream_t stream);
 
 // Fixed device scratch of the allocation-free decode entry point (decode.cu).
 size_t noalloc_scratch_bytes();
-cudaError_t noalloc_scratch_address(int device, void** addr);
+// Device address of that scratch in the calling thread's current context
+// (looked up once per context and cached).
+cudaError_t noalloc_scratch_address(void** addr);
 cudaError_t launch_int8_prefix(const PrefixParams& p, cudaStream_t stream);
 cudaError_t launch_bf16_prefix(const PrefixParams& p, cudaStream_t stream);
+cudaError_t launch_debug_prefix(const PrefixParams& p, cudaStream_t stream);
 
 }  // namespace i8kv

@@ -52,6 +52,7 @@
 // chunk's own keys as given), bf16 MMAs, and p~ handed to the PV MMA as bf16
 // with no group quantization.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -338,8 +339,12 @@ __global__ void __launch_bounds__(256) prefix_tiles_bf16_kernel(PrefixParams p) 
 
 // kBF: the high-precision variant -- bf16 query and tiles, no scales, and
 // the probabilities go to the PV MMA as bf16 p~ (no group quantization).
-template <int D, bool kBF>
+// kDbg (INT8 only): the same kernel that also records its raw integer
+// contractions -- S = Qq x Kq^T as read from TMEM, the codes Wq and each
+// group's Wq x Vq as read from TMEM -- for the debug entry point.
+template <int D, bool kBF, bool kDbg = false>
 __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p) {
+  static_assert(!(kDbg && kBF), "the debug record is for the INT8 path");
   using Ly = Lay<D>;
   using T = Tile<D>;
   constexpr int DH = D / 2;  // output dims per warpgroup
@@ -581,6 +586,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
           reinterpret_cast<const float4*>(smem + Ly::oTile + (size_t)(g % kStages) * T::kSlot + T::oSk);
       const float4* sv4 = sk4 + kGroup / 4;
       tmem_wait_ld();
+      if constexpr (kDbg) {
+        // the raw accumulators of the visible keys (exact integers in fp32)
+        if (valid) {
+          int32_t* srow = p.dbg_s + ((size_t)j * Hq + hq) * (H + C);
+#pragma unroll
+          for (int t = 0; t < 32; ++t)
+            if (key0 + t <= lim) srow[key0 + t] = __float2int_rn(s[t]);
+        }
+      }
       {
         const uint64_t cc = f2(c2, c2);
 #pragma unroll
@@ -637,6 +651,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
         for (int i = 0; i < 16; ++i) pk[i] = 0u;
       }
       }
+      if constexpr (kDbg) {
+        if (valid) {
+          uint8_t* wrow = p.dbg_wq + ((size_t)j * Hq + hq) * (size_t)(ngt * kGroup);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
+            if (key0 + 2 * i <= lim) wrow[key0 + 2 * i] = (uint8_t)__float2int_rn(c.x);
+            if (key0 + 2 * i + 1 <= lim) wrow[key0 + 2 * i + 1] = (uint8_t)__float2int_rn(c.y);
+          }
+        }
+      }
       // Wq (f16) or p~ (bf16) -> the PV A tile, row `row`; then the row statistics
       if (g >= 2) pwait(&pv_done[sl], ((g - 2) >> 1) & 1, abort_flag);  // PV(g-2) has read the slot
       uint8_t* p16 = smem + Ly::oP + (size_t)sl * Ly::kP16;
@@ -685,6 +710,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
           mbar_arrive(pv_free);  // every column of the accumulator is read
         }
         const float(&x)[32] = v[c & 1];
+        if constexpr (kDbg) {
+          // this group's Wq x Vq for this warpgroup's dims (exact integers in fp32)
+          if (valid) {
+            int32_t* prow = p.dbg_pv + (((size_t)j * Hq + hq) * ngt + (g_begin + h)) * D + wg * DH + 32 * c;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) prow[i] = __float2int_rn(x[i]);
+          }
+        }
         const uint64_t e2 = f2(e, e);
         if (rescale) {
           const uint64_t a2 = f2(alpha, alpha);
@@ -720,10 +753,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
       }
     } else if (valid) {
       const float inv = 1.0f / l;
-      float4* orow = reinterpret_cast<float4*>(p.out + ((size_t)j * Hq + hq) * D + wg * DH);
+      const size_t orow = ((size_t)j * Hq + hq) * D + wg * DH;
 #pragma unroll
       for (int i = 0; i < DH / 4; ++i)
-        orow[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+        store_out4(p.out, p.out_bf16, orow + 4 * i,
+                   make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv));
     }
   }
 
@@ -779,8 +813,8 @@ __global__ void __launch_bounds__(D / 4) prefix_merge_kernel(PrefixParams p) {
     }
   }
   const float inv = 1.0f / den;
-  reinterpret_cast<float4*>(p.out + ((size_t)j * p.Hq + hq) * D)[col] =
-      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  store_out4(p.out, p.out_bf16, ((size_t)j * p.Hq + hq) * D + 4 * col,
+             make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
 }
 
 constexpr int kMaxSplit = 6;
@@ -814,7 +848,7 @@ static void choose_split(int RB, int nsm, int& full_items, int& k) {
   full_items = k > 1 ? RB - tail : RB;
 }
 
-template <int D, bool kBF>
+template <int D, bool kBF, bool kDbg = false>
 cudaError_t launch_prefix_d(const PrefixParams& p0, cudaStream_t stream) {
   PrefixParams p = p0;
   const int ngt = (p.H + p.C + kGroup - 1) / kGroup;
@@ -826,7 +860,7 @@ cudaError_t launch_prefix_d(const PrefixParams& p0, cudaStream_t stream) {
   cudaGetDevice(&dev);
   static bool opted[64] = {false};
   if (dev < 0 || dev >= 64 || !opted[dev]) {
-    e = cudaFuncSetAttribute(prefix_attn_kernel<D, kBF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(prefix_attn_kernel<D, kBF, kDbg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Lay<D>::kTotal);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) opted[dev] = true;
@@ -837,7 +871,7 @@ cudaError_t launch_prefix_d(const PrefixParams& p0, cudaStream_t stream) {
   choose_split(RB, device_sms(), p.full_items, p.split_k);
   const int tail = RB - p.full_items;
   p.part = reinterpret_cast<float*>(p.tiles + (size_t)ngt * p.Hkv * Tile<D>::kBytes);
-  e = launch_pdl(prefix_attn_kernel<D, kBF>, dim3(p.full_items + tail * p.split_k), dim3(kThreads), Lay<D>::kTotal,
+  e = launch_pdl(prefix_attn_kernel<D, kBF, kDbg>, dim3(p.full_items + tail * p.split_k), dim3(kThreads), Lay<D>::kTotal,
                  stream, p);
   if (e != cudaSuccess || tail == 0) return e;
   return launch_pdl(prefix_merge_kernel<D>, dim3(tail * kRows), dim3(D / 4), 0, stream, p);
@@ -858,6 +892,17 @@ cudaError_t launch_int8_prefix(const PrefixParams& p, cudaStream_t stream) {
 
 cudaError_t launch_bf16_prefix(const PrefixParams& p, cudaStream_t stream) {
   return p.D == 256 ? launch_prefix_d<256, true>(p, stream) : launch_prefix_d<128, true>(p, stream);
+}
+
+cudaError_t launch_debug_prefix(const PrefixParams& p, cudaStream_t stream) {
+  // the records cover only the keys each row sees: clear them first
+  const size_t ng = ((size_t)p.H + p.C + kGroup - 1) / kGroup;
+  const size_t rows = (size_t)p.C * p.Hq;
+  cudaError_t e = cudaMemsetAsync(p.dbg_s, 0, rows * (p.H + p.C) * sizeof(int32_t), stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p.dbg_wq, 0, rows * ng * kGroup, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p.dbg_pv, 0, rows * ng * p.D * sizeof(int32_t), stream);
+  if (e != cudaSuccess) return e;
+  return p.D == 256 ? launch_prefix_d<256, false, true>(p, stream) : launch_prefix_d<128, false, true>(p, stream);
 }
 
 }  // namespace i8kv

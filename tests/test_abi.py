@@ -56,30 +56,40 @@ def test_argument_checks_without_gpu(lib):
     # decode: Hq not a multiple of Hkv, G > 8, partition != 256
     d = lib.i8kv_int8_paged_decode_attn
     d.restype = ctypes.c_int
-    d.argtypes = [P] * 9 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int, P, ctypes.c_size_t, P]
-    args = [P(16)] * 9
-    assert d(*args, 1, 10, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20, None) == 1
-    assert d(*args, 1, 72, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20, None) == 2
-    assert d(*args, 1, 24, 4, 256, 16, 8, 10, 0.0, 512, P(16), 1 << 20, None) == 2
+    d.argtypes = [P, ctypes.c_int] + [P] * 8 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int, P,
+                                                                   ctypes.c_size_t, P]
+    args = [P(16)] * 8
+    assert d(P(16), 0, *args, 1, 10, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20, None) == 1
+    assert d(P(16), 0, *args, 1, 72, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20, None) == 2
+    assert d(P(16), 0, *args, 1, 24, 4, 256, 16, 8, 10, 0.0, 512, P(16), 1 << 20, None) == 2
     assert "partition" in _last_error(lib)
+    # the output type: fp32 (0) or bf16 (1), 16-byte aligned
+    assert d(P(16), 2, *args, 1, 24, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20, None) == 1
+    assert "out_dtype" in _last_error(lib)
+    assert d(P(8), 1, *args, 1, 24, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20, None) == 1
+    assert "out must be 16-byte aligned" in _last_error(lib)
     # decode step: the new token's K/V are required and 16-byte aligned
     st = lib.i8kv_int8_decode_step
     st.restype = ctypes.c_int
-    st.argtypes = [P] * 10 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int, P, ctypes.c_size_t, P]
-    base = [P(16)] * 10
-    assert st(P(16), P(16), None, P(16), *([P(16)] * 6), 1, 24, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20,
+    st.argtypes = [P, ctypes.c_int] + [P] * 9 + [ctypes.c_int] * 7 + [ctypes.c_float, ctypes.c_int, P,
+                                                                    ctypes.c_size_t, P]
+    base = [P(16), 0] + [P(16)] * 9
+    assert st(P(16), 0, P(16), None, P(16), *([P(16)] * 6), 1, 24, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20,
               None) == 1
     assert "k_new" in _last_error(lib)
-    assert st(P(16), P(16), P(24), P(16), *([P(16)] * 6), 1, 24, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20,
+    assert st(P(16), 0, P(16), P(24), P(16), *([P(16)] * 6), 1, 24, 4, 256, 16, 8, 10, 0.0, 256, P(16), 1 << 20,
               None) == 1
     assert "aligned" in _last_error(lib)
     assert st(*base, 1, 24, 4, 64, 16, 8, 10, 0.0, 256, P(16), 1 << 20, None) == 2
     # prefix: chunk_len == 0 is a no-op; negative history rejected
     pf = lib.i8kv_int8_prefix_attn
     pf.restype = ctypes.c_int
-    pf.argtypes = [P] * 8 + [ctypes.c_int] * 7 + [ctypes.c_float, P, ctypes.c_size_t, P]
-    assert pf(*([P(16)] * 8), 100, 0, 24, 4, 256, 16, 10, 0.0, None, 0, None) == 0
-    assert pf(*([P(16)] * 8), -1, 5, 24, 4, 256, 16, 10, 0.0, P(16), 1 << 30, None) == 1
+    pf.argtypes = [P, ctypes.c_int] + [P] * 7 + [ctypes.c_int] * 7 + [ctypes.c_float, P, ctypes.c_size_t, P]
+    pa = [P(16), 0] + [P(16)] * 7
+    assert pf(*pa, 100, 0, 24, 4, 256, 16, 10, 0.0, None, 0, None) == 0
+    assert pf(*pa, -1, 5, 24, 4, 256, 16, 10, 0.0, P(16), 1 << 30, None) == 1
+    assert pf(P(16), 5, *([P(16)] * 7), 100, 5, 24, 4, 256, 16, 10, 0.0, P(16), 1 << 30, None) == 1
+    assert "out_dtype" in _last_error(lib)
     # the workspace: size from i8kv_prefix_workspace_bytes, checked before any launch
     wb = lib.i8kv_prefix_workspace_bytes
     wb.restype = ctypes.c_size_t
@@ -89,10 +99,10 @@ def test_argument_checks_without_gpu(lib):
     part_slot = 128 * (256 + 4) * 4  # the split parts' (o, m, l) rows, 2 per SM
     assert need > tiles and (need - tiles) % (2 * part_slot) == 0
     assert wb(100, 5, 4, 64) == 0
-    assert pf(*([P(16)] * 8), 100, 5, 24, 4, 256, 16, 10, 0.0, None, need, None) == 3
-    assert pf(*([P(16)] * 8), 100, 5, 24, 4, 256, 16, 10, 0.0, P(16), need - 1, None) == 3
+    assert pf(*pa, 100, 5, 24, 4, 256, 16, 10, 0.0, None, need, None) == 3
+    assert pf(*pa, 100, 5, 24, 4, 256, 16, 10, 0.0, P(16), need - 1, None) == 3
     assert "workspace" in _last_error(lib)
-    assert pf(*([P(16)] * 8), 100, 5, 24, 4, 256, 16, 10, 0.0, P(24), need, None) == 1
+    assert pf(*pa, 100, 5, 24, 4, 256, 16, 10, 0.0, P(24), need, None) == 1
 
 
 def test_rope_producer_argument_checks_without_gpu(lib):
@@ -131,12 +141,12 @@ def test_prefill_route_decision_without_gpu(lib):
     P = ctypes.c_void_p
     f = lib.i8kv_prefill_chunk
     f.restype = ctypes.c_int
-    f.argtypes = ([P] * 10 + [ctypes.c_int] * 8 + [ctypes.c_float, P, P, P, ctypes.c_size_t,
-                                                    ctypes.POINTER(ctypes.c_int), P])
+    f.argtypes = ([P, ctypes.c_int] + [P] * 9 + [ctypes.c_int] * 8 +
+                  [ctypes.c_float, P, P, P, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int), P])
 
     def route(history, threshold):
         r = ctypes.c_int(-1)
-        st = f(*([P(16)] * 10), history, 0, 24, 4, 256, 16, 10, threshold, 0.0, None, None, None, 0,
+        st = f(P(16), 0, *([P(16)] * 9), history, 0, 24, 4, 256, 16, 10, threshold, 0.0, None, None, None, 0,
                ctypes.byref(r), None)
         assert st == 0
         return r.value
@@ -147,4 +157,5 @@ def test_prefill_route_decision_without_gpu(lib):
     assert route(0, 0) == INT8  # threshold 0: every chunk INT8
     # bad shapes are rejected before the route is used
     r = ctypes.c_int(-1)
-    assert f(*([P(16)] * 10), 10, 4, 24, 5, 256, 16, 10, 0, 0.0, None, None, None, 0, ctypes.byref(r), None) != 0
+    assert f(P(16), 0, *([P(16)] * 9), 10, 4, 24, 5, 256, 16, 10, 0, 0.0, None, None, None, 0, ctypes.byref(r),
+             None) != 0

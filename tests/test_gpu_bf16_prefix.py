@@ -1,13 +1,20 @@
 """GPU parity of the high-precision chunk path (first prefill chunk, and chunks
 below the routing threshold) and of the routed prefill entry.
 
-The kernel rounds the dequantized history K/V and the probabilities p~ to bf16
-for the tensor-core MMAs, so it is compared with the oracle's fp64 attention
-within a bound derived from those roundings: p~ and a history V value each move
-by at most 2^-9 of themselves, so an output moves by at most 2^-8 max|V|; a
-history K rounding moves a score by about 2^-9 |q.k| / sqrt(D), allowed for by
-a further 1e-3.  The mean error must also stay below 1e-3 (random roundings
-average out; a systematic slip would not)."""
+Per-element bound, from the arithmetic the kernel documents.  It reads a
+history key or value back from the INT8 cache as bf16(code x scale) (the fp32
+product rounded to nearest-even bf16), while the oracle uses code x scale
+exactly; so the reference for the kernel's own rounding is A_r, fp64 softmax
+attention over exactly those bf16 values, computed here in numpy.  The kernel
+then rounds each p~ = exp(s - m) to bf16 for the P x V product (relative error
+<= 2^-9) while l sums the unrounded fp32 p~, which moves output element (j, d)
+by at most 2^-9 sum_t p_t |v_td|; the bound allows 2^-8 of it.  fp32 scores,
+ex2 and accumulation add at most 3e-4.  So, element by element,
+
+    |out - oracle| <= |oracle - A_r| + 2^-8 sum_t p_t |v_td| + 3e-4
+
+with p the softmax weights of A_r.  The history term |oracle - A_r| is computed,
+not bounded: it is the documented bf16 read-back of the INT8 history."""
 import numpy as np
 import pytest
 import torch
@@ -16,16 +23,53 @@ import int8_kv_cache_token_gb300 as i8
 import workloads as wl
 from oracle import oracle as orc
 from tests.gpu_helpers import dev, host, gpu_quantize_rows
+from tests.helpers import gather_int8
 
 pytestmark = pytest.mark.gpu
 
 
-def _check_close(got, ref, v_max, what):
-    err = np.abs(got - ref)
-    bound = 2.0 ** -8 * v_max + 1e-3
+def _bf16_round(x32: np.ndarray) -> np.ndarray:
+    return wl.bf16_values(wl.bf16_bits(x32)).astype(np.float64)
+
+
+def _kernel_reference(w, q, k, v, oc, rows):
+    """A_r [rows, Hq, D] and the bound's P-rounding term 2^-8 sum_t p_t |v_td|."""
+    H, C, Hq, Hkv, D = w.history, w.chunk, w.Hq, w.Hkv, w.D
+    G = Hq // Hkv
+    T = H + C
+    Kv = np.empty((T, Hkv, D))
+    Vv = np.empty((T, Hkv, D))
+    if H:
+        Kt, Vt, sK, sV = gather_int8(oc, w.block_table, H, Hkv, D)
+        # fp32 product code x scale, then RNE to bf16 (the kernel's read-back)
+        Kv[:H] = _bf16_round(Kt.astype(np.float32) * sK[:, :, None].astype(np.float32))
+        Vv[:H] = _bf16_round(Vt.astype(np.float32) * sV[:, :, None].astype(np.float32))
+    Kv[H:] = wl.bf16_values(k[H:])
+    Vv[H:] = wl.bf16_values(v[H:])
+    qv = wl.bf16_values(q).astype(np.float64)
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(D)))
+    rows = np.arange(C) if rows is None else np.asarray(rows)
+    ref = np.empty((rows.size, Hq, D))
+    pterm = np.empty((rows.size, Hq, D))
+    for i, j in enumerate(rows):
+        n = H + j + 1
+        for h in range(Hq):
+            s = Kv[:n, h // G, :] @ qv[j, h] * scale
+            p = np.exp(s - s.max())
+            p /= p.sum()
+            ref[i, h] = p @ Vv[:n, h // G, :]
+            pterm[i, h] = 2.0 ** -8 * (p @ np.abs(Vv[:n, h // G, :]))
+    return ref, pterm
+
+
+def _check_close(got, oracle_out, a_r, pterm, what):
+    err = np.abs(got - oracle_out)
+    bound = np.abs(oracle_out - a_r) + pterm + 3e-4
     assert np.isfinite(got).all(), what
-    assert err.max() <= bound and err.mean() <= 1e-3, \
-        f"{what}: max-abs {err.max():.3e} (bound {bound:.3e}), mean-abs {err.mean():.3e}"
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {int(bad.sum())} elements past the bound, worst at "
+                           f"{np.unravel_index(np.argmax(err - bound), err.shape)}: "
+                           f"err {err.max():.3e}, bound there {bound.flat[np.argmax(err - bound)]:.3e}")
     return err.max()
 
 
@@ -45,7 +89,8 @@ def _run_bf16(w: wl.PrefixWorkload, rows=None):
     ref = orc.bf16_prefix_attn(q, k[H:], v[H:], oc, w.block_table, H, w.block_size, rows=rows)
     if rows is not None:
         got = got[rows]
-    return _check_close(got, ref, np.abs(wl.bf16_values(v)).max(), w.name)
+    a_r, pterm = _kernel_reference(w, q, k, v, oc, rows)
+    return _check_close(got, ref, a_r, pterm, w.name), (got, ref, a_r, pterm)
 
 
 @pytest.mark.parametrize("H,C", [(0, 1), (0, 37), (0, 300), (100, 37), (256, 70), (1000, 200)])
@@ -59,6 +104,21 @@ def test_bf16_first_chunk_full_size_sampled_rows():
     w = wl.PrefixWorkload("first4k", 24, 4, 256, 0, 4096, seed=5)
     rows = np.array([0, 1, 31, 32, 127, 128, 1000, 2047, 2048, 4000, 4095], np.int32)
     _run_bf16(w, rows=rows)
+
+
+def test_bf16_prefix_bound_catches_a_one_row_slip():
+    # The bound is tight enough to fail on a 1e-2 error confined to one row
+    # (planted here in the GPU output, after the kernel ran).
+    w = wl.PrefixWorkload("plant", 24, 4, 256, 256, 70, seed=3)
+    _, (got, ref, a_r, pterm) = _run_bf16(w)
+    slipped = got.copy()
+    slipped[40, 7, :] += 1e-2
+    with pytest.raises(AssertionError):
+        _check_close(slipped, ref, a_r, pterm, "planted")
+    slipped = got.copy()
+    slipped[3, 0, 100] -= 1e-2
+    with pytest.raises(AssertionError):
+        _check_close(slipped, ref, a_r, pterm, "planted element")
 
 
 def test_bf16_prefix_single_key_returns_value():
@@ -114,7 +174,8 @@ def test_prefill_chunk_routes(H, thr):
     if route == i8.ROUTE_INT8:
         assert np.abs(host(out) - ref).max() <= 2e-3  # the INT8 path's own tolerance
     else:
-        _check_close(host(out), ref, np.abs(wl.bf16_values(v)).max(), "routed bf16")
+        a_r, pterm = _kernel_reference(w, q, k, v, oc, None)
+        _check_close(host(out), ref, a_r, pterm, "routed bf16")
 
 
 def test_bf16_prefix_split_tail_blocks():

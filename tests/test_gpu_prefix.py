@@ -65,10 +65,44 @@ def test_prefix_equal_scores_causal_mean_on_gpu():
         assert np.abs(out[j] - ref[None, :]).max() < 1e-3 * 127
 
 
+def split_row_blocks(C, G, Hkv, nsm, max_split=6):
+    """The launcher's work split, restated from its documented rule: 128-row blocks
+    (rows = (chunk token, q-head of the group) pairs, token-major) of each KV
+    head, ordered heaviest first, one CTA each; when the blocks outnumber the
+    SMs and leave a partial last wave, each block of that wave is split into k
+    parts over its key groups (k <= 6, tail * k <= 2 * SMs, minimizing
+    ceil(tail * k / SMs) / k).  Returns the split blocks as (KV head, first row)."""
+    R = C * G
+    nrb = (R + 127) // 128
+    RB = nrb * Hkv
+    tail = RB % nsm if RB > nsm else 0
+    k, best = 1, 1.0
+    for kk in range(2, max_split + 1):
+        if tail == 0 or tail * kk > 2 * nsm:
+            break
+        cost = ((tail * kk + nsm - 1) // nsm) / kk
+        if cost < best - 1e-9:
+            best, k = cost, kk
+    full = RB - tail if k > 1 else RB
+    return [(blk % Hkv, (nrb - 1 - blk // Hkv) * 128) for blk in range(full, RB)]
+
+
 def test_prefix_chunk_pages_shape_sampled():
-    # 2048 chunk queries after 16384 cached tokens, 24 q / 4 kv heads, head_dim 256
+    # 2048 chunk queries after 16384 cached tokens, 24 q / 4 kv heads, head_dim
+    # 256, as the benchmark launches it.  Checked rows: every 16th chunk token
+    # (128 tokens across the chunk, all heads) plus every token of one row block
+    # of two blocks of the split last wave (the lightest blocks, whose key
+    # groups are split over several CTAs and merged by log-sum-exp).
     w = wl.prefix_chunk()
-    rows = np.array([0, 1, 63, 64, 1000, 2047], np.int32)
+    G = w.Hq // w.Hkv
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    split = split_row_blocks(w.chunk, G, w.Hkv, nsm)
+    assert split, "the pages' chunk leaves a split last wave on this GPU"
+    rows = np.arange(0, w.chunk, 16)
+    for _, r0 in (split[0], split[-1]):  # the heaviest and the lightest split block
+        rows = np.union1d(rows, np.arange(r0 // G, min(w.chunk, (r0 + 128 + G - 1) // G)))
+    rows = np.union1d(rows, [w.chunk - 1]).astype(np.int32)
+    assert rows.size >= 128
     _prefix_parity(w, rows=rows)
 
 

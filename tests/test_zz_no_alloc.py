@@ -17,7 +17,6 @@ import workloads as wl
 from tests.gpu_helpers import dev, host, gpu_decode_cache, gpu_quantize_rows, gpu_decode
 
 pytestmark = pytest.mark.gpu
-TOL = 2e-3
 
 
 @pytest.mark.parametrize("lens,Hq,Hkv,D", [([5000, 1, 300, 0], 24, 4, 256), ([32768, 777], 32, 8, 128)])
@@ -36,8 +35,10 @@ def test_noalloc_matches_workspace_entry_point(lens, Hq, Hkv, D):
         torch.cuda.synchronize()
         got = host(out)
         assert np.isfinite(got).all()
-        err = np.abs(got - ref).max()
-        assert err <= TOL, f"call {call}: max-abs {err:.3e}"
+        # the same kernel with the same grid as the workspace entry point: the
+        # same bits, on the first call and on the one after it (a stale or
+        # aliased scratch would show here)
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), f"call {call}"
         assert i8.device_error() == 0
     assert torch.cuda.mem_get_info()[0] == free_before  # the calls took no device memory
 
