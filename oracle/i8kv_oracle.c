@@ -681,6 +681,55 @@ int orc_bf16_decode_attn(double* out, const uint16_t* q, const uint16_t* k_cache
   return ORC_OK;
 }
 
+/* The BF16-KV comparison of the prefix chunk (the BF16 control of [KV] §4.2,
+ * where BF16 and INT8 attention are compared on prefill chunks by history):
+ * chunk row j (position history_len + j) of the bf16 query [chunk_len, Hq, D]
+ * attends, causally, to keys 0 .. history_len + j of one sequence, every key
+ * (history and the chunk's own) read from the bf16 paged cache through
+ * block_table.  Plain softmax attention in fp64 on the bf16 values.  rows
+ * (nullable) selects chunk rows; out is [nrows, Hq, D]. */
+int orc_bf16_kv_prefix_attn(double* out, const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                            const int32_t* block_table, int history_len, int chunk_len, int Hq, int Hkv, int D, int bs,
+                            double softmax_scale, const int32_t* rows, int nrows, int nthreads) {
+  if (Hq % Hkv != 0 || D % 8 != 0 || history_len < 0 || chunk_len < 0) return ORC_BAD_ARG;
+  if (rows == NULL) nrows = chunk_len;
+  const int G = Hq / Hkv;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) num_threads(nthreads)
+#endif
+  for (int r = 0; r < nrows; ++r)
+    for (int h = 0; h < Hq; ++h) {
+      const int j = rows ? rows[r] : r;
+      const int kv_head = h / G;
+      const int visible = history_len + j + 1; /* keys 0 .. history_len + j */
+      const uint16_t* qv = q + ((size_t)j * Hq + h) * D;
+      double* O = out + ((size_t)r * Hq + h) * D;
+      double* s = (double*)malloc(sizeof(double) * (size_t)visible);
+      double m = -INFINITY;
+      for (int t = 0; t < visible; ++t) {
+        const int blk = block_table[t / bs], off = t % bs;
+        double a = 0.0;
+        for (int d = 0; d < D; ++d)
+          a += (double)bf16_to_f32(qv[d]) * (double)bf16_to_f32(k_cache[kb_index(blk, kv_head, d, off, Hkv, D, bs)]);
+        s[t] = a * softmax_scale;
+        if (s[t] > m) m = s[t];
+      }
+      double l = 0.0;
+      for (int d = 0; d < D; ++d) O[d] = 0.0;
+      for (int t = 0; t < visible; ++t) {
+        const int blk = block_table[t / bs], off = t % bs;
+        const double p = exp(s[t] - m);
+        l += p;
+        for (int d = 0; d < D; ++d)
+          O[d] += p * (double)bf16_to_f32(v_cache[v_index(blk, kv_head, d, off, Hkv, D, bs)]);
+      }
+      for (int d = 0; d < D; ++d) O[d] /= l;
+      free(s);
+    }
+  return ORC_OK;
+}
+
 /* Threads the OpenMP runtime would use by default (1 without OpenMP). */
 int orc_max_threads(void) {
 #ifdef _OPENMP

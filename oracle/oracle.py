@@ -77,8 +77,10 @@ def _load():
             lib.orc_bf16_prefix_attn.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, I,
                                                  I]
             lib.orc_bf16_decode_attn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, ctypes.c_double, I]
+            lib.orc_bf16_kv_prefix_attn.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_double, P, I, I]
             for name in ("orc_kv_quant_write", "orc_kv_rope_quant_write", "orc_qk_i32", "orc_decode_attn", "orc_prefix_attn",
-                         "orc_bf16_kv_write", "orc_bf16_decode_attn", "orc_bf16_prefix_attn", "orc_max_threads"):
+                         "orc_bf16_kv_write", "orc_bf16_decode_attn", "orc_bf16_prefix_attn",
+                         "orc_bf16_kv_prefix_attn", "orc_max_threads"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -330,6 +332,27 @@ def bf16_decode_attn(q, cache, block_tables, seq_lens, block_size, softmax_scale
                                       _p(sl), B, Hq, Hkv, D, block_size, bt.shape[1], float(softmax_scale),
                                       nthreads)
     _check(rc, "bf16_decode_attn")
+    return out
+
+
+def bf16_kv_prefix_attn(q, cache, block_table, history_len, block_size, softmax_scale=None, rows=None,
+                        nthreads=0):
+    """BF16-KV comparison of the prefix chunk: chunk rows of q (uint16 bf16
+    [C,Hq,D]) over keys 0 .. history_len + j of the bf16 paged cache (history
+    and chunk alike), causal, plain softmax in fp64.  Out [len(rows) or C, Hq, D]."""
+    q = _u16(q)
+    C, Hq, D = q.shape
+    Hkv = cache["k_cache"].shape[1]
+    if softmax_scale is None:
+        softmax_scale = float(np.float32(1.0) / np.sqrt(np.float32(D)))
+    r = None if rows is None else np.ascontiguousarray(rows, np.int32)
+    nrows = C if r is None else r.size
+    out = np.empty((nrows, Hq, D), np.float64)
+    bt = np.ascontiguousarray(block_table, np.int32).ravel()
+    rc = _load().orc_bf16_kv_prefix_attn(_p(out), _p(q), _p(cache["k_cache"]), _p(cache["v_cache"]), _p(bt),
+                                         history_len, C, Hq, Hkv, D, block_size, float(softmax_scale), _p(r), nrows,
+                                         nthreads)
+    _check(rc, "bf16_kv_prefix_attn")
     return out
 
 

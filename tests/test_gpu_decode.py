@@ -90,6 +90,19 @@ def test_decode_workspace_reuse_and_repeat():
     assert i8.device_error() == 0
 
 
+def test_decode_workspace_reuse_across_batches():
+    # One workspace (sized for the largest batch) serves calls whose batches,
+    # lengths and head shapes differ: every record a call reads is written
+    # earlier in the same call, whatever the previous calls left in the buffer.
+    shapes = [(24, 4, 256, [5000, 3000, 40]), (24, 4, 256, [40, 9000]), (24, 4, 256, [1, 1, 1, 20000, 7]),
+              (32, 8, 128, [700]), (24, 4, 256, [12000])]
+    nbytes = max(i8.decode_workspace_bytes(len(l), hq, hkv, d, (max(l) + 15) // 16) for hq, hkv, d, l in shapes)
+    ws = torch.zeros(nbytes + 4096, dtype=torch.uint8, device="cuda")
+    for k, (hq, hkv, d, lens) in enumerate(shapes):
+        _decode_parity(wl.DecodeWorkload(f"reuse{k}", hq, hkv, d, lens, seed=40 + k), workspace=ws)
+    assert i8.device_error() == 0
+
+
 def test_decode_rejects_small_workspace():
     w = wl.DecodeWorkload("ws", 24, 4, 256, [600], seed=1)
     cache = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)

@@ -51,3 +51,30 @@ def test_single_visible_key_returns_its_value():
     got = orc.bf16_prefix_attn(q, k, v, None, None, 0, BS)
     expect = np.repeat(orc.bf16_to_f64(v), 2, axis=1)  # q-heads 0,1 -> kv 0; 2,3 -> kv 1
     assert np.array_equal(got, expect)
+
+
+def test_bf16_kv_prefix_is_causal_attention_over_the_bf16_cache():
+    # The BF16-KV comparison of the prefix chunk: every key (history and chunk)
+    # comes from the bf16 paged cache; read back here through numpy reshapes of
+    # its documented layout ([NB, Hkv, D/8, 16, 8] and [NB, Hkv, D, 16]).
+    H, C, Hq, Hkv, D = 70, 21, 6, 2, 128
+    rng = np.random.default_rng(8)
+    k, v = wl.randn_bf16(rng, (H + C, Hkv, D)), wl.randn_bf16(rng, (H + C, Hkv, D))
+    q = wl.randn_bf16(rng, (C, Hq, D))
+    tables, NB = wl.paged_tables([H + C], perm_seed=9)
+    cache = orc.bf16_kv_write(k, v, wl.slot_mapping(tables[0], np.arange(H + C)), NB, BS)
+    rows = np.array([0, 1, 10, C - 1], np.int32)
+    got = orc.bf16_kv_prefix_attn(q, cache, tables[0], H, BS, rows=rows)
+    pos = np.arange(H + C)
+    blk, off = tables[0][pos // BS], pos % BS
+    K = cache["k_cache"].reshape(NB, Hkv, D // 8, BS, 8)[blk, :, :, off, :].reshape(H + C, Hkv, D)
+    V = cache["v_cache"].reshape(NB, Hkv, D, BS)[blk, :, :, off]
+    assert np.array_equal(K, k) and np.array_equal(V, v)  # the layout round trip
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(D)))
+    ref = orc.attention_fp64(orc.bf16_to_f64(q)[rows], orc.bf16_to_f64(K), orc.bf16_to_f64(V), H + rows + 1,
+                             softmax_scale=scale)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    # the last visible key matters: dropping it changes the row
+    short = orc.attention_fp64(orc.bf16_to_f64(q)[rows], orc.bf16_to_f64(K), orc.bf16_to_f64(V), H + rows,
+                               softmax_scale=scale)
+    assert np.abs(got - short).max() > 1e-3

@@ -61,6 +61,9 @@ MUTANTS = {
                            "const int n_keys = history_len + j;\n      const int kvh = h / G;\n      const uint16_t* qv"),
     "bf16_prefix_k_scale": ("const double sc = (double)k_scale[s_index(blk, kvh, off, Hkv, bs)];\n          for (int d = 0; d < D; ++d) kx[d]",
                             "const double sc = (double)v_scale[s_index(blk, kvh, off, Hkv, bs)];\n          for (int d = 0; d < D; ++d) kx[d]"),
+    # BF16-KV prefix comparison: causal limit off by one, query head -> KV head by modulo
+    "bf16kv_prefix_causal": ("const int visible = history_len + j + 1;", "const int visible = history_len + j;"),
+    "bf16kv_prefix_kv_head": ("const int kv_head = h / G;", "const int kv_head = h % Hkv;"),
     # K smoothing: K multiplied by s instead of 1/s; query head -> KV head by modulo
     "smooth_k_not_inverted": ("if (k_smooth) smooth_vec(x, D, k_smooth + (size_t)h * D, 1);",
                               "if (k_smooth) smooth_vec(x, D, k_smooth + (size_t)h * D, 0);"),
