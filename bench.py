@@ -473,6 +473,11 @@ def run_ours(args):
             except Exception as e:  # pragma: no cover - report, do not hide
                 secondary["decode_u8_probs_by_history"] = {"error": str(e)[:200]}
             try:
+                secondary["prefix_int8_vs_bf16_kv_by_history"] = run_prefix_by_history(torch, i8, tensor_peak,
+                                                                                        peak_kind)
+            except Exception as e:  # pragma: no cover - report, do not hide
+                secondary["prefix_int8_vs_bf16_kv_by_history"] = {"error": str(e)[:200]}
+            try:
                 secondary["bf16_kv_decode_by_history"] = run_bf16_comparison(
                     torch, i8, hbm_peak, {L: v * 1e3 for L, v in by_len.items()})
             except Exception as e:  # pragma: no cover - report, do not hide
@@ -818,6 +823,52 @@ def run_secondary(torch, i8, hbm_peak, tensor_peak=0.0, peak_kind="measured"):
         res["prefill_first_chunk_0+4096"] = first
     except Exception as e:  # pragma: no cover
         res["prefill_first_chunk_0+4096"] = {"error": str(e)[:200]}
+    return res
+
+
+PREFIX_HISTORIES = ((4096, 4096), (8192, 4096), (12288, 2242), (16384, 2048))
+
+
+def run_prefix_by_history(torch, i8, tensor_peak, peak_kind):
+    """The prefix chunk on the INT8 path and on the BF16-KV comparison path (every
+    key from a bf16 paged cache), at the pages' history/chunk pairs and the
+    16384 + 2048 chunk, 24 q / 4 KV heads, head_dim 256.  Each call is timed
+    whole (operand tiles + attention + merge of a split last wave), two copies of
+    its state rotating inside one graph."""
+    res = {}
+    for H, C in PREFIX_HISTORIES:
+        w = wl.PrefixWorkload(f"prefix_{H}+{C}", 24, 4, 256, H, C, seed=0)
+        k, v = w.kv()
+        kd, vd, sd, qd = to_dev(torch, k), to_dev(torch, v), to_dev(torch, w.slots()), to_dev(torch, w.q())
+        bt = to_dev(torch, w.block_table)
+        dummy = torch.zeros((C, w.Hkv, w.D), dtype=torch.bfloat16, device="cuda")
+        none = torch.full((C,), -1, dtype=torch.int32, device="cuda")
+        int8_calls, bf16_calls = [], []
+        for _ in range(2):
+            c8 = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+            i8.kv_quant_write(kd, vd, sd, **c8)
+            q_i8 = torch.empty(qd.shape, dtype=torch.int8, device="cuda")
+            q_s = torch.empty(qd.shape[:2], dtype=torch.float32, device="cuda")
+            i8.kv_quant_write(dummy, dummy, none, **c8, q=qd, q_i8=q_i8, q_scale=q_s)
+            cb = i8.alloc_bf16_cache(w.num_blocks, w.Hkv, w.D)
+            i8.bf16_kv_write(kd, vd, sd, **cb)
+            out = torch.empty((C, w.Hq, w.D), dtype=torch.float32, device="cuda")
+            ws = i8.prefix_workspace(H, C, w.Hkv, w.D)
+            int8_calls.append(lambda c=c8, qi=q_i8, qs=q_s, o=out, ws=ws: i8.int8_prefix_attn(
+                o, qi, qs, c["k_cache"], c["v_cache"], c["k_scale"], c["v_scale"], bt, H, workspace=ws))
+            bf16_calls.append(lambda c=cb, o=out, ws=ws: i8.bf16_kv_prefix_attn(
+                o, qd, c["k_cache"], c["v_cache"], bt, H, workspace=ws))
+        ms8 = time_rotating(torch, int8_calls, 3)
+        msb = time_rotating(torch, bf16_calls, 3)
+        torch.cuda.synchronize()
+        assert i8.device_error() == 0
+        ops = w.int8_ops()
+        res[f"{H}+{C}"] = {"int8_ms": ms8, "int8_tops": ops / (ms8 / 1e3) / 1e12,
+                           "int8_frac": ops / (ms8 / 1e3) / 1e12 / tensor_peak if tensor_peak else None,
+                           "bf16_kv_ms": msb, "bf16_kv_tflops": ops / (msb / 1e3) / 1e12,
+                           "int8_speedup": msb / ms8, "peak_kind": f"of {peak_kind} dense bf16 (burst)"}
+        del int8_calls, bf16_calls
+        torch.cuda.empty_cache()
     return res
 
 

@@ -382,6 +382,22 @@ i8kv_status i8kv_bf16_kv_write(const uint16_t* k, const uint16_t* v, const int32
                                int D, int block_size, int num_blocks, uint16_t* k_cache, uint16_t* v_cache,
                                void* stream);
 
+/* The prefix chunk over the bf16 cache (the BF16 control of the pages'      */
+/* prefill comparison, [KV] §4.2): chunk row j (bf16 q [C, Hq, D], position   */
+/* history_len + j) attends to keys 0 .. history_len + j of the sequence,    */
+/* every key -- history and the chunk's own, which must already be in the    */
+/* cache (i8kv_bf16_kv_write) -- read from the bf16 cache through            */
+/* block_table.  The kernels are those of i8kv_bf16_prefix_attn (bf16        */
+/* tensor-core MMAs, fp32 online softmax over 32-key groups, p~ rounded to   */
+/* bf16 for P x V, fp32 row sums) with operand tiles built from the bf16     */
+/* cache.  out: [C, Hq, D] of out_dtype.  workspace: as for                  */
+/* i8kv_int8_prefix_attn (same size function).  Launches two kernels (three  */
+/* with a split last wave).                                                  */
+i8kv_status i8kv_bf16_kv_prefix_attn(void* out, int out_dtype, const uint16_t* q, const uint16_t* k_cache,
+                                     const uint16_t* v_cache, const int32_t* block_table, int history_len,
+                                     int chunk_len, int Hq, int Hkv, int D, int block_size, int num_blocks,
+                                     float softmax_scale, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Plain softmax decode attention over the bf16 cache with the same 256-token
  * partitions and log-sum-exp merge.  q: bf16 [B, Hq, D]; out: [B, Hq, D] of
  * out_dtype.

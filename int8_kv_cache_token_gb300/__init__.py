@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     I8KVError,
     alloc_bf16_cache,
     alloc_int8_cache,
+    bf16_kv_prefix_attn,
     bf16_kv_write,
     bf16_paged_decode_attn,
     bf16_prefix_attn,

@@ -58,6 +58,7 @@ _SIGS = {
                               _P],
     "i8kv_debug_qk_i32": [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P],
     "i8kv_bf16_kv_write": [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P],
+    "i8kv_bf16_kv_prefix_attn": [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _Z, _P],
     "i8kv_bf16_paged_decode_attn": [_P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P],
 }
 
@@ -290,6 +291,21 @@ def bf16_paged_decode_attn(out, q, k_cache, v_cache, block_tables, seq_lens, wor
         _ptr(block_tables, torch.int32, "block_tables"), _ptr(seq_lens, torch.int32, "seq_lens"),
         B, Hq, Hkv, D, BLOCK_SIZE, block_tables.shape[1], NB, float(softmax_scale), partition,
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def bf16_kv_prefix_attn(out, q, k_cache, v_cache, block_table, history_len: int, workspace=None,
+                        softmax_scale: float = 0.0, stream=None):
+    """out [C, Hq, D] (float32 or bfloat16) <- the prefix chunk over the bf16 paged cache: bf16 q
+    [C, Hq, D] (positions history_len ..) over every cached key 0 .. history_len + j (the chunk's
+    own K/V already written by bf16_kv_write)."""
+    NB, Hkv, D = _cache_geom(k_cache, 8)
+    C, Hq, _ = q.shape
+    if workspace is None:
+        workspace = prefix_workspace(int(history_len), C, Hkv, D, device=out.device)
+    _check(lib().i8kv_bf16_kv_prefix_attn(
+        *_out(out), _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"),
+        _ptr(block_table, torch.int32, "block_table"), int(history_len), C, Hq, Hkv, D, BLOCK_SIZE, NB,
+        float(softmax_scale), _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)))
 
 
 def debug_qk_i32(acc, q_i8, k_cache, block_tables, seq_lens, stream=None):

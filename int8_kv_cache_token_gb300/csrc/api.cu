@@ -385,6 +385,36 @@ i8kv_status i8kv_bf16_prefix_attn(void* out, int out_dtype, const uint16_t* q, c
   return from_cuda(i8kv::launch_bf16_prefix(p, static_cast<cudaStream_t>(stream)), "bf16 prefix launch");
 }
 
+i8kv_status i8kv_bf16_kv_prefix_attn(void* out, int out_dtype, const uint16_t* q, const uint16_t* k_cache,
+                                     const uint16_t* v_cache, const int32_t* block_table, int history_len,
+                                     int chunk_len, int Hq, int Hkv, int D, int block_size, int num_blocks,
+                                     float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+  REQUIRE(history_len >= 0 && chunk_len >= 0, I8KV_ERR_INVALID_ARG, "history_len=%d chunk_len=%d", history_len,
+          chunk_len);
+  i8kv_status s = check_heads(Hq, Hkv, D);
+  if (s != I8KV_OK) return s;
+  REQUIRE(block_size == 16, I8KV_ERR_UNSUPPORTED, "block_size %d not supported (16)", block_size);
+  REQUIRE(num_blocks > 0, I8KV_ERR_INVALID_ARG, "num_blocks=%d", num_blocks);
+  if (chunk_len == 0) return I8KV_OK;
+  s = check_out(out, out_dtype);
+  if (s != I8KV_OK) return s;
+  REQUIRE(q && k_cache && v_cache && block_table, I8KV_ERR_INVALID_ARG, "null q/cache/block_table pointer");
+  REQUIRE(aligned16(q) && aligned16(k_cache) && aligned16(v_cache), I8KV_ERR_INVALID_ARG,
+          "q and the caches must be 16-byte aligned");
+  const size_t need = i8kv::prefix_workspace_bytes(history_len, chunk_len, Hkv, D);
+  REQUIRE(workspace != nullptr && workspace_bytes >= need, I8KV_ERR_WORKSPACE,
+          "prefix workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+  REQUIRE(aligned16(workspace), I8KV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  i8kv::PrefixParams p{out, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, block_table, history_len,
+                       chunk_len, Hq, Hkv, Hq / Hkv, D, num_blocks,
+                       softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D), static_cast<uint8_t*>(workspace)};
+  p.qb = q;
+  p.kb_cache = k_cache;
+  p.vb_cache = v_cache;
+  p.out_bf16 = out_dtype == I8KV_OUT_BF16;
+  return from_cuda(i8kv::launch_bf16_prefix(p, static_cast<cudaStream_t>(stream)), "bf16-kv prefix launch");
+}
+
 i8kv_status i8kv_prefill_chunk(void* out, int out_dtype, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                                const int32_t* slot_mapping, int8_t* k_cache, int8_t* v_cache, float* k_scale,
                                float* v_scale, const int32_t* block_table, int history_len, int chunk_len, int Hq,

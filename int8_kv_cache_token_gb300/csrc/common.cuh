@@ -298,6 +298,18 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// The same with A in tensor memory: row m of A in TMEM lane m, two 16-bit
+// elements per 32-bit column (the even one in the low half), so one K = 16
+// step reads 8 columns starting at a_tmem.
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+
 // The mbarrier receives one arrival when every tcgen05 operation this thread
 // issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -321,6 +333,14 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 
 // Whole warp: lane i reads columns [col, col + 16) (or 32) of TMEM lane
 // (warp % 4) * 32 + i; `taddr` = base + (lane offset << 16) + col.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
@@ -344,6 +364,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// Whole warp: lane i writes columns [col, col + 32) of TMEM lane (warp % 4) * 32
+// + i; taddr as for tmem_ld32.  tmem_wait_st() waits for this thread's stores.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Generic-proxy shared-memory writes made visible to the tensor cores.
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -472,9 +506,12 @@ __device__ __forceinline__ void div_rne_row(const float (&x)[N], float s, float 
 }
 
 // a / 127 correctly rounded, by the same method with the constant RN(1/127).
-// Checked exhaustively against IEEE division for every float in [1, 4), in the
-// two lowest normal binades and in the top binade (the rounding pattern
-// repeats in every binade); inputs below 2^-100 use the plain division.
+// Checked exhaustively against IEEE division for every float of [1, 2), of the
+// top binade [2^127, 2^128) and of [2^-100, 2^-98): scaling a by a power of
+// two scales the product, the residual and the corrected quotient exactly, so
+// every normal binade between repeats the pattern of [1, 2), and the top and
+// bottom binades are where overflow or underflow could break it.  Inputs below
+// 2^-100 use the plain division.
 __device__ __forceinline__ float div127(float a) {
   if (a < kTinyDivisor) return div127_tiny(a);
   const float y = 0.0078740157f;  // RN(1/127)

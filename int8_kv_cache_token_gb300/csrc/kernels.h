@@ -103,6 +103,9 @@ struct PrefixParams {
   int32_t* dbg_s;
   uint8_t* dbg_wq;
   int32_t* dbg_pv;
+  // BF16-KV comparison: every key (history and chunk) from the bf16 paged cache
+  const uint16_t* kb_cache;  // [NB, Hkv, D/8, 16, 8]
+  const uint16_t* vb_cache;  // [NB, Hkv, D, 16]
 };
 
 // Per-translation-unit device error words (read and cleared).

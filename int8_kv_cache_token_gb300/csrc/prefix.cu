@@ -66,12 +66,32 @@ constexpr int kBS = 16;
 constexpr int kRows = 128;       // query rows per CTA: the MMA's M, one TMEM lane each
 constexpr int kGroup = 32;       // keys per probability group
 constexpr int kPagesPG = kGroup / kBS;
-constexpr int kStages = 4;       // operand tiles in flight
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kLoadWarp = 0;
-constexpr int kMmaWarp = 1;
-constexpr int kCompWarp0 = 4;    // warps 4..11
+constexpr int kMmaWarp = 1;      // issues the QK MMAs
+constexpr int kPvWarp = 2;       // issues the PV MMAs
+constexpr int kUpdWarp0 = 4;     // warps 4..11: output update, warpgroup 1 = dims [0, D/2), 2 = [D/2, D)
+constexpr int kSmxWarp0 = 12;    // warps 12..15: the softmax of every group
 constexpr int kWGThreads = 128;
+// Register split (setmaxnreg) of the launch's 512 x 128 registers: copy/MMA
+// warpgroup 40, update warpgroups 184 each (o is D/2 fp32 per thread), softmax
+// warpgroup 104; 40 + 2 x 184 + 104 = 4 x 128.
+constexpr int kRegsCtl = 40, kRegsUpd = 184, kRegsSmx = 104;
+static_assert(kRegsCtl + 2 * kRegsUpd + kRegsSmx == 4 * (65536 / kThreads), "register split");
+// TMEM columns per load in the output update.
+constexpr int kUpdChunk = 32;
+template <int N>
+__device__ __forceinline__ void tmem_ld_chunk(uint32_t taddr, float (&v)[N]) {
+  if constexpr (N == 8)
+    tmem_ld8(taddr, v);
+  else if constexpr (N == 16)
+    tmem_ld16(taddr, v);
+  else
+    tmem_ld32(taddr, v);
+}
+// The output's reference maximum moves only when a group's maximum exceeds it
+// by more than this (log2 units), so o is rarely rescaled.
+constexpr float kLazyLog2 = 8.0f;
 
 // One (KV head, group) operand tile, in global memory and in shared memory.
 template <int D>
@@ -87,20 +107,30 @@ struct Tile {
 
 template <int D>
 struct Lay {
-  static constexpr int kQ16 = kRows * D * 2;          // f16 Q, D/64 atoms of [128 rows][128 B]
+  // Operand tiles in flight (an even number: QK takes the keys of two
+  // consecutive groups at once).  K goes to a ring of its own, atom-major --
+  // [D/64 atoms][kStages][32 keys][128 B] -- so the K rows of two adjacent
+  // stages are one 64-row operand; V and the scales go to a ring of stages.
+  static constexpr int kStages = D == 256 ? 6 : 8;
+  static constexpr int kKAtom = kGroup * 128;         // one stage's 32 rows of one 64-dim atom
+  static constexpr int kVBytes = Tile<D>::kBytes - Tile<D>::oV;  // V, then sK, sV
+  static constexpr int kVSlot = (kVBytes + 1023) / 1024 * 1024;
   static constexpr int kP16 = kRows * kGroup * 2;     // f16 Wq, [128][64 B]
-  static constexpr int oQ = 0;
-  static constexpr int oTile = oQ + kQ16;             // kStages tiles
-  static constexpr int oP = oTile + kStages * Tile<D>::kSlot;  // two slots
+  static constexpr int oK = 0;                        // the K ring
+  static constexpr int oVr = oK + (D / 64) * kStages * kKAtom;  // the V ring
+  static constexpr int oP = oVr + kStages * kVSlot;   // two slots
   static constexpr int oSt = oP + 2 * kP16;           // four slots of m_g[128], sW[128], l_g[128]
   static constexpr int oBar = oSt + 4 * 3 * kRows * 4;
-  // tile_full[4], tile_free[4], qk_done[2], s_free[2], p_full[2], pv_done[2], pv_free, st_full[4]
-  static constexpr int kBars = kStages + kStages + 2 + 2 + 2 + 2 + 1 + 4;
+  // tile_full[4], tile_free[4], qk_done[2], s_free[2], p_full[2], wq_free[2], pv_done[2], pv_free[2], st_full[4]
+  static constexpr int kBars = kStages + kStages + 2 + 2 + 2 + 2 + 2 + 2 + 4;
   static constexpr int oCtl = oBar + kBars * 8;       // TMEM base, abort flag
   static constexpr int kTotal = oCtl + 16;
-  // TMEM: S in columns [0, 64) (two slots of 32), PV in [kPVCol, kPVCol + D)
-  static constexpr uint32_t kPVCol = D == 256 ? 256 : 128;
-  static constexpr uint32_t kTmemCols = D == 256 ? 512 : 256;
+  // TMEM: S in columns [0, 128) (two slots of 64: a pair of groups each), the
+  // f16 query (the QK MMAs' A operand, D / 2 columns) in [kQCol, kPVCol), PV in
+  // [kPVCol, kPVCol + D)
+  static constexpr uint32_t kPVCol = 256;
+  static constexpr uint32_t kQCol = kPVCol - D / 2;
+  static constexpr uint32_t kTmemCols = 512;
 };
 
 // Byte offset of 16-byte chunk `chunk16` of row r in a K-major tile with
@@ -337,6 +367,71 @@ __global__ void __launch_bounds__(256) prefix_tiles_bf16_kernel(PrefixParams p) 
   }
 }
 
+// ---- bf16 operand tiles from the BF16 paged cache (the BF16-KV comparison of
+// the prefix chunk): one CTA per (group, KV head).  Every key, history and
+// chunk alike, comes from the bf16 cache (K [NB, Hkv, D/8, 16, 8], V [NB, Hkv,
+// D, 16]) through block_table; keys past the sequence are zero (their cache
+// slots may hold anything, and a NaN there would reach the P x V sums).
+template <int D>
+__global__ void __launch_bounds__(256) prefix_tiles_bf16kv_kernel(PrefixParams p) {
+  using T = Tile<D>;
+  griddep_wait();
+  griddep_launch_dependents();
+  const int g = blockIdx.x, kvh = blockIdx.y, tid = threadIdx.x;
+  const int Hkv = p.Hkv, n = p.H + p.C;
+  const int key0 = g * kGroup;
+  uint8_t* tile = p.tiles + ((size_t)kvh * gridDim.x + g) * T::kBytes;
+  int blk[kPagesPG];
+#pragma unroll
+  for (int i = 0; i < kPagesPG; ++i) {
+    const int lb = g * kPagesPG + i;
+    blk[i] = -1;
+    if (lb * kBS < n) {
+      const int b = p.block_table[lb];
+      if (b < 0 || b >= p.num_blocks) {
+        if (tid == 0) record_error(2);
+      } else {
+        blk[i] = b;
+      }
+    }
+  }
+  const uint16_t* kc = p.kb_cache;
+  const uint16_t* vc = p.vb_cache;
+  // K: (page, 8-dim chunk, token) -> one 16-byte chunk of row `key` (SW128 atoms of 64 dims)
+  for (int i = tid; i < kPagesPG * (D / 8) * kBS; i += 256) {
+    const int pg = i / ((D / 8) * kBS), rem = i % ((D / 8) * kBS);
+    const int c8 = rem / kBS, tok = rem % kBS, key = pg * kBS + tok;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (blk[pg] >= 0 && key0 + key < n)
+      v = __ldg(reinterpret_cast<const uint4*>(kc + ((size_t)blk[pg] * Hkv + kvh) * (D * kBS)) + rem);
+    uint8_t* atom = tile + T::oK + (size_t)(c8 / 8) * (kGroup * 128);
+    *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, c8 % 8)) = v;
+  }
+  // V: (page, dim) -> the page's 16 tokens of that dim, chunks 2 pg and 2 pg + 1 of row d (SW64)
+  for (int i = tid; i < kPagesPG * D; i += 256) {
+    const int pg = i / D, d = i % D;
+    uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+    if (blk[pg] >= 0) {
+      const uint4* src = reinterpret_cast<const uint4*>(vc + (((size_t)blk[pg] * Hkv + kvh) * D + d) * kBS);
+      h0 = __ldg(src);
+      h1 = __ldg(src + 1);
+      const int valid = n - (key0 + pg * kBS);  // tokens of this page inside the sequence
+      if (valid < kBS) {
+        uint32_t w[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (2 * e >= valid) w[e] = 0u;
+          else if (2 * e + 1 >= valid) w[e] &= 0xffffu;
+        }
+        h0 = make_uint4(w[0], w[1], w[2], w[3]);
+        h1 = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
+    *reinterpret_cast<uint4*>(tile + T::oV + swz_chunk<64>(d, 2 * pg)) = h0;
+    *reinterpret_cast<uint4*>(tile + T::oV + swz_chunk<64>(d, 2 * pg + 1)) = h1;
+  }
+}
+
 // kBF: the high-precision variant -- bf16 query and tiles, no scales, and
 // the probabilities go to the PV MMA as bf16 p~ (no group quantization).
 // kDbg (INT8 only): the same kernel that also records its raw integer
@@ -347,16 +442,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
   static_assert(!(kDbg && kBF), "the debug record is for the INT8 path");
   using Ly = Lay<D>;
   using T = Tile<D>;
-  constexpr int DH = D / 2;  // output dims per warpgroup
+  constexpr int DH = D / 2;  // output dims per update warpgroup (one PV half)
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* tile_full = reinterpret_cast<uint64_t*>(smem + Ly::oBar);  // [g % kStages]: tile g landed
-  uint64_t* tile_free = tile_full + kStages;  // [g % kStages]: PV(g) done, the tile slot may be refilled
-  uint64_t* qk_done = tile_free + kStages;    // [g & 1]: S(g) in TMEM
+  uint64_t* tile_full = reinterpret_cast<uint64_t*>(smem + Ly::oBar);  // [g % Ly::kStages]: tile g landed
+  uint64_t* tile_free = tile_full + Ly::kStages;  // [g % Ly::kStages]: PV(g) done, the tile slot may be refilled
+  uint64_t* qk_done = tile_free + Ly::kStages;    // [g & 1]: S(g) in TMEM
   uint64_t* s_free = qk_done + 2;             // [g & 1]: S(g) read
   uint64_t* p_full = s_free + 2;              // [g & 1]: Wq(g) in its slot
-  uint64_t* pv_done = p_full + 2;             // [g & 1]: PV(g) in TMEM; the Wq slot free
-  uint64_t* pv_free = pv_done + 2;            // PV accumulator read by both warpgroups
-  uint64_t* st_full = pv_free + 1;            // [g & 3]: the group's row statistics
+  uint64_t* wq_free = p_full + 2;             // [g & 1]: PV(g) done (both halves), the Wq slot may be rewritten
+  uint64_t* pv_done = wq_free + 2;            // [half]: PV(g) of that half in TMEM
+  uint64_t* pv_free = pv_done + 2;            // [half]: that half of the accumulator read
+  uint64_t* st_full = pv_free + 2;            // [g & 3]: the group's row statistics
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::oCtl);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly::oCtl + 4);
 
@@ -384,20 +480,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
   const int g_begin = (int)((long long)ng_all * part / nparts);
   const int ng = (int)((long long)ng_all * (part + 1) / nparts) - g_begin;
   const int ngt = (H + C + kGroup - 1) / kGroup;  // groups of the whole sequence (tiles per KV head)
+  // The online softmax takes the key groups in any order, so each row block
+  // starts its walk at its own (hashed) offset and wraps around: the CTAs that
+  // run at the same time on one KV head then read different operand tiles,
+  // instead of all asking L2 for the same tile at once.
+  const int rot = ng > 0 ? (int)(((unsigned)(blk / p.Hkv) * 2654435761u >> 7) % (unsigned)ng) : 0;
+  auto gid = [&](int g) { return g_begin + (g + rot < ng ? g + rot : g + rot - ng); };
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < Ly::kStages; ++s) {
       mbar_init(&tile_full[s], 1);
       mbar_init(&tile_free[s], 1);
     }
     for (int s = 0; s < 4; ++s) mbar_init(&st_full[s], kWGThreads);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&qk_done[s], 1);
-      mbar_init(&s_free[s], kWGThreads);
+      mbar_init(&s_free[s], 2 * kWGThreads);  // both groups of a pair
       mbar_init(&p_full[s], kWGThreads);
+      mbar_init(&wq_free[s], 1);
       mbar_init(&pv_done[s], 1);
+      mbar_init(&pv_free[s], kWGThreads);
     }
-    mbar_init(pv_free, 2 * kWGThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -411,98 +514,175 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
   griddep_wait();
   griddep_launch_dependents();
 
-  // ---- Q tile -> f16 (all threads), K-major SW128 ----
-  {
-    uint8_t* q16 = smem + Ly::oQ;
-    constexpr int CH = D / 16;  // int8 chunks per row
-    for (int i = tid; i < kRows * CH; i += kThreads) {
-      const int rr = i / CH, dc = i % CH;
-      const int r = r0 + rr;
-      uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+  // ---- the f16 query rows -> TMEM (the softmax warpgroup: thread = row), the
+  // QK MMAs' A operand; row r of the block in lane r, two elements per column ----
+  if (warp >= kSmxWarp0) {
+    const int qrow = (warp & 3) * 32 + lane;
+    const int r = r0 + qrow;
+    const uint32_t qt = tmem + ((uint32_t)((warp & 3) * 32) << 16) + Ly::kQCol;
+#pragma unroll 1
+    for (int c = 0; c < D / 64; ++c) {  // 64 elements = 32 columns at a time
+      uint32_t w[32];
       if constexpr (kBF) {
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = make_uint4(0, 0, 0, 0);
         if (r < R) {
           const int j = r / G, hq = kvh * G + r % G;
-          const uint4* src = reinterpret_cast<const uint4*>(p.qb + ((size_t)j * Hq + hq) * D) + 2 * dc;
-          h0 = __ldg(src);
-          h1 = __ldg(src + 1);
+          const uint4* src = reinterpret_cast<const uint4*>(p.qb + ((size_t)j * Hq + hq) * D + 64 * c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = __ldg(src + i);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          w[4 * i] = v[i].x;
+          w[4 * i + 1] = v[i].y;
+          w[4 * i + 2] = v[i].z;
+          w[4 * i + 3] = v[i].w;
         }
       } else {
-        uint4 v = make_uint4(0, 0, 0, 0);
+        uint4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = make_uint4(0, 0, 0, 0);
         if (r < R) {
           const int j = r / G, hq = kvh * G + r % G;
-          v = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)j * Hq + hq) * D) + dc);
+          const uint4* src = reinterpret_cast<const uint4*>(p.q + ((size_t)j * Hq + hq) * D + 64 * c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[i] = __ldg(src + i);
         }
-        s8x16_to_f16(v, h0, h1);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 h0, h1;
+          s8x16_to_f16(v[i], h0, h1);
+          w[8 * i] = h0.x;
+          w[8 * i + 1] = h0.y;
+          w[8 * i + 2] = h0.z;
+          w[8 * i + 3] = h0.w;
+          w[8 * i + 4] = h1.x;
+          w[8 * i + 5] = h1.y;
+          w[8 * i + 6] = h1.z;
+          w[8 * i + 7] = h1.w;
+        }
       }
-      uint8_t* atom = q16 + (size_t)(dc / 4) * (kRows * 128);
-      *reinterpret_cast<uint4*>(atom + swz_chunk<128>(rr, 2 * (dc % 4))) = h0;
-      *reinterpret_cast<uint4*>(atom + swz_chunk<128>(rr, 2 * (dc % 4) + 1)) = h1;
+      tmem_st32(qt + 32 * c, w);
     }
-    fence_async_smem();
+    tmem_wait_st();
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
 
-  if (warp < kCompWarp0) {
-    regs_dec<64>();  // warpgroup 0 hands registers to the softmax/output warpgroups
-    if (warp == kLoadWarp && lane == 0) {
-      // ================= tile copies (warp 0, lane 0) =================
+  // this thread's query row (softmax and update warpgroups: one TMEM lane each)
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const int r = r0 + row;
+  const bool valid = r < R;
+  const int j = valid ? r / G : 0, hq = kvh * G + (valid ? r % G : 0);
+  const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+  float* stats = reinterpret_cast<float*>(smem + Ly::oSt);  // [slot][m_g | sW | l_g][row]
+
+  if (warp < kUpdWarp0) {
+    regs_dec<kRegsCtl>();  // the copy and MMA warps hand registers to the others
+    if (warp == kLoadWarp) {
+      // ================= tile copies (warp 0) =================
+      // A tile is D/64 K atoms of 4 KB, each into its row of the K ring, and
+      // the V tile with the scales behind it, into the V ring: one bulk copy
+      // per lane.
+      constexpr int kCopies = D / 64 + 1;
       const uint8_t* src = p.tiles + (size_t)kvh * ngt * T::kBytes;
       int g = 0;
       for (; g < ng; ++g) {
-        const int st = g % kStages;
-        if (g >= kStages) pwait(&tile_free[st], ((g - kStages) / kStages) & 1, abort_flag);
-        if (*abort_flag) break;
-        mbar_expect_tx(&tile_full[st], T::kBytes);
-        bulk_g2s(smem + Ly::oTile + (size_t)st * T::kSlot, src + (size_t)(g_begin + g) * T::kBytes, T::kBytes,
-                 &tile_full[st]);
-        mbar_arrive(&tile_full[st]);
+        const int st = g % Ly::kStages;
+        if (g >= Ly::kStages) pwait(&tile_free[st], ((g - Ly::kStages) / Ly::kStages) & 1, abort_flag);
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+        if (lane == 0) mbar_expect_tx(&tile_full[st], T::kBytes);
+        __syncwarp();
+        const uint8_t* tsrc = src + (size_t)gid(g) * T::kBytes;
+        if (lane < D / 64)
+          bulk_g2s(smem + Ly::oK + ((size_t)lane * Ly::kStages + st) * Ly::kKAtom, tsrc + T::oK + lane * Ly::kKAtom,
+                   Ly::kKAtom, &tile_full[st]);
+        else if (lane == D / 64)
+          bulk_g2s(smem + Ly::oVr + (size_t)st * Ly::kVSlot, tsrc + T::oV, Ly::kVBytes, &tile_full[st]);
+        static_assert(kCopies <= 32, "one copy per lane");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tile_full[st]);
       }
       // copies issued but never waited for (after an abort) land before the CTA exits
-      for (int k = max(0, g - kStages); k < g; ++k) mbar_wait(&tile_full[k % kStages], (k / kStages) & 1);
-    } else if (warp == kMmaWarp && lane == 0) {
-      // ================= MMA issue (warp 1, lane 0) =================
-      // Whichever of the next QK and the next PV has its operands first is
-      // issued; the checks never suspend (test_wait), a pass with nothing to
-      // issue sleeps briefly, and the same time limit as pwait applies.
-      constexpr uint32_t idesc_qk = kBF ? umma_idesc_bf16(kRows, kGroup) : umma_idesc_f16(kRows, kGroup);
-      constexpr uint32_t idesc_pv = kBF ? umma_idesc_bf16(kRows, D) : umma_idesc_f16(kRows, D);
-      const uint32_t q16 = smem_u32(smem + Ly::oQ);
-      const uint32_t tiles = smem_u32(smem + Ly::oTile);
-      int nq = 0, np = 0;  // next QK, next PV
+      if (lane == 0)
+        for (int k = max(0, g - Ly::kStages); k < g; ++k) mbar_wait(&tile_full[k % Ly::kStages], (k / Ly::kStages) & 1);
+    } else if ((warp == kMmaWarp || warp == kPvWarp) && lane == 0) {
+      // ================= MMA issue (warp 1: QK; warp 2: PV; lane 0 each) =================
+      // Two issuing threads, so that issuing one kind never holds up the other
+      // (a tcgen05.mma takes a while to be accepted).  The checks never suspend
+      // (test_wait); an idle pass spins (a sleep delayed the next issue by most
+      // of a microsecond), with the abort flag and the time limit checked every
+      // 64 idle passes.  A group's PV runs as two halves of D/2 columns, one
+      // per update warpgroup, so each half waits only for its own warpgroup's
+      // read of the previous group; the high half of a group follows its low half.
+      constexpr uint32_t idesc_qk = kBF ? umma_idesc_bf16(kRows, 2 * kGroup) : umma_idesc_f16(kRows, 2 * kGroup);
+      constexpr uint32_t idesc_pv = kBF ? umma_idesc_bf16(kRows, DH) : umma_idesc_f16(kRows, DH);
+      const uint32_t kring = smem_u32(smem + Ly::oK), vring = smem_u32(smem + Ly::oVr);
+      const bool qk = warp == kMmaWarp;
+      int nq = 0, np[2] = {0, 0};  // next QK pair's first group; next PV of each half
+      uint64_t* last_bar = nullptr;  // this thread's latest commit (it completes after its earlier MMAs)
+      uint32_t last_par = 0;
       uint64_t t_idle = 0;
-      while (np < ng) {
+      uint32_t idle = 0;
+      while (qk ? nq < ng : np[1] < ng) {
         bool did = false;
-        if (nq < ng && mbar_test(&tile_full[nq % kStages], (nq / kStages) & 1) &&
-            (nq < 2 || mbar_test(&s_free[nq & 1], ((nq - 2) >> 1) & 1))) {
-          const uint32_t k16 = tiles + (nq % kStages) * T::kSlot + T::oK;
-          tc_fence_after();
+        if (qk) {
+          // QK of the pair of groups (nq, nq + 1), nq even: their K rows are
+          // adjacent in the K ring (N = 64); a last group without a partner
+          // still runs as a pair (its partner's half of S is never read)
+          if (mbar_test(&tile_full[nq % Ly::kStages], (nq / Ly::kStages) & 1) &&
+              (nq + 1 >= ng || mbar_test(&tile_full[(nq + 1) % Ly::kStages], ((nq + 1) / Ly::kStages) & 1)) &&
+              (nq < 4 || mbar_test(&s_free[(nq >> 1) & 1], ((nq - 4) >> 2) & 1))) {
+            const uint32_t k16 = kring + (nq % Ly::kStages) * Ly::kKAtom;
+            tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t a = q16 + (kk / 4) * (kRows * 128) + (kk % 4) * 32;
-            const uint32_t b = k16 + (kk / 4) * (kGroup * 128) + (kk % 4) * 32;
-            umma_f16(tmem + 32 * (nq & 1), umma_desc(a, 128), umma_desc(b, 128), idesc_qk, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t b = k16 + (kk / 4) * (Ly::kStages * Ly::kKAtom) + (kk % 4) * 32;
+              umma_f16_ta(tmem + 64 * ((nq >> 1) & 1), tmem + Ly::kQCol + 8 * kk, umma_desc(b, 128), idesc_qk,
+                          kk > 0);
+            }
+            umma_commit(&qk_done[(nq >> 1) & 1]);
+            last_bar = &qk_done[(nq >> 1) & 1];
+            last_par = (nq >> 2) & 1;
+            nq += 2;
+            did = true;
           }
-          umma_commit(&qk_done[nq & 1]);
-          ++nq;
-          did = true;
-        }
-        if (np < nq && mbar_test(&p_full[np & 1], (np >> 1) & 1) &&
-            (np < 1 || mbar_test(pv_free, (np - 1) & 1))) {
-          const uint32_t p16 = smem_u32(smem + Ly::oP + (size_t)(np & 1) * Ly::kP16);
-          const uint32_t v16 = tiles + (np % kStages) * T::kSlot + T::oV;
-          tc_fence_after();
+        } else {
 #pragma unroll
-          for (int kk = 0; kk < kGroup / 16; ++kk)
-            umma_f16(tmem + Ly::kPVCol, umma_desc(p16 + kk * 32, 64), umma_desc(v16 + kk * 32, 64), idesc_pv,
-                     kk > 0);
-          umma_commit(&pv_done[np & 1]);
-          umma_commit(&tile_free[np % kStages]);
-          ++np;
-          did = true;
+          for (int hf = 0; hf < 2; ++hf) {
+            const int g = np[hf];
+            if (g < ng && (hf == 0 || g < np[0]) && mbar_test(&p_full[g & 1], (g >> 1) & 1) &&
+                (g < 1 || mbar_test(&pv_free[hf], (g - 1) & 1))) {
+              const uint32_t p16 = smem_u32(smem + Ly::oP + (size_t)(g & 1) * Ly::kP16);
+              // V tile rows (head dims) [hf DH, (hf + 1) DH): a whole number of SW64 atoms further on
+              const uint32_t v16 = vring + (g % Ly::kStages) * Ly::kVSlot + hf * DH * 64;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < kGroup / 16; ++kk)
+                umma_f16(tmem + Ly::kPVCol + hf * DH, umma_desc(p16 + kk * 32, 64), umma_desc(v16 + kk * 32, 64),
+                         idesc_pv, kk > 0);
+              umma_commit(&pv_done[hf]);
+              last_bar = &pv_done[hf];
+              last_par = g & 1;
+              if (hf == 1) {
+                umma_commit(&wq_free[g & 1]);
+                umma_commit(&tile_free[g % Ly::kStages]);
+                last_bar = &wq_free[g & 1];
+                last_par = (g >> 1) & 1;
+              }
+              ++np[hf];
+              did = true;
+            }
+          }
         }
         if (did) {
           t_idle = 0;
-        } else {
+          idle = 0;
+        } else if ((++idle & 63) == 0) {
           if (*abort_flag) break;
           const uint64_t now = global_timer_ns();
           if (t_idle == 0) {
@@ -512,80 +692,131 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
             *abort_flag = 1;
             break;
           }
-          __nanosleep(32);
         }
       }
-      // every MMA issued has completed before TMEM is released (the last commit
-      // covers all earlier MMAs)
-      if (np >= 1) mbar_wait(&pv_done[(np - 1) & 1], ((np - 1) >> 1) & 1);
-      if (nq > np) mbar_wait(&qk_done[(nq - 1) & 1], ((nq - 1) >> 1) & 1);
+      // every MMA this thread issued has completed before TMEM is released
+      if (last_bar) mbar_wait(last_bar, last_par);
     }
     __syncwarp();
-  } else {
-    // ================= softmax and output (warpgroups 1, 2) =================
-    regs_inc<216>();
-    const int wg = (warp - kCompWarp0) >> 2, quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const int r = r0 + row;
-    const bool valid = r < R;
-    const int j = valid ? r / G : 0, hq = kvh * G + (valid ? r % G : 0);
-    const int lim = valid ? H + j : -1;  // last visible key
-    // score in log2 units: acc x sQ x scale x log2(e) x sK
-    const float c2 = !valid ? 0.f
-                     : kBF  ? __fmul_rn(p.sm_scale, kLog2e)
-                            : __fmul_rn(__fmul_rn(p.q_scale[(size_t)j * Hq + hq], p.sm_scale), kLog2e);
-    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    float* stats = reinterpret_cast<float*>(smem + Ly::oSt);  // [slot][m_g | sW | l_g][row]
+  } else if (warp < kSmxWarp0) {
+    // ================= output update (warpgroups 1, 2: one PV half each) =================
+    regs_inc<kRegsUpd>();
+    const int hf = (warp - kUpdWarp0) >> 2;
     float o[DH];
 #pragma unroll
     for (int i = 0; i < DH; ++i) o[i] = 0.f;
-    float m = -INFINITY, l = 0.f;
-
-    // softmax of group g (this warpgroup's parity): codes into the Wq slot,
-    // (m_g, sW, l_g) into the statistics slot
-    auto softmax = [&](int g) {
-      const int sl = g & 1;
-      pwait(&qk_done[sl], (g >> 1) & 1, abort_flag);
+    float m = -INFINITY, l = 0.f;  // m: the reference maximum o and l are scaled to (log2 units)
+    const uint32_t src = trow + Ly::kPVCol + hf * DH;
+    for (int g = 0; g < ng; ++g) {
+      // o = alpha o + 2^(m_g - m) sW (Wq x Vq), l = alpha l + 2^(m_g - m) l_g.  The
+      // reference maximum moves only when a group's maximum exceeds it by more than
+      // kLazyLog2 (then alpha = 2^(m - m_g)); otherwise alpha = 1 and the group's
+      // factor is at most 2^kLazyLog2, so o is rescaled only a few times per row.
+      pwait(&pv_done[hf], g & 1, abort_flag);
+      pwait(&st_full[g & 3], (g >> 2) & 1, abort_flag);
+      const float* st = stats + (g & 3) * 3 * kRows;
+      const float mg = st[row], sw = st[kRows + row], lg = st[2 * kRows + row];
+      float alpha = 1.f, e = 0.f;
+      if (mg != -INFINITY) {
+        if (mg > m + kLazyLog2) {  // also the first group (m = -inf)
+          alpha = m == -INFINITY ? 0.f : ex2(__fsub_rn(m, mg));
+          l = __fmul_rn(l, alpha);
+          m = mg;
+        }
+        const float f = ex2(__fsub_rn(mg, m));
+        e = __fmul_rn(f, sw);
+        l = __fmaf_rn(lg, f, l);
+      }
       tc_fence_after();
-      float s[32];
-      tmem_ld32(trow + 32 * sl, s);
-      const int key0 = (g_begin + g) * kGroup;
-      const bool full = __all_sync(0xffffffffu, key0 + kGroup - 1 <= lim);  // no key of the warp is masked
-      float mg, lg = 0.f, sw = 0.f;
-      uint32_t pk[16];
-      if constexpr (kBF) {
+      const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
+      // kCh-column chunks, two in flight: chunk c + 1 is loading while chunk c
+      // joins the output (tcgen05.wait::ld waits for every load issued so far)
+      // kCh-column chunks, one load in flight: the round trips, not the few
+      // fused multiply-adds between them, set the pace, so the widest load the
+      // registers allow (o takes D/2 of them) comes first
+      constexpr int kCh = kUpdChunk;
+#pragma unroll
+      for (int c = 0; c < DH / kCh; ++c) {
+        float x[kCh];
+        tmem_ld_chunk(src + kCh * c, x);
         tmem_wait_ld();
-        {
-          const uint64_t cc = f2(c2, c2);
-#pragma unroll
-          for (int t = 0; t < 16; ++t) f2_split(mul2(f2(s[2 * t], s[2 * t + 1]), cc), s[2 * t], s[2 * t + 1]);
+        if (c + 1 == DH / kCh) {
+          tc_fence_before();
+          mbar_arrive(&pv_free[hf]);  // every column of this half is read
         }
-        if (!full) {
+        if constexpr (kDbg) {
+          // this group's Wq x Vq for this half's dims (exact integers in fp32)
+          if (valid) {
+            int32_t* prow = p.dbg_pv + (((size_t)j * Hq + hq) * ngt + gid(g)) * D + hf * DH + kCh * c;
 #pragma unroll
-          for (int t = 0; t < 32; ++t)
-            if (key0 + t > lim) s[t] = -INFINITY;
+            for (int i = 0; i < kCh; ++i) prow[i] = __float2int_rn(x[i]);
+          }
         }
-        mg = tree_max(s);
-        if (mg != -INFINITY) {
+        const uint64_t e2 = f2(e, e);
+        if (rescale) {
+          const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
-          for (int t = 0; t < 32; ++t) s[t] = ex2(__fsub_rn(s[t], mg));  // p~; 0 for a masked key
-          lg = tree_sum(s);
-          sw = 1.f;
+          for (int i = 0; i < kCh / 2; ++i)
+            f2_split(fma2(f2(x[2 * i], x[2 * i + 1]), e2, mul2(f2(o[kCh * c + 2 * i], o[kCh * c + 2 * i + 1]), a2)),
+                     o[kCh * c + 2 * i], o[kCh * c + 2 * i + 1]);
         } else {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) s[t] = 0.f;
+          for (int i = 0; i < kCh / 2; ++i)
+            f2_split(fma2(f2(x[2 * i], x[2 * i + 1]), e2, f2(o[kCh * c + 2 * i], o[kCh * c + 2 * i + 1])),
+                     o[kCh * c + 2 * i], o[kCh * c + 2 * i + 1]);
         }
-        tc_fence_before();
-        mbar_arrive(&s_free[sl]);  // S is read; QK(g + 2) may overwrite it
-        // p~ as bf16, two per register (low half = the even key)
+      }
+    }
+    // ---- finish: O = o / l (both warpgroups hold the same l), or this part's
+    // unnormalized (o, m, l) for the merge ----
+    if (valid && nparts > 1) {
+      float* ps = p.part + ((size_t)(blockIdx.x - p.full_items) * kRows + row) * (D + 4);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = bf16x2_bits(s[2 * i], s[2 * i + 1]);
-      } else {
-      pwait(&tile_full[g % kStages], (g / kStages) & 1, abort_flag);  // the group's scales (already landed)
-      const float4* sk4 =
-          reinterpret_cast<const float4*>(smem + Ly::oTile + (size_t)(g % kStages) * T::kSlot + T::oSk);
-      const float4* sv4 = sk4 + kGroup / 4;
+      for (int i = 0; i < DH / 4; ++i)
+        reinterpret_cast<float4*>(ps + hf * DH)[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+      if (hf == 0) {
+        ps[D] = m;
+        ps[D + 1] = l;
+      }
+    } else if (valid) {
+      const float inv = 1.0f / l;
+      const size_t orow = ((size_t)j * Hq + hq) * D + hf * DH;
+#pragma unroll
+      for (int i = 0; i < DH / 4; ++i)
+        store_out4(p.out, p.out_bf16, orow + 4 * i,
+                   make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv));
+    }
+  } else {
+    // ================= softmax of every group (warpgroup 3) =================
+    regs_dec<kRegsSmx>();
+    const int lim = valid ? H + j : -1;  // last visible key
+    // score in log2 units: acc x sK x (sQ x scale x log2(e))
+    const float c2 = !valid ? 0.f
+                     : kBF  ? __fmul_rn(p.sm_scale, kLog2e)
+                            : __fmul_rn(__fmul_rn(p.q_scale[(size_t)j * Hq + hq], p.sm_scale), kLog2e);
+    const uint64_t c2p = f2(c2, c2);
+    for (int g = 0; g < ng; ++g) {
+      const int sl = g & 1;
+      pwait(&qk_done[(g >> 1) & 1], (g >> 2) & 1, abort_flag);
+      tc_fence_after();
+      float s[32];
+      tmem_ld32(trow + 64 * ((g >> 1) & 1) + 32 * sl, s);
+      const int key0 = gid(g) * kGroup;
+      const bool full = __all_sync(0xffffffffu, key0 + kGroup - 1 <= lim);  // no key of the warp is masked
+      float mg = -INFINITY, lg = 0.f, sw = 0.f;
+      uint32_t pk[16];
+      // x = acc x sK (INT8) or acc (BF16); m_g = c2 max x (c2 >= 0, so rounding
+      // keeps the order); p~ = 2^(x c2 - m_g), one fused multiply-add per key;
+      // a masked key has x = -inf and p~ = 0.
+      const float4* sk4 = nullptr;
+      if constexpr (!kBF) {
+        pwait(&tile_full[g % Ly::kStages], (g / Ly::kStages) & 1, abort_flag);  // the group's scales (already landed)
+        sk4 = reinterpret_cast<const float4*>(smem + Ly::oVr + (size_t)(g % Ly::kStages) * Ly::kVSlot +
+                                              (T::oSk - T::oV));
+      }
       tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&s_free[(g >> 1) & 1]);  // S is in registers; the QK of the pair after next may overwrite it
       if constexpr (kDbg) {
         // the raw accumulators of the visible keys (exact integers in fp32)
         if (valid) {
@@ -595,13 +826,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
             if (key0 + t <= lim) srow[key0 + t] = __float2int_rn(s[t]);
         }
       }
-      {
-        const uint64_t cc = f2(c2, c2);
+      if constexpr (!kBF) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const float4 k4 = sk4[i];
-          f2_split(mul2(mul2(f2(s[4 * i], s[4 * i + 1]), f2(k4.x, k4.y)), cc), s[4 * i], s[4 * i + 1]);
-          f2_split(mul2(mul2(f2(s[4 * i + 2], s[4 * i + 3]), f2(k4.z, k4.w)), cc), s[4 * i + 2], s[4 * i + 3]);
+          f2_split(mul2(f2(s[4 * i], s[4 * i + 1]), f2(k4.x, k4.y)), s[4 * i], s[4 * i + 1]);
+          f2_split(mul2(f2(s[4 * i + 2], s[4 * i + 3]), f2(k4.z, k4.w)), s[4 * i + 2], s[4 * i + 3]);
         }
       }
       if (!full) {
@@ -609,61 +839,77 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
         for (int t = 0; t < 32; ++t)
           if (key0 + t > lim) s[t] = -INFINITY;
       }
-      mg = tree_max(s);
+      const float mx = tree_max(s);
       float A = 0.f;
-      if (mg != -INFINITY) {
+      if (mx != -INFINITY) {
+        mg = __fmul_rn(mx, c2);
+        const uint64_t nm = f2(-mg, -mg);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) s[t] = ex2(__fsub_rn(s[t], mg));  // p~; 0 for a masked key
-        lg = tree_sum(s);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 v4 = sv4[i];
-          f2_split(mul2(f2(s[4 * i], s[4 * i + 1]), f2(v4.x, v4.y)), s[4 * i], s[4 * i + 1]);
-          f2_split(mul2(f2(s[4 * i + 2], s[4 * i + 3]), f2(v4.z, v4.w)), s[4 * i + 2], s[4 * i + 3]);
+        for (int i = 0; i < 16; ++i) {
+          float lo, hi;
+          f2_split(fma2(f2(s[2 * i], s[2 * i + 1]), c2p, nm), lo, hi);
+          s[2 * i] = ex2(lo);
+          s[2 * i + 1] = ex2(hi);
         }
-        if (!full) {
+        if (!full) {  // a masked key's -inf times c2 = 0 (a zero query) would be NaN
 #pragma unroll
           for (int t = 0; t < 32; ++t)
             if (key0 + t > lim) s[t] = 0.f;
         }
-        A = tree_max(s);
-      }
-      tc_fence_before();
-      mbar_arrive(&s_free[sl]);  // S is read; QK(g + 2) may overwrite it
-      // sW = A / 127 and the codes round(W / sW), both IEEE fp32 quotients (W / sW
-      // by Markstein's method); W / sW <= A / RN(A / 127) < 127.5, no clamp needed
-      sw = div127(A);
-      if (A > 0.f) {
-        // round-half-even(q) + 1024 as the f16 bit pattern 0x6400 + code, from the
-        // low bits of the fp32 sum q + 1.5 * 2^23 + 0x6400; two per register, then
-        // 1024 subtracted (exact)
-        uint32_t qb[32];
-        div_rne_row(s, sw, __frcp_rn(sw), qb, 12608512.0f);
+        lg = tree_sum(s);
+        if constexpr (!kBF) {
+          const float4* sv4 = sk4 + kGroup / 4;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t lo = qb[2 * i], hi = qb[2 * i + 1];
-          uint32_t h = __byte_perm(lo, hi, 0x5410);
-          asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(h) : "r"(0x64006400u));
-          pk[i] = h;
+          for (int i = 0; i < 8; ++i) {
+            const float4 v4 = sv4[i];
+            f2_split(mul2(f2(s[4 * i], s[4 * i + 1]), f2(v4.x, v4.y)), s[4 * i], s[4 * i + 1]);
+            f2_split(mul2(f2(s[4 * i + 2], s[4 * i + 3]), f2(v4.z, v4.w)), s[4 * i + 2], s[4 * i + 3]);
+          }
+          A = tree_max(s);
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = 0u;
+        for (int t = 0; t < 32; ++t) s[t] = 0.f;
       }
-      }
-      if constexpr (kDbg) {
-        if (valid) {
-          uint8_t* wrow = p.dbg_wq + ((size_t)j * Hq + hq) * (size_t)(ngt * kGroup);
+      if constexpr (kBF) {
+        sw = 1.f;
+        // p~ as bf16, two per register (low half = the even key)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = bf16x2_bits(s[2 * i], s[2 * i + 1]);
+      } else {
+        // sW = A / 127 and the codes round(W / sW), both IEEE fp32 quotients (W / sW
+        // by Markstein's method); W / sW <= A / RN(A / 127) < 127.5, no clamp needed
+        sw = div127(A);
+        if (A > 0.f) {
+          // round-half-even(q) + 1024 as the f16 bit pattern 0x6400 + code, from the
+          // low bits of the fp32 sum q + 1.5 * 2^23 + 0x6400; two per register, then
+          // 1024 subtracted (exact)
+          uint32_t qb[32];
+          div_rne_row(s, sw, __frcp_rn(sw), qb, 12608512.0f);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
-            if (key0 + 2 * i <= lim) wrow[key0 + 2 * i] = (uint8_t)__float2int_rn(c.x);
-            if (key0 + 2 * i + 1 <= lim) wrow[key0 + 2 * i + 1] = (uint8_t)__float2int_rn(c.y);
+            uint32_t h = __byte_perm(qb[2 * i], qb[2 * i + 1], 0x5410);
+            asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(h) : "r"(0x64006400u));
+            pk[i] = h;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = 0u;
+        }
+        if constexpr (kDbg) {
+          if (valid) {
+            uint8_t* wrow = p.dbg_wq + ((size_t)j * Hq + hq) * (size_t)(ngt * kGroup);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 cc = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
+              if (key0 + 2 * i <= lim) wrow[key0 + 2 * i] = (uint8_t)__float2int_rn(cc.x);
+              if (key0 + 2 * i + 1 <= lim) wrow[key0 + 2 * i + 1] = (uint8_t)__float2int_rn(cc.y);
+            }
           }
         }
       }
       // Wq (f16) or p~ (bf16) -> the PV A tile, row `row`; then the row statistics
-      if (g >= 2) pwait(&pv_done[sl], ((g - 2) >> 1) & 1, abort_flag);  // PV(g-2) has read the slot
+      if (g >= 2) pwait(&wq_free[sl], ((g - 2) >> 1) & 1, abort_flag);  // PV(g-2) has read the slot
       uint8_t* p16 = smem + Ly::oP + (size_t)sl * Ly::kP16;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
@@ -676,88 +922,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefix_attn_kernel(PrefixParams p
       st[kRows + row] = sw;
       st[2 * kRows + row] = lg;
       mbar_arrive(&st_full[g & 3]);
-    };
-
-    // o = alpha o + exp(m_g - m') sW (Wq x Vq), l = alpha l + exp(m_g - m') l_g
-    auto update = [&](int h) {
-      pwait(&pv_done[h & 1], (h >> 1) & 1, abort_flag);
-      pwait(&st_full[h & 3], (h >> 2) & 1, abort_flag);
-      const float* st = stats + (h & 3) * 3 * kRows;
-      const float mg = st[row], sw = st[kRows + row], lg = st[2 * kRows + row];
-      float alpha = 1.f, e = 0.f;
-      if (mg != -INFINITY) {
-        const float mn = fmaxf(m, mg);
-        alpha = m == -INFINITY ? 0.f : ex2(__fsub_rn(m, mn));
-        const float f = ex2(__fsub_rn(mg, mn));
-        e = __fmul_rn(f, sw);
-        l = __fmaf_rn(l, alpha, __fmul_rn(f, lg));
-        m = mn;
-      }
-      tc_fence_after();
-      const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
-      // 32-column chunks, two in flight: chunk c + 1 is loading while chunk c
-      // joins the output (tcgen05.wait::ld waits for every load issued so far)
-      const uint32_t src = trow + Ly::kPVCol + wg * DH;
-      float v[2][32];
-      tmem_ld32(src, v[0]);
-#pragma unroll
-      for (int c = 0; c < DH / 32; ++c) {
-        tmem_wait_ld();
-        if (c + 1 < DH / 32) {
-          tmem_ld32(src + 32 * (c + 1), v[(c + 1) & 1]);
-        } else {
-          tc_fence_before();
-          mbar_arrive(pv_free);  // every column of the accumulator is read
-        }
-        const float(&x)[32] = v[c & 1];
-        if constexpr (kDbg) {
-          // this group's Wq x Vq for this warpgroup's dims (exact integers in fp32)
-          if (valid) {
-            int32_t* prow = p.dbg_pv + (((size_t)j * Hq + hq) * ngt + (g_begin + h)) * D + wg * DH + 32 * c;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) prow[i] = __float2int_rn(x[i]);
-          }
-        }
-        const uint64_t e2 = f2(e, e);
-        if (rescale) {
-          const uint64_t a2 = f2(alpha, alpha);
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            f2_split(fma2(f2(x[2 * i], x[2 * i + 1]), e2, mul2(f2(o[32 * c + 2 * i], o[32 * c + 2 * i + 1]), a2)),
-                     o[32 * c + 2 * i], o[32 * c + 2 * i + 1]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            f2_split(fma2(f2(x[2 * i], x[2 * i + 1]), e2, f2(o[32 * c + 2 * i], o[32 * c + 2 * i + 1])),
-                     o[32 * c + 2 * i], o[32 * c + 2 * i + 1]);
-        }
-      }
-    };
-
-    for (int g = 0; g < ng; ++g) {
-      if ((g & 1) == wg) softmax(g);
-      if (g >= 1) update(g - 1);
-    }
-    if (ng >= 1) update(ng - 1);
-
-    // ---- finish: O = o / l (both warpgroups hold the same l), or this part's
-    // unnormalized (o, m, l) for the merge ----
-    if (valid && nparts > 1) {
-      float* ps = p.part + ((size_t)(blockIdx.x - p.full_items) * kRows + row) * (D + 4);
-#pragma unroll
-      for (int i = 0; i < DH / 4; ++i)
-        reinterpret_cast<float4*>(ps + wg * DH)[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-      if (wg == 0) {
-        ps[D] = m;
-        ps[D + 1] = l;
-      }
-    } else if (valid) {
-      const float inv = 1.0f / l;
-      const size_t orow = ((size_t)j * Hq + hq) * D + wg * DH;
-#pragma unroll
-      for (int i = 0; i < DH / 4; ++i)
-        store_out4(p.out, p.out_bf16, orow + 4 * i,
-                   make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv));
     }
   }
 
@@ -852,8 +1016,9 @@ template <int D, bool kBF, bool kDbg = false>
 cudaError_t launch_prefix_d(const PrefixParams& p0, cudaStream_t stream) {
   PrefixParams p = p0;
   const int ngt = (p.H + p.C + kGroup - 1) / kGroup;
-  cudaError_t e = kBF ? launch_pdl(prefix_tiles_bf16_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p)
-                      : launch_pdl(prefix_tiles_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p);
+  cudaError_t e = !kBF          ? launch_pdl(prefix_tiles_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p)
+                  : p.kb_cache ? launch_pdl(prefix_tiles_bf16kv_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p)
+                               : launch_pdl(prefix_tiles_bf16_kernel<D>, dim3(ngt, p.Hkv), dim3(256), 0, stream, p);
   if (e != cudaSuccess) return e;
   // the shared-memory opt-in, once per device (graph captures then make no attribute call)
   int dev = 0;
