@@ -792,6 +792,8 @@ def run_secondary(torch, i8, hbm_peak, tensor_peak=0.0, peak_kind="measured"):
                                       "tcgen05 f16 path, which has the bf16 rate",
                          "kernel": "prefix_tiles_kernel + prefix_attn_kernel<256, INT8> + prefix_merge_kernel",
                          "algorithmic_ops_per_launch": w.int8_ops(),
+                         "traffic": recorded_traffic("int8_prefix", kernel_hash(
+                             "int8_kv_cache_token_gb300/csrc/prefix.cu", "int8_kv_cache_token_gb300/csrc/common.cuh")),
                          "method": "3 rotating copies of cache + workspace + query + output (3x L2), 12 calls in "
                                    "one CUDA graph, CUDA events around it"}}
         del sets, calls
