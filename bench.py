@@ -35,6 +35,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -66,10 +67,15 @@ def measured_peaks():
 
 
 def kernel_hash(*rel):
+    """Hash of the kernel sources' code: comments and whitespace are dropped, so
+    a comment edit does not void a recorded ncu figure."""
     h = hashlib.sha256()
     for r in rel:
-        with open(os.path.join(ROOT, r), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, r), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -12,19 +12,22 @@
 // GB300 shape.  A CTA owns 128 query rows of one KV head -- (chunk token, query
 // head) pairs of that head's GQA group, token-major, so the query heads sharing
 // K/V read the same tiles -- and walks the keys in 32-key probability groups:
-//   S  = Qq x Kq^T        tcgen05, M = 128, N = 32, K = D, into TMEM
+//   S  = Qq x Kq^T        tcgen05, M = 128, N = 64 (two groups at once), K = D,
+//                         the query codes (A) held in tensor memory, into TMEM
 //   scores, causal mask, p~ = exp(s - m_g) against the group's own row
 //   maximum m_g, W = p~ sV, sW = max W / 127, Wq = round(W / sW)
 //                         CUDA cores, one thread per row
-//   PV = Wq x Vq          tcgen05, M = 128, N = D, K = 32, into TMEM
-//   o  = alpha o + exp(m_g - m') sW PV,  l = alpha l + exp(m_g - m') l_g
+//   PV = Wq x Vq          tcgen05, M = 128, N = D / 2 per half, K = 32, into TMEM
+//   o  = alpha o + exp(m_g - m) sW PV,  l = alpha l + exp(m_g - m) l_g
 //                         CUDA cores, o in registers (half of D per thread)
-// with m' = max(m, m_g) and alpha = exp(m - m').  The codes round(W / sW) do
-// not change when W is scaled, so quantizing each group against m_g and
-// bringing it to the running maximum in the output update is the pages' online
-// softmax, reordered; it lets the softmax of a group start before the previous
-// group's maximum is known.  Scores are kept in log2 units (the scale folds in
-// log2 e) so every exponential is one ex2.
+// where m is the row's reference maximum.  The codes round(W / sW) do not
+// change when W is scaled, so quantizing each group against m_g and bringing it
+// to the reference maximum in the output update is the pages' online softmax,
+// reordered; it lets the softmax of a group start before the previous group's
+// maximum is known.  The reference maximum moves only when a group's maximum
+// passes it by more than 2^8 (alpha = 1 otherwise), so o is rarely rescaled.
+// Scores are kept in log2 units (the scale folds in log2 e) so every
+// exponential is one ex2.
 //
 // The int8 codes are exact in f16, every product (<= 127^2) is exact and every
 // partial sum stays below 2^22, so f16 MMAs with fp32 accumulation give the
@@ -35,15 +38,27 @@
 // 32-key group) by prefix_tiles_kernel, into a workspace tile laid out exactly
 // as the MMAs read it in shared memory (K-major, 16-byte chunks XOR-swizzled:
 // K as [key][dim] in 128-byte rows, V as [dim][key] in 64-byte rows) followed
-// by the group's sK and sV.  The attention kernel moves each tile with one
-// bulk copy.
+// by the group's sK and sV.  The attention kernel moves a tile with D/64 + 1
+// bulk copies: K into a ring of its own, atom-major, so the K rows of two
+// adjacent stages form one 64-key operand, and V with the scales into a second
+// ring.  Each row block starts its walk over the key groups at its own hashed
+// offset and wraps around, so the CTAs that run together on one KV head read
+// different tiles.
 //
-// Warps of the attention kernel.  Warp 0 lane 0 issues the tiles' bulk copies
-// (a ring of four); warp 1 owns the TMEM allocation and its lane 0 issues every
-// MMA, each QK or PV as soon as its operands are ready.  Warpgroups 1 and 2
-// (warps 4-7, 8-11) take the softmax of the even and the odd groups, thread =
-// row, so the two run side by side; both apply every group's product to their
-// half of the output dims.
+// Warps of the attention kernel (512 threads, one CTA per SM):
+//   warp 0      the tile copies (one lane per copy)
+//   warp 1      lane 0 issues the QK MMAs of each pair of groups into one of two
+//               64-column S slots; the warp owns the TMEM allocation
+//   warp 2      lane 0 issues the PV MMAs, each group as two halves of D / 2
+//               columns, one per update warpgroup
+//   warps 4-11  two update warpgroups, one half of D each: o, l per row
+//   warps 12-15 the softmax warpgroup: loads the query rows into TMEM, then the
+//               softmax of every group (thread = row), handing the f16 codes
+//               (a swizzled Wq tile) and (m_g, sW, l_g) to the PV issuer and
+//               the update warpgroups
+// so the softmax of group g + 1 runs while the update warpgroups apply group g.
+// setmaxnreg splits the registers 40 / 184 / 184 / 104 between the control
+// warps, the update warpgroups and the softmax warpgroup.
 //
 // The same kernel, instantiated with kBF, is the high-precision chunk path
 // ("gfx936 DCU上实现INT8 KV与INT8 MMAC Attention推理优化" §3.1: the first
