@@ -305,11 +305,14 @@ __global__ void __launch_bounds__(kProdThreads, 1) kv_quant_write_kernel(Produce
       }
       return true;
     };
-    long long i = 0;
+    // The unit's tile n, its place k in the tile, its slot s and the slot's use
+    // advance by increments (no divisions per unit).
+    const int nloc = (int)(u1 - u0);
+    long long n = u0 / g.upt;
+    int k = (int)(u0 - n * g.upt), s = 0, use = 0, i = 0;
     bool ok = true;
-    for (long long u = u0; u < u1 && ok; ++u, ++i) {
-      const long long n = u / g.upt;
-      if (n != cur) {
+    for (; i < nloc; ++i) {
+      if (i == 0 || k == 0) {
         if (pending && !publish()) {
           ok = false;
           break;
@@ -321,8 +324,6 @@ __global__ void __launch_bounds__(kProdThreads, 1) kv_quant_write_kernel(Produce
         read_meta(n + 1, nx_s, nx_pos);
         pending = true;
       }
-      const int s = (int)(i % g.S);
-      const long long use = i / g.S;
       if (use > 0) {
         if (pending && !publish()) {
           ok = false;
@@ -333,7 +334,6 @@ __global__ void __launch_bounds__(kProdThreads, 1) kv_quant_write_kernel(Produce
           break;
         }
       }
-      const int k = (int)(u - n * g.upt);
       const int kind = k < g.nkv ? 1 : (k < 2 * g.nkv ? 0 : 2);  // 0 K, 1 V, 2 Q
       const int nh = kind == 2 ? g.qh : g.kvh;
       const int h0 = (kind == 2 ? k - 2 * g.nkv : (kind == 1 ? k : k - g.nkv)) * nh;
@@ -342,13 +342,21 @@ __global__ void __launch_bounds__(kProdThreads, 1) kv_quant_write_kernel(Produce
       const int ntv = (int)min((long long)kTok, (long long)T - n * kTok);
       const uint32_t rb = (uint32_t)nh * D * 2;
       if (lane == 0) {
-        slot_use[s] = (int)use;
+        slot_use[s] = use;
         mbar_expect_tx(&full[s], ntv * rb);
         mbar_arrive(&full[s]);
       }
       if (lane < ntv)
         bulk_g2s(ring + (size_t)s * g.slot_bytes + (size_t)lane * g.row_stride,
                  src + ((size_t)(n * kTok + lane) * H + h0) * D, rb, &full[s]);
+      if (++s == g.S) {
+        s = 0;
+        ++use;
+      }
+      if (++k == g.upt) {
+        k = 0;
+        ++n;
+      }
     }
     if (ok && pending) ok = publish();
     if (!ok) {
@@ -356,11 +364,11 @@ __global__ void __launch_bounds__(kProdThreads, 1) kv_quant_write_kernel(Produce
       // into it has landed.  Slot s's last issued item is the newest local
       // unit j < i with j % S == s.
       *abort_flag = 1;
-      for (int s = 0; s < g.S; ++s) {
-        const long long last = i - 1 - ((i - 1 - s) % g.S + g.S) % g.S;
+      for (int sl = 0; sl < g.S; ++sl) {
+        const int last = i - 1 - ((i - 1 - sl) % g.S + g.S) % g.S;
         if (last < 0 || last >= i) continue;
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(&full[s], (uint32_t)((last / g.S) & 1)) && global_timer_ns() - t0 < kWaitLimitNs) {
+        while (!mbar_try_wait(&full[sl], (uint32_t)((last / g.S) & 1)) && global_timer_ns() - t0 < kWaitLimitNs) {
         }
       }
     }
@@ -378,28 +386,40 @@ __global__ void __launch_bounds__(kProdThreads, 1) kv_quant_write_kernel(Produce
   float* nscr = reinterpret_cast<float*>(dsm + g.off_nscr) + warp * VPW * R;
   const int G = p.q ? p.Hq / p.Hkv : 1;
 
-  long long cur = -1, tbase = 0;
-  int tl = -1;
-  long long i = 0;
-  for (long long u = u0; u < u1; ++u, ++i) {
-    const long long n = u / g.upt;
-    if (n != cur) {
+  // Per unit: its tile n and place k, its slot s and the slot's use, and the
+  // CTA's task count modulo kNCW, all advanced by increments.
+  const int nloc = (int)(u1 - u0);
+  long long n = u0 / g.upt;
+  int k = (int)(u0 - n * g.upt), s = 0, use = 0, tmod = 0, tl = -1;
+  auto advance = [&](int nh) {
+    tmod += nh;
+    if (tmod >= kNCW) tmod -= kNCW;
+    if (++s == g.S) {
+      s = 0;
+      ++use;
+    }
+    if (++k == g.upt) {
+      k = 0;
+      ++n;
+    }
+  };
+  for (int i = 0; i < nloc; ++i) {
+    if (i == 0 || k == 0) {
       if (tl >= 0) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&tile_free[tl % kTR]);
       }
-      cur = n;
       ++tl;
       if (!wait_or_abort(&meta_full[tl % kTR], (uint32_t)((tl / kTR) & 1), abort_flag)) break;
     }
-    const int k = (int)(u - n * g.upt);
     const int kind = k < g.nkv ? 1 : (k < 2 * g.nkv ? 0 : 2);
     const int nh = kind == 2 ? g.qh : g.kvh;
-    const int hp = (int)((warp - tbase % kNCW + kNCW) % kNCW);  // this warp's task in the unit
-    tbase += nh;
-    if (hp >= nh) continue;
-    const int s = (int)(i % g.S);
-    const int use = (int)(i / g.S);
+    int hp = warp - tmod;  // this warp's task in the unit
+    if (hp < 0) hp += kNCW;
+    if (hp >= nh) {
+      advance(nh);
+      continue;
+    }
     if (slot_use[s] != use) {
       const uint64_t t0 = global_timer_ns();
       while (slot_use[s] != use && !*abort_flag) {
@@ -582,6 +602,7 @@ __global__ void __launch_bounds__(kProdThreads, 1) kv_quant_write_kernel(Produce
     }
     __syncwarp();
     if (lane == 0) mbar_arrive_n(&freeb[s], hp == 0 ? 1 + kNCW - nh : 1);
+    advance(nh);
   }
 }
 
