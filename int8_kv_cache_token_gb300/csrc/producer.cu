@@ -20,10 +20,14 @@
 //  * 15 compute warps: the unit's heads are its tasks, handed out round-robin
 //    (the CTA's task t goes to warp t % 15, so about two units are in work at
 //    once); a task is one head over the tile's 16 tokens.  With the loader the
-//    CTA has 16 warps, four per SM sub-partition, at 128 registers each.  A vector (token, head) is held by D/32 lanes, 32 elements per
-//    lane in two 16-element runs, so a warp pass covers 1024 / D tokens.  The
-//    absmax is a max over the lane's 32 values, then xor-shuffles inside the
-//    lane group.
+//    CTA has 16 warps, four per SM sub-partition, at 128 registers each.
+//    A vector (token, head) is held by D/32 lanes, 32 elements per lane in two
+//    16-element runs, so a warp pass covers VPW = 1024 / D tokens.  Lane =
+//    c * VPW + token, with c the lane's place in its vector: the 8 lanes of a
+//    quarter-warp then read the same run of 8 consecutive token rows, which the
+//    16-byte row padding puts on 8 different bank groups.  The absmax is a max
+//    over the lane's 32 values, then xor-shuffles across the vector's lanes
+//    (distances VPW, 2 VPW, ...).
 //  * Outputs leave as 16-byte stores: K and Q codes per run (K's 16-dim chunk
 //    layout makes a run contiguous), V per warp: when the tile fills one whole
 //    block in order (the common prefill case) the task's 16 x D codes are
@@ -123,15 +127,15 @@ __device__ __forceinline__ uint4 pack_codes16(const uint32_t* q) {
   return make_uint4(pk[0], pk[1], pk[2], pk[3]);
 }
 
-// Quantize the vector whose 32 elements this lane holds (a group of LPV lanes
-// holds one vector).  Every lane of the warp calls this (the absmax shuffles
+// Quantize the vector whose 32 elements this lane holds (the lanes VPW apart
+// hold one vector).  Every lane of the warp calls this (the absmax shuffles
 // across the whole warp).  Returns the vector's scale; codes of the lane's two
 // runs in ca, cb.
 //  Codes: round half to even by adding 1.5 * 2^23 (the fp32 sum keeps the
 //  integer part of x / scale in its low mantissa bits, so its low byte is the
 //  two's-complement code).  |x / scale| <= amax / RN(amax / 127) < 127.5, so no
 //  code ever needs clamping to [-127, 127].
-template <int LPV>
+template <int VPW>
 __device__ __forceinline__ float quantize32(const float (&x)[32], uint4& ca, uint4& cb) {
   float m0 = 0.f, m1 = 0.f;
 #pragma unroll
@@ -141,7 +145,7 @@ __device__ __forceinline__ float quantize32(const float (&x)[32], uint4& ca, uin
   }
   float amax = fmaxf(m0, m1);
 #pragma unroll
-  for (int o = LPV / 2; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  for (int o = 16; o >= VPW; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float scale = div127(amax);  // amax / 127, correctly rounded
   uint32_t q[32];
   if (amax > 0.f) {
@@ -376,14 +380,15 @@ __global__ void __launch_bounds__(kProdThreads, 1) kv_quant_write_kernel(Produce
   }
 
   // --------------------------------------------------------------- compute warps
-  const int c = lane % LPV, vi = lane / LPV;
+  const int c = lane / VPW, vi = lane % VPW;  // place in the vector, token of the pass
   const int hr = rd / 32;  // rotary runs per half
   const int ra = c < hr ? c : 2 * hr + 2 * (c - hr);
   const int rb = c < hr ? c + hr : ra + 1;
   const bool k_copy = kFused && p.k_out != nullptr;
   const float* s_w = reinterpret_cast<const float*>(dsm + g.off_w);
   const float* s_sm = reinterpret_cast<const float*>(dsm + g.off_sm);
-  float* nscr = reinterpret_cast<float*>(dsm + g.off_nscr) + warp * VPW * R;
+  constexpr int NS = R + 4;  // run sums per vector, padded (bank spread)
+  float* nscr = reinterpret_cast<float*>(dsm + g.off_nscr) + warp * VPW * NS;
   const int G = p.q ? p.Hq / p.Hkv : 1;
 
   // Per unit: its tile n and place k, its slot s and the slot's use, and the
@@ -455,13 +460,13 @@ __global__ void __launch_bounds__(kProdThreads, 1) kv_quant_write_kernel(Produce
       if constexpr (kFused) {
         if (kind != 1) {
           if (norm) {
-            nscr[vi * R + ra] = sum_sq16(x);
-            nscr[vi * R + rb] = sum_sq16(x + 16);
+            nscr[vi * NS + ra] = sum_sq16(x);
+            nscr[vi * NS + rb] = sum_sq16(x + 16);
             __syncwarp();
             float rs[R];
 #pragma unroll
             for (int j = 0; j < R / 4; ++j) {
-              const float4 f = *reinterpret_cast<const float4*>(nscr + vi * R + 4 * j);
+              const float4 f = *reinterpret_cast<const float4*>(nscr + vi * NS + 4 * j);
               rs[4 * j] = f.x;
               rs[4 * j + 1] = f.y;
               rs[4 * j + 2] = f.z;
@@ -533,7 +538,7 @@ __global__ void __launch_bounds__(kProdThreads, 1) kv_quant_write_kernel(Produce
         }
       }
       uint4 ca, cb;
-      const float scale = quantize32<LPV>(x, ca, cb);
+      const float scale = quantize32<VPW>(x, ca, cb);
       if (v_block) {
         // codes over the head's own bf16 rows, once every lane has read its values
         __syncwarp();
@@ -655,7 +660,7 @@ ProdGeo producer_geo(const ProducerParams& p, bool fused) {
   const int vpw = 32 / (D / 32), runs = D / 16;
   int off = 0;
   g.off_nscr = off;
-  off += fused ? kNCW * vpw * runs * 4 : 0;
+  off += fused ? kNCW * vpw * (runs + 4) * 4 : 0;
   g.off_meta = off;
   off += kTR * (int)sizeof(TileMeta);
   g.off_cs = off;
