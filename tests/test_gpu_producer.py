@@ -60,6 +60,25 @@ def test_producer_scattered_slots_bit_exact(D, Hkv, Hq, T):
     _assert_same(gc, ref, ["k_cache", "v_cache", "k_scale", "v_scale", "q_i8", "q_scale"])
 
 
+@pytest.mark.parametrize("D,Hkv,Hq,T", [(128, 3, 7, 200), (256, 6, 18, 333), (128, 5, 10, 1000), (256, 8, 64, 520),
+                                       (128, 1, 2, 5000)])
+def test_producer_uneven_head_groups_bit_exact(D, Hkv, Hq, T):
+    # The producer's work units hold up to 1024 / D heads of one tensor: head
+    # counts that do not fill them (3, 5, 6 KV heads; 7 query heads, not a
+    # multiple of the KV heads) give units of different sizes, warps without a
+    # task in some units, and -- with thousands of tokens -- several tiles per
+    # CTA.  One sequence's block-aligned slots (the transposed V path), the tail
+    # ragged.
+    rng = np.random.default_rng(T + Hkv)
+    tables, NB = wl.paged_tables([T], perm_seed=T)
+    slots = wl.slot_mapping(tables[0], np.arange(T))
+    k = wl.randn_bf16(rng, (T, Hkv, D))
+    v = wl.randn_bf16(rng, (T, Hkv, D))
+    q = wl.randn_bf16(rng, (T, Hq, D))
+    gc, ref = _run(k, v, slots, NB, q=q)
+    _assert_same(gc, ref, ["k_cache", "v_cache", "k_scale", "v_scale", "q_i8", "q_scale"])
+
+
 def test_producer_mixed_aligned_and_partial_tiles():
     # positions 5 .. 5+70 of one sequence: no tile starts on a block boundary
     D, Hkv = 256, 4

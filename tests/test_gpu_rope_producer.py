@@ -94,6 +94,24 @@ def test_rope_producer_scattered_bit_exact(D, rd, norm):
     _assert_same(gc, ref, ALL)
 
 
+@pytest.mark.parametrize("D,rd,Hkv,Hq,T", [(256, 192, 6, 18, 150), (128, 96, 3, 9, 400)])
+def test_rope_producer_uneven_heads_partial_rotation_bit_exact(D, rd, Hkv, Hq, T):
+    # Partial rotations whose rotary runs do not fill the lanes of a vector (the
+    # lanes past them hold the unrotated tail) with head counts that leave
+    # warps without a task in some units; block-aligned slots, both norms
+    rng = np.random.default_rng(rd + Hkv)
+    tables, NB = wl.paged_tables([T], perm_seed=rd)
+    slots = wl.slot_mapping(tables[0], np.arange(T))
+    k = wl.randn_bf16(rng, (T, Hkv, D))
+    v = wl.randn_bf16(rng, (T, Hkv, D))
+    q = wl.randn_bf16(rng, (T, Hq, D))
+    pos = np.arange(T, dtype=np.int32)
+    gc, ref = _run(k, v, slots, NB, positions=pos, cos_sin=wl.rope_cos_sin(T, rd), rotary_dim=rd, q=q,
+                   q_norm_weight=wl.norm_weight_bf16(rng, D), k_norm_weight=wl.norm_weight_bf16(rng, D),
+                   q_out=True, k_out=True)
+    _assert_same(gc, ref, ALL)
+
+
 def test_rope_producer_aligned_tiles_without_query():
     # one sequence, positions 32 .. 32+96: every tile fills one block; no query
     D, Hkv, rd = 256, 2, 256
