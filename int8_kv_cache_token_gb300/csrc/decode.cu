@@ -229,10 +229,18 @@ __device__ __forceinline__ int cta_of(long long u, long long U, int N) {
 struct Ring {
   int kK, nV;
   // A stream releases its K slot right after its QK MMAs, long before its unit
-  // is done, so one K slot per stream (two at 12 slots) keeps it fed; the rest
-  // of the ring holds V items, which wait for the QK warps' handoff.
+  // is done.  With two streams their units alternate, so one K slot each (two
+  // at 12 slots) keeps them fed: one stream's next K lands while the other
+  // computes.  A single stream (head_dim 128) gets two K slots, so its own next
+  // unit's K is in flight while it computes the current one (config 4's batch
+  // decode: 245 -> 224 us; at head_dim 256 the V side cannot spare the slots).
+  // The rest of the ring holds V items, which wait for the QK warps' handoff.
+  __host__ __device__ static int k_slots(int nslots, int streams) {
+    const int k = nslots / 6 > 0 ? nslots / 6 : 1;
+    return streams == 1 && k < 2 ? 2 : k;
+  }
   __host__ __device__ Ring(int nslots, int streams)
-      : kK(nslots / 6 > 0 ? nslots / 6 : 1), nV(nslots - streams * (nslots / 6 > 0 ? nslots / 6 : 1)) {}
+      : kK(k_slots(nslots, streams)), nV(nslots - streams * k_slots(nslots, streams)) {}
 };
 
 // A position in a ring of n slots: the slot, and how many times the ring was

@@ -34,8 +34,15 @@ class Bar:
         return (self.n & 1) != (phase & 1)
 
 
+def k_slots(nslots, streams):
+    """K slots per stream (Ring::k_slots): nslots // 6, at least one; a single
+    stream gets at least two, so its next unit's K is in flight meanwhile."""
+    k = max(1, nslots // 6)
+    return max(k, 2) if streams == 1 else k
+
+
 def kernel_ring(nslots, streams=2):
-    kK = max(1, nslots // 6)
+    kK = k_slots(nslots, streams)
     nV = nslots - streams * kK
     return dict(kslot=lambda i: (i % streams) * kK + (i // streams) % kK, kuse=lambda i: (i // streams) // kK,
                 vslot=lambda i: streams * kK + i % nV, vuse=lambda i: i // nV)
@@ -148,7 +155,7 @@ class RingPos:
 @pytest.mark.parametrize("streams", [1, 2])
 @pytest.mark.parametrize("nslots", [4, 6, 8, 10, 12])
 def test_stepped_positions_equal_the_closed_forms(nslots, streams):
-    kK = max(1, nslots // 6)
+    kK = k_slots(nslots, streams)
     nV = nslots - streams * kK
     ring = kernel_ring(nslots, streams)
     # producer: one K position per stream, swapped after every unit (two streams); one V position
