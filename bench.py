@@ -471,9 +471,9 @@ def run_ours(args):
         if not args.quick:
             secondary.update(run_secondary(torch, i8, hbm_peak, tensor_peak, peak_kind))
             try:
-                secondary["decode_other_configs"] = run_batch_decodes(torch, i8, hbm_peak)
+                secondary["decode_other_workloads"] = run_batch_decodes(torch, i8, hbm_peak)
             except Exception as e:  # pragma: no cover - report, do not hide
-                secondary["decode_other_configs"] = {"error": str(e)[:200]}
+                secondary["decode_other_workloads"] = {"error": str(e)[:200]}
             try:
                 secondary["decode_u8_probs_by_history"] = run_u8p_comparison(torch, i8, hbm_peak)
             except Exception as e:  # pragma: no cover - report, do not hide
@@ -668,18 +668,18 @@ def run_u8p_comparison(torch, i8, hbm_peak):
 
 
 def run_batch_decodes(torch, i8, hbm_peak):
-    """The other decode configurations, timed only (their parity is in the tests):
-    single sequence at 4096 (config 0), 64 sequences with lengths uniform in
-    [1024, 32768] (config 3) and batch 16 at 32768 with 32 q / 8 KV heads, head_dim
-    128 (config 4).  Shapes, lengths and paging come from workloads.py; the K/V
-    values are drawn on the device (torch generator, seed 0) and written through
-    the producer, the query quantized by its query path.  Each cache exceeds L2
-    except config 0's, which rotates copies."""
+    """The other decode workloads, timed only (their parity is in the tests): a
+    single sequence at 4096 tokens (24 q / 4 KV heads, head_dim 256), 64 sequences
+    with lengths uniform in [1024, 32768] (same heads) and batch 16 at 32768 with
+    32 q / 8 KV heads, head_dim 128.  Shapes, lengths and paging come from
+    workloads.py; the K/V values are drawn on the device (torch generator, seed 0)
+    and written through the producer, the query quantized by its query path.
+    Each cache exceeds L2 except the 4096-token one's, which rotates copies."""
     res = {}
     gen = torch.Generator(device="cuda")
     gen.manual_seed(0)
-    for name, w in (("config0_decode_4k", wl.decode_4k()), ("config3_decode_batch64", wl.decode_batch()),
-                    ("config4_decode_gqa_b16_32k", wl.producer_gqa_decode())):
+    for name, w in (("decode_single_4096", wl.decode_4k()), ("decode_batch64_mixed_lengths", wl.decode_batch()),
+                    ("decode_gqa128_batch16_32768", wl.producer_gqa_decode())):
         try:
             cache = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
             for b in range(w.B):
@@ -953,8 +953,8 @@ def run_profile_prefix(args):
 
 def run_profile_gqa128(args):
     """Decode launches at head_dim 128 for profilers: batch 4 at 32768 with 32 q /
-    8 KV heads (config 4's shape at a quarter of its batch, 277 MB of cache, above
-    L2); device-drawn seeded values; `--warmup` then `--steps` launches."""
+    8 KV heads (the batch-16 decode's shape at a quarter of its batch, 277 MB of
+    cache, above L2); device-drawn seeded values; `--warmup` then `--steps` launches."""
     import torch
 
     from int8_kv_cache_token_gb300 import build as ibuild

@@ -232,8 +232,9 @@ struct Ring {
   // is done.  With two streams their units alternate, so one K slot each (two
   // at 12 slots) keeps them fed: one stream's next K lands while the other
   // computes.  A single stream (head_dim 128) gets two K slots, so its own next
-  // unit's K is in flight while it computes the current one (config 4's batch
-  // decode: 245 -> 224 us; at head_dim 256 the V side cannot spare the slots).
+  // unit's K is in flight while it computes the current one (batch-16 decode
+  // at 32768 tokens, 32 q / 8 KV heads: 245 -> 221 us; at head_dim 256 the V
+  // side cannot spare the slots).
   // The rest of the ring holds V items, which wait for the QK warps' handoff.
   __host__ __device__ static int k_slots(int nslots, int streams) {
     const int k = nslots / 6 > 0 ? nslots / 6 : 1;
