@@ -89,9 +89,12 @@ struct Geo {
   static constexpr int kPage = D * kBS * EB;                    // one (block, KV head) page
   static constexpr int kPages = kBlocksU * kPage;
   static constexpr int kScales = kPages;                         // INT8: float2 (sK, sV) per token (K items)
-  static constexpr int kPatch = kPages + kUnit * 8;             // decode step: the new token's codes [D]
-  static constexpr int kSlot = (kPages + (BF16 ? 0 : kUnit * 8 + D) + 127) / 128 * 128;
-  static constexpr int kQBuf = BF16 ? 0 : kRows * D + kRows * 4;  // decode step: a stream's query codes, scales
+  static constexpr int kSlot = (kPages + (BF16 ? 0 : kUnit * 8) + 127) / 128 * 128;
+  // decode step: a stream's buffer of quantized rows, the query rows then the
+  // new token's K and V (codes [kRows + 2][D], then their scales)
+  static constexpr int kQNewK = kRows, kQNewV = kRows + 1;
+  static constexpr int kQScl = (kRows + 2) * D;
+  static constexpr int kQBuf = BF16 ? 0 : kQScl + 48;
   static constexpr int kWTok = kUnit / kQW;                     // tokens per QK warp
   static constexpr int kGran = kWTok;                           // work-split granule (one QK warp's tokens)
   static constexpr int MT = kWTok / 16;                         // 16-token blocks per QK warp
@@ -99,11 +102,14 @@ struct Geo {
   static constexpr int NDT = kDimsPW / 16;                      // 16-dim MMA tiles per PV warp
   static constexpr int kFrag = 8;                               // B-fragment bytes per lane (bf16 p~ or s8 codes)
   // handoff buffer: [kQW][32 lanes] B fragments, then per row r and group q
-  // (QK warp): sW [8][kQW] | m [8][kQW] | l [8][kQW] (a row's 4 groups in 16 bytes)
+  // (QK warp): sW [8][kQW] | m [8][kQW] | l [8][kQW] (a row's 4 groups in 16
+  // bytes), then (decode step) the new token's V codes [D] for the unit holding it
   static constexpr int kHSw = kQW * 32 * kFrag;
   static constexpr int kHM = kHSw + kQW * kRows * 4;
   static constexpr int kHL = kHM + kQW * kRows * 4;
-  static constexpr int kHand = kHL + kQW * kRows * 4;
+  static constexpr int kHPatch = kHL + kQW * kRows * 4;
+  static constexpr int kHand = kHPatch + (BF16 ? 0 : D);
+  static_assert(kQBuf % 16 == 0 && kHand % 16 == 0, "buffers are read as 16-byte vectors");
   static constexpr int kStage = kRows * kWTok * EB;             // per-QK-warp code/weight transpose
   static_assert(kGroup == kWTok || BF16, "an INT8 QK warp owns exactly one probability group");
   static_assert(kSlot % 128 == 0 && kHand % 16 == 0, "alignment");
@@ -652,7 +658,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     int blk_n = wn.n > 0 ? load_blk(wn) : -1;
     int n_k = 0, n_v = 0;  // K and V items issued
     RingPos kp_cur, kp_oth, vp;  // K positions of this unit's stream and of the other; V position
-    uint32_t nt_k[D / 128], nt_v[D / 128];  // decode step: the new token's codes
     for (int i = 0; wk.n > 0; ++i) {
       if (*abort_flag) break;
       const int blk_nn = wnn.n > 0 ? load_blk(wnn) : -1;  // in flight meanwhile
@@ -677,58 +682,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       if (ok)
         bulk_g2s_hint(kdst + (size_t)lane * kPage, kc + ((size_t)blk * Hkv + wk.kvh) * kPage, kPage, &full[kslot],
                       pol);
-      // Decode step: this unit holds the pair's newest token (position L - 1).
-      // Quantize its K/V here, write them into the cache for later steps, and
-      // stage them in the slots' patch areas; the consumers patch their
-      // shared-memory copy of the page (which may predate the write).
-      const bool patched = STEP && (wk.gi + wk.n == wk.ngp);
-      const int pos = wk.L - 1 - t0;  // the new token within the unit
+      // The decode step's new token (position L - 1) is quantized and written by
+      // the QK warps; its entries read here may predate that write and are
+      // replaced in the consumers.
       if constexpr (!BF16) {
-        float sk_new = 0.f, sv_new = 0.f;
-        if (patched) {
-          const size_t ri = ((size_t)wk.b * Hkv + wk.kvh) * D;
-          const RowRaw<D> kr = load_row_warp<D>(p.k_new + ri, lane), vr = load_row_warp<D>(p.v_new + ri, lane);
-          sk_new = quant_row_warp<D>(kr, nt_k);
-          sv_new = quant_row_warp<D>(vr, nt_v);
-          const uint32_t(&kcodes)[D / 128] = nt_k;
-          const int blk_new = __shfl_sync(0xffffffffu, blk, pos / kBS), off_new = (wk.L - 1) % kBS;
-          constexpr int E = D / 32;
-          const int d0 = lane * E;
-          if (blk_new >= 0) {
-            int8_t* kg = p.k_cache_w + ((((size_t)blk_new * Hkv + wk.kvh) * (D / 16) + d0 / 16) * kBS + off_new) * 16 +
-                         d0 % 16;
-            if constexpr (E == 8)
-              *reinterpret_cast<uint2*>(kg) = make_uint2(kcodes[0], kcodes[1]);
-            else
-              *reinterpret_cast<uint32_t*>(kg) = kcodes[0];
-            int8_t* vg = p.v_cache_w + (((size_t)blk_new * Hkv + wk.kvh) * D + d0) * kBS + off_new;
-#pragma unroll
-            for (int e = 0; e < E; ++e) vg[(size_t)e * kBS] = (int8_t)((nt_v[e >> 2] >> (8 * (e & 3))) & 0xff);
-            if (lane == 0) {
-              const size_t si = ((size_t)blk_new * kBS + off_new) * Hkv + wk.kvh;
-              p.k_scale_w[si] = sk_new;
-              p.v_scale_w[si] = sv_new;
-            }
-          }
-          if constexpr (E == 8)
-            *reinterpret_cast<uint2*>(kdst + Gm::kPatch + d0) = make_uint2(kcodes[0], kcodes[1]);
-          else
-            *reinterpret_cast<uint32_t*>(kdst + Gm::kPatch + d0) = kcodes[0];
-        }
         float* sdst = reinterpret_cast<float*>(kdst + Gm::kScales);
 #pragma unroll
         for (int r = 0; r < kUnit / 32; ++r) {
           const int tok = lane + 32 * r;
           const int bj = __shfl_sync(0xffffffffu, blk, tok / kBS);  // every lane takes part in the shuffle
-          if (patched && tok == pos) {  // the new token's scales come from this warp, not the cache
-            sdst[2 * tok] = sk_new;
-            sdst[2 * tok + 1] = sv_new;
-          } else {
-            const bool v = tok < ntok && bj >= 0;
-            const size_t si = ((size_t)(v ? bj : 0) * kBS + tok % kBS) * Hkv + wk.kvh;
-            cp_async_4(sdst + 2 * tok, p.k_scale + si, v ? 4u : 0u);
-            cp_async_4(sdst + 2 * tok + 1, p.v_scale + si, v ? 4u : 0u);
-          }
+          const bool v = tok < ntok && bj >= 0;
+          const size_t si = ((size_t)(v ? bj : 0) * kBS + tok % kBS) * Hkv + wk.kvh;
+          cp_async_4(sdst + 2 * tok, p.k_scale + si, v ? 4u : 0u);
+          cp_async_4(sdst + 2 * tok + 1, p.v_scale + si, v ? 4u : 0u);
         }
         cp_async_mbar_arrive(&full[kslot]);
       }
@@ -749,16 +715,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       if (ok)
         bulk_g2s_hint(ring + (size_t)vslot * kSlot + (size_t)lane * kPage,
                       vc + ((size_t)blk * Hkv + wk.kvh) * kPage, kPage, &full[vslot], pol);
-      if constexpr (!BF16) {
-        if (patched) {
-          constexpr int E = D / 32;
-          uint8_t* vpatch = ring + (size_t)vslot * kSlot + Gm::kPatch + lane * E;
-          if constexpr (E == 8)
-            *reinterpret_cast<uint2*>(vpatch) = make_uint2(nt_v[0], nt_v[1]);
-          else
-            *reinterpret_cast<uint32_t*>(vpatch) = nt_v[0];
-        }
-      }
       mbar_arrive(&full[vslot]);
       ++n_v;
       vp.next(rg.nV);
@@ -809,6 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
     uint32_t qfb[D / 16][2];   // BF16: query fragments
     float sq[2] = {0.f, 0.f};
     RingPos kpos;  // this stream's K slots
+    uint8_t* const qb = smem + lay.qbuf + (size_t)st * Gm::kQBuf;  // decode step: the stream's quantized rows
     for (int i = st; wk.n > 0; i += kStreams) {
       const int pair = wk.b * Hkv + wk.kvh;
       if (pair != cur_pair) {
@@ -816,36 +773,85 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         if constexpr (BF16) {
           load_q_frags_bf16<D>(static_cast<const uint16_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qfb);
         } else if constexpr (STEP) {
-          // Decode step: the stream's 4 warps quantize the pair's query rows
-          // (warp w: rows w and w + 4) by the producer's rule into the stream's
-          // buffer, then each builds its fragments from it.
-          uint8_t* qb = smem + lay.qbuf + (size_t)st * Gm::kQBuf;
-          RowRaw<D> qr[2];
+          // Decode step: the stream's warps quantize the pair's query rows (warp
+          // w: rows w and w + kQW) by the producer's rule into the stream's
+          // buffer, then each builds its fragments from it.  The stream that
+          // holds the unit with the pair's newest token (position L - 1) also
+          // quantizes that token's K (warp kQW - 2) and V (warp kQW - 1) here,
+          // writes them into the cache for later steps and keeps them in the
+          // buffer: the unit's consumers patch their copies of the cache, which
+          // may predate the write.  Units of a pair follow one another every kQW
+          // granules, alternating between the streams.
+          const long long g_last = wk.gc - wk.gi + wk.ngp - 1;  // the pair's last granule
+          const bool own_new = g_last < g_end && ((wk.ngp - 1 - wk.gi) / kQW) % kStreams == 0;
+          const int nrow = qw - (kQW - 2);  // 0: the new K row, 1: the new V row
+          const bool new_row = own_new && nrow >= 0;
+          RowRaw<D> qr[2], nr;
+          int blk_new = -1;
+          if (new_row) {
+            nr = load_row_warp<D>((nrow == 0 ? p.k_new : p.v_new) + ((size_t)wk.b * Hkv + wk.kvh) * D, lane);
+            blk_new = p.block_tables[(size_t)wk.b * p.max_blocks + (wk.L - 1) / kBS];
+          }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int r = qw + kQW * h;
             if (r < G) qr[h] = load_row_warp<D>(p.q_bf16 + ((size_t)wk.b * Hq + wk.kvh * G + r) * D, lane);
           }
+          constexpr int E = D / 32;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const int r = qw + kQW * h;
             if (r < G) {
               uint32_t codes[D / 128];
               const float sc = quant_row_warp<D>(qr[h], codes);
-              constexpr int E = D / 32;
               if constexpr (E == 8)
                 *reinterpret_cast<uint2*>(qb + r * D + lane * E) = make_uint2(codes[0], codes[1]);
               else
                 *reinterpret_cast<uint32_t*>(qb + r * D + lane * E) = codes[0];
-              if (lane == 0) reinterpret_cast<float*>(qb + kRows * D)[r] = sc;
+              if (lane == 0) reinterpret_cast<float*>(qb + Gm::kQScl)[r] = sc;
             }
           }
-          named_bar_sync(1 + st, kQW * 32);  // the rows are in the buffer
+          uint32_t ncodes[D / 128];
+          float nsc = 0.f;
+          if (new_row) nsc = quant_row_warp<D>(nr, ncodes);
+          // the query rows are in the buffer; the previous pair's new-token rows
+          // were read by every warp of the stream
+          named_bar_sync(1 + st, kQW * 32);
+          if (new_row) {
+            const int r = Gm::kQNewK + nrow;
+            if constexpr (E == 8)
+              *reinterpret_cast<uint2*>(qb + r * D + lane * E) = make_uint2(ncodes[0], ncodes[1]);
+            else
+              *reinterpret_cast<uint32_t*>(qb + r * D + lane * E) = ncodes[0];
+            if (lane == 0) reinterpret_cast<float*>(qb + Gm::kQScl)[r] = nsc;
+            // the cache entry (an invalid block is reported by the producer warp)
+            if (blk_new >= 0 && blk_new < p.num_blocks) {
+              const int off_new = (wk.L - 1) % kBS, d0 = lane * E;
+              if (nrow == 0) {
+                int8_t* kg = p.k_cache_w +
+                             ((((size_t)blk_new * Hkv + wk.kvh) * (D / 16) + d0 / 16) * kBS + off_new) * 16 + d0 % 16;
+                if constexpr (E == 8)
+                  *reinterpret_cast<uint2*>(kg) = make_uint2(ncodes[0], ncodes[1]);
+                else
+                  *reinterpret_cast<uint32_t*>(kg) = ncodes[0];
+              } else {
+                int8_t* vg = p.v_cache_w + (((size_t)blk_new * Hkv + wk.kvh) * D + d0) * kBS + off_new;
+#pragma unroll
+                for (int e = 0; e < E; ++e) vg[(size_t)e * kBS] = (int8_t)((ncodes[e >> 2] >> (8 * (e & 3))) & 0xff);
+              }
+              if (lane == 0) {
+                const size_t si = ((size_t)blk_new * kBS + off_new) * Hkv + wk.kvh;
+                (nrow == 0 ? p.k_scale_w : p.v_scale_w)[si] = nsc;
+              }
+            }
+          }
           load_q_frags_smem<D>(qb, G, lane, qf);
-          const float* qsc = reinterpret_cast<const float*>(qb + kRows * D);
+          const float* qsc = reinterpret_cast<const float*>(qb + Gm::kQScl);
           sq[0] = 2 * t < G ? qsc[2 * t] : 0.f;
           sq[1] = 2 * t + 1 < G ? qsc[2 * t + 1] : 0.f;
-          named_bar_sync(1 + st, kQW * 32);  // every warp has read it before it is reused
+          // every warp has read the query rows before they are reused; the
+          // new-token rows are in the buffer
+          named_bar_sync(1 + st, kQW * 32);
         } else {
           load_q_frags<D>(static_cast<const int8_t*>(p.q), wk.b, Hq, wk.kvh, G, lane, qf);
 #pragma unroll
@@ -857,6 +863,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       }
       const int ntok = min(wk.n * kGran, wk.L - wk.gi * kGran);
       const bool active = qw < wk.n;  // every granule of the unit holds tokens
+      // decode step: the new token's position in the unit, and whether it is in this warp's granule
+      const int pos_new = wk.L - 1 - wk.gi * kGran;
+      const bool new_here = STEP && wk.gi + wk.n == wk.ngp && pos_new / kGran == qw;
 
       // ---- K item: QK of this warp's tokens, and their scales ----
       const int kslot = st * rg.kK + kpos.s;
@@ -865,12 +874,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       const uint8_t* kb = ring + (size_t)kslot * kSlot;
       if constexpr (!BF16) {
         // decode step: the warp whose granule holds the new token patches its K row
-        const int pos = wk.L - 1 - wk.gi * kGran;
-        if (STEP && wk.gi + wk.n == wk.ngp && pos / kGran == qw) {
+        if (new_here) {
           if (lane < D / 16) {
-            uint8_t* page = ring + (size_t)kslot * kSlot + (size_t)(pos / kBS) * kPage;
-            *reinterpret_cast<uint4*>(page + (size_t)lane * (kBS * 16) + (pos % kBS) * 16) =
-                *reinterpret_cast<const uint4*>(kb + Gm::kPatch + lane * 16);
+            uint8_t* page = ring + (size_t)kslot * kSlot + (size_t)(pos_new / kBS) * kPage;
+            *reinterpret_cast<uint4*>(page + (size_t)lane * (kBS * 16) + (pos_new % kBS) * 16) =
+                *reinterpret_cast<const uint4*>(qb + Gm::kQNewK * D + lane * 16);
           }
           __syncwarp();
         }
@@ -897,6 +905,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
             sk[2 * m + h] = v.x;
             sv[2 * m + h] = v.y;
           }
+        if (new_here) {  // decode step: the new token's scales, from the stream's buffer
+          const float* nsc = reinterpret_cast<const float*>(qb + Gm::kQScl);
+#pragma unroll
+          for (int m = 0; m < 2; ++m)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              if (tok0 + 16 * m + g + 8 * h == pos_new) {
+                sk[2 * m + h] = nsc[Gm::kQNewK];
+                sv[2 * m + h] = nsc[Gm::kQNewV];
+              }
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[kslot]);
@@ -979,6 +998,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       const int hbi = i % kHandBufs;
       if (i >= kHandBufs) pipe_wait(&hempty[hbi], ((i / kHandBufs) - 1) & 1, abort_flag);
       uint8_t* hb = hand + (size_t)hbi * Gm::kHand;
+      if (new_here) {  // decode step: the new token's V codes, for the PV warps' patch
+        constexpr int E = D / 32;
+        if constexpr (E == 8)
+          *reinterpret_cast<uint2*>(hb + Gm::kHPatch + lane * E) =
+              *reinterpret_cast<const uint2*>(qb + Gm::kQNewV * D + lane * E);
+        else
+          *reinterpret_cast<uint32_t*>(hb + Gm::kHPatch + lane * E) =
+              *reinterpret_cast<const uint32_t*>(qb + Gm::kQNewV * D + lane * E);
+      }
       if constexpr (BF16) {
         uint2 f;
         f.x = *reinterpret_cast<const uint32_t*>(stg + g * 32 + 4 * t);
@@ -1099,7 +1127,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
         if (lane < Gm::kDimsPW) {
           const int d = pv_w * Gm::kDimsPW + lane;
           uint8_t* vp = ring + (size_t)vslot * kSlot;
-          vp[(size_t)(pos / kBS) * kPage + (size_t)d * kBS + pos % kBS] = vp[Gm::kPatch + d];
+          vp[(size_t)(pos / kBS) * kPage + (size_t)d * kBS + pos % kBS] = hb[Gm::kHPatch + d];
         }
         __syncwarp();
       }

@@ -175,3 +175,48 @@ def test_stepped_positions_equal_the_closed_forms(nslots, streams):
         qk[st].next(kK)
         assert (streams * kK + pv.s, pv.use) == (ring["vslot"](i), ring["vuse"](i))
         pv.next(nV)
+
+
+def cta_units(ngps, g0, g1, qw):
+    """The units of one CTA (granules [g0, g1) of the (sequence, KV head) pairs
+    laid end to end): (pair, first granule in the pair, granules)."""
+    units, base = [], 0
+    for pair, ngp in enumerate(ngps):
+        gi = max(g0 - base, 0)
+        while gi < ngp and base + gi < g1:
+            n = min(qw, ngp - gi, g1 - base - gi)
+            units.append((pair, gi, n))
+            gi += n
+        base += ngp
+    return units
+
+
+@pytest.mark.parametrize("streams,qw", [(1, 8), (2, 4)])
+def test_decode_step_new_token_has_one_owner(streams, qw):
+    """Decode step: the stream holding the unit with a pair's newest token
+    quantizes that token at its first unit of the pair, judged from that unit
+    alone (the pair's last granule inside the CTA's range, and the units from
+    there to it, kQW granules each, a multiple of the stream count).  Exactly
+    one (CTA, stream) claims each pair, and it is the one that processes the
+    unit holding the token."""
+    rnd = random.Random(7)
+    for _ in range(300):
+        ngps = [rnd.choice([0, 1, 2, 3, 5, 8, 9, 17, 33, 128]) for _ in range(rnd.randint(1, 12))]
+        U, N = sum(ngps), rnd.randint(1, 40)
+        claims, holders = {}, {}
+        for c in range(N):
+            g0, g1 = U * c // N, U * (c + 1) // N
+            seen = [None] * streams
+            base = {p: sum(ngps[:p]) for p in range(len(ngps))}
+            for i, (pair, gi, n) in enumerate(cta_units(ngps, g0, g1, qw)):
+                st = i % streams
+                if gi + n == ngps[pair]:
+                    holders.setdefault(pair, []).append((c, st))
+                if seen[st] != pair:  # the stream's pair start
+                    seen[st] = pair
+                    g_last = base[pair] + ngps[pair] - 1
+                    if g_last < g1 and ((ngps[pair] - 1 - gi) // qw) % streams == 0:
+                        claims.setdefault(pair, []).append((c, st))
+        for pair, ngp in enumerate(ngps):
+            if ngp:
+                assert len(holders[pair]) == 1 and claims.get(pair) == holders[pair], (ngps, N, pair)
