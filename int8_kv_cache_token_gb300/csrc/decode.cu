@@ -33,8 +33,8 @@
 //    row sums l_g.  No QK warp waits for another: the group quantization gives
 //    the same codes for W scaled by any positive factor, so each group is
 //    quantized against its own maximum and brought to the common one afterwards.
-//  * 8 PV warps: warp v owns head-dims [D/8 v, D/8 (v+1)) of the output and
-//    keeps the pair's running maximum m.  Per unit, m_new = max(m, m_g), the
+//  * PV warps (8 at head_dim 256, 4 at head_dim 128): warp v owns head-dims
+//    [32 v, 32 (v+1)) of the output and keeps the pair's running maximum m.  Per unit, m_new = max(m, m_g), the
 //    accumulator and l are rescaled once by 2^(m - m_new), and group g adds
 //    2^(m_g - m_new) sW_g (Wq x Vq) (mma.sync m16n8k32 s8, exact int32, K = the
 //    group's 32 tokens; s8 x u8 for UINT8 probability codes) and
@@ -63,10 +63,7 @@ constexpr int kPart = 256;   // the pages' decode partition (debug QK tiles)
 constexpr int kBS = 16;      // block size
 constexpr int kGroup = 32;   // probability group
 constexpr int kQKWarps = 8;  // QK / softmax warps, in kStreams streams of kQW (per variant, below)
-constexpr int kPW = 8;       // PV warps
-constexpr int kPVWarp0 = kQKWarps;
-constexpr int kProdWarp = kPVWarp0 + kPW;
-constexpr int kThreads = (kProdWarp + 1) * 32;
+constexpr int kPVWarp0 = kQKWarps;  // then the PV warps (kPW per variant), then the producer warp
 constexpr int kHandBufs = 4;  // handoff buffers, unit i uses buffer i % 4
 constexpr int kRows = 8;     // query rows in the MMA N dimension
 __host__ __device__ constexpr int kSlotFloats(int D) { return kRows * D + 2 * kRows; }
@@ -78,10 +75,15 @@ __host__ __device__ constexpr int kSlotFloats(int D) { return kRows * D + 2 * kR
 // At D = 256 two streams of 4 warps: 128-token INT8 units of 66 KB of K and V.
 // At D = 128 one stream of 8 warps: 256-token units, the same bytes per ring
 // item, so the per-unit work (copies, handoff, rescale) is spread over as many
-// bytes as at D = 256.
+// bytes as at D = 256.  PV warps: 8 of 32 head-dims at D = 256; 4 of 32 at
+// D = 128, where 8 warps of 16 dims spent more issue slots on each unit's
+// group factors (every PV warp computes them for all rows) than on their MMAs.
 template <int D, bool BF16>
 struct Geo {
   static constexpr int kStreams = D == 128 ? 1 : 2;             // QK streams
+  static constexpr int kPW = D == 128 ? 4 : 8;                  // PV warps
+  static constexpr int kProdWarp = kPVWarp0 + kPW;              // the producer warp
+  static constexpr int kThreads = (kProdWarp + 1) * 32;
   static constexpr int kQW = kQKWarps / kStreams;               // QK warps per stream = granules per unit
   static constexpr int EB = BF16 ? 2 : 1;                       // bytes per cache element
   static constexpr int kUnit = kQW * (BF16 ? 16 : 32);          // tokens per unit
@@ -438,7 +440,7 @@ __device__ __forceinline__ void load_q_frags_smem(const uint8_t* qa, int G, int 
 // still exact in fp32); the pages' notes on PV weigh this variant and leave it
 // for want of a mixed-sign MMA, which sm_103a's mma.sync has.
 template <int D, bool BF16, bool STEP = false, bool U8P = false>
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int nslots) {
+__global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(DecodeParams p, int nslots) {
   static_assert(!(STEP && BF16), "the decode step is INT8 only");
   constexpr int kQW = Geo<D, BF16>::kQW, kStreams = Geo<D, BF16>::kStreams;
   static_assert(!(U8P && (BF16 || STEP)), "UINT8 probabilities: plain INT8 decode only");
@@ -446,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
   constexpr int kUnit = Gm::kUnit, kBlocksU = Gm::kBlocksU, kPage = Gm::kPage, kSlot = Gm::kSlot;
   constexpr int kGran = Gm::kGran;
   constexpr int kWTok = Gm::kWTok, MT = Gm::MT, NDT = Gm::NDT;
+  constexpr int kPW = Gm::kPW, kProdWarp = Gm::kProdWarp;
   extern __shared__ __align__(1024) uint8_t smem[];
   const SmemLayout lay = decode_layout<D, BF16>(nslots);
   uint8_t* ring = smem + lay.ring;
@@ -1124,8 +1127,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(DecodeParams p, int
       // decode step: every PV warp patches its own head-dims of the new token's V column
       if (STEP && wk.gi + wk.n == wk.ngp) {
         const int pos = wk.L - 1 - wk.gi * kGran;
-        if (lane < Gm::kDimsPW) {
-          const int d = pv_w * Gm::kDimsPW + lane;
+        for (int dd = lane; dd < Gm::kDimsPW; dd += 32) {
+          const int d = pv_w * Gm::kDimsPW + dd;
           uint8_t* vp = ring + (size_t)vslot * kSlot;
           vp[(size_t)(pos / kBS) * kPage + (size_t)d * kBS + pos % kBS] = hb[Gm::kHPatch + d];
         }
@@ -1450,7 +1453,8 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
-  cudaError_t e = launch_pdl(decode_kernel<D, BF16, STEP, U8P>, dim3(p.grid), dim3(kThreads), smem, stream, p, ns);
+  cudaError_t e =
+      launch_pdl(decode_kernel<D, BF16, STEP, U8P>, dim3(p.grid), dim3(Geo<D, BF16>::kThreads), smem, stream, p, ns);
   if (e != cudaSuccess) return e;
   return launch_pdl(decode_merge_kernel<D, BF16>, dim3(p.B * p.Hkv * p.G), dim3(kMergeThreads), 0, stream, p);
 }
