@@ -535,9 +535,6 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
     if (lane == 0) {
       ctrl[0] = (int)(ue - ub);
       ctrl[8] = 0;
-      ctrl[10] = Nw;
-      ctrl[6] = (int)(U & 0x7fffffff);
-      ctrl[7] = (int)(U >> 31);
     }
     if (ue > ub) {
       long long run = 0;
@@ -632,8 +629,6 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
     if (warp == kProdWarp) check_inputs();
     return;
   }
-  const long long U = (long long)ctrl[6] | ((long long)ctrl[7] << 31);
-  const int Nw = ctrl[10];
   const int g = lane >> 2, t = lane & 3;
   const Ring rg(nslots, Gm::kStreams);
 
@@ -1182,10 +1177,12 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
 
     // ---- end of this CTA's share of the (sequence, KV head) pair ----
     if (seg_end) {
+      // The pair lies in this CTA's granule range [w0.gc, g_end) alone: the
+      // merge kernel's test (first and last granule in one CTA), without its
+      // divisions.
       const long long Up = wk.gb + (long long)wk.kvh * wk.ngp;  // the pair's first granule
-      const int cf = cta_of(Up, U, Nw), cl = cta_of(Up + wk.ngp - 1, U, Nw);
       const int d0 = pv_w * Gm::kDimsPW;
-      if (cf == cl) {
+      if (Up >= w0.gc && Up + wk.ngp - 1 < g_end) {
         const size_t dst = ((size_t)wk.b * Hq + wk.kvh * G) * D;
         const float inv0 = 1.0f / lrun[0], inv1 = 1.0f / lrun[1];
 #pragma unroll
