@@ -466,6 +466,9 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
   const int N = gridDim.x, c = blockIdx.x;
   const int maxL = p.max_blocks * kBS;
 
+  // The producer warp's first 32 sequence lengths (see the split below) are in
+  // flight while lane 0 initializes the barriers.
+  const int raw0 = (warp == kProdWarp && lane < B) ? __ldcg(p.seq_lens + lane) : 0;
   if (warp == kProdWarp && lane == 0) {
     const Ring rg(nslots, Gm::kStreams);
     for (int s = 0; s < nslots; ++s) {
@@ -512,7 +515,7 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
       const int b = b0 + lane;
       int u = 0, L = 0;
       if (b < B) {
-        const int raw = __ldcg(p.seq_lens + b);
+        const int raw = ck == 0 ? raw0 : __ldcg(p.seq_lens + b);
         lhash = len_hash(lhash, raw);
         L = clamp_len(raw, maxL);
         u = (L + kGran - 1) / kGran * Hkv;
@@ -1228,11 +1231,13 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
 //
 // Which CTAs hold the pair's partials follows from the attention kernel's work
 // split, so warp 0 recomputes it from seq_lens (the same arithmetic) before the
-// grid-dependency wait, while the attention kernel still runs; after the wait
-// the partials' loads go out at once.
+// grid-dependency wait, while the attention kernel still runs.  A CTA whose pair
+// has no partials exits there without waiting (in batched decode most do); for
+// the others the partials' loads go out at once after the wait.
 constexpr int kMaxSeg = 1024;
 constexpr int kMergeThreads = 512;
 constexpr int kMB = 8;
+constexpr int kMergeSpreadSmem = 120 * 1024;  // more than half an SM's shared memory
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
@@ -1279,10 +1284,12 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
     }
   }
   __syncthreads();
+  const int cf = s_seg[0], cl = s_seg[1], nseg = cl - cf + 1;
+  // No partials (the attention kernel wrote the rows, or the sequence is
+  // empty): nothing of the attention kernel's is read, so no wait for it.
+  if (cf == cl) return;
   griddep_wait();
   griddep_launch_dependents();
-  const int cf = s_seg[0], cl = s_seg[1], nseg = cl - cf + 1;
-  if (cf == cl) return;  // no partials: the attention kernel wrote the rows (or the sequence is empty)
   if (nseg > kMaxSeg) {
     record_error(2);
     return;
@@ -1448,12 +1455,20 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, BF16, STEP, U8P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          max_smem_optin(dev));
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_merge_kernel<D, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMergeSpreadSmem);
+    if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = 1;
   }
   cudaError_t e =
       launch_pdl(decode_kernel<D, BF16, STEP, U8P>, dim3(p.grid), dim3(Geo<D, BF16>::kThreads), smem, stream, p, ns);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_merge_kernel<D, BF16>, dim3(p.B * p.Hkv * p.G), dim3(kMergeThreads), 0, stream, p);
+  // A merge grid that fits on the SMs (a few long sequences) gets one CTA per
+  // SM, through an unused shared-memory request that two merge CTAs cannot
+  // share: packed two to an SM, single-sequence calls took 0.4 us longer.
+  // Larger grids (batched decode, where most CTAs exit at once) keep two per SM.
+  const int mgrid = p.B * p.Hkv * p.G;
+  return launch_pdl(decode_merge_kernel<D, BF16>, dim3(mgrid), dim3(kMergeThreads),
+                    mgrid <= num_sms(dev) ? (size_t)kMergeSpreadSmem : 0, stream, p);
 }
 
 }  // namespace
