@@ -1239,6 +1239,40 @@ constexpr int kMergeThreads = 512;
 constexpr int kMB = 8;
 constexpr int kMergeSpreadSmem = 120 * 1024;  // more than half an SM's shared memory
 
+// The first and last attention CTA of a (sequence, KV head) pair, from the
+// attention kernel's work split recomputed from seq_lens by one warp (the same
+// arithmetic; every lane gets the result); (-1, -1) for an empty sequence, which
+// has zero rows and no partials.
+template <int kGran>
+__device__ __forceinline__ int2 pair_ctas(const DecodeParams& p, int pair, int lane) {
+  const int Hkv = p.Hkv, maxL = p.max_blocks * kBS;
+  const int bp = pair / Hkv, kvh = pair % Hkv;
+  long long total = 0, before = 0;  // granules of all sequences; of the sequences before bp
+  int Lp = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int b = b0 + lane;
+    int u = 0, L = 0;
+    if (b < p.B) {
+      L = clamp_len(__ldcg(p.seq_lens + b), maxL);
+      u = (L + kGran - 1) / kGran * Hkv;
+    }
+    int su = u, sb = b < bp ? u : 0, lp = b == bp ? L : 0;
+    for (int o = 16; o >= 1; o >>= 1) {
+      su += __shfl_xor_sync(0xffffffffu, su, o);
+      sb += __shfl_xor_sync(0xffffffffu, sb, o);
+      lp += __shfl_xor_sync(0xffffffffu, lp, o);
+    }
+    total += su;
+    before += sb;
+    Lp += lp;
+  }
+  const int ngp = (Lp + kGran - 1) / kGran;
+  if (ngp == 0) return make_int2(-1, -1);
+  const long long U = total, Up = before + (long long)kvh * ngp;
+  const int Nw = (int)(U < p.grid ? U : p.grid);
+  return make_int2(cta_of(Up, U, Nw), cta_of(Up + ngp - 1, U, Nw));
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
   constexpr int COLS = D / 4, SL = kMergeThreads / COLS;
@@ -1249,38 +1283,10 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
   const int tid = threadIdx.x;
   const int pair = blockIdx.x / p.G, row = blockIdx.x % p.G;
   if (tid < 32) {
-    const int lane = tid, Hkv = p.Hkv, maxL = p.max_blocks * kBS;
-    const int bp = pair / Hkv, kvh = pair % Hkv;
-    long long total = 0, before = 0;  // granules of all sequences; of the sequences before bp
-    int Lp = 0;
-    for (int b0 = 0; b0 < p.B; b0 += 32) {
-      const int b = b0 + lane;
-      int u = 0, L = 0;
-      if (b < p.B) {
-        L = clamp_len(__ldcg(p.seq_lens + b), maxL);
-        u = (L + kGran - 1) / kGran * Hkv;
-      }
-      int su = u, sb = b < bp ? u : 0, lp = b == bp ? L : 0;
-      for (int o = 16; o >= 1; o >>= 1) {
-        su += __shfl_xor_sync(0xffffffffu, su, o);
-        sb += __shfl_xor_sync(0xffffffffu, sb, o);
-        lp += __shfl_xor_sync(0xffffffffu, lp, o);
-      }
-      total += su;
-      before += sb;
-      Lp += lp;
-    }
-    if (lane == 0) {
-      const int ngp = (Lp + kGran - 1) / kGran;
-      int cf = -1, cl = -1;
-      if (ngp > 0) {  // an empty sequence has zero rows and no partials
-        const long long U = total, Up = before + (long long)kvh * ngp;
-        const int Nw = (int)(U < p.grid ? U : p.grid);
-        cf = cta_of(Up, U, Nw);
-        cl = cta_of(Up + ngp - 1, U, Nw);
-      }
-      s_seg[0] = cf;
-      s_seg[1] = cl;
+    const int2 cs = pair_ctas<kGran>(p, pair, tid);
+    if (tid == 0) {
+      s_seg[0] = cs.x;
+      s_seg[1] = cs.y;
     }
   }
   __syncthreads();
@@ -1362,6 +1368,81 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
     store_out4(p.out, p.out_bf16, ((size_t)b * p.Hq + kvh * p.G + row) * D + 4 * tid,
                make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv));
   }
+}
+
+// Batched decode: one warp per (pair, query row), kMergeWarpItems per CTA.
+// With many pairs a pair spans few CTAs, so one warp folds its partials --
+// lane l holds head-dims [l D/32, (l+1) D/32) -- in batches of kWB segments
+// (value, m, l) whose loads are in flight together, with no block-level
+// reduction.  The host takes this kernel when B * Hkv >= #SM / 4.
+constexpr int kMergeWarpItems = 8;
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kMergeWarpItems * 32) decode_merge_warp_kernel(DecodeParams p) {
+  constexpr int kGran = Geo<D, BF16>::kGran, E = D / 32, kWB = 4;
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x * kMergeWarpItems + (threadIdx.x >> 5);
+  if (item >= p.B * p.Hkv * p.G) return;
+  const int pair = item / p.G, row = item % p.G;
+  const int2 cs = pair_ctas<kGran>(p, pair, lane);
+  if (cs.x == cs.y) return;  // no partials: nothing of the attention kernel's is read
+  const int nseg = cs.y - cs.x + 1;
+  const size_t obase = ((size_t)(pair / p.Hkv) * p.Hq + (pair % p.Hkv) * p.G + row) * D + lane * E;
+  griddep_wait();
+  griddep_launch_dependents();
+  if (nseg > kMaxSeg) {
+    if (lane == 0) record_error(2);
+    return;
+  }
+  const float* part0 = p.ws_part + (size_t)(pair + cs.x) * kSlotFloats(D);
+  float m = -INFINITY, den = 0.f, a[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) a[e] = 0.f;
+  for (int s0 = 0; s0 < nseg; s0 += kWB) {
+    float ms[kWB], ls[kWB];
+    float4 v[kWB][E / 4];
+#pragma unroll
+    for (int j = 0; j < kWB; ++j) {
+      const int sg = s0 + j;
+      if (sg < nseg) {
+        const float* ps = part0 + (size_t)sg * kSlotFloats(D);
+        ms[j] = ps[kRows * D + row];
+        ls[j] = ps[kRows * D + kRows + row];
+#pragma unroll
+        for (int k = 0; k < E / 4; ++k) v[j][k] = reinterpret_cast<const float4*>(ps + row * D + lane * E)[k];
+      } else {
+        ms[j] = -INFINITY;
+        ls[j] = 0.f;
+#pragma unroll
+        for (int k = 0; k < E / 4; ++k) v[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float mb = m;
+#pragma unroll
+    for (int j = 0; j < kWB; ++j) mb = fmaxf(mb, ms[j]);
+    if (mb == -INFINITY) continue;
+    const float f = ex2(m - mb);  // the partials' maxima are in log2 units
+#pragma unroll
+    for (int e = 0; e < E; ++e) a[e] *= f;
+    den *= f;
+#pragma unroll
+    for (int j = 0; j < kWB; ++j) {
+      const float w = ex2(ms[j] - mb);  // 0 for the padding entries
+      den = fmaf(ls[j], w, den);
+#pragma unroll
+      for (int k = 0; k < E / 4; ++k) {
+        a[4 * k] = fmaf(v[j][k].x, w, a[4 * k]);
+        a[4 * k + 1] = fmaf(v[j][k].y, w, a[4 * k + 1]);
+        a[4 * k + 2] = fmaf(v[j][k].z, w, a[4 * k + 2]);
+        a[4 * k + 3] = fmaf(v[j][k].w, w, a[4 * k + 3]);
+      }
+    }
+    m = mb;
+  }
+  const float inv = 1.0f / den;
+#pragma unroll
+  for (int k = 0; k < E / 4; ++k)
+    store_out4(p.out, p.out_bf16, obase + 4 * k,
+               make_float4(a[4 * k] * inv, a[4 * k + 1] * inv, a[4 * k + 2] * inv, a[4 * k + 3] * inv));
 }
 
 // Debug QK: one CTA per (sequence, KV head, 256-token partition); K pages are
@@ -1467,6 +1548,9 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   // share: packed two to an SM, single-sequence calls took 0.4 us longer.
   // Larger grids (batched decode, where most CTAs exit at once) keep two per SM.
   const int mgrid = p.B * p.Hkv * p.G;
+  if (4 * p.B * p.Hkv >= num_sms(dev))  // many pairs, each over few CTAs: one warp per row
+    return launch_pdl(decode_merge_warp_kernel<D, BF16>, dim3((mgrid + kMergeWarpItems - 1) / kMergeWarpItems),
+                      dim3(kMergeWarpItems * 32), 0, stream, p);
   return launch_pdl(decode_merge_kernel<D, BF16>, dim3(mgrid), dim3(kMergeThreads),
                     mgrid <= num_sms(dev) ? (size_t)kMergeSpreadSmem : 0, stream, p);
 }

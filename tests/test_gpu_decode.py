@@ -73,6 +73,22 @@ def test_decode_small(lens, D, Hq, Hkv):
             assert not out[b].any()
 
 
+@pytest.mark.parametrize("D,Hq,Hkv,lens", [
+    (256, 8, 1, [8000] + [50] * 39),      # 40 pairs; the long pair spans about 100 CTAs
+    (128, 16, 2, [33] * 19 + [6000]),     # 40 pairs, the long sequence last
+    (256, 24, 4, [700, 0, 9000, 5] * 3),  # 48 pairs, with empty sequences
+])
+def test_decode_many_pairs_merge(D, Hq, Hkv, lens):
+    """Calls with at least #SM / 4 (sequence, KV head) pairs take the merge with
+    one warp per query row; a long pair among short ones gives that warp a long
+    run of partials (many batches of its loads)."""
+    w = wl.DecodeWorkload("manypairs", Hq, Hkv, D, lens, seed=sum(lens) % 997 + D)
+    out, _ = _decode_parity(w)
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert not out[b].any()
+
+
 def test_decode_workspace_reuse_and_repeat():
     # The workspace's tickets reset themselves: repeated calls on one workspace give
     # identical results, each written into a NaN-filled output (no stale rows).
