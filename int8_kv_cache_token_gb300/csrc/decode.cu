@@ -1232,8 +1232,9 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
 // Which CTAs hold the pair's partials follows from the attention kernel's work
 // split, so warp 0 recomputes it from seq_lens (the same arithmetic) before the
 // grid-dependency wait, while the attention kernel still runs.  A CTA whose pair
-// has no partials exits there without waiting (in batched decode most do); for
-// the others the partials' loads go out at once after the wait.
+// has no partials exits there without waiting (in batched decode most do), but
+// for the grid's first CTA; for the others the partials' loads go out at once
+// after the wait.
 constexpr int kMaxSeg = 1024;
 constexpr int kMergeThreads = 512;
 constexpr int kMB = 8;
@@ -1292,10 +1293,13 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
   __syncthreads();
   const int cf = s_seg[0], cl = s_seg[1], nseg = cl - cf + 1;
   // No partials (the attention kernel wrote the rows, or the sequence is
-  // empty): nothing of the attention kernel's is read, so no wait for it.
-  if (cf == cl) return;
+  // empty): nothing of the attention kernel's is read, so no wait for it --
+  // except in the first CTA.  A kernel launched after this one waits for this
+  // grid only, so this grid must not end before the attention kernel does.
+  if (cf == cl && blockIdx.x != 0) return;
   griddep_wait();
   griddep_launch_dependents();
+  if (cf == cl) return;
   if (nseg > kMaxSeg) {
     record_error(2);
     return;
@@ -1384,11 +1388,15 @@ __global__ void __launch_bounds__(kMergeWarpItems * 32) decode_merge_warp_kernel
   if (item >= p.B * p.Hkv * p.G) return;
   const int pair = item / p.G, row = item % p.G;
   const int2 cs = pair_ctas<kGran>(p, pair, lane);
-  if (cs.x == cs.y) return;  // no partials: nothing of the attention kernel's is read
+  // No partials: nothing of the attention kernel's is read, so no wait for it
+  // -- except in the first item, so that this grid ends after the attention
+  // kernel (a kernel launched after this one waits for this grid only).
+  if (cs.x == cs.y && item != 0) return;
   const int nseg = cs.y - cs.x + 1;
   const size_t obase = ((size_t)(pair / p.Hkv) * p.Hq + (pair % p.Hkv) * p.G + row) * D + lane * E;
   griddep_wait();
   griddep_launch_dependents();
+  if (cs.x == cs.y) return;
   if (nseg > kMaxSeg) {
     if (lane == 0) record_error(2);
     return;

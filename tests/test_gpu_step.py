@@ -98,3 +98,68 @@ def test_step_matches_oracle_long_outlier_history():
     oq, oqs = oracle_query(w, [0])
     ref = orc.decode_attn(oq, oqs, oc, w.block_tables, w.seq_lens, w.block_size)
     assert np.abs(out2 - ref).max() <= TOL
+
+
+def test_back_to_back_steps_see_the_previous_token():
+    """Two steps enqueued back to back on many short sequences: every (sequence,
+    KV head) pair lies in one attention CTA, so no merge CTA has partials.  The
+    second step's history holds the first step's token, written by the first
+    attention kernel; the merge grid between them must still end after that
+    kernel, or the second step could read the cache before the write.  The
+    result must equal the producer writing both tokens, then one decode."""
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(3, 33, size=48)]  # one 32-token group per pair
+    w = wl.DecodeWorkload("steps2", 24, 4, 256, lens, seed=17)
+    L = w.seq_lens.astype(np.int64)
+    bt = dev(w.block_tables)
+    ws = i8.decode_workspace(w.B, w.Hq, w.Hkv, w.D, w.block_tables.shape[1])
+
+    def token(pos_of):  # the bf16 K/V and slot of position pos_of(b) of every sequence
+        k_t = np.zeros((w.B, w.Hkv, w.D), np.uint16)
+        v_t = np.zeros((w.B, w.Hkv, w.D), np.uint16)
+        sl = np.full((w.B,), -1, np.int32)
+        for b in range(w.B):
+            k, v = w.kv(b)
+            pos = pos_of(b)
+            k_t[b], v_t[b] = k[pos], v[pos]
+            sl[b] = w.slots(b, pos, pos + 1)[0]
+        return k_t, v_t, sl
+
+    first = token(lambda b: int(L[b]) - 2)
+    second = token(lambda b: int(L[b]) - 1)
+    q1 = dev(np.asarray(wl.randn_bf16(np.random.default_rng(6), (w.B, w.Hq, w.D))))
+    q2 = dev(w.q())
+    # reference: the producer writes positions 0 .. L-1, then one decode
+    c1 = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+    for b in range(w.B):
+        k, v = w.kv(b)
+        i8.kv_quant_write(dev(k[:int(L[b])]), dev(v[:int(L[b])]), dev(w.slots(b, 0, int(L[b]))), **c1)
+    q_i8 = torch.empty((w.B, w.Hq, w.D), dtype=torch.int8, device="cuda")
+    q_s = torch.empty((w.B, w.Hq), dtype=torch.float32, device="cuda")
+    dummy = torch.zeros((w.B, w.Hkv, w.D), dtype=torch.bfloat16, device="cuda")
+    i8.kv_quant_write(dummy, dummy, torch.full((w.B,), -1, dtype=torch.int32, device="cuda"), **c1, q=q2,
+                      q_i8=q_i8, q_scale=q_s)
+    out1 = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device="cuda")
+    i8.int8_paged_decode_attn(out1, q_i8, q_s, c1["k_cache"], c1["v_cache"], c1["k_scale"], c1["v_scale"], bt,
+                              dev(w.seq_lens), ws)
+    # two steps from the cache of positions 0 .. L-3, no synchronization between them
+    c2 = i8.alloc_int8_cache(w.num_blocks, w.Hkv, w.D)
+    for b in range(w.B):
+        if L[b] > 2:
+            k, v = w.kv(b)
+            i8.kv_quant_write(dev(k[:int(L[b]) - 2]), dev(v[:int(L[b]) - 2]), dev(w.slots(b, 0, int(L[b]) - 2)), **c2)
+    torch.cuda.synchronize()
+    out_a = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device="cuda")
+    out_b = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.float32, device="cuda")
+    sl_a, sl_b = dev((w.seq_lens - 1).astype(np.int32)), dev(w.seq_lens)
+    for _ in range(3):  # repeated, so that a race would have several chances to show
+        c2w = {n: t.clone() for n, t in c2.items()}
+        i8.int8_decode_step(out_a, q1, dev(first[0]), dev(first[1]), c2w["k_cache"], c2w["v_cache"],
+                            c2w["k_scale"], c2w["v_scale"], bt, sl_a, ws)
+        i8.int8_decode_step(out_b, q2, dev(second[0]), dev(second[1]), c2w["k_cache"], c2w["v_cache"],
+                            c2w["k_scale"], c2w["v_scale"], bt, sl_b, ws)
+        torch.cuda.synchronize()
+        assert i8.device_error() == 0
+        for name in ("k_cache", "v_cache", "k_scale", "v_scale"):
+            assert torch.equal(c1[name], c2w[name]), name
+        assert np.array_equal(host(out1), host(out_b))
