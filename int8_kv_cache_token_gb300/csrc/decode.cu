@@ -34,13 +34,13 @@
 //    the same codes for W scaled by any positive factor, so each group is
 //    quantized against its own maximum and brought to the common one afterwards.
 //  * PV warps (8 at head_dim 256, 4 at head_dim 128): warp v owns head-dims
-//    [32 v, 32 (v+1)) of the output and keeps the pair's running maximum m.  Per unit, m_new = max(m, m_g), the
-//    accumulator and l are rescaled once by 2^(m - m_new), and group g adds
-//    2^(m_g - m_new) sW_g (Wq x Vq) (mma.sync m16n8k32 s8, exact int32, K = the
-//    group's 32 tokens; s8 x u8 for UINT8 probability codes) and
-//    2^(m_g - m_new) l_g.  The accumulator covers disjoint dims, so the end of a
-//    segment needs no cross-warp reduction: each PV warp writes its own dims
-//    (final output or partial).
+//    [32 v, 32 (v+1)) of the output and keeps the pair's running maximum m.
+//    Per unit, m_new = max(m, m_g), the accumulator and l are rescaled once by
+//    2^(m - m_new), and group g adds 2^(m_g - m_new) sW_g (Wq x Vq)
+//    (mma.sync m16n8k32 s8, exact int32, K = the group's 32 tokens; s8 x u8 for
+//    UINT8 probability codes) and 2^(m_g - m_new) l_g.  The accumulator covers
+//    disjoint dims, so the end of a segment needs no cross-warp reduction: each
+//    PV warp writes its own dims (final output or partial).
 //  * Ring slots: each QK stream has its own K slot(s), consumed in order, and
 //    the other slots carry V items in unit order, so every slot is refilled
 //    only after its previous item was consumed.
