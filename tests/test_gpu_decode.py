@@ -90,8 +90,9 @@ def test_decode_many_pairs_merge(D, Hq, Hkv, lens):
 
 
 def test_decode_workspace_reuse_and_repeat():
-    # The workspace's tickets reset themselves: repeated calls on one workspace give
-    # identical results, each written into a NaN-filled output (no stale rows).
+    # The workspace holds only this call's partials (no state carried between
+    # calls): repeated calls on one workspace give identical results, each written
+    # into a NaN-filled output (no stale rows).
     w = wl.DecodeWorkload("rep", 24, 4, 256, [5000, 3000, 40], seed=9)
     cache = gpu_decode_cache(w)
     q_i8, q_s = gpu_quantize_rows(w.q(), w.Hkv, cache)
