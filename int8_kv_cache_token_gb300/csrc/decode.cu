@@ -1223,8 +1223,10 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
   }
 }
 
-// Log-sum-exp merge of the partials of pairs that span CTAs: one CTA of 512
-// threads per (pair, query row).  Thread (slice, column) owns every SL-th
+// Log-sum-exp merge of the partials of pairs that span CTAs: two CTAs of 256
+// threads per (pair, query row), each half of the row's columns (one CTA of
+// 512 threads per row, or four of 128, were slower on single sequences).
+// Thread (slice, column) owns every SL-th
 // segment of one float4 column.  It loads a batch of kMB segments (value, m, l)
 // at once -- independent loads, all in flight together -- then folds them into
 // its running (max, denominator, sum); the slices are combined in a fixed order.
@@ -1236,7 +1238,8 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
 // for the grid's first CTA; for the others the partials' loads go out at once
 // after the wait.
 constexpr int kMaxSeg = 1024;
-constexpr int kMergeThreads = 512;
+constexpr int kMergeSplit = 2;    // CTAs per (pair, query row), each half of the row's columns
+constexpr int kMergeThreads = 256;
 constexpr int kMB = 8;
 constexpr int kMergeSpreadSmem = 120 * 1024;  // more than half an SM's shared memory
 
@@ -1276,13 +1279,14 @@ __device__ __forceinline__ int2 pair_ctas(const DecodeParams& p, int pair, int l
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParams p) {
-  constexpr int COLS = D / 4, SL = kMergeThreads / COLS;
+  constexpr int COLS = D / 4 / kMergeSplit, SL = kMergeThreads / COLS;
   constexpr int kGran = Geo<D, BF16>::kGran;
   __shared__ float4 red[SL][COLS];
   __shared__ float msh[SL], dsh[SL];
   __shared__ int s_seg[2];
   const int tid = threadIdx.x;
-  const int pair = blockIdx.x / p.G, row = blockIdx.x % p.G;
+  const int half = blockIdx.x % kMergeSplit, prw = blockIdx.x / kMergeSplit;
+  const int pair = prw / p.G, row = prw % p.G;
   if (tid < 32) {
     const int2 cs = pair_ctas<kGran>(p, pair, tid);
     if (tid == 0) {
@@ -1316,7 +1320,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
       const int s = s0 + j * SL;
       if (s < nseg) {
         const float* ps = part0 + (size_t)s * kSlotFloats(D);
-        v[j] = *reinterpret_cast<const float4*>(ps + row * D + 4 * col);
+        v[j] = *reinterpret_cast<const float4*>(ps + row * D + 4 * (half * COLS + col));
         ms[j] = ps[kRows * D + row];
         ls[j] = ps[kRows * D + kRows + row];
       } else {
@@ -1369,7 +1373,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
     }
     const float inv = 1.0f / dd;
     const int b = pair / p.Hkv, kvh = pair % p.Hkv;
-    store_out4(p.out, p.out_bf16, ((size_t)b * p.Hq + kvh * p.G + row) * D + 4 * tid,
+    store_out4(p.out, p.out_bf16, ((size_t)b * p.Hq + kvh * p.G + row) * D + 4 * (half * COLS + tid),
                make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv));
   }
 }
@@ -1559,8 +1563,8 @@ cudaError_t launch_decode_d(const DecodeParams& p, cudaStream_t stream) {
   if (4 * p.B * p.Hkv >= num_sms(dev))  // many pairs, each over few CTAs: one warp per row
     return launch_pdl(decode_merge_warp_kernel<D, BF16>, dim3((mgrid + kMergeWarpItems - 1) / kMergeWarpItems),
                       dim3(kMergeWarpItems * 32), 0, stream, p);
-  return launch_pdl(decode_merge_kernel<D, BF16>, dim3(mgrid), dim3(kMergeThreads),
-                    mgrid <= num_sms(dev) ? (size_t)kMergeSpreadSmem : 0, stream, p);
+  return launch_pdl(decode_merge_kernel<D, BF16>, dim3(mgrid * kMergeSplit), dim3(kMergeThreads),
+                    mgrid * kMergeSplit <= num_sms(dev) ? (size_t)kMergeSpreadSmem : 0, stream, p);
 }
 
 }  // namespace
