@@ -89,6 +89,17 @@ def test_decode_many_pairs_merge(D, Hq, Hkv, lens):
             assert not out[b].any()
 
 
+@pytest.mark.parametrize("B", [37, 38])
+def test_decode_merge_choice_boundary(B):
+    """The host takes the one-warp-per-row merge at B * Hkv >= #SM / 4 pairs (38
+    on 152 SMs) and the CTA merge below; on either side of it the pairs span
+    several attention CTAs (about 600 tokens each)."""
+    rng = np.random.default_rng(B)
+    lens = [int(x) for x in rng.integers(300, 900, size=B)]
+    w = wl.DecodeWorkload("mergeedge", 8, 1, 256, lens, seed=B)
+    _decode_parity(w)
+
+
 def test_decode_workspace_reuse_and_repeat():
     # The workspace holds only this call's partials (no state carried between
     # calls): repeated calls on one workspace give identical results, each written
