@@ -137,7 +137,7 @@ __host__ __device__ inline SmemLayout decode_layout(int nslots) {
   L.bars = off;  // full[nslots], empty[nslots], hfull[4], hempty[4]
   off += (size_t)(2 * nslots + 2 * kHandBufs) * sizeof(uint64_t);
   L.ctrl = off;
-  off += 16 * sizeof(int);
+  off += 32 * sizeof(int);
   L.total = off;
   return L;
 }
@@ -449,6 +449,7 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
   constexpr int kGran = Gm::kGran;
   constexpr int kWTok = Gm::kWTok, MT = Gm::MT, NDT = Gm::NDT;
   constexpr int kPW = Gm::kPW, kProdWarp = Gm::kProdWarp;
+  static_assert(kBlocksU <= 16, "a unit's block-table row fits ctrl[16 .. 31]");
   extern __shared__ __align__(1024) uint8_t smem[];
   const SmemLayout lay = decode_layout<D, BF16>(nslots);
   uint8_t* ring = smem + lay.ring;
@@ -466,10 +467,12 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
   const int N = gridDim.x, c = blockIdx.x;
   const int maxL = p.max_blocks * kBS;
 
-  // The producer warp's first 32 sequence lengths (see the split below) are in
-  // flight while lane 0 initializes the barriers.
+  // The prologue before the wait runs in three warps at once: the producer
+  // warp computes the work split, warp 0 initializes the barriers and warp 1
+  // guesses the first unit of a single sequence (below).  In one warp they took
+  // about 1.8 us, past the release of the wait in most CTAs.
   const int raw0 = (warp == kProdWarp && lane < B) ? __ldcg(p.seq_lens + lane) : 0;
-  if (warp == kProdWarp && lane == 0) {
+  if (warp == 0 && lane == 0) {
     const Ring rg(nslots, Gm::kStreams);
     for (int s = 0; s < nslots; ++s) {
       mbar_init(&full[s], 32);
@@ -490,22 +493,27 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
   // it the producer warp reads them again and records error 3 if they changed
   // (the caller wrote them in the kernel just before this one).
   //
-  // One sequence in the batch (the long-context decode case): guess the first
-  // unit from max_blocks and load its block-table row together with seq_lens,
-  // so the two dependent loads overlap; the guess is checked below.
-  int spec_gi = -1, spec_blk = -1;
+  // One sequence in the batch (the long-context decode case): warp 1 guesses
+  // the first unit from max_blocks and loads its block-table row while the
+  // producer warp loads seq_lens, so the two dependent loads overlap; the guess
+  // (ctrl[15], the row in ctrl[16 ..]) is checked below.
   uint32_t lhash = 0;  // this lane's sequence lengths, for the check after the wait
-  if (warp == kProdWarp && B == 1) {
-    const int ngp_g = (maxL + kGran - 1) / kGran;
-    const long long U_g = (long long)ngp_g * Hkv;
-    const int Nw_g = (int)(U_g < N ? U_g : N);
-    if (c < Nw_g) {
-      const long long ub_g = split_point(U_g, c, Nw_g);  // < U_g
-      spec_gi = ub_g < (1ll << 31) ? (int)((unsigned)ub_g - udiv_fast((unsigned)ub_g, ngp_g) * ngp_g)
-                                   : (int)(ub_g % ngp_g);
-      const int pg = spec_gi * kGran / kBS + lane;
-      if (lane < kBlocksU && pg < p.max_blocks) spec_blk = __ldcg(p.block_tables + pg);
+  if (warp == 1) {
+    int spec_gi = -1, spec_blk = -1;
+    if (B == 1) {
+      const int ngp_g = (maxL + kGran - 1) / kGran;
+      const long long U_g = (long long)ngp_g * Hkv;
+      const int Nw_g = (int)(U_g < N ? U_g : N);
+      if (c < Nw_g) {
+        const long long ub_g = split_point(U_g, c, Nw_g);  // < U_g
+        spec_gi = ub_g < (1ll << 31) ? (int)((unsigned)ub_g - udiv_fast((unsigned)ub_g, ngp_g) * ngp_g)
+                                     : (int)(ub_g % ngp_g);
+        const int pg = spec_gi * kGran / kBS + lane;
+        if (lane < kBlocksU && pg < p.max_blocks) spec_blk = __ldcg(p.block_tables + pg);
+      }
     }
+    if (lane == 0) ctrl[15] = spec_gi;
+    if (lane < 16) ctrl[16 + lane] = spec_blk;
   }
   if (warp == kProdWarp) {
     constexpr int kKeep = 8;  // chunks of 32 sequences whose unit counts stay in registers
@@ -599,8 +607,8 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
   };
   int blk_first = -1;
   if (warp == kProdWarp && n_gran > 0 && lane < first_blk_lanes()) {
-    blk_first = (B == 1 && w0.gi == spec_gi)
-                    ? spec_blk
+    blk_first = (B == 1 && w0.gi == ctrl[15])
+                    ? ctrl[16 + lane]
                     : __ldcg(p.block_tables + (size_t)w0.b * p.max_blocks + w0.gi * kGran / kBS + lane);
   }
   // From here on the kernel reads and writes what earlier work on the stream uses.
