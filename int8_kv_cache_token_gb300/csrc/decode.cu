@@ -515,7 +515,29 @@ __global__ void __launch_bounds__(Geo<D, BF16>::kThreads, 1) decode_kernel(Decod
     if (lane == 0) ctrl[15] = spec_gi;
     if (lane < 16) ctrl[16 + lane] = spec_blk;
   }
-  if (warp == kProdWarp) {
+  if (warp == kProdWarp && B == 1) {
+    // One sequence: no reduction or scan over the batch.  The same values as the
+    // general split below (sequence 0 starts at granule 0).
+    lhash = lane == 0 ? len_hash(0u, raw0) : 0u;
+    const int L = clamp_len(__shfl_sync(0xffffffffu, raw0, 0), maxL);
+    const int ngp = (L + kGran - 1) / kGran;  // granules per pair
+    const long long U = (long long)ngp * Hkv;
+    const int Nw = (int)(U < N ? U : N);
+    const long long ub = c < Nw ? split_point(U, c, Nw) : 0, ue = c < Nw ? split_point(U, c + 1, Nw) : 0;
+    if (lane == 0) {
+      ctrl[0] = (int)(ue - ub);
+      ctrl[8] = 0;
+      if (ue > ub) {
+        const unsigned kv = udiv_fast((unsigned)ub, (unsigned)ngp);  // ub < ngp * Hkv, as in the scan below
+        ctrl[1] = 0;
+        ctrl[2] = (int)kv;
+        ctrl[3] = (int)((unsigned)ub - kv * (unsigned)ngp);
+        ctrl[4] = 0;
+        ctrl[5] = 0;
+        ctrl[9] = L;
+      }
+    }
+  } else if (warp == kProdWarp) {
     constexpr int kKeep = 8;  // chunks of 32 sequences whose unit counts stay in registers
     int ukeep[kKeep], lkeep[kKeep];
     long long total = 0;
