@@ -100,6 +100,28 @@ def test_decode_merge_choice_boundary(B):
     _decode_parity(w)
 
 
+@pytest.mark.parametrize("D,Hq,Hkv,L,pad", [(256, 24, 4, 5000, 300), (128, 32, 8, 777, 64), (256, 8, 1, 40, 1)])
+def test_decode_single_sequence_wide_block_table(D, Hq, Hkv, L, pad):
+    """One sequence with a block table wider than its length needs.  Before the
+    lengths arrive the kernel guesses each CTA's first unit from the table width
+    and loads that unit's block-table row; here the guess misses, and the row is
+    read again once the work split is known."""
+    w = wl.DecodeWorkload("wide", Hq, Hkv, D, [L], seed=L + D)
+    cache = gpu_decode_cache(w)
+    q_i8, q_scale = gpu_quantize_rows(w.q(), w.Hkv, cache)
+    wide = np.pad(w.block_tables, ((0, 0), (0, pad)), constant_values=-1)
+    ws = i8.decode_workspace(w.B, w.Hq, w.Hkv, w.D, wide.shape[1])
+    out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.float32, device="cuda")
+    i8.int8_paged_decode_attn(out, q_i8, q_scale, cache["k_cache"], cache["v_cache"], cache["k_scale"],
+                              cache["v_scale"], dev(wide), dev(w.seq_lens), ws)
+    got = host(out)
+    assert i8.device_error() == 0
+    oc = oracle_decode_cache(w, [0])
+    oq, oqs = oracle_query(w, [0])
+    ref = orc.decode_attn(oq, oqs, oc, w.block_tables, w.seq_lens, w.block_size)
+    assert np.abs(got - ref).max() <= TOL
+
+
 def test_decode_workspace_reuse_and_repeat():
     # The workspace holds only this call's partials (no state carried between
     # calls): repeated calls on one workspace give identical results, each written
