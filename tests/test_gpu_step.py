@@ -163,3 +163,16 @@ def test_back_to_back_steps_see_the_previous_token():
         for name in ("k_cache", "v_cache", "k_scale", "v_scale"):
             assert torch.equal(c1[name], c2w[name]), name
         assert np.array_equal(host(out1), host(out_b))
+
+
+@pytest.mark.parametrize("lens", [[3000], [129, 5, 2000]])
+def test_step_wide_block_table(lens):
+    """Block tables wider than the lengths need (columns past them are -1): the
+    guessed first unit misses and the new token's block comes from the table;
+    still bit-identical to the two calls."""
+    w = wl.DecodeWorkload("stepwide", 24, 4, 256, lens, seed=sum(lens) + 3)
+    w.block_tables = np.pad(w.block_tables, ((0, 0), (0, 100)), constant_values=-1)
+    c1, c2, out1, out2 = _run_both(w)
+    for name in ("k_cache", "v_cache", "k_scale", "v_scale"):
+        assert torch.equal(c1[name], c2[name]), name
+    assert np.array_equal(out1, out2)
