@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(kProdThreads, 1) kv_quant_write_kernel(Produce
 
   if (warp == kNCW) {
     // ------------------------------------------------------------ loader warp
+    const uint64_t l2_first = policy_evict_first();
     // Tile metadata is read one tile ahead (registers), published just before
     // the loader could block on a slot that this tile's units may occupy.
     auto read_meta = [&](long long n, int& s, int& pos) {
@@ -350,9 +351,9 @@ __global__ void __launch_bounds__(kProdThreads, 1) kv_quant_write_kernel(Produce
         mbar_expect_tx(&full[s], ntv * rb);
         mbar_arrive(&full[s]);
       }
-      if (lane < ntv)
-        bulk_g2s(ring + (size_t)s * g.slot_bytes + (size_t)lane * g.row_stride,
-                 src + ((size_t)(n * kTok + lane) * H + h0) * D, rb, &full[s]);
+      if (lane < ntv)  // the bf16 rows are read once: L2 lets them go first
+        bulk_g2s_hint(ring + (size_t)s * g.slot_bytes + (size_t)lane * g.row_stride,
+                      src + ((size_t)(n * kTok + lane) * H + h0) * D, rb, &full[s], l2_first);
       if (++s == g.S) {
         s = 0;
         ++use;
