@@ -194,7 +194,7 @@ def cta_units(ngps, g0, g1, qw):
 @pytest.mark.parametrize("streams,qw", [(1, 8), (2, 4)])
 def test_decode_step_new_token_has_one_owner(streams, qw):
     """Decode step: the stream holding the unit with a pair's newest token
-    quantizes that token at its first unit of the pair, judged from that unit
+    quantizes that token at its first unit of the pair, decided from that unit
     alone (the pair's last granule inside the CTA's range, and the units from
     there to it, kQW granules each, a multiple of the stream count).  Exactly
     one (CTA, stream) claims each pair, and it is the one that processes the
