@@ -73,6 +73,27 @@ def test_reference_arm_prints_on_rank0_only():
     assert p.stdout.strip() == ""
 
 
+def test_reference_arm_line_matches_the_headline_config():
+    """Rank 0 of the reference arm times the oracle on the headline's own config,
+    metric and unit, and reports its sample as the cpu_baseline."""
+    sys.path.insert(0, ROOT)
+    import bench
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    p = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "1"], env=env, capture_output=True, text=True, timeout=600)
+    assert p.returncode == 0, p.stderr
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["config"] == bench.headline_config(1, bench.LAYERS)
+    assert d["metric"] == bench.METRIC and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1 and "sample" in d["cpu_baseline"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
 def test_whole_job_value_scales_with_ranks():
     sys.path.insert(0, ROOT)
     import bench
