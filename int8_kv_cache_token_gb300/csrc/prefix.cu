@@ -237,28 +237,46 @@ __global__ void __launch_bounds__(256) prefix_tiles_kernel(PrefixParams p) {
       blk[i] = -1;
     }
   }
-  // K page [D/16][16 tokens][16 B] -> [key][D] (SW128 atoms): chunk i = (page, dim chunk, token)
-  constexpr int KC = kPagesPG * (D / 16) * kBS;
-  for (int i = tid; i < KC; i += 256) {
+  // K page [D/16][16 tokens][16 B] -> [key][D] (SW128 atoms): chunk i = (page, dim chunk, token);
+  // V page [D][16 tokens] -> [D][32 keys] (SW64): chunk i = (page, dim).  Every
+  // thread loads all of its chunks before it stores any, so the loads are in
+  // flight together.
+  constexpr int KC = kPagesPG * (D / 16) * kBS, VC = kPagesPG * D;
+  static_assert(KC % 256 == 0 && VC % 256 == 0, "whole chunks per thread");
+  uint4 kv[KC / 256], vv[VC / 256];
+#pragma unroll
+  for (int j = 0; j < KC / 256; ++j) {
+    const int i = tid + 256 * j;
+    const int pg = i / ((D / 16) * kBS), rem = i % ((D / 16) * kBS);
+    kv[j] = blk[pg] >= 0
+                ? __ldg(reinterpret_cast<const uint4*>(p.k_cache + ((size_t)blk[pg] * Hkv + kvh) * (D * kBS)) + rem)
+                : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int j = 0; j < VC / 256; ++j) {
+    const int i = tid + 256 * j;
+    const int pg = i / D, d = i % D;
+    vv[j] = blk[pg] >= 0
+                ? __ldg(reinterpret_cast<const uint4*>(p.v_cache + ((size_t)blk[pg] * Hkv + kvh) * (D * kBS)) + d)
+                : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int j = 0; j < KC / 256; ++j) {
+    const int i = tid + 256 * j;
     const int pg = i / ((D / 16) * kBS), rem = i % ((D / 16) * kBS);
     const int dc = rem / kBS, key = pg * kBS + rem % kBS;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (blk[pg] >= 0)
-      v = __ldg(reinterpret_cast<const uint4*>(p.k_cache + ((size_t)blk[pg] * Hkv + kvh) * (D * kBS)) + rem);
     uint4 h0, h1;
-    s8x16_to_f16(v, h0, h1);
+    s8x16_to_f16(kv[j], h0, h1);
     uint8_t* atom = tile + T::oK + (size_t)(dc / 4) * (kGroup * 128);
     *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4))) = h0;
     *reinterpret_cast<uint4*>(atom + swz_chunk<128>(key, 2 * (dc % 4) + 1)) = h1;
   }
-  // V page [D][16 tokens] -> [D][32 keys] (SW64): chunk i = (page, dim)
-  for (int i = tid; i < kPagesPG * D; i += 256) {
+#pragma unroll
+  for (int j = 0; j < VC / 256; ++j) {
+    const int i = tid + 256 * j;
     const int pg = i / D, d = i % D;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (blk[pg] >= 0)
-      v = __ldg(reinterpret_cast<const uint4*>(p.v_cache + ((size_t)blk[pg] * Hkv + kvh) * (D * kBS)) + d);
     uint4 h0, h1;
-    s8x16_to_f16(v, h0, h1);
+    s8x16_to_f16(vv[j], h0, h1);
     *reinterpret_cast<uint4*>(tile + T::oV + swz_chunk<64>(d, 2 * pg)) = h0;
     *reinterpret_cast<uint4*>(tile + T::oV + swz_chunk<64>(d, 2 * pg + 1)) = h1;
   }
