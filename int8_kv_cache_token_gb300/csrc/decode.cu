@@ -1323,6 +1323,12 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
   __shared__ float4 red[SL][COLS];
   __shared__ float msh[SL], dsh[SL];
   __shared__ int s_seg[2];
+  // The next kernel on the stream may start its launch (and its pre-wait
+  // prologue) at once: its own grid-dependency wait still waits for this grid
+  // to complete, which happens after the attention kernel (see below).
+  // Single-sequence calls are 0.2 us shorter than when this signal followed
+  // the wait.
+  griddep_launch_dependents();
   const int tid = threadIdx.x;
   const int half = blockIdx.x % kMergeSplit, prw = blockIdx.x / kMergeSplit;
   const int pair = prw / p.G, row = prw % p.G;
@@ -1341,7 +1347,6 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeParam
   // grid only, so this grid must not end before the attention kernel does.
   if (cf == cl && blockIdx.x != 0) return;
   griddep_wait();
-  griddep_launch_dependents();
   if (cf == cl) return;
   if (nseg > kMaxSeg) {
     record_error(2);
@@ -1427,6 +1432,7 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kMergeWarpItems * 32) decode_merge_warp_kernel(DecodeParams p) {
   constexpr int kGran = Geo<D, BF16>::kGran, E = D / 32, kWB = 4;
   const int lane = threadIdx.x & 31;
+  griddep_launch_dependents();  // as in decode_merge_kernel
   const int item = blockIdx.x * kMergeWarpItems + (threadIdx.x >> 5);
   if (item >= p.B * p.Hkv * p.G) return;
   const int pair = item / p.G, row = item % p.G;
@@ -1438,7 +1444,6 @@ __global__ void __launch_bounds__(kMergeWarpItems * 32) decode_merge_warp_kernel
   const int nseg = cs.y - cs.x + 1;
   const size_t obase = ((size_t)(pair / p.Hkv) * p.Hq + (pair % p.Hkv) * p.G + row) * D + lane * E;
   griddep_wait();
-  griddep_launch_dependents();
   if (cs.x == cs.y) return;
   if (nseg > kMaxSeg) {
     if (lane == 0) record_error(2);
