@@ -17,10 +17,14 @@
  *    while the previous kernel on the stream is still running, but it reads
  *    no global memory before that kernel has finished -- with one exception:
  *    the decode kernels read seq_lens and block_tables early (no kernel of
- *    this library writes them), so these two inputs must not be written by
- *    the kernel launched just before on the same stream (a host copy, or any
- *    earlier kernel, is fine).  The decode kernels read them again after the
- *    wait and record error 3 in the device error word if they changed.
+ *    this library writes them), so these two inputs must not be written by a
+ *    kernel that may still be running when the decode call starts: the kernel
+ *    launched just before it on the same stream, and any kernel before that
+ *    one which let its successor start early (the decode merge kernels do so
+ *    at their start, so after a decode call the kernel before its attention
+ *    kernel counts too).  A host copy, or a kernel that completed before, is
+ *    fine.  The decode kernels read them again after the wait and record
+ *    error 3 in the device error word if they changed.
  *  - Argument errors are reported synchronously through the status code, before
  *    anything is launched; i8kv_last_error() gives a one-line reason.  A launch
  *    failure reported by the CUDA runtime maps to I8KV_ERR_CUDA.
