@@ -21,9 +21,9 @@
  *    kernel that may still be running when the decode call starts: the kernel
  *    launched just before it on the same stream, and any kernel before that
  *    one which let its successor start early (the decode merge kernels do so
- *    at their start, so after a decode call the kernel before its attention
- *    kernel counts too).  A host copy, or a kernel that completed before, is
- *    fine.  The decode kernels read them again after the wait and record
+ *    at their start, so a decode call may start while the previous call's
+ *    attention kernel still runs; that kernel does not write them).  A host
+ *    copy, or a kernel that completed before, is fine.  The decode kernels read them again after the wait and record
  *    error 3 in the device error word if they changed.
  *  - Argument errors are reported synchronously through the status code, before
  *    anything is launched; i8kv_last_error() gives a one-line reason.  A launch
